@@ -1,0 +1,190 @@
+"""Float64 oracle: ctypes driver for the C recurrence and numpy restatements.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Shapes (row-major):
+    x [b,L,nh,P]   dt [b,L,nh]   A [nh]   B, C [b,L,ng,S]   D [nh]
+    h0 / final_state [b,nh,P,S]   states / dstates [b,nh,nc,P,S]
+    y [b,L,nh,P]   G [b,nh,nc*T]  (natural-log units; the CUDA path stores
+    G times log2(e))
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssd_oracle.c")
+_LIB = os.path.join(_HERE, "libssd_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ssd_oracle.c into a shared library next to it (gcc, OpenMP)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    os.close(fd)
+    cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+    try:
+        subprocess.run(cmd, check=True, capture_output=True, text=True)
+        os.replace(tmp, _LIB)
+    finally:
+        if os.path.exists(tmp):
+            os.unlink(tmp)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        i64, dp = ctypes.c_int64, ctypes.c_void_p
+        lib.ssd_oracle_forward.restype = ctypes.c_int
+        lib.ssd_oracle_forward.argtypes = [i64] * 7 + [dp] * 7 + [dp, i64] + [dp] * 5
+        _lib = lib
+        # libgomp is linked into the library; its thread controls are
+        # reachable through the same handle.
+        _lib.omp_set_num_threads.argtypes = [ctypes.c_int]
+        _lib.omp_get_max_threads.restype = ctypes.c_int
+    return _lib
+
+
+def set_threads(n: int) -> None:
+    """Number of OpenMP threads the C recurrence uses from now on."""
+    _load().omp_set_num_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(_load().omp_get_max_threads())
+
+
+def _f64(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _dims(x, dt, A, B):
+    b, L, nh, P = x.shape
+    ng, S = B.shape[2], B.shape[3]
+    assert dt.shape == (b, L, nh) and A.shape == (nh,) and B.shape == (b, L, ng, S)
+    assert nh % ng == 0
+    return b, L, nh, P, S, ng
+
+
+def recurrence(x, dt, A, B, C, D=None, h0=None, chunk=256, bh=None,
+               want=("y", "final_state")):
+    """Run the C token-by-token recurrence.  Returns a dict with the requested
+    outputs among y, final_state, states, dstates, G (float64 numpy)."""
+    x, dt, A, B, C, D, h0 = map(_f64, (x, dt, A, B, C, D, h0))
+    b, L, nh, P, S, ng = _dims(x, dt, A, B)
+    assert C.shape == B.shape
+    T = int(chunk)
+    nc = (L + T - 1) // T
+    shapes = {
+        "y": (b, L, nh, P),
+        "final_state": (b, nh, P, S),
+        "states": (b, nh, nc, P, S),
+        "dstates": (b, nh, nc, P, S),
+        "G": (b, nh, nc * T),
+    }
+    out = {k: np.full(shapes[k], np.nan) for k in want}
+    bh_arr = None if bh is None else np.ascontiguousarray(bh, dtype=np.int64)
+
+    def ptr(a):
+        return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+    rc = _load().ssd_oracle_forward(
+        b, L, nh, P, S, ng, T,
+        ptr(x), ptr(dt), ptr(A), ptr(B), ptr(C), ptr(D), ptr(h0),
+        ptr(bh_arr), 0 if bh_arr is None else len(bh_arr),
+        ptr(out.get("y")), ptr(out.get("final_state")), ptr(out.get("states")),
+        ptr(out.get("dstates")), ptr(out.get("G")))
+    if rc != 0:
+        raise ValueError(f"ssd_oracle_forward rejected its arguments (code {rc})")
+    return out
+
+
+def recurrence_np(x, dt, A, B, C, D=None, h0=None):
+    """The same recurrence in numpy, vectorised over (P, S) only; for tiny
+    inputs.  Returns (y, final_state)."""
+    x, dt, A, B, C, D, h0 = map(_f64, (x, dt, A, B, C, D, h0))
+    b, L, nh, P, S, ng = _dims(x, dt, A, B)
+    hpg = nh // ng
+    y = np.zeros((b, L, nh, P))
+    final = np.zeros((b, nh, P, S))
+    for bi in range(b):
+        for h in range(nh):
+            g = h // hpg
+            H = np.zeros((P, S)) if h0 is None else h0[bi, h].copy()
+            for t in range(L):
+                H = np.exp(A[h] * dt[bi, t, h]) * H + np.outer(dt[bi, t, h] * x[bi, t, h], B[bi, t, g])
+                y[bi, t, h] = H @ C[bi, t, g] + (0.0 if D is None else D[h]) * x[bi, t, h]
+            final[bi, h] = H
+    return y, final
+
+
+def chunked(x, dt, A, B, C, D=None, h0=None, chunk=256):
+    """The chunked log-space formulas, float64, per (batch, head, chunk):
+
+        G      = inclusive cumsum of a = A*dt inside the chunk
+        Y      = exp(G) * (C h^T) + ((C B^T) * exp(G_i - G_j) * M) (dt * X) + D X
+        h_next = exp(G_last) h + (exp(G_last - G) * dt * X)^T B      (P x S)
+
+    with M the causal mask including the diagonal.  Returns a dict with y,
+    final_state, states (start of chunk), dstates (chunk-local jump term),
+    G (natural log, padded like the recurrence) and max_kept_exponent, the
+    largest exponent that survives the mask (non-positive by construction
+    when every a_t <= 0)."""
+    x, dt, A, B, C, D, h0 = map(_f64, (x, dt, A, B, C, D, h0))
+    b, L, nh, P, S, ng = _dims(x, dt, A, B)
+    hpg = nh // ng
+    T = int(chunk)
+    nc = (L + T - 1) // T
+    y = np.zeros((b, L, nh, P))
+    final = np.zeros((b, nh, P, S))
+    states = np.zeros((b, nh, nc, P, S))
+    dstates = np.zeros((b, nh, nc, P, S))
+    Gall = np.zeros((b, nh, nc * T))
+    kept = -np.inf
+    for bi in range(b):
+        for h in range(nh):
+            g = h // hpg
+            H = np.zeros((P, S)) if h0 is None else h0[bi, h].copy()
+            for k in range(nc):
+                lo, hi = k * T, min((k + 1) * T, L)
+                n = hi - lo
+                X = x[bi, lo:hi, h]            # n x P
+                Bc = B[bi, lo:hi, g]           # n x S
+                Cc = C[bi, lo:hi, g]           # n x S
+                d = dt[bi, lo:hi, h]           # n
+                G = np.cumsum(A[h] * d)        # n
+                Gall[bi, h, lo:lo + n] = G
+                Gall[bi, h, lo + n:(k + 1) * T] = G[-1]
+                states[bi, h, k] = H
+                mask = np.tril(np.ones((n, n), dtype=bool))
+                expo = G[:, None] - G[None, :]
+                if n:
+                    kept = max(kept, expo[mask].max())
+                decay = np.where(mask, np.exp(np.where(mask, expo, 0.0)), 0.0)
+                Yc = np.exp(G)[:, None] * (Cc @ H.T)
+                Yc += ((Cc @ Bc.T) * decay) @ (d[:, None] * X)
+                if D is not None:
+                    Yc += D[h] * X
+                y[bi, lo:hi, h] = Yc
+                w = np.exp(G[-1] - G) * d      # exp(G_last - G) * dt
+                kept = max(kept, (G[-1] - G).max())
+                dH = (w[:, None] * X).T @ Bc   # P x S
+                dstates[bi, h, k] = dH
+                H = np.exp(G[-1]) * H + dH
+            final[bi, h] = H
+    return {"y": y, "final_state": final, "states": states, "dstates": dstates,
+            "G": Gall, "max_kept_exponent": kept}
