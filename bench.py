@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark of the Mamba-2 chunked SSD forward pass on GB300.
+
+One step = one ssd_forward over one batch of the workload (seeded synthetic
+inputs already resident in HBM).  Prints ONE JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--skip-cpu-baseline] [--skip-e2e]
+
+Timing: W untimed warm-up steps, then exactly K timed steps bracketed by a
+barrier and torch.cuda.synchronize() on both sides.  Each step is timed with
+CUDA events recorded by the library between its own launches on the
+launching stream; L2 is flushed (a 256 MB write, outside the events) before
+every step.  Under torchrun every rank runs the whole workload on its own GPU
+(independent batches: weak scaling, no data-path collective) and the slowest
+rank's time is reported.
+
+--impl reference times the float64 CPU oracle on the host cores instead, on
+a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mamba_ssd_forward_gb300 import inputs as W  # noqa: E402
+
+METRIC = "SSD forward tokens/s at 1 GB300; achieved TFLOP/s + HBM GB/s vs roofline"
+DEFAULT_WORKLOAD = W.MAMBA2_130M
+KERNEL_NAMES = ["chunk_cumsum", "chunk_state", "state_passing", "chunk_scan"]
+KERNEL_SOURCES = {"chunk_cumsum": "chunk_cumsum.cu", "chunk_state": "chunk_state.cu",
+                  "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan.cu"}
+FALLBACK_HBM_GBS = 6800.0
+
+
+def workload_by_name(name: str) -> W.Workload:
+    for w in W.NAMED + W.sweep():
+        if w.name == name or w.name.startswith(name):
+            return w
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+
+def io_bytes(w: W.Workload) -> int:
+    return 2 if w.dtype == "bf16" else 4
+
+
+def compulsory_bytes(w: W.Workload) -> int:
+    """Bytes the forward pass must move at least once: read x, dt, B, C, A, D
+    (and h0), write y and the final state."""
+    e = io_bytes(w)
+    tok = w.batch * w.seqlen
+    n = tok * w.nheads * w.headdim * e * 2            # x in, y out
+    n += tok * w.nheads * e                             # dt
+    n += 2 * tok * w.ngroups * w.dstate * e             # B, C
+    n += 2 * w.nheads * 4                               # A, D
+    st = w.batch * w.nheads * w.headdim * w.dstate * 4
+    n += st * (2 if w.has_h0 else 1)                    # h0, final state
+    return n
+
+
+def algorithmic_flops(w: W.Workload) -> float:
+    """Tensor-core flops per token-head: 4 S P (C h and the chunk state)
+    + (T+1) P (causal interaction times X) + (T+1) S / hpg (C B^T, once per
+    group), times the token-heads."""
+    hpg = w.nheads // w.ngroups
+    per = 4 * w.dstate * w.headdim + (w.chunk + 1) * w.headdim + (w.chunk + 1) * w.dstate / hpg
+    return per * w.batch * w.seqlen * w.nheads
+
+
+def kernel_bytes(w: W.Workload) -> dict:
+    """Algorithmic bytes of one launch of each kernel: its own inputs read
+    once and outputs written once."""
+    e = io_bytes(w)
+    tok = w.batch * w.seqlen
+    x = tok * w.nheads * w.headdim * e
+    dt = tok * w.nheads * e
+    bc = tok * w.ngroups * w.dstate * e
+    G = w.batch * w.nheads * w.nchunks * w.chunk * 4
+    st = w.batch * w.nheads * w.nchunks * w.headdim * w.dstate * 4
+    fin = w.batch * w.nheads * w.headdim * w.dstate * 4
+    return {
+        "chunk_cumsum": dt + G + w.nheads * 4,
+        "chunk_state": x + bc + dt + G + st,
+        "state_passing": 2 * st + w.batch * w.nheads * w.nchunks * 4 + fin * (2 if w.has_h0 else 1),
+        "chunk_scan": 2 * x + 2 * bc + dt + G + st + w.nheads * 4,
+    }
+
+
+# ---------------------------------------------------------------------------
+# peaks, traffic, clocks
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(kernel: str) -> str:
+    path = os.path.join(ROOT, "mamba_ssd_forward_gb300", "csrc", KERNEL_SOURCES[kernel])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, w: W.Workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of that kernel and this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(f"{kernel}@{w.name}")
+    except Exception:
+        return None
+    if not rec or rec.get("source_sha256_16") != source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.lines = []
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].strip().lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def time_oracle(w: W.Workload, inp, target_s: float):
+    """Time the float64 oracle on as many (batch, head) pairs of the workload
+    as fit in about target_s seconds.  Returns (tokens/s, threads, sample)."""
+    import oracle
+    oracle.build()
+    threads = oracle.max_threads()
+    total = w.batch * w.nheads
+    t = time.perf_counter()
+    oracle.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"],
+                      chunk=w.chunk, bh=[0])
+    one = max(time.perf_counter() - t, 1e-4)
+    n = int(max(1, min(total, target_s / one * threads)))
+    if n >= threads:
+        n = (n // threads) * threads
+    bh = list(range(n))
+    t = time.perf_counter()
+    oracle.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"],
+                      chunk=w.chunk, bh=bh)
+    dt_s = time.perf_counter() - t
+    reps = 1
+    if n == total:
+        # the whole workload fits the budget: repeat it for a steadier number
+        while dt_s < min(target_s, 5.0) and reps < 64:
+            t = time.perf_counter()
+            oracle.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                              inp["h0"], chunk=w.chunk, bh=bh)
+            dt_s += time.perf_counter() - t
+            reps += 1
+    tok_per_s = reps * n * w.seqlen / w.nheads / dt_s
+    what = f"{n} of {total} (batch, head) pairs at full length L={w.seqlen}"
+    if reps > 1:
+        what += f", whole workload repeated {reps} times"
+    return tok_per_s, threads, what, dt_s / reps
+
+
+def host_inputs(w):
+    inp = W.make_inputs(w, seed=0)
+    return inp
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    inp = host_inputs(w)
+    # each step: a bounded sample sized so that W + K steps take a few minutes
+    budget = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    times, vals = [], []
+    threads = sample = None
+    for i in range(args.warmup + args.steps):
+        v, threads, sample, secs = time_oracle(w, inp, budget)
+        if i >= args.warmup:
+            vals.append(v)
+            times.append(secs)
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import mamba_ssd_forward_gb300 as ssd
+    from mamba_ssd_forward_gb300 import build
+
+    world, rank, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+
+    inp = host_inputs(w)
+    d = {k: (None if v is None else v.to(dev).contiguous()) for k, v in inp.items()}
+    ws = torch.empty(ssd.workspace_size(d["x"], d["B"], w.chunk), dtype=torch.uint8, device=dev)
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    nev = 8
+
+    def step(events):
+        return ssd.forward_profiled(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"],
+                                    w.chunk, ws, y, fin, events)
+
+    warm_ev = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(warm_ev)
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_start()
+    launches = 0
+    n_l = 0
+    for i in range(args.steps):
+        flush.zero_()
+        n_l = step(ev[i])
+        launches += n_l
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if sampler:
+        sampler.mark_end()
+    clocks = sampler.stop() if sampler else None
+
+    step_ms = [ev[i][0].elapsed_time(ev[i][n_l]) for i in range(args.steps)]
+    kern_ms = {KERNEL_NAMES[j]: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1])
+                                                for i in range(args.steps))
+               for j in range(n_l)}
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = w.batch * w.seqlen
+    value = world * tokens / (ms / 1e3)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    # roofline of the dominant kernel
+    dom = max(kern_ms, key=kern_ms.get)
+    kb = kernel_bytes(w)
+    peak, peak_src = hbm_peak()
+    achieved = kb[dom] / (kern_ms[dom] / 1e3) / 1e9
+    roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": kb[dom], "traffic": ncu_traffic(dom, w),
+            "kernel_ms": kern_ms,
+            "kernel_share": {k: v / sum(kern_ms.values()) for k, v in kern_ms.items()}}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded, distributions of the layer; no dataset)",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen,
+                   "nheads": w.nheads, "headdim": w.headdim, "dstate": w.dstate,
+                   "ngroups": w.ngroups, "chunk": w.chunk, "h0": w.has_h0,
+                   "l2": "flushed before every step (256 MB write outside the timed events)",
+                   "parallelism": f"replicas x{world} (independent batches per GPU)"},
+        "achieved_tflops": algorithmic_flops(w) / (ms / 1e3) / 1e12,
+        "achieved_gbs_compulsory": compulsory_bytes(w) / (ms / 1e3) / 1e9,
+        "roofline_forward": {"bound": "hbm", "frac": compulsory_bytes(w) / (ms / 1e3) / 1e9 / peak,
+                             "compulsory_bytes": compulsory_bytes(w)},
+        "roofline": roof,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+
+    if not args.skip_e2e:
+        line["e2e"] = e2e(args, w, inp, dev)
+    if not args.skip_cpu_baseline and world == 1:
+        v, threads, sample, _ = time_oracle(w, inp, 15.0)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e(args, w, inp, dev):
+    """Same metric through ssd_forward_host: pinned host inputs copied in,
+    forward, y and the final state copied out, every step."""
+    import torch
+
+    import mamba_ssd_forward_gb300 as ssd
+    h = {k: (None if v is None else v.contiguous().pin_memory()) for k, v in inp.items()}
+    y = torch.empty_like(h["x"]).pin_memory()
+    fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32).pin_memory()
+    ws = torch.empty(ssd.host_workspace_size(h["x"], h["B"], w.chunk, has_D=True,
+                                             has_h0=h["h0"] is not None),
+                     dtype=torch.uint8, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in h.values() if v is not None)
+    d2h = y.numel() * y.element_size() + fin.numel() * fin.element_size()
+    for _ in range(max(3, args.warmup)):
+        ssd.forward_host(h["x"], h["dt"], h["A"], h["B"], h["C"], h["D"], h["h0"], w.chunk,
+                         ws, y, fin)
+    torch.cuda.synchronize()
+    n = max(args.steps, 3)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(n):
+        ssd.forward_host(h["x"], h["dt"], h["A"], h["B"], h["C"], h["D"], h["h0"], w.chunk,
+                         ws, y, fin)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    return {"value": w.batch * w.seqlen / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD.name)
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    w = workload_by_name(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

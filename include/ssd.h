@@ -1,0 +1,185 @@
+/*
+ * ssd.h -- C ABI of the GB300 (sm_103a) Mamba-2 chunked SSD forward pass.
+ *
+ * Method: "Accelerating Mamba-2 with High-Performance Forward Pass Kernels in
+ * NVIDIA CUDA Tile", section "Mamba-2 architecture".  Per batch b and head h,
+ * with a_t = A[h] dt_t and b_t = dt_t B_t, the layer computes
+ *
+ *     h_t = exp(a_t) h_{t-1} + x_t (outer) b_t          state, P x S
+ *     y_t = h_t c_t + D[h] x_t                          output, P
+ *
+ * y uses the post-update state h_t: the page's chunked output equation keeps
+ * the diagonal of the causal mask (one line of the page writes h_{t-1}; this
+ * library follows the chunked equations).  The work is split as on the page
+ * (section "three kernels"): an in-chunk cumulative sum of a, the chunk
+ * state jump h_{t+T} = exp(G_last) h_t + (exp(G_last - G) b)^T x, a
+ * sequential pass over chunks, and the per-chunk output
+ * Y = exp(G) C h + ((C B^T) * exp(G_i - G_j) * M) (dt X) + D X.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers to dense row-major arrays in the
+ *   layouts listed below; each must be 16-byte aligned.  The caller owns and
+ *   allocates every buffer, including the workspace of ssd_forward.  The
+ *   library never allocates, frees or synchronises, and keeps no state
+ *   between calls.
+ * - `stream` is a cudaStream_t (NULL = legacy default stream); all work is
+ *   enqueued on it and runs asynchronously.
+ * - Arguments are validated before anything is launched; a rejected call
+ *   returns an error code and enqueues nothing.  A launch failure returns
+ *   SSD_ERR_CUDA.  SSD_ERR_TIMEOUT reports that a bounded device-side wait
+ *   gave up (the results of that call are then undefined).  Nothing throws.
+ * - Preconditions that are documented but not checked: A <= 0 and dt >= 0 (so
+ *   every a_t <= 0, the page's stability condition), finite inputs, and
+ *   output buffers that do not overlap inputs.
+ *
+ * Dimensions (ssd_dims): batch b >= 1, seqlen L >= 1, nheads nh >= 1,
+ * headdim P, dstate S, ngroups ng (nh % ng == 0; head h reads group
+ * h / (nh / ng), as on the page), chunk T.  Supported: P, S multiples of 16
+ * with 16 <= P <= 128 and 16 <= S <= 256; T in {64, 128, 256}.  Anything
+ * else returns SSD_ERR_UNSUPPORTED.  nc = ceil(L / T); the last chunk may be
+ * partial and is treated as zero-padded (dt = 0), which changes nothing.
+ *
+ * Layouts ("io" = the I/O element type given by ssd_dtype):
+ *   x  [b, L, nh, P] io        dt [b, L, nh] io        A [nh] f32
+ *   B  [b, L, ng, S] io        C  [b, L, ng, S] io     D [nh] f32
+ *   h0, final_state [b, nh, P, S] f32
+ *   G  [b, nh, nc*T] f32  -- chunk-local inclusive cumsum of a, times log2(e)
+ *   dstates, states [b, nh, nc, P, S] f32
+ *   y  [b, L, nh, P] io
+ * With SSD_F32 the tensor-core products run in TF32 with fp32 accumulation;
+ * with SSD_BF16 they take bf16 operands and accumulate in fp32.
+ */
+#ifndef SSD_GB300_H
+#define SSD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, nh % ng */
+  SSD_ERR_UNSUPPORTED = 2, /* dims outside the supported range */
+  SSD_ERR_CUDA = 3,        /* a CUDA call or launch failed */
+  SSD_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up */
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+typedef struct {
+  int64_t batch, seqlen, nheads, headdim, dstate, ngroups, chunk;
+} ssd_dims;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+SSD_API const char *ssd_status_string(ssd_status s);
+
+/* Bytes of device workspace ssd_forward needs for these dims and dtype
+ * (0 if the dims are invalid or unsupported). */
+SSD_API size_t ssd_forward_workspace_size(const ssd_dims *dims, ssd_dtype dtype);
+
+/* Kernel 1 of the page ("Kernel 1: Computing cumulative sums"):
+ *   G[b,h,k*T+i] = log2(e) * sum_{s=0..i} A[h] * dt[b, k*T+s, h]
+ * i.e. the inclusive cumsum of a restarted at every chunk, scaled so later
+ * steps can use exp2.  Positions past L hold the chunk's last real value.
+ * In: dt (io), A.  Out: G. */
+SSD_API ssd_status ssd_chunk_cumsum(const ssd_dims *dims, ssd_dtype dtype,
+                            const void *dt, const float *A, float *G,
+                            void *stream);
+
+/* The jump term of the state update (page section "Mamba-2 architecture",
+ * decayed jump formula; the tensor-core product inside fwd_pass_state):
+ *   dstates[b,h,k][p][s] = sum_{j in chunk k}
+ *        exp2(G_last,k - G_j) * dt_j * x[b,j,h,p] * B[b,j,g,s]
+ * i.e. the state chunk k alone would produce from a zero start.
+ * In: x, B, dt (io), G (from ssd_chunk_cumsum).  Out: dstates. */
+SSD_API ssd_status ssd_chunk_state(const ssd_dims *dims, ssd_dtype dtype,
+                           const void *x, const void *B, const void *dt,
+                           const float *G, float *dstates, void *stream);
+
+/* The sequential pass over chunks of the page's fwd_pass_state, which stores
+ * the state at the start of every chunk:
+ *   h = h0 (or 0 if h0 == NULL);  for k in 0..nc-1:
+ *       states[b,h,k] = h;   h = exp2(G_last,k) * h + dstates[b,h,k]
+ *   final_state = h  (skipped if final_state == NULL).
+ * In: dstates, G, h0 (nullable).  Out: states, final_state (nullable). */
+SSD_API ssd_status ssd_state_passing(const ssd_dims *dims, const float *dstates,
+                             const float *G, const float *h0, float *states,
+                             float *final_state, void *stream);
+
+/* The page's compute_out (chunked output equation), per chunk k:
+ *   y_i = exp2(G_i) * states[k] c_i
+ *       + sum_{j<=i in chunk} (c_i . B_j) exp2(G_i - G_j) dt_j x_j
+ *       + D[h] x_i
+ * The T x T interaction tile stays on chip.  D == NULL means D = 0.
+ * In: x, B, C, dt (io), G, states, D.  Out: y (io). */
+SSD_API ssd_status ssd_chunk_scan(const ssd_dims *dims, ssd_dtype dtype,
+                          const void *x, const void *B, const void *C,
+                          const void *dt, const float *G, const float *states,
+                          const float *D, void *y, void *stream);
+
+/* The whole forward pass on one stream: the four steps above (or a fused
+ * equivalent) with G and the per-chunk states kept in `workspace`
+ * (>= ssd_forward_workspace_size bytes, 256-byte aligned).  h0, D and
+ * final_state may be NULL.  Out: y (io), final_state (f32). */
+SSD_API ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                       const void *dt, const float *A, const void *B,
+                       const void *C, const float *D, const float *h0,
+                       void *y, float *final_state, void *workspace,
+                       size_t ws_bytes, void *stream);
+
+/* Synchronises `stream` and reports whether any kernel of this library gave
+ * up a bounded device-side wait since the previous call (SSD_ERR_TIMEOUT;
+ * the outputs of that launch are undefined), then clears the record.  The
+ * record is one word in device memory shared by all calls on the device.
+ * Returns SSD_ERR_CUDA if the synchronisation itself fails. */
+SSD_API ssd_status ssd_device_error(void *stream);
+
+/* ssd_forward with per-launch timing.  `events` holds n_events cudaEvent_t
+ * handles created by the caller; events[0] is recorded on `stream` before
+ * the first launch and events[i+1] right after launch i (while i + 1 <
+ * n_events).  *n_launches (if not NULL) receives the number of kernel
+ * launches the call enqueued.  events may be NULL (then nothing is recorded).
+ * Same arguments, results and errors as ssd_forward otherwise. */
+SSD_API ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype,
+                                        const void *x, const void *dt, const float *A,
+                                        const void *B, const void *C, const float *D,
+                                        const float *h0, void *y, float *final_state,
+                                        void *workspace, size_t ws_bytes, void *stream,
+                                        void *const *events, int n_events,
+                                        int *n_launches);
+
+/* Bytes of device workspace ssd_forward_host needs: room for the device copies
+ * of every input and output plus the workspace of ssd_forward (0 if the dims
+ * are invalid or unsupported). */
+SSD_API size_t ssd_forward_host_workspace_size(const ssd_dims *dims, ssd_dtype dtype,
+                                               int has_D, int has_h0,
+                                               int want_final_state);
+
+/* ssd_forward on HOST buffers: copies x, dt, A, B, C, D, h0 from host memory
+ * into `workspace` (device, >= ssd_forward_host_workspace_size bytes, 256-byte
+ * aligned), runs the forward pass there, and copies y (and final_state, if
+ * not NULL) back to host memory, all enqueued on `stream`.  The host buffers
+ * must stay valid until the stream reaches the end of the call; page-locked
+ * host memory makes the copies asynchronous.  D, h0 and final_state may be
+ * NULL.  Host pointers need no particular alignment. */
+SSD_API ssd_status ssd_forward_host(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                                    const void *dt, const float *A, const void *B,
+                                    const void *C, const float *D, const float *h0,
+                                    void *y, float *final_state, void *workspace,
+                                    size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_GB300_H */

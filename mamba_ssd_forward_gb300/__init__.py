@@ -1,0 +1,195 @@
+"""Mamba-2 chunked SSD forward pass for GB300 (sm_103a).
+
+Thin Python binding over the C ABI in include/ssd.h: it infers the
+dimensions from tensor shapes, allocates outputs and workspace with torch on
+the current CUDA stream, and passes raw device pointers.  All arithmetic runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback.
+
+Tensor layouts (all contiguous, on one CUDA device):
+    x [b, L, nh, P], dt [b, L, nh], B/C [b, L, ng, S] -- float32 or bfloat16
+    A [nh], D [nh], h0 [b, nh, P, S]                   -- float32
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import SSD_BF16, SSD_F32, SsdError  # noqa: F401
+
+__all__ = ["forward", "chunk_cumsum", "chunk_state", "state_passing", "chunk_scan",
+           "workspace_size", "dims_of", "SsdError"]
+
+
+def _io_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSD_F32
+    if t.dtype == torch.bfloat16:
+        return SSD_BF16
+    raise TypeError(f"I/O tensors must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("tensors passed to the SSD library must be contiguous CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _f32(t, name):
+    if t is not None and t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32")
+    return t
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def dims_of(x: torch.Tensor, B: torch.Tensor, chunk: int) -> _abi.SsdDims:
+    b, L, nh, P = x.shape
+    ng, S = B.shape[2], B.shape[3]
+    return _abi.SsdDims(b, L, nh, P, S, ng, int(chunk))
+
+
+def _nchunks(d: _abi.SsdDims) -> int:
+    return (d.seqlen + d.chunk - 1) // d.chunk
+
+
+def workspace_size(x: torch.Tensor, B: torch.Tensor, chunk: int = 256) -> int:
+    d = dims_of(x, B, chunk)
+    return int(_abi.load().ssd_forward_workspace_size(ctypes.byref(d), _io_code(x)))
+
+
+def forward(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, workspace=None,
+            y=None, final_state=None, return_final_state: bool = True):
+    """y, final_state = the SSD forward pass (ssd_forward).
+
+    `workspace`, `y` and `final_state` may be preallocated (a uint8 CUDA
+    tensor of at least workspace_size() bytes, and outputs of the right shape
+    and dtype); otherwise they are allocated here."""
+    lib = _abi.load()
+    d = dims_of(x, B, chunk)
+    io = _io_code(x)
+    ws_need = lib.ssd_forward_workspace_size(ctypes.byref(d), io)
+    if ws_need == 0:
+        raise SsdError("ssd_forward_workspace_size", _abi.SSD_ERR_UNSUPPORTED,
+                       "dimensions are invalid or unsupported")
+    if workspace is None:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=x.device)
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((d.batch, d.nheads, d.headdim, d.dstate),
+                                  dtype=torch.float32, device=x.device)
+    _abi.check("ssd_forward", lib.ssd_forward(
+        ctypes.byref(d), io, _ptr(x), _ptr(dt), _ptr(_f32(A, "A")), _ptr(B), _ptr(C),
+        _ptr(_f32(D, "D")), _ptr(_f32(h0, "h0")), _ptr(y), _ptr(final_state),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream()))
+    return y, final_state
+
+
+def chunk_cumsum(dt, A, chunk: int, headdim: int = 16, dstate: int = 16):
+    """G [b, nh, nc*T] float32 (log2 units) = ssd_chunk_cumsum.  headdim and
+    dstate only need to lie in the supported range; they do not affect G."""
+    lib = _abi.load()
+    b, L, nh = dt.shape
+    d = _abi.SsdDims(b, L, nh, headdim, dstate, 1, int(chunk))
+    G = torch.empty((b, nh, _nchunks(d) * d.chunk), dtype=torch.float32, device=dt.device)
+    _abi.check("ssd_chunk_cumsum", lib.ssd_chunk_cumsum(
+        ctypes.byref(d), _io_code(dt), _ptr(dt), _ptr(_f32(A, "A")), _ptr(G), _stream()))
+    return G
+
+
+def chunk_state(x, B, dt, G, chunk: int):
+    """dstates [b, nh, nc, P, S] float32 = ssd_chunk_state."""
+    lib = _abi.load()
+    d = dims_of(x, B, chunk)
+    out = torch.empty((d.batch, d.nheads, _nchunks(d), d.headdim, d.dstate),
+                      dtype=torch.float32, device=x.device)
+    _abi.check("ssd_chunk_state", lib.ssd_chunk_state(
+        ctypes.byref(d), _io_code(x), _ptr(x), _ptr(B), _ptr(dt), _ptr(_f32(G, "G")),
+        _ptr(out), _stream()))
+    return out
+
+
+def state_passing(dstates, G, h0=None, chunk: int = 256, seqlen: int | None = None,
+                  ngroups: int = 1, return_final_state: bool = True):
+    """states [b, nh, nc, P, S], final_state [b, nh, P, S] = ssd_state_passing."""
+    lib = _abi.load()
+    b, nh, nc, P, S = dstates.shape
+    L = seqlen if seqlen is not None else nc * chunk
+    d = _abi.SsdDims(b, L, nh, P, S, ngroups, int(chunk))
+    states = torch.empty_like(dstates)
+    final = (torch.empty((b, nh, P, S), dtype=torch.float32, device=dstates.device)
+             if return_final_state else None)
+    _abi.check("ssd_state_passing", lib.ssd_state_passing(
+        ctypes.byref(d), _ptr(_f32(dstates, "dstates")), _ptr(_f32(G, "G")),
+        _ptr(_f32(h0, "h0")), _ptr(states), _ptr(final), _stream()))
+    return states, final
+
+
+def chunk_scan(x, B, C, dt, G, states, D=None, chunk: int = 256):
+    """y [b, L, nh, P] (I/O dtype) = ssd_chunk_scan."""
+    lib = _abi.load()
+    d = dims_of(x, B, chunk)
+    y = torch.empty_like(x)
+    _abi.check("ssd_chunk_scan", lib.ssd_chunk_scan(
+        ctypes.byref(d), _io_code(x), _ptr(x), _ptr(B), _ptr(C), _ptr(dt),
+        _ptr(_f32(G, "G")), _ptr(_f32(states, "states")), _ptr(_f32(D, "D")), _ptr(y),
+        _stream()))
+    return y
+
+
+def forward_profiled(x, dt, A, B, C, D, h0, chunk, workspace, y, final_state, events):
+    """ssd_forward recording `events` (torch.cuda.Event, enable_timing) around
+    each of its launches on the current stream; returns the launch count."""
+    lib = _abi.load()
+    d = dims_of(x, B, chunk)
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event on its first record
+            e.record()
+    handles = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    n = ctypes.c_int(0)
+    _abi.check("ssd_forward_profiled", lib.ssd_forward_profiled(
+        ctypes.byref(d), _io_code(x), _ptr(x), _ptr(dt), _ptr(_f32(A, "A")), _ptr(B), _ptr(C),
+        _ptr(_f32(D, "D")), _ptr(_f32(h0, "h0")), _ptr(y), _ptr(final_state), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(), handles, len(events),
+        ctypes.byref(n)))
+    return n.value
+
+
+def host_workspace_size(x, B, chunk, has_D=True, has_h0=False, want_final_state=True) -> int:
+    d = dims_of(x, B, chunk)
+    return int(_abi.load().ssd_forward_host_workspace_size(
+        ctypes.byref(d), _io_code(x), int(has_D), int(has_h0), int(want_final_state)))
+
+
+def _host_ptr(t):
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError("ssd_forward_host takes contiguous host tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def forward_host(x, dt, A, B, C, D, h0, chunk, workspace, y, final_state=None):
+    """ssd_forward_host: host tensors in (x, dt, A, B, C, D, h0) and out (y,
+    final_state), a device uint8 `workspace` of host_workspace_size() bytes.
+    Enqueued on the current stream; synchronise before reading y."""
+    lib = _abi.load()
+    d = dims_of(x, B, chunk)
+    if not workspace.is_cuda:
+        raise ValueError("the workspace of ssd_forward_host lives on the device")
+    _abi.check("ssd_forward_host", lib.ssd_forward_host(
+        ctypes.byref(d), _io_code(x), _host_ptr(x), _host_ptr(dt), _host_ptr(A), _host_ptr(B),
+        _host_ptr(C), _host_ptr(D), _host_ptr(h0), _host_ptr(y), _host_ptr(final_state),
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream()))
+
+
+def device_error() -> None:
+    """Synchronise the current stream and raise SsdError if a kernel of the
+    library gave up a bounded wait since the last check."""
+    _abi.check("ssd_device_error", _abi.load().ssd_device_error(_stream()))

@@ -1,0 +1,273 @@
+// C ABI of libssd_gb300: argument validation, workspace layout and the
+// launch sequence.  Every computation happens in the kernels; this file only
+// checks arguments and enqueues launches on the caller's stream.
+#include <cstdint>
+
+#include "ssd_internal.cuh"
+
+namespace {
+
+using ssd::Dims;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by every entry point.  INVALID_ARG for malformed
+// shapes, UNSUPPORTED for well-formed shapes outside the supported range.
+ssd_status check_dims(const ssd_dims *in, Dims *out) {
+  if (!in) return SSD_ERR_INVALID_ARG;
+  const ssd_dims d = *in;
+  if (d.batch < 1 || d.seqlen < 1 || d.nheads < 1 || d.headdim < 1 || d.dstate < 1 ||
+      d.ngroups < 1 || d.chunk < 1)
+    return SSD_ERR_INVALID_ARG;
+  if (d.nheads % d.ngroups != 0) return SSD_ERR_INVALID_ARG;
+  if (d.headdim % 16 || d.headdim > 128 || d.dstate % 16 || d.dstate > 256)
+    return SSD_ERR_UNSUPPORTED;
+  if (d.chunk != 64 && d.chunk != 128 && d.chunk != 256) return SSD_ERR_UNSUPPORTED;
+  // Grid limits (batch and heads index grid dimensions) and 62-bit element
+  // counts for every tensor.
+  if (d.batch > 65535 || d.nheads > 65535) return SSD_ERR_UNSUPPORTED;
+  const int64_t nc = (d.seqlen + d.chunk - 1) / d.chunk;
+  const double big = 4.0e18;
+  if ((double)d.batch * d.seqlen * d.nheads * d.headdim > big ||
+      (double)d.batch * d.nheads * nc * d.headdim * d.dstate > big ||
+      (double)d.batch * d.seqlen * d.ngroups * d.dstate > big || nc > (int64_t)1 << 31)
+    return SSD_ERR_UNSUPPORTED;
+  out->b = d.batch;
+  out->L = d.seqlen;
+  out->nh = d.nheads;
+  out->P = d.headdim;
+  out->S = d.dstate;
+  out->ng = d.ngroups;
+  out->T = d.chunk;
+  out->nc = nc;
+  out->hpg = d.nheads / d.ngroups;
+  return SSD_OK;
+}
+
+bool valid_dtype(ssd_dtype t) { return t == SSD_F32 || t == SSD_BF16; }
+
+// Required pointer: non-null and 16-byte aligned.
+bool req(const void *p) { return p && aligned16(p); }
+// Optional pointer: null, or 16-byte aligned.
+bool opt(const void *p) { return !p || aligned16(p); }
+
+ssd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
+
+// Workspace of ssd_forward: G, then dstates, then states, each 256-byte
+// aligned.
+struct WsLayout {
+  size_t G, dstates, states, total;
+};
+
+size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
+
+WsLayout ws_layout(const Dims &d) {
+  WsLayout w;
+  w.G = 0;
+  w.dstates = round256(sizeof(float) * d.b * d.nh * d.nc * d.T);
+  const size_t st = round256(sizeof(float) * d.b * d.nh * d.nc * d.P * d.S);
+  w.states = w.dstates + st;
+  w.total = w.states + st;
+  return w;
+}
+
+size_t io_size(ssd_dtype t) { return t == SSD_BF16 ? 2 : 4; }
+
+// Device workspace of ssd_forward_host: the forward's own workspace, then a
+// device copy of every input and output, each 256-byte aligned.
+struct HostLayout {
+  size_t fwd, fwd_bytes, x, dt, A, B, C, D, h0, y, fin, total;
+};
+
+HostLayout host_layout(const Dims &d, ssd_dtype t, int has_D, int has_h0, int has_fin) {
+  HostLayout h;
+  const size_t e = io_size(t);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += round256(bytes);
+    return at;
+  };
+  h.fwd_bytes = ws_layout(d).total;
+  h.fwd = take(h.fwd_bytes);
+  h.x = take(e * d.b * d.L * d.nh * d.P);
+  h.dt = take(e * d.b * d.L * d.nh);
+  h.A = take(sizeof(float) * d.nh);
+  h.B = take(e * d.b * d.L * d.ng * d.S);
+  h.C = take(e * d.b * d.L * d.ng * d.S);
+  h.D = take(has_D ? sizeof(float) * d.nh : 0);
+  h.h0 = take(has_h0 ? sizeof(float) * d.b * d.nh * d.P * d.S : 0);
+  h.y = take(e * d.b * d.L * d.nh * d.P);
+  h.fin = take(has_fin ? sizeof(float) * d.b * d.nh * d.P * d.S : 0);
+  h.total = off;
+  return h;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ssd_status_string(ssd_status s) {
+  switch (s) {
+    case SSD_OK: return "SSD_OK";
+    case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG: null, misaligned or malformed argument";
+    case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: dimensions outside the supported range";
+    case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA call or kernel launch failed";
+    case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: a bounded device-side wait gave up";
+  }
+  return "SSD_ERR_UNKNOWN";
+}
+
+ssd_status ssd_device_error(void *stream) {
+  int code = 0;
+  if (ssd::read_and_clear_device_error((cudaStream_t)stream, &code) != cudaSuccess)
+    return SSD_ERR_CUDA;
+  return code ? SSD_ERR_TIMEOUT : SSD_OK;
+}
+
+size_t ssd_forward_workspace_size(const ssd_dims *dims, ssd_dtype dtype) {
+  Dims d;
+  if (!valid_dtype(dtype) || check_dims(dims, &d) != SSD_OK) return 0;
+  return ws_layout(d).total;
+}
+
+ssd_status ssd_chunk_cumsum(const ssd_dims *dims, ssd_dtype dtype, const void *dt,
+                            const float *A, float *G, void *stream) {
+  Dims d;
+  ssd_status s = check_dims(dims, &d);
+  if (s != SSD_OK) return s;
+  if (!valid_dtype(dtype) || !req(dt) || !req(A) || !req(G)) return SSD_ERR_INVALID_ARG;
+  return from_cuda(ssd::launch_chunk_cumsum(d, dtype, dt, A, G, (cudaStream_t)stream));
+}
+
+ssd_status ssd_chunk_state(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                           const void *B, const void *dt, const float *G, float *dstates,
+                           void *stream) {
+  Dims d;
+  ssd_status s = check_dims(dims, &d);
+  if (s != SSD_OK) return s;
+  if (!valid_dtype(dtype) || !req(x) || !req(B) || !req(dt) || !req(G) || !req(dstates))
+    return SSD_ERR_INVALID_ARG;
+  return from_cuda(
+      ssd::launch_chunk_state(d, dtype, x, B, dt, G, dstates, (cudaStream_t)stream));
+}
+
+ssd_status ssd_state_passing(const ssd_dims *dims, const float *dstates, const float *G,
+                             const float *h0, float *states, float *final_state,
+                             void *stream) {
+  Dims d;
+  ssd_status s = check_dims(dims, &d);
+  if (s != SSD_OK) return s;
+  if (!req(dstates) || !req(G) || !opt(h0) || !req(states) || !opt(final_state))
+    return SSD_ERR_INVALID_ARG;
+  return from_cuda(ssd::launch_state_passing(d, dstates, G, h0, states, final_state,
+                                             (cudaStream_t)stream));
+}
+
+ssd_status ssd_chunk_scan(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *B,
+                          const void *C, const void *dt, const float *G, const float *states,
+                          const float *D, void *y, void *stream) {
+  Dims d;
+  ssd_status s = check_dims(dims, &d);
+  if (s != SSD_OK) return s;
+  if (!valid_dtype(dtype) || !req(x) || !req(B) || !req(C) || !req(dt) || !req(G) ||
+      !req(states) || !opt(D) || !req(y))
+    return SSD_ERR_INVALID_ARG;
+  return from_cuda(ssd::launch_chunk_scan(d, dtype, x, B, C, dt, G, states, D, y,
+                                          (cudaStream_t)stream));
+}
+
+ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
+                       const float *A, const void *B, const void *C, const float *D,
+                       const float *h0, void *y, float *final_state, void *workspace,
+                       size_t ws_bytes, void *stream) {
+  return ssd_forward_profiled(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, workspace,
+                              ws_bytes, stream, nullptr, 0, nullptr);
+}
+
+ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                                const void *dt, const float *A, const void *B, const void *C,
+                                const float *D, const float *h0, void *y, float *final_state,
+                                void *workspace, size_t ws_bytes, void *stream,
+                                void *const *events, int n_events, int *n_launches) {
+  Dims d;
+  ssd_status s = check_dims(dims, &d);
+  if (s != SSD_OK) return s;
+  if (!valid_dtype(dtype) || !req(x) || !req(dt) || !req(A) || !req(B) || !req(C) ||
+      !opt(D) || !opt(h0) || !req(y) || !opt(final_state) || !workspace ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) || n_events < 0)
+    return SSD_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(d);
+  if (ws_bytes < w.total) return SSD_ERR_INVALID_ARG;
+  char *ws = static_cast<char *>(workspace);
+  float *G = reinterpret_cast<float *>(ws + w.G);
+  float *dst = reinterpret_cast<float *>(ws + w.dstates);
+  float *sts = reinterpret_cast<float *>(ws + w.states);
+  cudaStream_t st = (cudaStream_t)stream;
+  int launched = 0;
+  auto mark = [&](int i) -> cudaError_t {
+    if (events && i < n_events) return cudaEventRecord((cudaEvent_t)events[i], st);
+    return cudaSuccess;
+  };
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = ssd::launch_chunk_cumsum(d, dtype, dt, A, G, st);
+  if (e == cudaSuccess && ++launched) e = mark(launched);
+  if (e == cudaSuccess) e = ssd::launch_chunk_state(d, dtype, x, B, dt, G, dst, st);
+  if (e == cudaSuccess && ++launched) e = mark(launched);
+  if (e == cudaSuccess) e = ssd::launch_state_passing(d, dst, G, h0, sts, final_state, st);
+  if (e == cudaSuccess && ++launched) e = mark(launched);
+  if (e == cudaSuccess) e = ssd::launch_chunk_scan(d, dtype, x, B, C, dt, G, sts, D, y, st);
+  if (e == cudaSuccess && ++launched) e = mark(launched);
+  if (n_launches) *n_launches = launched;
+  return from_cuda(e);
+}
+
+size_t ssd_forward_host_workspace_size(const ssd_dims *dims, ssd_dtype dtype, int has_D,
+                                       int has_h0, int want_final_state) {
+  Dims d;
+  if (!valid_dtype(dtype) || check_dims(dims, &d) != SSD_OK) return 0;
+  return host_layout(d, dtype, has_D, has_h0, want_final_state).total;
+}
+
+ssd_status ssd_forward_host(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                            const void *dt, const float *A, const void *B, const void *C,
+                            const float *D, const float *h0, void *y, float *final_state,
+                            void *workspace, size_t ws_bytes, void *stream) {
+  Dims d;
+  ssd_status s = check_dims(dims, &d);
+  if (s != SSD_OK) return s;
+  if (!valid_dtype(dtype) || !x || !dt || !A || !B || !C || !y || !workspace ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return SSD_ERR_INVALID_ARG;
+  const HostLayout hl = host_layout(d, dtype, D != nullptr, h0 != nullptr, final_state != nullptr);
+  if (ws_bytes < hl.total) return SSD_ERR_INVALID_ARG;
+  char *ws = static_cast<char *>(workspace);
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t e = io_size(dtype);
+  cudaError_t err = cudaSuccess;
+  auto h2d = [&](size_t off, const void *src, size_t bytes) {
+    if (err == cudaSuccess && src)
+      err = cudaMemcpyAsync(ws + off, src, bytes, cudaMemcpyHostToDevice, st);
+  };
+  h2d(hl.x, x, e * d.b * d.L * d.nh * d.P);
+  h2d(hl.dt, dt, e * d.b * d.L * d.nh);
+  h2d(hl.A, A, sizeof(float) * d.nh);
+  h2d(hl.B, B, e * d.b * d.L * d.ng * d.S);
+  h2d(hl.C, C, e * d.b * d.L * d.ng * d.S);
+  h2d(hl.D, D, sizeof(float) * d.nh);
+  h2d(hl.h0, h0, sizeof(float) * d.b * d.nh * d.P * d.S);
+  if (err != cudaSuccess) return SSD_ERR_CUDA;
+  s = ssd_forward(dims, dtype, ws + hl.x, ws + hl.dt, reinterpret_cast<float *>(ws + hl.A),
+                  ws + hl.B, ws + hl.C, D ? reinterpret_cast<float *>(ws + hl.D) : nullptr,
+                  h0 ? reinterpret_cast<float *>(ws + hl.h0) : nullptr, ws + hl.y,
+                  final_state ? reinterpret_cast<float *>(ws + hl.fin) : nullptr, ws + hl.fwd,
+                  hl.fwd_bytes, stream);
+  if (s != SSD_OK) return s;
+  err = cudaMemcpyAsync(y, ws + hl.y, e * d.b * d.L * d.nh * d.P, cudaMemcpyDeviceToHost, st);
+  if (err == cudaSuccess && final_state)
+    err = cudaMemcpyAsync(final_state, ws + hl.fin, sizeof(float) * d.b * d.nh * d.P * d.S,
+                          cudaMemcpyDeviceToHost, st);
+  return from_cuda(err);
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// Step 3: the sequential pass over chunks (the loop of the page's
+// fwd_pass_state, "Kernel 2"), given every chunk's jump term:
+//
+//   h = h0;  for k: states[k] = h;  h = exp2(G_last,k) h + dstates[k]
+//   final_state = h
+//
+// A bandwidth kernel: each thread owns four consecutive elements of one
+// (batch, head) state and walks the chunks; one read of dstates, one write
+// of states.  The loads of the next chunk's dstates are issued before the
+// current chunk's stores so that each thread keeps two loads in flight.
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads)
+state_passing_kernel(const float4 *__restrict__ dstates,
+                     const float *__restrict__ G, const float4 *__restrict__ h0,
+                     float4 *__restrict__ states, float4 *__restrict__ final_state,
+                     int64_t ps4, int64_t nc, int64_t T) {
+  const int64_t bh = blockIdx.y;
+  const int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x;  // float4 index in P*S
+  if (e >= ps4) return;
+  float4 h = h0 ? h0[bh * ps4 + e] : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float *Gbh = G + bh * nc * T;
+  const float4 *dsrc = dstates + bh * nc * ps4 + e;
+  float4 *sdst = states + bh * nc * ps4 + e;
+  float4 next = nc > 0 ? dsrc[0] : h;
+  for (int64_t k = 0; k < nc; ++k) {
+    const float4 cur = next;
+    if (k + 1 < nc) next = dsrc[(k + 1) * ps4];
+    const float decay = exp2f(Gbh[k * T + T - 1]);
+    sdst[k * ps4] = h;
+    h.x = fmaf(decay, h.x, cur.x);
+    h.y = fmaf(decay, h.y, cur.y);
+    h.z = fmaf(decay, h.z, cur.z);
+    h.w = fmaf(decay, h.w, cur.w);
+  }
+  if (final_state) final_state[bh * ps4 + e] = h;
+}
+
+}  // namespace
+
+cudaError_t launch_state_passing(const Dims &d, const float *dstates,
+                                 const float *G, const float *h0,
+                                 float *states, float *final_state,
+                                 cudaStream_t st) {
+  const int64_t ps4 = d.P * d.S / 4;
+  dim3 grid((unsigned)((ps4 + kThreads - 1) / kThreads), (unsigned)(d.b * d.nh));
+  state_passing_kernel<<<grid, kThreads, 0, st>>>(
+      reinterpret_cast<const float4 *>(dstates), G,
+      reinterpret_cast<const float4 *>(h0), reinterpret_cast<float4 *>(states),
+      reinterpret_cast<float4 *>(final_state), ps4, d.nc, d.T);
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

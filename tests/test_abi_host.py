@@ -1,0 +1,136 @@
+"""Host-side checks of the C ABI: the library builds, loads, exports every
+symbol include/ssd.h declares, and rejects bad arguments before launching
+anything (so these run without a GPU)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mamba_ssd_forward_gb300 import _abi, build
+    build.build()
+    return _abi.load()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"SSD_API\s+[\w\s\*]+?\b(\w+)\s*\(", src))
+    return names
+
+
+def test_header_declares_the_five_steps():
+    names = declared_functions()
+    for n in ("ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
+              "ssd_chunk_scan", "ssd_forward", "ssd_forward_workspace_size",
+              "ssd_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from mamba_ssd_forward_gb300 import _abi
+    out = subprocess.run(["nm", "-D", "--defined-only", _abi.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(lib, n)
+    assert set(_abi.EXPORTS) == declared_functions()
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = lib.ssd_status_string(code).decode()
+        assert s.startswith("SSD_")
+    assert lib.ssd_status_string(77).decode() == "SSD_ERR_UNKNOWN"
+
+
+def dims(**kw):
+    from mamba_ssd_forward_gb300 import _abi
+    base = dict(batch=2, seqlen=1000, nheads=8, headdim=64, dstate=128, ngroups=2, chunk=256)
+    base.update(kw)
+    return _abi.SsdDims(**base)
+
+
+def test_workspace_size(lib):
+    d = dims()
+    nc = 4
+    ws = lib.ssd_forward_workspace_size(ctypes.byref(d), 1)
+    assert ws >= 4 * 2 * 8 * nc * 256 + 2 * 4 * 2 * 8 * nc * 64 * 128
+    assert ws % 256 == 0
+    assert lib.ssd_forward_workspace_size(ctypes.byref(d), 7) == 0
+    assert lib.ssd_forward_workspace_size(None, 1) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ngroups=3), 1),            # nh % ng != 0
+    (dict(batch=0), 1),
+    (dict(seqlen=0), 1),
+    (dict(headdim=48 + 1), 2),       # not a multiple of 16
+    (dict(headdim=144), 2),          # > 128
+    (dict(dstate=272), 2),           # > 256
+    (dict(dstate=8), 2),
+    (dict(chunk=96), 2),
+    (dict(chunk=512), 2),
+])
+def test_rejects_bad_dims_before_launch(lib, kw, code):
+    d = dims(**kw)
+    fake = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: validation fails first
+    assert lib.ssd_chunk_cumsum(ctypes.byref(d), 1, fake, fake, fake, None) == code
+    assert lib.ssd_forward_workspace_size(ctypes.byref(d), 1) == 0
+    rc = lib.ssd_forward(ctypes.byref(d), 1, fake, fake, fake, fake, fake, None, None, fake,
+                         None, fake, 1 << 40, None)
+    assert rc == code
+
+
+def test_rejects_null_and_misaligned_pointers(lib):
+    d = dims()
+    ok = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p((1 << 20) + 4)
+    assert lib.ssd_chunk_cumsum(ctypes.byref(d), 1, None, ok, ok, None) == 1
+    assert lib.ssd_chunk_cumsum(ctypes.byref(d), 1, bad, ok, ok, None) == 1
+    assert lib.ssd_chunk_cumsum(ctypes.byref(d), 5, ok, ok, ok, None) == 1  # dtype
+    assert lib.ssd_chunk_state(ctypes.byref(d), 1, ok, ok, ok, ok, None, None) == 1
+    assert lib.ssd_state_passing(ctypes.byref(d), ok, ok, bad, ok, None, None) == 1
+    assert lib.ssd_chunk_scan(ctypes.byref(d), 1, ok, ok, ok, ok, ok, ok, bad, ok, None) == 1
+    ws = lib.ssd_forward_workspace_size(ctypes.byref(d), 1)
+    # workspace too small, and workspace not 256-byte aligned
+    assert lib.ssd_forward(ctypes.byref(d), 1, ok, ok, ok, ok, ok, None, None, ok, None,
+                           ok, ws - 1, None) == 1
+    assert lib.ssd_forward(ctypes.byref(d), 1, ok, ok, ok, ok, ok, None, None, ok, None,
+                           ctypes.c_void_p((1 << 20) + 16), ws, None) == 1
+    assert lib.ssd_chunk_cumsum(None, 1, ok, ok, ok, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from mamba_ssd_forward_gb300 import _abi
+    with pytest.raises(RuntimeError, match="missing"):
+        _abi.load(str(tmp_path / "nope.so"))
+
+
+def test_product_path_never_touches_the_oracle():
+    """The package and the CUDA sources do not import, load or name the
+    oracle; the oracle does not import the package."""
+    pkg = os.path.join(ROOT, "mamba_ssd_forward_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, fn)).read()
+                for pat in (r"\bimport\s+oracle", r"\bfrom\s+oracle", r"ssd_oracle",
+                            r"libssd_oracle"):
+                    assert not re.search(pat, src), (fn, pat)
+    for fn in os.listdir(os.path.join(ROOT, "oracle")):
+        if fn.endswith((".py", ".c")):
+            src = open(os.path.join(ROOT, "oracle", fn)).read()
+            assert "mamba_ssd_forward_gb300" not in src, fn
