@@ -9,172 +9,300 @@
 // The causal mask keeps the diagonal (post-update convention), and the
 // retained exponents G_i - G_j are <= 0 because every a_t <= 0.
 //
-// First-cut SIMT kernel: one block per (64-row tile of a chunk, 64-wide
-// headdim tile, head, batch).  The 64 x 32 interaction blocks are formed in
-// shared memory, decayed and masked there, and never written to memory.
-#include "ssd_internal.cuh"
+// Tensor-core kernel (tcgen05).  One CTA per (128-row tile i of a chunk,
+// chunk, head, batch), 128 threads (thread = row = TMEM lane):
+//   phase 1, over 128-byte blocks of S:  TMA stages C (rows i) and B (rows
+//     j <= the tile's last row); the threads stage the carried state h
+//     (fp32 -> operand type); one thread issues
+//       Yoff += C h^T      (M = 128, N = P)
+//       S    += C B^T      (M = 128, N = tokens j)
+//     into tensor memory;
+//   phase 2, over 128-byte blocks of tokens j:  each thread reads its row of
+//     S from TMEM, applies exp2(G_i - G_j) dt_j and the causal mask, and
+//     writes the row into a K-major swizzled tile; TMA stages x_j; one thread
+//     issues Ydiag += S' X  (M = 128, N = P, X as an MN-major operand);
+//   epilogue: y_i = exp2(G_i) Yoff_i + Ydiag_i + D x_i, stored in the I/O
+//     type.  The T x T interaction tile lives only in TMEM and shared memory.
+// With fp32 I/O (kind::tf32, K-major operands only) the threads stage x
+// transposed in phase 2 instead of TMA.
+#include "tc_common.cuh"
 
 namespace ssd {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kRows = 64;   // rows i per block
-constexpr int kCols = 64;   // headdim p per block
-constexpr int kJ = 32;      // tokens j per interaction block
-constexpr int kSc = 32;     // state entries s per staging step
+constexpr int kThreads = 128;
+constexpr int kRows = 128;  // rows i per CTA (MMA M)
 
 template <typename IO>
 __global__ void __launch_bounds__(kThreads)
-chunk_scan_simt(const IO *__restrict__ x, const IO *__restrict__ Bm,
-                const IO *__restrict__ Cm, const IO *__restrict__ dt,
-                const float *__restrict__ G, const float *__restrict__ states,
-                const float *__restrict__ Dv, IO *__restrict__ y, int64_t L,
-                int64_t nh, int64_t P, int64_t S, int64_t ng, int64_t T,
-                int64_t nc) {
-  __shared__ float cs[kRows][kSc + 1];
-  __shared__ float hs[kCols][kSc + 1];
-  __shared__ float bs[kJ][kSc + 1];
-  __shared__ float sb[kRows][kJ + 1];
-  __shared__ float xs[kJ][kCols];
-  __shared__ float gi[kRows];
+chunk_scan_tc(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
+              const __grid_constant__ CUtensorMap tm_x, const IO *__restrict__ x,
+              const IO *__restrict__ dt, const float *__restrict__ G,
+              const float *__restrict__ states, const float *__restrict__ Dv,
+              IO *__restrict__ y, int *__restrict__ err, int L, int nh, int P, int S, int hpg,
+              int T, int nc) {
+  using Tr = IoT<IO>;
+  constexpr int kAE = Tr::kAE;
+  constexpr int kE = Tr::kE;
+  constexpr int kC = kRows * 128;  // bytes of the C block (128 rows)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ __align__(8) uint64_t full[2], mmad[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ float Gs[256], dts[256];
 
-  const int64_t ptiles = (P + kCols - 1) / kCols, itiles = T / kRows;
-  int64_t r = blockIdx.x;
-  const int64_t pt = r % ptiles;
-  r /= ptiles;
-  const int64_t it = r % itiles;
-  const int64_t k = r / itiles;
-  const int64_t h = blockIdx.y, b = blockIdx.z, g = h / (nh / ng);
-  const int64_t row0 = k * T + it * kRows;  // first token of this tile
-  if (row0 >= L) return;
-  const float *Gc = G + ((b * nh + h) * nc + k) * T;
-  const float *hst = states + ((b * nh + h) * nc + k) * P * S;
-  const int tid = threadIdx.x, ti = tid / 16, tp = tid % 16;
+  const int n_it = (T + kRows - 1) / kRows;
+  const int k = blockIdx.x / n_it, it = blockIdx.x % n_it;
+  const int h = blockIdx.y, b = blockIdx.z, g = h / hpg;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int tok0 = k * T;
+  const int valid = min(T, L - tok0);            // real tokens in this chunk
+  const int i0 = it * kRows;                     // first row (chunk-relative)
+  if (i0 >= valid) return;                       // whole tile past the end
+  const int jext = min(min(T, i0 + kRows), (valid + 15) & ~15);  // tokens j used
+  const int nBr = (jext + 127) / 128;            // 128-row B boxes
+  const int nsb = (S + kAE - 1) / kAE;           // phase-1 blocks along S
+  const int njb = (jext + kAE - 1) / kAE;        // phase-2 blocks along j
+  const int nPb = (P + kAE - 1) / kAE;
+  // phase-1 stage: C (128 rows) | B (nBr*128 rows) | h (P rows), 128 B each
+  const int st1 = kC + nBr * 128 * 128 + ((P * 128 + 1023) & ~1023);
+  // phase-2 stage: S' (128 rows x 128 B) | X (nPb blocks of kAE rows)
+  const int st2 = kC + nPb * kAE * 128;
+  const uint32_t col_S = 0, col_off = 256, col_diag = 256 + P;
+  const uint32_t ncols = 512;
 
-  if (tid < kRows) gi[tid] = Gc[it * kRows + tid];
-
-  // Carried-state term: sum_s C_i[s] h[p][s].
-  float acc_off[4][4] = {};
-  for (int64_t s0 = 0; s0 < S; s0 += kSc) {
-    for (int idx = tid; idx < kRows * kSc; idx += kThreads) {
-      const int rr = idx / kSc, c = idx % kSc;
-      const int64_t tok = row0 + rr, s = s0 + c;
-      cs[rr][c] = (tok < L && s < S) ? ld_io(Cm + ((b * L + tok) * ng + g) * S + s) : 0.f;
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&mmad[i], 1);
     }
-    for (int idx = tid; idx < kCols * kSc; idx += kThreads) {
-      const int pp = idx / kSc, c = idx % kSc;
-      const int64_t p = pt * kCols + pp, s = s0 + c;
-      hs[pp][c] = (p < P && s < S) ? hst[p * S + s] : 0.f;
-    }
-    __syncthreads();
-    for (int c = 0; c < kSc; ++c) {
-      float cv[4], hv[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        cv[q] = cs[ti * 4 + q][c];
-        hv[q] = hs[tp * 4 + q][c];
-      }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc_off[a][e] = fmaf(cv[a], hv[e], acc_off[a][e]);
-    }
-    __syncthreads();
+    ptx::fence_mbar_init();
   }
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_slot, ncols);
+    ptx::tmem_relinquish();
+  }
+  const float *Gc = G + ((int64_t)(b * nh + h) * nc + k) * T;
+  for (int j = tid; j < T; j += kThreads) {
+    Gs[j] = Gc[j];
+    dts[j] = j < valid ? ld_io(dt + ((int64_t)b * L + tok0 + j) * nh + h) : 0.f;
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const float *hst = states + ((int64_t)(b * nh + h) * nc + k) * P * S;
 
-  // Intra-chunk term over j-blocks up to the tile's last row.
-  float acc[4][4] = {};
-  const int64_t jend = (it + 1) * kRows;  // chunk-relative
-  for (int64_t j0 = 0; j0 < jend; j0 += kJ) {
-    // sb[i][j] = c_i . B_j, accumulated over s in steps of kSc.
-    float sacc[8] = {};
-    const int si = tid / 4, sj = (tid % 4) * 8;
-    for (int64_t s0 = 0; s0 < S; s0 += kSc) {
-      for (int idx = tid; idx < kRows * kSc; idx += kThreads) {
-        const int rr = idx / kSc, c = idx % kSc;
-        const int64_t tok = row0 + rr, s = s0 + c;
-        cs[rr][c] = (tok < L && s < S) ? ld_io(Cm + ((b * L + tok) * ng + g) * S + s) : 0.f;
-      }
-      for (int idx = tid; idx < kJ * kSc; idx += kThreads) {
-        const int jj = idx / kSc, c = idx % kSc;
-        const int64_t tok = k * T + j0 + jj, s = s0 + c;
-        bs[jj][c] = (tok < L && s < S) ? ld_io(Bm + ((b * L + tok) * ng + g) * S + s) : 0.f;
-      }
-      __syncthreads();
-      for (int c = 0; c < kSc; ++c) {
-        const float cv = cs[si][c];
+  // ---------------- phase 1: Yoff = C h^T, S = C B^T over blocks of S
+  auto load1 = [&](int sb) {
+    const int s = sb & 1;
+    uint8_t *Cb = smem + s * st1;
+    uint8_t *Bb = Cb + kC;
+    ptx::mbar_arrive_expect_tx(&full[s], kC + nBr * 128 * 128);
+    ptx::tma_load_4d(Cb, &tm_C, sb * kAE, g, tok0 + i0, b, &full[s]);
+    for (int r = 0; r < nBr; ++r)
+      ptx::tma_load_4d(Bb + r * 128 * 128, &tm_B, sb * kAE, g, tok0 + r * 128, b, &full[s]);
+  };
+  if (tid == 0)
+    for (int sb = 0; sb < min(nsb, 2); ++sb) load1(sb);
+
+  const uint32_t id_off = mma_idesc<IO>(128, P, false, false);
+  const uint32_t id_S = mma_idesc<IO>(128, jext, false, false);
+  for (int sb = 0; sb < nsb; ++sb) {
+    const int s = sb & 1;
+    const uint32_t ph = (sb >> 1) & 1;
+    uint8_t *Cb = smem + s * st1;
+    uint8_t *Bb = Cb + kC;
+    uint8_t *Hb = Bb + nBr * 128 * 128;
+    // stage h[:, sb*kAE .. +kAE) as a K-major operand (rows p, 128 B each)
+    for (int c = tid; c < P * 8; c += kThreads) {
+      const int p = c >> 3, ch = c & 7;
+      const int s_first = sb * kAE + ch * (16 / kE);
+      float v[8];
+      if (s_first < S) {
+        const float4 *src = reinterpret_cast<const float4 *>(hst + (int64_t)p * S + s_first);
+        const float4 a = src[0];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        if (kE == 2) {
+          const float4 bq = src[1];
+          v[4] = bq.x; v[5] = bq.y; v[6] = bq.z; v[7] = bq.w;
+        }
+      } else {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) sacc[q] = fmaf(cv, bs[sj + q][c], sacc[q]);
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
       }
-      __syncthreads();
+      *reinterpret_cast<uint4 *>(Hb + sw128(p, ch * 16)) = pack_op16(v, (IO *)nullptr);
     }
-    // Decay, dt and causal mask (diagonal kept); padded tokens have dt = 0.
-    {
-      const int64_t i_rel = it * kRows + si;
+    ptx::mbar_wait(&full[s], ph, err, 41);
+    ptx::fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      ptx::tc_fence_after();
+      const uint32_t c0 = ptx::smem_u32(Cb), b0 = ptx::smem_u32(Bb), h0 = ptx::smem_u32(Hb);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int64_t j_rel = j0 + sj + q, tok = k * T + j_rel;
+      for (int kk = 0; kk < kAE / Tr::kKmma; ++kk) {
+        const uint32_t adv = kk * 32;  // K step inside the 128-byte row
+        const uint64_t ad = ptx::smem_desc(c0 + adv, 16, 1024, ptx::kSw128);
+        const uint64_t hd = ptx::smem_desc(h0 + adv, 16, 1024, ptx::kSw128);
+        const uint64_t bd = ptx::smem_desc(b0 + adv, 16, 1024, ptx::kSw128);
+        const uint32_t acc = (sb | kk) ? 1u : 0u;
+        ptx::mma_ss<Tr::kTf32>(tmem + col_off, ad, hd, id_off, acc);
+        ptx::mma_ss<Tr::kTf32>(tmem + col_S, ad, bd, id_S, acc);
+      }
+      ptx::mma_commit(&mmad[s]);
+      if (sb + 2 < nsb) {
+        ptx::mbar_wait(&mmad[s], ph, err, 42);
+        load1(sb + 2);
+      }
+    }
+  }
+  ptx::mbar_wait(&mmad[(nsb - 1) & 1], ((nsb - 1) >> 1) & 1, err, 43);
+  ptx::tc_fence_after();
+  __syncthreads();  // every thread is past phase 1 before its buffers are reused
+
+  // ---------------- phase 2: Ydiag = (S * decay * mask) X over blocks of j
+  const int row = warp * 32 + lane;  // this thread's row of the tile
+  const int i_rel = i0 + row;        // chunk-relative row index
+  const float Gi = Gs[min(i_rel, T - 1)];
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  // the phase-1 pipeline left its barriers at a known phase count: continue
+  // the parity sequence from there.
+  const int base1 = nsb;
+  auto load2 = [&](int jb) {
+    const int u = base1 + jb, s = u & 1;
+    uint8_t *Xb = smem + s * st2 + kC;
+    ptx::mbar_arrive_expect_tx(&full[s], nPb * kAE * 128);
+    for (int pb = 0; pb < nPb; ++pb)
+      ptx::tma_load_4d(Xb + pb * kAE * 128, &tm_x, pb * kAE, h, tok0 + jb * kAE, b, &full[s]);
+  };
+  if (!Tr::kTf32 && tid == 0)
+    for (int jb = 0; jb < min(njb, 2); ++jb) load2(jb);
+
+  const uint32_t id_diag = mma_idesc<IO>(128, P, false, !Tr::kTf32);
+  for (int jb = 0; jb < njb; ++jb) {
+    const int u = base1 + jb, s = u & 1;
+    const uint32_t ph = (u >> 1) & 1;
+    uint8_t *Pb = smem + s * st2;
+    uint8_t *Xb = Pb + kC;
+    // this thread's row of S for tokens jb*kAE .. +kAE -> decayed, masked
+#pragma unroll
+    for (int q = 0; q < kAE / 16; ++q) {
+      float v[16];
+      ptx::tmem_ld16_sync(tmem + lane_base + col_S + jb * kAE + q * 16, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int j = jb * kAE + q * 16 + e;
+        v[e] = (j <= i_rel && j < valid) ? v[e] * exp2f(Gi - Gs[j]) * dts[j] : 0.f;
+      }
+      constexpr int per16 = 16 / kE;  // values per 16-byte chunk
+#pragma unroll
+      for (int c = 0; c < 16 / per16; ++c) {
+        const int chunk = (q * 16) / per16 + c;
+        *reinterpret_cast<uint4 *>(Pb + sw128(row, chunk * 16)) =
+            pack_op16(v + c * per16, (IO *)nullptr);
+      }
+    }
+    if constexpr (Tr::kTf32) {
+      // X^T (rows p, tokens along the 128-byte row), rounded to tf32
+      for (int idx = tid; idx < P * kAE; idx += kThreads) {
+        const int pp = idx % P, j = idx / P, jt = jb * kAE + j;
         float v = 0.f;
-        if (j_rel <= i_rel && tok < L)
-          v = sacc[q] * exp2f(gi[si] - Gc[j_rel]) * ld_io(dt + (b * L + tok) * nh + h);
-        sb[si][sj + q] = v;
+        if (jt < valid) v = ld_io(x + (((int64_t)b * L + tok0 + jt) * nh + h) * P + pp);
+        *reinterpret_cast<uint32_t *>(Xb + sw128(pp, j * 4)) = to_tf32(v);
+      }
+    } else {
+      ptx::mbar_wait(&full[s], ph, err, 44);
+    }
+    ptx::fence_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      ptx::tc_fence_after();
+      const uint32_t p0 = ptx::smem_u32(Pb), x0 = ptx::smem_u32(Xb);
+#pragma unroll
+      for (int kk = 0; kk < kAE / Tr::kKmma; ++kk) {
+        const uint64_t ad = ptx::smem_desc(p0 + kk * 32, 16, 1024, ptx::kSw128);
+        const uint64_t xd =
+            Tr::kTf32 ? ptx::smem_desc(x0 + kk * 32, 16, 1024, ptx::kSw128)
+                      : ptx::smem_desc(x0 + kk * Tr::kKmma * 128, kAE * 128, 1024, ptx::kSw128);
+        ptx::mma_ss<Tr::kTf32>(tmem + col_diag, ad, xd, id_diag, (jb | kk) ? 1u : 0u);
+      }
+      ptx::mma_commit(&mmad[s]);
+      if (jb + 2 < njb) {
+        ptx::mbar_wait(&mmad[s], ph, err, 45);
+        if (!Tr::kTf32) load2(jb + 2);
       }
     }
-    for (int idx = tid; idx < kJ * kCols; idx += kThreads) {
-      const int jj = idx / kCols, pp = idx % kCols;
-      const int64_t tok = k * T + j0 + jj, p = pt * kCols + pp;
-      xs[jj][pp] = (tok < L && p < P) ? ld_io(x + ((b * L + tok) * nh + h) * P + p) : 0.f;
-    }
-    __syncthreads();
-    for (int jj = 0; jj < kJ; ++jj) {
-      float sv[4], xv[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        sv[q] = sb[ti * 4 + q][jj];
-        xv[q] = xs[jj][tp * 4 + q];
-      }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[a][e] = fmaf(sv[a], xv[e], acc[a][e]);
-    }
-    __syncthreads();
   }
+  {
+    const int u = base1 + njb - 1;
+    ptx::mbar_wait(&mmad[u & 1], (u >> 1) & 1, err, 46);
+  }
+  ptx::tc_fence_after();
 
+  // ---------------- epilogue: y = exp2(G_i) Yoff + Ydiag + D x
+  const bool row_ok = i_rel < valid;
+  const float eg = exp2f(Gi);
   const float Dh = Dv ? Dv[h] : 0.f;
+  const int64_t yoff = (((int64_t)b * L + tok0 + i_rel) * nh + h) * P;
+  for (int c0 = 0; c0 < P; c0 += 16) {
+    float a[16], d[16];
+    ptx::tmem_ld16_sync(tmem + lane_base + col_off + c0, a);
+    ptx::tmem_ld16_sync(tmem + lane_base + col_diag + c0, d);
+    if (row_ok) {
+      constexpr int per16 = 16 / kE;
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int64_t tok = row0 + ti * 4 + a;
-    if (tok >= L) continue;
-    const float eg = exp2f(gi[ti * 4 + a]);
+      for (int c = 0; c < 16 / per16; ++c) {
+        float xv[8], o[8];
+        unpack16(*reinterpret_cast<const uint4 *>(x + yoff + c0 + c * per16), xv, (IO *)nullptr);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int64_t p = pt * kCols + tp * 4 + e;
-      if (p >= P) continue;
-      const int64_t off = ((b * L + tok) * nh + h) * P + p;
-      st_io(y + off, eg * acc_off[a][e] + acc[a][e] + Dh * ld_io(x + off));
+        for (int e = 0; e < per16; ++e)
+          o[e] = fmaf(eg, a[c * per16 + e], d[c * per16 + e]) + Dh * xv[e];
+        *reinterpret_cast<uint4 *>(y + yoff + c0 + c * per16) = pack_io16(o, (IO *)nullptr);
+      }
     }
   }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tmem, ncols);
+}
+
+template <typename IO>
+cudaError_t launch_t(const Dims &d, const void *x, const void *B, const void *C, const void *dt,
+                     const float *G, const float *states, const float *D, void *y,
+                     cudaStream_t st) {
+  constexpr int kAE = IoT<IO>::kAE;
+  constexpr bool bf = !IoT<IO>::kTf32;
+  CUtensorMap tC, tB, tx;
+  if (!make_tmap_bl(&tC, C, bf, d.b, d.L, d.ng, d.S, kRows) ||
+      !make_tmap_bl(&tB, B, bf, d.b, d.L, d.ng, d.S, 128) ||
+      !make_tmap_bl(&tx, x, bf, d.b, d.L, d.nh, d.P, kAE))
+    return cudaErrorInvalidValue;
+  const int nBr = (int)((std::min<int64_t>(d.T, 256) + 127) / 128);
+  const int nPb = (int)((d.P + kAE - 1) / kAE);
+  const int st1 = kRows * 128 + nBr * 128 * 128 + (int)((d.P * 128 + 1023) & ~1023);
+  const int st2 = kRows * 128 + nPb * kAE * 128;
+  const int smem = 2 * std::max(st1, st2) + 1024;
+  auto kern = chunk_scan_tc<IO>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int n_it = (int)((d.T + kRows - 1) / kRows);
+  dim3 grid((unsigned)(d.nc * n_it), (unsigned)d.nh, (unsigned)d.b);
+  kern<<<grid, kThreads, smem, st>>>(tC, tB, tx, static_cast<const IO *>(x),
+                                     static_cast<const IO *>(dt), G, states, D,
+                                     static_cast<IO *>(y), device_error_word(), (int)d.L,
+                                     (int)d.nh, (int)d.P, (int)d.S, (int)d.hpg, (int)d.T,
+                                     (int)d.nc);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_chunk_scan(const Dims &d, ssd_dtype io, const void *x,
-                              const void *B, const void *C, const void *dt,
-                              const float *G, const float *states,
-                              const float *D, void *y, cudaStream_t st) {
-  const int64_t tiles = ((d.P + kCols - 1) / kCols) * (d.T / kRows);
-  dim3 grid((unsigned)(d.nc * tiles), (unsigned)d.nh, (unsigned)d.b);
-  if (io == SSD_BF16)
-    chunk_scan_simt<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-        (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)B, (const __nv_bfloat16 *)C,
-        (const __nv_bfloat16 *)dt, G, states, D, (__nv_bfloat16 *)y, d.L, d.nh, d.P, d.S,
-        d.ng, d.T, d.nc);
-  else
-    chunk_scan_simt<float><<<grid, kThreads, 0, st>>>(
-        (const float *)x, (const float *)B, (const float *)C, (const float *)dt, G, states, D,
-        (float *)y, d.L, d.nh, d.P, d.S, d.ng, d.T, d.nc);
-  return cudaGetLastError();
+cudaError_t launch_chunk_scan(const Dims &d, ssd_dtype io, const void *x, const void *B,
+                              const void *C, const void *dt, const float *G,
+                              const float *states, const float *D, void *y, cudaStream_t st) {
+  return io == SSD_BF16 ? launch_t<__nv_bfloat16>(d, x, B, C, dt, G, states, D, y, st)
+                        : launch_t<float>(d, x, B, C, dt, G, states, D, y, st);
 }
 
 }  // namespace ssd

@@ -7,97 +7,291 @@
 // CUDA Tile", section "Mamba-2 architecture", the log-space jump formula
 // h_{t+T} = exp(G_last) h_t + (exp(G_last - G) B)^T X, second term.)
 //
-// First-cut SIMT kernel: one block per (chunk, 64x64 state tile, head,
-// batch); 256 threads, each accumulating a 4x4 patch over the chunk's tokens
-// staged 32 at a time in shared memory.
-#include "ssd_internal.cuh"
+// Tensor-core kernel (tcgen05).  One CTA per (chunk, 128-wide slice of S,
+// head, batch) computes D[s][p] = sum_j B[j][s] (w_j x[j][p]) as an
+// M = 128 (s) x N = P MMA with K = the chunk's tokens:
+//   - TMA stages 64-token blocks of B (A operand, s contiguous: MN-major) and
+//     x (B operand, p contiguous: MN-major) into 128-byte-swizzled shared
+//     memory, two stages deep;
+//   - the threads scale each x row by w_j in place (a row of the swizzled
+//     tile holds one token, so the swizzle does not matter);
+//   - one thread issues the MMAs, accumulating in tensor memory (TMEM);
+//   - the epilogue reads TMEM lane s and writes dstates[p][s], coalesced
+//     along s.
+// With fp32 I/O the MMAs run as kind::tf32, which takes K-major operands
+// only; there the threads stage both operands transposed (tokens along the
+// 128-byte rows), 32 tokens per stage, rounding to tf32.
+#include "tc_common.cuh"
 
 namespace ssd {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kTile = 64;
-constexpr int kTok = 32;
+constexpr int kThreads = 128;
+constexpr int kKB = 64;   // tokens per pipeline stage
+constexpr int kMT = 128;  // s per CTA (MMA M)
 
 template <typename IO>
 __global__ void __launch_bounds__(kThreads)
-chunk_state_simt(const IO *__restrict__ x, const IO *__restrict__ Bm,
-                 const IO *__restrict__ dt, const float *__restrict__ G,
-                 float *__restrict__ dstates, int64_t L, int64_t nh, int64_t P,
-                 int64_t S, int64_t ng, int64_t T, int64_t nc) {
-  __shared__ float xs[kTok][kTile];
-  __shared__ float bs[kTok][kTile];
-  const int64_t ptiles = (P + kTile - 1) / kTile, stiles = (S + kTile - 1) / kTile;
-  int64_t r = blockIdx.x;
-  const int64_t st = r % stiles;
-  r /= stiles;
-  const int64_t pt = r % ptiles;
-  const int64_t k = r / ptiles;
-  const int64_t h = blockIdx.y, b = blockIdx.z, g = h / (nh / ng);
-  const float *Gc = G + ((b * nh + h) * nc + k) * T;
-  const float Glast = Gc[T - 1];
-  const int tid = threadIdx.x, tp = tid / 16, ts = tid % 16;
+chunk_state_tc(const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_x,
+               const IO *__restrict__ dt, const float *__restrict__ G,
+               float *__restrict__ dstates, int *__restrict__ err, int L, int nh, int P, int S,
+               int hpg, int T, int nc) {
+  using Tr = IoT<IO>;
+  constexpr int kAE = Tr::kAE;
+  constexpr int nMb = kMT / kAE;  // A-operand 128-byte blocks along s
+  constexpr int kBlk = kKB * 128; // bytes of one 64-row block
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ __align__(8) uint64_t full[2], mmad[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ float w[256];
 
-  float acc[4][4] = {};
-  for (int64_t j0 = 0; j0 < T; j0 += kTok) {
-    for (int idx = tid; idx < kTok * kTile; idx += kThreads) {
-      const int jj = idx / kTile, c = idx % kTile;
-      const int64_t tok = k * T + j0 + jj;
-      const int64_t p = pt * kTile + c, s = st * kTile + c;
-      float xv = 0.f, bv = 0.f;
-      if (tok < L) {
-        const float w = exp2f(Glast - Gc[j0 + jj]) * ld_io(dt + (b * L + tok) * nh + h);
-        if (p < P) xv = w * ld_io(x + ((b * L + tok) * nh + h) * P + p);
-        if (s < S) bv = ld_io(Bm + ((b * L + tok) * ng + g) * S + s);
-      }
-      xs[jj][c] = xv;
-      bs[jj][c] = bv;
+  const int nPb = (P + kAE - 1) / kAE;
+  const int stage_bytes = (nMb + nPb) * kBlk;
+  const int k = blockIdx.x;
+  const int n_st = (S + kMT - 1) / kMT;
+  const int h = blockIdx.y / n_st, st_idx = blockIdx.y % n_st;
+  const int b = blockIdx.z, g = h / hpg;
+  const int s0 = st_idx * kMT;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int tok0 = k * T;
+  const int valid = min(T, L - tok0);
+  const int nkb = (valid + kKB - 1) / kKB;
+  const uint32_t ncols = P <= 32 ? 32 : (P <= 64 ? 64 : 128);
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&mmad[i], 1);
     }
-    __syncthreads();
-#pragma unroll 4
-    for (int jj = 0; jj < kTok; ++jj) {
-      float xv[4], bv[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        xv[q] = xs[jj][tp * 4 + q];
-        bv[q] = bs[jj][ts * 4 + q];
-      }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(xv[a], bv[c], acc[a][c]);
-    }
-    __syncthreads();
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tm_B);
+    ptx::prefetch_tmap(&tm_x);
   }
-  float *out = dstates + ((b * nh + h) * nc + k) * P * S;
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_slot, ncols);
+    ptx::tmem_relinquish();
+  }
+  // w_j = exp2(G_last - G_j) dt_j, zero past the end of the sequence.
+  const float *Gc = G + ((int64_t)(b * nh + h) * nc + k) * T;
+  const float Glast = Gc[T - 1];
+  for (int j = tid; j < T; j += kThreads) {
+    float v = 0.f;
+    if (j < valid) v = exp2f(Glast - Gc[j]) * ld_io(dt + ((int64_t)b * L + tok0 + j) * nh + h);
+    w[j] = v;
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  auto issue_loads = [&](int kb) {
+    const int s = kb & 1;
+    uint8_t *A = smem + s * stage_bytes;
+    uint8_t *X = A + nMb * kBlk;
+    ptx::mbar_arrive_expect_tx(&full[s], stage_bytes);
+    for (int mb = 0; mb < nMb; ++mb)
+      ptx::tma_load_4d(A + mb * kBlk, &tm_B, s0 + mb * kAE, g, tok0 + kb * kKB, b, &full[s]);
+    for (int pb = 0; pb < nPb; ++pb)
+      ptx::tma_load_4d(X + pb * kBlk, &tm_x, pb * kAE, h, tok0 + kb * kKB, b, &full[s]);
+  };
+
+  if (tid == 0)
+    for (int kb = 0; kb < min(nkb, 2); ++kb) issue_loads(kb);
+
+  const uint32_t idesc = mma_idesc<IO>(128, P, true, true);
+  for (int kb = 0; kb < nkb; ++kb) {
+    const int s = kb & 1;
+    const uint32_t ph = (kb >> 1) & 1;
+    uint8_t *A = smem + s * stage_bytes;
+    uint8_t *X = A + nMb * kBlk;
+    ptx::mbar_wait(&full[s], ph, err, 21);
+    // scale the x rows of this block by w_j (16-byte chunks, row = token)
+    for (int c = tid; c < nPb * kKB * 8; c += kThreads) {
+      const int row = (c >> 3) & (kKB - 1);
+      const float ws = w[kb * kKB + row];
+      uint4 *p4 = reinterpret_cast<uint4 *>(X + c * 16);
+      float v[8];
+      unpack16(*p4, v, (IO *)nullptr);
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int64_t p = pt * kTile + tp * 4 + a;
-    if (p >= P) continue;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int64_t s = st * kTile + ts * 4 + c;
-      if (s < S) out[p * S + s] = acc[a][c];
+      for (int i = 0; i < 16 / Tr::kE; ++i) v[i] *= ws;
+      *p4 = pack_op16(v, (IO *)nullptr);
     }
+    ptx::fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      ptx::tc_fence_after();
+      const uint32_t a0 = ptx::smem_u32(A), x0 = ptx::smem_u32(X);
+#pragma unroll
+      for (int kk = 0; kk < kKB / Tr::kKmma; ++kk) {
+        const uint64_t ad = ptx::smem_desc(a0 + kk * Tr::kKmma * 128, kBlk, 1024, ptx::kSw128);
+        const uint64_t bd = ptx::smem_desc(x0 + kk * Tr::kKmma * 128, kBlk, 1024, ptx::kSw128);
+        ptx::mma_ss<Tr::kTf32>(tmem, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+      }
+      ptx::mma_commit(&mmad[s]);
+      if (kb + 2 < nkb) {
+        ptx::mbar_wait(&mmad[s], ph, err, 22);
+        issue_loads(kb + 2);
+      }
+    }
+  }
+  // all MMAs done (the last commit tracks every earlier MMA of the thread)
+  ptx::mbar_wait(&mmad[(nkb - 1) & 1], ((nkb - 1) >> 1) & 1, err, 23);
+  ptx::tc_fence_after();
+
+  const int srow = s0 + warp * 32 + lane;
+  float *out = dstates + ((int64_t)(b * nh + h) * nc + k) * P * S;
+  for (int c0 = 0; c0 < P; c0 += 16) {
+    float v[16];
+    ptx::tmem_ld16_sync(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+    if (srow < S) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) out[(int64_t)(c0 + j) * S + srow] = v[j];
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tmem, ncols);
+}
+
+// fp32 I/O: K-major staging by the threads (kind::tf32 has no MN-major mode).
+constexpr int kKB32 = 32;  // tokens per stage: one 128-byte row of fp32
+
+__global__ void __launch_bounds__(kThreads)
+chunk_state_tf32(const float *__restrict__ x, const float *__restrict__ Bm,
+                 const float *__restrict__ dt, const float *__restrict__ G,
+                 float *__restrict__ dstates, int *__restrict__ err, int L, int nh, int P, int S,
+                 int hpg, int T, int nc) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ __align__(8) uint64_t mmad[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ float w[256];
+
+  const int aBytes = kMT * 128;                       // A: 128 rows s
+  const int stage_bytes = aBytes + ((P * 128 + 1023) & ~1023);  // + X: P rows p
+  const int k = blockIdx.x;
+  const int n_st = (S + kMT - 1) / kMT;
+  const int h = blockIdx.y / n_st, st_idx = blockIdx.y % n_st;
+  const int b = blockIdx.z, g = h / hpg;
+  const int s0 = st_idx * kMT;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int tok0 = k * T;
+  const int valid = min(T, L - tok0);
+  const int nkb = (valid + kKB32 - 1) / kKB32;
+  const uint32_t ncols = P <= 32 ? 32 : (P <= 64 ? 64 : 128);
+
+  if (tid == 0) {
+    ptx::mbar_init(&mmad[0], 1);
+    ptx::mbar_init(&mmad[1], 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_slot, ncols);
+    ptx::tmem_relinquish();
+  }
+  const float *Gc = G + ((int64_t)(b * nh + h) * nc + k) * T;
+  const float Glast = Gc[T - 1];
+  for (int j = tid; j < T; j += kThreads)
+    w[j] = j < valid ? exp2f(Glast - Gc[j]) * dt[((int64_t)b * L + tok0 + j) * nh + h] : 0.f;
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t idesc = ptx::idesc_tf32(128, P, false, false);
+
+  for (int kb = 0; kb < nkb; ++kb) {
+    const int s = kb & 1;
+    if (kb >= 2) ptx::mbar_wait(&mmad[s], ((kb >> 1) - 1) & 1, err, 24);
+    uint8_t *A = smem + s * stage_bytes;
+    uint8_t *X = A + aBytes;
+    // A[s][j] = B[token j][s]: read along s (coalesced), write transposed
+    for (int idx = tid; idx < kMT * kKB32; idx += kThreads) {
+      const int sl = idx % kMT, j = idx / kMT, jt = kb * kKB32 + j;
+      float v = 0.f;
+      if (s0 + sl < S && jt < valid)
+        v = Bm[(((int64_t)b * L + tok0 + jt) * (nh / hpg) + g) * S + s0 + sl];
+      *reinterpret_cast<uint32_t *>(A + sw128(sl, j * 4)) = to_tf32(v);
+    }
+    // X[p][j] = w_j x[token j][p]
+    for (int idx = tid; idx < P * kKB32; idx += kThreads) {
+      const int p = idx % P, j = idx / P, jt = kb * kKB32 + j;
+      float v = 0.f;
+      if (jt < valid) v = w[jt] * x[(((int64_t)b * L + tok0 + jt) * nh + h) * P + p];
+      *reinterpret_cast<uint32_t *>(X + sw128(p, j * 4)) = to_tf32(v);
+    }
+    ptx::fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      ptx::tc_fence_after();
+      const uint32_t a0 = ptx::smem_u32(A), x0 = ptx::smem_u32(X);
+#pragma unroll
+      for (int kk = 0; kk < kKB32 / 8; ++kk) {
+        const uint64_t ad = ptx::smem_desc(a0 + kk * 32, 16, 1024, ptx::kSw128);
+        const uint64_t bd = ptx::smem_desc(x0 + kk * 32, 16, 1024, ptx::kSw128);
+        ptx::mma_ss<true>(tmem, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+      }
+      ptx::mma_commit(&mmad[s]);
+    }
+  }
+  ptx::mbar_wait(&mmad[(nkb - 1) & 1], ((nkb - 1) >> 1) & 1, err, 25);
+  ptx::tc_fence_after();
+
+  const int srow = s0 + warp * 32 + lane;
+  float *out = dstates + ((int64_t)(b * nh + h) * nc + k) * P * S;
+  for (int c0 = 0; c0 < P; c0 += 16) {
+    float v[16];
+    ptx::tmem_ld16_sync(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+    if (srow < S) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) out[(int64_t)(c0 + j) * S + srow] = v[j];
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tmem, ncols);
+}
+
+template <typename IO>
+cudaError_t launch_t(const Dims &d, const void *x, const void *B, const void *dt,
+                     const float *G, float *dstates, cudaStream_t st) {
+  const int n_st = (int)((d.S + kMT - 1) / kMT);
+  dim3 grid((unsigned)d.nc, (unsigned)(d.nh * n_st), (unsigned)d.b);
+  if constexpr (IoT<IO>::kTf32) {
+    const int smem = 2 * (kMT * 128 + (int)((d.P * 128 + 1023) & ~1023)) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(chunk_state_tf32,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    chunk_state_tf32<<<grid, kThreads, smem, st>>>(
+        static_cast<const float *>(x), static_cast<const float *>(B),
+        static_cast<const float *>(dt), G, dstates, device_error_word(), (int)d.L, (int)d.nh,
+        (int)d.P, (int)d.S, (int)d.hpg, (int)d.T, (int)d.nc);
+    return cudaGetLastError();
+  } else {
+    constexpr bool bf = true;
+    CUtensorMap tB, tx;
+    if (!make_tmap_bl(&tB, B, bf, d.b, d.L, d.ng, d.S, kKB) ||
+        !make_tmap_bl(&tx, x, bf, d.b, d.L, d.nh, d.P, kKB))
+      return cudaErrorInvalidValue;
+    const int nPb = (int)((d.P + IoT<IO>::kAE - 1) / IoT<IO>::kAE);
+    const int smem = 2 * (kMT / IoT<IO>::kAE + nPb) * kKB * 128 + 1024;
+    auto kern = chunk_state_tc<IO>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, st>>>(tB, tx, static_cast<const IO *>(dt), G, dstates,
+                                       device_error_word(), (int)d.L, (int)d.nh, (int)d.P,
+                                       (int)d.S, (int)d.hpg, (int)d.T, (int)d.nc);
+    return cudaGetLastError();
   }
 }
 
 }  // namespace
 
-cudaError_t launch_chunk_state(const Dims &d, ssd_dtype io, const void *x,
-                               const void *B, const void *dt, const float *G,
-                               float *dstates, cudaStream_t st) {
-  const int64_t tiles = ((d.P + kTile - 1) / kTile) * ((d.S + kTile - 1) / kTile);
-  dim3 grid((unsigned)(d.nc * tiles), (unsigned)d.nh, (unsigned)d.b);
-  if (io == SSD_BF16)
-    chunk_state_simt<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-        (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)B, (const __nv_bfloat16 *)dt, G,
-        dstates, d.L, d.nh, d.P, d.S, d.ng, d.T, d.nc);
-  else
-    chunk_state_simt<float><<<grid, kThreads, 0, st>>>(
-        (const float *)x, (const float *)B, (const float *)dt, G, dstates, d.L, d.nh, d.P,
-        d.S, d.ng, d.T, d.nc);
-  return cudaGetLastError();
+cudaError_t launch_chunk_state(const Dims &d, ssd_dtype io, const void *x, const void *B,
+                               const void *dt, const float *G, float *dstates,
+                               cudaStream_t st) {
+  return io == SSD_BF16 ? launch_t<__nv_bfloat16>(d, x, B, dt, G, dstates, st)
+                        : launch_t<float>(d, x, B, dt, G, dstates, st);
 }
 
 }  // namespace ssd

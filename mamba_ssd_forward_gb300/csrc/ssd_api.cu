@@ -25,7 +25,7 @@ ssd_status check_dims(const ssd_dims *in, Dims *out) {
   if (d.chunk != 64 && d.chunk != 128 && d.chunk != 256) return SSD_ERR_UNSUPPORTED;
   // Grid limits (batch and heads index grid dimensions) and 62-bit element
   // counts for every tensor.
-  if (d.batch > 65535 || d.nheads > 65535) return SSD_ERR_UNSUPPORTED;
+  if (d.batch > 65535 || d.nheads > 32767 || d.seqlen > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
   const int64_t nc = (d.seqlen + d.chunk - 1) / d.chunk;
   const double big = 4.0e18;
   if ((double)d.batch * d.seqlen * d.nheads * d.headdim > big ||
