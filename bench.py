@@ -37,9 +37,13 @@ from mamba_ssd_forward_gb300 import inputs as W  # noqa: E402
 
 METRIC = "SSD forward tokens/s at 1 GB300; achieved TFLOP/s + HBM GB/s vs roofline"
 DEFAULT_WORKLOAD = W.MAMBA2_130M
-KERNEL_NAMES = ["chunk_cumsum", "chunk_state", "state_passing", "chunk_scan"]
+# Launch sequence of ssd_forward: bf16 I/O runs the fused state pass and the
+# output pass; fp32 I/O runs the four step kernels.
+KERNEL_NAMES = {"bf16": ["fwd_state", "fwd_scan"],
+                "fp32": ["chunk_cumsum", "chunk_state", "state_passing", "chunk_scan"]}
 KERNEL_SOURCES = {"chunk_cumsum": "chunk_cumsum.cu", "chunk_state": "chunk_state.cu",
-                  "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan.cu"}
+                  "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan.cu",
+                  "fwd_state": "fwd_state.cu", "fwd_scan": "fwd_scan.cu"}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -92,7 +96,11 @@ def kernel_bytes(w: W.Workload) -> dict:
     G = w.batch * w.nheads * w.nchunks * w.chunk * 4
     st = w.batch * w.nheads * w.nchunks * w.headdim * w.dstate * 4
     fin = w.batch * w.nheads * w.headdim * w.dstate * 4
+    st16 = w.batch * w.nheads * w.nchunks * w.headdim * w.dstate * 2
+    h0 = fin if w.has_h0 else 0
     return {
+        "fwd_state": x + bc + dt + w.nheads * 4 + h0 + st16 + fin,
+        "fwd_scan": 2 * x + 2 * bc + dt + 2 * w.nheads * 4 + st16,
         "chunk_cumsum": dt + G + w.nheads * 4,
         "chunk_state": x + bc + dt + G + st,
         "state_passing": 2 * st + w.batch * w.nheads * w.nchunks * 4 + fin * (2 if w.has_h0 else 1),
@@ -319,7 +327,8 @@ def run_ours(args, w):
     clocks = sampler.stop() if sampler else None
 
     step_ms = [ev[i][0].elapsed_time(ev[i][n_l]) for i in range(args.steps)]
-    kern_ms = {KERNEL_NAMES[j]: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1])
+    names = KERNEL_NAMES[w.dtype]
+    kern_ms = {names[j]: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1])
                                                 for i in range(args.steps))
                for j in range(n_l)}
     ms = statistics.mean(step_ms)

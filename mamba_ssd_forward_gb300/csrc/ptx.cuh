@@ -56,11 +56,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Wait until the phase with the given parity completes.  Gives up after
-// about `limit_ns` nanoseconds of wall time, records `code` in *err and
-// returns false (the caller then carries on with undefined data; the host
-// sees the code through ssd_device_error).
+// about `limit_ns` nanoseconds of wall time, or at once when another thread
+// has already given up (the error word is nonzero), records `code` in *err
+// and returns false; the caller then carries on with undefined data, so a
+// broken pipeline ends quickly instead of hanging, and the host sees the
+// code through ssd_device_error.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code,
-                                          uint64_t limit_ns = 2000000000ull) {
+                                          uint64_t limit_ns = 1000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -68,6 +70,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > limit_ns) break;
+    if (err && *reinterpret_cast<volatile int *>(err) != 0) return false;
   }
   if (err) atomicExch(err, code);
   return false;
@@ -79,6 +82,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
 // (tensor-core reads of shared memory, TMA).
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Barrier over a subset of the CTA's warps (`count` threads, id 1..15).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -229,6 +237,24 @@ template <int N>
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
 #pragma unroll
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// Store 16 fp32 columns (lane = taddr.lane + thread, as for tmem_ld16).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32"
+      " [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Load 16 fp32 columns and wait for them.

@@ -3,6 +3,7 @@
 // checks arguments and enqueues launches on the caller's stream.
 #include <cstdint>
 
+#include "fwd.cuh"
 #include "ssd_internal.cuh"
 
 namespace {
@@ -53,16 +54,22 @@ bool opt(const void *p) { return !p || aligned16(p); }
 
 ssd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
 
-// Workspace of ssd_forward: G, then dstates, then states, each 256-byte
-// aligned.
+// Workspace of ssd_forward.  bf16 I/O: the per-chunk start states in bf16,
+// [b, nh, nc, S, P].  fp32 I/O: G, then the chunk jump terms, then the
+// per-chunk states (fp32, the step-wise layouts), each 256-byte aligned.
 struct WsLayout {
   size_t G, dstates, states, total;
 };
 
 size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
-WsLayout ws_layout(const Dims &d) {
+WsLayout ws_layout(const Dims &d, ssd_dtype t) {
   WsLayout w;
+  if (t == SSD_BF16) {
+    w.G = w.dstates = w.states = 0;
+    w.total = round256(2 * (size_t)(d.b * d.nh * d.nc * d.S * d.P));
+    return w;
+  }
   w.G = 0;
   w.dstates = round256(sizeof(float) * d.b * d.nh * d.nc * d.T);
   const size_t st = round256(sizeof(float) * d.b * d.nh * d.nc * d.P * d.S);
@@ -88,7 +95,7 @@ HostLayout host_layout(const Dims &d, ssd_dtype t, int has_D, int has_h0, int ha
     off += round256(bytes);
     return at;
   };
-  h.fwd_bytes = ws_layout(d).total;
+  h.fwd_bytes = ws_layout(d, t).total;
   h.fwd = take(h.fwd_bytes);
   h.x = take(e * d.b * d.L * d.nh * d.P);
   h.dt = take(e * d.b * d.L * d.nh);
@@ -128,7 +135,7 @@ ssd_status ssd_device_error(void *stream) {
 size_t ssd_forward_workspace_size(const ssd_dims *dims, ssd_dtype dtype) {
   Dims d;
   if (!valid_dtype(dtype) || check_dims(dims, &d) != SSD_OK) return 0;
-  return ws_layout(d).total;
+  return ws_layout(d, dtype).total;
 }
 
 ssd_status ssd_chunk_cumsum(const ssd_dims *dims, ssd_dtype dtype, const void *dt,
@@ -197,12 +204,9 @@ ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype, const voi
       !opt(D) || !opt(h0) || !req(y) || !opt(final_state) || !workspace ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) || n_events < 0)
     return SSD_ERR_INVALID_ARG;
-  const WsLayout w = ws_layout(d);
+  const WsLayout w = ws_layout(d, dtype);
   if (ws_bytes < w.total) return SSD_ERR_INVALID_ARG;
   char *ws = static_cast<char *>(workspace);
-  float *G = reinterpret_cast<float *>(ws + w.G);
-  float *dst = reinterpret_cast<float *>(ws + w.dstates);
-  float *sts = reinterpret_cast<float *>(ws + w.states);
   cudaStream_t st = (cudaStream_t)stream;
   int launched = 0;
   auto mark = [&](int i) -> cudaError_t {
@@ -210,14 +214,26 @@ ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype, const voi
     return cudaSuccess;
   };
   cudaError_t e = mark(0);
-  if (e == cudaSuccess) e = ssd::launch_chunk_cumsum(d, dtype, dt, A, G, st);
-  if (e == cudaSuccess && ++launched) e = mark(launched);
-  if (e == cudaSuccess) e = ssd::launch_chunk_state(d, dtype, x, B, dt, G, dst, st);
-  if (e == cudaSuccess && ++launched) e = mark(launched);
-  if (e == cudaSuccess) e = ssd::launch_state_passing(d, dst, G, h0, sts, final_state, st);
-  if (e == cudaSuccess && ++launched) e = mark(launched);
-  if (e == cudaSuccess) e = ssd::launch_chunk_scan(d, dtype, x, B, C, dt, G, sts, D, y, st);
-  if (e == cudaSuccess && ++launched) e = mark(launched);
+  if (dtype == SSD_BF16) {
+    // state pass (cumsum + chunk jump + sequential pass), then output pass
+    void *sts = ws;
+    if (e == cudaSuccess) e = ssd::launch_fwd_state(d, x, B, dt, A, h0, sts, final_state, st);
+    if (e == cudaSuccess && ++launched) e = mark(launched);
+    if (e == cudaSuccess) e = ssd::launch_fwd_scan(d, x, B, C, dt, A, sts, D, y, st);
+    if (e == cudaSuccess && ++launched) e = mark(launched);
+  } else {
+    float *G = reinterpret_cast<float *>(ws + w.G);
+    float *dst = reinterpret_cast<float *>(ws + w.dstates);
+    float *sts = reinterpret_cast<float *>(ws + w.states);
+    if (e == cudaSuccess) e = ssd::launch_chunk_cumsum(d, dtype, dt, A, G, st);
+    if (e == cudaSuccess && ++launched) e = mark(launched);
+    if (e == cudaSuccess) e = ssd::launch_chunk_state(d, dtype, x, B, dt, G, dst, st);
+    if (e == cudaSuccess && ++launched) e = mark(launched);
+    if (e == cudaSuccess) e = ssd::launch_state_passing(d, dst, G, h0, sts, final_state, st);
+    if (e == cudaSuccess && ++launched) e = mark(launched);
+    if (e == cudaSuccess) e = ssd::launch_chunk_scan(d, dtype, x, B, C, dt, G, sts, D, y, st);
+    if (e == cudaSuccess && ++launched) e = mark(launched);
+  }
   if (n_launches) *n_launches = launched;
   return from_cuda(e);
 }

@@ -5,6 +5,8 @@
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
 #include "tmap.cuh"

@@ -64,7 +64,12 @@ def dims(**kw):
 def test_workspace_size(lib):
     d = dims()
     nc = 4
+    # bf16: the per-chunk start states in bf16
     ws = lib.ssd_forward_workspace_size(ctypes.byref(d), 1)
+    assert ws >= 2 * 2 * 8 * nc * 64 * 128
+    assert ws % 256 == 0
+    # fp32: G, the chunk jump terms and the states, fp32
+    ws = lib.ssd_forward_workspace_size(ctypes.byref(d), 0)
     assert ws >= 4 * 2 * 8 * nc * 256 + 2 * 4 * 2 * 8 * nc * 64 * 128
     assert ws % 256 == 0
     assert lib.ssd_forward_workspace_size(ctypes.byref(d), 7) == 0

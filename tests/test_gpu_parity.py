@@ -47,6 +47,9 @@ SMALL_CASES = [
     small("max_dims_fp32", 200, 2, 128, 256, 1, 128, "fp32"),
     small("odd_multiples", 190, 3, 48, 80, 3, 64, "bf16", h0=False),
     small("no_h0_fp32", 512, 2, 64, 64, 1, 128, "fp32", h0=False),
+    small("bf16_hpg6_three_heads_per_cta", 600, 12, 64, 128, 2, 256, "bf16", batch=2),
+    small("bf16_S256_groups", 520, 12, 64, 256, 2, 256, "bf16"),
+    small("bf16_P96_S48", 300, 4, 96, 48, 1, 128, "bf16"),
 ]
 
 
