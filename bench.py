@@ -39,11 +39,12 @@ METRIC = "SSD forward tokens/s at 1 GB300; achieved TFLOP/s + HBM GB/s vs roofli
 DEFAULT_WORKLOAD = W.MAMBA2_130M
 # Launch sequence of ssd_forward: bf16 I/O runs the fused state pass and the
 # output pass; fp32 I/O runs the four step kernels.
-KERNEL_NAMES = {"bf16": ["fwd_state", "fwd_scan"],
+KERNEL_NAMES = {"bf16": ["fwd_chunk_state", "fwd_state_pass", "fwd_scan"],
                 "fp32": ["chunk_cumsum", "chunk_state", "state_passing", "chunk_scan"]}
 KERNEL_SOURCES = {"chunk_cumsum": "chunk_cumsum.cu", "chunk_state": "chunk_state.cu",
                   "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan.cu",
-                  "fwd_state": "fwd_state.cu", "fwd_scan": "fwd_scan.cu"}
+                  "fwd_chunk_state": "fwd_chunk_state.cu", "fwd_state_pass": "fwd_state_pass.cu",
+                  "fwd_scan": "fwd_scan.cu"}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -97,9 +98,11 @@ def kernel_bytes(w: W.Workload) -> dict:
     st = w.batch * w.nheads * w.nchunks * w.headdim * w.dstate * 4
     fin = w.batch * w.nheads * w.headdim * w.dstate * 4
     st16 = w.batch * w.nheads * w.nchunks * w.headdim * w.dstate * 2
+    gam = w.batch * w.nheads * w.nchunks * 4
     h0 = fin if w.has_h0 else 0
     return {
-        "fwd_state": x + bc + dt + w.nheads * 4 + h0 + st16 + fin,
+        "fwd_chunk_state": x + bc + dt + w.nheads * 4 + st16 + gam,
+        "fwd_state_pass": 2 * st16 + gam + h0 + fin,
         "fwd_scan": 2 * x + 2 * bc + dt + 2 * w.nheads * 4 + st16,
         "chunk_cumsum": dt + G + w.nheads * 4,
         "chunk_state": x + bc + dt + G + st,
@@ -292,7 +295,18 @@ def run_ours(args, w):
     ws = torch.empty(ssd.workspace_size(d["x"], d["B"], w.chunk), dtype=torch.uint8, device=dev)
     y = torch.empty_like(d["x"])
     fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # L2 flush between steps: write a 256 MB buffer, then read another 256 MB
+    # one, so that L2 holds neither the workload's data nor dirty lines whose
+    # write-back would land inside the next timed step.
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.zero_()
+        if args.flush == "write+read":
+            torch.sum(flush_r, dim=0, keepdim=True, out=flush_sink)
+
     nev = 8
 
     def step(events):
@@ -301,7 +315,7 @@ def run_ours(args, w):
 
     warm_ev = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step(warm_ev)
     torch.cuda.synchronize()
 
@@ -316,7 +330,7 @@ def run_ours(args, w):
     launches = 0
     n_l = 0
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         n_l = step(ev[i])
         launches += n_l
     torch.cuda.synchronize()
@@ -363,7 +377,8 @@ def run_ours(args, w):
         "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen,
                    "nheads": w.nheads, "headdim": w.headdim, "dstate": w.dstate,
                    "ngroups": w.ngroups, "chunk": w.chunk, "h0": w.has_h0,
-                   "l2": "flushed before every step (256 MB write outside the timed events)",
+                   "l2": ("flushed before every step outside the timed events: 256 MB write"
+                          + (" then 256 MB read (clean L2)" if args.flush == "write+read" else "")),
                    "parallelism": f"replicas x{world} (independent batches per GPU)"},
         "achieved_tflops": algorithmic_flops(w) / (ms / 1e3) / 1e12,
         "achieved_gbs_compulsory": compulsory_bytes(w) / (ms / 1e3) / 1e9,
@@ -426,6 +441,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD.name)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--flush", choices=["write+read", "write"], default="write+read",
+                    help="L2 flush between steps (default: write a buffer, then read another)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

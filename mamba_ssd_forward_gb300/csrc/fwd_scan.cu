@@ -7,26 +7,40 @@
 //
 // One CTA per (128-row tile of a chunk, chunk, group of H heads that share
 // B and C, batch), warp-specialised:
-//   warp 4 (TMA):  C and B blocks of 64 state entries, the H heads' start
+//   warp 16 (TMA): C and B blocks of 64 state entries and the H heads' start
 //                  states (bf16 [s][p] tiles), then 64-token blocks of x;
-//   warp 5 (MMA):  phase 1, per block of S:  Sc += C B^T (once for all H
+//   warp 17 (MMA): phase 1, per block of S:  Sc += C B^T (once for all H
 //                  heads: they share B and C) and Y_q += C h_q^T;
 //                  phase 2, per head q and 64-token block: Y_q += S'_q X_q;
-//   warps 0-3 (one thread per row i):  the in-chunk cumsums of the H heads;
+//   warps 0-15 (four warps per 32-row quadrant of the tile, each taking a
+//                  quarter of the columns):  the in-chunk cumsums of the H heads;
 //                  Y_q *= exp2(G_i) once phase 1 is done; the decayed, masked
-//                  interaction tile S'_q = Sc * exp2(G_i - G_j) dt_j [j <= i]
-//                  written to shared memory as a K-major operand, one block
-//                  of 64 tokens at a time; and the epilogue y = Y_q + D x.
+//                  interaction tile S'_q written to shared memory as a
+//                  K-major operand, one block of 64 tokens at a time; and the
+//                  epilogue y = Y_q + D x.
 // Sc lives in tensor-memory columns [0, 256), Y_q in 256 + q P.  The
 // interaction tile is never written to global memory.
+//
+// Decay factors.  For row i and a 64-token column block that ends at r
+// strictly before row i's own block, exp2(G_i - G_j) = exp2(G_i - G_r) *
+// exp2(G_r - G_j) with both exponents <= 0 (G falls along the chunk): one
+// exp per (row, block) and one per column replace one per element.  The
+// block holding the diagonal takes exp2(G_i - G_j) directly, and the causal
+// mask (j <= i, diagonal kept) zeroes the rest.  No exponent above zero is
+// ever evaluated.
 #include "fwd.cuh"
 
 namespace ssd {
 namespace {
 
-constexpr int kRowThreads = 128;
-constexpr int kThreads = 192;
+constexpr int kRowWarps = 16;
+constexpr int kRowThreads = kRowWarps * 32;
+constexpr int kThreads = kRowThreads + 64;
+constexpr int kProducerWarp = kRowWarps, kMmaWarp = kRowWarps + 1;
 constexpr int kMaxH = 4;
+constexpr int kMaxX = 8;        // x pipeline stages (at most)
+constexpr int kNP = 4;          // stages of the decayed interaction tile S'
+
 constexpr int kBlk = 64 * 128;  // one 64-row, 128-byte-wide block
 
 struct ScanArgs {
@@ -34,22 +48,27 @@ struct ScanArgs {
   const float *A, *D;
   __nv_bfloat16 *y;
   int *err;
-  int L, nh, P, S, hpg, T, nc, H;
+  int L, nh, P, S, hpg, T, nc, H, nX;
 };
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
 fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
               const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_st,
               const ScanArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t full1[2], empty1[2], s1_done, pm_full[2], pm_empty[2],
-      x_full[2], x_empty[2], ysc[kMaxH], ydone[kMaxH];
+  __shared__ __align__(8) uint64_t full1[2], empty1[2], s1_done, pm_full[kNP], pm_empty[kNP],
+      x_full[kMaxX], x_empty[kMaxX], ysc[kMaxH], ydone[kMaxH];
   __shared__ uint32_t tmem_slot;
-  __shared__ float Gs[kMaxH][256], dts[kMaxH][256];
-  __shared__ float warp_tot[4];
+  // per head: G (log2 units), dt, and the column factors v_j of the
+  // factored decay (exp2(G_r - G_j) dt_j, r = end of j's 64-token block)
+  // read with 16-byte vector loads: each array 16-byte aligned
+  __shared__ __align__(16) float Gs[kMaxH][256];
+  __shared__ __align__(16) float dts[kMaxH][256];
+  __shared__ __align__(16) float vs[kMaxH][256];
+  __shared__ float warp_tot[kRowWarps];
 
-  const int L = a.L, nh = a.nh, P = a.P, S = a.S, T = a.T, nc = a.nc, H = a.H;
+  const int L = a.L, nh = a.nh, P = a.P, S = a.S, T = a.T, nc = a.nc, H = a.H, nX = a.nX;
   const int n_it = (T + 127) / 128;
   const int k = blockIdx.x / n_it, it = blockIdx.x % n_it;
   const int hbase = blockIdx.y * H, b = blockIdx.z, g = hbase / a.hpg;
@@ -66,14 +85,21 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
   const int st1 = kBlk * 2 + nBr * kBlk * 2 + H * nPb * kBlk;  // C | B | states
   const int st2p = kBlk * 2;                                 // S' (128 rows)
   const int st2x = nPb * kBlk;                               // X (64 rows)
+  // x stages live after the two phase-1 stages, so their loads overlap
+  // phase 1; the kNP S' stages reuse the phase-1 space once it is consumed.
+  uint8_t *xbase = smem + 2 * st1;
   const uint32_t ncols = 512;
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&full1[i], 1);
       ptx::mbar_init(&empty1[i], 1);
+    }
+    for (int i = 0; i < kNP; ++i) {
       ptx::mbar_init(&pm_full[i], kRowThreads);
       ptx::mbar_init(&pm_empty[i], 1);
+    }
+    for (int i = 0; i < kMaxX; ++i) {
       ptx::mbar_init(&x_full[i], 1);
       ptx::mbar_init(&x_empty[i], 1);
     }
@@ -84,7 +110,7 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
     }
     ptx::fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(&tmem_slot, ncols);
     ptx::tmem_relinquish();
   }
@@ -93,15 +119,16 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 4) {
+  const bool leader = (tid & 31) == 0;
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if ((tid & 31) == 0) {
-      for (int sb = 0; sb < nsb; ++sb) {
-        const int s = sb & 1;
-        uint8_t *Cb = smem + s * st1;
-        uint8_t *Bb = Cb + 2 * kBlk;
-        uint8_t *Hb = Bb + nBr * 2 * kBlk;
-        ptx::mbar_wait(&empty1[s], ((sb >> 1) & 1) ^ 1, a.err, 81);
+    for (int sb = 0; sb < nsb; ++sb) {
+      const int s = sb & 1;
+      uint8_t *Cb = smem + s * st1;
+      uint8_t *Bb = Cb + 2 * kBlk;
+      uint8_t *Hb = Bb + nBr * 2 * kBlk;
+      ptx::mbar_wait(&empty1[s], ((sb >> 1) & 1) ^ 1, a.err, 81);
+      if (leader) {
         ptx::mbar_arrive_expect_tx(&full1[s], st1);
         ptx::tma_load_4d(Cb, &tm_C, sb * 64, g, tok0 + i0, b, &full1[s]);
         for (int r = 0; r < nBr; ++r)
@@ -113,31 +140,33 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
                              &full1[s]);
         }
       }
-      // phase-2 buffers overlay phase 1: wait until phase 1 is consumed
-      ptx::mbar_wait(&s1_done, 0, a.err, 82);
-      for (int q = 0; q < H; ++q)
-        for (int jb = 0; jb < njb; ++jb) {
-          const int u = q * njb + jb, s = u & 1;
-          uint8_t *Xb = smem + 2 * st2p + s * st2x;
-          ptx::mbar_wait(&x_empty[s], ((u >> 1) & 1) ^ 1, a.err, 83);
+      __syncwarp();
+    }
+    for (int q = 0; q < H; ++q)
+      for (int jb = 0; jb < njb; ++jb) {
+        const int u = q * njb + jb, s = u % nX;
+        uint8_t *Xb = xbase + s * st2x;
+        ptx::mbar_wait(&x_empty[s], ((u / nX) & 1) ^ 1, a.err, 83);
+        if (leader) {
           ptx::mbar_arrive_expect_tx(&x_full[s], st2x);
           for (int pb = 0; pb < nPb; ++pb)
             ptx::tma_load_4d(Xb + pb * kBlk, &tm_x, pb * 64, hbase + q, tok0 + jb * 64, b,
                              &x_full[s]);
         }
-    }
-  } else if (warp == 5) {
+        __syncwarp();
+      }
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if ((tid & 31) == 0) {
-      const uint32_t id_S = ptx::idesc_bf16(128, jext, false, false);
-      const uint32_t id_Y = ptx::idesc_bf16(128, P, false, true);
-      for (int sb = 0; sb < nsb; ++sb) {
-        const int s = sb & 1;
-        uint8_t *Cb = smem + s * st1;
-        uint8_t *Bb = Cb + 2 * kBlk;
-        uint8_t *Hb = Bb + nBr * 2 * kBlk;
-        ptx::mbar_wait(&full1[s], (sb >> 1) & 1, a.err, 84);
-        ptx::tc_fence_after();
+    const uint32_t id_S = ptx::idesc_bf16(128, jext, false, false);
+    const uint32_t id_Y = ptx::idesc_bf16(128, P, false, true);
+    for (int sb = 0; sb < nsb; ++sb) {
+      const int s = sb & 1;
+      uint8_t *Cb = smem + s * st1;
+      uint8_t *Bb = Cb + 2 * kBlk;
+      uint8_t *Hb = Bb + nBr * 2 * kBlk;
+      ptx::mbar_wait(&full1[s], (sb >> 1) & 1, a.err, 84);
+      ptx::tc_fence_after();
+      if (leader) {
         const uint32_t c0 = ptx::smem_u32(Cb), b0 = ptx::smem_u32(Bb), h0 = ptx::smem_u32(Hb);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -153,18 +182,21 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
         }
         ptx::mma_commit(&empty1[s]);
       }
-      ptx::mma_commit(&s1_done);
-      for (int q = 0; q < H; ++q) {
-        ptx::mbar_wait(&ysc[q], 0, a.err, 85);
+      __syncwarp();
+    }
+    if (leader) ptx::mma_commit(&s1_done);
+    __syncwarp();
+    for (int q = 0; q < H; ++q) {
+      ptx::mbar_wait(&ysc[q], 0, a.err, 85);
+      ptx::tc_fence_after();
+      for (int jb = 0; jb < njb; ++jb) {
+        const int u = q * njb + jb, s = u % kNP, sx = u % nX;
+        ptx::mbar_wait(&pm_full[s], (u / kNP) & 1, a.err, 86);
+        ptx::mbar_wait(&x_full[sx], (u / nX) & 1, a.err, 87);
         ptx::tc_fence_after();
-        for (int jb = 0; jb < njb; ++jb) {
-          const int u = q * njb + jb, s = u & 1;
-          const uint32_t ph = (u >> 1) & 1;
-          ptx::mbar_wait(&pm_full[s], ph, a.err, 86);
-          ptx::mbar_wait(&x_full[s], ph, a.err, 87);
-          ptx::tc_fence_after();
+        if (leader) {
           const uint32_t p0 = ptx::smem_u32(smem + s * st2p);
-          const uint32_t x0 = ptx::smem_u32(smem + 2 * st2p + s * st2x);
+          const uint32_t x0 = ptx::smem_u32(xbase + sx * st2x);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t pd = ptx::smem_desc(p0 + kk * 32, 16, 1024, ptx::kSw128);
@@ -172,50 +204,70 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
             ptx::mma_ss<false>(tmem + 256 + q * P, pd, xd, id_Y, 1u);
           }
           ptx::mma_commit(&pm_empty[s]);
-          ptx::mma_commit(&x_empty[s]);
+          ptx::mma_commit(&x_empty[sx]);
         }
-        ptx::mma_commit(&ydone[q]);
+        __syncwarp();
       }
+      if (leader) ptx::mma_commit(&ydone[q]);
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ row warps
-    const int row = tid;  // 0..127 = TMEM lane
+    const int quad = warp & 3, qtr = warp >> 2;  // TMEM lane quadrant, column quarter
+    const int row = quad * 32 + (tid & 31);       // 0..127 = TMEM lane
     const int i_rel = i0 + row;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    // in-chunk cumsums (log2 units) of the H heads
-    const int per = T > 128 ? 2 : 1;
-    for (int q = 0; q < H; ++q) {
-      const int h = hbase + q;
-      const float Ah = a.A[h] * kLog2e;
-      float d[2] = {0.f, 0.f}, c[2] = {0.f, 0.f}, run = 0.f;
-      for (int e = 0; e < per; ++e) {
-        const int j = row * per + e;
-        if (j < valid) d[e] = __bfloat162float(a.dt[((int64_t)b * L + tok0 + j) * nh + h]);
-        run += Ah * d[e];
-        c[e] = run;
-      }
+    const int rb = i_rel >> 6;                    // row's 64-token block
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+
+    // in-chunk cumsums (log2 units) of the H heads, one token per thread;
+    // every dt load is issued before the first scan
+    float dh[kMaxH];
+#pragma unroll
+    for (int q = 0; q < kMaxH; ++q)
+      dh[q] = (q < H && tid < valid)
+                  ? __bfloat162float(a.dt[((int64_t)b * L + tok0 + tid) * nh + hbase + q])
+                  : 0.f;
+#pragma unroll
+    for (int q = 0; q < kMaxH; ++q) {
+      if (q >= H) break;
+      const float run = a.A[hbase + q] * kLog2e * dh[q];
       float incl = run;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const float o = __shfl_up_sync(0xffffffffu, incl, off);
-        if ((row & 31) >= off) incl += o;
+        if ((tid & 31) >= off) incl += o;
       }
-      if ((row & 31) == 31) warp_tot[warp] = incl;
+      if ((tid & 31) == 31) warp_tot[warp] = incl;
       ptx::named_bar_sync(1, kRowThreads);
-      float base = incl - run;
-      for (int w2 = 0; w2 < warp; ++w2) base += warp_tot[w2];
-      for (int e = 0; e < per; ++e) {
-        const int j = row * per + e;
-        if (j < T) {
-          Gs[q][j] = base + c[e];
-          dts[q][j] = d[e];
-        }
+      float Gj = incl;
+      for (int w2 = 0; w2 < warp; ++w2) Gj += warp_tot[w2];
+      if (tid < T) {
+        Gs[q][tid] = Gj;
+        dts[q][tid] = dh[q];
       }
       ptx::named_bar_sync(1, kRowThreads);
+      if (tid < T) vs[q][tid] = exp2f(Gs[q][tid | 63] - Gj) * dh[q];
     }
+    ptx::named_bar_sync(1, kRowThreads);
     ptx::mbar_wait(&s1_done, 0, a.err, 88);
     ptx::tc_fence_after();
 
+    // x of this thread's row and column groups (16-column group g belongs to
+    // the warp with g % 4 == qtr), fetched before the wait on the head's
+    // MMAs so the load latency overlaps other work
+    uint4 xr[4];
+    auto fetch_x = [&](int q) {
+      const int64_t off = (((int64_t)b * L + tok0 + i_rel) * nh + hbase + q) * P;
+      const bool ok = i_rel < valid;
+#pragma unroll
+      for (int gi = 0; gi < 2; ++gi) {
+        const int c0 = (qtr + 4 * gi) * 16;
+        if (c0 < P && ok) {
+          xr[2 * gi] = *reinterpret_cast<const uint4 *>(a.x + off + c0);
+          xr[2 * gi + 1] = *reinterpret_cast<const uint4 *>(a.x + off + c0 + 8);
+        }
+      }
+    };
     auto epilogue = [&](int q) {
       ptx::mbar_wait(&ydone[q], 0, a.err, 89);
       ptx::tc_fence_after();
@@ -223,29 +275,35 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
       const float Dh = a.D ? a.D[h] : 0.f;
       const bool ok = i_rel < valid;
       const int64_t off = (((int64_t)b * L + tok0 + i_rel) * nh + h) * P;
-      for (int c0 = 0; c0 < P; c0 += 16) {
+#pragma unroll
+      for (int gi = 0; gi < 2; ++gi) {
+        const int c0 = (qtr + 4 * gi) * 16;
+        if (c0 >= P) break;
         float v[16];
         ptx::tmem_ld16_sync(tmem + lane_base + 256 + q * P + c0, v);
         if (ok) {
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
+          for (int hh = 0; hh < 2; ++hh) {
             float xv[8];
-            unpack16(*reinterpret_cast<const uint4 *>(a.x + off + c0 + half * 8), xv,
-                     (__nv_bfloat16 *)nullptr);
+            unpack16(xr[2 * gi + hh], xv, (__nv_bfloat16 *)nullptr);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xv[e] = fmaf(Dh, xv[e], v[half * 8 + e]);
-            *reinterpret_cast<uint4 *>(a.y + off + c0 + half * 8) =
+            for (int e = 0; e < 8; ++e) xv[e] = fmaf(Dh, xv[e], v[hh * 8 + e]);
+            *reinterpret_cast<uint4 *>(a.y + off + c0 + hh * 8) =
                 pack_io16(xv, (__nv_bfloat16 *)nullptr);
           }
         }
       }
     };
 
+    fetch_x(0);
     for (int q = 0; q < H; ++q) {
       const float Gi = Gs[q][min(i_rel, T - 1)];
       // carried-state term: Y_q *= exp2(G_i), then release Y_q to phase 2
       const float eg = exp2f(Gi);
-      for (int c0 = 0; c0 < P; c0 += 16) {
+#pragma unroll
+      for (int gi = 0; gi < 2; ++gi) {
+        const int c0 = (qtr + 4 * gi) * 16;
+        if (c0 >= P) break;
         float v[16];
         ptx::tmem_ld16_sync(tmem + lane_base + 256 + q * P + c0, v);
 #pragma unroll
@@ -255,37 +313,63 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&ysc[q]);
-      // decayed, masked interaction rows, 64 tokens at a time
+      // decayed, masked interaction rows: this thread takes 16 of each
+      // block's 64 tokens
       for (int jb = 0; jb < njb; ++jb) {
-        const int u = q * njb + jb, s = u & 1;
-        ptx::mbar_wait(&pm_empty[s], ((u >> 1) & 1) ^ 1, a.err, 90);
+        const int u = q * njb + jb, s = u % kNP;
+        ptx::mbar_wait(&pm_empty[s], ((u / kNP) & 1) ^ 1, a.err, 90);
         uint8_t *Pb = smem + s * st2p;
+        const int jc0 = jb * 64 + qtr * 16;
+        float v[16];
+        ptx::tmem_ld16_sync(tmem + lane_base + jc0, v);  // every lane of the warp
+        if (jb < rb) {
+          // whole block before the row's block: factored decay
+          const float ui = exp2f(Gi - Gs[q][jb * 64 + 63]);
+          const float4 *vp = reinterpret_cast<const float4 *>(&vs[q][jc0]);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int jc = jb * 64 + c4 * 16;
-          float v[16];
-          ptx::tmem_ld16_sync(tmem + lane_base + jc, v);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int j = jc + e;
-            v[e] = (j <= i_rel && j < valid) ? v[e] * exp2f(Gi - Gs[q][j]) * dts[q][j] : 0.f;
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 f = vp[e4];
+            v[4 * e4 + 0] *= ui * f.x;
+            v[4 * e4 + 1] *= ui * f.y;
+            v[4 * e4 + 2] *= ui * f.z;
+            v[4 * e4 + 3] *= ui * f.w;
           }
-          *reinterpret_cast<uint4 *>(Pb + sw128(row, c4 * 32)) =
-              pack_op16(v, (__nv_bfloat16 *)nullptr);
-          *reinterpret_cast<uint4 *>(Pb + sw128(row, c4 * 32 + 16)) =
-              pack_op16(v + 8, (__nv_bfloat16 *)nullptr);
+        } else if (jb == rb) {
+          const float4 *gp = reinterpret_cast<const float4 *>(&Gs[q][jc0]);
+          const float4 *dp = reinterpret_cast<const float4 *>(&dts[q][jc0]);
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 gj = gp[e4], dj = dp[e4];
+            const float ga[4] = {gj.x, gj.y, gj.z, gj.w}, da[4] = {dj.x, dj.y, dj.z, dj.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int j = jc0 + 4 * e4 + c;
+              v[4 * e4 + c] =
+                  (j <= i_rel && j < valid) ? v[4 * e4 + c] * exp2f(Gi - ga[c]) * da[c] : 0.f;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = 0.f;
         }
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          *reinterpret_cast<uint4 *>(Pb + sw128(row, (qtr * 2 + c) * 16)) =
+              pack_op16(v + c * 8, (__nv_bfloat16 *)nullptr);
         ptx::fence_async_smem();
         ptx::tc_fence_before();
         ptx::mbar_arrive(&pm_full[s]);
       }
-      if (q > 0) epilogue(q - 1);
+      if (q > 0) {
+        epilogue(q - 1);  // uses the x rows of head q-1 fetched earlier
+        fetch_x(q);       // in flight during the next head's decay pass
+      }
     }
     epilogue(H - 1);
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 5) ptx::tmem_dealloc(tmem, ncols);
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, ncols);
 }
 
 }  // namespace
@@ -308,8 +392,12 @@ cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const v
   const int nBr = (int)((std::min<int64_t>(d.T, 256) + 127) / 128);
   const int nPb = (int)((d.P + 63) / 64);
   const int st1 = kBlk * 2 + nBr * kBlk * 2 + H * nPb * kBlk;
-  const int st2 = 2 * (kBlk * 2) + 2 * nPb * kBlk;
-  const int smem = std::max(2 * st1, st2) + 1024;
+  const int st2x = nPb * kBlk;
+  // dynamic shared memory: two phase-1 stages and nX x stages, within the
+  // 227 KB per CTA less the static arrays
+  const int budget = 212 * 1024 - 2 * st1;
+  const int nX = std::max(2, std::min(kMaxX, budget / st2x));
+  const int smem = 2 * st1 + nX * st2x + 1024;
   cudaError_t e =
       cudaFuncSetAttribute(fwd_scan_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -328,6 +416,7 @@ cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const v
   a.T = (int)d.T;
   a.nc = (int)d.nc;
   a.H = H;
+  a.nX = nX;
   const int n_it = (int)((d.T + 127) / 128);
   dim3 grid((unsigned)(d.nc * n_it), (unsigned)(d.nh / H), (unsigned)d.b);
   fwd_scan_bf16<<<grid, kThreads, smem, st>>>(tC, tB, tx, tS, a);

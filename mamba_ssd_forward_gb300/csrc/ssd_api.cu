@@ -66,8 +66,12 @@ size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 WsLayout ws_layout(const Dims &d, ssd_dtype t) {
   WsLayout w;
   if (t == SSD_BF16) {
-    w.G = w.dstates = w.states = 0;
-    w.total = round256(2 * (size_t)(d.b * d.nh * d.nc * d.S * d.P));
+    // states (bf16) | jump terms (bf16) | per-chunk decays (fp32)
+    const size_t st = round256(2 * (size_t)(d.b * d.nh * d.nc * d.S * d.P));
+    w.states = 0;
+    w.dstates = st;
+    w.G = 2 * st;
+    w.total = w.G + round256(sizeof(float) * d.b * d.nh * d.nc);
     return w;
   }
   w.G = 0;
@@ -215,9 +219,14 @@ ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype, const voi
   };
   cudaError_t e = mark(0);
   if (dtype == SSD_BF16) {
-    // state pass (cumsum + chunk jump + sequential pass), then output pass
-    void *sts = ws;
-    if (e == cudaSuccess) e = ssd::launch_fwd_state(d, x, B, dt, A, h0, sts, final_state, st);
+    // chunk jump terms (all chunks in parallel), the sequential pass over
+    // chunks, then the output pass
+    void *sts = ws + w.states;
+    void *dH = ws + w.dstates;
+    float *gam = reinterpret_cast<float *>(ws + w.G);
+    if (e == cudaSuccess) e = ssd::launch_fwd_chunk_state(d, x, B, dt, A, dH, gam, st);
+    if (e == cudaSuccess && ++launched) e = mark(launched);
+    if (e == cudaSuccess) e = ssd::launch_fwd_state_pass(d, dH, gam, h0, sts, final_state, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
     if (e == cudaSuccess) e = ssd::launch_fwd_scan(d, x, B, C, dt, A, sts, D, y, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);

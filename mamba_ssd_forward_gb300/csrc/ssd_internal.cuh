@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ssd.h"
+#include "ssd.h"
 
 namespace ssd {
 
