@@ -178,6 +178,52 @@ SSD_API ssd_status ssd_forward_host(const ssd_dims *dims, ssd_dtype dtype, const
                                     void *y, float *final_state, void *workspace,
                                     size_t ws_bytes, void *stream);
 
+/* Size in bytes of the fixed device scratch array ssd_forward_noalloc uses as
+ * its workspace (32 MiB, reserved per device once the library's module is
+ * loaded there). */
+#define SSD_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* ssd_forward with no workspace argument and no allocation.  The page has no
+ * counterpart: this is a calling convention, not a step of the method.
+ *
+ * Who needs it: callers that cannot allocate device memory when they run the
+ * layer -- a runtime that has given all free device memory to its own pool
+ * up front and must not take more per call; a plain C caller with no
+ * allocator of its own to hand out a workspace; a latency-sensitive loop that
+ * cannot accept the device-wide synchronisation that cudaFree implies.
+ * Instead of a caller-provided workspace it uses a statically sized array
+ * inside this library (SSD_NOALLOC_SCRATCH_BYTES per device), so it calls
+ * neither cudaMalloc nor cudaFree nor any library routine that allocates.
+ *
+ * Limit: dims whose ssd_forward_workspace_size(dims, dtype) exceeds
+ * SSD_NOALLOC_SCRATCH_BYTES are rejected with SSD_ERR_UNSUPPORTED before
+ * anything is enqueued; use ssd_forward with your own workspace for those
+ * (for example bf16, b 4, L 2048, nh 24, P 64, S 128, T 256 needs about
+ * 25 MB and fits; b 2, L 4096, nh 80 with the same P, S, T needs about 84 MB
+ * and does not).  Invalid dims, dtype or pointers return the same codes as
+ * ssd_forward, with nothing enqueued.
+ *
+ * First-call set-up: the first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress, which may also load the library's
+ * module on that device) and caches it under a mutex.  Make one call on each
+ * device before starting any stream capture or other region that must not
+ * see such set-up; later calls only read the cache.  SSD_ERR_CUDA if the
+ * look-up fails.
+ *
+ * Concurrency: there is ONE array per device, shared by every call on that
+ * device.  Calls whose execution overlaps -- on different streams, or from
+ * different host threads without stream ordering between them -- race on it
+ * and corrupt each other's results.  Calls on one stream are ordered and
+ * safe.  Nothing in the array has to start at zero: each call writes every
+ * scratch byte it reads before reading it, so no clearing is needed between
+ * calls.  Arguments, layouts, outputs and errors are otherwise those of
+ * ssd_forward; the outputs are the values ssd_forward computes for the same
+ * inputs. */
+SSD_API ssd_status ssd_forward_noalloc(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                                       const void *dt, const float *A, const void *B,
+                                       const void *C, const float *D, const float *h0,
+                                       void *y, float *final_state, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,6 +14,8 @@ LIB_PATH = os.path.join(PKG, "libssd_gb300.so")
 
 SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT = range(5)
 SSD_F32, SSD_BF16 = 0, 1
+# Size of the fixed scratch array of ssd_forward_noalloc (SSD_NOALLOC_SCRATCH_BYTES).
+SSD_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # Every symbol include/ssd.h declares.
 EXPORTS = (
@@ -28,6 +30,7 @@ EXPORTS = (
     "ssd_forward_profiled",
     "ssd_forward_host_workspace_size",
     "ssd_forward_host",
+    "ssd_forward_noalloc",
 )
 
 
@@ -80,6 +83,8 @@ def load(path: str | None = None):
     lib.ssd_forward_host_workspace_size.argtypes = [dims_p, i32, i32, i32, i32]
     lib.ssd_forward_host.restype = i32
     lib.ssd_forward_host.argtypes = [dims_p, i32] + [vp] * 10 + [sz, vp]
+    lib.ssd_forward_noalloc.restype = i32
+    lib.ssd_forward_noalloc.argtypes = [dims_p, i32] + [vp] * 9 + [vp]
     if path is None:
         _lib = lib
     return lib

@@ -139,3 +139,22 @@ def test_product_path_never_touches_the_oracle():
         if fn.endswith((".py", ".c")):
             src = open(os.path.join(ROOT, "oracle", fn)).read()
             assert "mamba_ssd_forward_gb300" not in src, fn
+
+
+def test_noalloc_limit_and_rejections(lib):
+    """ssd_forward_noalloc: the header's scratch size matches the binding's,
+    and oversize or invalid dims are rejected before any CUDA call (so this
+    runs without a GPU)."""
+    from mamba_ssd_forward_gb300 import _abi
+    hdr = open(os.path.join(ROOT, "include", "ssd.h")).read()
+    m = re.search(r"#define\s+SSD_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", hdr)
+    assert m and int(m.group(1)) << int(m.group(2)) == _abi.SSD_NOALLOC_SCRATCH_BYTES
+    fake = ctypes.c_void_p(1 << 20)
+    big = dims(batch=2, seqlen=4096, nheads=80, ngroups=1)
+    assert lib.ssd_forward_workspace_size(ctypes.byref(big), 1) > _abi.SSD_NOALLOC_SCRATCH_BYTES
+    args = [fake, fake, fake, fake, fake, None, None, fake, None, None]
+    assert lib.ssd_forward_noalloc(ctypes.byref(big), 1, *args) == _abi.SSD_ERR_UNSUPPORTED
+    assert lib.ssd_forward_noalloc(ctypes.byref(dims(ngroups=3)), 1, *args) == 1
+    assert lib.ssd_forward_noalloc(ctypes.byref(dims(chunk=96)), 1, *args) == 2
+    assert lib.ssd_forward_noalloc(ctypes.byref(dims()), 7, *args) == 1
+    assert lib.ssd_forward_noalloc(None, 1, *args) == 1
