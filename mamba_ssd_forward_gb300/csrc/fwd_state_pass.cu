@@ -7,15 +7,16 @@
 //
 // A bandwidth kernel: each thread owns eight consecutive elements of one
 // (batch, head) state in the [S][P] layout, keeps them in fp32 registers, and
-// walks the chunks with the next chunk's load in flight.  dH and the stored
-// states are bf16 [b, nh, nc, S, P]; h0 and the final state are fp32
-// [b, nh, P, S] (the public layout).
+// walks the chunks with the next group of eight chunks' loads in flight.  dH
+// and the stored states are bf16 [b, nh, nc, S, P]; h0 and the final state
+// are fp32 [b, nh, P, S] (the public layout).
 #include "fwd.cuh"
 
 namespace ssd {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kDepth = 8;  // chunks per prefetch group
 
 __global__ void __launch_bounds__(kThreads)
 fwd_state_pass_bf16(const uint4 *__restrict__ dH, const float *__restrict__ gamma,
@@ -32,16 +33,37 @@ fwd_state_pass_bf16(const uint4 *__restrict__ dH, const float *__restrict__ gamm
   const uint4 *src = dH + bh * nc * n8 + e8;
   uint4 *dst = states + bh * nc * n8 + e8;
   const float *gm = gamma + bh * nc;
-  uint4 next = src[0];
-  for (int k = 0; k < nc; ++k) {
-    const uint4 cur = next;
-    if (k + 1 < nc) next = src[(int64_t)(k + 1) * n8];
-    dst[(int64_t)k * n8] = pack_io16(h, (__nv_bfloat16 *)nullptr);
-    float d[8];
-    unpack16(cur, d, (__nv_bfloat16 *)nullptr);
-    const float g = gm[k];
+  // Two groups of kDepth chunks: the next group's loads are issued before the
+  // current group is consumed, so up to 2 kDepth 16-byte loads are in flight.
+  uint4 cur[kDepth], nxt[kDepth];
+  float gcur[kDepth], gnxt[kDepth];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = fmaf(g, h[i], d[i]);
+  for (int i = 0; i < kDepth; ++i)
+    if (i < nc) {
+      cur[i] = src[(int64_t)i * n8];
+      gcur[i] = gm[i];
+    }
+  for (int k0 = 0; k0 < nc; k0 += kDepth) {
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i)
+      if (k0 + kDepth + i < nc) {
+        nxt[i] = src[(int64_t)(k0 + kDepth + i) * n8];
+        gnxt[i] = gm[k0 + kDepth + i];
+      }
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i)
+      if (k0 + i < nc) {
+        dst[(int64_t)(k0 + i) * n8] = pack_io16(h, (__nv_bfloat16 *)nullptr);
+        float d[8];
+        unpack16(cur[i], d, (__nv_bfloat16 *)nullptr);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) h[j] = fmaf(gcur[i], h[j], d[j]);
+      }
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i) {
+      cur[i] = nxt[i];
+      gcur[i] = gnxt[i];
+    }
   }
   if (final_state) {
 #pragma unroll
