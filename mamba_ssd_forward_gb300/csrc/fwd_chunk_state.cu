@@ -10,62 +10,99 @@
 // independent, so this runs fully in parallel; the sequential part is the
 // bandwidth kernel in fwd_state_pass.cu.
 //
-// One CTA per (chunk, 128-wide slice of S, group of H heads that share B,
-// batch).  Warp roles:
-//   warp 4 (TMA):  64-token blocks of B (MN-major, s contiguous; loaded once
-//                  for the H heads) and of x for each head (MN-major);
-//   warp 5 (MMA):  per block and head, M = 128 (s) x N = P MMAs into the
-//                  head's tensor-memory accumulator (lane = s, column = p);
-//   warps 0-3:     the heads' in-chunk cumsums and jump weights, the scaling
-//                  of each x row by its weight (in shared memory), and the
-//                  epilogue: dH as bf16 [b, nh, nc, S, P] (p contiguous, the
-//                  layout the output kernel reads), gamma as fp32.
+// Persistent: one CTA per SM walks a strided list of work items, an item
+// being (chunk, 128-wide slice of S, group of H heads that share B, batch).
+// The shared-memory ring of 64-token blocks runs across item boundaries, and
+// the tensor-memory accumulators are double-buffered by item, so the loads
+// of item j+1 stream in while item j is reduced and item j-1 is written out.
+// Warp roles:
+//   warp 8 (TMA):  per block, B (MN-major, s contiguous; once for the H heads)
+//                  and x of each head (MN-major);
+//   warp 9 (MMA):  per block and head, M = 128 (s) x N = P MMAs into the
+//                  item's accumulator set (lane = s, column = p);
+//   warps 0-7:     per item, the heads' in-chunk cumsums and jump weights
+//                  (dt and A fetched one item ahead), the scaling of each x
+//                  row by its weight in shared memory, then the previous
+//                  item's epilogue: each head's dH tile staged in shared
+//                  memory and written by a TMA store as bf16
+//                  [b, nh, nc, S, P] (p contiguous, the layout the output
+//                  kernel reads); gamma as fp32.
 #include "fwd.cuh"
 
 namespace ssd {
 namespace {
 
-constexpr int kStateThreads = 128;
-constexpr int kThreads = kStateThreads + 64;
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
-constexpr int kKB = 64;  // tokens per pipeline stage
-constexpr int kNST = 2;  // pipeline stages
+constexpr int kRowWarps = 8;
+constexpr int kRowThreads = kRowWarps * 32;
+constexpr int kThreads = kRowThreads + 64;
+constexpr int kProducerWarp = kRowWarps, kMmaWarp = kRowWarps + 1;
+constexpr int kKB = 64;     // tokens per pipeline stage
+constexpr int kMaxNST = 4;  // pipeline stages (at most)
 constexpr int kMaxH = 4;
-constexpr int kBlk = kKB * 128;
+constexpr int kBlk = kKB * 128;   // 64 rows of 128 bytes
+constexpr int kOutBlk = 128 * 128;  // one staged dH tile: 128 s rows x 64 p
 
-__global__ void __launch_bounds__(kThreads, 2)
+struct CsArgs {
+  const __nv_bfloat16 *dt;
+  const float *A;
+  float *gamma;
+  int *err;
+  int L, nh, P, S, hpg, T, nc, H, n_st, n_hg, nst, n_items;
+};
+
+// Work item -> (batch, chunk, S slice, first head).  The head groups of one
+// (chunk, slice) are adjacent, so CTAs running at the same time share B in L2.
+struct Item {
+  int b, k, st, hbase;
+};
+__device__ __forceinline__ Item decode(int item, const CsArgs &a) {
+  Item it;
+  const int hg = item % a.n_hg;
+  int r = item / a.n_hg;
+  it.st = r % a.n_st;
+  r /= a.n_st;
+  it.k = r % a.nc;
+  it.b = r / a.nc;
+  it.hbase = hg * a.H;
+  return it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
 fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
-                     const __grid_constant__ CUtensorMap tm_x, const __nv_bfloat16 *__restrict__ dt,
-                     const float *__restrict__ A, __nv_bfloat16 *__restrict__ dH,
-                     float *__restrict__ gamma, int *__restrict__ err, int L, int nh, int P, int S,
-                     int hpg, int T, int nc, int H) {
+                     const __grid_constant__ CUtensorMap tm_x,
+                     const __grid_constant__ CUtensorMap tm_dH, const CsArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t full[kNST], scaled[kNST], empty[kNST], done;
+  __shared__ __align__(8) uint64_t full[kMaxNST], scaled[kMaxNST], empty[kMaxNST], acc_full[2],
+      acc_free[2];
   __shared__ uint32_t tmem_slot;
-  __shared__ float w_s[kMaxH][256];
-  __shared__ float warp_tot[4];
+  __shared__ float w_s[2][kMaxH][256];             // jump weights, by item parity
+  __shared__ float warp_tot[2][kMaxH][kRowWarps];  // cumsum partials, by item parity
 
-  const int n_st = (S + 127) / 128;
-  const int k = blockIdx.x / n_st, st_idx = blockIdx.x % n_st;
-  const int hbase = blockIdx.y * H, b = blockIdx.z, g = hbase / hpg;
-  const int s0 = st_idx * 128;
+  const int L = a.L, nh = a.nh, P = a.P, T = a.T, nc = a.nc, H = a.H, nst = a.nst;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int nPb = (P + 63) / 64;
-  const int xbytes = nPb * kBlk;                       // one head's x block
-  const int stage_bytes = 2 * kBlk + H * xbytes;       // B block | x blocks
-  const int tok0 = k * T;
-  const int valid = min(T, L - tok0);
-  const int nkb = (valid + kKB - 1) / kKB;
-  const uint32_t ncols = H * P <= 32 ? 32 : (H * P <= 64 ? 64 : (H * P <= 128 ? 128 : 256));
+  const int xbytes = nPb * kBlk;                  // one head's x block
+  const int stage_bytes = 2 * kBlk + H * xbytes;  // B block | x blocks
+  uint8_t *ostage = smem + nst * stage_bytes;     // two staged dH tiles
+  const int obytes = nPb * kOutBlk;
+  const int HP = H * P;
+  const uint32_t ncols = 2 * HP <= 32    ? 32
+                         : 2 * HP <= 64  ? 64
+                         : 2 * HP <= 128 ? 128
+                         : 2 * HP <= 256 ? 256
+                                         : 512;
 
   if (tid == 0) {
-    for (int i = 0; i < kNST; ++i) {
+    for (int i = 0; i < nst; ++i) {
       ptx::mbar_init(&full[i], 1);
-      ptx::mbar_init(&scaled[i], kStateThreads);
+      ptx::mbar_init(&scaled[i], kRowThreads);
       ptx::mbar_init(&empty[i], 1);
     }
-    ptx::mbar_init(&done, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&acc_full[i], 1);
+      ptx::mbar_init(&acc_free[i], kRowThreads);
+    }
     ptx::fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -80,163 +117,300 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int st = kb % kNST;
-      ptx::mbar_wait(&empty[st], ((kb / kNST) & 1) ^ 1, err, 101);
-      if (leader) {
-        uint8_t *Bb = smem + st * stage_bytes;
-        uint8_t *Xb = Bb + 2 * kBlk;
-        const int tok = tok0 + kb * kKB;
-        ptx::mbar_arrive_expect_tx(&full[st], stage_bytes);
-        for (int mb = 0; mb < 2; ++mb)
-          ptx::tma_load_4d(Bb + mb * kBlk, &tm_B, s0 + mb * 64, g, tok, b, &full[st]);
-        for (int q = 0; q < H; ++q)
-          for (int pb = 0; pb < nPb; ++pb)
-            ptx::tma_load_4d(Xb + q * xbytes + pb * kBlk, &tm_x, pb * 64, hbase + q, tok, b,
-                             &full[st]);
+    if (leader) {
+      ptx::prefetch_tmap(&tm_B);
+      ptx::prefetch_tmap(&tm_x);
+    }
+    int u = 0;
+    for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+      const Item it = decode(item, a);
+      const int tok0 = it.k * T;
+      const int nkb = (min(T, L - tok0) + kKB - 1) / kKB;
+      const int g = it.hbase / a.hpg;  // the heads' group: B[b, t, g, :]
+      for (int kb = 0; kb < nkb; ++kb, ++u) {
+        const int s = u % nst;
+        ptx::mbar_wait(&empty[s], ((u / nst) & 1) ^ 1, a.err, 101);
+        if (leader) {
+          uint8_t *Bb = smem + s * stage_bytes;
+          uint8_t *Xb = Bb + 2 * kBlk;
+          const int tok = tok0 + kb * kKB;
+          ptx::mbar_arrive_expect_tx(&full[s], stage_bytes);
+          for (int mb = 0; mb < 2; ++mb)
+            ptx::tma_load_4d(Bb + mb * kBlk, &tm_B, it.st * 128 + mb * 64, g, tok, it.b,
+                             &full[s]);
+          for (int q = 0; q < H; ++q)
+            for (int pb = 0; pb < nPb; ++pb)
+              ptx::tma_load_4d(Xb + q * xbytes + pb * kBlk, &tm_x, pb * 64, it.hbase + q, tok,
+                               it.b, &full[s]);
+        }
+        __syncwarp();
       }
-      __syncwarp();
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = ptx::idesc_bf16(128, P, true, true);
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int st = kb % kNST;
-      ptx::mbar_wait(&scaled[st], (kb / kNST) & 1, err, 102);
+    int u = 0, jl = 0;
+    for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++jl) {
+      const Item it = decode(item, a);
+      const int nkb = (min(T, L - it.k * T) + kKB - 1) / kKB;
+      const int set = jl & 1;
+      ptx::mbar_wait(&acc_free[set], ((jl >> 1) & 1) ^ 1, a.err, 102);
       ptx::tc_fence_after();
-      if (leader) {
-        const uint32_t b0 = ptx::smem_u32(smem + st * stage_bytes);
-        const uint32_t x0 = b0 + 2 * kBlk;
-        for (int q = 0; q < H; ++q) {
+      for (int kb = 0; kb < nkb; ++kb, ++u) {
+        const int s = u % nst;
+        ptx::mbar_wait(&scaled[s], (u / nst) & 1, a.err, 103);
+        ptx::tc_fence_after();
+        if (leader) {
+          const uint32_t b0 = ptx::smem_u32(smem + s * stage_bytes);
+          const uint32_t x0 = b0 + 2 * kBlk;
+          for (int q = 0; q < H; ++q) {
 #pragma unroll
-          for (int kk = 0; kk < kKB / 16; ++kk) {
-            const uint64_t ad = ptx::smem_desc(b0 + kk * 2048, kBlk, 1024, ptx::kSw128);
-            const uint64_t bd =
-                ptx::smem_desc(x0 + q * xbytes + kk * 2048, kBlk, 1024, ptx::kSw128);
-            ptx::mma_ss<false>(tmem + q * P, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+            for (int kk = 0; kk < kKB / 16; ++kk) {
+              const uint64_t ad = ptx::smem_desc(b0 + kk * 2048, kBlk, 1024, ptx::kSw128);
+              const uint64_t bd =
+                  ptx::smem_desc(x0 + q * xbytes + kk * 2048, kBlk, 1024, ptx::kSw128);
+              ptx::mma_ss<false>(tmem + set * HP + q * P, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+            }
           }
+          ptx::mma_commit(&empty[s]);
         }
-        ptx::mma_commit(&empty[st]);
+        __syncwarp();
       }
+      if (leader) ptx::mma_commit(&acc_full[set]);
       __syncwarp();
     }
-    if (leader) ptx::mma_commit(&done);
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ row warps
-    // in-chunk cumsums of the H heads (two tokens per thread), jump weights
-    const int per = T > 128 ? 2 : 1;
-    float d[kMaxH][2];
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, column half
+    const int lrow = quad * 32 + (tid & 31);       // row of the S slice = TMEM lane
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const int ngrp = P / 16;                       // 16-column groups of a head
+
+    // dt and A of the next item, one token per thread
+    float d[kMaxH], Aq[kMaxH];
+    auto fetch = [&](int item) {
 #pragma unroll
-    for (int q = 0; q < kMaxH; ++q)
+      for (int q = 0; q < kMaxH; ++q) d[q] = Aq[q] = 0.f;
+      if (item >= a.n_items) return;
+      const Item it = decode(item, a);
+      const int tok0 = it.k * T, valid = min(T, L - tok0);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int j = tid * per + e;
-        d[q][e] = (q < H && e < per && j < valid)
-                      ? __bfloat162float(dt[((int64_t)b * L + tok0 + j) * nh + hbase + q])
-                      : 0.f;
-      }
+      for (int q = 0; q < kMaxH; ++q)
+        if (q < H) {
+          Aq[q] = a.A[it.hbase + q];
+          if (tid < valid)
+            d[q] = __bfloat162float(a.dt[((int64_t)it.b * L + tok0 + tid) * nh + it.hbase + q]);
+        }
+    };
+
+    int n_out = 0;  // dH tiles staged so far; tile n uses staging buffer n & 1
+    auto epilogue = [&](const Item &it, int jl) {
+      const int set = jl & 1;
+      ptx::mbar_wait(&acc_full[set], (jl >> 1) & 1, a.err, 104);
+      ptx::tc_fence_after();
+      for (int q = 0; q < H; ++q, ++n_out) {
+        uint8_t *stg = ostage + (n_out & 1) * obytes;
+        // the store issued two tiles ago has finished reading this buffer
+        if (tid == 0 && n_out >= 2) ptx::bulk_wait_read<1>();
+        ptx::named_bar_sync(2, kRowThreads);
+        for (int g0 = half; g0 < ngrp; g0 += 4) {
+          // up to two 16-column groups per pass: g0 and g0 + 2
+          uint32_t r0[16], r1[16];
+          const bool two = g0 + 2 < ngrp;
+          ptx::tmem_ld16(tmem + lane_base + set * HP + q * P + g0 * 16, r0);
+          if (two) ptx::tmem_ld16(tmem + lane_base + set * HP + q * P + (g0 + 2) * 16, r1);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence(r0);
+          ptx::reg_fence(r1);
 #pragma unroll
-    for (int q = 0; q < kMaxH; ++q) {
-      if (q >= H) break;
-      const float Ah = A[hbase + q] * kLog2e;
-      float c[2], run = 0.f;
+          for (int t = 0; t < 2; ++t) {
+            if (t == 1 && !two) break;
+            const int gg = g0 + 2 * t;
+            const uint32_t *r = t ? r1 : r0;
+            float v[16];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        run += Ah * d[q][e];
-        c[e] = run;
-      }
-      float incl = run;
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+            uint8_t *blk = stg + (gg >> 2) * kOutBlk;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_up_sync(0xffffffffu, incl, off);
-        if ((tid & 31) >= off) incl += o;
-      }
-      if ((tid & 31) == 31) warp_tot[warp] = incl;
-      ptx::named_bar_sync(1, kStateThreads);
-      float base = incl - run;
-      for (int w2 = 0; w2 < warp; ++w2) base += warp_tot[w2];
-      // the chunk's last real token is the last nonzero contribution, so the
-      // block total equals G at position valid - 1
-      float tot = 0.f;
-      for (int w2 = 0; w2 < 4; ++w2) tot += warp_tot[w2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int j = tid * per + e;
-        if (e < per && j < T) w_s[q][j] = j < valid ? exp2f(tot - (base + c[e])) * d[q][e] : 0.f;
-      }
-      if (tid == 0 && st_idx == 0) gamma[((int64_t)b * nh + hbase + q) * nc + k] = exp2f(tot);
-      ptx::named_bar_sync(1, kStateThreads);
-    }
-    // scale each head's x rows by its weights
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int st = kb % kNST;
-      uint8_t *Xb = smem + st * stage_bytes + 2 * kBlk;
-      ptx::mbar_wait(&full[st], (kb / kNST) & 1, err, 103);
-      const int nchunks = nPb * kKB * 8;  // 16-byte chunks of one head's block
-      for (int c = tid; c < H * nchunks; c += kStateThreads) {
-        const int q = c / nchunks, cc = c % nchunks;
-        const float ws = w_s[q][kb * kKB + ((cc >> 3) & (kKB - 1))];
-        uint4 *p4 = reinterpret_cast<uint4 *>(Xb + q * xbytes + cc * 16);
-        float v[8];
-        unpack16(*p4, v, (__nv_bfloat16 *)nullptr);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] *= ws;
-        *p4 = pack_op16(v, (__nv_bfloat16 *)nullptr);
-      }
-      ptx::fence_async_smem();
-      ptx::mbar_arrive(&scaled[st]);
-    }
-    // epilogue: this thread's row s of every head's dH
-    ptx::mbar_wait(&done, 0, err, 104);
-    ptx::tc_fence_after();
-    const int srow = s0 + tid;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    for (int q = 0; q < H; ++q) {
-      __nv_bfloat16 *o = dH + ((((int64_t)b * nh + hbase + q) * nc + k) * S + srow) * P;
-      for (int c0 = 0; c0 < P; c0 += 16) {
-        float v[16];
-        ptx::tmem_ld16_sync(tmem + lane_base + q * P + c0, v);
-        if (srow < S) {
-          uint4 *o4 = reinterpret_cast<uint4 *>(o + c0);
-          o4[0] = pack_io16(v, (__nv_bfloat16 *)nullptr);
-          o4[1] = pack_io16(v + 8, (__nv_bfloat16 *)nullptr);
+            for (int e = 0; e < 2; ++e)
+              *reinterpret_cast<uint4 *>(blk + sw128(lrow, ((gg & 3) * 2 + e) * 16)) =
+                  pack_io16(v + 8 * e, (__nv_bfloat16 *)nullptr);
+          }
+        }
+        ptx::fence_async_smem();
+        ptx::named_bar_sync(2, kRowThreads);
+        if (tid == 0) {
+          const int row3 = ((it.b * nh + it.hbase + q) * nc + it.k);
+          for (int pb = 0; pb < nPb; ++pb)
+            ptx::tma_store_3d(&tm_dH, stg + pb * kOutBlk, pb * 64, it.st * 128, row3);
+          ptx::bulk_commit();
         }
       }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&acc_free[set]);
+    };
+
+    fetch(blockIdx.x);
+    Item prev{0, 0, 0, 0};
+    int u = 0, jl = 0;
+    for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++jl) {
+      const Item it = decode(item, a);
+      const int tok0 = it.k * T, valid = min(T, L - tok0);
+      const int nkb = (valid + kKB - 1) / kKB;
+      float(*w)[256] = w_s[jl & 1];
+      float(*wt)[kRowWarps] = warp_tot[jl & 1];
+      // in-chunk cumsums of the H heads (one token per thread) and the jump
+      // weights; the last real token is the last nonzero contribution, so
+      // the block total equals G at position valid - 1
+      float incl[kMaxH];
+#pragma unroll
+      for (int q = 0; q < kMaxH; ++q) {
+        incl[q] = Aq[q] * kLog2e * d[q];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float o = __shfl_up_sync(0xffffffffu, incl[q], off);
+          if ((tid & 31) >= off) incl[q] += o;
+        }
+        if ((tid & 31) == 31 && q < H) wt[q][warp] = incl[q];
+      }
+      ptx::named_bar_sync(1, kRowThreads);
+#pragma unroll
+      for (int q = 0; q < kMaxH; ++q) {
+        if (q >= H) break;
+        float base = 0.f, tot = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kRowWarps; ++w2) {
+          const float t = wt[q][w2];
+          tot += t;
+          if (w2 < warp) base += t;
+        }
+        if (tid < T) w[q][tid] = tid < valid ? exp2f(tot - (base + incl[q])) * d[q] : 0.f;
+        if (tid == 0 && it.st == 0)
+          a.gamma[((int64_t)it.b * nh + it.hbase + q) * nc + it.k] = exp2f(tot);
+      }
+      ptx::named_bar_sync(1, kRowThreads);
+      fetch(item + gridDim.x);  // in flight while this item is scaled
+
+      // scale each head's x rows by its weights: thread = (row, quarter of
+      // the row's eight 16-byte chunks), every load issued before the math
+      const int r = tid & 63, part = tid >> 6;
+      const int nqp = H * nPb;  // 64-column x blocks in a stage, <= 4
+      for (int kb = 0; kb < nkb; ++kb, ++u) {
+        const int s = u % nst;
+        uint8_t *Xb = smem + s * stage_bytes + 2 * kBlk;
+        ptx::mbar_wait(&full[s], (u / nst) & 1, a.err, 105);
+        uint4 buf[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if ((i >> 1) < nqp)
+            buf[i] = *reinterpret_cast<const uint4 *>(Xb + (i >> 1) * kBlk +
+                                                      sw128(r, (part * 2 + (i & 1)) * 16));
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if ((i >> 1) < nqp) {
+            const float ws = w[(i >> 1) / nPb][kb * kKB + r];
+            float v[8];
+            unpack16(buf[i], v, (__nv_bfloat16 *)nullptr);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] *= ws;
+            *reinterpret_cast<uint4 *>(Xb + (i >> 1) * kBlk +
+                                       sw128(r, (part * 2 + (i & 1)) * 16)) =
+                pack_op16(v, (__nv_bfloat16 *)nullptr);
+          }
+        ptx::fence_async_smem();
+        ptx::mbar_arrive(&scaled[s]);
+      }
+      if (jl > 0) epilogue(prev, jl - 1);
+      prev = it;
     }
+    if (jl > 0) epilogue(prev, jl - 1);
+    if (tid == 0) ptx::bulk_wait<0>();  // every dH store complete
   }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, ncols);
 }
 
+int sm_count() {
+  static int n[256];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 148;
+  if (!n[dev] &&
+      cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    n[dev] = 148;
+  return n[dev];
+}
+
 }  // namespace
 
+// Heads per item: a divisor of the heads per group with H * P <= 256 (two
+// accumulator sets fit the 512 tensor-memory columns) and at most four
+// 64-column x blocks per stage, chosen to minimise
+// the bytes the busiest CTA loads (items per CTA, rounded up, times B's
+// slice plus H heads of x per item).
 int fwd_state_heads(const Dims &d) {
   const int hmax = (int)std::min<int64_t>(kMaxH, 256 / d.P);
-  for (int h = hmax; h > 1; --h)
-    if (d.hpg % h == 0) return h;
-  return 1;
+  const int64_t n_st = (d.S + 127) / 128;
+  const int64_t ctas = sm_count();
+  int best = 1;
+  double best_cost = 1e300;
+  for (int h = 1; h <= hmax; ++h) {
+    if (d.hpg % h || h * ((d.P + 63) / 64) > 4) continue;  // <= 4 x blocks per stage
+    const int64_t items = d.b * d.nc * n_st * (d.nh / h);
+    const double per_item = 2.0 * kBlk + h * ((d.P + 63) / 64) * (double)kBlk;
+    const double cost = (double)((items + ctas - 1) / ctas) * per_item;
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = h;
+    }
+  }
+  return best;
 }
 
 cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, const void *dt,
                                    const float *A, void *dH, float *gamma, cudaStream_t st) {
+  if (d.T > kRowThreads) return cudaErrorInvalidValue;  // one token per row thread
   const int H = fwd_state_heads(d);
-  CUtensorMap tB, tx;
+  CUtensorMap tB, tx, tD;
   if (!make_tmap_bl(&tB, B, true, d.b, d.L, d.ng, d.S, kKB) ||
       !make_tmap_bl(&tx, x, true, d.b, d.L, d.nh, d.P, kKB))
     return cudaErrorInvalidValue;
+  {
+    // dH as [b * nh * nc][S][P]; one box = 128 rows of S x 64 columns of P
+    const uint64_t dims[3] = {(uint64_t)d.P, (uint64_t)d.S, (uint64_t)(d.b * d.nh * d.nc)};
+    const uint64_t strides[2] = {(uint64_t)d.P * 2, (uint64_t)(d.S * d.P * 2)};
+    const uint32_t box[3] = {64u, 128u, 1u};
+    if (!make_tmap_sw128(&tD, dH, true, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
   const int nPb = (int)((d.P + 63) / 64);
-  const int smem = kNST * (2 * kBlk + H * nPb * kBlk) + 1024;
+  const int stage_bytes = 2 * kBlk + H * nPb * kBlk;
+  const int obytes = 2 * nPb * kOutBlk;
+  const int nst = std::max(2, std::min(kMaxNST, (208 * 1024 - obytes) / stage_bytes));
+  const int smem = nst * stage_bytes + obytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(fwd_chunk_state_bf16,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int n_st = (int)((d.S + 127) / 128);
-  dim3 grid((unsigned)(d.nc * n_st), (unsigned)(d.nh / H), (unsigned)d.b);
-  fwd_chunk_state_bf16<<<grid, kThreads, smem, st>>>(
-      tB, tx, static_cast<const __nv_bfloat16 *>(dt), A, static_cast<__nv_bfloat16 *>(dH), gamma,
-      device_error_word(), (int)d.L, (int)d.nh, (int)d.P, (int)d.S, (int)d.hpg, (int)d.T,
-      (int)d.nc, H);
+  CsArgs a;
+  a.dt = static_cast<const __nv_bfloat16 *>(dt);
+  a.A = A;
+  a.gamma = gamma;
+  a.err = device_error_word();
+  a.L = (int)d.L;
+  a.nh = (int)d.nh;
+  a.P = (int)d.P;
+  a.S = (int)d.S;
+  a.hpg = (int)d.hpg;
+  a.T = (int)d.T;
+  a.nc = (int)d.nc;
+  a.H = H;
+  a.n_st = (int)((d.S + 127) / 128);
+  a.n_hg = (int)(d.nh / H);
+  a.nst = nst;
+  const int64_t n_items = d.b * d.nc * a.n_st * a.n_hg;
+  if (n_items > 0x7fffffffLL || d.b * d.nh * d.nc > 0x7fffffffLL) return cudaErrorInvalidValue;
+  a.n_items = (int)n_items;
+  const int grid = (int)std::min<int64_t>(n_items, sm_count());
+  fwd_chunk_state_bf16<<<grid, kThreads, smem, st>>>(tB, tx, tD, a);
   return cudaGetLastError();
 }
 
