@@ -331,7 +331,13 @@ def run_ours(args, w):
     n_l = 0
     for i in range(args.steps):
         flush()
-        n_l = step(ev[i])
+        if args.kernel_events == "separate":
+            ev[i][0].record()
+            n_l = step([])
+            for j in range(1, n_l + 1):
+                ev[i][j].record()  # all after the step: step time = ev[0] -> ev[n_l]
+        else:
+            n_l = step(ev[i])
         launches += n_l
     torch.cuda.synchronize()
     if world > 1:
@@ -345,6 +351,19 @@ def run_ours(args, w):
     kern_ms = {names[j]: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1])
                                                 for i in range(args.steps))
                for j in range(n_l)}
+    if args.kernel_events == "separate":
+        # the timed steps above recorded only their first and last events;
+        # the per-kernel split comes from as many steps again with an event
+        # between launches (events between launches serialise them)
+        ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush()
+            step(ev2[i])
+        torch.cuda.synchronize()
+        kern_ms = {names[j]: statistics.mean(ev2[i][j].elapsed_time(ev2[i][j + 1])
+                                                    for i in range(args.steps))
+                   for j in range(n_l)}
     ms = statistics.mean(step_ms)
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -439,6 +458,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD.name)
+    ap.add_argument("--kernel-events", choices=["inline", "separate"], default="inline",
+                    help="inline: CUDA events between the launches of every timed step; "
+                         "separate: timed steps carry only start/end events and the "
+                         "per-kernel split is taken from extra steps after the timed region")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--flush", choices=["write+read", "write"], default="write+read",

@@ -18,8 +18,9 @@
 // Warp roles:
 //   warp 8 (TMA):  per block, B (MN-major, s contiguous; once for the H heads)
 //                  and x of each head (MN-major);
-//   warp 9 (MMA):  per block and head, M = 128 (s) x N = P MMAs into the
-//                  item's accumulator set (lane = s, column = p);
+//   warp 9 (MMA):  per block, M = 128 (s) x N = H P MMAs (one per head when
+//                  P is not a multiple of 64) into the item's accumulator set
+//                  (lane = s, column = head * P + p);
 //   warps 0-7:     per item, the heads' in-chunk cumsums and jump weights
 //                  (dt and A fetched one item ahead), the scaling of each x
 //                  row by its weight in shared memory, then the previous
@@ -114,6 +115,7 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const bool leader = (tid & 31) == 0;
+  ptx::griddep_launch_dependents();  // the state pass may be scheduled now
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -148,7 +150,11 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = ptx::idesc_bf16(128, P, true, true);
+    // With P a multiple of 64 the heads' x blocks abut in shared memory and
+    // form one N = H P operand: one MMA per K step reads the B tile once.
+    const bool merged = (P % 64) == 0;
+    const uint32_t idesc = ptx::idesc_bf16(128, merged ? HP : P, true, true);
+    const int n_mma = merged ? 1 : H;
     int u = 0, jl = 0;
     for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++jl) {
       const Item it = decode(item, a);
@@ -163,7 +169,7 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
         if (leader) {
           const uint32_t b0 = ptx::smem_u32(smem + s * stage_bytes);
           const uint32_t x0 = b0 + 2 * kBlk;
-          for (int q = 0; q < H; ++q) {
+          for (int q = 0; q < n_mma; ++q) {
 #pragma unroll
             for (int kk = 0; kk < kKB / 16; ++kk) {
               const uint64_t ad = ptx::smem_desc(b0 + kk * 2048, kBlk, 1024, ptx::kSw128);
@@ -186,20 +192,26 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const int ngrp = P / 16;                       // 16-column groups of a head
 
-    // dt and A of the next item, one token per thread
-    float d[kMaxH], Aq[kMaxH];
+    // dt and A of the next item, one token per thread.  dt stays in its
+    // bf16 bits until the cumsum uses it, so no instruction waits on the
+    // loads before then.
+    unsigned short draw[kMaxH];
+    float Aq[kMaxH];
     auto fetch = [&](int item) {
 #pragma unroll
-      for (int q = 0; q < kMaxH; ++q) d[q] = Aq[q] = 0.f;
+      for (int q = 0; q < kMaxH; ++q) {
+        draw[q] = 0;
+        Aq[q] = 0.f;
+      }
       if (item >= a.n_items) return;
       const Item it = decode(item, a);
       const int tok0 = it.k * T, valid = min(T, L - tok0);
+      const unsigned short *dtp = reinterpret_cast<const unsigned short *>(a.dt);
 #pragma unroll
       for (int q = 0; q < kMaxH; ++q)
         if (q < H) {
           Aq[q] = a.A[it.hbase + q];
-          if (tid < valid)
-            d[q] = __bfloat162float(a.dt[((int64_t)it.b * L + tok0 + tid) * nh + it.hbase + q]);
+          if (tid < valid) draw[q] = dtp[((int64_t)it.b * L + tok0 + tid) * nh + it.hbase + q];
         }
     };
 
@@ -262,9 +274,10 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
       // in-chunk cumsums of the H heads (one token per thread) and the jump
       // weights; the last real token is the last nonzero contribution, so
       // the block total equals G at position valid - 1
-      float incl[kMaxH];
+      float incl[kMaxH], d[kMaxH];
 #pragma unroll
       for (int q = 0; q < kMaxH; ++q) {
+        d[q] = __uint_as_float((uint32_t)draw[q] << 16);  // bf16 -> fp32, exact
         incl[q] = Aq[q] * kLog2e * d[q];
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {

@@ -133,6 +133,9 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
         ptx::tma_load_4d(Cb, &tm_C, sb * 64, g, tok0 + i0, b, &full1[s]);
         for (int r = 0; r < nBr; ++r)
           ptx::tma_load_4d(Bb + r * 2 * kBlk, &tm_B, sb * 64, g, tok0 + r * 128, b, &full1[s]);
+        // the start states are written by the preceding kernel (the state
+        // pass), which may still be running when this CTA starts
+        if (sb == 0) ptx::griddep_wait();
         for (int q = 0; q < H; ++q) {
           const int row = (b * nh + hbase + q) * nc + k;
           for (int pb = 0; pb < nPb; ++pb)
@@ -159,6 +162,11 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
     // ------------------------------------------------------------ MMA issuer
     const uint32_t id_S = ptx::idesc_bf16(128, jext, false, false);
     const uint32_t id_Y = ptx::idesc_bf16(128, P, false, true);
+    // with P a multiple of 64 the heads' state tiles abut in shared memory:
+    // Y_q += C h_q^T for every head in one N = H P MMA
+    const bool merged = (P % 64) == 0;
+    const uint32_t id_Yall = ptx::idesc_bf16(128, merged ? H * P : P, false, true);
+    const int n_ymma = merged ? 1 : H;
     for (int sb = 0; sb < nsb; ++sb) {
       const int s = sb & 1;
       uint8_t *Cb = smem + s * st1;
@@ -174,10 +182,10 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
           const uint64_t bd = ptx::smem_desc(b0 + kk * 32, 16, 1024, ptx::kSw128);
           const uint32_t acc = (sb | kk) ? 1u : 0u;
           ptx::mma_ss<false>(tmem, cd, bd, id_S, acc);
-          for (int q = 0; q < H; ++q) {
+          for (int q = 0; q < n_ymma; ++q) {
             const uint64_t hd = ptx::smem_desc(h0 + q * nPb * kBlk + kk * 2048, kBlk, 1024,
                                                ptx::kSw128);
-            ptx::mma_ss<false>(tmem + 256 + q * P, cd, hd, id_Y, acc);
+            ptx::mma_ss<false>(tmem + 256 + q * P, cd, hd, id_Yall, acc);
           }
         }
         ptx::mma_commit(&empty1[s]);
@@ -419,8 +427,20 @@ cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const v
   a.nX = nX;
   const int n_it = (int)((d.T + 127) / 128);
   dim3 grid((unsigned)(d.nc * n_it), (unsigned)(d.nh / H), (unsigned)d.b);
-  fwd_scan_bf16<<<grid, kThreads, smem, st>>>(tC, tB, tx, tS, a);
-  return cudaGetLastError();
+  // programmatic stream serialisation: CTAs may start (barriers, tensor
+  // memory, cumsums, C and B loads) while the state pass finishes; the
+  // producer waits on the device before loading the start states
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fwd_scan_bf16, tC, tB, tx, tS, a);
 }
 
 }  // namespace ssd

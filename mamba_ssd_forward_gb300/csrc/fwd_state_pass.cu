@@ -27,9 +27,11 @@ fwd_state_pass_bf16(const uint4 *__restrict__ dH, const float *__restrict__ gamm
   const int e8 = blockIdx.x * kThreads + threadIdx.x;
   if (e8 >= n8) return;
   const int s = (e8 * 8) / P, p0 = (e8 * 8) % P;
+  ptx::griddep_launch_dependents();  // the output pass may be scheduled now
   float h[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) h[i] = h0 ? h0[(bh * P + p0 + i) * S + s] : 0.f;
+  ptx::griddep_wait();  // dH and gamma come from the preceding kernel
   const uint4 *src = dH + bh * nc * n8 + e8;
   uint4 *dst = states + bh * nc * n8 + e8;
   const float *gm = gamma + bh * nc;
@@ -78,10 +80,21 @@ cudaError_t launch_fwd_state_pass(const Dims &d, const void *dH, const float *ga
                                   cudaStream_t st) {
   const int n8 = (int)(d.S * d.P / 8);
   dim3 grid((unsigned)((n8 + kThreads - 1) / kThreads), (unsigned)(d.b * d.nh));
-  fwd_state_pass_bf16<<<grid, kThreads, 0, st>>>(static_cast<const uint4 *>(dH), gamma, h0,
-                                                 static_cast<uint4 *>(states), final_state,
-                                                 (int)d.P, (int)d.S, (int)d.nc);
-  return cudaGetLastError();
+  // programmatic stream serialisation: this kernel may start while
+  // fwd_chunk_state finishes; it waits on the device before reading dH
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fwd_state_pass_bf16, static_cast<const uint4 *>(dH), gamma,
+                            h0, static_cast<uint4 *>(states), final_state, (int)d.P,
+                            (int)d.S, (int)d.nc);
 }
 
 }  // namespace ssd

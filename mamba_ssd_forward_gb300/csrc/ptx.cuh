@@ -76,6 +76,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
   return false;
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Wait until every grid this one depends on (the preceding kernel on the
+// stream, when this kernel was launched with programmatic stream
+// serialisation) has completed and its memory writes are visible.  A no-op
+// for kernels launched the ordinary way.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel on the stream (if launched with programmatic stream
+// serialisation) to start once every CTA of this grid has signalled or
+// exited; that kernel still waits (griddep_wait) before reading our output.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ fences
 
 // Generic-proxy writes to shared memory become visible to the async proxy
