@@ -25,6 +25,14 @@ cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const v
                             const void *dt, const float *A, const void *states, const float *D,
                             void *y, cudaStream_t st);
 
+// Output pass with C B^T of a whole chunk shared by a slice of heads (P = 64,
+// S in {64, 128}, T in {128, 256}); fwd_scan_chunk_supported says whether
+// the dims qualify.
+bool fwd_scan_chunk_supported(const Dims &d);
+cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
+                                  const void *dt, const float *A, const void *states,
+                                  const float *D, void *y, cudaStream_t st);
+
 // Heads per CTA of the output pass: the largest divisor of nheads/ngroups
 // that is at most 4 and keeps heads * P <= 256 tensor-memory columns.
 inline int fwd_scan_heads(const Dims &d) {

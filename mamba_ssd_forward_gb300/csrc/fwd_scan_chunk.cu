@@ -1,0 +1,562 @@
+// Forward path, output pass (bf16 I/O) with the interaction tile of a whole
+// chunk computed once and shared by a slice of heads.  Same equation as
+// fwd_scan.cu (the page's compute_out, chunked output equation of
+// "Accelerating Mamba-2 with High-Performance Forward Pass Kernels in NVIDIA
+// CUDA Tile", section "Mamba-2 architecture"):
+//
+//   y_i = exp2(G_i) (h_k c_i) + sum_{j<=i in chunk} (c_i . B_j) exp2(G_i - G_j) dt_j x_j
+//         + D x_i
+//
+// The heads of one group share B and C, so C B^T of a chunk is the same for
+// all of them.  One CTA per (slice of hs heads of one group, chunk, batch):
+//   phase 1: Sc = C B^T for the whole chunk into tensor memory (row tile 0:
+//            columns [0, 128); row tile 1: columns [128, 384)), from C and B
+//            resident in shared memory;
+//   per head q of the slice (state and x tiles double-buffered, so the next
+//            head's loads overlap this head):
+//            Y = C h_q^T (both row tiles, columns [384, 512)), Y *= exp2(G_i),
+//            the decayed, masked tile S'_q from Sc written to shared memory
+//            two 64-token blocks at a time, Y += S'_q X_q, and the epilogue
+//            y = Y + D x computed over x in shared memory and written by TMA
+//            stores (the next head's cumsum runs while this head's last MMAs
+//            finish).
+// Warp roles: warp 8 loads (TMA), warp 9 issues the MMAs, warps 0-7 do the
+// cumsums, the rescale, the decay and the epilogue (two warps per 32-lane
+// quadrant, each taking 32 of every 64 columns).
+//
+// Supported: P = 64, S in {64, 128}, T in {128, 256}; other shapes use
+// fwd_scan.cu.  The decay factors are those of fwd_scan.cu: for a 64-token
+// column block ending at r strictly before row i's block,
+// exp2(G_i - G_j) = exp2(G_i - G_r) * exp2(G_r - G_j), both exponents <= 0.
+#include "fwd.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kRowWarps = 8;
+constexpr int kRowThreads = kRowWarps * 32;
+constexpr int kThreads = kRowThreads + 64;
+constexpr int kProducerWarp = kRowWarps, kMmaWarp = kRowWarps + 1;
+constexpr int kP = 64;              // head dimension handled here
+constexpr int kNP = 2;              // stages of the decayed interaction tile S'
+constexpr int kBlk = 64 * 128;      // 64 rows of 128 bytes
+constexpr int kTile = 128 * 128;    // 128 rows of 128 bytes
+constexpr uint32_t kYCol = 384;
+// tensor-memory column of the interaction tile of row tile t
+__device__ __forceinline__ uint32_t sc_col(int t) { return t ? 128u : 0u; }
+
+struct ChunkArgs {
+  const __nv_bfloat16 *x, *dt;
+  const float *A, *D;
+  __nv_bfloat16 *y;
+  int *err;
+  int L, nh, S, hpg, T, nc, hs;
+  // shared-memory layout (byte offsets from the 1024-aligned base)
+  int off_C, off_B, off_hx0, off_hx1, off_sp;
+  int hx_bytes;  // states (S x P) followed by x (T x P), bf16
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
+                    const __grid_constant__ CUtensorMap tm_B,
+                    const __grid_constant__ CUtensorMap tm_x,
+                    const __grid_constant__ CUtensorMap tm_st,
+                    const __grid_constant__ CUtensorMap tm_y, const ChunkArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ __align__(8) uint64_t p1_full[2], sc_done, hx_full[2], hx_empty[2], ych, ysc,
+      pm_full[kNP], pm_empty[kNP], ydone, yfree;
+  __shared__ uint32_t tmem_slot;
+  // per head (double-buffered by head parity): G in log2 units, dt, and the
+  // column factors v_j = exp2(G_r - G_j) dt_j of the factored decay; read
+  // with 16-byte vector loads, so each array is 16-byte aligned
+  __shared__ __align__(16) float Gs[2][256];
+  __shared__ __align__(16) float dts[2][256];
+  __shared__ __align__(16) float vs[2][256];
+  __shared__ float warp_tot[2][8];
+
+  const int L = a.L, nh = a.nh, S = a.S, T = a.T, nc = a.nc, hs = a.hs;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int k = blockIdx.y, b = blockIdx.z;
+  const int hbase = blockIdx.x * hs, g = hbase / a.hpg;
+  const int tok0 = k * T;
+  const int valid = min(T, L - tok0);
+  const int ntile = T / 128;
+  const int nsb = S / 64;
+  const int st_bytes = S * kP * 2;
+  const uint32_t ncols = 512;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&p1_full[i], 1);
+      ptx::mbar_init(&hx_full[i], 1);
+      ptx::mbar_init(&hx_empty[i], 2);  // MMA commit + the y store has read the tile
+    }
+    ptx::mbar_init(&sc_done, 1);
+    ptx::mbar_init(&ych, 1);
+    ptx::mbar_init(&ysc, kRowThreads);
+    for (int i = 0; i < kNP; ++i) {
+      ptx::mbar_init(&pm_full[i], kRowThreads);
+      ptx::mbar_init(&pm_empty[i], 1);
+    }
+    ptx::mbar_init(&ydone, 1);
+    ptx::mbar_init(&yfree, kRowThreads);
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(&tmem_slot, ncols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const bool leader = (tid & 31) == 0;
+  const bool alias_hx1 = a.off_hx1 == a.off_B;  // second head buffer reuses B's space
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (leader) {
+      // phase 1: C (rows of the chunk, per row tile) and B (rows 0..T-1),
+      // one 64-wide block of S at a time
+      for (int sb = 0; sb < nsb; ++sb) {
+        ptx::mbar_arrive_expect_tx(&p1_full[sb], 2 * ntile * kTile);
+        for (int t = 0; t < ntile; ++t) {
+          ptx::tma_load_4d(smem + a.off_C + (t * nsb + sb) * kTile, &tm_C, sb * 64, g,
+                           tok0 + t * 128, b, &p1_full[sb]);
+          ptx::tma_load_4d(smem + a.off_B + (sb * ntile + t) * kTile, &tm_B, sb * 64, g,
+                           tok0 + t * 128, b, &p1_full[sb]);
+        }
+      }
+    }
+    __syncwarp();
+    for (int q = 0; q < hs; ++q) {
+      const int buf = q & 1;
+      ptx::mbar_wait(&hx_empty[buf], ((q >> 1) & 1) ^ 1, a.err, 121);
+      if (q == 1 && alias_hx1) ptx::mbar_wait(&sc_done, 0, a.err, 122);
+      if (leader) {
+        uint8_t *hx = smem + (buf ? a.off_hx1 : a.off_hx0);
+        ptx::mbar_arrive_expect_tx(&hx_full[buf], a.hx_bytes);
+        // x rows of the chunk (64-token blocks, p contiguous)
+        for (int jb = 0; jb < T / 64; ++jb)
+          ptx::tma_load_4d(hx + st_bytes + jb * kBlk, &tm_x, 0, hbase + q, tok0 + jb * 64, b,
+                           &hx_full[buf]);
+        // the start state comes from the preceding kernel (the state pass),
+        // which may still be running when this CTA starts
+        if (q == 0) ptx::griddep_wait();
+        const int row = (b * nh + hbase + q) * nc + k;
+        for (int sb = 0; sb < nsb; ++sb)
+          ptx::tma_load_3d(hx + sb * kBlk, &tm_st, 0, sb * 64, row, &hx_full[buf]);
+      }
+      __syncwarp();
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    // phase 1: Sc = C B^T; row tile t needs columns j < 128 (t + 1)
+    for (int sb = 0; sb < nsb; ++sb) {
+      ptx::mbar_wait(&p1_full[sb], 0, a.err, 123);
+      ptx::tc_fence_after();
+      if (leader) {
+        const uint32_t b0 = ptx::smem_u32(smem + a.off_B + sb * ntile * kTile);
+        for (int t = 0; t < ntile; ++t) {
+          const uint32_t c0 = ptx::smem_u32(smem + a.off_C + (t * nsb + sb) * kTile);
+          const uint32_t idS = ptx::idesc_bf16(128, 128 * (t + 1), false, false);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t cd = ptx::smem_desc(c0 + kk * 32, 16, 1024, ptx::kSw128);
+            const uint64_t bd = ptx::smem_desc(b0 + kk * 32, 16, 1024, ptx::kSw128);
+            ptx::mma_ss<false>(tmem + sc_col(t), cd, bd, idS, (sb | kk) ? 1u : 0u);
+          }
+        }
+      }
+      __syncwarp();
+    }
+    if (leader) ptx::mma_commit(&sc_done);
+    __syncwarp();
+    const uint32_t idY = ptx::idesc_bf16(128, kP, false, true);
+    int cnt = 0;  // S' blocks consumed so far
+    for (int q = 0; q < hs; ++q) {
+      const int buf = q & 1;
+      const uint32_t hx = ptx::smem_u32(smem + (buf ? a.off_hx1 : a.off_hx0));
+      ptx::mbar_wait(&hx_full[buf], (q >> 1) & 1, a.err, 124);
+      if (q > 0) ptx::mbar_wait(&yfree, (q - 1) & 1, a.err, 125);
+      ptx::tc_fence_after();
+      // Y = C h_q^T for each row tile
+      if (leader) {
+        for (int t = 0; t < ntile; ++t)
+          for (int sb = 0; sb < nsb; ++sb) {
+            const uint32_t c0 = ptx::smem_u32(smem + a.off_C + (t * nsb + sb) * kTile);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t cd = ptx::smem_desc(c0 + kk * 32, 16, 1024, ptx::kSw128);
+              const uint64_t hd =
+                  ptx::smem_desc(hx + sb * kBlk + kk * 2048, kBlk, 1024, ptx::kSw128);
+              ptx::mma_ss<false>(tmem + kYCol + t * kP, cd, hd, idY, (sb | kk) ? 1u : 0u);
+            }
+          }
+        ptx::mma_commit(&ych);
+      }
+      __syncwarp();
+      ptx::mbar_wait(&ysc, q & 1, a.err, 126);
+      ptx::tc_fence_after();
+      // Y += S'_q X_q, one 64-token block of each row tile at a time
+      for (int t = 0; t < ntile; ++t)
+        for (int jb = 0; jb < 2 * (t + 1); ++jb, ++cnt) {
+          const int s = cnt % kNP;
+          ptx::mbar_wait(&pm_full[s], (cnt / kNP) & 1, a.err, 127);
+          ptx::tc_fence_after();
+          if (leader) {
+            const uint32_t p0 = ptx::smem_u32(smem + a.off_sp + s * kTile);
+            const uint32_t x0 = hx + st_bytes + jb * kBlk;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t pd = ptx::smem_desc(p0 + kk * 32, 16, 1024, ptx::kSw128);
+              const uint64_t xd = ptx::smem_desc(x0 + kk * 2048, kBlk, 1024, ptx::kSw128);
+              ptx::mma_ss<false>(tmem + kYCol + t * kP, pd, xd, idY, 1u);
+            }
+            ptx::mma_commit(&pm_empty[s]);
+          }
+          __syncwarp();
+        }
+      if (leader) {
+        ptx::mma_commit(&ydone);
+        ptx::mma_commit(&hx_empty[buf]);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ row warps
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, 32-column half
+    const int r = quad * 32 + (tid & 31);         // row within a tile = TMEM lane
+    const int c32 = half * 32;                    // this thread's columns of a 64-block
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+
+    // dt of the next head for token tid (tid < T), as raw bf16 bits until
+    // the cumsum uses it, so no instruction waits on the load before then
+    const unsigned short *dtp = reinterpret_cast<const unsigned short *>(a.dt);
+    const bool tok_ok = tid < valid;
+    const int64_t dt_off = ((int64_t)b * L + tok0 + (tok_ok ? tid : 0)) * nh + hbase;
+    unsigned short draw = tok_ok ? dtp[dt_off] : (unsigned short)0;
+    float Aq = a.A[hbase];
+    // in-chunk cumsum of head q (one token per thread, threads < T) into the
+    // buffers of parity q & 1, and the column factors of the factored decay;
+    // then the dt of head q + 1 is fetched
+    auto cumsum = [&](int q) {
+      const int pb = q & 1;
+      const float d = __uint_as_float((uint32_t)draw << 16);  // bf16 -> fp32, exact
+      float incl = Aq * kLog2e * d;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, incl, off);
+        if ((tid & 31) >= off) incl += o;
+      }
+      if ((tid & 31) == 31 && warp < 8) warp_tot[pb][warp] = incl;
+      ptx::named_bar_sync(1, kRowThreads);
+      float Gj = incl;
+      for (int w2 = 0; w2 < warp && w2 < 8; ++w2) Gj += warp_tot[pb][w2];
+      if (tid < T) {
+        Gs[pb][tid] = Gj;
+        dts[pb][tid] = d;
+      }
+      ptx::named_bar_sync(1, kRowThreads);
+      if (tid < T) vs[pb][tid] = exp2f(Gs[pb][tid | 63] - Gj) * d;
+      ptx::named_bar_sync(1, kRowThreads);
+      if (q + 1 < hs) {
+        draw = tok_ok ? dtp[dt_off + q + 1] : (unsigned short)0;
+        Aq = a.A[hbase + q + 1];
+      }
+    };
+
+    ptx::mbar_wait(&sc_done, 0, a.err, 128);
+    ptx::tc_fence_after();
+    cumsum(0);
+    int cnt = 0;
+    for (int q = 0; q < hs; ++q) {
+      const int pb = q & 1, buf = q & 1;
+      const int h = hbase + q;
+
+      // carried-state term: Y *= exp2(G_i) for both row tiles
+      ptx::mbar_wait(&ych, q & 1, a.err, 129);
+      ptx::tc_fence_after();
+      {
+        uint32_t yr[2][2][16];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t >= ntile) break;
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            ptx::tmem_ld16(tmem + lane_base + kYCol + t * kP + c32 + c * 16, yr[t][c]);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) ptx::reg_fence(yr[t][c]);
+          const float eg = exp2f(Gs[pb][t * 128 + r]);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(yr[t][c][e]) * eg;
+            ptx::tmem_st16(tmem + lane_base + kYCol + t * kP + c32 + c * 16, v);
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&ysc);
+      }
+      // the previous head's y store has had the rescale's time to read its
+      // shared-memory tile: release that head buffer to the producer
+      if (tid == 0 && q > 0) {
+        ptx::bulk_wait_read<0>();
+        ptx::mbar_arrive(&hx_empty[(q - 1) & 1]);
+      }
+
+      // decayed, masked interaction rows, one 64-token block (one S' stage)
+      // per tensor-memory load wait
+      for (int t = 0; t < ntile; ++t) {
+        const int i_rel = t * 128 + r;
+        const int rb = i_rel >> 6;
+        const float Git = Gs[pb][i_rel];
+        for (int jb = 0; jb < 2 * (t + 1); ++jb, ++cnt) {
+          uint32_t sr[2][16];
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            ptx::tmem_ld16(tmem + lane_base + sc_col(t) + jb * 64 + c32 + c * 16, sr[c]);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence(sr[0]);
+          ptx::reg_fence(sr[1]);
+          uint4 pk[4];
+          if (jb < rb) {
+            // whole block before the row's block: factored decay
+            const float ui = exp2f(Git - Gs[pb][jb * 64 + 63]);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const float4 *vp = reinterpret_cast<const float4 *>(&vs[pb][jb * 64 + c32 + c * 16]);
+              float v[16];
+#pragma unroll
+              for (int e4 = 0; e4 < 4; ++e4) {
+                const float4 f = vp[e4];
+                v[4 * e4 + 0] = __uint_as_float(sr[c][4 * e4 + 0]) * (ui * f.x);
+                v[4 * e4 + 1] = __uint_as_float(sr[c][4 * e4 + 1]) * (ui * f.y);
+                v[4 * e4 + 2] = __uint_as_float(sr[c][4 * e4 + 2]) * (ui * f.z);
+                v[4 * e4 + 3] = __uint_as_float(sr[c][4 * e4 + 3]) * (ui * f.w);
+              }
+              pk[2 * c] = pack_op16(v, (__nv_bfloat16 *)nullptr);
+              pk[2 * c + 1] = pack_op16(v + 8, (__nv_bfloat16 *)nullptr);
+            }
+          } else if (jb == rb) {
+            // the row's own block: direct exponent, causal mask (j <= i)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int jc0 = jb * 64 + c32 + c * 16;
+              const float4 *gp = reinterpret_cast<const float4 *>(&Gs[pb][jc0]);
+              const float4 *dp = reinterpret_cast<const float4 *>(&dts[pb][jc0]);
+              float v[16];
+#pragma unroll
+              for (int e4 = 0; e4 < 4; ++e4) {
+                const float4 gj = gp[e4], dj = dp[e4];
+                const float ga[4] = {gj.x, gj.y, gj.z, gj.w};
+                const float da[4] = {dj.x, dj.y, dj.z, dj.w};
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                  const int j = jc0 + 4 * e4 + cc;
+                  v[4 * e4 + cc] = (j <= i_rel && j < valid)
+                                       ? __uint_as_float(sr[c][4 * e4 + cc]) *
+                                             exp2f(Git - ga[cc]) * da[cc]
+                                       : 0.f;
+                }
+              }
+              pk[2 * c] = pack_op16(v, (__nv_bfloat16 *)nullptr);
+              pk[2 * c + 1] = pack_op16(v + 8, (__nv_bfloat16 *)nullptr);
+            }
+          } else {
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) pk[k4] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          const int s = cnt % kNP;
+          ptx::mbar_wait(&pm_empty[s], ((cnt / kNP) & 1) ^ 1, a.err, 130);
+          uint8_t *Pb = smem + a.off_sp + s * kTile;
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4)
+            *reinterpret_cast<uint4 *>(Pb + sw128(r, (half * 4 + k4) * 16)) = pk[k4];
+          ptx::fence_async_smem();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&pm_full[s]);
+        }
+      }
+
+      // the next head's cumsum while this head's last MMAs finish
+      if (q + 1 < hs) cumsum(q + 1);
+
+      // epilogue: y = Y + D x, written over x in the head's shared-memory
+      // tile and stored by TMA
+      ptx::mbar_wait(&ydone, q & 1, a.err, 131);
+      ptx::tc_fence_after();
+      uint8_t *xs = smem + (buf ? a.off_hx1 : a.off_hx0) + st_bytes;
+      {
+        const float Dh = a.D ? a.D[h] : 0.f;
+        uint32_t yr[2][2][16];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (t < ntile)
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              ptx::tmem_ld16(tmem + lane_base + kYCol + t * kP + c32 + c * 16, yr[t][c]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) ptx::reg_fence(yr[t][c]);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&yfree);  // Y may now be overwritten by the next head
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t >= ntile) break;
+          const int i_rel = t * 128 + r;
+          uint8_t *xrow = xs + (i_rel >> 6) * kBlk;
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            uint4 *p4 = reinterpret_cast<uint4 *>(xrow + sw128(i_rel & 63, (half * 4 + k4) * 16));
+            float xv[8];
+            unpack16(*p4, xv, (__nv_bfloat16 *)nullptr);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              xv[e] = fmaf(Dh, xv[e], __uint_as_float(yr[t][k4 >> 1][(k4 & 1) * 8 + e]));
+            *p4 = pack_io16(xv, (__nv_bfloat16 *)nullptr);
+          }
+        }
+      }
+      ptx::fence_async_smem();
+      ptx::named_bar_sync(2, kRowThreads);
+      if (tid == 0) {
+        for (int jb = 0; jb < T / 64; ++jb)
+          ptx::tma_store_4d(&tm_y, xs + jb * kBlk, 0, h, tok0 + jb * 64, b);
+        ptx::bulk_commit();
+      }
+    }
+    if (tid == 0) ptx::bulk_wait<0>();  // every y store complete
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, ncols);
+}
+
+int sm_count_scan() {
+  static int n[256];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 148;
+  if (!n[dev] &&
+      cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    n[dev] = 148;
+  return n[dev];
+}
+
+struct Layout {
+  int off_C, off_B, off_hx[2], off_sp, hx_bytes, total;
+};
+
+Layout chunk_layout(const Dims &d) {
+  Layout l;
+  const int ntile = (int)(d.T / 128), nsb = (int)(d.S / 64);
+  const int cb = ntile * nsb * kTile;  // C, and B, of the chunk
+  l.hx_bytes = (int)(d.S * kP * 2 + d.T * kP * 2);
+  l.off_C = 0;
+  l.off_B = cb;
+  l.off_hx[0] = 2 * cb;
+  l.off_sp = l.off_hx[0] + l.hx_bytes;
+  const int base = l.off_sp + kNP * kTile;
+  if (base + l.hx_bytes <= 200 * 1024) {
+    l.off_hx[1] = base;
+    l.total = base + l.hx_bytes;
+  } else {
+    l.off_hx[1] = l.off_B;  // the second head buffer reuses B once phase 1 is done
+    l.total = base;
+  }
+  return l;
+}
+
+}  // namespace
+
+bool fwd_scan_chunk_supported(const Dims &d) {
+  if (d.P != kP || (d.S != 64 && d.S != 128) || (d.T != 128 && d.T != 256)) return false;
+  const Layout l = chunk_layout(d);
+  if (l.off_hx[1] == l.off_B && l.hx_bytes > l.off_hx[0] - l.off_B) return false;
+  return l.total + 1024 <= 210 * 1024;
+}
+
+// Heads per CTA: a divisor of the heads per group minimising
+// waves * (phase-1 cost + heads), the phase-1 cost counted as one head.
+int fwd_scan_chunk_heads(const Dims &d) {
+  const int64_t sms = sm_count_scan();
+  int best = 1;
+  double best_cost = 1e300;
+  for (int hs = 1; hs <= d.hpg; ++hs) {
+    if (d.hpg % hs) continue;
+    const int64_t ctas = d.b * d.nc * (d.nh / hs);
+    const double cost = (double)((ctas + sms - 1) / sms) * (1.0 + hs);
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = hs;
+    }
+  }
+  return best;
+}
+
+cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
+                                  const void *dt, const float *A, const void *states,
+                                  const float *D, void *y, cudaStream_t st) {
+  if (!fwd_scan_chunk_supported(d)) return cudaErrorInvalidValue;
+  const int hs = fwd_scan_chunk_heads(d);
+  CUtensorMap tC, tB, tx, tS, tY;
+  if (!make_tmap_bl(&tC, C, true, d.b, d.L, d.ng, d.S, 128) ||
+      !make_tmap_bl(&tB, B, true, d.b, d.L, d.ng, d.S, 128) ||
+      !make_tmap_bl(&tx, x, true, d.b, d.L, d.nh, d.P, 64) ||
+      !make_tmap_bl(&tY, y, true, d.b, d.L, d.nh, d.P, 64))
+    return cudaErrorInvalidValue;
+  {
+    const uint64_t dims[3] = {(uint64_t)d.P, (uint64_t)d.S, (uint64_t)(d.b * d.nh * d.nc)};
+    const uint64_t strides[2] = {(uint64_t)d.P * 2, (uint64_t)(d.S * d.P * 2)};
+    const uint32_t box[3] = {64u, 64u, 1u};
+    if (!make_tmap_sw128(&tS, states, true, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  const Layout l = chunk_layout(d);
+  const int smem = l.total + 1024;
+  cudaError_t e = cudaFuncSetAttribute(fwd_scan_chunk_bf16,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  ChunkArgs a;
+  a.x = static_cast<const __nv_bfloat16 *>(x);
+  a.dt = static_cast<const __nv_bfloat16 *>(dt);
+  a.A = A;
+  a.D = D;
+  a.y = static_cast<__nv_bfloat16 *>(y);
+  a.err = device_error_word();
+  a.L = (int)d.L;
+  a.nh = (int)d.nh;
+  a.S = (int)d.S;
+  a.hpg = (int)d.hpg;
+  a.T = (int)d.T;
+  a.nc = (int)d.nc;
+  a.hs = hs;
+  a.off_C = l.off_C;
+  a.off_B = l.off_B;
+  a.off_hx0 = l.off_hx[0];
+  a.off_hx1 = l.off_hx[1];
+  a.off_sp = l.off_sp;
+  a.hx_bytes = l.hx_bytes;
+  dim3 grid((unsigned)(d.nh / hs), (unsigned)d.nc, (unsigned)d.b);
+  if (d.nc > 65535) return cudaErrorInvalidValue;
+  // programmatic stream serialisation, as for fwd_scan: the producer waits
+  // on the device before loading the first start state
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fwd_scan_chunk_bf16, tC, tB, tx, tS, tY, a);
+}
+
+}  // namespace ssd

@@ -228,7 +228,10 @@ ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype, const voi
     if (e == cudaSuccess && ++launched) e = mark(launched);
     if (e == cudaSuccess) e = ssd::launch_fwd_state_pass(d, dH, gam, h0, sts, final_state, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
-    if (e == cudaSuccess) e = ssd::launch_fwd_scan(d, x, B, C, dt, A, sts, D, y, st);
+    if (e == cudaSuccess)
+      e = ssd::fwd_scan_chunk_supported(d)
+              ? ssd::launch_fwd_scan_chunk(d, x, B, C, dt, A, sts, D, y, st)
+              : ssd::launch_fwd_scan(d, x, B, C, dt, A, sts, D, y, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
   } else {
     float *G = reinterpret_cast<float *>(ws + w.G);
