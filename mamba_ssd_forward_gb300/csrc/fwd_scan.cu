@@ -254,7 +254,7 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
         dts[q][tid] = dh[q];
       }
       ptx::named_bar_sync(1, kRowThreads);
-      if (tid < T) vs[q][tid] = exp2f(Gs[q][tid | 63] - Gj) * dh[q];
+      if (tid < T) vs[q][tid] = ptx::ex2_approx(Gs[q][tid | 63] - Gj) * dh[q];
     }
     ptx::named_bar_sync(1, kRowThreads);
     ptx::mbar_wait(&s1_done, 0, a.err, 88);
@@ -307,7 +307,7 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
     for (int q = 0; q < H; ++q) {
       const float Gi = Gs[q][min(i_rel, T - 1)];
       // carried-state term: Y_q *= exp2(G_i), then release Y_q to phase 2
-      const float eg = exp2f(Gi);
+      const float eg = ptx::ex2_approx(Gi);
 #pragma unroll
       for (int gi = 0; gi < 2; ++gi) {
         const int c0 = (qtr + 4 * gi) * 16;
@@ -332,7 +332,7 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
         ptx::tmem_ld16_sync(tmem + lane_base + jc0, v);  // every lane of the warp
         if (jb < rb) {
           // whole block before the row's block: factored decay
-          const float ui = exp2f(Gi - Gs[q][jb * 64 + 63]);
+          const float ui = ptx::ex2_approx(Gi - Gs[q][jb * 64 + 63]);
           const float4 *vp = reinterpret_cast<const float4 *>(&vs[q][jc0]);
 #pragma unroll
           for (int e4 = 0; e4 < 4; ++e4) {
@@ -353,7 +353,7 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
             for (int c = 0; c < 4; ++c) {
               const int j = jc0 + 4 * e4 + c;
               v[4 * e4 + c] =
-                  (j <= i_rel && j < valid) ? v[4 * e4 + c] * exp2f(Gi - ga[c]) * da[c] : 0.f;
+                  (j <= i_rel && j < valid) ? v[4 * e4 + c] * ptx::ex2_approx(Gi - ga[c]) * da[c] : 0.f;
             }
           }
         } else {

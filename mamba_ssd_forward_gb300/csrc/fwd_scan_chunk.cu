@@ -259,7 +259,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
         dts[pb][tid] = d;
       }
       ptx::named_bar_sync(1, kRowThreads);
-      if (tid < T) vs[pb][tid] = exp2f(Gs[pb][tid | 63] - Gj) * d;
+      if (tid < T) vs[pb][tid] = ptx::ex2_approx(Gs[pb][tid | 63] - Gj) * d;
       ptx::named_bar_sync(1, kRowThreads);
       if (q + 1 < hs) {
         draw = tok_ok ? dtp[dt_off + q + 1] : (unsigned short)0;
@@ -289,7 +289,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 2; ++c) ptx::reg_fence(yr[t][c]);
-          const float eg = exp2f(Gs[pb][t * 128 + r]);
+          const float eg = ptx::ex2_approx(Gs[pb][t * 128 + r]);
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             float v[16];
@@ -326,7 +326,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
           uint4 pk[4];
           if (jb < rb) {
             // whole block before the row's block: factored decay
-            const float ui = exp2f(Git - Gs[pb][jb * 64 + 63]);
+            const float ui = ptx::ex2_approx(Git - Gs[pb][jb * 64 + 63]);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
               const float4 *vp = reinterpret_cast<const float4 *>(&vs[pb][jb * 64 + c32 + c * 16]);
@@ -360,7 +360,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
                   const int j = jc0 + 4 * e4 + cc;
                   v[4 * e4 + cc] = (j <= i_rel && j < valid)
                                        ? __uint_as_float(sr[c][4 * e4 + cc]) *
-                                             exp2f(Git - ga[cc]) * da[cc]
+                                             ptx::ex2_approx(Git - ga[cc]) * da[cc]
                                        : 0.f;
                 }
               }
