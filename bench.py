@@ -44,7 +44,7 @@ KERNEL_NAMES = {"bf16": ["fwd_chunk_state", "fwd_state_pass", "fwd_scan"],
 KERNEL_SOURCES = {"chunk_cumsum": "chunk_cumsum.cu", "chunk_state": "chunk_state.cu",
                   "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan.cu",
                   "fwd_chunk_state": "fwd_chunk_state.cu", "fwd_state_pass": "fwd_state_pass.cu",
-                  "fwd_scan": "fwd_scan.cu"}
+                  "fwd_scan": "fwd_scan.cu", "fwd_scan_chunk": "fwd_scan_chunk.cu"}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -86,6 +86,17 @@ def algorithmic_flops(w: W.Workload) -> float:
     return per * w.batch * w.seqlen * w.nheads
 
 
+def kernel_names(w: W.Workload) -> list:
+    """Labels of the kernels ssd_forward launches for this workload, in
+    launch order.  The bf16 output pass is fwd_scan_chunk for P = 64,
+    S in {64, 128}, T in {128, 256} (the library's own dispatch rule), else
+    fwd_scan."""
+    names = list(KERNEL_NAMES[w.dtype])
+    if w.dtype == "bf16" and w.headdim == 64 and w.dstate in (64, 128) and w.chunk in (128, 256):
+        names[2] = "fwd_scan_chunk"
+    return names
+
+
 def kernel_bytes(w: W.Workload) -> dict:
     """Algorithmic bytes of one launch of each kernel: its own inputs read
     once and outputs written once."""
@@ -104,6 +115,7 @@ def kernel_bytes(w: W.Workload) -> dict:
         "fwd_chunk_state": x + bc + dt + w.nheads * 4 + st16 + gam,
         "fwd_state_pass": 2 * st16 + gam + h0 + fin,
         "fwd_scan": 2 * x + 2 * bc + dt + 2 * w.nheads * 4 + st16,
+        "fwd_scan_chunk": 2 * x + 2 * bc + dt + 2 * w.nheads * 4 + st16,
         "chunk_cumsum": dt + G + w.nheads * 4,
         "chunk_state": x + bc + dt + G + st,
         "state_passing": 2 * st + w.batch * w.nheads * w.nchunks * 4 + fin * (2 if w.has_h0 else 1),
@@ -347,7 +359,7 @@ def run_ours(args, w):
     clocks = sampler.stop() if sampler else None
 
     step_ms = [ev[i][0].elapsed_time(ev[i][n_l]) for i in range(args.steps)]
-    names = KERNEL_NAMES[w.dtype]
+    names = kernel_names(w)
     kern_ms = {names[j]: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1])
                                                 for i in range(args.steps))
                for j in range(n_l)}
