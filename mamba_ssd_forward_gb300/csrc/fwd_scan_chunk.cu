@@ -252,14 +252,20 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       }
       if ((tid & 31) == 31 && warp < 8) warp_tot[pb][warp] = incl;
       ptx::named_bar_sync(1, kRowThreads);
-      float Gj = incl;
-      for (int w2 = 0; w2 < warp && w2 < 8; ++w2) Gj += warp_tot[pb][w2];
+      // G at this token, and at the last token of its 64-token block (the
+      // end of warp (warp | 1)), both from the warp totals
+      float Gj = incl, Gr = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < 8; ++w2) {
+        const float tw = warp_tot[pb][w2];
+        if (w2 < warp) Gj += tw;
+        if (w2 <= (warp | 1)) Gr += tw;
+      }
       if (tid < T) {
         Gs[pb][tid] = Gj;
         dts[pb][tid] = d;
+        vs[pb][tid] = ptx::ex2_approx(Gr - Gj) * d;
       }
-      ptx::named_bar_sync(1, kRowThreads);
-      if (tid < T) vs[pb][tid] = ptx::ex2_approx(Gs[pb][tid | 63] - Gj) * d;
       ptx::named_bar_sync(1, kRowThreads);
       if (q + 1 < hs) {
         draw = tok_ok ? dtp[dt_off + q + 1] : (unsigned short)0;

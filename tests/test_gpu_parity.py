@@ -50,6 +50,12 @@ SMALL_CASES = [
     small("bf16_hpg6_three_heads_per_cta", 600, 12, 64, 128, 2, 256, "bf16", batch=2),
     small("bf16_S256_groups", 520, 12, 64, 256, 2, 256, "bf16"),
     small("bf16_P96_S48", 300, 4, 96, 48, 1, 128, "bf16"),
+    # output pass with C B^T shared by a slice of heads: two groups, and 20
+    # chunks x 24 heads, where four heads share one CTA (alternating state
+    # and x buffers, the second reusing B's shared memory)
+    small("bf16_chunk_two_groups", 700, 6, 64, 128, 2, 256, "bf16", batch=2),
+    small("bf16_chunk_T128_S64", 500, 4, 64, 64, 1, 128, "bf16"),
+    small("bf16_chunk_four_heads_per_cta", 5120, 24, 64, 128, 1, 256, "bf16"),
 ]
 
 
