@@ -10,8 +10,9 @@
 // independent, so this runs fully in parallel; the sequential part is the
 // bandwidth kernel in fwd_state_pass.cu.
 //
-// Persistent: one CTA per SM walks a strided list of work items, an item
-// being (chunk, 128-wide slice of S, group of H heads that share B, batch).
+// Persistent: one or two CTAs per SM (chunk_state_plan) walk a strided list
+// of work items, an item being (chunk, 128-wide slice of S, group of H heads
+// that share B, batch).
 // The shared-memory ring of 64-token blocks runs across item boundaries, and
 // the tensor-memory accumulators are double-buffered by item, so the loads
 // of item j+1 stream in while item j is reduced and item j-1 is written out.
@@ -39,7 +40,6 @@ constexpr int kThreads = kRowThreads + 64;
 constexpr int kProducerWarp = kRowWarps, kMmaWarp = kRowWarps + 1;
 constexpr int kKB = 64;     // tokens per pipeline stage
 constexpr int kMaxNST = 4;  // pipeline stages (at most)
-constexpr int kMaxH = 4;
 constexpr int kBlk = kKB * 128;   // 64 rows of 128 bytes
 constexpr int kOutBlk = 128 * 128;  // one staged dH tile: 128 s rows x 64 p
 
@@ -48,7 +48,7 @@ struct CsArgs {
   const float *A;
   float *gamma;
   int *err;
-  int L, nh, P, S, hpg, T, nc, H, n_st, n_hg, nst, n_items;
+  int L, nh, P, S, hpg, T, nc, H, n_st, n_hg, nst, n_items, nout;
 };
 
 // Work item -> (batch, chunk, S slice, first head).  The head groups of one
@@ -68,10 +68,14 @@ __device__ __forceinline__ Item decode(int item, const CsArgs &a) {
   return it;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// kCtas CTAs per SM: 1 (items of up to 4 heads, H P <= 256) or 2 (up to 2
+// heads, H P <= 128, so that two CTAs share the tensor memory).
+template <int kCtas>
+__global__ void __launch_bounds__(kThreads, kCtas)
 fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
                      const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_dH, const CsArgs a) {
+  constexpr int kMaxH = kCtas == 1 ? 4 : 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t full[kMaxNST], scaled[kMaxNST], empty[kMaxNST], acc_full[2],
@@ -85,7 +89,7 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
   const int nPb = (P + 63) / 64;
   const int xbytes = nPb * kBlk;                  // one head's x block
   const int stage_bytes = 2 * kBlk + H * xbytes;  // B block | x blocks
-  uint8_t *ostage = smem + nst * stage_bytes;     // two staged dH tiles
+  uint8_t *ostage = smem + nst * stage_bytes;     // a.nout staged dH tiles
   const int obytes = nPb * kOutBlk;
   const int HP = H * P;
   const uint32_t ncols = 2 * HP <= 32    ? 32
@@ -221,9 +225,14 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
       ptx::mbar_wait(&acc_full[set], (jl >> 1) & 1, a.err, 104);
       ptx::tc_fence_after();
       for (int q = 0; q < H; ++q, ++n_out) {
-        uint8_t *stg = ostage + (n_out & 1) * obytes;
-        // the store issued two tiles ago has finished reading this buffer
-        if (tid == 0 && n_out >= 2) ptx::bulk_wait_read<1>();
+        uint8_t *stg = ostage + (n_out % a.nout) * obytes;
+        // the store that last used this buffer has finished reading it
+        if (tid == 0 && n_out >= a.nout) {
+          if (a.nout == 2)
+            ptx::bulk_wait_read<1>();
+          else
+            ptx::bulk_wait_read<0>();
+        }
         ptx::named_bar_sync(2, kRowThreads);
         for (int g0 = half; g0 < ngrp; g0 += 4) {
           // up to two 16-column groups per pass: g0 and g0 + 2
@@ -354,36 +363,55 @@ int sm_count() {
   return n[dev];
 }
 
+
+struct CsPlan {
+  int H, ctas;  // heads per item, CTAs per SM
+};
+
+// Heads per item and CTAs per SM.  For each mode (one CTA per SM with
+// H * P <= 256 and up to 4 heads, or two with H * P <= 128 and up to 2, the
+// two accumulator sets of every resident CTA fitting the 512 tensor-memory
+// columns) H is the divisor of the heads per group minimising the bytes the
+// busiest CTA loads (items per CTA, rounded up, times B's slice plus H heads
+// of x per item).  Two CTAs per SM overlap one CTA's cumsum and epilogue with
+// the other's loads and MMAs, which pays once each CTA has several items (3
+// or more); with fewer, one CTA with larger items starts and drains faster.
+CsPlan chunk_state_plan(const Dims &d) {
+  const int64_t n_st = (d.S + 127) / 128;
+  const int64_t sms = sm_count();
+  const int nPb = (int)((d.P + 63) / 64);
+  auto best_h = [&](int ctas, int hmax, int64_t cols, int64_t *items_out) {
+    int best = 1;
+    double best_cost = 1e300;
+    for (int h = 1; h <= hmax; ++h) {
+      if (d.hpg % h || h * d.P > cols || h * nPb > 4) continue;
+      const int64_t items = d.b * d.nc * n_st * (d.nh / h);
+      const double per_item = 2.0 * kBlk + h * nPb * (double)kBlk;
+      const double cost = (double)((items + ctas * sms - 1) / (ctas * sms)) * per_item;
+      if (cost < best_cost * 0.999) {
+        best_cost = cost;
+        best = h;
+      }
+    }
+    *items_out = d.b * d.nc * n_st * (d.nh / best);
+    return best;
+  };
+  int64_t items2 = 0, items1 = 0;
+  const int h2 = best_h(2, 2, 128, &items2);
+  if (items2 >= 3 * 2 * sms) return CsPlan{h2, 2};
+  const int h1 = best_h(1, 4, 256, &items1);
+  return CsPlan{h1, 1};
+}
+
 }  // namespace
 
-// Heads per item: a divisor of the heads per group with H * P <= 256 (two
-// accumulator sets fit the 512 tensor-memory columns) and at most four
-// 64-column x blocks per stage, chosen to minimise
-// the bytes the busiest CTA loads (items per CTA, rounded up, times B's
-// slice plus H heads of x per item).
-int fwd_state_heads(const Dims &d) {
-  const int hmax = (int)std::min<int64_t>(kMaxH, 256 / d.P);
-  const int64_t n_st = (d.S + 127) / 128;
-  const int64_t ctas = sm_count();
-  int best = 1;
-  double best_cost = 1e300;
-  for (int h = 1; h <= hmax; ++h) {
-    if (d.hpg % h || h * ((d.P + 63) / 64) > 4) continue;  // <= 4 x blocks per stage
-    const int64_t items = d.b * d.nc * n_st * (d.nh / h);
-    const double per_item = 2.0 * kBlk + h * ((d.P + 63) / 64) * (double)kBlk;
-    const double cost = (double)((items + ctas - 1) / ctas) * per_item;
-    if (cost < best_cost * 0.999) {
-      best_cost = cost;
-      best = h;
-    }
-  }
-  return best;
-}
+int fwd_state_heads(const Dims &d) { return chunk_state_plan(d).H; }
 
 cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, const void *dt,
                                    const float *A, void *dH, float *gamma, cudaStream_t st) {
   if (d.T > kRowThreads) return cudaErrorInvalidValue;  // one token per row thread
-  const int H = fwd_state_heads(d);
+  const CsPlan plan = chunk_state_plan(d);
+  const int H = plan.H;
   CUtensorMap tB, tx, tD;
   if (!make_tmap_bl(&tB, B, true, d.b, d.L, d.ng, d.S, kKB) ||
       !make_tmap_bl(&tx, x, true, d.b, d.L, d.nh, d.P, kKB))
@@ -397,11 +425,18 @@ cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, 
   }
   const int nPb = (int)((d.P + 63) / 64);
   const int stage_bytes = 2 * kBlk + H * nPb * kBlk;
-  const int obytes = 2 * nPb * kOutBlk;
-  const int nst = std::max(2, std::min(kMaxNST, (208 * 1024 - obytes) / stage_bytes));
-  const int smem = nst * stage_bytes + obytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(fwd_chunk_state_bf16,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // dynamic shared memory (1 KB of it alignment slack) within 208 KB for
+  // one CTA per SM, 104 KB each for two; two staged dH tiles when they fit,
+  // else one
+  const int budget = (plan.ctas == 1 ? 207 : 103) * 1024;
+  const int out1 = nPb * kOutBlk;
+  const int nout = (2 * stage_bytes + 2 * out1 <= budget) ? 2 : 1;
+  const int nst = std::min(kMaxNST, (budget - nout * out1) / stage_bytes);
+  if (nst < 2) return cudaErrorInvalidValue;
+  const int smem = nst * stage_bytes + nout * out1 + 1024;
+  auto kernel = plan.ctas == 1 ? fwd_chunk_state_bf16<1> : fwd_chunk_state_bf16<2>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   CsArgs a;
   a.dt = static_cast<const __nv_bfloat16 *>(dt);
@@ -419,11 +454,12 @@ cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, 
   a.n_st = (int)((d.S + 127) / 128);
   a.n_hg = (int)(d.nh / H);
   a.nst = nst;
+  a.nout = nout;
   const int64_t n_items = d.b * d.nc * a.n_st * a.n_hg;
   if (n_items > 0x7fffffffLL || d.b * d.nh * d.nc > 0x7fffffffLL) return cudaErrorInvalidValue;
   a.n_items = (int)n_items;
-  const int grid = (int)std::min<int64_t>(n_items, sm_count());
-  fwd_chunk_state_bf16<<<grid, kThreads, smem, st>>>(tB, tx, tD, a);
+  const int grid = (int)std::min<int64_t>(n_items, plan.ctas * (int64_t)sm_count());
+  kernel<<<grid, kThreads, smem, st>>>(tB, tx, tD, a);
   return cudaGetLastError();
 }
 
