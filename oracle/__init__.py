@@ -15,14 +15,19 @@ CUDA Tile", section "Mamba-2 architecture":
 * ``chunked`` -- the chunked log-space formulas of the same section (the
   decayed state jump and the chunked output equation), in numpy, used only
   to cross-check the recurrence and to pin the chunking semantics.
+* ``decode_step`` -- one token of the recurrence for a batch of states, in
+  numpy: the reference for the single-token decode step.
 
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests
 (hand-worked example, brute-force unrolled sum, linear-attention, B = 0 and
-dt = 0 special cases, chunk invariance, padding, resume, linearity in h0).
+dt = 0 special cases, chunk invariance, padding, resume, linearity in h0;
+for decode_step: the hand-worked example token by token, agreement with the
+C recurrence over whole sequences, dt = 0, and planted mistakes).
 """
 from .ssd_oracle import (  # noqa: F401
     build,
     chunked,
+    decode_step,
     max_threads,
     recurrence,
     recurrence_np,

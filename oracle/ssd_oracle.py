@@ -132,6 +132,31 @@ def recurrence_np(x, dt, A, B, C, D=None, h0=None):
     return y, final
 
 
+def decode_step(x, dt, A, B, C, D=None, h=None):
+    """One token of the recurrence ("Mamba-2 architecture": the state update
+    h_t = exp(A dt_t) h_{t-1} + (dt_t x_t) outer B_t, output taken from the
+    updated state, y_t = h_t . c_t + D x_t), float64, for a batch of
+    (batch, head) states at once.
+
+    Shapes: x [b,nh,P], dt [b,nh], A [nh], B, C [b,ng,S], D [nh] or None,
+    h [b,nh,P,S] or None (zero).  Head hd reads group hd // (nh // ng).
+    Returns (y [b,nh,P], h_new [b,nh,P,S])."""
+    x, dt, A, B, C, D, h = map(_f64, (x, dt, A, B, C, D, h))
+    b, nh, P = x.shape
+    ng, S = B.shape[1], B.shape[2]
+    if nh % ng:
+        raise ValueError("nheads must be a multiple of ngroups")
+    grp = np.arange(nh) // (nh // ng)
+    Bh, Ch = B[:, grp], C[:, grp]                       # [b, nh, S]
+    decay = np.exp(A[None, :] * dt)                     # [b, nh]
+    h_prev = np.zeros((b, nh, P, S)) if h is None else h
+    h_new = decay[:, :, None, None] * h_prev + (dt[:, :, None] * x)[:, :, :, None] * Bh[:, :, None, :]
+    y = np.einsum("bhps,bhs->bhp", h_new, Ch)
+    if D is not None:
+        y = y + D[None, :, None] * x
+    return y, h_new
+
+
 def chunked(x, dt, A, B, C, D=None, h0=None, chunk=256):
     """The chunked log-space formulas, float64, per (batch, head, chunk):
 
