@@ -463,6 +463,62 @@ def e2e(args, w, inp, dev):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
 
+def run_decode(args, w):
+    """The single-token decode step (ssd_decode_step) on the workload's layer
+    shape with --decode-batch sequences: one token for every (batch, head)
+    state per step, the state resident in HBM and L2 flushed between steps.
+    Prints its own JSON line (mode "decode"); not the headline metric."""
+    import torch
+
+    import mamba_ssd_forward_gb300 as ssd
+    from mamba_ssd_forward_gb300 import build
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    b = args.decode_batch or w.batch
+    dw = W.Workload(w.name + "_decode", b, 1, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk,
+                    w.dtype, True)
+    inp = host_inputs(dw)
+    d = {k: (None if v is None else v.to(dev).contiguous()) for k, v in inp.items()}
+    x, dt, Bm, Cm = (d[k][:, 0].clone() for k in ("x", "dt", "B", "C"))
+    state = d["h0"].clone()
+    y = torch.empty_like(x)
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        flush_w.zero_()
+        ssd.decode_step(x, dt, d["A"], Bm, Cm, d["D"], state, y)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for e0, e1 in ev:
+        flush_w.zero_()
+        e0.record()
+        ssd.decode_step(x, dt, d["A"], Bm, Cm, d["D"], state, y)
+        e1.record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    e = io_bytes(dw)
+    st_bytes = 2 * b * w.nheads * w.headdim * w.dstate * 4
+    io = b * w.nheads * (2 * w.headdim + 1) * e + 2 * b * w.ngroups * w.dstate * e
+    peak, peak_src = hbm_peak()
+    gbs = (st_bytes + io) / (ms / 1e3) / 1e9
+    line = {
+        "metric": "SSD decode step tokens/s (one token for each of batch sequences)",
+        "mode": "decode", "value": b / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": dw.name, "batch": b, "nheads": w.nheads, "headdim": w.headdim,
+                   "dstate": w.dstate, "ngroups": w.ngroups,
+                   "l2": "flushed before every step (256 MB write), outside the events"},
+        "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": gbs, "peak": peak,
+                     "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": st_bytes + io, "traffic": None},
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -478,12 +534,18 @@ def main(argv=None):
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--flush", choices=["write+read", "write"], default="write+read",
                     help="L2 flush between steps (default: write a buffer, then read another)")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the single-token decode step instead of the forward pass")
+    ap.add_argument("--decode-batch", type=int, default=0,
+                    help="sequences per decode step (default: the workload's batch)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     w = workload_by_name(args.workload)
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.decode:
+        return run_decode(args, w)
     return run_ours(args, w)
 
 

@@ -178,6 +178,26 @@ SSD_API ssd_status ssd_forward_host(const ssd_dims *dims, ssd_dtype dtype, const
                                     void *y, float *final_state, void *workspace,
                                     size_t ws_bytes, void *stream);
 
+/* One token of the recurrence for every (batch, head) state -- the
+ * recurrent form of the page's section "Mamba-2 architecture", the
+ * single-token step of sequential inference:
+ *   h[b,h]     = exp(A[h] dt[b,h]) h[b,h] + (dt[b,h] x[b,h,:]) (outer) B[b,g,:]
+ *   y[b,h,p]   = sum_s h[b,h,p,s] C[b,g,s] + D[h] x[b,h,p]
+ * with g = h / (nh / ng) and the output taken from the updated state.
+ * dims: batch, nheads, headdim, dstate, ngroups as for ssd_forward; seqlen
+ * must be 1; chunk is ignored.
+ * Layouts: x, y [b, nh, P] io; dt [b, nh] io; B, C [b, ng, S] io;
+ *   A, D [nh] f32; state [b, nh, P, S] f32, read and overwritten in place.
+ *   state has the layout of h0 / final_state of ssd_forward, so decoding can
+ *   continue from a forward pass's final state.  D may be NULL (D = 0).
+ * Supported: any P >= 1; S a multiple of 4, at most 1024; else
+ * SSD_ERR_UNSUPPORTED.  Pointers 16-byte aligned (SSD_ERR_INVALID_ARG
+ * otherwise).  Enqueued on `stream`; nothing is allocated. */
+SSD_API ssd_status ssd_decode_step(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                                   const void *dt, const float *A, const void *B,
+                                   const void *C, const float *D, float *state, void *y,
+                                   void *stream);
+
 /* Size in bytes of the fixed device scratch array ssd_forward_noalloc uses as
  * its workspace (32 MiB, reserved per device once the library's module is
  * loaded there). */

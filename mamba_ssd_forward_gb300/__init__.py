@@ -19,7 +19,7 @@ from . import _abi
 from ._abi import SSD_BF16, SSD_F32, SsdError  # noqa: F401
 
 __all__ = ["forward", "chunk_cumsum", "chunk_state", "state_passing", "chunk_scan",
-           "workspace_size", "dims_of", "SsdError"]
+           "decode_step", "workspace_size", "dims_of", "SsdError"]
 
 
 def _io_code(t: torch.Tensor) -> int:
@@ -140,6 +140,22 @@ def chunk_scan(x, B, C, dt, G, states, D=None, chunk: int = 256):
         ctypes.byref(d), _io_code(x), _ptr(x), _ptr(B), _ptr(C), _ptr(dt),
         _ptr(_f32(G, "G")), _ptr(_f32(states, "states")), _ptr(_f32(D, "D")), _ptr(y),
         _stream()))
+    return y
+
+
+def decode_step(x, dt, A, B, C, D, state, y=None):
+    """y [b, nh, P] (I/O dtype) = ssd_decode_step: one token for every
+    (batch, head) state.  x [b, nh, P], dt [b, nh], B/C [b, ng, S] in the I/O
+    dtype; state [b, nh, P, S] float32 is updated in place."""
+    lib = _abi.load()
+    b, nh, P = x.shape
+    ng, S = B.shape[1], B.shape[2]
+    d = _abi.SsdDims(b, 1, nh, P, S, ng, 256)
+    if y is None:
+        y = torch.empty_like(x)
+    _abi.check("ssd_decode_step", lib.ssd_decode_step(
+        ctypes.byref(d), _io_code(x), _ptr(x), _ptr(dt), _ptr(_f32(A, "A")), _ptr(B), _ptr(C),
+        _ptr(_f32(D, "D")), _ptr(_f32(state, "state")), _ptr(y), _stream()))
     return y
 
 

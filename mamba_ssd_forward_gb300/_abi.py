@@ -31,6 +31,7 @@ EXPORTS = (
     "ssd_forward_host_workspace_size",
     "ssd_forward_host",
     "ssd_forward_noalloc",
+    "ssd_decode_step",
 )
 
 
@@ -83,6 +84,8 @@ def load(path: str | None = None):
     lib.ssd_forward_host_workspace_size.argtypes = [dims_p, i32, i32, i32, i32]
     lib.ssd_forward_host.restype = i32
     lib.ssd_forward_host.argtypes = [dims_p, i32] + [vp] * 10 + [sz, vp]
+    lib.ssd_decode_step.restype = i32
+    lib.ssd_decode_step.argtypes = [dims_p, i32] + [vp] * 9
     lib.ssd_forward_noalloc.restype = i32
     lib.ssd_forward_noalloc.argtypes = [dims_p, i32] + [vp] * 9 + [vp]
     if path is None:

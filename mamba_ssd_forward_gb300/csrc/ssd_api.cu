@@ -188,6 +188,26 @@ ssd_status ssd_chunk_scan(const ssd_dims *dims, ssd_dtype dtype, const void *x, 
                                           (cudaStream_t)stream));
 }
 
+ssd_status ssd_decode_step(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
+                           const float *A, const void *B, const void *C, const float *D,
+                           float *state, void *y, void *stream) {
+  if (!dims) return SSD_ERR_INVALID_ARG;
+  const ssd_dims d = *dims;
+  if (d.batch < 1 || d.nheads < 1 || d.headdim < 1 || d.dstate < 1 || d.ngroups < 1 ||
+      d.seqlen != 1 || d.nheads % d.ngroups != 0)
+    return SSD_ERR_INVALID_ARG;
+  if (d.dstate % 4 || d.dstate > 1024 || d.headdim > (1 << 20) ||
+      (double)d.batch * d.nheads > 2147483647.0 ||
+      (double)d.batch * d.nheads * d.headdim * d.dstate > 4.0e18)
+    return SSD_ERR_UNSUPPORTED;
+  if (!valid_dtype(dtype) || !req(x) || !req(dt) || !req(A) || !req(B) || !req(C) || !opt(D) ||
+      !req(state) || !req(y))
+    return SSD_ERR_INVALID_ARG;
+  return from_cuda(ssd::launch_decode_step(d.batch, d.nheads, d.headdim, d.dstate, d.ngroups,
+                                           dtype, x, dt, A, B, C, D, state, y,
+                                           (cudaStream_t)stream));
+}
+
 ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
                        const float *A, const void *B, const void *C, const float *D,
                        const float *h0, void *y, float *final_state, void *workspace,

@@ -50,4 +50,10 @@ cudaError_t launch_chunk_scan(const Dims &d, ssd_dtype io, const void *x,
                               const float *G, const float *states,
                               const float *D, void *y, cudaStream_t st);
 
+// Single-token decode step (decode_step.cu).
+cudaError_t launch_decode_step(int64_t b, int64_t nh, int64_t P, int64_t S, int64_t ng,
+                               ssd_dtype io, const void *x, const void *dt, const float *A,
+                               const void *B, const void *C, const float *D, float *state,
+                               void *y, cudaStream_t st);
+
 }  // namespace ssd

@@ -158,3 +158,22 @@ def test_noalloc_limit_and_rejections(lib):
     assert lib.ssd_forward_noalloc(ctypes.byref(dims(chunk=96)), 1, *args) == 2
     assert lib.ssd_forward_noalloc(ctypes.byref(dims()), 7, *args) == 1
     assert lib.ssd_forward_noalloc(None, 1, *args) == 1
+
+
+def test_decode_step_rejections(lib):
+    """ssd_decode_step validates before launching: seqlen must be 1, S a
+    multiple of 4 up to 1024, nh a multiple of ng, pointers aligned."""
+    from mamba_ssd_forward_gb300 import _abi
+    ok = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p((1 << 20) + 4)
+    args = lambda st, y: [ok, ok, ok, ok, ok, None, st, y, None]  # noqa: E731
+    d1 = dims(seqlen=1)
+    assert lib.ssd_decode_step(ctypes.byref(dims(seqlen=2)), 1, *args(ok, ok)) == 1
+    assert lib.ssd_decode_step(ctypes.byref(dims(seqlen=1, dstate=6)), 1, *args(ok, ok)) == 2
+    assert lib.ssd_decode_step(ctypes.byref(dims(seqlen=1, dstate=1028)), 1, *args(ok, ok)) == 2
+    assert lib.ssd_decode_step(ctypes.byref(dims(seqlen=1, ngroups=3)), 1, *args(ok, ok)) == 1
+    assert lib.ssd_decode_step(ctypes.byref(d1), 1, *args(bad, ok)) == 1
+    assert lib.ssd_decode_step(ctypes.byref(d1), 1, *args(ok, None)) == 1
+    assert lib.ssd_decode_step(ctypes.byref(d1), 9, *args(ok, ok)) == 1
+    assert lib.ssd_decode_step(None, 1, *args(ok, ok)) == 1
+    assert _abi.SSD_OK == 0
