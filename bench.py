@@ -421,7 +421,8 @@ def run_ours(args, w):
     }
 
     if not args.skip_e2e:
-        line["e2e"] = e2e(args, w, inp, dev)
+        line["e2e"] = e2e(args, w, inp, dev, overlapped=True)
+        line["e2e_serial"] = e2e(args, w, inp, dev, overlapped=False)
     if not args.skip_cpu_baseline and world == 1:
         v, threads, sample, _ = time_oracle(w, inp, 15.0)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": threads,
@@ -432,35 +433,55 @@ def run_ours(args, w):
     return 0
 
 
-def e2e(args, w, inp, dev):
-    """Same metric through ssd_forward_host: pinned host inputs copied in,
-    forward, y and the final state copied out, every step."""
+def e2e(args, w, inp, dev, overlapped=True):
+    """Same metric through the host-buffer API: pinned host inputs copied in,
+    forward, y and the final state copied out, every step.  overlapped:
+    ssd_forward_host_overlapped (the copies of up to 4 slices overlap the
+    computation on two extra streams); else ssd_forward_host (serial)."""
     import torch
 
     import mamba_ssd_forward_gb300 as ssd
     h = {k: (None if v is None else v.contiguous().pin_memory()) for k, v in inp.items()}
     y = torch.empty_like(h["x"]).pin_memory()
     fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32).pin_memory()
-    ws = torch.empty(ssd.host_workspace_size(h["x"], h["B"], w.chunk, has_D=True,
-                                             has_h0=h["h0"] is not None),
-                     dtype=torch.uint8, device=dev)
+    n_slices = 4
+    if overlapped:
+        ws = torch.empty(ssd.host_overlapped_workspace_size(h["x"], h["B"], w.chunk, n_slices,
+                                                            True, h["h0"] is not None, True),
+                         dtype=torch.uint8, device=dev)
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+        def call():
+            ssd.forward_host_overlapped(h["x"], h["dt"], h["A"], h["B"], h["C"], h["D"], h["h0"],
+                                        w.chunk, ws, y, fin, n_slices=n_slices, h2d_stream=s_in,
+                                        d2h_stream=s_out)
+    else:
+        ws = torch.empty(ssd.host_workspace_size(h["x"], h["B"], w.chunk, has_D=True,
+                                                 has_h0=h["h0"] is not None),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            ssd.forward_host(h["x"], h["dt"], h["A"], h["B"], h["C"], h["D"], h["h0"], w.chunk,
+                             ws, y, fin)
     h2d = sum(v.numel() * v.element_size() for v in h.values() if v is not None)
     d2h = y.numel() * y.element_size() + fin.numel() * fin.element_size()
     for _ in range(max(3, args.warmup)):
-        ssd.forward_host(h["x"], h["dt"], h["A"], h["B"], h["C"], h["D"], h["h0"], w.chunk,
-                         ws, y, fin)
+        call()
     torch.cuda.synchronize()
     n = max(args.steps, 3)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record()
     for _ in range(n):
-        ssd.forward_host(h["x"], h["dt"], h["A"], h["B"], h["C"], h["D"], h["h0"], w.chunk,
-                         ws, y, fin)
+        call()
     e.record()
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / n
-    return {"value": w.batch * w.seqlen / (ms / 1e3), "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+    out = {"value": w.batch * w.seqlen / (ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+           "api": "ssd_forward_host_overlapped" if overlapped else "ssd_forward_host"}
+    if overlapped:
+        out["n_slices"] = n_slices
+    return out
 
 
 def run_decode(args, w):

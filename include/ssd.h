@@ -178,6 +178,36 @@ SSD_API ssd_status ssd_forward_host(const ssd_dims *dims, ssd_dtype dtype, const
                                     void *y, float *final_state, void *workspace,
                                     size_t ws_bytes, void *stream);
 
+/* Device workspace of ssd_forward_host_overlapped for these dims and slice
+ * count (0 if the dims are invalid or unsupported). */
+SSD_API size_t ssd_forward_host_overlapped_workspace_size(const ssd_dims *dims, ssd_dtype dtype,
+                                                          int has_D, int has_h0,
+                                                          int want_final_state, int n_slices);
+
+/* ssd_forward_host with the copies overlapped with the computation.  The
+ * work is cut into up to n_slices slices: along the batch when batch >= 2,
+ * else along the tokens in runs of whole chunks, each slice starting from
+ * the previous slice's final state (the recurrence resumes exactly from a
+ * final state).  Slice i's host->device copies run on h2d_stream, its
+ * forward pass on `stream`, its device->host copies on d2h_stream, so that
+ * slice i+1 uploads while slice i computes and slice i-1 downloads; input
+ * and output buffers in `workspace` are double-buffered.  The ordering
+ * between the three streams uses CUDA events that the call creates and
+ * releases itself; no memory is allocated.  `stream` waits for both copy
+ * streams before the call returns control of it, so work enqueued on
+ * `stream` afterwards sees y and final_state in host memory once it runs.
+ * h2d_stream / d2h_stream may be NULL (that direction then runs on
+ * `stream`).  Other arguments as for ssd_forward_host; workspace >=
+ * ssd_forward_host_overlapped_workspace_size bytes, 256-byte aligned.  The
+ * host buffers should be page-locked for the copies to overlap. */
+SSD_API ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype,
+                                               const void *x, const void *dt, const float *A,
+                                               const void *B, const void *C, const float *D,
+                                               const float *h0, void *y, float *final_state,
+                                               void *workspace, size_t ws_bytes, int n_slices,
+                                               void *stream, void *h2d_stream,
+                                               void *d2h_stream);
+
 /* One token of the recurrence for every (batch, head) state -- the
  * recurrent form of the page's section "Mamba-2 architecture", the
  * single-token step of sequential inference:

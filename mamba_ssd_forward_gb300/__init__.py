@@ -205,6 +205,31 @@ def forward_host(x, dt, A, B, C, D, h0, chunk, workspace, y, final_state=None):
         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream()))
 
 
+def host_overlapped_workspace_size(x, B, chunk, n_slices, has_D=True, has_h0=False,
+                                   want_final_state=True) -> int:
+    d = dims_of(x, B, chunk)
+    return int(_abi.load().ssd_forward_host_overlapped_workspace_size(
+        ctypes.byref(d), _io_code(x), int(has_D), int(has_h0), int(want_final_state),
+        int(n_slices)))
+
+
+def forward_host_overlapped(x, dt, A, B, C, D, h0, chunk, workspace, y, final_state=None,
+                            n_slices=4, h2d_stream=None, d2h_stream=None):
+    """ssd_forward_host_overlapped: as forward_host, cut into up to n_slices
+    slices whose uploads (h2d_stream), forward passes (current stream) and
+    downloads (d2h_stream) overlap.  Streams are torch.cuda.Stream or None."""
+    lib = _abi.load()
+    d = dims_of(x, B, chunk)
+    if not workspace.is_cuda:
+        raise ValueError("the workspace of ssd_forward_host_overlapped lives on the device")
+    sh = lambda s: None if s is None else ctypes.c_void_p(s.cuda_stream)  # noqa: E731
+    _abi.check("ssd_forward_host_overlapped", lib.ssd_forward_host_overlapped(
+        ctypes.byref(d), _io_code(x), _host_ptr(x), _host_ptr(dt), _host_ptr(A), _host_ptr(B),
+        _host_ptr(C), _host_ptr(D), _host_ptr(h0), _host_ptr(y), _host_ptr(final_state),
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), int(n_slices), _stream(),
+        sh(h2d_stream), sh(d2h_stream)))
+
+
 def device_error() -> None:
     """Synchronise the current stream and raise SsdError if a kernel of the
     library gave up a bounded wait since the last check."""

@@ -32,6 +32,8 @@ EXPORTS = (
     "ssd_forward_host",
     "ssd_forward_noalloc",
     "ssd_decode_step",
+    "ssd_forward_host_overlapped_workspace_size",
+    "ssd_forward_host_overlapped",
 )
 
 
@@ -84,6 +86,10 @@ def load(path: str | None = None):
     lib.ssd_forward_host_workspace_size.argtypes = [dims_p, i32, i32, i32, i32]
     lib.ssd_forward_host.restype = i32
     lib.ssd_forward_host.argtypes = [dims_p, i32] + [vp] * 10 + [sz, vp]
+    lib.ssd_forward_host_overlapped_workspace_size.restype = sz
+    lib.ssd_forward_host_overlapped_workspace_size.argtypes = [dims_p, i32, i32, i32, i32, i32]
+    lib.ssd_forward_host_overlapped.restype = i32
+    lib.ssd_forward_host_overlapped.argtypes = [dims_p, i32] + [vp] * 10 + [sz, i32, vp, vp, vp]
     lib.ssd_decode_step.restype = i32
     lib.ssd_decode_step.argtypes = [dims_p, i32] + [vp] * 9
     lib.ssd_forward_noalloc.restype = i32

@@ -177,3 +177,25 @@ def test_decode_step_rejections(lib):
     assert lib.ssd_decode_step(ctypes.byref(d1), 9, *args(ok, ok)) == 1
     assert lib.ssd_decode_step(None, 1, *args(ok, ok)) == 1
     assert _abi.SSD_OK == 0
+
+
+def test_host_overlapped_sizes_and_rejections(lib):
+    """ssd_forward_host_overlapped: a workspace size for both slicing modes,
+    and bad arguments rejected before anything is enqueued."""
+    d4 = dims(batch=4, seqlen=1000)
+    d1 = dims(batch=1, seqlen=1000)
+    for d in (d4, d1):
+        for n in (1, 2, 4):
+            assert lib.ssd_forward_host_overlapped_workspace_size(ctypes.byref(d), 1, 1, 1, 1, n) > 0
+    assert lib.ssd_forward_host_overlapped_workspace_size(ctypes.byref(d4), 1, 1, 1, 1, 0) == 0
+    assert lib.ssd_forward_host_overlapped_workspace_size(ctypes.byref(dims(chunk=96)), 1, 1, 1,
+                                                          1, 2) == 0
+    ok = ctypes.c_void_p(1 << 20)
+    host = [ok] * 5 + [None, None, ok, None]
+    ws = lib.ssd_forward_host_overlapped_workspace_size(ctypes.byref(d4), 1, 0, 0, 0, 2)
+    assert lib.ssd_forward_host_overlapped(ctypes.byref(d4), 1, *host, ok, ws, 0, None, None,
+                                           None) == 1  # n_slices
+    assert lib.ssd_forward_host_overlapped(ctypes.byref(d4), 1, *host, ok, ws - 256, 2, None,
+                                           None, None) == 1  # workspace too small
+    assert lib.ssd_forward_host_overlapped(ctypes.byref(dims(headdim=144)), 1, *host, ok, ws, 2,
+                                           None, None, None) == 2
