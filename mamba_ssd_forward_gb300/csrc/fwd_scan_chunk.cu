@@ -35,6 +35,13 @@ namespace {
 
 constexpr int kRowWarps = 8;
 constexpr int kRowThreads = kRowWarps * 32;
+// column split of every 64-column block between the row warps of a TMEM
+// lane quadrant: kCG groups of kCPT columns (kC16 16-column loads, kCH
+// 16-byte chunks of a 128-byte smem row)
+constexpr int kCG = kRowWarps / 4;
+constexpr int kCPT = 64 / kCG;
+constexpr int kC16 = kCPT / 16;
+constexpr int kCH = kCPT / 8;
 constexpr int kThreads = kRowThreads + 64;
 constexpr int kProducerWarp = kRowWarps, kMmaWarp = kRowWarps + 1;
 constexpr int kP = 64;              // head dimension handled here
@@ -226,9 +233,9 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
     }
   } else {
     // ------------------------------------------------------------ row warps
-    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, 32-column half
-    const int r = quad * 32 + (tid & 31);         // row within a tile = TMEM lane
-    const int c32 = half * 32;                    // this thread's columns of a 64-block
+    const int quad = warp & 3, cg = warp >> 2;  // TMEM lane quadrant, column group
+    const int r = quad * 32 + (tid & 31);       // row within a tile = TMEM lane
+    const int c32 = cg * kCPT;                  // this thread's columns of a 64-block
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
 
     // dt of the next head for token tid (tid < T), as raw bf16 bits until
@@ -285,19 +292,19 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       ptx::mbar_wait(&ych, q & 1, a.err, 129);
       ptx::tc_fence_after();
       {
-        uint32_t yr[2][2][16];
+        uint32_t yr[2][kC16][16];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (t >= ntile) break;
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < kC16; ++c)
             ptx::tmem_ld16(tmem + lane_base + kYCol + t * kP + c32 + c * 16, yr[t][c]);
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 2; ++c) ptx::reg_fence(yr[t][c]);
+          for (int c = 0; c < kC16; ++c) ptx::reg_fence(yr[t][c]);
           const float eg = ptx::ex2_approx(Gs[pb][t * 128 + r]);
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < kC16; ++c) {
             float v[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(yr[t][c][e]) * eg;
@@ -322,19 +329,19 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
         const int rb = i_rel >> 6;
         const float Git = Gs[pb][i_rel];
         for (int jb = 0; jb < 2 * (t + 1); ++jb, ++cnt) {
-          uint32_t sr[2][16];
+          uint32_t sr[kC16][16];
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < kC16; ++c)
             ptx::tmem_ld16(tmem + lane_base + sc_col(t) + jb * 64 + c32 + c * 16, sr[c]);
           ptx::tmem_ld_wait();
-          ptx::reg_fence(sr[0]);
-          ptx::reg_fence(sr[1]);
-          uint4 pk[4];
+#pragma unroll
+          for (int c = 0; c < kC16; ++c) ptx::reg_fence(sr[c]);
+          uint4 pk[kCH];
           if (jb < rb) {
             // whole block before the row's block: factored decay
             const float ui = ptx::ex2_approx(Git - Gs[pb][jb * 64 + 63]);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kC16; ++c) {
               const float4 *vp = reinterpret_cast<const float4 *>(&vs[pb][jb * 64 + c32 + c * 16]);
               float v[16];
 #pragma unroll
@@ -351,7 +358,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
           } else if (jb == rb) {
             // the row's own block: direct exponent, causal mask (j <= i)
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kC16; ++c) {
               const int jc0 = jb * 64 + c32 + c * 16;
               const float4 *gp = reinterpret_cast<const float4 *>(&Gs[pb][jc0]);
               const float4 *dp = reinterpret_cast<const float4 *>(&dts[pb][jc0]);
@@ -375,14 +382,14 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
             }
           } else {
 #pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) pk[k4] = make_uint4(0u, 0u, 0u, 0u);
+            for (int k4 = 0; k4 < kCH; ++k4) pk[k4] = make_uint4(0u, 0u, 0u, 0u);
           }
           const int s = cnt % kNP;
           ptx::mbar_wait(&pm_empty[s], ((cnt / kNP) & 1) ^ 1, a.err, 130);
           uint8_t *Pb = smem + a.off_sp + s * kTile;
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4)
-            *reinterpret_cast<uint4 *>(Pb + sw128(r, (half * 4 + k4) * 16)) = pk[k4];
+          for (int k4 = 0; k4 < kCH; ++k4)
+            *reinterpret_cast<uint4 *>(Pb + sw128(r, (cg * kCH + k4) * 16)) = pk[k4];
           ptx::fence_async_smem();
           ptx::tc_fence_before();
           ptx::mbar_arrive(&pm_full[s]);
@@ -399,18 +406,18 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       uint8_t *xs = smem + (buf ? a.off_hx1 : a.off_hx0) + st_bytes;
       {
         const float Dh = a.D ? a.D[h] : 0.f;
-        uint32_t yr[2][2][16];
+        uint32_t yr[2][kC16][16];
 #pragma unroll
         for (int t = 0; t < 2; ++t)
           if (t < ntile)
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < kC16; ++c)
               ptx::tmem_ld16(tmem + lane_base + kYCol + t * kP + c32 + c * 16, yr[t][c]);
         ptx::tmem_ld_wait();
 #pragma unroll
         for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int c = 0; c < 2; ++c) ptx::reg_fence(yr[t][c]);
+          for (int c = 0; c < kC16; ++c) ptx::reg_fence(yr[t][c]);
         ptx::tc_fence_before();
         ptx::mbar_arrive(&yfree);  // Y may now be overwritten by the next head
 #pragma unroll
@@ -419,8 +426,8 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
           const int i_rel = t * 128 + r;
           uint8_t *xrow = xs + (i_rel >> 6) * kBlk;
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            uint4 *p4 = reinterpret_cast<uint4 *>(xrow + sw128(i_rel & 63, (half * 4 + k4) * 16));
+          for (int k4 = 0; k4 < kCH; ++k4) {
+            uint4 *p4 = reinterpret_cast<uint4 *>(xrow + sw128(i_rel & 63, (cg * kCH + k4) * 16));
             float xv[8];
             unpack16(*p4, xv, (__nv_bfloat16 *)nullptr);
 #pragma unroll
