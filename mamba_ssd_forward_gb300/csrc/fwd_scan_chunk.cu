@@ -9,14 +9,15 @@
 //
 // The heads of one group share B and C, so C B^T of a chunk is the same for
 // all of them.  One CTA per (slice of hs heads of one group, chunk, batch):
-//   phase 1: Sc = C B^T for the whole chunk into tensor memory (row tile 0:
-//            columns [0, 128); row tile 1: columns [128, 384)), from C and B
-//            resident in shared memory;
+//   phase 1: Sc = C B^T for the whole chunk into tensor memory in fp32,
+//            from C and B resident in shared memory, then re-packed by the
+//            row warps as fp16 pairs (half the columns);
 //   per head q of the slice (state and x tiles double-buffered, so the next
 //            head's loads overlap this head):
-//            Y = C h_q^T (both row tiles, columns [384, 512)), Y *= exp2(G_i),
-//            the decayed, masked tile S'_q from Sc written to shared memory
-//            two 64-token blocks at a time, Y += S'_q X_q, and the epilogue
+//            Y = C h_q^T (both row tiles), Y *= exp2(G_i), the decayed,
+//            masked tile S'_q from Sc written to tensor memory as bf16 pairs
+//            one 64-token block at a time (two stages), Y += S'_q X_q with
+//            S'_q read from tensor memory, and the epilogue
 //            y = Y + D x computed over x in shared memory and written by TMA
 //            stores (the next head's cumsum runs while this head's last MMAs
 //            finish).
@@ -28,6 +29,8 @@
 // fwd_scan.cu.  The decay factors are those of fwd_scan.cu: for a 64-token
 // column block ending at r strictly before row i's block,
 // exp2(G_i - G_j) = exp2(G_i - G_r) * exp2(G_r - G_j), both exponents <= 0.
+#include <cuda_fp16.h>
+
 #include "fwd.cuh"
 
 namespace ssd {
@@ -48,9 +51,28 @@ constexpr int kP = 64;              // head dimension handled here
 constexpr int kNP = 2;              // stages of the decayed interaction tile S'
 constexpr int kBlk = 64 * 128;      // 64 rows of 128 bytes
 constexpr int kTile = 128 * 128;    // 128 rows of 128 bytes
-constexpr uint32_t kYCol = 384;
-// tensor-memory column of the interaction tile of row tile t
-__device__ __forceinline__ uint32_t sc_col(int t) { return t ? 128u : 0u; }
+static_assert(kCPT == 32, "a thread's S' row segment is one 16-column tensor-memory store");
+// Tensor-memory columns.  Phase 1 accumulates C B^T in fp32 (row tile 1:
+// [0, 256), row tile 0: [256, 384)); the row warps re-pack it as fp16 pairs
+// (row tile 1: [256, 384), row tile 0: [384, 448)), which frees [0, 256) for
+// Y (row tile t at 64 t) and the two stages of the decayed tile S' as bf16
+// pairs, the A operand of the S' X MMAs ([128, 160), [160, 192)).
+constexpr uint32_t kYCol = 0;
+__device__ __forceinline__ uint32_t scf_col(int t) { return t ? 0u : 256u; }
+__device__ __forceinline__ uint32_t sch_col(int t) { return t ? 256u : 384u; }
+__device__ __forceinline__ uint32_t sp_col(int s) { return 128u + 32u * (uint32_t)s; }
+
+// The fp16 copy of C B^T holds 2^-4 C B^T: magnitudes up to 2^20 stay
+// finite, and values below 2^-10 (subnormal) keep an absolute error of at
+// most 2^-21.  The decay factors carry the 2^4 back.
+constexpr float kScDown = 0.0625f, kScUp = 16.f, kScUpLog2 = 4.f;
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo * kScDown, hi * kScDown);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+__device__ __forceinline__ float2 unpack_h2(uint32_t u) {
+  return __half22float2(*reinterpret_cast<const __half2 *>(&u));
+}
 
 struct ChunkArgs {
   const __nv_bfloat16 *x, *dt;
@@ -59,7 +81,7 @@ struct ChunkArgs {
   int *err;
   int L, nh, S, hpg, T, nc, hs;
   // shared-memory layout (byte offsets from the 1024-aligned base)
-  int off_C, off_B, off_hx0, off_hx1, off_sp;
+  int off_C, off_B, off_hx0, off_hx1;
   int hx_bytes;  // states (S x P) followed by x (T x P), bf16
 };
 
@@ -71,7 +93,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
                     const __grid_constant__ CUtensorMap tm_y, const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t p1_full[2], sc_done, hx_full[2], hx_empty[2], ych, ysc,
+  __shared__ __align__(8) uint64_t p1_full[2], sc_done, pack_done, hx_full[2], hx_empty[2], ych, ysc,
       pm_full[kNP], pm_empty[kNP], ydone, yfree;
   __shared__ uint32_t tmem_slot;
   // per head (double-buffered by head parity): G in log2 units, dt, and the
@@ -100,6 +122,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       ptx::mbar_init(&hx_empty[i], 2);  // MMA commit + the y store has read the tile
     }
     ptx::mbar_init(&sc_done, 1);
+    ptx::mbar_init(&pack_done, kRowThreads);
     ptx::mbar_init(&ych, 1);
     ptx::mbar_init(&ysc, kRowThreads);
     for (int i = 0; i < kNP; ++i) {
@@ -172,7 +195,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t cd = ptx::smem_desc(c0 + kk * 32, 16, 1024, ptx::kSw128);
             const uint64_t bd = ptx::smem_desc(b0 + kk * 32, 16, 1024, ptx::kSw128);
-            ptx::mma_ss<false>(tmem + sc_col(t), cd, bd, idS, (sb | kk) ? 1u : 0u);
+            ptx::mma_ss<false>(tmem + scf_col(t), cd, bd, idS, (sb | kk) ? 1u : 0u);
           }
         }
       }
@@ -181,6 +204,8 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
     if (leader) ptx::mma_commit(&sc_done);
     __syncwarp();
     const uint32_t idY = ptx::idesc_bf16(128, kP, false, true);
+    // Y and the S' stages overlap the fp32 C B^T: wait for its re-packing
+    ptx::mbar_wait(&pack_done, 0, a.err, 133);
     int cnt = 0;  // S' blocks consumed so far
     for (int q = 0; q < hs; ++q) {
       const int buf = q & 1;
@@ -213,13 +238,11 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
           ptx::mbar_wait(&pm_full[s], (cnt / kNP) & 1, a.err, 127);
           ptx::tc_fence_after();
           if (leader) {
-            const uint32_t p0 = ptx::smem_u32(smem + a.off_sp + s * kTile);
             const uint32_t x0 = hx + st_bytes + jb * kBlk;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t pd = ptx::smem_desc(p0 + kk * 32, 16, 1024, ptx::kSw128);
               const uint64_t xd = ptx::smem_desc(x0 + kk * 2048, kBlk, 1024, ptx::kSw128);
-              ptx::mma_ss<false>(tmem + kYCol + t * kP, pd, xd, idY, 1u);
+              ptx::mma_ts_bf16(tmem + kYCol + t * kP, tmem + sp_col(s) + kk * 8, xd, idY, 1u);
             }
             ptx::mma_commit(&pm_empty[s]);
           }
@@ -282,6 +305,35 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
 
     ptx::mbar_wait(&sc_done, 0, a.err, 128);
     ptx::tc_fence_after();
+    // re-pack the fp32 C B^T as fp16 pairs (at most 2^-11 relative rounding
+    // before the decay, well below the bf16 rounding of S'), row tile 0
+    // first: its fp32 columns are then overwritten by row tile 1's copy
+    for (int t = 0; t < ntile; ++t) {
+      if (t == 1) {
+        ptx::tc_fence_before();
+        ptx::named_bar_sync(1, kRowThreads);  // every thread has read tile 0's fp32
+        ptx::tc_fence_after();
+      }
+      for (int jb = 0; jb < 2 * (t + 1); ++jb) {
+        uint32_t f[kC16][16];
+#pragma unroll
+        for (int c = 0; c < kC16; ++c)
+          ptx::tmem_ld16(tmem + lane_base + scf_col(t) + jb * 64 + c32 + c * 16, f[c]);
+        ptx::tmem_ld_wait();
+        uint32_t hv[16];
+#pragma unroll
+        for (int c = 0; c < kC16; ++c) {
+          ptx::reg_fence(f[c]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            hv[c * 8 + e] = pack_h2(__uint_as_float(f[c][2 * e]), __uint_as_float(f[c][2 * e + 1]));
+        }
+        ptx::tmem_st16u(tmem + lane_base + sch_col(t) + jb * 32 + cg * 16, hv);
+      }
+    }
+    ptx::tmem_st_wait();
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(&pack_done);
     cumsum(0);
     int cnt = 0;
     for (int q = 0; q < hs; ++q) {
@@ -328,18 +380,26 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
         const int i_rel = t * 128 + r;
         const int rb = i_rel >> 6;
         const float Git = Gs[pb][i_rel];
+        const float Git4 = Git + kScUpLog2;  // exp2(Git4 - G_j) = 2^4 exp2(Git - G_j)
         for (int jb = 0; jb < 2 * (t + 1); ++jb, ++cnt) {
-          uint32_t sr[kC16][16];
+          // this thread's 32 columns of the block, as 16 fp16 pairs
+          uint32_t sh[16];
+          ptx::tmem_ld16(tmem + lane_base + sch_col(t) + jb * 32 + cg * 16, sh);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence(sh);
+          float sf[kC16][16];
 #pragma unroll
           for (int c = 0; c < kC16; ++c)
-            ptx::tmem_ld16(tmem + lane_base + sc_col(t) + jb * 64 + c32 + c * 16, sr[c]);
-          ptx::tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < kC16; ++c) ptx::reg_fence(sr[c]);
+            for (int e = 0; e < 8; ++e) {
+              const float2 f2 = unpack_h2(sh[c * 8 + e]);
+              sf[c][2 * e] = f2.x;
+              sf[c][2 * e + 1] = f2.y;
+            }
           uint4 pk[kCH];
           if (jb < rb) {
             // whole block before the row's block: factored decay
-            const float ui = ptx::ex2_approx(Git - Gs[pb][jb * 64 + 63]);
+            const float ui = kScUp * ptx::ex2_approx(Git - Gs[pb][jb * 64 + 63]);
 #pragma unroll
             for (int c = 0; c < kC16; ++c) {
               const float4 *vp = reinterpret_cast<const float4 *>(&vs[pb][jb * 64 + c32 + c * 16]);
@@ -347,10 +407,10 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
 #pragma unroll
               for (int e4 = 0; e4 < 4; ++e4) {
                 const float4 f = vp[e4];
-                v[4 * e4 + 0] = __uint_as_float(sr[c][4 * e4 + 0]) * (ui * f.x);
-                v[4 * e4 + 1] = __uint_as_float(sr[c][4 * e4 + 1]) * (ui * f.y);
-                v[4 * e4 + 2] = __uint_as_float(sr[c][4 * e4 + 2]) * (ui * f.z);
-                v[4 * e4 + 3] = __uint_as_float(sr[c][4 * e4 + 3]) * (ui * f.w);
+                v[4 * e4 + 0] = sf[c][4 * e4 + 0] * (ui * f.x);
+                v[4 * e4 + 1] = sf[c][4 * e4 + 1] * (ui * f.y);
+                v[4 * e4 + 2] = sf[c][4 * e4 + 2] * (ui * f.z);
+                v[4 * e4 + 3] = sf[c][4 * e4 + 3] * (ui * f.w);
               }
               pk[2 * c] = pack_op16(v, (__nv_bfloat16 *)nullptr);
               pk[2 * c + 1] = pack_op16(v + 8, (__nv_bfloat16 *)nullptr);
@@ -372,8 +432,8 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
                 for (int cc = 0; cc < 4; ++cc) {
                   const int j = jc0 + 4 * e4 + cc;
                   v[4 * e4 + cc] = (j <= i_rel && j < valid)
-                                       ? __uint_as_float(sr[c][4 * e4 + cc]) *
-                                             ptx::ex2_approx(Git - ga[cc]) * da[cc]
+                                       ? sf[c][4 * e4 + cc] *
+                                             ptx::ex2_approx(Git4 - ga[cc]) * da[cc]
                                        : 0.f;
                 }
               }
@@ -384,13 +444,21 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
 #pragma unroll
             for (int k4 = 0; k4 < kCH; ++k4) pk[k4] = make_uint4(0u, 0u, 0u, 0u);
           }
+          // into tensor-memory stage s as 16 columns of bf16 pairs (the even
+          // column in the low half), the A operand of the S' X MMA
           const int s = cnt % kNP;
           ptx::mbar_wait(&pm_empty[s], ((cnt / kNP) & 1) ^ 1, a.err, 130);
-          uint8_t *Pb = smem + a.off_sp + s * kTile;
+          ptx::tc_fence_after();
+          uint32_t pu[16];
 #pragma unroll
-          for (int k4 = 0; k4 < kCH; ++k4)
-            *reinterpret_cast<uint4 *>(Pb + sw128(r, (cg * kCH + k4) * 16)) = pk[k4];
-          ptx::fence_async_smem();
+          for (int k4 = 0; k4 < kCH; ++k4) {
+            pu[4 * k4 + 0] = pk[k4].x;
+            pu[4 * k4 + 1] = pk[k4].y;
+            pu[4 * k4 + 2] = pk[k4].z;
+            pu[4 * k4 + 3] = pk[k4].w;
+          }
+          ptx::tmem_st16u(tmem + lane_base + sp_col(s) + cg * 16, pu);
+          ptx::tmem_st_wait();
           ptx::tc_fence_before();
           ptx::mbar_arrive(&pm_full[s]);
         }
@@ -463,7 +531,7 @@ int sm_count_scan() {
 }
 
 struct Layout {
-  int off_C, off_B, off_hx[2], off_sp, hx_bytes, total;
+  int off_C, off_B, off_hx[2], hx_bytes, total;
 };
 
 Layout chunk_layout(const Dims &d) {
@@ -474,8 +542,7 @@ Layout chunk_layout(const Dims &d) {
   l.off_C = 0;
   l.off_B = cb;
   l.off_hx[0] = 2 * cb;
-  l.off_sp = l.off_hx[0] + l.hx_bytes;
-  const int base = l.off_sp + kNP * kTile;
+  const int base = l.off_hx[0] + l.hx_bytes;
   if (base + l.hx_bytes <= 200 * 1024) {
     l.off_hx[1] = base;
     l.total = base + l.hx_bytes;
@@ -553,7 +620,6 @@ cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, c
   a.off_B = l.off_B;
   a.off_hx0 = l.off_hx[0];
   a.off_hx1 = l.off_hx[1];
-  a.off_sp = l.off_sp;
   a.hx_bytes = l.hx_bytes;
   dim3 grid((unsigned)(d.nh / hs), (unsigned)d.nc, (unsigned)d.b);
   if (d.nc > 65535) return cudaErrorInvalidValue;
