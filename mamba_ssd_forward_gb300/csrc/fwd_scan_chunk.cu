@@ -73,6 +73,10 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 __device__ __forceinline__ float2 unpack_h2(uint32_t u) {
   return __half22float2(*reinterpret_cast<const __half2 *>(&u));
 }
+__device__ __forceinline__ uint32_t pack_bf2(float2 v) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+  return *reinterpret_cast<const uint32_t *>(&b);
+}
 
 struct ChunkArgs {
   const __nv_bfloat16 *x, *dt;
@@ -382,81 +386,63 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
         const float Git = Gs[pb][i_rel];
         const float Git4 = Git + kScUpLog2;  // exp2(Git4 - G_j) = 2^4 exp2(Git - G_j)
         for (int jb = 0; jb < 2 * (t + 1); ++jb, ++cnt) {
-          // this thread's 32 columns of the block, as 16 fp16 pairs
-          uint32_t sh[16];
-          ptx::tmem_ld16(tmem + lane_base + sch_col(t) + jb * 32 + cg * 16, sh);
-          ptx::tmem_ld_wait();
-          ptx::reg_fence(sh);
-          float sf[kC16][16];
+          // pu: this thread's 32 columns of S' as 16 bf16 pairs, the even
+          // column in the low half (blocks right of the row's block are 0)
+          uint32_t pu[16];
+          if (jb <= rb) {
+            // the same 32 columns of C B^T, as 16 fp16 pairs
+            uint32_t sh[16];
+            ptx::tmem_ld16(tmem + lane_base + sch_col(t) + jb * 32 + cg * 16, sh);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence(sh);
+            if (jb < rb) {
+              // whole block before the row's block: factored decay
+              const float ui = kScUp * ptx::ex2_approx(Git - Gs[pb][jb * 64 + 63]);
+              const float2 ui2 = make_float2(ui, ui);
+              const float4 *vp = reinterpret_cast<const float4 *>(&vs[pb][jb * 64 + c32]);
 #pragma unroll
-          for (int c = 0; c < kC16; ++c)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float2 f2 = unpack_h2(sh[c * 8 + e]);
-              sf[c][2 * e] = f2.x;
-              sf[c][2 * e + 1] = f2.y;
-            }
-          uint4 pk[kCH];
-          if (jb < rb) {
-            // whole block before the row's block: factored decay
-            const float ui = kScUp * ptx::ex2_approx(Git - Gs[pb][jb * 64 + 63]);
-#pragma unroll
-            for (int c = 0; c < kC16; ++c) {
-              const float4 *vp = reinterpret_cast<const float4 *>(&vs[pb][jb * 64 + c32 + c * 16]);
-              float v[16];
-#pragma unroll
-              for (int e4 = 0; e4 < 4; ++e4) {
-                const float4 f = vp[e4];
-                v[4 * e4 + 0] = sf[c][4 * e4 + 0] * (ui * f.x);
-                v[4 * e4 + 1] = sf[c][4 * e4 + 1] * (ui * f.y);
-                v[4 * e4 + 2] = sf[c][4 * e4 + 2] * (ui * f.z);
-                v[4 * e4 + 3] = sf[c][4 * e4 + 3] * (ui * f.w);
+              for (int m = 0; m < 8; ++m) {
+                const float4 f = vp[m];
+                const float2 w0 = ptx::mul_f32x2(make_float2(f.x, f.y), ui2);
+                const float2 w1 = ptx::mul_f32x2(make_float2(f.z, f.w), ui2);
+                pu[2 * m] = pack_bf2(ptx::mul_f32x2(unpack_h2(sh[2 * m]), w0));
+                pu[2 * m + 1] = pack_bf2(ptx::mul_f32x2(unpack_h2(sh[2 * m + 1]), w1));
               }
-              pk[2 * c] = pack_op16(v, (__nv_bfloat16 *)nullptr);
-              pk[2 * c + 1] = pack_op16(v + 8, (__nv_bfloat16 *)nullptr);
-            }
-          } else if (jb == rb) {
-            // the row's own block: direct exponent, causal mask (j <= i)
+            } else {
+              // the row's own block: direct exponent, causal mask; columns
+              // k <= klim of the thread's 32 are kept (j <= i, j < valid)
+              const int klim = min(i_rel, valid - 1) - (jb * 64 + c32);
+              const float4 *gp = reinterpret_cast<const float4 *>(&Gs[pb][jb * 64 + c32]);
+              const float4 *dp = reinterpret_cast<const float4 *>(&dts[pb][jb * 64 + c32]);
+              const float2 g2 = make_float2(Git4, Git4);
 #pragma unroll
-            for (int c = 0; c < kC16; ++c) {
-              const int jc0 = jb * 64 + c32 + c * 16;
-              const float4 *gp = reinterpret_cast<const float4 *>(&Gs[pb][jc0]);
-              const float4 *dp = reinterpret_cast<const float4 *>(&dts[pb][jc0]);
-              float v[16];
-#pragma unroll
-              for (int e4 = 0; e4 < 4; ++e4) {
-                const float4 gj = gp[e4], dj = dp[e4];
-                const float ga[4] = {gj.x, gj.y, gj.z, gj.w};
-                const float da[4] = {dj.x, dj.y, dj.z, dj.w};
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                  const int j = jc0 + 4 * e4 + cc;
-                  v[4 * e4 + cc] = (j <= i_rel && j < valid)
-                                       ? sf[c][4 * e4 + cc] *
-                                             ptx::ex2_approx(Git4 - ga[cc]) * da[cc]
-                                       : 0.f;
-                }
+              for (int m = 0; m < 8; ++m) {
+                const float4 gj = gp[m], dj = dp[m];
+                float2 e0 = ptx::sub_f32x2(g2, make_float2(gj.x, gj.y));
+                float2 e1 = ptx::sub_f32x2(g2, make_float2(gj.z, gj.w));
+                e0 = make_float2(ptx::ex2_approx(e0.x), ptx::ex2_approx(e0.y));
+                e1 = make_float2(ptx::ex2_approx(e1.x), ptx::ex2_approx(e1.y));
+                float2 v0 = ptx::mul_f32x2(ptx::mul_f32x2(unpack_h2(sh[2 * m]), e0),
+                                           make_float2(dj.x, dj.y));
+                float2 v1 = ptx::mul_f32x2(ptx::mul_f32x2(unpack_h2(sh[2 * m + 1]), e1),
+                                           make_float2(dj.z, dj.w));
+                v0.x = 4 * m + 0 <= klim ? v0.x : 0.f;
+                v0.y = 4 * m + 1 <= klim ? v0.y : 0.f;
+                v1.x = 4 * m + 2 <= klim ? v1.x : 0.f;
+                v1.y = 4 * m + 3 <= klim ? v1.y : 0.f;
+                pu[2 * m] = pack_bf2(v0);
+                pu[2 * m + 1] = pack_bf2(v1);
               }
-              pk[2 * c] = pack_op16(v, (__nv_bfloat16 *)nullptr);
-              pk[2 * c + 1] = pack_op16(v + 8, (__nv_bfloat16 *)nullptr);
             }
           } else {
 #pragma unroll
-            for (int k4 = 0; k4 < kCH; ++k4) pk[k4] = make_uint4(0u, 0u, 0u, 0u);
+            for (int m = 0; m < 16; ++m) pu[m] = 0u;
           }
           // into tensor-memory stage s as 16 columns of bf16 pairs (the even
           // column in the low half), the A operand of the S' X MMA
           const int s = cnt % kNP;
           ptx::mbar_wait(&pm_empty[s], ((cnt / kNP) & 1) ^ 1, a.err, 130);
           ptx::tc_fence_after();
-          uint32_t pu[16];
-#pragma unroll
-          for (int k4 = 0; k4 < kCH; ++k4) {
-            pu[4 * k4 + 0] = pk[k4].x;
-            pu[4 * k4 + 1] = pk[k4].y;
-            pu[4 * k4 + 2] = pk[k4].z;
-            pu[4 * k4 + 3] = pk[k4].w;
-          }
           ptx::tmem_st16u(tmem + lane_base + sp_col(s) + cg * 16, pu);
           ptx::tmem_st_wait();
           ptx::tc_fence_before();

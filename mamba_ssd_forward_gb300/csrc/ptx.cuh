@@ -88,6 +88,29 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Packed fp32 pairs: one instruction operates on both lanes of a 64-bit
+// register pair (round to nearest, as the scalar forms).
+__device__ __forceinline__ unsigned long long f32x2_bits(float2 a) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+  return r;
+}
+__device__ __forceinline__ float2 f32x2_of(unsigned long long r) {
+  float2 a;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+  return a;
+}
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f32x2_bits(a)), "l"(f32x2_bits(b)));
+  return f32x2_of(r);
+}
+__device__ __forceinline__ float2 sub_f32x2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f32x2_bits(a)), "l"(f32x2_bits(b)));
+  return f32x2_of(r);
+}
+
 // ------------------------------------------- programmatic dependent launch
 
 // Wait until every grid this one depends on (the preceding kernel on the
