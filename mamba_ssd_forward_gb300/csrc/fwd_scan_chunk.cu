@@ -14,15 +14,15 @@
 //            row warps as fp16 pairs (half the columns);
 //   per head q of the slice (state and x tiles double-buffered, so the next
 //            head's loads overlap this head):
-//            Y = C h_q^T (both row tiles), Y *= exp2(G_i), the decayed,
-//            masked tile S'_q from Sc written to tensor memory as bf16 pairs
-//            one 64-token block at a time (two stages), Y += S'_q X_q with
-//            S'_q read from tensor memory, and the epilogue
-//            y = Y + D x computed over x in shared memory and written by TMA
-//            stores (the next head's cumsum runs while this head's last MMAs
-//            finish).
+//            Yc = C h_q^T (both row tiles), the decayed, masked tile S'_q
+//            from Sc written to tensor memory as bf16 pairs one 64-token
+//            block at a time (two stages), Ys = S'_q X_q with S'_q read from
+//            tensor memory, and the epilogue
+//            y = exp2(G_i) Yc + Ys + D x computed over x in shared memory and
+//            written by TMA stores (the next head's cumsum runs while this
+//            head's last MMAs finish).
 // Warp roles: warp 8 loads (TMA), warp 9 issues the MMAs, warps 0-7 do the
-// cumsums, the rescale, the decay and the epilogue (two warps per 32-lane
+// cumsums, the re-packing, the decay and the epilogue (two warps per 32-lane
 // quadrant, each taking 32 of every 64 columns).
 //
 // Supported: P = 64, S in {64, 128}, T in {128, 256}; other shapes use
@@ -54,10 +54,13 @@ constexpr int kTile = 128 * 128;    // 128 rows of 128 bytes
 static_assert(kCPT == 32, "a thread's S' row segment is one 16-column tensor-memory store");
 // Tensor-memory columns.  Phase 1 accumulates C B^T in fp32 (row tile 1:
 // [0, 256), row tile 0: [256, 384)); the row warps re-pack it as fp16 pairs
-// (row tile 1: [256, 384), row tile 0: [384, 448)), which frees [0, 256) for
-// Y (row tile t at 64 t) and the two stages of the decayed tile S' as bf16
-// pairs, the A operand of the S' X MMAs ([128, 160), [160, 192)).
-constexpr uint32_t kYCol = 0;
+// (row tile 1: [256, 384), row tile 0: [384, 448)), which frees the rest for
+// the two accumulators of a head, Ys = S' X (row tile t at 64 t) and
+// Yc = C h^T (row tile 0 at 192, row tile 1 at 448), and the two stages of
+// the decayed tile S' as bf16 pairs, the A operand of the S' X MMAs ([128,
+// 160), [160, 192)).  The epilogue combines y = exp2(G_i) Yc + Ys + D x.
+__device__ __forceinline__ uint32_t ys_col(int t) { return 64u * (uint32_t)t; }
+__device__ __forceinline__ uint32_t yc_col(int t) { return t ? 448u : 192u; }
 __device__ __forceinline__ uint32_t scf_col(int t) { return t ? 0u : 256u; }
 __device__ __forceinline__ uint32_t sch_col(int t) { return t ? 256u : 384u; }
 __device__ __forceinline__ uint32_t sp_col(int s) { return 128u + 32u * (uint32_t)s; }
@@ -97,7 +100,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
                     const __grid_constant__ CUtensorMap tm_y, const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t p1_full[2], sc_done, pack_done, hx_full[2], hx_empty[2], ych, ysc,
+  __shared__ __align__(8) uint64_t p1_full[2], sc_done, pack_done, hx_full[2], hx_empty[2],
       pm_full[kNP], pm_empty[kNP], ydone, yfree;
   __shared__ uint32_t tmem_slot;
   // per head (double-buffered by head parity): G in log2 units, dt, and the
@@ -127,8 +130,6 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
     }
     ptx::mbar_init(&sc_done, 1);
     ptx::mbar_init(&pack_done, kRowThreads);
-    ptx::mbar_init(&ych, 1);
-    ptx::mbar_init(&ysc, kRowThreads);
     for (int i = 0; i < kNP; ++i) {
       ptx::mbar_init(&pm_full[i], kRowThreads);
       ptx::mbar_init(&pm_empty[i], 1);
@@ -208,7 +209,8 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
     if (leader) ptx::mma_commit(&sc_done);
     __syncwarp();
     const uint32_t idY = ptx::idesc_bf16(128, kP, false, true);
-    // Y and the S' stages overlap the fp32 C B^T: wait for its re-packing
+    // the accumulators and the S' stages overlap the fp32 C B^T: wait for
+    // its re-packing
     ptx::mbar_wait(&pack_done, 0, a.err, 133);
     int cnt = 0;  // S' blocks consumed so far
     for (int q = 0; q < hs; ++q) {
@@ -217,7 +219,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       ptx::mbar_wait(&hx_full[buf], (q >> 1) & 1, a.err, 124);
       if (q > 0) ptx::mbar_wait(&yfree, (q - 1) & 1, a.err, 125);
       ptx::tc_fence_after();
-      // Y = C h_q^T for each row tile
+      // Yc = C h_q^T for each row tile
       if (leader) {
         for (int t = 0; t < ntile; ++t)
           for (int sb = 0; sb < nsb; ++sb) {
@@ -227,15 +229,12 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
               const uint64_t cd = ptx::smem_desc(c0 + kk * 32, 16, 1024, ptx::kSw128);
               const uint64_t hd =
                   ptx::smem_desc(hx + sb * kBlk + kk * 2048, kBlk, 1024, ptx::kSw128);
-              ptx::mma_ss<false>(tmem + kYCol + t * kP, cd, hd, idY, (sb | kk) ? 1u : 0u);
+              ptx::mma_ss<false>(tmem + yc_col(t), cd, hd, idY, (sb | kk) ? 1u : 0u);
             }
           }
-        ptx::mma_commit(&ych);
       }
       __syncwarp();
-      ptx::mbar_wait(&ysc, q & 1, a.err, 126);
-      ptx::tc_fence_after();
-      // Y += S'_q X_q, one 64-token block of each row tile at a time
+      // Ys = S'_q X_q, one 64-token block of each row tile at a time
       for (int t = 0; t < ntile; ++t)
         for (int jb = 0; jb < 2 * (t + 1); ++jb, ++cnt) {
           const int s = cnt % kNP;
@@ -246,7 +245,8 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t xd = ptx::smem_desc(x0 + kk * 2048, kBlk, 1024, ptx::kSw128);
-              ptx::mma_ts_bf16(tmem + kYCol + t * kP, tmem + sp_col(s) + kk * 8, xd, idY, 1u);
+              ptx::mma_ts_bf16(tmem + ys_col(t), tmem + sp_col(s) + kk * 8, xd, idY,
+                               (jb | kk) ? 1u : 0u);
             }
             ptx::mma_commit(&pm_empty[s]);
           }
@@ -344,39 +344,6 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       const int pb = q & 1, buf = q & 1;
       const int h = hbase + q;
 
-      // carried-state term: Y *= exp2(G_i) for both row tiles
-      ptx::mbar_wait(&ych, q & 1, a.err, 129);
-      ptx::tc_fence_after();
-      {
-        uint32_t yr[2][kC16][16];
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t >= ntile) break;
-#pragma unroll
-          for (int c = 0; c < kC16; ++c)
-            ptx::tmem_ld16(tmem + lane_base + kYCol + t * kP + c32 + c * 16, yr[t][c]);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < kC16; ++c) ptx::reg_fence(yr[t][c]);
-          const float eg = ptx::ex2_approx(Gs[pb][t * 128 + r]);
-#pragma unroll
-          for (int c = 0; c < kC16; ++c) {
-            float v[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(yr[t][c][e]) * eg;
-            ptx::tmem_st16(tmem + lane_base + kYCol + t * kP + c32 + c * 16, v);
-          }
-        }
-        ptx::tmem_st_wait();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&ysc);
-      }
-      // the previous head's y store has had the rescale's time to read its
-      // shared-memory tile: release that head buffer to the producer
-      if (tid == 0 && q > 0) {
-        ptx::bulk_wait_read<0>();
-        ptx::mbar_arrive(&hx_empty[(q - 1) & 1]);
-      }
 
       // decayed, masked interaction rows, one 64-token block (one S' stage)
       // per tensor-memory load wait
@@ -447,14 +414,20 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
           ptx::tmem_st_wait();
           ptx::tc_fence_before();
           ptx::mbar_arrive(&pm_full[s]);
+          // the previous head's y store has had the first row tile's time to
+          // read its shared-memory tile: release that head buffer
+          if (tid == 0 && q > 0 && t == 0 && jb == 1) {
+            ptx::bulk_wait_read<0>();
+            ptx::mbar_arrive(&hx_empty[(q - 1) & 1]);
+          }
         }
       }
 
       // the next head's cumsum while this head's last MMAs finish
       if (q + 1 < hs) cumsum(q + 1);
 
-      // epilogue: y = Y + D x, written over x in the head's shared-memory
-      // tile and stored by TMA
+      // epilogue: y = exp2(G_i) Yc + Ys + D x, written over x in the head's
+      // shared-memory tile and stored by TMA
       ptx::mbar_wait(&ydone, q & 1, a.err, 131);
       ptx::tc_fence_after();
       uint8_t *xs = smem + (buf ? a.off_hx1 : a.off_hx0) + st_bytes;
@@ -462,18 +435,30 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
         const float Dh = a.D ? a.D[h] : 0.f;
         uint32_t yr[2][kC16][16];
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (t < ntile)
+        for (int t = 0; t < 2; ++t) {
+          if (t >= ntile) break;
+          uint32_t yc[kC16][16];
 #pragma unroll
-            for (int c = 0; c < kC16; ++c)
-              ptx::tmem_ld16(tmem + lane_base + kYCol + t * kP + c32 + c * 16, yr[t][c]);
-        ptx::tmem_ld_wait();
+          for (int c = 0; c < kC16; ++c) {
+            ptx::tmem_ld16(tmem + lane_base + ys_col(t) + c32 + c * 16, yr[t][c]);
+            ptx::tmem_ld16(tmem + lane_base + yc_col(t) + c32 + c * 16, yc[c]);
+          }
+          ptx::tmem_ld_wait();
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+          for (int c = 0; c < kC16; ++c) {
+            ptx::reg_fence(yr[t][c]);
+            ptx::reg_fence(yc[c]);
+          }
+          const float eg = ptx::ex2_approx(Gs[pb][t * 128 + r]);  // carried-state decay
 #pragma unroll
-          for (int c = 0; c < kC16; ++c) ptx::reg_fence(yr[t][c]);
+          for (int c = 0; c < kC16; ++c)
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              yr[t][c][e] = __float_as_uint(
+                  fmaf(eg, __uint_as_float(yc[c][e]), __uint_as_float(yr[t][c][e])));
+        }
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&yfree);  // Y may now be overwritten by the next head
+        ptx::mbar_arrive(&yfree);  // Yc and Ys may now take the next head
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (t >= ntile) break;
