@@ -51,7 +51,9 @@ constexpr int kP = 64;              // head dimension handled here
 constexpr int kNP = 2;              // stages of the decayed interaction tile S'
 constexpr int kBlk = 64 * 128;      // 64 rows of 128 bytes
 constexpr int kTile = 128 * 128;    // 128 rows of 128 bytes
-static_assert(kCPT == 32, "a thread's S' row segment is one 16-column tensor-memory store");
+// packed (two-column) tensor-memory columns of a thread's part of a block
+constexpr int kPP = kCPT / 2;
+static_assert(kCPT == 32 || kCPT == 16, "a thread's S' row segment is one 8- or 16-column store");
 // Tensor-memory columns.  Phase 1 accumulates C B^T in fp32 (row tile 1:
 // [0, 256), row tile 0: [256, 384)); the row warps re-pack it as fp16 pairs
 // (row tile 1: [256, 384), row tile 0: [384, 448)), which frees the rest for
@@ -69,6 +71,9 @@ __device__ __forceinline__ uint32_t sp_col(int s) { return 128u + 32u * (uint32_
 // finite, and values below 2^-10 (subnormal) keep an absolute error of at
 // most 2^-21.  The decay factors carry the 2^4 back.
 constexpr float kScDown = 0.0625f, kScUp = 16.f, kScUpLog2 = 4.f;
+// Largest total decay (log2 units, the sum of -A dt log2(e) over a 64-token
+// block) for which the row's own block uses the factored decay.
+constexpr float kSpanMax = 96.f;
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo * kScDown, hi * kScDown);
   return *reinterpret_cast<const uint32_t *>(&h);
@@ -129,13 +134,14 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       ptx::mbar_init(&hx_empty[i], 2);  // MMA commit + the y store has read the tile
     }
     ptx::mbar_init(&sc_done, 1);
-    ptx::mbar_init(&pack_done, kRowThreads);
+    // the row warps arrive once per warp (lane 0, after __syncwarp)
+    ptx::mbar_init(&pack_done, kRowWarps);
     for (int i = 0; i < kNP; ++i) {
-      ptx::mbar_init(&pm_full[i], kRowThreads);
+      ptx::mbar_init(&pm_full[i], kRowWarps);
       ptx::mbar_init(&pm_empty[i], 1);
     }
     ptx::mbar_init(&ydone, 1);
-    ptx::mbar_init(&yfree, kRowThreads);
+    ptx::mbar_init(&yfree, kRowWarps);
     ptx::fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -324,7 +330,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
         for (int c = 0; c < kC16; ++c)
           ptx::tmem_ld16(tmem + lane_base + scf_col(t) + jb * 64 + c32 + c * 16, f[c]);
         ptx::tmem_ld_wait();
-        uint32_t hv[16];
+        uint32_t hv[kPP];
 #pragma unroll
         for (int c = 0; c < kC16; ++c) {
           ptx::reg_fence(f[c]);
@@ -332,12 +338,13 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
           for (int e = 0; e < 8; ++e)
             hv[c * 8 + e] = pack_h2(__uint_as_float(f[c][2 * e]), __uint_as_float(f[c][2 * e + 1]));
         }
-        ptx::tmem_st16u(tmem + lane_base + sch_col(t) + jb * 32 + cg * 16, hv);
+        ptx::tmem_stu<kPP>(tmem + lane_base + sch_col(t) + jb * 32 + cg * kPP, hv);
       }
     }
     ptx::tmem_st_wait();
     ptx::tc_fence_before();
-    ptx::mbar_arrive(&pack_done);
+    __syncwarp();
+    if ((tid & 31) == 0) ptx::mbar_arrive(&pack_done);
     cumsum(0);
     int cnt = 0;
     for (int q = 0; q < hs; ++q) {
@@ -353,13 +360,13 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
         const float Git = Gs[pb][i_rel];
         const float Git4 = Git + kScUpLog2;  // exp2(Git4 - G_j) = 2^4 exp2(Git - G_j)
         for (int jb = 0; jb < 2 * (t + 1); ++jb, ++cnt) {
-          // pu: this thread's 32 columns of S' as 16 bf16 pairs, the even
+          // pu: this thread's kCPT columns of S' as kPP bf16 pairs, the even
           // column in the low half (blocks right of the row's block are 0)
-          uint32_t pu[16];
+          uint32_t pu[kPP];
           if (jb <= rb) {
-            // the same 32 columns of C B^T, as 16 fp16 pairs
-            uint32_t sh[16];
-            ptx::tmem_ld16(tmem + lane_base + sch_col(t) + jb * 32 + cg * 16, sh);
+            // the same columns of C B^T, as fp16 pairs
+            uint32_t sh[kPP];
+            ptx::tmem_ldu<kPP>(tmem + lane_base + sch_col(t) + jb * 32 + cg * kPP, sh);
             ptx::tmem_ld_wait();
             ptx::reg_fence(sh);
             if (jb < rb) {
@@ -368,22 +375,46 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
               const float2 ui2 = make_float2(ui, ui);
               const float4 *vp = reinterpret_cast<const float4 *>(&vs[pb][jb * 64 + c32]);
 #pragma unroll
-              for (int m = 0; m < 8; ++m) {
+              for (int m = 0; m < kCPT / 4; ++m) {
                 const float4 f = vp[m];
                 const float2 w0 = ptx::mul_f32x2(make_float2(f.x, f.y), ui2);
                 const float2 w1 = ptx::mul_f32x2(make_float2(f.z, f.w), ui2);
                 pu[2 * m] = pack_bf2(ptx::mul_f32x2(unpack_h2(sh[2 * m]), w0));
                 pu[2 * m + 1] = pack_bf2(ptx::mul_f32x2(unpack_h2(sh[2 * m + 1]), w1));
               }
+            } else if (-(warp_tot[pb][2 * jb] + warp_tot[pb][2 * jb + 1]) < kSpanMax) {
+              // the row's own block, whose total decay exp2(-span) is above
+              // 2^-kSpanMax: the same factors about its last token r, now
+              // exp2(G_i - G_r) <= 2^kSpanMax and exp2(G_r - G_j) >= 2^-kSpanMax
+              // (no overflow, no underflow), with the causal mask: columns
+              // k <= klim of the thread's kCPT are kept (j <= i, j < valid)
+              const int klim = min(i_rel, valid - 1) - (jb * 64 + c32);
+              const float ui = kScUp * ptx::ex2_approx(Git - Gs[pb][jb * 64 + 63]);
+              const float2 ui2 = make_float2(ui, ui);
+              const float4 *vp = reinterpret_cast<const float4 *>(&vs[pb][jb * 64 + c32]);
+#pragma unroll
+              for (int m = 0; m < kCPT / 4; ++m) {
+                const float4 f = vp[m];
+                const float2 w0 = ptx::mul_f32x2(make_float2(f.x, f.y), ui2);
+                const float2 w1 = ptx::mul_f32x2(make_float2(f.z, f.w), ui2);
+                float2 v0 = ptx::mul_f32x2(unpack_h2(sh[2 * m]), w0);
+                float2 v1 = ptx::mul_f32x2(unpack_h2(sh[2 * m + 1]), w1);
+                v0.x = 4 * m + 0 <= klim ? v0.x : 0.f;
+                v0.y = 4 * m + 1 <= klim ? v0.y : 0.f;
+                v1.x = 4 * m + 2 <= klim ? v1.x : 0.f;
+                v1.y = 4 * m + 3 <= klim ? v1.y : 0.f;
+                pu[2 * m] = pack_bf2(v0);
+                pu[2 * m + 1] = pack_bf2(v1);
+              }
             } else {
-              // the row's own block: direct exponent, causal mask; columns
-              // k <= klim of the thread's 32 are kept (j <= i, j < valid)
+              // the row's own block with a steep decay: direct exponent,
+              // causal mask (columns k <= klim kept, as above)
               const int klim = min(i_rel, valid - 1) - (jb * 64 + c32);
               const float4 *gp = reinterpret_cast<const float4 *>(&Gs[pb][jb * 64 + c32]);
               const float4 *dp = reinterpret_cast<const float4 *>(&dts[pb][jb * 64 + c32]);
               const float2 g2 = make_float2(Git4, Git4);
 #pragma unroll
-              for (int m = 0; m < 8; ++m) {
+              for (int m = 0; m < kCPT / 4; ++m) {
                 const float4 gj = gp[m], dj = dp[m];
                 float2 e0 = ptx::sub_f32x2(g2, make_float2(gj.x, gj.y));
                 float2 e1 = ptx::sub_f32x2(g2, make_float2(gj.z, gj.w));
@@ -403,17 +434,18 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
             }
           } else {
 #pragma unroll
-            for (int m = 0; m < 16; ++m) pu[m] = 0u;
+            for (int m = 0; m < kPP; ++m) pu[m] = 0u;
           }
           // into tensor-memory stage s as 16 columns of bf16 pairs (the even
           // column in the low half), the A operand of the S' X MMA
           const int s = cnt % kNP;
           ptx::mbar_wait(&pm_empty[s], ((cnt / kNP) & 1) ^ 1, a.err, 130);
           ptx::tc_fence_after();
-          ptx::tmem_st16u(tmem + lane_base + sp_col(s) + cg * 16, pu);
+          ptx::tmem_stu<kPP>(tmem + lane_base + sp_col(s) + cg * kPP, pu);
           ptx::tmem_st_wait();
           ptx::tc_fence_before();
-          ptx::mbar_arrive(&pm_full[s]);
+          __syncwarp();
+          if ((tid & 31) == 0) ptx::mbar_arrive(&pm_full[s]);
           // the previous head's y store has had the first row tile's time to
           // read its shared-memory tile: release that head buffer
           if (tid == 0 && q > 0 && t == 0 && jb == 1) {
@@ -458,7 +490,8 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
                   fmaf(eg, __uint_as_float(yc[c][e]), __uint_as_float(yr[t][c][e])));
         }
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&yfree);  // Yc and Ys may now take the next head
+        __syncwarp();
+        if ((tid & 31) == 0) ptx::mbar_arrive(&yfree);  // Yc, Ys may now take the next head
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (t >= ntile) break;

@@ -177,3 +177,33 @@ def test_resume_matches_one_shot(ssd):
     torch.cuda.synchronize()
     assert rel_l2(to64(torch.cat([ya, yb], 1)), to64(y)) < 2e-3
     assert rel_l2(to64(fb), to64(fin)) < 2e-3
+
+
+def test_steep_decay_blocks(ssd):
+    """The output pass factors the decay of a row's own 64-token block about
+    the block's last token only while the block's total decay stays above
+    2^-96; steeper blocks take the direct exponent.  One input with both kinds
+    of block in the same chunk (and heads with only one kind), against the
+    oracle."""
+    w = small("bf16_steep_decay", 1024, 4, 64, 128, 1, 256, "bf16")
+    inp = make(w)
+    A = inp["A"].clone()
+    A[0] = A[1] = -16.0
+    dt = inp["dt"].double().clone()
+    tok = torch.arange(w.seqlen)
+    dt[0, (tok // 64) % 2 == 1, 0] = 0.5  # head 0: every other block steep
+    dt[0, :, 1] = 0.1                     # head 1: every block steep
+    inp["A"], inp["dt"] = A, dt.to(inp["dt"].dtype)
+    a = -(A.double()[None, None, :] * inp["dt"].double()) * LOG2E
+    span = a.reshape(1, w.seqlen // 64, 64, w.nheads).sum(2)
+    assert (span > 96).any() and (span < 96).any()
+    ref = oracle_run(w, inp)
+    dev = device_inputs(inp)
+    y, fin = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                         dev["h0"], chunk=w.chunk)
+    ssd.device_error()
+    y64, x64 = to64(y), to64(inp["x"])
+    Dx = to64(inp["D"])[None, None, :, None] * x64
+    check_io(y64, ref["y"], w.dtype, "steep y")
+    check_io(y64 - Dx, ref["y"] - Dx, w.dtype, "steep y - D x")
+    check_io(to64(fin), ref["final_state"], w.dtype, "steep final_state")
