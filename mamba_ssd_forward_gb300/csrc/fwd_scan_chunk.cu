@@ -106,7 +106,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t p1_full[2], sc_done, pack_done, hx_full[2], hx_empty[2],
-      pm_full[kNP], pm_empty[kNP], ydone, yfree;
+      pm_full[kNP], pm_empty[kNP], ydone, yfree[2];
   __shared__ uint32_t tmem_slot;
   // per head (double-buffered by head parity): G in log2 units, dt, and the
   // column factors v_j = exp2(G_r - G_j) dt_j of the factored decay; read
@@ -141,7 +141,8 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       ptx::mbar_init(&pm_empty[i], 1);
     }
     ptx::mbar_init(&ydone, 1);
-    ptx::mbar_init(&yfree, kRowWarps);
+    ptx::mbar_init(&yfree[0], kRowWarps);  // per row tile
+    ptx::mbar_init(&yfree[1], kRowWarps);
     ptx::fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -223,11 +224,12 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       const int buf = q & 1;
       const uint32_t hx = ptx::smem_u32(smem + (buf ? a.off_hx1 : a.off_hx0));
       ptx::mbar_wait(&hx_full[buf], (q >> 1) & 1, a.err, 124);
-      if (q > 0) ptx::mbar_wait(&yfree, (q - 1) & 1, a.err, 125);
-      ptx::tc_fence_after();
-      // Yc = C h_q^T for each row tile
-      if (leader) {
-        for (int t = 0; t < ntile; ++t)
+      // Yc = C h_q^T for each row tile, once the previous head's epilogue
+      // has read that tile's accumulators
+      for (int t = 0; t < ntile; ++t) {
+        if (q > 0) ptx::mbar_wait(&yfree[t], (q - 1) & 1, a.err, 125);
+        ptx::tc_fence_after();
+        if (leader) {
           for (int sb = 0; sb < nsb; ++sb) {
             const uint32_t c0 = ptx::smem_u32(smem + a.off_C + (t * nsb + sb) * kTile);
 #pragma unroll
@@ -238,8 +240,9 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
               ptx::mma_ss<false>(tmem + yc_col(t), cd, hd, idY, (sb | kk) ? 1u : 0u);
             }
           }
+        }
+        __syncwarp();
       }
-      __syncwarp();
       // Ys = S'_q X_q, one 64-token block of each row tile at a time
       for (int t = 0; t < ntile; ++t)
         for (int jb = 0; jb < 2 * (t + 1); ++jb, ++cnt) {
@@ -350,6 +353,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
     for (int q = 0; q < hs; ++q) {
       const int pb = q & 1, buf = q & 1;
       const int h = hbase + q;
+      const float Dh = a.D ? a.D[h] : 0.f;  // used in the epilogue: load it early
 
 
       // decayed, masked interaction rows, one 64-token block (one S' stage)
@@ -463,50 +467,39 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       ptx::mbar_wait(&ydone, q & 1, a.err, 131);
       ptx::tc_fence_after();
       uint8_t *xs = smem + (buf ? a.off_hx1 : a.off_hx0) + st_bytes;
-      {
-        const float Dh = a.D ? a.D[h] : 0.f;
-        uint32_t yr[2][kC16][16];
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t >= ntile) break;
-          uint32_t yc[kC16][16];
+      for (int t = 0; t < 2; ++t) {
+        if (t >= ntile) break;
+        const int i_rel = t * 128 + r;
+        uint8_t *xrow = xs + (i_rel >> 6) * kBlk;
+        uint32_t ys[kC16][16], yc[kC16][16];
 #pragma unroll
-          for (int c = 0; c < kC16; ++c) {
-            ptx::tmem_ld16(tmem + lane_base + ys_col(t) + c32 + c * 16, yr[t][c]);
-            ptx::tmem_ld16(tmem + lane_base + yc_col(t) + c32 + c * 16, yc[c]);
-          }
-          ptx::tmem_ld_wait();
+        for (int c = 0; c < kC16; ++c) {
+          ptx::tmem_ld16(tmem + lane_base + ys_col(t) + c32 + c * 16, ys[c]);
+          ptx::tmem_ld16(tmem + lane_base + yc_col(t) + c32 + c * 16, yc[c]);
+        }
+        ptx::tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < kC16; ++c) {
-            ptx::reg_fence(yr[t][c]);
-            ptx::reg_fence(yc[c]);
-          }
-          const float eg = ptx::ex2_approx(Gs[pb][t * 128 + r]);  // carried-state decay
-#pragma unroll
-          for (int c = 0; c < kC16; ++c)
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              yr[t][c][e] = __float_as_uint(
-                  fmaf(eg, __uint_as_float(yc[c][e]), __uint_as_float(yr[t][c][e])));
+        for (int c = 0; c < kC16; ++c) {
+          ptx::reg_fence(ys[c]);
+          ptx::reg_fence(yc[c]);
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if ((tid & 31) == 0) ptx::mbar_arrive(&yfree);  // Yc, Ys may now take the next head
+        // this row tile's Yc and Ys may now take the next head
+        if ((tid & 31) == 0) ptx::mbar_arrive(&yfree[t]);
+        const float eg = ptx::ex2_approx(Gs[pb][i_rel]);  // carried-state decay
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t >= ntile) break;
-          const int i_rel = t * 128 + r;
-          uint8_t *xrow = xs + (i_rel >> 6) * kBlk;
+        for (int k4 = 0; k4 < kCH; ++k4) {
+          uint4 *p4 = reinterpret_cast<uint4 *>(xrow + sw128(i_rel & 63, (cg * kCH + k4) * 16));
+          float xv[8];
+          unpack16(*p4, xv, (__nv_bfloat16 *)nullptr);
 #pragma unroll
-          for (int k4 = 0; k4 < kCH; ++k4) {
-            uint4 *p4 = reinterpret_cast<uint4 *>(xrow + sw128(i_rel & 63, (cg * kCH + k4) * 16));
-            float xv[8];
-            unpack16(*p4, xv, (__nv_bfloat16 *)nullptr);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              xv[e] = fmaf(Dh, xv[e], __uint_as_float(yr[t][k4 >> 1][(k4 & 1) * 8 + e]));
-            *p4 = pack_io16(xv, (__nv_bfloat16 *)nullptr);
+          for (int e = 0; e < 8; ++e) {
+            const int c = k4 >> 1, ce = (k4 & 1) * 8 + e;
+            xv[e] = fmaf(Dh, xv[e], fmaf(eg, __uint_as_float(yc[c][ce]), __uint_as_float(ys[c][ce])));
           }
+          *p4 = pack_io16(xv, (__nv_bfloat16 *)nullptr);
         }
       }
       ptx::fence_async_smem();
