@@ -86,13 +86,12 @@ def algorithmic_flops(w: W.Workload) -> float:
     return per * w.batch * w.seqlen * w.nheads
 
 
-def kernel_names(w: W.Workload) -> list:
+def kernel_names(w: W.Workload, plan: dict | None = None) -> list:
     """Labels of the kernels ssd_forward launches for this workload, in
-    launch order.  The bf16 output pass is fwd_scan_chunk for P = 64,
-    S in {64, 128}, T in {128, 256} (the library's own dispatch rule), else
-    fwd_scan."""
+    launch order.  The bf16 output pass is the plan's output kernel:
+    fwd_scan_chunk (scan_kernel 1) or fwd_scan (0)."""
     names = list(KERNEL_NAMES[w.dtype])
-    if w.dtype == "bf16" and w.headdim == 64 and w.dstate in (64, 128) and w.chunk in (128, 256):
+    if w.dtype == "bf16" and plan is not None and plan["scan_kernel"] == 1:
         names[2] = "fwd_scan_chunk"
     return names
 
@@ -325,6 +324,18 @@ def run_ours(args, w):
         return ssd.forward_profiled(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"],
                                     w.chunk, ws, y, fin, events)
 
+    # launch plan: the timing autotuner's choice for this shape (once, before
+    # the warm-up; installed for every later call), or the cost model's
+    plan, tuned = None, False
+    if w.dtype == "bf16":
+        dims = ssd.dims_of(d["x"], d["B"], w.chunk)
+        if args.tune:
+            plan, _, _ = ssd.tune(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"],
+                                  chunk=w.chunk, reps=5, workspace=ws)
+            tuned = True
+        else:
+            plan = ssd.get_plan(dims)
+
     warm_ev = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
     for _ in range(args.warmup):
         flush()
@@ -359,7 +370,7 @@ def run_ours(args, w):
     clocks = sampler.stop() if sampler else None
 
     step_ms = [ev[i][0].elapsed_time(ev[i][n_l]) for i in range(args.steps)]
-    names = kernel_names(w)
+    names = kernel_names(w, plan)
     kern_ms = {names[j]: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1])
                                                 for i in range(args.steps))
                for j in range(n_l)}
@@ -410,7 +421,8 @@ def run_ours(args, w):
                    "ngroups": w.ngroups, "chunk": w.chunk, "h0": w.has_h0,
                    "l2": ("flushed before every step outside the timed events: 256 MB write"
                           + (" then 256 MB read (clean L2)" if args.flush == "write+read" else "")),
-                   "parallelism": f"replicas x{world} (independent batches per GPU)"},
+                   "parallelism": f"replicas x{world} (independent batches per GPU)",
+                   "plan": plan, "plan_source": "timing autotuner" if tuned else "cost model"},
         "achieved_tflops": algorithmic_flops(w) / (ms / 1e3) / 1e12,
         "achieved_gbs_compulsory": compulsory_bytes(w) / (ms / 1e3) / 1e9,
         "roofline_forward": {"bound": "hbm", "frac": compulsory_bytes(w) / (ms / 1e3) / 1e9 / peak,
@@ -552,6 +564,8 @@ def main(argv=None):
                          "separate: timed steps carry only start/end events and the "
                          "per-kernel split is taken from extra steps after the timed region")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--no-tune", dest="tune", action="store_false",
+                    help="use the cost-model launch plan instead of timing the candidates")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--flush", choices=["write+read", "write"], default="write+read",
                     help="L2 flush between steps (default: write a buffer, then read another)")

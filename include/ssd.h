@@ -21,8 +21,11 @@
  * - All tensor pointers are DEVICE pointers to dense row-major arrays in the
  *   layouts listed below; each must be 16-byte aligned.  The caller owns and
  *   allocates every buffer, including the workspace of ssd_forward.  The
- *   library never allocates, frees or synchronises, and keeps no state
- *   between calls.
+ *   library never allocates device memory, frees or synchronises (except
+ *   ssd_forward_tune, which times candidates and waits for them), and keeps
+ *   no state between calls other than the launch-plan table of
+ *   ssd_forward_set_plan / ssd_forward_tune and the scratch array of
+ *   ssd_forward_noalloc.
  * - `stream` is a cudaStream_t (NULL = legacy default stream); all work is
  *   enqueued on it and runs asynchronously.
  * - Arguments are validated before anything is launched; a rejected call
@@ -273,6 +276,72 @@ SSD_API ssd_status ssd_forward_noalloc(const ssd_dims *dims, ssd_dtype dtype, co
                                        const void *dt, const float *A, const void *B,
                                        const void *C, const float *D, const float *h0,
                                        void *y, float *final_state, void *stream);
+
+/* ---------------------------------------------------------------- plans
+ *
+ * Launch plan of the bf16 forward path (ssd_forward with SSD_BF16, and the
+ * calls built on it): the knobs that change how fast the kernels run, never
+ * what they compute.  No counterpart on the pages beyond their remark that
+ * an autotuner picks tile sizes, stages and occupancy per shape; these are
+ * this library's knobs:
+ *   chunk_state_heads  heads per work item of the chunk-jump kernel (they
+ *                      share one load of B; divides nheads / ngroups)
+ *   chunk_state_ctas   CTAs per SM of that kernel: 1 (up to 4 heads per
+ *                      item) or 2 (up to 2)
+ *   scan_kernel        output kernel: 0 = per-(chunk, head slice) kernel
+ *                      for every shape; 1 = kernel sharing one C B^T of a
+ *                      chunk between a slice of heads (P = 64, S in {64,
+ *                      128}, T in {128, 256})
+ *   scan_heads         heads per CTA of that output kernel (divides
+ *                      nheads / ngroups; at most 4, and heads * P <= 256, for
+ *                      kernel 0)
+ * Without an installed plan, ssd_forward uses the default plan of a cost
+ * model (ssd_forward_default_plan).  Installed plans live in one table per
+ * process, keyed by (device, dims, dtype), guarded by a mutex. */
+typedef struct {
+  int32_t chunk_state_heads, chunk_state_ctas, scan_kernel, scan_heads;
+} ssd_plan;
+
+/* Every valid plan for these dims: writes up to max_out plans to `out` (may
+ * be NULL when max_out is 0) and returns how many there are (0 for SSD_F32,
+ * which has no plan, and for invalid or unsupported dims).  Host-only; needs
+ * no GPU. */
+SSD_API int ssd_forward_plan_candidates(const ssd_dims *dims, ssd_dtype dtype, ssd_plan *out,
+                                        int max_out);
+
+/* The cost-model plan (SSD_ERR_UNSUPPORTED for SSD_F32; the usual codes for
+ * invalid dims).  Host-only. */
+SSD_API ssd_status ssd_forward_default_plan(const ssd_dims *dims, ssd_dtype dtype,
+                                            ssd_plan *out);
+
+/* The plan ssd_forward uses for these dims on the current device: the
+ * installed one, else the default. */
+SSD_API ssd_status ssd_forward_get_plan(const ssd_dims *dims, ssd_dtype dtype, ssd_plan *out);
+
+/* Install `plan` for these dims on the current device (SSD_ERR_INVALID_ARG
+ * unless it is one of the candidates; SSD_ERR_CUDA when there is no current
+ * device); plan == NULL removes the entry.  The
+ * table is read by every later forward call on the device with these dims,
+ * on any stream or thread; do not change it while such a call is being
+ * enqueued elsewhere if that call must see a particular plan. */
+SSD_API ssd_status ssd_forward_set_plan(const ssd_dims *dims, ssd_dtype dtype,
+                                        const ssd_plan *plan);
+
+/* Timing autotuner for these dims on the current device.  Arguments as for
+ * ssd_forward (SSD_BF16 only, else SSD_ERR_UNSUPPORTED).  Runs the forward
+ * pass once with the current plan, then times every chunk-jump plan and
+ * every output-kernel plan on `stream` (one untimed launch, then `reps`
+ * launches between two CUDA events, 1 <= reps <= 1000), picks the fastest
+ * of each (the two kernels are independent), installs the combination as by
+ * ssd_forward_set_plan, runs the forward pass once more with it, and waits
+ * for the stream.  On return y and final_state hold that last pass's
+ * results and *chosen (if not NULL) the installed plan.  Blocks the host and
+ * creates and destroys CUDA events: not for use inside a stream capture. */
+SSD_API ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                                    const void *dt, const float *A, const void *B,
+                                    const void *C, const float *D, const float *h0, void *y,
+                                    float *final_state, void *workspace, size_t ws_bytes,
+                                    int reps, void *stream, ssd_plan *chosen);
 
 #ifdef __cplusplus
 }

@@ -230,6 +230,64 @@ def forward_host_overlapped(x, dt, A, B, C, D, h0, chunk, workspace, y, final_st
         sh(h2d_stream), sh(d2h_stream)))
 
 
+def plan_candidates(d: _abi.SsdDims, io: int = 1) -> list[dict]:
+    """Every valid launch plan for dims `d` (ssd_forward_plan_candidates);
+    empty for fp32 I/O (io 0), which has none."""
+    lib = _abi.load()
+    n = lib.ssd_forward_plan_candidates(ctypes.byref(d), int(io), None, 0)
+    arr = (_abi.SsdPlan * max(n, 1))()
+    lib.ssd_forward_plan_candidates(ctypes.byref(d), int(io), arr, n)
+    return [arr[i].as_dict() for i in range(n)]
+
+
+def _plan_call(fn: str, d: _abi.SsdDims, io: int) -> dict:
+    p = _abi.SsdPlan()
+    _abi.check(fn, getattr(_abi.load(), fn)(ctypes.byref(d), int(io), ctypes.byref(p)))
+    return p.as_dict()
+
+
+def default_plan(d: _abi.SsdDims, io: int = 1) -> dict:
+    """The cost-model launch plan (ssd_forward_default_plan)."""
+    return _plan_call("ssd_forward_default_plan", d, io)
+
+
+def get_plan(d: _abi.SsdDims, io: int = 1) -> dict:
+    """The plan ssd_forward uses for `d` on the current device."""
+    return _plan_call("ssd_forward_get_plan", d, io)
+
+
+def set_plan(d: _abi.SsdDims, plan: dict | None, io: int = 1) -> None:
+    """Install `plan` (a dict of the four fields) for `d` on the current
+    device; None removes the entry (ssd_forward_set_plan)."""
+    ref = None
+    if plan is not None:
+        ref = ctypes.byref(_abi.SsdPlan(**{k: int(v) for k, v in plan.items()}))
+    _abi.check("ssd_forward_set_plan",
+               _abi.load().ssd_forward_set_plan(ctypes.byref(d), int(io), ref))
+
+
+def tune(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, reps: int = 5, workspace=None):
+    """Time every launch plan on these inputs and install the fastest
+    (ssd_forward_tune).  Returns (plan dict, y, final_state) of the final
+    pass with the chosen plan."""
+    lib = _abi.load()
+    d = dims_of(x, B, chunk)
+    io = _io_code(x)
+    if workspace is None:
+        workspace = torch.empty(lib.ssd_forward_workspace_size(ctypes.byref(d), io),
+                                dtype=torch.uint8, device=x.device)
+    y = torch.empty_like(x)
+    final_state = torch.empty((d.batch, d.nheads, d.headdim, d.dstate), dtype=torch.float32,
+                              device=x.device)
+    p = _abi.SsdPlan()
+    _abi.check("ssd_forward_tune", lib.ssd_forward_tune(
+        ctypes.byref(d), io, _ptr(x), _ptr(dt), _ptr(_f32(A, "A")), _ptr(B), _ptr(C),
+        _ptr(_f32(D, "D")), _ptr(_f32(h0, "h0")), _ptr(y), _ptr(final_state),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), int(reps), _stream(),
+        ctypes.byref(p)))
+    return p.as_dict(), y, final_state
+
+
 def device_error() -> None:
     """Synchronise the current stream and raise SsdError if a kernel of the
     library gave up a bounded wait since the last check."""

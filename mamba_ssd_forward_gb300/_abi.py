@@ -34,12 +34,25 @@ EXPORTS = (
     "ssd_decode_step",
     "ssd_forward_host_overlapped_workspace_size",
     "ssd_forward_host_overlapped",
+    "ssd_forward_plan_candidates",
+    "ssd_forward_default_plan",
+    "ssd_forward_get_plan",
+    "ssd_forward_set_plan",
+    "ssd_forward_tune",
 )
 
 
 class SsdDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in
                 ("batch", "seqlen", "nheads", "headdim", "dstate", "ngroups", "chunk")]
+
+
+class SsdPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("chunk_state_heads", "chunk_state_ctas", "scan_kernel", "scan_heads")]
+
+    def as_dict(self) -> dict:
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
 
 
 class SsdError(RuntimeError):
@@ -94,6 +107,14 @@ def load(path: str | None = None):
     lib.ssd_decode_step.argtypes = [dims_p, i32] + [vp] * 9
     lib.ssd_forward_noalloc.restype = i32
     lib.ssd_forward_noalloc.argtypes = [dims_p, i32] + [vp] * 9 + [vp]
+    plan_p = ctypes.POINTER(SsdPlan)
+    lib.ssd_forward_plan_candidates.restype = i32
+    lib.ssd_forward_plan_candidates.argtypes = [dims_p, i32, plan_p, i32]
+    for fn in ("ssd_forward_default_plan", "ssd_forward_get_plan", "ssd_forward_set_plan"):
+        getattr(lib, fn).restype = i32
+        getattr(lib, fn).argtypes = [dims_p, i32, plan_p]
+    lib.ssd_forward_tune.restype = i32
+    lib.ssd_forward_tune.argtypes = [dims_p, i32] + [vp] * 10 + [sz, i32, vp, plan_p]
     if path is None:
         _lib = lib
     return lib

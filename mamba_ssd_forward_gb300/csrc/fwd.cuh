@@ -4,6 +4,8 @@
 // and fwd_scan.cu.
 #pragma once
 
+#include <vector>
+
 #include "tc_common.cuh"
 
 namespace ssd {
@@ -20,6 +22,17 @@ cudaError_t launch_fwd_state_pass(const Dims &d, const void *dH, const float *ga
 // Heads per CTA of fwd_chunk_state (B shared by the heads of a group).
 int fwd_state_heads(const Dims &d);
 
+// Launch plans: knobs that change the speed of a kernel, never its results.
+// fwd_chunk_state: heads per work item and CTAs per SM.
+struct CsPlan {
+  int H, ctas;
+};
+CsPlan chunk_state_plan(const Dims &d);  // the cost-model choice
+bool chunk_state_plan_ok(const Dims &d, const CsPlan &plan);
+cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, const void *dt,
+                                   const float *A, void *dH, float *gamma, const CsPlan &plan,
+                                   cudaStream_t st);
+
 // y from x, B, C, dt, A, D and the bf16 per-chunk states.
 cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const void *C,
                             const void *dt, const float *A, const void *states, const float *D,
@@ -32,6 +45,18 @@ bool fwd_scan_chunk_supported(const Dims &d);
 cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
                                   const void *dt, const float *A, const void *states,
                                   const float *D, void *y, cudaStream_t st);
+// The same two output kernels with an explicit number of heads per CTA:
+// fwd_scan_heads(d) and fwd_scan_chunk_heads(d) are the cost-model choices,
+// the _ok functions say which values a launch accepts.
+int fwd_scan_chunk_heads(const Dims &d);
+bool fwd_scan_heads_ok(const Dims &d, int H);
+bool fwd_scan_chunk_heads_ok(const Dims &d, int hs);
+cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const void *C,
+                            const void *dt, const float *A, const void *states, const float *D,
+                            void *y, int H, cudaStream_t st);
+cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
+                                  const void *dt, const float *A, const void *states,
+                                  const float *D, void *y, int hs, cudaStream_t st);
 
 // Heads per CTA of the output pass: the largest divisor of nheads/ngroups
 // that is at most 4 and keeps heads * P <= 256 tensor-memory columns.
@@ -41,5 +66,24 @@ inline int fwd_scan_heads(const Dims &d) {
     if (d.hpg % h == 0) return h;
   return 1;
 }
+
+// Launch plan of the whole bf16 forward path (the public ssd_plan): the
+// chunk-jump plan, and the output kernel (1 = fwd_scan_chunk, 0 = fwd_scan)
+// with its heads per CTA.
+struct FwdPlan {
+  CsPlan cs;
+  int scan_kernel, scan_heads;
+};
+FwdPlan fwd_default_plan(const Dims &d);
+// The plan installed for d on the current device, else the default.
+FwdPlan fwd_current_plan(const Dims &d);
+// Valid chunk-jump plans and output-kernel plans (as FwdPlan with only the
+// relevant fields meaningful), appended to the vectors.
+void fwd_cs_candidates(const Dims &d, std::vector<CsPlan> *out);
+void fwd_scan_candidates(const Dims &d, std::vector<FwdPlan> *out);
+bool fwd_plan_ok(const Dims &d, const FwdPlan &p);
+// Install (or, p NULL, remove) the plan for d on the current device; false
+// when there is no current device.
+bool fwd_install_plan(const Dims &d, const FwdPlan *p);
 
 }  // namespace ssd

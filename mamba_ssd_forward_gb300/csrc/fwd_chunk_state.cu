@@ -364,9 +364,6 @@ int sm_count() {
 }
 
 
-struct CsPlan {
-  int H, ctas;  // heads per item, CTAs per SM
-};
 
 // Heads per item and CTAs per SM.  For each mode (one CTA per SM with
 // H * P <= 256 and up to 4 heads, or two with H * P <= 128 and up to 2, the
@@ -376,6 +373,8 @@ struct CsPlan {
 // of x per item).  Two CTAs per SM overlap one CTA's cumsum and epilogue with
 // the other's loads and MMAs, which pays once each CTA has several items (3
 // or more); with fewer, one CTA with larger items starts and drains faster.
+}  // namespace
+
 CsPlan chunk_state_plan(const Dims &d) {
   const int64_t n_st = (d.S + 127) / 128;
   const int64_t sms = sm_count();
@@ -403,14 +402,52 @@ CsPlan chunk_state_plan(const Dims &d) {
   return CsPlan{h1, 1};
 }
 
+namespace {
+
+// Shared-memory plan of a launch: ring stages and staged output tiles, or
+// nst < 2 when the plan does not fit.
+struct CsSmem {
+  int stage_bytes, nout, nst, smem;
+};
+CsSmem cs_smem(const Dims &d, const CsPlan &plan) {
+  const int nPb = (int)((d.P + 63) / 64);
+  CsSmem m;
+  m.stage_bytes = 2 * kBlk + plan.H * nPb * kBlk;
+  // dynamic shared memory (1 KB of it alignment slack) within 208 KB for
+  // one CTA per SM, 104 KB each for two; two staged dH tiles when they fit,
+  // else one
+  const int budget = (plan.ctas == 1 ? 207 : 103) * 1024;
+  const int out1 = nPb * kOutBlk;
+  m.nout = (2 * m.stage_bytes + 2 * out1 <= budget) ? 2 : 1;
+  m.nst = std::min(kMaxNST, (budget - m.nout * out1) / m.stage_bytes);
+  m.smem = m.nst * m.stage_bytes + m.nout * out1 + 1024;
+  return m;
+}
+
 }  // namespace
+
+bool chunk_state_plan_ok(const Dims &d, const CsPlan &plan) {
+  if (d.T > kRowThreads || (plan.ctas != 1 && plan.ctas != 2)) return false;
+  const int nPb = (int)((d.P + 63) / 64);
+  const int hmax = plan.ctas == 1 ? 4 : 2;
+  const int64_t cols = plan.ctas == 1 ? 256 : 128;
+  if (plan.H < 1 || plan.H > hmax || d.hpg % plan.H || plan.H * d.P > cols ||
+      plan.H * nPb > 4)
+    return false;
+  return cs_smem(d, plan).nst >= 2;
+}
 
 int fwd_state_heads(const Dims &d) { return chunk_state_plan(d).H; }
 
 cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, const void *dt,
                                    const float *A, void *dH, float *gamma, cudaStream_t st) {
-  if (d.T > kRowThreads) return cudaErrorInvalidValue;  // one token per row thread
-  const CsPlan plan = chunk_state_plan(d);
+  return launch_fwd_chunk_state(d, x, B, dt, A, dH, gamma, chunk_state_plan(d), st);
+}
+
+cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, const void *dt,
+                                   const float *A, void *dH, float *gamma, const CsPlan &plan,
+                                   cudaStream_t st) {
+  if (!chunk_state_plan_ok(d, plan)) return cudaErrorInvalidValue;
   const int H = plan.H;
   CUtensorMap tB, tx, tD;
   if (!make_tmap_bl(&tB, B, true, d.b, d.L, d.ng, d.S, kKB) ||
@@ -423,17 +460,8 @@ cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, 
     const uint32_t box[3] = {64u, 128u, 1u};
     if (!make_tmap_sw128(&tD, dH, true, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  const int nPb = (int)((d.P + 63) / 64);
-  const int stage_bytes = 2 * kBlk + H * nPb * kBlk;
-  // dynamic shared memory (1 KB of it alignment slack) within 208 KB for
-  // one CTA per SM, 104 KB each for two; two staged dH tiles when they fit,
-  // else one
-  const int budget = (plan.ctas == 1 ? 207 : 103) * 1024;
-  const int out1 = nPb * kOutBlk;
-  const int nout = (2 * stage_bytes + 2 * out1 <= budget) ? 2 : 1;
-  const int nst = std::min(kMaxNST, (budget - nout * out1) / stage_bytes);
-  if (nst < 2) return cudaErrorInvalidValue;
-  const int smem = nst * stage_bytes + nout * out1 + 1024;
+  const CsSmem m = cs_smem(d, plan);
+  const int nst = m.nst, nout = m.nout, smem = m.smem;
   auto kernel = plan.ctas == 1 ? fwd_chunk_state_bf16<1> : fwd_chunk_state_bf16<2>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

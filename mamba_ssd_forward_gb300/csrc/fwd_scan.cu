@@ -382,10 +382,42 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
 
 }  // namespace
 
+namespace {
+
+// Shared memory of a launch with H heads per CTA: two phase-1 stages and nX
+// x stages, within the 227 KB per CTA less the static arrays.
+struct ScanSmem {
+  int nX, smem;
+};
+ScanSmem scan_smem(const Dims &d, int H) {
+  const int nBr = (int)((std::min<int64_t>(d.T, 256) + 127) / 128);
+  const int nPb = (int)((d.P + 63) / 64);
+  const int st1 = kBlk * 2 + nBr * kBlk * 2 + H * nPb * kBlk;
+  const int st2x = nPb * kBlk;
+  const int budget = 212 * 1024 - 2 * st1;
+  ScanSmem m;
+  m.nX = std::max(2, std::min(kMaxX, budget / st2x));
+  m.smem = 2 * st1 + m.nX * st2x + 1024;
+  return m;
+}
+
+}  // namespace
+
+bool fwd_scan_heads_ok(const Dims &d, int H) {
+  if (H < 1 || H > kMaxH || d.hpg % H || H * d.P > 256) return false;
+  return scan_smem(d, H).smem <= 213 * 1024;
+}
+
 cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const void *C,
                             const void *dt, const float *A, const void *states, const float *D,
                             void *y, cudaStream_t st) {
-  const int H = fwd_scan_heads(d);
+  return launch_fwd_scan(d, x, B, C, dt, A, states, D, y, fwd_scan_heads(d), st);
+}
+
+cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const void *C,
+                            const void *dt, const float *A, const void *states, const float *D,
+                            void *y, int H, cudaStream_t st) {
+  if (!fwd_scan_heads_ok(d, H)) return cudaErrorInvalidValue;
   CUtensorMap tC, tB, tx, tS;
   if (!make_tmap_bl(&tC, C, true, d.b, d.L, d.ng, d.S, 128) ||
       !make_tmap_bl(&tB, B, true, d.b, d.L, d.ng, d.S, 128) ||
@@ -397,15 +429,8 @@ cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const v
     const uint32_t box[3] = {64u, 64u, 1u};
     if (!make_tmap_sw128(&tS, states, true, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  const int nBr = (int)((std::min<int64_t>(d.T, 256) + 127) / 128);
-  const int nPb = (int)((d.P + 63) / 64);
-  const int st1 = kBlk * 2 + nBr * kBlk * 2 + H * nPb * kBlk;
-  const int st2x = nPb * kBlk;
-  // dynamic shared memory: two phase-1 stages and nX x stages, within the
-  // 227 KB per CTA less the static arrays
-  const int budget = 212 * 1024 - 2 * st1;
-  const int nX = std::max(2, std::min(kMaxX, budget / st2x));
-  const int smem = 2 * st1 + nX * st2x + 1024;
+  const ScanSmem m = scan_smem(d, H);
+  const int nX = m.nX, smem = m.smem;
   cudaError_t e =
       cudaFuncSetAttribute(fwd_scan_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

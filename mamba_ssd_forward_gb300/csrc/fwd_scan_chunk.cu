@@ -577,11 +577,21 @@ int fwd_scan_chunk_heads(const Dims &d) {
   return best;
 }
 
+bool fwd_scan_chunk_heads_ok(const Dims &d, int hs) {
+  return fwd_scan_chunk_supported(d) && hs >= 1 && hs <= d.hpg && d.hpg % hs == 0;
+}
+
 cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
                                   const void *dt, const float *A, const void *states,
                                   const float *D, void *y, cudaStream_t st) {
   if (!fwd_scan_chunk_supported(d)) return cudaErrorInvalidValue;
-  const int hs = fwd_scan_chunk_heads(d);
+  return launch_fwd_scan_chunk(d, x, B, C, dt, A, states, D, y, fwd_scan_chunk_heads(d), st);
+}
+
+cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
+                                  const void *dt, const float *A, const void *states,
+                                  const float *D, void *y, int hs, cudaStream_t st) {
+  if (!fwd_scan_chunk_heads_ok(d, hs)) return cudaErrorInvalidValue;
   CUtensorMap tC, tB, tx, tS, tY;
   if (!make_tmap_bl(&tC, C, true, d.b, d.L, d.ng, d.S, 128) ||
       !make_tmap_bl(&tB, B, true, d.b, d.L, d.ng, d.S, 128) ||

@@ -2,6 +2,7 @@
 // launch sequence.  Every computation happens in the kernels; this file only
 // checks arguments and enqueues launches on the caller's stream.
 #include <cstdint>
+#include <vector>
 
 #include "fwd.cuh"
 #include "ssd_internal.cuh"
@@ -83,6 +84,45 @@ WsLayout ws_layout(const Dims &d, ssd_dtype t) {
 }
 
 size_t io_size(ssd_dtype t) { return t == SSD_BF16 ? 2 : 4; }
+
+cudaError_t launch_scan(const Dims &d, const ssd::FwdPlan &plan, const void *x, const void *B,
+                        const void *C, const void *dt, const float *A, const void *states,
+                        const float *D, void *y, cudaStream_t st) {
+  return plan.scan_kernel
+             ? ssd::launch_fwd_scan_chunk(d, x, B, C, dt, A, states, D, y, plan.scan_heads, st)
+             : ssd::launch_fwd_scan(d, x, B, C, dt, A, states, D, y, plan.scan_heads, st);
+}
+
+ssd_plan to_public(const ssd::FwdPlan &p) {
+  ssd_plan o;
+  o.chunk_state_heads = p.cs.H;
+  o.chunk_state_ctas = p.cs.ctas;
+  o.scan_kernel = p.scan_kernel;
+  o.scan_heads = p.scan_heads;
+  return o;
+}
+ssd::FwdPlan from_public(const ssd_plan &p) {
+  ssd::FwdPlan o;
+  o.cs = ssd::CsPlan{p.chunk_state_heads, p.chunk_state_ctas};
+  o.scan_kernel = p.scan_kernel;
+  o.scan_heads = p.scan_heads;
+  return o;
+}
+
+// Mean milliseconds per launch of `launch` over reps launches (after one
+// untimed launch), timed with two events on st.
+template <typename F>
+cudaError_t time_launches(F launch, int reps, cudaStream_t st, cudaEvent_t e0, cudaEvent_t e1,
+                          float *ms) {
+  cudaError_t e = launch();
+  if (e == cudaSuccess) e = cudaEventRecord(e0, st);
+  for (int i = 0; i < reps && e == cudaSuccess; ++i) e = launch();
+  if (e == cudaSuccess) e = cudaEventRecord(e1, st);
+  if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(ms, e0, e1);
+  if (e == cudaSuccess) *ms /= (float)reps;
+  return e;
+}
 
 // Device workspace of ssd_forward_host: the forward's own workspace, then a
 // device copy of every input and output, each 256-byte aligned.
@@ -244,14 +284,12 @@ ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype, const voi
     void *sts = ws + w.states;
     void *dH = ws + w.dstates;
     float *gam = reinterpret_cast<float *>(ws + w.G);
-    if (e == cudaSuccess) e = ssd::launch_fwd_chunk_state(d, x, B, dt, A, dH, gam, st);
+    const ssd::FwdPlan plan = ssd::fwd_current_plan(d);
+    if (e == cudaSuccess) e = ssd::launch_fwd_chunk_state(d, x, B, dt, A, dH, gam, plan.cs, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
     if (e == cudaSuccess) e = ssd::launch_fwd_state_pass(d, dH, gam, h0, sts, final_state, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
-    if (e == cudaSuccess)
-      e = ssd::fwd_scan_chunk_supported(d)
-              ? ssd::launch_fwd_scan_chunk(d, x, B, C, dt, A, sts, D, y, st)
-              : ssd::launch_fwd_scan(d, x, B, C, dt, A, sts, D, y, st);
+    if (e == cudaSuccess) e = launch_scan(d, plan, x, B, C, dt, A, sts, D, y, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
   } else {
     float *G = reinterpret_cast<float *>(ws + w.G);
@@ -268,6 +306,123 @@ ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype, const voi
   }
   if (n_launches) *n_launches = launched;
   return from_cuda(e);
+}
+
+int ssd_forward_plan_candidates(const ssd_dims *dims, ssd_dtype dtype, ssd_plan *out,
+                                int max_out) {
+  Dims d;
+  if (dtype != SSD_BF16 || check_dims(dims, &d) != SSD_OK || max_out < 0 ||
+      (max_out > 0 && !out))
+    return 0;
+  std::vector<ssd::CsPlan> cs;
+  std::vector<ssd::FwdPlan> sc;
+  ssd::fwd_cs_candidates(d, &cs);
+  ssd::fwd_scan_candidates(d, &sc);
+  int n = 0;
+  for (const ssd::CsPlan &c : cs)
+    for (ssd::FwdPlan p : sc) {
+      p.cs = c;
+      if (n < max_out) out[n] = to_public(p);
+      ++n;
+    }
+  return n;
+}
+
+ssd_status ssd_forward_default_plan(const ssd_dims *dims, ssd_dtype dtype, ssd_plan *out) {
+  Dims d;
+  const ssd_status s = check_dims(dims, &d);
+  if (s != SSD_OK) return s;
+  if (!valid_dtype(dtype) || !out) return SSD_ERR_INVALID_ARG;
+  if (dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
+  *out = to_public(ssd::fwd_default_plan(d));
+  return SSD_OK;
+}
+
+ssd_status ssd_forward_get_plan(const ssd_dims *dims, ssd_dtype dtype, ssd_plan *out) {
+  Dims d;
+  const ssd_status s = check_dims(dims, &d);
+  if (s != SSD_OK) return s;
+  if (!valid_dtype(dtype) || !out) return SSD_ERR_INVALID_ARG;
+  if (dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
+  *out = to_public(ssd::fwd_current_plan(d));
+  return SSD_OK;
+}
+
+ssd_status ssd_forward_set_plan(const ssd_dims *dims, ssd_dtype dtype, const ssd_plan *plan) {
+  Dims d;
+  const ssd_status s = check_dims(dims, &d);
+  if (s != SSD_OK) return s;
+  if (!valid_dtype(dtype)) return SSD_ERR_INVALID_ARG;
+  if (dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
+  if (!plan) return ssd::fwd_install_plan(d, nullptr) ? SSD_OK : SSD_ERR_CUDA;
+  const ssd::FwdPlan p = from_public(*plan);
+  if (!ssd::fwd_plan_ok(d, p)) return SSD_ERR_INVALID_ARG;
+  return ssd::fwd_install_plan(d, &p) ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
+                            const float *A, const void *B, const void *C, const float *D,
+                            const float *h0, void *y, float *final_state, void *workspace,
+                            size_t ws_bytes, int reps, void *stream, ssd_plan *chosen) {
+  Dims d;
+  ssd_status s = check_dims(dims, &d);
+  if (s != SSD_OK) return s;
+  if (!valid_dtype(dtype) || !req(x) || !req(dt) || !req(A) || !req(B) || !req(C) ||
+      !opt(D) || !opt(h0) || !req(y) || !opt(final_state) || !workspace ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) || reps < 1 || reps > 1000)
+    return SSD_ERR_INVALID_ARG;
+  if (dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
+  const WsLayout w = ws_layout(d, dtype);
+  if (ws_bytes < w.total) return SSD_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  // the start states the output kernels read, from one pass with the
+  // current plan
+  s = ssd_forward(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, workspace, ws_bytes,
+                  stream);
+  if (s != SSD_OK) return s;
+  char *ws = static_cast<char *>(workspace);
+  void *sts = ws + w.states;
+  void *dH = ws + w.dstates;
+  float *gam = reinterpret_cast<float *>(ws + w.G);
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  cudaError_t e = cudaEventCreate(&e0);
+  if (e == cudaSuccess) e = cudaEventCreate(&e1);
+  ssd::FwdPlan best = ssd::fwd_current_plan(d);
+  std::vector<ssd::CsPlan> cs;
+  std::vector<ssd::FwdPlan> sc;
+  ssd::fwd_cs_candidates(d, &cs);
+  ssd::fwd_scan_candidates(d, &sc);
+  float best_ms = 3.0e38f;
+  for (size_t i = 0; i < cs.size() && e == cudaSuccess; ++i) {
+    float ms = 0.f;
+    e = time_launches(
+        [&] { return ssd::launch_fwd_chunk_state(d, x, B, dt, A, dH, gam, cs[i], st); }, reps,
+        st, e0, e1, &ms);
+    if (e == cudaSuccess && ms < best_ms) {
+      best_ms = ms;
+      best.cs = cs[i];
+    }
+  }
+  best_ms = 3.0e38f;
+  for (size_t i = 0; i < sc.size() && e == cudaSuccess; ++i) {
+    float ms = 0.f;
+    e = time_launches([&] { return launch_scan(d, sc[i], x, B, C, dt, A, sts, D, y, st); },
+                      reps, st, e0, e1, &ms);
+    if (e == cudaSuccess && ms < best_ms) {
+      best_ms = ms;
+      best.scan_kernel = sc[i].scan_kernel;
+      best.scan_heads = sc[i].scan_heads;
+    }
+  }
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  if (e != cudaSuccess || !ssd::fwd_install_plan(d, &best)) return SSD_ERR_CUDA;
+  s = ssd_forward(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, workspace, ws_bytes,
+                  stream);
+  if (s != SSD_OK) return s;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
+  if (chosen) *chosen = to_public(best);
+  return SSD_OK;
 }
 
 size_t ssd_forward_host_workspace_size(const ssd_dims *dims, ssd_dtype dtype, int has_D,

@@ -199,3 +199,67 @@ def test_host_overlapped_sizes_and_rejections(lib):
                                            None, None) == 1  # workspace too small
     assert lib.ssd_forward_host_overlapped(ctypes.byref(dims(headdim=144)), 1, *host, ok, ws, 2,
                                            None, None, None) == 2
+
+
+def _dims(b, L, nh, P, S, ng, T):
+    from mamba_ssd_forward_gb300 import _abi
+    return _abi.SsdDims(b, L, nh, P, S, ng, T)
+
+
+@pytest.mark.parametrize("shape", [
+    (4, 2048, 24, 64, 128, 1, 256),   # 130M-like layer
+    (2, 4096, 80, 64, 128, 1, 256),   # 2.7B-like layer
+    (1, 32768, 48, 64, 256, 8, 256),  # long context, S = 256
+    (2, 500, 12, 32, 64, 3, 128),     # P = 32: only the per-slice output kernel
+    (1, 300, 2, 128, 256, 1, 256),    # largest P and S
+])
+def test_plan_candidates_are_valid_and_hold_the_default(lib, shape):
+    import mamba_ssd_forward_gb300 as m
+    b, L, nh, P, S, ng, T = shape
+    d = _dims(*shape)
+    cands = m.plan_candidates(d)
+    assert cands
+    hpg = nh // ng
+    chunk_kernel_ok = P == 64 and S in (64, 128) and T in (128, 256)
+    for c in cands:
+        assert c["chunk_state_ctas"] in (1, 2)
+        hmax = 4 if c["chunk_state_ctas"] == 1 else 2
+        assert 1 <= c["chunk_state_heads"] <= hmax and hpg % c["chunk_state_heads"] == 0
+        assert c["chunk_state_heads"] * P <= (256 if c["chunk_state_ctas"] == 1 else 128)
+        assert c["scan_kernel"] in (0, 1) and hpg % c["scan_heads"] == 0
+        if c["scan_kernel"] == 1:
+            assert chunk_kernel_ok
+        else:
+            assert c["scan_heads"] <= 4 and c["scan_heads"] * P <= 256
+    assert len({tuple(c.values()) for c in cands}) == len(cands)
+    default = m.default_plan(d)
+    assert default in cands
+    assert (default["scan_kernel"] == 1) == chunk_kernel_ok
+    # without an installed plan the forward pass uses the default
+    assert m.get_plan(d) == default
+
+
+def test_plan_rejections(lib):
+    import mamba_ssd_forward_gb300 as m
+    from mamba_ssd_forward_gb300 import _abi
+    d = _dims(2, 4096, 80, 64, 128, 1, 256)
+    assert m.plan_candidates(d, io=0) == []  # fp32 I/O has no plan
+    with pytest.raises(_abi.SsdError) as e:
+        m.default_plan(d, io=0)
+    assert e.value.code == _abi.SSD_ERR_UNSUPPORTED
+    assert m.plan_candidates(_dims(2, 4096, 80, 64, 128, 3, 256)) == []  # nh % ng
+    assert m.plan_candidates(_dims(2, 4096, 80, 64, 128, 1, 100)) == []  # chunk
+    bad = [
+        {"chunk_state_heads": 3, "chunk_state_ctas": 1, "scan_kernel": 1, "scan_heads": 20},
+        {"chunk_state_heads": 4, "chunk_state_ctas": 2, "scan_kernel": 1, "scan_heads": 20},
+        {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 1, "scan_heads": 3},
+        {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 0, "scan_heads": 8},
+        {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 2, "scan_heads": 1},
+    ]
+    for p in bad:
+        assert p not in m.plan_candidates(d)
+        with pytest.raises(_abi.SsdError) as e:
+            m.set_plan(d, p)
+        assert e.value.code == _abi.SSD_ERR_INVALID_ARG
+    rc = lib.ssd_forward_tune(ctypes.byref(d), 1, *([None] * 10), 0, 5, None, None)
+    assert rc == _abi.SSD_ERR_INVALID_ARG

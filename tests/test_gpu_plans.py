@@ -1,0 +1,92 @@
+"""GPU checks of the launch plans and the timing autotuner: every candidate
+plan gives results within the parity tolerance of the oracle, plans that
+only change heads per CTA of the output kernel give identical bits, and the
+tuner installs one of the candidates."""
+import numpy as np
+import pytest
+import torch
+
+from parity import check_io, device_inputs, make, oracle_run, to64
+
+pytestmark = pytest.mark.gpu
+
+from mamba_ssd_forward_gb300 import inputs as W  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def ssd():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import oracle
+    from mamba_ssd_forward_gb300 import build
+    build.build()
+    oracle.build()
+    import mamba_ssd_forward_gb300 as m
+    return m
+
+
+# 8 heads per group: several chunk-jump plans and output-kernel slices
+CASE = W.Workload("bf16_plans", 2, 700, 8, 64, 128, 1, 256, "bf16", True)
+
+
+@pytest.fixture(scope="module")
+def case(ssd):
+    inp = make(CASE)
+    ref = oracle_run(CASE, inp)
+    dev = device_inputs(inp)
+    d = ssd.dims_of(dev["x"], dev["B"], CASE.chunk)
+    yield inp, ref, dev, d
+    ssd.set_plan(d, None)
+
+
+def _run(ssd, dev):
+    y, fin = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                         dev["h0"], chunk=CASE.chunk)
+    ssd.device_error()
+    return y, fin
+
+
+def test_every_candidate_plan_matches_the_oracle(ssd, case):
+    inp, ref, dev, d = case
+    cands = ssd.plan_candidates(d)
+    assert len(cands) > 4
+    by_kernel = {}
+    for p in cands:
+        ssd.set_plan(d, p)
+        assert ssd.get_plan(d) == p
+        y, fin = _run(ssd, dev)
+        check_io(to64(y), ref["y"], "bf16", f"y {p}")
+        check_io(to64(fin), ref["final_state"], "bf16", f"final_state {p}")
+        key = (p["chunk_state_heads"], p["chunk_state_ctas"], p["scan_kernel"])
+        by_kernel.setdefault(key, []).append(y.clone())
+    # heads per CTA of the output kernel only change the launch shape
+    for ys in by_kernel.values():
+        for y in ys[1:]:
+            assert torch.equal(y, ys[0])
+    ssd.set_plan(d, None)
+    assert ssd.get_plan(d) == ssd.default_plan(d)
+
+
+def test_tune_installs_a_candidate(ssd, case):
+    inp, ref, dev, d = case
+    plan, y, fin = ssd.tune(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                            dev["h0"], chunk=CASE.chunk, reps=3)
+    ssd.device_error()
+    assert plan in ssd.plan_candidates(d)
+    assert ssd.get_plan(d) == plan
+    check_io(to64(y), ref["y"], "bf16", "tuned y")
+    check_io(to64(fin), ref["final_state"], "bf16", "tuned final_state")
+    y2, _ = _run(ssd, dev)
+    assert torch.equal(y2, y)  # later calls use the installed plan
+    ssd.set_plan(d, None)
+
+
+def test_tune_rejects_fp32(ssd):
+    from mamba_ssd_forward_gb300 import _abi
+    w = W.Workload("fp32_plans", 1, 256, 2, 64, 64, 1, 128, "fp32", False)
+    dev = device_inputs(make(w))
+    with pytest.raises(_abi.SsdError) as e:
+        ssd.tune(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], None,
+                 chunk=w.chunk)
+    assert e.value.code == _abi.SSD_ERR_UNSUPPORTED
+    assert np.isfinite(to64(dev["x"])).all()
