@@ -89,9 +89,10 @@ def algorithmic_flops(w: W.Workload) -> float:
 def kernel_names(w: W.Workload, plan: dict | None = None) -> list:
     """Labels of the kernels ssd_forward launches for this workload, in
     launch order.  The bf16 output pass is the plan's output kernel:
-    fwd_scan_chunk (scan_kernel 1) or fwd_scan (0)."""
+    fwd_scan_chunk (scan_kernel 1, or 2: one row tile per CTA) or fwd_scan
+    (0)."""
     names = list(KERNEL_NAMES[w.dtype])
-    if w.dtype == "bf16" and plan is not None and plan["scan_kernel"] == 1:
+    if w.dtype == "bf16" and plan is not None and plan["scan_kernel"] in (1, 2):
         names[2] = "fwd_scan_chunk"
     return names
 

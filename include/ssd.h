@@ -288,10 +288,12 @@ SSD_API ssd_status ssd_forward_noalloc(const ssd_dims *dims, ssd_dtype dtype, co
  *                      share one load of B; divides nheads / ngroups)
  *   chunk_state_ctas   CTAs per SM of that kernel: 1 (up to 4 heads per
  *                      item) or 2 (up to 2)
- *   scan_kernel        output kernel: 0 = per-(chunk, head slice) kernel
- *                      for every shape; 1 = kernel sharing one C B^T of a
- *                      chunk between a slice of heads (P = 64, S in {64,
- *                      128}, T in {128, 256})
+ *   scan_kernel        output kernel: 0 = per-(128-row tile, chunk, head
+ *                      slice) kernel for every shape; 1 = kernel sharing one
+ *                      C B^T of a whole chunk between a slice of heads (P =
+ *                      64, S in {64, 128}, T in {128, 256}); 2 = the same
+ *                      with one 128-row tile of the chunk per CTA (P = 64,
+ *                      S in {64, 128, 256}, T = 256)
  *   scan_heads         heads per CTA of that output kernel (divides
  *                      nheads / ngroups; at most 4, and heads * P <= 256, for
  *                      kernel 0)

@@ -48,15 +48,18 @@ cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, c
 // The same two output kernels with an explicit number of heads per CTA:
 // fwd_scan_heads(d) and fwd_scan_chunk_heads(d) are the cost-model choices,
 // the _ok functions say which values a launch accepts.
-int fwd_scan_chunk_heads(const Dims &d);
+// split: one 128-row tile of a chunk per CTA (T = 256; S up to 256).
+bool fwd_scan_chunk_split_supported(const Dims &d);
+int fwd_scan_chunk_heads(const Dims &d, bool split);
 bool fwd_scan_heads_ok(const Dims &d, int H);
-bool fwd_scan_chunk_heads_ok(const Dims &d, int hs);
+bool fwd_scan_chunk_heads_ok(const Dims &d, int hs, bool split);
 cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const void *C,
                             const void *dt, const float *A, const void *states, const float *D,
                             void *y, int H, cudaStream_t st);
 cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
                                   const void *dt, const float *A, const void *states,
-                                  const float *D, void *y, int hs, cudaStream_t st);
+                                  const float *D, void *y, int hs, bool split,
+                                  cudaStream_t st);
 
 // Heads per CTA of the output pass: the largest divisor of nheads/ngroups
 // that is at most 4 and keeps heads * P <= 256 tensor-memory columns.
@@ -68,8 +71,8 @@ inline int fwd_scan_heads(const Dims &d) {
 }
 
 // Launch plan of the whole bf16 forward path (the public ssd_plan): the
-// chunk-jump plan, and the output kernel (1 = fwd_scan_chunk, 0 = fwd_scan)
-// with its heads per CTA.
+// chunk-jump plan, and the output kernel (0 = fwd_scan, 1 = fwd_scan_chunk,
+// 2 = fwd_scan_chunk with one row tile per CTA) with its heads per CTA.
 struct FwdPlan {
   CsPlan cs;
   int scan_kernel, scan_heads;

@@ -92,9 +92,12 @@ struct ChunkArgs {
   __nv_bfloat16 *y;
   int *err;
   int L, nh, S, hpg, T, nc, hs;
+  // 1: one 128-row tile of the chunk per CTA (blockIdx.y = chunk * tiles +
+  // tile), B streamed through a two-slot ring in the second head buffer
+  // during phase 1; 0: both row tiles per CTA, B resident
+  int split;
   // shared-memory layout (byte offsets from the 1024-aligned base)
   int off_C, off_B, off_hx0, off_hx1;
-  int hx_bytes;  // states (S x P) followed by x (T x P), bf16
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -105,7 +108,8 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
                     const __grid_constant__ CUtensorMap tm_y, const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t p1_full[2], sc_done, pack_done, hx_full[2], hx_empty[2],
+  __shared__ __align__(8) uint64_t p1_full[2], p1_empty[2], sc_done, pack_done, hx_full[2],
+      hx_empty[2],
       pm_full[kNP], pm_empty[kNP], ydone, yfree[2];
   __shared__ uint32_t tmem_slot;
   // per head (double-buffered by head parity): G in log2 units, dt, and the
@@ -118,18 +122,27 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
 
   const int L = a.L, nh = a.nh, S = a.S, T = a.T, nc = a.nc, hs = a.hs;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int k = blockIdx.y, b = blockIdx.z;
+  const int split = a.split;
+  const int ntile_all = T / 128;
+  const int k = split ? blockIdx.y / ntile_all : blockIdx.y, b = blockIdx.z;
+  // the row tiles [t_lo, t_hi) of the chunk this CTA computes
+  const int t_lo = split ? blockIdx.y % ntile_all : 0;
+  const int t_hi = split ? t_lo + 1 : ntile_all;
   const int hbase = blockIdx.x * hs, g = hbase / a.hpg;
   const int tok0 = k * T;
   const int valid = min(T, L - tok0);
-  const int ntile = T / 128;
   const int nsb = S / 64;
   const int st_bytes = S * kP * 2;
+  // a head's tiles: its start state, then x rows 0 .. 128 t_hi - 1
+  const int hx_bytes = st_bytes + t_hi * 2 * kBlk;
+  // C rows of this CTA's tiles, per 64-wide block of S
+  auto c_off = [&](int t, int sb) { return a.off_C + ((t - t_lo) * nsb + sb) * kTile; };
   const uint32_t ncols = 512;
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&p1_full[i], 1);
+      ptx::mbar_init(&p1_empty[i], 1);
       ptx::mbar_init(&hx_full[i], 1);
       ptx::mbar_init(&hx_empty[i], 2);  // MMA commit + the y store has read the tile
     }
@@ -154,33 +167,45 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const bool leader = (tid & 31) == 0;
-  const bool alias_hx1 = a.off_hx1 == a.off_B;  // second head buffer reuses B's space
+  // second head buffer reuses B's space (resident B) or holds the B ring
+  const bool alias_hx1 = split || a.off_hx1 == a.off_B;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (leader) {
-      // phase 1: C (rows of the chunk, per row tile) and B (rows 0..T-1),
-      // one 64-wide block of S at a time
-      for (int sb = 0; sb < nsb; ++sb) {
-        ptx::mbar_arrive_expect_tx(&p1_full[sb], 2 * ntile * kTile);
-        for (int t = 0; t < ntile; ++t) {
-          ptx::tma_load_4d(smem + a.off_C + (t * nsb + sb) * kTile, &tm_C, sb * 64, g,
-                           tok0 + t * 128, b, &p1_full[sb]);
-          ptx::tma_load_4d(smem + a.off_B + (sb * ntile + t) * kTile, &tm_B, sb * 64, g,
-                           tok0 + t * 128, b, &p1_full[sb]);
-        }
+    // phase 1, one 64-wide block sb of S at a time: C rows of this CTA's
+    // tiles and B rows 0 .. 128 t_hi - 1.  Resident B: every block at once.
+    // Split: B block sb into ring slot sb & 1 (in the second head buffer),
+    // once the MMAs of block sb - 2 are done; blocks 2 and up are issued
+    // after head 0's loads, which need no slot
+    auto load_p1 = [&](int sb) {
+      const int slot = split ? (sb & 1) : sb;
+      if (split && sb >= 2) ptx::mbar_wait(&p1_empty[slot], ((sb >> 1) - 1) & 1, a.err, 120);
+      if (leader) {
+        ptx::mbar_arrive_expect_tx(&p1_full[slot], (t_hi - t_lo + t_hi) * kTile);
+        for (int t = t_lo; t < t_hi; ++t)
+          ptx::tma_load_4d(smem + c_off(t, sb), &tm_C, sb * 64, g, tok0 + t * 128, b,
+                           &p1_full[slot]);
+        uint8_t *bdst = split ? smem + a.off_hx1 + slot * 2 * kTile
+                              : smem + a.off_B + sb * ntile_all * kTile;
+        for (int t = 0; t < t_hi; ++t)
+          ptx::tma_load_4d(bdst + t * kTile, &tm_B, sb * 64, g, tok0 + t * 128, b,
+                           &p1_full[slot]);
       }
-    }
-    __syncwarp();
+      __syncwarp();
+    };
+    const int nsb_first = split ? min(nsb, 2) : nsb;
+    for (int sb = 0; sb < nsb_first; ++sb) load_p1(sb);
     for (int q = 0; q < hs; ++q) {
       const int buf = q & 1;
+      if (q == 1)
+        for (int sb = nsb_first; sb < nsb; ++sb) load_p1(sb);
       ptx::mbar_wait(&hx_empty[buf], ((q >> 1) & 1) ^ 1, a.err, 121);
       if (q == 1 && alias_hx1) ptx::mbar_wait(&sc_done, 0, a.err, 122);
       if (leader) {
         uint8_t *hx = smem + (buf ? a.off_hx1 : a.off_hx0);
-        ptx::mbar_arrive_expect_tx(&hx_full[buf], a.hx_bytes);
+        ptx::mbar_arrive_expect_tx(&hx_full[buf], hx_bytes);
         // x rows of the chunk (64-token blocks, p contiguous)
-        for (int jb = 0; jb < T / 64; ++jb)
+        for (int jb = 0; jb < 2 * t_hi; ++jb)
           ptx::tma_load_4d(hx + st_bytes + jb * kBlk, &tm_x, 0, hbase + q, tok0 + jb * 64, b,
                            &hx_full[buf]);
         // the start state comes from the preceding kernel (the state pass),
@@ -192,16 +217,20 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       }
       __syncwarp();
     }
+    if (hs == 1)
+      for (int sb = nsb_first; sb < nsb; ++sb) load_p1(sb);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // phase 1: Sc = C B^T; row tile t needs columns j < 128 (t + 1)
     for (int sb = 0; sb < nsb; ++sb) {
-      ptx::mbar_wait(&p1_full[sb], 0, a.err, 123);
+      const int slot = split ? (sb & 1) : sb;
+      ptx::mbar_wait(&p1_full[slot], split ? (sb >> 1) & 1 : 0, a.err, 123);
       ptx::tc_fence_after();
       if (leader) {
-        const uint32_t b0 = ptx::smem_u32(smem + a.off_B + sb * ntile * kTile);
-        for (int t = 0; t < ntile; ++t) {
-          const uint32_t c0 = ptx::smem_u32(smem + a.off_C + (t * nsb + sb) * kTile);
+        const uint32_t b0 = ptx::smem_u32(split ? smem + a.off_hx1 + slot * 2 * kTile
+                                                : smem + a.off_B + sb * ntile_all * kTile);
+        for (int t = t_lo; t < t_hi; ++t) {
+          const uint32_t c0 = ptx::smem_u32(smem + c_off(t, sb));
           const uint32_t idS = ptx::idesc_bf16(128, 128 * (t + 1), false, false);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
@@ -210,6 +239,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
             ptx::mma_ss<false>(tmem + scf_col(t), cd, bd, idS, (sb | kk) ? 1u : 0u);
           }
         }
+        if (split) ptx::mma_commit(&p1_empty[slot]);
       }
       __syncwarp();
     }
@@ -226,12 +256,12 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       ptx::mbar_wait(&hx_full[buf], (q >> 1) & 1, a.err, 124);
       // Yc = C h_q^T for each row tile, once the previous head's epilogue
       // has read that tile's accumulators
-      for (int t = 0; t < ntile; ++t) {
+      for (int t = t_lo; t < t_hi; ++t) {
         if (q > 0) ptx::mbar_wait(&yfree[t], (q - 1) & 1, a.err, 125);
         ptx::tc_fence_after();
         if (leader) {
           for (int sb = 0; sb < nsb; ++sb) {
-            const uint32_t c0 = ptx::smem_u32(smem + a.off_C + (t * nsb + sb) * kTile);
+            const uint32_t c0 = ptx::smem_u32(smem + c_off(t, sb));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t cd = ptx::smem_desc(c0 + kk * 32, 16, 1024, ptx::kSw128);
@@ -244,7 +274,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
         __syncwarp();
       }
       // Ys = S'_q X_q, one 64-token block of each row tile at a time
-      for (int t = 0; t < ntile; ++t)
+      for (int t = t_lo; t < t_hi; ++t)
         for (int jb = 0; jb < 2 * (t + 1); ++jb, ++cnt) {
           const int s = cnt % kNP;
           ptx::mbar_wait(&pm_full[s], (cnt / kNP) & 1, a.err, 127);
@@ -321,8 +351,8 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
     // re-pack the fp32 C B^T as fp16 pairs (at most 2^-11 relative rounding
     // before the decay, well below the bf16 rounding of S'), row tile 0
     // first: its fp32 columns are then overwritten by row tile 1's copy
-    for (int t = 0; t < ntile; ++t) {
-      if (t == 1) {
+    for (int t = t_lo; t < t_hi; ++t) {
+      if (t > t_lo) {
         ptx::tc_fence_before();
         ptx::named_bar_sync(1, kRowThreads);  // every thread has read tile 0's fp32
         ptx::tc_fence_after();
@@ -358,7 +388,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
 
       // decayed, masked interaction rows, one 64-token block (one S' stage)
       // per tensor-memory load wait
-      for (int t = 0; t < ntile; ++t) {
+      for (int t = t_lo; t < t_hi; ++t) {
         const int i_rel = t * 128 + r;
         const int rb = i_rel >> 6;
         const float Git = Gs[pb][i_rel];
@@ -452,7 +482,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
           if ((tid & 31) == 0) ptx::mbar_arrive(&pm_full[s]);
           // the previous head's y store has had the first row tile's time to
           // read its shared-memory tile: release that head buffer
-          if (tid == 0 && q > 0 && t == 0 && jb == 1) {
+          if (tid == 0 && q > 0 && t == t_lo && jb == 1) {
             ptx::bulk_wait_read<0>();
             ptx::mbar_arrive(&hx_empty[(q - 1) & 1]);
           }
@@ -469,7 +499,8 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       uint8_t *xs = smem + (buf ? a.off_hx1 : a.off_hx0) + st_bytes;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        if (t >= ntile) break;
+        if (t < t_lo) continue;
+        if (t >= t_hi) break;
         const int i_rel = t * 128 + r;
         uint8_t *xrow = xs + (i_rel >> 6) * kBlk;
         uint32_t ys[kC16][16], yc[kC16][16];
@@ -505,7 +536,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       ptx::fence_async_smem();
       ptx::named_bar_sync(2, kRowThreads);
       if (tid == 0) {
-        for (int jb = 0; jb < T / 64; ++jb)
+        for (int jb = 2 * t_lo; jb < 2 * t_hi; ++jb)
           ptx::tma_store_4d(&tm_y, xs + jb * kBlk, 0, h, tok0 + jb * 64, b);
         ptx::bulk_commit();
       }
@@ -530,6 +561,22 @@ int sm_count_scan() {
 struct Layout {
   int off_C, off_B, off_hx[2], hx_bytes, total;
 };
+
+// Split launches: C of one row tile, then two head buffers of at least
+// four 16 KB tiles each (the second one holds the two-slot B ring of
+// phase 1).
+Layout split_layout(const Dims &d) {
+  Layout l;
+  const int nsb = (int)(d.S / 64);
+  l.hx_bytes = (int)(d.S * kP * 2 + d.T * kP * 2);
+  const int buf = std::max(l.hx_bytes, 4 * kTile);
+  l.off_C = 0;
+  l.off_B = -1;
+  l.off_hx[0] = nsb * kTile;
+  l.off_hx[1] = l.off_hx[0] + buf;
+  l.total = l.off_hx[1] + buf;
+  return l;
+}
 
 Layout chunk_layout(const Dims &d) {
   Layout l;
@@ -559,15 +606,21 @@ bool fwd_scan_chunk_supported(const Dims &d) {
   return l.total + 1024 <= 210 * 1024;
 }
 
+bool fwd_scan_chunk_split_supported(const Dims &d) {
+  if (d.P != kP || (d.S != 64 && d.S != 128 && d.S != 256) || d.T != 256) return false;
+  if (d.nc * (d.T / 128) > 65535) return false;
+  return split_layout(d).total + 1024 <= 210 * 1024;
+}
+
 // Heads per CTA: a divisor of the heads per group minimising
 // waves * (phase-1 cost + heads), the phase-1 cost counted as one head.
-int fwd_scan_chunk_heads(const Dims &d) {
+int fwd_scan_chunk_heads(const Dims &d, bool split) {
   const int64_t sms = sm_count_scan();
   int best = 1;
   double best_cost = 1e300;
   for (int hs = 1; hs <= d.hpg; ++hs) {
     if (d.hpg % hs) continue;
-    const int64_t ctas = d.b * d.nc * (d.nh / hs);
+    const int64_t ctas = d.b * d.nc * (split ? d.T / 128 : 1) * (d.nh / hs);
     const double cost = (double)((ctas + sms - 1) / sms) * (1.0 + hs);
     if (cost < best_cost * 0.999) {
       best_cost = cost;
@@ -577,21 +630,24 @@ int fwd_scan_chunk_heads(const Dims &d) {
   return best;
 }
 
-bool fwd_scan_chunk_heads_ok(const Dims &d, int hs) {
-  return fwd_scan_chunk_supported(d) && hs >= 1 && hs <= d.hpg && d.hpg % hs == 0;
+bool fwd_scan_chunk_heads_ok(const Dims &d, int hs, bool split) {
+  return (split ? fwd_scan_chunk_split_supported(d) : fwd_scan_chunk_supported(d)) &&
+         hs >= 1 && hs <= d.hpg && d.hpg % hs == 0;
 }
 
 cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
                                   const void *dt, const float *A, const void *states,
                                   const float *D, void *y, cudaStream_t st) {
   if (!fwd_scan_chunk_supported(d)) return cudaErrorInvalidValue;
-  return launch_fwd_scan_chunk(d, x, B, C, dt, A, states, D, y, fwd_scan_chunk_heads(d), st);
+  return launch_fwd_scan_chunk(d, x, B, C, dt, A, states, D, y,
+                               fwd_scan_chunk_heads(d, false), false, st);
 }
 
 cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
                                   const void *dt, const float *A, const void *states,
-                                  const float *D, void *y, int hs, cudaStream_t st) {
-  if (!fwd_scan_chunk_heads_ok(d, hs)) return cudaErrorInvalidValue;
+                                  const float *D, void *y, int hs, bool split,
+                                  cudaStream_t st) {
+  if (!fwd_scan_chunk_heads_ok(d, hs, split)) return cudaErrorInvalidValue;
   CUtensorMap tC, tB, tx, tS, tY;
   if (!make_tmap_bl(&tC, C, true, d.b, d.L, d.ng, d.S, 128) ||
       !make_tmap_bl(&tB, B, true, d.b, d.L, d.ng, d.S, 128) ||
@@ -604,7 +660,7 @@ cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, c
     const uint32_t box[3] = {64u, 64u, 1u};
     if (!make_tmap_sw128(&tS, states, true, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  const Layout l = chunk_layout(d);
+  const Layout l = split ? split_layout(d) : chunk_layout(d);
   const int smem = l.total + 1024;
   cudaError_t e = cudaFuncSetAttribute(fwd_scan_chunk_bf16,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -627,9 +683,10 @@ cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, c
   a.off_B = l.off_B;
   a.off_hx0 = l.off_hx[0];
   a.off_hx1 = l.off_hx[1];
-  a.hx_bytes = l.hx_bytes;
-  dim3 grid((unsigned)(d.nh / hs), (unsigned)d.nc, (unsigned)d.b);
-  if (d.nc > 65535) return cudaErrorInvalidValue;
+  a.split = split ? 1 : 0;
+  const int64_t gy = d.nc * (split ? d.T / 128 : 1);
+  if (gy > 65535) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)(d.nh / hs), (unsigned)gy, (unsigned)d.b);
   // programmatic stream serialisation, as for fwd_scan: the producer waits
   // on the device before loading the first start state
   cudaLaunchConfig_t cfg = {};

@@ -89,7 +89,8 @@ cudaError_t launch_scan(const Dims &d, const ssd::FwdPlan &plan, const void *x, 
                         const void *C, const void *dt, const float *A, const void *states,
                         const float *D, void *y, cudaStream_t st) {
   return plan.scan_kernel
-             ? ssd::launch_fwd_scan_chunk(d, x, B, C, dt, A, states, D, y, plan.scan_heads, st)
+             ? ssd::launch_fwd_scan_chunk(d, x, B, C, dt, A, states, D, y, plan.scan_heads,
+                                          plan.scan_kernel == 2, st)
              : ssd::launch_fwd_scan(d, x, B, C, dt, A, states, D, y, plan.scan_heads, st);
 }
 

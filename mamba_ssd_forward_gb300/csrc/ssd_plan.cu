@@ -34,8 +34,8 @@ bool key_of(const Dims &d, Key *k) {
 FwdPlan fwd_default_plan(const Dims &d) {
   FwdPlan p;
   p.cs = chunk_state_plan(d);
-  p.scan_kernel = fwd_scan_chunk_supported(d) ? 1 : 0;
-  p.scan_heads = p.scan_kernel ? fwd_scan_chunk_heads(d) : fwd_scan_heads(d);
+  p.scan_kernel = fwd_scan_chunk_supported(d) ? 1 : fwd_scan_chunk_split_supported(d) ? 2 : 0;
+  p.scan_heads = p.scan_kernel ? fwd_scan_chunk_heads(d, p.scan_kernel == 2) : fwd_scan_heads(d);
   return p;
 }
 
@@ -58,10 +58,10 @@ void fwd_cs_candidates(const Dims &d, std::vector<CsPlan> *out) {
 void fwd_scan_candidates(const Dims &d, std::vector<FwdPlan> *out) {
   FwdPlan p{};
   p.cs = CsPlan{0, 0};
-  if (fwd_scan_chunk_supported(d))
+  for (int kind = 1; kind <= 2; ++kind)
     for (int hs = 1; hs <= d.hpg; ++hs)
-      if (fwd_scan_chunk_heads_ok(d, hs)) {
-        p.scan_kernel = 1;
+      if (fwd_scan_chunk_heads_ok(d, hs, kind == 2)) {
+        p.scan_kernel = kind;
         p.scan_heads = hs;
         out->push_back(p);
       }
@@ -75,7 +75,8 @@ void fwd_scan_candidates(const Dims &d, std::vector<FwdPlan> *out) {
 
 bool fwd_plan_ok(const Dims &d, const FwdPlan &p) {
   if (!chunk_state_plan_ok(d, p.cs)) return false;
-  if (p.scan_kernel == 1) return fwd_scan_chunk_heads_ok(d, p.scan_heads);
+  if (p.scan_kernel == 1 || p.scan_kernel == 2)
+    return fwd_scan_chunk_heads_ok(d, p.scan_heads, p.scan_kernel == 2);
   if (p.scan_kernel == 0) return fwd_scan_heads_ok(d, p.scan_heads);
   return false;
 }

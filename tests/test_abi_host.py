@@ -221,20 +221,24 @@ def test_plan_candidates_are_valid_and_hold_the_default(lib, shape):
     assert cands
     hpg = nh // ng
     chunk_kernel_ok = P == 64 and S in (64, 128) and T in (128, 256)
+    split_kernel_ok = P == 64 and S in (64, 128, 256) and T == 256
     for c in cands:
         assert c["chunk_state_ctas"] in (1, 2)
         hmax = 4 if c["chunk_state_ctas"] == 1 else 2
         assert 1 <= c["chunk_state_heads"] <= hmax and hpg % c["chunk_state_heads"] == 0
         assert c["chunk_state_heads"] * P <= (256 if c["chunk_state_ctas"] == 1 else 128)
-        assert c["scan_kernel"] in (0, 1) and hpg % c["scan_heads"] == 0
+        assert c["scan_kernel"] in (0, 1, 2) and hpg % c["scan_heads"] == 0
         if c["scan_kernel"] == 1:
             assert chunk_kernel_ok
+        elif c["scan_kernel"] == 2:
+            assert split_kernel_ok
         else:
             assert c["scan_heads"] <= 4 and c["scan_heads"] * P <= 256
     assert len({tuple(c.values()) for c in cands}) == len(cands)
     default = m.default_plan(d)
     assert default in cands
-    assert (default["scan_kernel"] == 1) == chunk_kernel_ok
+    expect = 1 if chunk_kernel_ok else 2 if split_kernel_ok else 0
+    assert default["scan_kernel"] == expect
     # without an installed plan the forward pass uses the default
     assert m.get_plan(d) == default
 
@@ -254,7 +258,7 @@ def test_plan_rejections(lib):
         {"chunk_state_heads": 4, "chunk_state_ctas": 2, "scan_kernel": 1, "scan_heads": 20},
         {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 1, "scan_heads": 3},
         {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 0, "scan_heads": 8},
-        {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 2, "scan_heads": 1},
+        {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 3, "scan_heads": 1},
     ]
     for p in bad:
         assert p not in m.plan_candidates(d)
