@@ -92,14 +92,11 @@ struct ChunkArgs {
   __nv_bfloat16 *y;
   int *err;
   int L, nh, S, hpg, T, nc, hs;
-  // 1: one 128-row tile of the chunk per CTA (blockIdx.y = chunk * tiles +
-  // tile), B streamed through a two-slot ring in the second head buffer
-  // during phase 1; 0: both row tiles per CTA, B resident
-  int split;
   // shared-memory layout (byte offsets from the 1024-aligned base)
   int off_C, off_B, off_hx0, off_hx1;
 };
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
                     const __grid_constant__ CUtensorMap tm_B,
@@ -122,7 +119,7 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
 
   const int L = a.L, nh = a.nh, S = a.S, T = a.T, nc = a.nc, hs = a.hs;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int split = a.split;
+  constexpr bool split = kSplit;
   const int ntile_all = T / 128;
   const int k = split ? blockIdx.y / ntile_all : blockIdx.y, b = blockIdx.z;
   // the row tiles [t_lo, t_hi) of the chunk this CTA computes
@@ -662,7 +659,11 @@ cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, c
   }
   const Layout l = split ? split_layout(d) : chunk_layout(d);
   const int smem = l.total + 1024;
-  cudaError_t e = cudaFuncSetAttribute(fwd_scan_chunk_bf16,
+  // kSplit: one 128-row tile of the chunk per CTA (blockIdx.y = chunk *
+  // tiles + tile), B streamed through a two-slot ring in the second head
+  // buffer during phase 1; else both row tiles per CTA, B resident
+  auto kernel = split ? fwd_scan_chunk_bf16<true> : fwd_scan_chunk_bf16<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   ChunkArgs a;
@@ -683,7 +684,6 @@ cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, c
   a.off_B = l.off_B;
   a.off_hx0 = l.off_hx[0];
   a.off_hx1 = l.off_hx[1];
-  a.split = split ? 1 : 0;
   const int64_t gy = d.nc * (split ? d.T / 128 : 1);
   if (gy > 65535) return cudaErrorInvalidValue;
   dim3 grid((unsigned)(d.nh / hs), (unsigned)gy, (unsigned)d.b);
@@ -699,7 +699,7 @@ cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fwd_scan_chunk_bf16, tC, tB, tx, tS, tY, a);
+  return cudaLaunchKernelEx(&cfg, kernel, tC, tB, tx, tS, tY, a);
 }
 
 }  // namespace ssd
