@@ -70,7 +70,7 @@ __device__ __forceinline__ Item decode(int item, const CsArgs &a) {
 
 // kCtas CTAs per SM: 1 (items of up to 4 heads, H P <= 256) or 2 (up to 2
 // heads, H P <= 128, so that two CTAs share the tensor memory).
-template <int kCtas>
+template <int kCtas, int kNsl>
 __global__ void __launch_bounds__(kThreads, kCtas)
 fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
                      const __grid_constant__ CUtensorMap tm_x,
@@ -88,15 +88,19 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
   const int tid = threadIdx.x, warp = tid >> 5;
   const int nPb = (P + 63) / 64;
   const int xbytes = nPb * kBlk;                  // one head's x block
-  const int stage_bytes = 2 * kBlk + H * xbytes;  // B block | x blocks
+  constexpr int nsl = kNsl;
+  const int stage_bytes = 2 * nsl * kBlk + H * xbytes;  // B blocks | x blocks
   uint8_t *ostage = smem + nst * stage_bytes;     // a.nout staged dH tiles
   const int obytes = nPb * kOutBlk;
   const int HP = H * P;
-  const uint32_t ncols = 2 * HP <= 32    ? 32
-                         : 2 * HP <= 64  ? 64
-                         : 2 * HP <= 128 ? 128
-                         : 2 * HP <= 256 ? 256
-                                         : 512;
+  // accumulator set (item parity) `set`, S slice sl, head q: columns
+  // (set nsl + sl) H P + q P
+  const int acc_cols = nsl * HP;
+  const uint32_t ncols = 2 * acc_cols <= 32    ? 32
+                         : 2 * acc_cols <= 64  ? 64
+                         : 2 * acc_cols <= 128 ? 128
+                         : 2 * acc_cols <= 256 ? 256
+                                               : 512;
 
   if (tid == 0) {
     for (int i = 0; i < nst; ++i) {
@@ -138,11 +142,11 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
         ptx::mbar_wait(&empty[s], ((u / nst) & 1) ^ 1, a.err, 101);
         if (leader) {
           uint8_t *Bb = smem + s * stage_bytes;
-          uint8_t *Xb = Bb + 2 * kBlk;
+          uint8_t *Xb = Bb + 2 * nsl * kBlk;
           const int tok = tok0 + kb * kKB;
           ptx::mbar_arrive_expect_tx(&full[s], stage_bytes);
-          for (int mb = 0; mb < 2; ++mb)
-            ptx::tma_load_4d(Bb + mb * kBlk, &tm_B, it.st * 128 + mb * 64, g, tok, it.b,
+          for (int mb = 0; mb < 2 * nsl; ++mb)
+            ptx::tma_load_4d(Bb + mb * kBlk, &tm_B, it.st * nsl * 128 + mb * 64, g, tok, it.b,
                              &full[s]);
           for (int q = 0; q < H; ++q)
             for (int pb = 0; pb < nPb; ++pb)
@@ -171,15 +175,19 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
         ptx::mbar_wait(&scaled[s], (u / nst) & 1, a.err, 103);
         ptx::tc_fence_after();
         if (leader) {
-          const uint32_t b0 = ptx::smem_u32(smem + s * stage_bytes);
-          const uint32_t x0 = b0 + 2 * kBlk;
-          for (int q = 0; q < n_mma; ++q) {
+          const uint32_t bs = ptx::smem_u32(smem + s * stage_bytes);
+          const uint32_t x0 = bs + 2 * nsl * kBlk;
+          for (int sl = 0; sl < nsl; ++sl) {
+            const uint32_t b0 = bs + sl * 2 * kBlk;
+            for (int q = 0; q < n_mma; ++q) {
 #pragma unroll
-            for (int kk = 0; kk < kKB / 16; ++kk) {
-              const uint64_t ad = ptx::smem_desc(b0 + kk * 2048, kBlk, 1024, ptx::kSw128);
-              const uint64_t bd =
-                  ptx::smem_desc(x0 + q * xbytes + kk * 2048, kBlk, 1024, ptx::kSw128);
-              ptx::mma_ss<false>(tmem + set * HP + q * P, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+              for (int kk = 0; kk < kKB / 16; ++kk) {
+                const uint64_t ad = ptx::smem_desc(b0 + kk * 2048, kBlk, 1024, ptx::kSw128);
+                const uint64_t bd =
+                    ptx::smem_desc(x0 + q * xbytes + kk * 2048, kBlk, 1024, ptx::kSw128);
+                ptx::mma_ss<false>(tmem + (set * nsl + sl) * HP + q * P, ad, bd, idesc,
+                                   (kb | kk) ? 1u : 0u);
+              }
             }
           }
           ptx::mma_commit(&empty[s]);
@@ -224,7 +232,9 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
       const int set = jl & 1;
       ptx::mbar_wait(&acc_full[set], (jl >> 1) & 1, a.err, 104);
       ptx::tc_fence_after();
+      for (int sl = 0; sl < nsl; ++sl)
       for (int q = 0; q < H; ++q, ++n_out) {
+        const uint32_t acc = tmem + lane_base + (set * nsl + sl) * HP + q * P;
         uint8_t *stg = ostage + (n_out % a.nout) * obytes;
         // the store that last used this buffer has finished reading it
         if (tid == 0 && n_out >= a.nout) {
@@ -238,8 +248,8 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
           // up to two 16-column groups per pass: g0 and g0 + 2
           uint32_t r0[16], r1[16];
           const bool two = g0 + 2 < ngrp;
-          ptx::tmem_ld16(tmem + lane_base + set * HP + q * P + g0 * 16, r0);
-          if (two) ptx::tmem_ld16(tmem + lane_base + set * HP + q * P + (g0 + 2) * 16, r1);
+          ptx::tmem_ld16(acc + g0 * 16, r0);
+          if (two) ptx::tmem_ld16(acc + (g0 + 2) * 16, r1);
           ptx::tmem_ld_wait();
           ptx::reg_fence(r0);
           ptx::reg_fence(r1);
@@ -263,7 +273,8 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
         if (tid == 0) {
           const int row3 = ((it.b * nh + it.hbase + q) * nc + it.k);
           for (int pb = 0; pb < nPb; ++pb)
-            ptx::tma_store_3d(&tm_dH, stg + pb * kOutBlk, pb * 64, it.st * 128, row3);
+            ptx::tma_store_3d(&tm_dH, stg + pb * kOutBlk, pb * 64, (it.st * nsl + sl) * 128,
+                              row3);
           ptx::bulk_commit();
         }
       }
@@ -319,7 +330,7 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
       const int nqp = H * nPb;  // 64-column x blocks in a stage, <= 4
       for (int kb = 0; kb < nkb; ++kb, ++u) {
         const int s = u % nst;
-        uint8_t *Xb = smem + s * stage_bytes + 2 * kBlk;
+        uint8_t *Xb = smem + s * stage_bytes + 2 * nsl * kBlk;
         ptx::mbar_wait(&full[s], (u / nst) & 1, a.err, 105);
         uint4 buf[8];
 #pragma unroll
@@ -365,27 +376,32 @@ int sm_count() {
 
 
 
-// Heads per item and CTAs per SM.  For each mode (one CTA per SM with
-// H * P <= 256 and up to 4 heads, or two with H * P <= 128 and up to 2, the
-// two accumulator sets of every resident CTA fitting the 512 tensor-memory
-// columns) H is the divisor of the heads per group minimising the bytes the
-// busiest CTA loads (items per CTA, rounded up, times B's slice plus H heads
-// of x per item).  Two CTAs per SM overlap one CTA's cumsum and epilogue with
-// the other's loads and MMAs, which pays once each CTA has several items (3
-// or more); with fewer, one CTA with larger items starts and drains faster.
+// 128-row slices of S per item: both slices when S > 128 (the heads' x is
+// scaled once for the two), else one.
+int cs_slices(const Dims &d) { return d.S > 128 ? 2 : 1; }
+
+// Heads per item and CTAs per SM.  For each mode (one CTA per SM with up to
+// 4 heads, or two with up to 2; the two accumulator sets, 2 nsl H P columns,
+// of every resident CTA fitting the 512 tensor-memory columns) H is the
+// divisor of the heads per group minimising the bytes the busiest CTA loads
+// (items per CTA, rounded up, times B's slices plus H heads of x per item).
+// Two CTAs per SM overlap one CTA's cumsum and epilogue with the other's
+// loads and MMAs, which pays once each CTA has several items (3 or more);
+// with fewer, one CTA with larger items starts and drains faster.
 }  // namespace
 
 CsPlan chunk_state_plan(const Dims &d) {
-  const int64_t n_st = (d.S + 127) / 128;
+  const int nsl = cs_slices(d);
+  const int64_t n_st = (d.S + 128 * nsl - 1) / (128 * nsl);
   const int64_t sms = sm_count();
   const int nPb = (int)((d.P + 63) / 64);
   auto best_h = [&](int ctas, int hmax, int64_t cols, int64_t *items_out) {
     int best = 1;
     double best_cost = 1e300;
     for (int h = 1; h <= hmax; ++h) {
-      if (d.hpg % h || h * d.P > cols || h * nPb > 4) continue;
+      if (d.hpg % h || nsl * h * d.P > cols || h * nPb > 4) continue;
       const int64_t items = d.b * d.nc * n_st * (d.nh / h);
-      const double per_item = 2.0 * kBlk + h * nPb * (double)kBlk;
+      const double per_item = 2.0 * nsl * kBlk + h * nPb * (double)kBlk;
       const double cost = (double)((items + ctas * sms - 1) / (ctas * sms)) * per_item;
       if (cost < best_cost * 0.999) {
         best_cost = cost;
@@ -412,7 +428,7 @@ struct CsSmem {
 CsSmem cs_smem(const Dims &d, const CsPlan &plan) {
   const int nPb = (int)((d.P + 63) / 64);
   CsSmem m;
-  m.stage_bytes = 2 * kBlk + plan.H * nPb * kBlk;
+  m.stage_bytes = 2 * cs_slices(d) * kBlk + plan.H * nPb * kBlk;
   // dynamic shared memory (1 KB of it alignment slack) within 208 KB for
   // one CTA per SM, 104 KB each for two; two staged dH tiles when they fit,
   // else one
@@ -431,7 +447,7 @@ bool chunk_state_plan_ok(const Dims &d, const CsPlan &plan) {
   const int nPb = (int)((d.P + 63) / 64);
   const int hmax = plan.ctas == 1 ? 4 : 2;
   const int64_t cols = plan.ctas == 1 ? 256 : 128;
-  if (plan.H < 1 || plan.H > hmax || d.hpg % plan.H || plan.H * d.P > cols ||
+  if (plan.H < 1 || plan.H > hmax || d.hpg % plan.H || cs_slices(d) * plan.H * d.P > cols ||
       plan.H * nPb > 4)
     return false;
   return cs_smem(d, plan).nst >= 2;
@@ -462,7 +478,11 @@ cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, 
   }
   const CsSmem m = cs_smem(d, plan);
   const int nst = m.nst, nout = m.nout, smem = m.smem;
-  auto kernel = plan.ctas == 1 ? fwd_chunk_state_bf16<1> : fwd_chunk_state_bf16<2>;
+  // kNsl: 128-row slices of S per item (2 when S > 128: the heads' x is
+  // scaled once for both; n_st then counts items along S)
+  const int nsl = cs_slices(d);
+  auto kernel = plan.ctas == 1 ? (nsl == 1 ? fwd_chunk_state_bf16<1, 1> : fwd_chunk_state_bf16<1, 2>)
+                               : (nsl == 1 ? fwd_chunk_state_bf16<2, 1> : fwd_chunk_state_bf16<2, 2>);
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -479,7 +499,7 @@ cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, 
   a.T = (int)d.T;
   a.nc = (int)d.nc;
   a.H = H;
-  a.n_st = (int)((d.S + 127) / 128);
+  a.n_st = (int)((d.S + 128 * nsl - 1) / (128 * nsl));
   a.n_hg = (int)(d.nh / H);
   a.nst = nst;
   a.nout = nout;
