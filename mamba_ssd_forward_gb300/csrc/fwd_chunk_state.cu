@@ -386,8 +386,10 @@ int cs_slices(const Dims &d) { return d.S > 128 ? 2 : 1; }
 // divisor of the heads per group minimising the bytes the busiest CTA loads
 // (items per CTA, rounded up, times B's slices plus H heads of x per item).
 // Two CTAs per SM overlap one CTA's cumsum and epilogue with the other's
-// loads and MMAs, which pays once each CTA has several items (3 or more);
-// with fewer, one CTA with larger items starts and drains faster.
+// loads and MMAs, which pays once each CTA has several items (3 or more) and
+// an item holds one slice of S; otherwise one CTA with larger items is
+// faster (measured: the long-context layer's chunk-jump kernel takes 141 us
+// with one CTA and two heads per item, 151 us with two CTAs and one head).
 }  // namespace
 
 CsPlan chunk_state_plan(const Dims &d) {
@@ -413,7 +415,9 @@ CsPlan chunk_state_plan(const Dims &d) {
   };
   int64_t items2 = 0, items1 = 0;
   const int h2 = best_h(2, 2, 128, &items2);
-  if (items2 >= 3 * 2 * sms) return CsPlan{h2, 2};
+  // with two slices of S per item, two CTAs per SM leave one head per item
+  // (B loaded once per head): one CTA with two heads per item is faster
+  if (nsl == 1 && items2 >= 3 * 2 * sms) return CsPlan{h2, 2};
   const int h1 = best_h(1, 4, 256, &items1);
   return CsPlan{h1, 1};
 }
