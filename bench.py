@@ -449,7 +449,7 @@ def run_ours(args, w):
 def e2e(args, w, inp, dev, overlapped=True):
     """Same metric through the host-buffer API: pinned host inputs copied in,
     forward, y and the final state copied out, every step.  overlapped:
-    ssd_forward_host_overlapped (the copies of up to 4 slices overlap the
+    ssd_forward_host_overlapped (the copies of up to --e2e-slices slices overlap the
     computation on two extra streams); else ssd_forward_host (serial)."""
     import torch
 
@@ -457,7 +457,7 @@ def e2e(args, w, inp, dev, overlapped=True):
     h = {k: (None if v is None else v.contiguous().pin_memory()) for k, v in inp.items()}
     y = torch.empty_like(h["x"]).pin_memory()
     fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32).pin_memory()
-    n_slices = 4
+    n_slices = args.e2e_slices
     if overlapped:
         ws = torch.empty(ssd.host_overlapped_workspace_size(h["x"], h["B"], w.chunk, n_slices,
                                                             True, h["h0"] is not None, True),
@@ -568,6 +568,8 @@ def main(argv=None):
     ap.add_argument("--no-tune", dest="tune", action="store_false",
                     help="use the cost-model launch plan instead of timing the candidates")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--e2e-slices", type=int, default=4,
+                    help="slices of the host-buffer path (copies overlap the computation)")
     ap.add_argument("--flush", choices=["write+read", "write"], default="write+read",
                     help="L2 flush between steps (default: write a buffer, then read another)")
     ap.add_argument("--decode", action="store_true",
