@@ -90,3 +90,27 @@ def test_tune_rejects_fp32(ssd):
                  chunk=w.chunk)
     assert e.value.code == _abi.SSD_ERR_UNSUPPORTED
     assert np.isfinite(to64(dev["x"])).all()
+
+
+# dstate 64 and 256: the one-tile-per-CTA output kernel (2) beside the
+# others, every candidate against the oracle
+@pytest.mark.parametrize("S", [64, 256])
+def test_candidates_other_dstate(ssd, S):
+    w = W.Workload(f"bf16_plans_S{S}", 1, 600, 6, 64, S, 2, 256, "bf16", True)
+    inp = make(w)
+    ref = oracle_run(w, inp)
+    dev = device_inputs(inp)
+    d = ssd.dims_of(dev["x"], dev["B"], w.chunk)
+    cands = ssd.plan_candidates(d)
+    assert any(p["scan_kernel"] == 2 for p in cands)
+    assert all(p["scan_kernel"] != 1 for p in cands) or S == 64
+    try:
+        for p in cands:
+            ssd.set_plan(d, p)
+            y, fin = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                                 dev["h0"], chunk=w.chunk)
+            ssd.device_error()
+            check_io(to64(y), ref["y"], "bf16", f"y {p}")
+            check_io(to64(fin), ref["final_state"], "bf16", f"final_state {p}")
+    finally:
+        ssd.set_plan(d, None)
