@@ -34,6 +34,8 @@ CASES = [
     W.Workload("dec_bf16_groups_S256", 1, 5, 48, 64, 256, 8, 256, "bf16", True),
     W.Workload("dec_fp32_odd", 3, 5, 6, 5, 12, 3, 64, "fp32", True),
     W.Workload("dec_bf16_S1024", 1, 5, 2, 8, 1024, 1, 64, "bf16", True),
+    # enough (batch, head) pairs that the kernel does not slice P across CTAs
+    W.Workload("dec_bf16_many_pairs", 8, 3, 80, 64, 128, 1, 256, "bf16", True),
 ]
 
 
