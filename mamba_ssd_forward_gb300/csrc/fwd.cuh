@@ -1,7 +1,7 @@
 // Kernels of the bf16 forward path (ssd_forward): the chunk jump terms (all
 // chunks in parallel), the sequential pass over chunks, and the
-// warp-specialised output pass.  See fwd_chunk_state.cu, fwd_state_pass.cu
-// and fwd_scan.cu.
+// warp-specialised output passes.  See fwd_chunk_state.cu, fwd_state_pass.cu,
+// fwd_scan_chunk.cu and fwd_scan.cu; ssd_plan.cu holds the launch plans.
 #pragma once
 
 #include <vector>
@@ -10,20 +10,17 @@
 
 namespace ssd {
 
-// Jump term of every chunk (bf16, [b, nh, nc, S, P]) and its decay
-// exp2(G_last) (fp32, [b, nh, nc]); all chunks in parallel.
-cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, const void *dt,
-                                   const float *A, void *dH, float *gamma, cudaStream_t st);
 // Sequential pass over chunks: per-chunk start states (bf16, [b, nh, nc, S,
 // P]) and the final state (fp32, [b, nh, P, S]) from the jump terms.
 cudaError_t launch_fwd_state_pass(const Dims &d, const void *dH, const float *gamma,
                                   const float *h0, void *states, float *final_state,
                                   cudaStream_t st);
-// Heads per CTA of fwd_chunk_state (B shared by the heads of a group).
-int fwd_state_heads(const Dims &d);
 
 // Launch plans: knobs that change the speed of a kernel, never its results.
-// fwd_chunk_state: heads per work item and CTAs per SM.
+
+// fwd_chunk_state: jump term of every chunk (bf16, [b, nh, nc, S, P]) and its
+// decay exp2(G_last) (fp32, [b, nh, nc]), all chunks in parallel, with H
+// heads per work item (sharing one load of B) and `ctas` CTAs per SM.
 struct CsPlan {
   int H, ctas;
 };
@@ -33,22 +30,16 @@ cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, 
                                    const float *A, void *dH, float *gamma, const CsPlan &plan,
                                    cudaStream_t st);
 
-// y from x, B, C, dt, A, D and the bf16 per-chunk states.
-cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const void *C,
-                            const void *dt, const float *A, const void *states, const float *D,
-                            void *y, cudaStream_t st);
-
-// Output pass with C B^T of a whole chunk shared by a slice of heads (P = 64,
-// S in {64, 128}, T in {128, 256}); fwd_scan_chunk_supported says whether
-// the dims qualify.
+// Output pass, y from x, B, C, dt, A, D and the bf16 per-chunk states, by
+// one of two kernels with an explicit number of heads per CTA.
+// fwd_scan: any shape, H heads per CTA.
+// fwd_scan_chunk: C B^T of a whole chunk (fwd_scan_chunk_supported: P = 64,
+// S in {64, 128}, T in {128, 256}) or, split, of one 128-row tile of a chunk
+// (fwd_scan_chunk_split_supported: P = 64, S up to 256, T = 256) shared by a
+// slice of hs heads.
+// fwd_scan_heads(d) and fwd_scan_chunk_heads(d, split) are the cost-model
+// choices; the _ok functions say which values a launch accepts.
 bool fwd_scan_chunk_supported(const Dims &d);
-cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
-                                  const void *dt, const float *A, const void *states,
-                                  const float *D, void *y, cudaStream_t st);
-// The same two output kernels with an explicit number of heads per CTA:
-// fwd_scan_heads(d) and fwd_scan_chunk_heads(d) are the cost-model choices,
-// the _ok functions say which values a launch accepts.
-// split: one 128-row tile of a chunk per CTA (T = 256; S up to 256).
 bool fwd_scan_chunk_split_supported(const Dims &d);
 int fwd_scan_chunk_heads(const Dims &d, bool split);
 bool fwd_scan_heads_ok(const Dims &d, int H);
@@ -61,8 +52,8 @@ cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, c
                                   const float *D, void *y, int hs, bool split,
                                   cudaStream_t st);
 
-// Heads per CTA of the output pass: the largest divisor of nheads/ngroups
-// that is at most 4 and keeps heads * P <= 256 tensor-memory columns.
+// Heads per CTA of fwd_scan: the largest divisor of nheads/ngroups that is
+// at most 4 and keeps heads * P <= 256 tensor-memory columns.
 inline int fwd_scan_heads(const Dims &d) {
   const int hmax = (int)std::min<int64_t>(4, 256 / d.P);
   for (int h = hmax; h > 1; --h)

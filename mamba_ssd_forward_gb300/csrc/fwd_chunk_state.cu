@@ -496,13 +496,6 @@ bool chunk_state_plan_ok(const Dims &d, const CsPlan &plan) {
   return cs_smem(d, plan).nst >= 2;
 }
 
-int fwd_state_heads(const Dims &d) { return chunk_state_plan(d).H; }
-
-cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, const void *dt,
-                                   const float *A, void *dH, float *gamma, cudaStream_t st) {
-  return launch_fwd_chunk_state(d, x, B, dt, A, dH, gamma, chunk_state_plan(d), st);
-}
-
 cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, const void *dt,
                                    const float *A, void *dH, float *gamma, const CsPlan &plan,
                                    cudaStream_t st) {

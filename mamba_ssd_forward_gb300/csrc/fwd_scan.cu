@@ -410,12 +410,6 @@ bool fwd_scan_heads_ok(const Dims &d, int H) {
 
 cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const void *C,
                             const void *dt, const float *A, const void *states, const float *D,
-                            void *y, cudaStream_t st) {
-  return launch_fwd_scan(d, x, B, C, dt, A, states, D, y, fwd_scan_heads(d), st);
-}
-
-cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const void *C,
-                            const void *dt, const float *A, const void *states, const float *D,
                             void *y, int H, cudaStream_t st) {
   if (!fwd_scan_heads_ok(d, H)) return cudaErrorInvalidValue;
   CUtensorMap tC, tB, tx, tS;

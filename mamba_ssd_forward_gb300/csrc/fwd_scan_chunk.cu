@@ -634,14 +634,6 @@ bool fwd_scan_chunk_heads_ok(const Dims &d, int hs, bool split) {
 
 cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
                                   const void *dt, const float *A, const void *states,
-                                  const float *D, void *y, cudaStream_t st) {
-  if (!fwd_scan_chunk_supported(d)) return cudaErrorInvalidValue;
-  return launch_fwd_scan_chunk(d, x, B, C, dt, A, states, D, y,
-                               fwd_scan_chunk_heads(d, false), false, st);
-}
-
-cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
-                                  const void *dt, const float *A, const void *states,
                                   const float *D, void *y, int hs, bool split,
                                   cudaStream_t st) {
   if (!fwd_scan_chunk_heads_ok(d, hs, split)) return cudaErrorInvalidValue;
