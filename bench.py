@@ -258,6 +258,20 @@ def dist_info():
     return world, rank, local
 
 
+def job_throughput(ms_local: float, tokens_per_rank: int, world: int, device=None):
+    """Whole-job step time and tokens/s of `world` replicas: the slowest
+    rank's step time (max over ranks, one all-reduce) and every rank's
+    tokens.  world == 1 needs no process group."""
+    ms = ms_local
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * tokens_per_rank / (ms / 1e3)
+
+
 def run_reference(args, w):
     world, rank, _ = dist_info()
     if rank != 0:
@@ -388,13 +402,7 @@ def run_ours(args, w):
         kern_ms = {names[j]: statistics.mean(ev2[i][j].elapsed_time(ev2[i][j + 1])
                                                     for i in range(args.steps))
                    for j in range(n_l)}
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens = w.batch * w.seqlen
-    value = world * tokens / (ms / 1e3)
+    ms, value = job_throughput(statistics.mean(step_ms), w.batch * w.seqlen, world, dev)
 
     if rank != 0:
         if world > 1:
