@@ -147,6 +147,16 @@ SSD_API ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void
  * Returns SSD_ERR_CUDA if the synchronisation itself fails. */
 SSD_API ssd_status ssd_device_error(void *stream);
 
+/* Self-test of the bounded device-side waits (no counterpart on the pages):
+ * enqueues on `stream` one CTA whose wait on a barrier that nothing arrives
+ * on gives up after limit_ns nanoseconds (1e3 <= limit_ns <= 1e9, else
+ * SSD_ERR_INVALID_ARG) and records the give-up in the device error word, as
+ * any kernel of the library would; the kernel then returns.  The next
+ * ssd_device_error on the device reports SSD_ERR_TIMEOUT and clears the
+ * word.  Until then, every bounded wait of the library returns at once, so
+ * call ssd_device_error before any other work on the device. */
+SSD_API ssd_status ssd_selftest_bounded_wait(uint64_t limit_ns, void *stream);
+
 /* ssd_forward with per-launch timing.  `events` holds n_events cudaEvent_t
  * handles created by the caller; events[0] is recorded on `stream` before
  * the first launch and events[i+1] right after launch i (while i + 1 <

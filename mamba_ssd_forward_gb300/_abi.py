@@ -39,6 +39,7 @@ EXPORTS = (
     "ssd_forward_get_plan",
     "ssd_forward_set_plan",
     "ssd_forward_tune",
+    "ssd_selftest_bounded_wait",
 )
 
 
@@ -113,6 +114,8 @@ def load(path: str | None = None):
     for fn in ("ssd_forward_default_plan", "ssd_forward_get_plan", "ssd_forward_set_plan"):
         getattr(lib, fn).restype = i32
         getattr(lib, fn).argtypes = [dims_p, i32, plan_p]
+    lib.ssd_selftest_bounded_wait.restype = i32
+    lib.ssd_selftest_bounded_wait.argtypes = [ctypes.c_uint64, vp]
     lib.ssd_forward_tune.restype = i32
     lib.ssd_forward_tune.argtypes = [dims_p, i32] + [vp] * 10 + [sz, i32, vp, plan_p]
     if path is None:

@@ -267,3 +267,9 @@ def test_plan_rejections(lib):
         assert e.value.code == _abi.SSD_ERR_INVALID_ARG
     rc = lib.ssd_forward_tune(ctypes.byref(d), 1, *([None] * 10), 0, 5, None, None)
     assert rc == _abi.SSD_ERR_INVALID_ARG
+
+
+def test_selftest_rejects_limits_out_of_range(lib):
+    from mamba_ssd_forward_gb300 import _abi
+    for bad in (0, 999, 1_000_000_001):
+        assert lib.ssd_selftest_bounded_wait(bad, None) == _abi.SSD_ERR_INVALID_ARG
