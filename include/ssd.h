@@ -133,7 +133,11 @@ SSD_API ssd_status ssd_chunk_scan(const ssd_dims *dims, ssd_dtype dtype,
 /* The whole forward pass on one stream: the four steps above (or a fused
  * equivalent) with G and the per-chunk states kept in `workspace`
  * (>= ssd_forward_workspace_size bytes, 256-byte aligned).  h0, D and
- * final_state may be NULL.  Out: y (io), final_state (f32). */
+ * final_state may be NULL.  Out: y (io), final_state (f32).
+ * The call allocates nothing and never synchronises, so after one eager call
+ * on the device (which does the one-time set-up) it can be captured in a CUDA
+ * graph and replayed on new inputs written into the same buffers; the launch
+ * plan in force at capture time is the one the graph replays. */
 SSD_API ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x,
                        const void *dt, const float *A, const void *B,
                        const void *C, const float *D, const float *h0,

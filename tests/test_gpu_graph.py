@@ -1,0 +1,63 @@
+"""ssd_forward inside a CUDA graph: the call allocates nothing, never
+synchronises and only enqueues launches on the caller's stream, so it can be
+captured once (after one eager call, which does the per-process set-up) and
+replayed on new inputs written into the same buffers."""
+import pytest
+import torch
+
+from parity import check_io, device_inputs, make, oracle_run, to64
+
+pytestmark = pytest.mark.gpu
+
+from mamba_ssd_forward_gb300 import inputs as W  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def ssd():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import oracle
+    from mamba_ssd_forward_gb300 import build
+    build.build()
+    oracle.build()
+    import mamba_ssd_forward_gb300 as m
+    return m
+
+
+@pytest.mark.parametrize("w", [
+    W.Workload("graph_bf16", 2, 600, 8, 64, 128, 1, 256, "bf16", True),
+    W.Workload("graph_bf16_S256", 1, 520, 6, 64, 256, 2, 256, "bf16", True),
+    W.Workload("graph_fp32", 1, 300, 4, 32, 64, 2, 128, "fp32", True),
+], ids=lambda w: w.name)
+def test_forward_replays_in_a_cuda_graph(ssd, w):
+    dev = device_inputs(make(w, seed=0))
+    ws = torch.empty(ssd.workspace_size(dev["x"], dev["B"], w.chunk), dtype=torch.uint8,
+                     device="cuda")
+    y = torch.empty_like(dev["x"])
+    fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32,
+                      device="cuda")
+
+    def call():
+        ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], dev["h0"],
+                    chunk=w.chunk, workspace=ws, y=y, final_state=fin)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()  # eager: the one-time set-up happens here
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    # new inputs in the same buffers, then replay
+    inp2 = make(w, seed=7)
+    for k, v in device_inputs(inp2).items():
+        if v is not None:
+            dev[k].copy_(v)
+    g.replay()
+    torch.cuda.synchronize()
+    ssd.device_error()
+    ref = oracle_run(w, inp2)
+    check_io(to64(y), ref["y"], w.dtype, "graph replay y")
+    check_io(to64(fin), ref["final_state"], w.dtype, "graph replay final_state")
