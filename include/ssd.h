@@ -307,7 +307,7 @@ SSD_API ssd_status ssd_forward_noalloc(const ssd_dims *dims, ssd_dtype dtype, co
  *                      C B^T of a whole chunk between a slice of heads (P =
  *                      64, S in {64, 128}, T in {128, 256}); 2 = the same
  *                      with one 128-row tile of the chunk per CTA (P = 64,
- *                      S in {64, 128, 256}, T = 256)
+ *                      S in {64, 128, 256}, T in {128, 256})
  *   scan_heads         heads per CTA of that output kernel (divides
  *                      nheads / ngroups; at most 4, and heads * P <= 256, for
  *                      kernel 0)

@@ -35,8 +35,8 @@ cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, 
 // fwd_scan: any shape, H heads per CTA.
 // fwd_scan_chunk: C B^T of a whole chunk (fwd_scan_chunk_supported: P = 64,
 // S in {64, 128}, T in {128, 256}) or, split, of one 128-row tile of a chunk
-// (fwd_scan_chunk_split_supported: P = 64, S up to 256, T = 256) shared by a
-// slice of hs heads.
+// (fwd_scan_chunk_split_supported: P = 64, S up to 256, T in {128, 256})
+// shared by a slice of hs heads.
 // fwd_scan_heads(d) and fwd_scan_chunk_heads(d, split) are the cost-model
 // choices; the _ok functions say which values a launch accepts.
 bool fwd_scan_chunk_supported(const Dims &d);

@@ -604,7 +604,8 @@ bool fwd_scan_chunk_supported(const Dims &d) {
 }
 
 bool fwd_scan_chunk_split_supported(const Dims &d) {
-  if (d.P != kP || (d.S != 64 && d.S != 128 && d.S != 256) || d.T != 256) return false;
+  if (d.P != kP || (d.S != 64 && d.S != 128 && d.S != 256) || (d.T != 128 && d.T != 256))
+    return false;
   if (d.nc * (d.T / 128) > 65535) return false;
   return split_layout(d).total + 1024 <= 210 * 1024;
 }

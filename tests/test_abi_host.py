@@ -221,7 +221,7 @@ def test_plan_candidates_are_valid_and_hold_the_default(lib, shape):
     assert cands
     hpg = nh // ng
     chunk_kernel_ok = P == 64 and S in (64, 128) and T in (128, 256)
-    split_kernel_ok = P == 64 and S in (64, 128, 256) and T == 256
+    split_kernel_ok = P == 64 and S in (64, 128, 256) and T in (128, 256)
     for c in cands:
         assert c["chunk_state_ctas"] in (1, 2)
         hmax = 4 if c["chunk_state_ctas"] == 1 else 2
