@@ -10,22 +10,24 @@
 // independent, so this runs fully in parallel; the sequential part is the
 // bandwidth kernel in fwd_state_pass.cu.
 //
-// Persistent: one or two CTAs per SM (chunk_state_plan) walk a strided list
-// of work items, an item being (chunk, 128-wide slice of S, group of H heads
-// that share B, batch).
+// Persistent: one or two CTAs per SM (the launch plan) walk a strided list
+// of work items, an item being (chunk, S slice, group of H heads that share
+// B, batch); an S slice is 128 rows of S, or both halves of S when S > 128
+// (kNsl = 2: x is then scaled once for the two M = 128 accumulations).
 // The shared-memory ring of 64-token blocks runs across item boundaries, and
 // the tensor-memory accumulators are double-buffered by item, so the loads
 // of item j+1 stream in while item j is reduced and item j-1 is written out.
 // Warp roles:
 //   warp 8 (TMA):  per block, B (MN-major, s contiguous; once for the H heads)
 //                  and x of each head (MN-major);
-//   warp 9 (MMA):  per block, M = 128 (s) x N = H P MMAs (one per head when
-//                  P is not a multiple of 64) into the item's accumulator set
-//                  (lane = s, column = head * P + p);
+//   warp 9 (MMA):  per block and slice, M = 128 (s) x N = H P MMAs (one per
+//                  head when P is not a multiple of 64) into the item's
+//                  accumulator set (lane = s, column = (slice H + head) P + p);
 //   warps 0-7:     per item, the heads' in-chunk cumsums and jump weights
 //                  (dt and A fetched one item ahead), the scaling of each x
 //                  row by its weight in shared memory, then the previous
-//                  item's epilogue: each head's dH tile staged in shared
+//                  item's epilogue (with one CTA per SM and kNsl = 2 spread
+//                  over the item's stages): each dH tile staged in shared
 //                  memory and written by a TMA store as bf16
 //                  [b, nh, nc, S, P] (p contiguous, the layout the output
 //                  kernel reads); gamma as fp32.

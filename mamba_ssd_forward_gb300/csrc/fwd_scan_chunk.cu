@@ -1,5 +1,5 @@
-// Forward path, output pass (bf16 I/O) with the interaction tile of a whole
-// chunk computed once and shared by a slice of heads.  Same equation as
+// Forward path, output pass (bf16 I/O) with the interaction tile of a chunk
+// computed once and shared by a slice of heads.  Same equation as
 // fwd_scan.cu (the page's compute_out, chunked output equation of
 // "Accelerating Mamba-2 with High-Performance Forward Pass Kernels in NVIDIA
 // CUDA Tile", section "Mamba-2 architecture"):
@@ -8,27 +8,33 @@
 //         + D x_i
 //
 // The heads of one group share B and C, so C B^T of a chunk is the same for
-// all of them.  One CTA per (slice of hs heads of one group, chunk, batch):
-//   phase 1: Sc = C B^T for the whole chunk into tensor memory in fp32,
-//            from C and B resident in shared memory, then re-packed by the
-//            row warps as fp16 pairs (half the columns);
+// all of them.  One CTA per (slice of hs heads of one group, chunk, batch)
+// or, with kSplit, per (slice, 128-row tile of a chunk, batch):
+//   phase 1: Sc = C B^T of the CTA's row tiles into tensor memory in fp32,
+//            from C resident in shared memory and B resident too (whole
+//            chunk) or streamed through a two-slot ring in the second head
+//            buffer (kSplit, which is what lets S = 256 fit), then re-packed
+//            by the row warps as fp16 pairs (half the columns);
 //   per head q of the slice (state and x tiles double-buffered, so the next
 //            head's loads overlap this head):
-//            Yc = C h_q^T (both row tiles), the decayed, masked tile S'_q
+//            Yc = C h_q^T for each row tile, the decayed, masked tile S'_q
 //            from Sc written to tensor memory as bf16 pairs one 64-token
 //            block at a time (two stages), Ys = S'_q X_q with S'_q read from
-//            tensor memory, and the epilogue
+//            tensor memory, and the epilogue, row tile by row tile,
 //            y = exp2(G_i) Yc + Ys + D x computed over x in shared memory and
 //            written by TMA stores (the next head's cumsum runs while this
-//            head's last MMAs finish).
+//            head's last MMAs finish).  y may overwrite x only once every
+//            S'_q X_q product of the head has completed.
 // Warp roles: warp 8 loads (TMA), warp 9 issues the MMAs, warps 0-7 do the
 // cumsums, the re-packing, the decay and the epilogue (two warps per 32-lane
 // quadrant, each taking 32 of every 64 columns).
 //
-// Supported: P = 64, S in {64, 128}, T in {128, 256}; other shapes use
-// fwd_scan.cu.  The decay factors are those of fwd_scan.cu: for a 64-token
-// column block ending at r strictly before row i's block,
-// exp2(G_i - G_j) = exp2(G_i - G_r) * exp2(G_r - G_j), both exponents <= 0.
+// Supported: P = 64; S in {64, 128} with T in {128, 256}, and with kSplit S
+// up to 256; other shapes use fwd_scan.cu.  The decay factors are those of
+// fwd_scan.cu: for a 64-token column block ending at r strictly before row
+// i's block, exp2(G_i - G_j) = exp2(G_i - G_r) * exp2(G_r - G_j), both
+// exponents <= 0; the row's own block uses the same factors when its total
+// decay is bounded (see kSpanMax).
 #include <cuda_fp16.h>
 
 #include "fwd.cuh"
