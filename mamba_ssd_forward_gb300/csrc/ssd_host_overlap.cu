@@ -44,8 +44,14 @@ std::vector<Slice> plan_slices(const ssd_dims &d, int n) {
   return out;
 }
 
+// x, dt and y go through double buffers slice by slice (each slice's dt
+// then starts on a 256-byte boundary, as ssd_forward needs 16); B, C and h0
+// (whose slices start on 16-byte boundaries anyway) are uploaded whole
+// before the first slice, and the final state of batch slices is gathered
+// whole and downloaded after the last slice: fewer, larger copies, each copy
+// having a fixed cost on the copy engines.
 struct Layout {
-  size_t fwd, fwd_bytes, A, D, carry[2], x[2], dt[2], B[2], C[2], h0[2], y[2], fin[2], total;
+  size_t fwd, fwd_bytes, A, D, B, C, h0, fin, carry[2], x[2], dt[2], y[2], total;
 };
 
 Layout layout(const ssd_dims &d, ssd_dtype t, const std::vector<Slice> &sl, bool has_D,
@@ -72,15 +78,16 @@ Layout layout(const ssd_dims &d, ssd_dtype t, const std::vector<Slice> &sl, bool
   l.A = take(sizeof(float) * d.nheads);
   l.D = take(has_D ? sizeof(float) * d.nheads : 0);
   const size_t state = sizeof(float) * d.nheads * d.headdim * d.dstate;  // one batch row
+  const size_t tok = (size_t)d.batch * d.seqlen;
+  l.B = take(e * tok * d.ngroups * d.dstate);
+  l.C = take(e * tok * d.ngroups * d.dstate);
+  l.h0 = take(!seq && has_h0 ? state * d.batch : 0);
+  l.fin = take(!seq && want_fin ? state * d.batch : 0);
   for (int p = 0; p < 2; ++p) {
     l.carry[p] = take(seq ? state : 0);
     l.x[p] = take(e * nb * nt * d.nheads * d.headdim);
     l.dt[p] = take(e * nb * nt * d.nheads);
-    l.B[p] = take(e * nb * nt * d.ngroups * d.dstate);
-    l.C[p] = take(e * nb * nt * d.ngroups * d.dstate);
-    l.h0[p] = take(!seq && has_h0 ? state * nb : 0);
     l.y[p] = take(e * nb * nt * d.nheads * d.headdim);
-    l.fin[p] = take(!seq && want_fin ? state * nb : 0);
   }
   l.total = off;
   return l;
@@ -155,7 +162,13 @@ ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype, co
   if (ds != st) ok(cudaStreamWaitEvent(ds, ev_begin, 0));
   up(l.A, A, sizeof(float) * d.nheads);
   up(l.D, D, sizeof(float) * d.nheads);
-  if (seq) up(l.carry[0], h0, state);
+  const size_t tok_all = (size_t)d.batch * d.seqlen;
+  up(l.B, B, e * tok_all * d.ngroups * d.dstate);
+  up(l.C, C, e * tok_all * d.ngroups * d.dstate);
+  if (seq)
+    up(l.carry[0], h0, state);
+  else
+    up(l.h0, h0, state * d.batch);
   ssd_status status = SSD_OK;
   for (int i = 0; i < n && err == cudaSuccess && status == SSD_OK; ++i) {
     const Slice &s = sl[i];
@@ -166,11 +179,6 @@ ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype, co
     up(l.x[p], static_cast<const char *>(x) + e * tok0 * d.nheads * d.headdim,
        e * ntok * d.nheads * d.headdim);
     up(l.dt[p], static_cast<const char *>(dt) + e * tok0 * d.nheads, e * ntok * d.nheads);
-    up(l.B[p], static_cast<const char *>(B) + e * tok0 * d.ngroups * d.dstate,
-       e * ntok * d.ngroups * d.dstate);
-    up(l.C[p], static_cast<const char *>(C) + e * tok0 * d.ngroups * d.dstate,
-       e * ntok * d.ngroups * d.dstate);
-    if (!seq) up(l.h0[p], h0 ? h0 + s.b0 * state / sizeof(float) : nullptr, state * s.nb);
     ok(cudaEventRecord(ev_in(i), hs));
     // forward of slice i (its y buffer is free once the download of slice
     // i - 2 is done)
@@ -182,11 +190,14 @@ ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype, co
     sd.seqlen = s.nt;
     const float *h_in =
         seq ? ((i == 0 && !h0) ? nullptr : reinterpret_cast<const float *>(ws + l.carry[p]))
-            : (h0 ? reinterpret_cast<const float *>(ws + l.h0[p]) : nullptr);
+            : (h0 ? reinterpret_cast<const float *>(ws + l.h0 + s.b0 * state) : nullptr);
     float *h_out = seq ? reinterpret_cast<float *>(ws + l.carry[p ^ 1])
-                       : (final_state ? reinterpret_cast<float *>(ws + l.fin[p]) : nullptr);
+                       : (final_state ? reinterpret_cast<float *>(ws + l.fin + s.b0 * state)
+                                      : nullptr);
     status = ssd_forward(&sd, dtype, ws + l.x[p], ws + l.dt[p],
-                         reinterpret_cast<const float *>(ws + l.A), ws + l.B[p], ws + l.C[p],
+                         reinterpret_cast<const float *>(ws + l.A),
+                         ws + l.B + e * tok0 * d.ngroups * d.dstate,
+                         ws + l.C + e * tok0 * d.ngroups * d.dstate,
                          D ? reinterpret_cast<const float *>(ws + l.D) : nullptr, h_in,
                          ws + l.y[p], h_out, ws + l.fwd, l.fwd_bytes, stream);
     ok(cudaEventRecord(ev_done(i), st));
@@ -194,9 +205,12 @@ ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype, co
     ok(cudaStreamWaitEvent(ds, ev_done(i), 0));
     down(static_cast<char *>(y) + e * tok0 * d.nheads * d.headdim, l.y[p],
          e * ntok * d.nheads * d.headdim);
-    if (!seq) down(final_state ? final_state + s.b0 * state / sizeof(float) : nullptr, l.fin[p],
-                   state * s.nb);
-    else if (i == n - 1) down(final_state, l.carry[p ^ 1], state);
+    if (i == n - 1) {
+      if (seq)
+        down(final_state, l.carry[p ^ 1], state);
+      else
+        down(final_state, l.fin, state * d.batch);
+    }
     ok(cudaEventRecord(ev_out(i), ds));
   }
   // the caller's stream is ordered after the uploads and the downloads
