@@ -22,10 +22,13 @@
  *   layouts listed below; each must be 16-byte aligned.  The caller owns and
  *   allocates every buffer, including the workspace of ssd_forward.  The
  *   library never allocates device memory, frees or synchronises (except
- *   ssd_forward_tune, which times candidates and waits for them), and keeps
- *   no state between calls other than the launch-plan table of
- *   ssd_forward_set_plan / ssd_forward_tune and the scratch array of
- *   ssd_forward_noalloc.
+ *   ssd_forward_tune, which times candidates and waits for them, and the
+ *   error read-outs).  Launch plans are passed to each call, never stored.
+ *   The only state the library keeps between calls is the scratch array of
+ *   ssd_forward_noalloc and one library-wide device error word, which only
+ *   the calls without a workspace of their own report to (the step-wise
+ *   entry points and ssd_forward_noalloc); ssd_forward and the calls built
+ *   on it report to a word inside the caller's workspace.
  * - `stream` is a cudaStream_t (NULL = legacy default stream); all work is
  *   enqueued on it and runs asynchronously.
  * - Arguments are validated before anything is launched; a rejected call
@@ -34,7 +37,16 @@
  *   gave up (the results of that call are then undefined).  Nothing throws.
  * - Preconditions that are documented but not checked: A <= 0 and dt >= 0 (so
  *   every a_t <= 0, the page's stability condition), finite inputs, and
- *   output buffers that do not overlap inputs.
+ *   output buffers that do not overlap inputs.  The bf16 output kernels 1
+ *   and 2 of the launch plans (below) also need |c_i . b_j| < 2^20 for
+ *   every pair of tokens of a chunk (they keep C B^T as fp16 scaled by
+ *   2^-4); larger products come out as inf / NaN without an error code.
+ *   The other output kernels keep C B^T in fp32 or bf16 and have no such
+ *   limit.  Inside the row's own 64-token block, kernels 1 and 2 factor the
+ *   decay exp2(G_i - G_j) into exp2(G_i - G_r) exp2(G_r - G_j) about the
+ *   block's last token r, which keeps a positive exponent of at most +96
+ *   (log2 units) in fp32; blocks whose total decay is steeper than 2^-96 use
+ *   the direct exponent instead, so no input makes that factor overflow.
  *
  * Dimensions (ssd_dims): batch b >= 1, seqlen L >= 1, nheads nh >= 1,
  * headdim P, dstate S, ngroups ng (nh % ng == 0; head h reads group
@@ -83,11 +95,44 @@ typedef struct {
   int64_t batch, seqlen, nheads, headdim, dstate, ngroups, chunk;
 } ssd_dims;
 
+/* Launch plan of the bf16 forward path: the knobs that change how fast the
+ * kernels run, never what they compute.  No counterpart on the pages beyond
+ * their remark that an autotuner picks tile sizes, stages and occupancy per
+ * shape; these are this library's knobs:
+ *   chunk_state_heads  heads per work item of the chunk-jump kernel (they
+ *                      share one load of B; divides nheads / ngroups)
+ *   chunk_state_ctas   CTAs per SM of that kernel: 1 (up to 4 heads per
+ *                      item) or 2 (up to 2)
+ *   scan_kernel        output kernel: 0 = per-(128-row tile, chunk, head
+ *                      slice) kernel for every shape; 1 = kernel sharing one
+ *                      C B^T of a whole chunk between a slice of heads (P =
+ *                      64, S in {64, 128}, T in {128, 256}); 2 = the same
+ *                      with one 128-row tile of the chunk per CTA (P = 64,
+ *                      S in {64, 128, 256}, T in {128, 256})
+ *   scan_heads         heads per CTA of that output kernel (divides
+ *                      nheads / ngroups; at most 4, and heads * P <= 256, for
+ *                      kernel 0)
+ * A plan is an argument of the calls that take one (NULL = the cost-model
+ * default, ssd_forward_default_plan); the library keeps no table of plans.
+ * Only SSD_BF16 has plans: an fp32 call must pass NULL. */
+typedef struct {
+  int32_t chunk_state_heads, chunk_state_ctas, scan_kernel, scan_heads;
+} ssd_plan;
+
+/* Bytes at the start of every workspace of ssd_forward, ssd_forward_host and
+ * ssd_forward_host_overlapped that hold the call's device error word.  A new
+ * workspace must have them zeroed once before its first use (for example
+ * cudaMemsetAsync(ws, 0, SSD_WS_HEADER_BYTES, stream)); after that the
+ * library writes the word only when a bounded device-side wait gives up, and
+ * ssd_workspace_error reads and clears it. */
+#define SSD_WS_HEADER_BYTES 256u
+
 /* Human-readable name of a status code (static storage, never NULL). */
 SSD_API const char *ssd_status_string(ssd_status s);
 
-/* Bytes of device workspace ssd_forward needs for these dims and dtype
- * (0 if the dims are invalid or unsupported). */
+/* Bytes of device workspace ssd_forward needs for these dims and dtype,
+ * including the SSD_WS_HEADER_BYTES header (0 if the dims are invalid or
+ * unsupported). */
 SSD_API size_t ssd_forward_workspace_size(const ssd_dims *dims, ssd_dtype dtype);
 
 /* Kernel 1 of the page ("Kernel 1: Computing cumulative sums"):
@@ -132,59 +177,87 @@ SSD_API ssd_status ssd_chunk_scan(const ssd_dims *dims, ssd_dtype dtype,
 
 /* The whole forward pass on one stream: the four steps above (or a fused
  * equivalent) with G and the per-chunk states kept in `workspace`
- * (>= ssd_forward_workspace_size bytes, 256-byte aligned).  h0, D and
- * final_state may be NULL.  Out: y (io), final_state (f32).
+ * (>= ssd_forward_workspace_size bytes, 256-byte aligned, its first
+ * SSD_WS_HEADER_BYTES zeroed before its first use).  h0, D and final_state
+ * may be NULL.  Out: y (io), final_state (f32).  Runs the default launch
+ * plan (ssd_forward_ex takes one).  A bounded device-side wait that gives up
+ * is recorded in the workspace's error word (ssd_workspace_error).
  * The call allocates nothing and never synchronises, so after one eager call
  * on the device (which does the one-time set-up) it can be captured in a CUDA
- * graph and replayed on new inputs written into the same buffers; the launch
- * plan in force at capture time is the one the graph replays. */
+ * graph and replayed on new inputs written into the same buffers. */
 SSD_API ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x,
                        const void *dt, const float *A, const void *B,
                        const void *C, const float *D, const float *h0,
                        void *y, float *final_state, void *workspace,
                        size_t ws_bytes, void *stream);
 
-/* Synchronises `stream` and reports whether any kernel of this library gave
- * up a bounded device-side wait since the previous call (SSD_ERR_TIMEOUT;
- * the outputs of that launch are undefined), then clears the record.  The
- * record is one word in device memory shared by all calls on the device.
- * Returns SSD_ERR_CUDA if the synchronisation itself fails. */
+/* ssd_forward with an explicit launch plan (NULL = the default plan; must be
+ * NULL for SSD_F32).  A plan that is not one of
+ * ssd_forward_plan_candidates(dims, dtype) returns SSD_ERR_INVALID_ARG with
+ * nothing enqueued. */
+SSD_API ssd_status ssd_forward_ex(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                                  const void *dt, const float *A, const void *B,
+                                  const void *C, const float *D, const float *h0,
+                                  void *y, float *final_state, void *workspace,
+                                  size_t ws_bytes, const ssd_plan *plan, void *stream);
+
+/* Synchronises `stream` and reports whether a kernel of a call that used
+ * `workspace` (ssd_forward, ssd_forward_ex, ssd_forward_profiled,
+ * ssd_forward_tune, ssd_forward_host, ssd_forward_host_overlapped) gave up a
+ * bounded device-side wait since the word was last cleared
+ * (SSD_ERR_TIMEOUT; the outputs of that call are undefined), then clears
+ * the word.  Each workspace has its own word, so calls on other workspaces
+ * or streams neither see nor clear it.  SSD_ERR_INVALID_ARG for a NULL or
+ * misaligned workspace; SSD_ERR_CUDA if the synchronisation fails. */
+SSD_API ssd_status ssd_workspace_error(void *workspace, void *stream);
+
+/* The same for the library-wide error word, which only the calls without a
+ * workspace of their own report to: ssd_chunk_state, ssd_chunk_scan (the
+ * step-wise entry points with tensor-core kernels) and ssd_forward_noalloc.
+ * Synchronises `stream`, reports SSD_ERR_TIMEOUT if any of them gave up a
+ * bounded wait on this device since the word was last cleared, and clears
+ * it. */
 SSD_API ssd_status ssd_device_error(void *stream);
 
 /* Self-test of the bounded device-side waits (no counterpart on the pages):
  * enqueues on `stream` one CTA whose wait on a barrier that nothing arrives
  * on gives up after limit_ns nanoseconds (1e3 <= limit_ns <= 1e9, else
- * SSD_ERR_INVALID_ARG) and records the give-up in the device error word, as
- * any kernel of the library would; the kernel then returns.  The next
- * ssd_device_error on the device reports SSD_ERR_TIMEOUT and clears the
- * word.  Until then, every bounded wait of the library returns at once, so
- * call ssd_device_error before any other work on the device. */
-SSD_API ssd_status ssd_selftest_bounded_wait(uint64_t limit_ns, void *stream);
+ * SSD_ERR_INVALID_ARG) and records the give-up in *err_word -- a 4-byte
+ * aligned device int, such as the header of a workspace (read it back with
+ * ssd_workspace_error) -- or, with err_word NULL, in the library-wide word
+ * (ssd_device_error).  The kernel then returns.  While a word holds a
+ * give-up, the bounded waits of later calls reporting to the same word
+ * return at once, so read it back before using that word again. */
+SSD_API ssd_status ssd_selftest_bounded_wait(uint64_t limit_ns, int *err_word, void *stream);
 
-/* ssd_forward with per-launch timing.  `events` holds n_events cudaEvent_t
- * handles created by the caller; events[0] is recorded on `stream` before
- * the first launch and events[i+1] right after launch i (while i + 1 <
- * n_events).  *n_launches (if not NULL) receives the number of kernel
- * launches the call enqueued.  events may be NULL (then nothing is recorded).
- * Same arguments, results and errors as ssd_forward otherwise. */
+/* ssd_forward_ex with per-launch timing.  `events` holds n_events
+ * cudaEvent_t handles created by the caller; events[0] is recorded on
+ * `stream` before the first launch and events[i+1] right after launch i
+ * (while i + 1 < n_events).  *n_launches (if not NULL) receives the number
+ * of kernel launches the call enqueued.  events may be NULL when n_events is
+ * 0 (then nothing is recorded).  Same arguments, results and errors as
+ * ssd_forward_ex otherwise. */
 SSD_API ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype,
                                         const void *x, const void *dt, const float *A,
                                         const void *B, const void *C, const float *D,
                                         const float *h0, void *y, float *final_state,
-                                        void *workspace, size_t ws_bytes, void *stream,
+                                        void *workspace, size_t ws_bytes,
+                                        const ssd_plan *plan, void *stream,
                                         void *const *events, int n_events,
                                         int *n_launches);
 
 /* Bytes of device workspace ssd_forward_host needs: room for the device copies
- * of every input and output plus the workspace of ssd_forward (0 if the dims
- * are invalid or unsupported). */
+ * of every input and output plus the workspace of ssd_forward, which comes
+ * first (so the header is this workspace's first SSD_WS_HEADER_BYTES); 0 if
+ * the dims are invalid or unsupported. */
 SSD_API size_t ssd_forward_host_workspace_size(const ssd_dims *dims, ssd_dtype dtype,
                                                int has_D, int has_h0,
                                                int want_final_state);
 
 /* ssd_forward on HOST buffers: copies x, dt, A, B, C, D, h0 from host memory
  * into `workspace` (device, >= ssd_forward_host_workspace_size bytes, 256-byte
- * aligned), runs the forward pass there, and copies y (and final_state, if
+ * aligned, header zeroed before its first use), runs the forward pass there
+ * with `plan` (as for ssd_forward_ex), and copies y (and final_state, if
  * not NULL) back to host memory, all enqueued on `stream`.  The host buffers
  * must stay valid until the stream reaches the end of the call; page-locked
  * host memory makes the copies asynchronous.  D, h0 and final_state may be
@@ -193,7 +266,7 @@ SSD_API ssd_status ssd_forward_host(const ssd_dims *dims, ssd_dtype dtype, const
                                     const void *dt, const float *A, const void *B,
                                     const void *C, const float *D, const float *h0,
                                     void *y, float *final_state, void *workspace,
-                                    size_t ws_bytes, void *stream);
+                                    size_t ws_bytes, const ssd_plan *plan, void *stream);
 
 /* Device workspace of ssd_forward_host_overlapped for these dims and slice
  * count (0 if the dims are invalid or unsupported). */
@@ -205,25 +278,29 @@ SSD_API size_t ssd_forward_host_overlapped_workspace_size(const ssd_dims *dims, 
  * work is cut into up to n_slices slices: along the batch when batch >= 2,
  * else along the tokens in runs of whole chunks, each slice starting from
  * the previous slice's final state (the recurrence resumes exactly from a
- * final state).  Slice i's host->device copies run on h2d_stream, its
- * forward pass on `stream`, its device->host copies on d2h_stream, so that
- * slice i+1 uploads while slice i computes and slice i-1 downloads; input
- * and output buffers in `workspace` are double-buffered.  The ordering
- * between the three streams uses CUDA events that the call creates and
- * releases itself; no memory is allocated.  `stream` waits for both copy
- * streams before the call returns control of it, so work enqueued on
- * `stream` afterwards sees y and final_state in host memory once it runs.
+ * final state).  Slice i's host->device copies (its x, dt, B and C rows) run
+ * on h2d_stream, its forward pass on `stream`, its device->host copies on
+ * d2h_stream, so that slice i+1 uploads while slice i computes and slice i-1
+ * downloads; x, dt and y buffers in `workspace` are double-buffered.  The
+ * ordering between the three streams uses CUDA events that the call creates
+ * and releases itself; no memory is allocated.  `stream` waits for both
+ * copy streams before the call returns control of it -- also when the call
+ * fails after enqueueing some copies -- so work enqueued on `stream`
+ * afterwards sees y and final_state in host memory once it runs, and the
+ * host buffers and the workspace may be reused once `stream` reaches it.
  * h2d_stream / d2h_stream may be NULL (that direction then runs on
- * `stream`).  Other arguments as for ssd_forward_host; workspace >=
- * ssd_forward_host_overlapped_workspace_size bytes, 256-byte aligned.  The
- * host buffers should be page-locked for the copies to overlap. */
+ * `stream`).  `plan` as for ssd_forward_ex (checked against every slice's
+ * dims before anything is enqueued).  Other arguments as for
+ * ssd_forward_host; workspace >= ssd_forward_host_overlapped_workspace_size
+ * bytes, 256-byte aligned, header zeroed before its first use.  The host
+ * buffers should be page-locked for the copies to overlap. */
 SSD_API ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype,
                                                const void *x, const void *dt, const float *A,
                                                const void *B, const void *C, const float *D,
                                                const float *h0, void *y, float *final_state,
                                                void *workspace, size_t ws_bytes, int n_slices,
-                                               void *stream, void *h2d_stream,
-                                               void *d2h_stream);
+                                               const ssd_plan *plan, void *stream,
+                                               void *h2d_stream, void *d2h_stream);
 
 /* One token of the recurrence for every (batch, head) state -- the
  * recurrent form of the page's section "Mamba-2 architecture", the
@@ -268,14 +345,19 @@ SSD_API ssd_status ssd_decode_step(const ssd_dims *dims, ssd_dtype dtype, const 
  * (for example bf16, b 4, L 2048, nh 24, P 64, S 128, T 256 needs about
  * 25 MB and fits; b 2, L 4096, nh 80 with the same P, S, T needs about 84 MB
  * and does not).  Invalid dims, dtype or pointers return the same codes as
- * ssd_forward, with nothing enqueued.
+ * ssd_forward, with nothing enqueued; they are checked before the size, so
+ * an oversize call with a NULL tensor still returns SSD_ERR_INVALID_ARG.
  *
- * First-call set-up: the first call on each device looks up the array's
- * device address (cudaGetSymbolAddress, which may also load the library's
- * module on that device) and caches it under a mutex.  Make one call on each
- * device before starting any stream capture or other region that must not
- * see such set-up; later calls only read the cache.  SSD_ERR_CUDA if the
- * look-up fails.
+ * First-call set-up: the first call in each CUDA context (per device, and
+ * again after a device reset or with another context current) looks up the
+ * array's device address in that context (cudaGetSymbolAddress, which may
+ * also load the library's module there) and caches it under a mutex, keyed
+ * by (device, context).  Make one call on each device before starting any
+ * stream capture or other region that must not see such set-up; later calls
+ * in the same context only read the cache.  SSD_ERR_CUDA if the look-up
+ * fails.  A bounded device-side wait that gives up is reported to the
+ * library-wide error word (ssd_device_error): the array is not the caller's
+ * to read.
  *
  * Concurrency: there is ONE array per device, shared by every call on that
  * device.  Calls whose execution overlaps -- on different streams, or from
@@ -291,32 +373,7 @@ SSD_API ssd_status ssd_forward_noalloc(const ssd_dims *dims, ssd_dtype dtype, co
                                        const void *C, const float *D, const float *h0,
                                        void *y, float *final_state, void *stream);
 
-/* ---------------------------------------------------------------- plans
- *
- * Launch plan of the bf16 forward path (ssd_forward with SSD_BF16, and the
- * calls built on it): the knobs that change how fast the kernels run, never
- * what they compute.  No counterpart on the pages beyond their remark that
- * an autotuner picks tile sizes, stages and occupancy per shape; these are
- * this library's knobs:
- *   chunk_state_heads  heads per work item of the chunk-jump kernel (they
- *                      share one load of B; divides nheads / ngroups)
- *   chunk_state_ctas   CTAs per SM of that kernel: 1 (up to 4 heads per
- *                      item) or 2 (up to 2)
- *   scan_kernel        output kernel: 0 = per-(128-row tile, chunk, head
- *                      slice) kernel for every shape; 1 = kernel sharing one
- *                      C B^T of a whole chunk between a slice of heads (P =
- *                      64, S in {64, 128}, T in {128, 256}); 2 = the same
- *                      with one 128-row tile of the chunk per CTA (P = 64,
- *                      S in {64, 128, 256}, T in {128, 256})
- *   scan_heads         heads per CTA of that output kernel (divides
- *                      nheads / ngroups; at most 4, and heads * P <= 256, for
- *                      kernel 0)
- * Without an installed plan, ssd_forward uses the default plan of a cost
- * model (ssd_forward_default_plan).  Installed plans live in one table per
- * process, keyed by (device, dims, dtype), guarded by a mutex. */
-typedef struct {
-  int32_t chunk_state_heads, chunk_state_ctas, scan_kernel, scan_heads;
-} ssd_plan;
+/* ---------------------------------------------------------------- plans */
 
 /* Every valid plan for these dims: writes up to max_out plans to `out` (may
  * be NULL when max_out is 0) and returns how many there are (0 for SSD_F32,
@@ -330,29 +387,17 @@ SSD_API int ssd_forward_plan_candidates(const ssd_dims *dims, ssd_dtype dtype, s
 SSD_API ssd_status ssd_forward_default_plan(const ssd_dims *dims, ssd_dtype dtype,
                                             ssd_plan *out);
 
-/* The plan ssd_forward uses for these dims on the current device: the
- * installed one, else the default. */
-SSD_API ssd_status ssd_forward_get_plan(const ssd_dims *dims, ssd_dtype dtype, ssd_plan *out);
-
-/* Install `plan` for these dims on the current device (SSD_ERR_INVALID_ARG
- * unless it is one of the candidates; SSD_ERR_CUDA when there is no current
- * device); plan == NULL removes the entry.  The
- * table is read by every later forward call on the device with these dims,
- * on any stream or thread; do not change it while such a call is being
- * enqueued elsewhere if that call must see a particular plan. */
-SSD_API ssd_status ssd_forward_set_plan(const ssd_dims *dims, ssd_dtype dtype,
-                                        const ssd_plan *plan);
-
 /* Timing autotuner for these dims on the current device.  Arguments as for
  * ssd_forward (SSD_BF16 only, else SSD_ERR_UNSUPPORTED).  Runs the forward
- * pass once with the current plan, then times every chunk-jump plan and
+ * pass once with the default plan, then times every chunk-jump plan and
  * every output-kernel plan on `stream` (one untimed launch, then `reps`
  * launches between two CUDA events, 1 <= reps <= 1000), picks the fastest
- * of each (the two kernels are independent), installs the combination as by
- * ssd_forward_set_plan, runs the forward pass once more with it, and waits
- * for the stream.  On return y and final_state hold that last pass's
- * results and *chosen (if not NULL) the installed plan.  Blocks the host and
- * creates and destroys CUDA events: not for use inside a stream capture. */
+ * of each (the two kernels are independent), runs the forward pass once
+ * more with that combination, and waits for the stream.  On return y and
+ * final_state hold that last pass's results and *chosen (required) the
+ * plan, which the caller passes to later calls (ssd_forward_ex); nothing is
+ * installed or remembered.  Blocks the host and creates and destroys CUDA
+ * events: not for use inside a stream capture. */
 SSD_API ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x,
                                     const void *dt, const float *A, const void *B,
                                     const void *C, const float *D, const float *h0, void *y,

@@ -19,7 +19,8 @@ from . import _abi
 from ._abi import SSD_BF16, SSD_F32, SsdError  # noqa: F401
 
 __all__ = ["forward", "chunk_cumsum", "chunk_state", "state_passing", "chunk_scan",
-           "decode_step", "workspace_size", "dims_of", "SsdError"]
+           "decode_step", "workspace_size", "new_workspace", "workspace_error", "dims_of",
+           "SsdError"]
 
 
 def _io_code(t: torch.Tensor) -> int:
@@ -63,13 +64,32 @@ def workspace_size(x: torch.Tensor, B: torch.Tensor, chunk: int = 256) -> int:
     return int(_abi.load().ssd_forward_workspace_size(ctypes.byref(d), _io_code(x)))
 
 
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A uint8 device workspace of `nbytes` bytes with its error-word header
+    (the first SSD_WS_HEADER_BYTES) zeroed, as every workspace of the forward
+    calls must be before its first use."""
+    ws = torch.empty(max(int(nbytes), _abi.SSD_WS_HEADER_BYTES), dtype=torch.uint8,
+                     device=device)
+    ws[:_abi.SSD_WS_HEADER_BYTES].zero_()
+    return ws
+
+
+def _plan_ref(plan):
+    """ctypes reference to an ssd_plan from a dict of its four fields, or
+    None (the default plan)."""
+    if plan is None:
+        return None
+    return ctypes.byref(_abi.SsdPlan(**{k: int(v) for k, v in plan.items()}))
+
+
 def forward(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, workspace=None,
-            y=None, final_state=None, return_final_state: bool = True):
-    """y, final_state = the SSD forward pass (ssd_forward).
+            y=None, final_state=None, return_final_state: bool = True, plan=None):
+    """y, final_state = the SSD forward pass (ssd_forward_ex).
 
     `workspace`, `y` and `final_state` may be preallocated (a uint8 CUDA
-    tensor of at least workspace_size() bytes, and outputs of the right shape
-    and dtype); otherwise they are allocated here."""
+    tensor of at least workspace_size() bytes made by new_workspace(), and
+    outputs of the right shape and dtype); otherwise they are allocated here.
+    `plan` is a launch plan dict (bf16 only; None = the default)."""
     lib = _abi.load()
     d = dims_of(x, B, chunk)
     io = _io_code(x)
@@ -78,16 +98,17 @@ def forward(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, workspace=None,
         raise SsdError("ssd_forward_workspace_size", _abi.SSD_ERR_UNSUPPORTED,
                        "dimensions are invalid or unsupported")
     if workspace is None:
-        workspace = torch.empty(ws_need, dtype=torch.uint8, device=x.device)
+        workspace = new_workspace(ws_need, x.device)
     if y is None:
         y = torch.empty_like(x)
     if final_state is None and return_final_state:
         final_state = torch.empty((d.batch, d.nheads, d.headdim, d.dstate),
                                   dtype=torch.float32, device=x.device)
-    _abi.check("ssd_forward", lib.ssd_forward(
+    _abi.check("ssd_forward_ex", lib.ssd_forward_ex(
         ctypes.byref(d), io, _ptr(x), _ptr(dt), _ptr(_f32(A, "A")), _ptr(B), _ptr(C),
         _ptr(_f32(D, "D")), _ptr(_f32(h0, "h0")), _ptr(y), _ptr(final_state),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream()))
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _plan_ref(plan),
+        _stream()))
     return y, final_state
 
 
@@ -159,7 +180,8 @@ def decode_step(x, dt, A, B, C, D, state, y=None):
     return y
 
 
-def forward_profiled(x, dt, A, B, C, D, h0, chunk, workspace, y, final_state, events):
+def forward_profiled(x, dt, A, B, C, D, h0, chunk, workspace, y, final_state, events,
+                     plan=None):
     """ssd_forward recording `events` (torch.cuda.Event, enable_timing) around
     each of its launches on the current stream; returns the launch count."""
     lib = _abi.load()
@@ -172,8 +194,8 @@ def forward_profiled(x, dt, A, B, C, D, h0, chunk, workspace, y, final_state, ev
     _abi.check("ssd_forward_profiled", lib.ssd_forward_profiled(
         ctypes.byref(d), _io_code(x), _ptr(x), _ptr(dt), _ptr(_f32(A, "A")), _ptr(B), _ptr(C),
         _ptr(_f32(D, "D")), _ptr(_f32(h0, "h0")), _ptr(y), _ptr(final_state), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(), handles, len(events),
-        ctypes.byref(n)))
+        workspace.numel() * workspace.element_size(), _plan_ref(plan), _stream(), handles,
+        len(events), ctypes.byref(n)))
     return n.value
 
 
@@ -191,7 +213,7 @@ def _host_ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def forward_host(x, dt, A, B, C, D, h0, chunk, workspace, y, final_state=None):
+def forward_host(x, dt, A, B, C, D, h0, chunk, workspace, y, final_state=None, plan=None):
     """ssd_forward_host: host tensors in (x, dt, A, B, C, D, h0) and out (y,
     final_state), a device uint8 `workspace` of host_workspace_size() bytes.
     Enqueued on the current stream; synchronise before reading y."""
@@ -202,7 +224,7 @@ def forward_host(x, dt, A, B, C, D, h0, chunk, workspace, y, final_state=None):
     _abi.check("ssd_forward_host", lib.ssd_forward_host(
         ctypes.byref(d), _io_code(x), _host_ptr(x), _host_ptr(dt), _host_ptr(A), _host_ptr(B),
         _host_ptr(C), _host_ptr(D), _host_ptr(h0), _host_ptr(y), _host_ptr(final_state),
-        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream()))
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _plan_ref(plan), _stream()))
 
 
 def host_overlapped_workspace_size(x, B, chunk, n_slices, has_D=True, has_h0=False,
@@ -214,7 +236,7 @@ def host_overlapped_workspace_size(x, B, chunk, n_slices, has_D=True, has_h0=Fal
 
 
 def forward_host_overlapped(x, dt, A, B, C, D, h0, chunk, workspace, y, final_state=None,
-                            n_slices=4, h2d_stream=None, d2h_stream=None):
+                            n_slices=4, h2d_stream=None, d2h_stream=None, plan=None):
     """ssd_forward_host_overlapped: as forward_host, cut into up to n_slices
     slices whose uploads (h2d_stream), forward passes (current stream) and
     downloads (d2h_stream) overlap.  Streams are torch.cuda.Stream or None."""
@@ -226,8 +248,8 @@ def forward_host_overlapped(x, dt, A, B, C, D, h0, chunk, workspace, y, final_st
     _abi.check("ssd_forward_host_overlapped", lib.ssd_forward_host_overlapped(
         ctypes.byref(d), _io_code(x), _host_ptr(x), _host_ptr(dt), _host_ptr(A), _host_ptr(B),
         _host_ptr(C), _host_ptr(D), _host_ptr(h0), _host_ptr(y), _host_ptr(final_state),
-        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), int(n_slices), _stream(),
-        sh(h2d_stream), sh(d2h_stream)))
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), int(n_slices),
+        _plan_ref(plan), _stream(), sh(h2d_stream), sh(d2h_stream)))
 
 
 def plan_candidates(d: _abi.SsdDims, io: int = 1) -> list[dict]:
@@ -240,42 +262,23 @@ def plan_candidates(d: _abi.SsdDims, io: int = 1) -> list[dict]:
     return [arr[i].as_dict() for i in range(n)]
 
 
-def _plan_call(fn: str, d: _abi.SsdDims, io: int) -> dict:
+def default_plan(d: _abi.SsdDims, io: int = 1) -> dict:
+    """The cost-model launch plan (ssd_forward_default_plan)."""
     p = _abi.SsdPlan()
-    _abi.check(fn, getattr(_abi.load(), fn)(ctypes.byref(d), int(io), ctypes.byref(p)))
+    _abi.check("ssd_forward_default_plan",
+               _abi.load().ssd_forward_default_plan(ctypes.byref(d), int(io), ctypes.byref(p)))
     return p.as_dict()
 
 
-def default_plan(d: _abi.SsdDims, io: int = 1) -> dict:
-    """The cost-model launch plan (ssd_forward_default_plan)."""
-    return _plan_call("ssd_forward_default_plan", d, io)
-
-
-def get_plan(d: _abi.SsdDims, io: int = 1) -> dict:
-    """The plan ssd_forward uses for `d` on the current device."""
-    return _plan_call("ssd_forward_get_plan", d, io)
-
-
-def set_plan(d: _abi.SsdDims, plan: dict | None, io: int = 1) -> None:
-    """Install `plan` (a dict of the four fields) for `d` on the current
-    device; None removes the entry (ssd_forward_set_plan)."""
-    ref = None
-    if plan is not None:
-        ref = ctypes.byref(_abi.SsdPlan(**{k: int(v) for k, v in plan.items()}))
-    _abi.check("ssd_forward_set_plan",
-               _abi.load().ssd_forward_set_plan(ctypes.byref(d), int(io), ref))
-
-
 def tune(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, reps: int = 5, workspace=None):
-    """Time every launch plan on these inputs and install the fastest
-    (ssd_forward_tune).  Returns (plan dict, y, final_state) of the final
-    pass with the chosen plan."""
+    """Time every launch plan on these inputs (ssd_forward_tune).  Returns
+    (plan dict, y, final_state) of the final pass with the fastest plan; pass
+    the plan to later calls (forward(..., plan=...)): nothing is installed."""
     lib = _abi.load()
     d = dims_of(x, B, chunk)
     io = _io_code(x)
     if workspace is None:
-        workspace = torch.empty(lib.ssd_forward_workspace_size(ctypes.byref(d), io),
-                                dtype=torch.uint8, device=x.device)
+        workspace = new_workspace(lib.ssd_forward_workspace_size(ctypes.byref(d), io), x.device)
     y = torch.empty_like(x)
     final_state = torch.empty((d.batch, d.nheads, d.headdim, d.dstate), dtype=torch.float32,
                               device=x.device)
@@ -288,7 +291,15 @@ def tune(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, reps: int = 5, works
     return p.as_dict(), y, final_state
 
 
+def workspace_error(workspace) -> None:
+    """Synchronise the current stream and raise SsdError if a kernel of a
+    call that used `workspace` gave up a bounded wait since the last check
+    (ssd_workspace_error); clears the workspace's error word."""
+    _abi.check("ssd_workspace_error", _abi.load().ssd_workspace_error(_ptr(workspace), _stream()))
+
+
 def device_error() -> None:
-    """Synchronise the current stream and raise SsdError if a kernel of the
-    library gave up a bounded wait since the last check."""
+    """Synchronise the current stream and raise SsdError if a call without a
+    workspace (the step-wise entry points, ssd_forward_noalloc) gave up a
+    bounded wait since the last check (ssd_device_error)."""
     _abi.check("ssd_device_error", _abi.load().ssd_device_error(_stream()))

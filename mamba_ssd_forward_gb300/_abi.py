@@ -16,6 +16,8 @@ SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT 
 SSD_F32, SSD_BF16 = 0, 1
 # Size of the fixed scratch array of ssd_forward_noalloc (SSD_NOALLOC_SCRATCH_BYTES).
 SSD_NOALLOC_SCRATCH_BYTES = 32 << 20
+# Workspace header holding a call's device error word (SSD_WS_HEADER_BYTES).
+SSD_WS_HEADER_BYTES = 256
 
 # Every symbol include/ssd.h declares.
 EXPORTS = (
@@ -26,6 +28,8 @@ EXPORTS = (
     "ssd_state_passing",
     "ssd_chunk_scan",
     "ssd_forward",
+    "ssd_forward_ex",
+    "ssd_workspace_error",
     "ssd_device_error",
     "ssd_forward_profiled",
     "ssd_forward_host_workspace_size",
@@ -36,8 +40,6 @@ EXPORTS = (
     "ssd_forward_host_overlapped",
     "ssd_forward_plan_candidates",
     "ssd_forward_default_plan",
-    "ssd_forward_get_plan",
-    "ssd_forward_set_plan",
     "ssd_forward_tune",
     "ssd_selftest_bounded_wait",
 )
@@ -89,33 +91,37 @@ def load(path: str | None = None):
     lib.ssd_state_passing.argtypes = [dims_p, vp, vp, vp, vp, vp, vp]
     lib.ssd_chunk_scan.restype = i32
     lib.ssd_chunk_scan.argtypes = [dims_p, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    plan_p = ctypes.POINTER(SsdPlan)
     lib.ssd_forward.restype = i32
     lib.ssd_forward.argtypes = [dims_p, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_forward_ex.restype = i32
+    lib.ssd_forward_ex.argtypes = [dims_p, i32] + [vp] * 10 + [sz, plan_p, vp]
+    lib.ssd_workspace_error.restype = i32
+    lib.ssd_workspace_error.argtypes = [vp, vp]
     lib.ssd_device_error.restype = i32
     lib.ssd_device_error.argtypes = [vp]
     lib.ssd_forward_profiled.restype = i32
-    lib.ssd_forward_profiled.argtypes = ([dims_p, i32] + [vp] * 10 + [sz, vp, vp, i32,
+    lib.ssd_forward_profiled.argtypes = ([dims_p, i32] + [vp] * 10 + [sz, plan_p, vp, vp, i32,
                                          ctypes.POINTER(ctypes.c_int)])
     lib.ssd_forward_host_workspace_size.restype = sz
     lib.ssd_forward_host_workspace_size.argtypes = [dims_p, i32, i32, i32, i32]
     lib.ssd_forward_host.restype = i32
-    lib.ssd_forward_host.argtypes = [dims_p, i32] + [vp] * 10 + [sz, vp]
+    lib.ssd_forward_host.argtypes = [dims_p, i32] + [vp] * 10 + [sz, plan_p, vp]
     lib.ssd_forward_host_overlapped_workspace_size.restype = sz
     lib.ssd_forward_host_overlapped_workspace_size.argtypes = [dims_p, i32, i32, i32, i32, i32]
     lib.ssd_forward_host_overlapped.restype = i32
-    lib.ssd_forward_host_overlapped.argtypes = [dims_p, i32] + [vp] * 10 + [sz, i32, vp, vp, vp]
+    lib.ssd_forward_host_overlapped.argtypes = ([dims_p, i32] + [vp] * 10 +
+                                                [sz, i32, plan_p, vp, vp, vp])
     lib.ssd_decode_step.restype = i32
     lib.ssd_decode_step.argtypes = [dims_p, i32] + [vp] * 9
     lib.ssd_forward_noalloc.restype = i32
     lib.ssd_forward_noalloc.argtypes = [dims_p, i32] + [vp] * 9 + [vp]
-    plan_p = ctypes.POINTER(SsdPlan)
     lib.ssd_forward_plan_candidates.restype = i32
     lib.ssd_forward_plan_candidates.argtypes = [dims_p, i32, plan_p, i32]
-    for fn in ("ssd_forward_default_plan", "ssd_forward_get_plan", "ssd_forward_set_plan"):
-        getattr(lib, fn).restype = i32
-        getattr(lib, fn).argtypes = [dims_p, i32, plan_p]
+    lib.ssd_forward_default_plan.restype = i32
+    lib.ssd_forward_default_plan.argtypes = [dims_p, i32, plan_p]
     lib.ssd_selftest_bounded_wait.restype = i32
-    lib.ssd_selftest_bounded_wait.argtypes = [ctypes.c_uint64, vp]
+    lib.ssd_selftest_bounded_wait.argtypes = [ctypes.c_uint64, vp, vp]
     lib.ssd_forward_tune.restype = i32
     lib.ssd_forward_tune.argtypes = [dims_p, i32] + [vp] * 10 + [sz, i32, vp, plan_p]
     if path is None:

@@ -270,7 +270,7 @@ chunk_scan_tc(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
 template <typename IO>
 cudaError_t launch_t(const Dims &d, const void *x, const void *B, const void *C, const void *dt,
                      const float *G, const float *states, const float *D, void *y,
-                     cudaStream_t st) {
+                     int *err, cudaStream_t st) {
   constexpr int kAE = IoT<IO>::kAE;
   constexpr bool bf = !IoT<IO>::kTf32;
   CUtensorMap tC, tB, tx;
@@ -290,7 +290,7 @@ cudaError_t launch_t(const Dims &d, const void *x, const void *B, const void *C,
   dim3 grid((unsigned)(d.nc * n_it), (unsigned)d.nh, (unsigned)d.b);
   kern<<<grid, kThreads, smem, st>>>(tC, tB, tx, static_cast<const IO *>(x),
                                      static_cast<const IO *>(dt), G, states, D,
-                                     static_cast<IO *>(y), device_error_word(), (int)d.L,
+                                     static_cast<IO *>(y), err, (int)d.L,
                                      (int)d.nh, (int)d.P, (int)d.S, (int)d.hpg, (int)d.T,
                                      (int)d.nc);
   return cudaGetLastError();
@@ -300,9 +300,10 @@ cudaError_t launch_t(const Dims &d, const void *x, const void *B, const void *C,
 
 cudaError_t launch_chunk_scan(const Dims &d, ssd_dtype io, const void *x, const void *B,
                               const void *C, const void *dt, const float *G,
-                              const float *states, const float *D, void *y, cudaStream_t st) {
-  return io == SSD_BF16 ? launch_t<__nv_bfloat16>(d, x, B, C, dt, G, states, D, y, st)
-                        : launch_t<float>(d, x, B, C, dt, G, states, D, y, st);
+                              const float *states, const float *D, void *y, int *err,
+                              cudaStream_t st) {
+  return io == SSD_BF16 ? launch_t<__nv_bfloat16>(d, x, B, C, dt, G, states, D, y, err, st)
+                        : launch_t<float>(d, x, B, C, dt, G, states, D, y, err, st);
 }
 
 }  // namespace ssd

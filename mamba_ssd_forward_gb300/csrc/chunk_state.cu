@@ -254,7 +254,7 @@ chunk_state_tf32(const float *__restrict__ x, const float *__restrict__ Bm,
 
 template <typename IO>
 cudaError_t launch_t(const Dims &d, const void *x, const void *B, const void *dt,
-                     const float *G, float *dstates, cudaStream_t st) {
+                     const float *G, float *dstates, int *err, cudaStream_t st) {
   const int n_st = (int)((d.S + kMT - 1) / kMT);
   dim3 grid((unsigned)d.nc, (unsigned)(d.nh * n_st), (unsigned)d.b);
   if constexpr (IoT<IO>::kTf32) {
@@ -264,7 +264,7 @@ cudaError_t launch_t(const Dims &d, const void *x, const void *B, const void *dt
     if (e != cudaSuccess) return e;
     chunk_state_tf32<<<grid, kThreads, smem, st>>>(
         static_cast<const float *>(x), static_cast<const float *>(B),
-        static_cast<const float *>(dt), G, dstates, device_error_word(), (int)d.L, (int)d.nh,
+        static_cast<const float *>(dt), G, dstates, err, (int)d.L, (int)d.nh,
         (int)d.P, (int)d.S, (int)d.hpg, (int)d.T, (int)d.nc);
     return cudaGetLastError();
   } else {
@@ -279,7 +279,7 @@ cudaError_t launch_t(const Dims &d, const void *x, const void *B, const void *dt
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, st>>>(tB, tx, static_cast<const IO *>(dt), G, dstates,
-                                       device_error_word(), (int)d.L, (int)d.nh, (int)d.P,
+                                       err, (int)d.L, (int)d.nh, (int)d.P,
                                        (int)d.S, (int)d.hpg, (int)d.T, (int)d.nc);
     return cudaGetLastError();
   }
@@ -288,10 +288,10 @@ cudaError_t launch_t(const Dims &d, const void *x, const void *B, const void *dt
 }  // namespace
 
 cudaError_t launch_chunk_state(const Dims &d, ssd_dtype io, const void *x, const void *B,
-                               const void *dt, const float *G, float *dstates,
+                               const void *dt, const float *G, float *dstates, int *err,
                                cudaStream_t st) {
-  return io == SSD_BF16 ? launch_t<__nv_bfloat16>(d, x, B, dt, G, dstates, st)
-                        : launch_t<float>(d, x, B, dt, G, dstates, st);
+  return io == SSD_BF16 ? launch_t<__nv_bfloat16>(d, x, B, dt, G, dstates, err, st)
+                        : launch_t<float>(d, x, B, dt, G, dstates, err, st);
 }
 
 }  // namespace ssd

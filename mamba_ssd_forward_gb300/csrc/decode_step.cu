@@ -127,13 +127,7 @@ cudaError_t launch_decode_step(int64_t b, int64_t nh, int64_t P, int64_t S, int6
                                void *y, cudaStream_t st) {
   // slice P when the (batch, head) pairs alone would leave SMs idle
   // (measured: 96 pairs 10.1 -> 9.4 us; 5120 pairs are faster unsliced)
-  static int sm_count[256];  // per device, looked up once
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) dev = 0;
-  if (!sm_count[dev] &&
-      cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sm_count[dev] = 148;
-  const bool sliced = b * nh < 4 * (int64_t)sm_count[dev];
+  const bool sliced = b * nh < 4 * (int64_t)sm_count();
   const dim3 grid((unsigned)(b * nh), sliced ? (unsigned)((P + kSliceRows - 1) / kSliceRows) : 1u);
   const int hpg = (int)(nh / ng);
   if (io == SSD_BF16)

@@ -28,7 +28,7 @@ CsPlan chunk_state_plan(const Dims &d);  // the cost-model choice
 bool chunk_state_plan_ok(const Dims &d, const CsPlan &plan);
 cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, const void *dt,
                                    const float *A, void *dH, float *gamma, const CsPlan &plan,
-                                   cudaStream_t st);
+                                   int *err, cudaStream_t st);
 
 // Output pass, y from x, B, C, dt, A, D and the bf16 per-chunk states, by
 // one of two kernels with an explicit number of heads per CTA.
@@ -46,11 +46,22 @@ bool fwd_scan_heads_ok(const Dims &d, int H);
 bool fwd_scan_chunk_heads_ok(const Dims &d, int hs, bool split);
 cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const void *C,
                             const void *dt, const float *A, const void *states, const float *D,
-                            void *y, int H, cudaStream_t st);
+                            void *y, int H, int *err, cudaStream_t st);
 cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
                                   const void *dt, const float *A, const void *states,
-                                  const float *D, void *y, int hs, bool split,
+                                  const float *D, void *y, int hs, bool split, int *err,
                                   cudaStream_t st);
+
+// fwd_out: the output pass with the decay factored about one anchor per
+// chunk and head, so that the masked C B^T of a chunk is shared unchanged by
+// a slice of hs heads (P = 64, S a multiple of 64 up to 256, T in {128,
+// 256}).
+bool fwd_out_supported(const Dims &d);
+bool fwd_out_heads_ok(const Dims &d, int hs);
+int fwd_out_heads(const Dims &d);  // the cost-model choice
+cudaError_t launch_fwd_out(const Dims &d, const void *x, const void *B, const void *C,
+                           const void *dt, const float *A, const void *states, const float *D,
+                           void *y, int hs, int *err, cudaStream_t st);
 
 // Heads per CTA of fwd_scan: the largest divisor of nheads/ngroups that is
 // at most 4 and keeps heads * P <= 256 tensor-memory columns.
@@ -63,21 +74,17 @@ inline int fwd_scan_heads(const Dims &d) {
 
 // Launch plan of the whole bf16 forward path (the public ssd_plan): the
 // chunk-jump plan, and the output kernel (0 = fwd_scan, 1 = fwd_scan_chunk,
-// 2 = fwd_scan_chunk with one row tile per CTA) with its heads per CTA.
+// 2 = fwd_scan_chunk with one row tile per CTA, 3 = fwd_out) with its heads
+// per CTA.
 struct FwdPlan {
   CsPlan cs;
   int scan_kernel, scan_heads;
 };
 FwdPlan fwd_default_plan(const Dims &d);
-// The plan installed for d on the current device, else the default.
-FwdPlan fwd_current_plan(const Dims &d);
 // Valid chunk-jump plans and output-kernel plans (as FwdPlan with only the
 // relevant fields meaningful), appended to the vectors.
 void fwd_cs_candidates(const Dims &d, std::vector<CsPlan> *out);
 void fwd_scan_candidates(const Dims &d, std::vector<FwdPlan> *out);
 bool fwd_plan_ok(const Dims &d, const FwdPlan &p);
-// Install (or, p NULL, remove) the plan for d on the current device; false
-// when there is no current device.
-bool fwd_install_plan(const Dims &d, const FwdPlan *p);
 
 }  // namespace ssd

@@ -405,18 +405,6 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
   if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, ncols);
 }
 
-int sm_count() {
-  static int n[256];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 148;
-  if (!n[dev] &&
-      cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    n[dev] = 148;
-  return n[dev];
-}
-
-
-
 // 128-row slices of S per item: both slices when S > 128 (the heads' x is
 // scaled once for the two), else one.
 int cs_slices(const Dims &d) { return d.S > 128 ? 2 : 1; }
@@ -500,7 +488,7 @@ bool chunk_state_plan_ok(const Dims &d, const CsPlan &plan) {
 
 cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, const void *dt,
                                    const float *A, void *dH, float *gamma, const CsPlan &plan,
-                                   cudaStream_t st) {
+                                   int *err, cudaStream_t st) {
   if (!chunk_state_plan_ok(d, plan)) return cudaErrorInvalidValue;
   const int H = plan.H;
   CUtensorMap tB, tx, tD;
@@ -528,7 +516,7 @@ cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, 
   a.dt = static_cast<const __nv_bfloat16 *>(dt);
   a.A = A;
   a.gamma = gamma;
-  a.err = device_error_word();
+  a.err = err;
   a.L = (int)d.L;
   a.nh = (int)d.nh;
   a.P = (int)d.P;

@@ -410,7 +410,7 @@ bool fwd_scan_heads_ok(const Dims &d, int H) {
 
 cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const void *C,
                             const void *dt, const float *A, const void *states, const float *D,
-                            void *y, int H, cudaStream_t st) {
+                            void *y, int H, int *err, cudaStream_t st) {
   if (!fwd_scan_heads_ok(d, H)) return cudaErrorInvalidValue;
   CUtensorMap tC, tB, tx, tS;
   if (!make_tmap_bl(&tC, C, true, d.b, d.L, d.ng, d.S, 128) ||
@@ -434,7 +434,7 @@ cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const v
   a.A = A;
   a.D = D;
   a.y = static_cast<__nv_bfloat16 *>(y);
-  a.err = device_error_word();
+  a.err = err;
   a.L = (int)d.L;
   a.nh = (int)d.nh;
   a.P = (int)d.P;

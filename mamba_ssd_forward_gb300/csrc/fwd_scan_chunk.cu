@@ -551,16 +551,6 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
   if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, ncols);
 }
 
-int sm_count_scan() {
-  static int n[256];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 148;
-  if (!n[dev] &&
-      cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    n[dev] = 148;
-  return n[dev];
-}
-
 struct Layout {
   int off_C, off_B, off_hx[2], hx_bytes, total;
 };
@@ -619,7 +609,7 @@ bool fwd_scan_chunk_split_supported(const Dims &d) {
 // Heads per CTA: a divisor of the heads per group minimising
 // waves * (phase-1 cost + heads), the phase-1 cost counted as one head.
 int fwd_scan_chunk_heads(const Dims &d, bool split) {
-  const int64_t sms = sm_count_scan();
+  const int64_t sms = sm_count();
   int best = 1;
   double best_cost = 1e300;
   for (int hs = 1; hs <= d.hpg; ++hs) {
@@ -641,7 +631,7 @@ bool fwd_scan_chunk_heads_ok(const Dims &d, int hs, bool split) {
 
 cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, const void *C,
                                   const void *dt, const float *A, const void *states,
-                                  const float *D, void *y, int hs, bool split,
+                                  const float *D, void *y, int hs, bool split, int *err,
                                   cudaStream_t st) {
   if (!fwd_scan_chunk_heads_ok(d, hs, split)) return cudaErrorInvalidValue;
   CUtensorMap tC, tB, tx, tS, tY;
@@ -671,7 +661,7 @@ cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, c
   a.A = A;
   a.D = D;
   a.y = static_cast<__nv_bfloat16 *>(y);
-  a.err = device_error_word();
+  a.err = err;
   a.L = (int)d.L;
   a.nh = (int)d.nh;
   a.S = (int)d.S;

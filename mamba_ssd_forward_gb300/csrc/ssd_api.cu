@@ -55,9 +55,11 @@ bool opt(const void *p) { return !p || aligned16(p); }
 
 ssd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
 
-// Workspace of ssd_forward.  bf16 I/O: the per-chunk start states in bf16,
-// [b, nh, nc, S, P].  fp32 I/O: G, then the chunk jump terms, then the
-// per-chunk states (fp32, the step-wise layouts), each 256-byte aligned.
+// Workspace of ssd_forward: the header (the call's error word), then for
+// bf16 I/O the per-chunk start states in bf16, [b, nh, nc, S, P], the chunk
+// jump terms and the per-chunk decays; for fp32 I/O G, the chunk jump terms
+// and the per-chunk states (fp32, the step-wise layouts).  Each part is
+// 256-byte aligned.
 struct WsLayout {
   size_t G, dstates, states, total;
 };
@@ -66,17 +68,18 @@ size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
 WsLayout ws_layout(const Dims &d, ssd_dtype t) {
   WsLayout w;
+  const size_t h = ssd::kWsHeader;
   if (t == SSD_BF16) {
-    // states (bf16) | jump terms (bf16) | per-chunk decays (fp32)
+    // header | states (bf16) | jump terms (bf16) | per-chunk decays (fp32)
     const size_t st = round256(2 * (size_t)(d.b * d.nh * d.nc * d.S * d.P));
-    w.states = 0;
-    w.dstates = st;
-    w.G = 2 * st;
+    w.states = h;
+    w.dstates = h + st;
+    w.G = h + 2 * st;
     w.total = w.G + round256(sizeof(float) * d.b * d.nh * d.nc);
     return w;
   }
-  w.G = 0;
-  w.dstates = round256(sizeof(float) * d.b * d.nh * d.nc * d.T);
+  w.G = h;
+  w.dstates = h + round256(sizeof(float) * d.b * d.nh * d.nc * d.T);
   const size_t st = round256(sizeof(float) * d.b * d.nh * d.nc * d.P * d.S);
   w.states = w.dstates + st;
   w.total = w.states + st;
@@ -87,11 +90,13 @@ size_t io_size(ssd_dtype t) { return t == SSD_BF16 ? 2 : 4; }
 
 cudaError_t launch_scan(const Dims &d, const ssd::FwdPlan &plan, const void *x, const void *B,
                         const void *C, const void *dt, const float *A, const void *states,
-                        const float *D, void *y, cudaStream_t st) {
+                        const float *D, void *y, int *err, cudaStream_t st) {
+  if (plan.scan_kernel == 3)
+    return ssd::launch_fwd_out(d, x, B, C, dt, A, states, D, y, plan.scan_heads, err, st);
   return plan.scan_kernel
              ? ssd::launch_fwd_scan_chunk(d, x, B, C, dt, A, states, D, y, plan.scan_heads,
-                                          plan.scan_kernel == 2, st)
-             : ssd::launch_fwd_scan(d, x, B, C, dt, A, states, D, y, plan.scan_heads, st);
+                                          plan.scan_kernel == 2, err, st)
+             : ssd::launch_fwd_scan(d, x, B, C, dt, A, states, D, y, plan.scan_heads, err, st);
 }
 
 ssd_plan to_public(const ssd::FwdPlan &p) {
@@ -108,6 +113,21 @@ ssd::FwdPlan from_public(const ssd_plan &p) {
   o.scan_kernel = p.scan_kernel;
   o.scan_heads = p.scan_heads;
   return o;
+}
+
+// The plan a forward call runs: *plan when given (bf16 only, and one of the
+// candidates), else the cost-model default.  INVALID_ARG for a plan that is
+// not a candidate, or any plan with fp32 I/O.
+ssd_status resolve_plan(const Dims &d, ssd_dtype t, const ssd_plan *plan, ssd::FwdPlan *out) {
+  if (!plan) {
+    if (t == SSD_BF16) *out = ssd::fwd_default_plan(d);
+    return SSD_OK;
+  }
+  if (t != SSD_BF16) return SSD_ERR_INVALID_ARG;
+  const ssd::FwdPlan p = from_public(*plan);
+  if (!ssd::fwd_plan_ok(d, p)) return SSD_ERR_INVALID_ARG;
+  *out = p;
+  return SSD_OK;
 }
 
 // Mean milliseconds per launch of `launch` over reps launches (after one
@@ -171,8 +191,18 @@ const char *ssd_status_string(ssd_status s) {
 }
 
 ssd_status ssd_device_error(void *stream) {
+  int *word = ssd::device_error_word();
   int code = 0;
-  if (ssd::read_and_clear_device_error((cudaStream_t)stream, &code) != cudaSuccess)
+  if (!word || ssd::read_and_clear_error(word, (cudaStream_t)stream, &code) != cudaSuccess)
+    return SSD_ERR_CUDA;
+  return code ? SSD_ERR_TIMEOUT : SSD_OK;
+}
+
+ssd_status ssd_workspace_error(void *workspace, void *stream) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SSD_ERR_INVALID_ARG;
+  int code = 0;
+  if (ssd::read_and_clear_error(static_cast<int *>(workspace), (cudaStream_t)stream, &code) !=
+      cudaSuccess)
     return SSD_ERR_CUDA;
   return code ? SSD_ERR_TIMEOUT : SSD_OK;
 }
@@ -200,8 +230,10 @@ ssd_status ssd_chunk_state(const ssd_dims *dims, ssd_dtype dtype, const void *x,
   if (s != SSD_OK) return s;
   if (!valid_dtype(dtype) || !req(x) || !req(B) || !req(dt) || !req(G) || !req(dstates))
     return SSD_ERR_INVALID_ARG;
+  int *err = ssd::device_error_word();
+  if (!err) return SSD_ERR_CUDA;
   return from_cuda(
-      ssd::launch_chunk_state(d, dtype, x, B, dt, G, dstates, (cudaStream_t)stream));
+      ssd::launch_chunk_state(d, dtype, x, B, dt, G, dstates, err, (cudaStream_t)stream));
 }
 
 ssd_status ssd_state_passing(const ssd_dims *dims, const float *dstates, const float *G,
@@ -225,7 +257,9 @@ ssd_status ssd_chunk_scan(const ssd_dims *dims, ssd_dtype dtype, const void *x, 
   if (!valid_dtype(dtype) || !req(x) || !req(B) || !req(C) || !req(dt) || !req(G) ||
       !req(states) || !opt(D) || !req(y))
     return SSD_ERR_INVALID_ARG;
-  return from_cuda(ssd::launch_chunk_scan(d, dtype, x, B, C, dt, G, states, D, y,
+  int *err = ssd::device_error_word();
+  if (!err) return SSD_ERR_CUDA;
+  return from_cuda(ssd::launch_chunk_scan(d, dtype, x, B, C, dt, G, states, D, y, err,
                                           (cudaStream_t)stream));
 }
 
@@ -249,30 +283,49 @@ ssd_status ssd_decode_step(const ssd_dims *dims, ssd_dtype dtype, const void *x,
                                            (cudaStream_t)stream));
 }
 
-ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
-                       const float *A, const void *B, const void *C, const float *D,
-                       const float *h0, void *y, float *final_state, void *workspace,
-                       size_t ws_bytes, void *stream) {
-  return ssd_forward_profiled(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, workspace,
-                              ws_bytes, stream, nullptr, 0, nullptr);
-}
+}  // extern "C"
 
-ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype, const void *x,
-                                const void *dt, const float *A, const void *B, const void *C,
-                                const float *D, const float *h0, void *y, float *final_state,
-                                void *workspace, size_t ws_bytes, void *stream,
-                                void *const *events, int n_events, int *n_launches) {
-  Dims d;
-  ssd_status s = check_dims(dims, &d);
+namespace ssd {
+
+ssd_status check_forward_args(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                              const void *dt, const float *A, const void *B, const void *C,
+                              const float *D, const float *h0, const void *y,
+                              const float *final_state, Dims *out) {
+  ssd_status s = check_dims(dims, out);
   if (s != SSD_OK) return s;
   if (!valid_dtype(dtype) || !req(x) || !req(dt) || !req(A) || !req(B) || !req(C) ||
-      !opt(D) || !opt(h0) || !req(y) || !opt(final_state) || !workspace ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) || n_events < 0)
+      !opt(D) || !opt(h0) || !req(y) || !opt(final_state))
+    return SSD_ERR_INVALID_ARG;
+  return SSD_OK;
+}
+
+ssd_status plan_status(const ssd_dims *dims, ssd_dtype dtype, const ssd_plan *plan) {
+  Dims d;
+  const ssd_status s = check_dims(dims, &d);
+  if (s != SSD_OK) return s;
+  if (!valid_dtype(dtype)) return SSD_ERR_INVALID_ARG;
+  ssd::FwdPlan fp{};
+  return resolve_plan(d, dtype, plan, &fp);
+}
+
+ssd_status forward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
+                        const float *A, const void *B, const void *C, const float *D,
+                        const float *h0, void *y, float *final_state, void *workspace,
+                        size_t ws_bytes, const ssd_plan *plan, int *err, cudaStream_t st,
+                        void *const *events, int n_events, int *n_launches) {
+  Dims d;
+  ssd_status s = check_forward_args(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, &d);
+  if (s != SSD_OK) return s;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || n_events < 0 ||
+      (n_events > 0 && !events))
     return SSD_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(d, dtype);
   if (ws_bytes < w.total) return SSD_ERR_INVALID_ARG;
+  ssd::FwdPlan fp{};
+  s = resolve_plan(d, dtype, plan, &fp);
+  if (s != SSD_OK) return s;
+  if (!err) err = static_cast<int *>(workspace);  // the workspace's own error word
   char *ws = static_cast<char *>(workspace);
-  cudaStream_t st = (cudaStream_t)stream;
   int launched = 0;
   auto mark = [&](int i) -> cudaError_t {
     if (events && i < n_events) return cudaEventRecord((cudaEvent_t)events[i], st);
@@ -285,12 +338,11 @@ ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype, const voi
     void *sts = ws + w.states;
     void *dH = ws + w.dstates;
     float *gam = reinterpret_cast<float *>(ws + w.G);
-    const ssd::FwdPlan plan = ssd::fwd_current_plan(d);
-    if (e == cudaSuccess) e = ssd::launch_fwd_chunk_state(d, x, B, dt, A, dH, gam, plan.cs, st);
+    if (e == cudaSuccess) e = ssd::launch_fwd_chunk_state(d, x, B, dt, A, dH, gam, fp.cs, err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
     if (e == cudaSuccess) e = ssd::launch_fwd_state_pass(d, dH, gam, h0, sts, final_state, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
-    if (e == cudaSuccess) e = launch_scan(d, plan, x, B, C, dt, A, sts, D, y, st);
+    if (e == cudaSuccess) e = launch_scan(d, fp, x, B, C, dt, A, sts, D, y, err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
   } else {
     float *G = reinterpret_cast<float *>(ws + w.G);
@@ -298,15 +350,47 @@ ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype, const voi
     float *sts = reinterpret_cast<float *>(ws + w.states);
     if (e == cudaSuccess) e = ssd::launch_chunk_cumsum(d, dtype, dt, A, G, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
-    if (e == cudaSuccess) e = ssd::launch_chunk_state(d, dtype, x, B, dt, G, dst, st);
+    if (e == cudaSuccess) e = ssd::launch_chunk_state(d, dtype, x, B, dt, G, dst, err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
     if (e == cudaSuccess) e = ssd::launch_state_passing(d, dst, G, h0, sts, final_state, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
-    if (e == cudaSuccess) e = ssd::launch_chunk_scan(d, dtype, x, B, C, dt, G, sts, D, y, st);
+    if (e == cudaSuccess)
+      e = ssd::launch_chunk_scan(d, dtype, x, B, C, dt, G, sts, D, y, err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
   }
   if (n_launches) *n_launches = launched;
   return from_cuda(e);
+}
+
+}  // namespace ssd
+
+extern "C" {
+
+ssd_status ssd_forward(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
+                       const float *A, const void *B, const void *C, const float *D,
+                       const float *h0, void *y, float *final_state, void *workspace,
+                       size_t ws_bytes, void *stream) {
+  return ssd::forward_impl(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, workspace,
+                           ws_bytes, nullptr, nullptr, (cudaStream_t)stream, nullptr, 0, nullptr);
+}
+
+ssd_status ssd_forward_ex(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
+                          const float *A, const void *B, const void *C, const float *D,
+                          const float *h0, void *y, float *final_state, void *workspace,
+                          size_t ws_bytes, const ssd_plan *plan, void *stream) {
+  return ssd::forward_impl(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, workspace,
+                           ws_bytes, plan, nullptr, (cudaStream_t)stream, nullptr, 0, nullptr);
+}
+
+ssd_status ssd_forward_profiled(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                                const void *dt, const float *A, const void *B, const void *C,
+                                const float *D, const float *h0, void *y, float *final_state,
+                                void *workspace, size_t ws_bytes, const ssd_plan *plan,
+                                void *stream, void *const *events, int n_events,
+                                int *n_launches) {
+  return ssd::forward_impl(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, workspace,
+                           ws_bytes, plan, nullptr, (cudaStream_t)stream, events, n_events,
+                           n_launches);
 }
 
 int ssd_forward_plan_candidates(const ssd_dims *dims, ssd_dtype dtype, ssd_plan *out,
@@ -339,45 +423,23 @@ ssd_status ssd_forward_default_plan(const ssd_dims *dims, ssd_dtype dtype, ssd_p
   return SSD_OK;
 }
 
-ssd_status ssd_forward_get_plan(const ssd_dims *dims, ssd_dtype dtype, ssd_plan *out) {
-  Dims d;
-  const ssd_status s = check_dims(dims, &d);
-  if (s != SSD_OK) return s;
-  if (!valid_dtype(dtype) || !out) return SSD_ERR_INVALID_ARG;
-  if (dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
-  *out = to_public(ssd::fwd_current_plan(d));
-  return SSD_OK;
-}
-
-ssd_status ssd_forward_set_plan(const ssd_dims *dims, ssd_dtype dtype, const ssd_plan *plan) {
-  Dims d;
-  const ssd_status s = check_dims(dims, &d);
-  if (s != SSD_OK) return s;
-  if (!valid_dtype(dtype)) return SSD_ERR_INVALID_ARG;
-  if (dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
-  if (!plan) return ssd::fwd_install_plan(d, nullptr) ? SSD_OK : SSD_ERR_CUDA;
-  const ssd::FwdPlan p = from_public(*plan);
-  if (!ssd::fwd_plan_ok(d, p)) return SSD_ERR_INVALID_ARG;
-  return ssd::fwd_install_plan(d, &p) ? SSD_OK : SSD_ERR_CUDA;
-}
-
 ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
                             const float *A, const void *B, const void *C, const float *D,
                             const float *h0, void *y, float *final_state, void *workspace,
                             size_t ws_bytes, int reps, void *stream, ssd_plan *chosen) {
   Dims d;
-  ssd_status s = check_dims(dims, &d);
+  ssd_status s = ssd::check_forward_args(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, &d);
   if (s != SSD_OK) return s;
-  if (!valid_dtype(dtype) || !req(x) || !req(dt) || !req(A) || !req(B) || !req(C) ||
-      !opt(D) || !opt(h0) || !req(y) || !opt(final_state) || !workspace ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) || reps < 1 || reps > 1000)
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || reps < 1 ||
+      reps > 1000 || !chosen)
     return SSD_ERR_INVALID_ARG;
   if (dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
   const WsLayout w = ws_layout(d, dtype);
   if (ws_bytes < w.total) return SSD_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
+  int *err = static_cast<int *>(workspace);
   // the start states the output kernels read, from one pass with the
-  // current plan
+  // default plan
   s = ssd_forward(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, workspace, ws_bytes,
                   stream);
   if (s != SSD_OK) return s;
@@ -388,7 +450,7 @@ ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   cudaError_t e = cudaEventCreate(&e0);
   if (e == cudaSuccess) e = cudaEventCreate(&e1);
-  ssd::FwdPlan best = ssd::fwd_current_plan(d);
+  ssd::FwdPlan best = ssd::fwd_default_plan(d);
   std::vector<ssd::CsPlan> cs;
   std::vector<ssd::FwdPlan> sc;
   ssd::fwd_cs_candidates(d, &cs);
@@ -397,8 +459,8 @@ ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x
   for (size_t i = 0; i < cs.size() && e == cudaSuccess; ++i) {
     float ms = 0.f;
     e = time_launches(
-        [&] { return ssd::launch_fwd_chunk_state(d, x, B, dt, A, dH, gam, cs[i], st); }, reps,
-        st, e0, e1, &ms);
+        [&] { return ssd::launch_fwd_chunk_state(d, x, B, dt, A, dH, gam, cs[i], err, st); },
+        reps, st, e0, e1, &ms);
     if (e == cudaSuccess && ms < best_ms) {
       best_ms = ms;
       best.cs = cs[i];
@@ -407,7 +469,7 @@ ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x
   best_ms = 3.0e38f;
   for (size_t i = 0; i < sc.size() && e == cudaSuccess; ++i) {
     float ms = 0.f;
-    e = time_launches([&] { return launch_scan(d, sc[i], x, B, C, dt, A, sts, D, y, st); },
+    e = time_launches([&] { return launch_scan(d, sc[i], x, B, C, dt, A, sts, D, y, err, st); },
                       reps, st, e0, e1, &ms);
     if (e == cudaSuccess && ms < best_ms) {
       best_ms = ms;
@@ -417,12 +479,13 @@ ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x
   }
   if (e0) cudaEventDestroy(e0);
   if (e1) cudaEventDestroy(e1);
-  if (e != cudaSuccess || !ssd::fwd_install_plan(d, &best)) return SSD_ERR_CUDA;
-  s = ssd_forward(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, workspace, ws_bytes,
-                  stream);
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
+  const ssd_plan pub = to_public(best);
+  s = ssd_forward_ex(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, workspace, ws_bytes,
+                     &pub, stream);
   if (s != SSD_OK) return s;
   if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
-  if (chosen) *chosen = to_public(best);
+  *chosen = pub;
   return SSD_OK;
 }
 
@@ -436,13 +499,17 @@ size_t ssd_forward_host_workspace_size(const ssd_dims *dims, ssd_dtype dtype, in
 ssd_status ssd_forward_host(const ssd_dims *dims, ssd_dtype dtype, const void *x,
                             const void *dt, const float *A, const void *B, const void *C,
                             const float *D, const float *h0, void *y, float *final_state,
-                            void *workspace, size_t ws_bytes, void *stream) {
+                            void *workspace, size_t ws_bytes, const ssd_plan *plan,
+                            void *stream) {
   Dims d;
   ssd_status s = check_dims(dims, &d);
   if (s != SSD_OK) return s;
   if (!valid_dtype(dtype) || !x || !dt || !A || !B || !C || !y || !workspace ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return SSD_ERR_INVALID_ARG;
+  ssd::FwdPlan fp{};
+  s = resolve_plan(d, dtype, plan, &fp);
+  if (s != SSD_OK) return s;
   const HostLayout hl = host_layout(d, dtype, D != nullptr, h0 != nullptr, final_state != nullptr);
   if (ws_bytes < hl.total) return SSD_ERR_INVALID_ARG;
   char *ws = static_cast<char *>(workspace);
@@ -461,11 +528,13 @@ ssd_status ssd_forward_host(const ssd_dims *dims, ssd_dtype dtype, const void *x
   h2d(hl.D, D, sizeof(float) * d.nh);
   h2d(hl.h0, h0, sizeof(float) * d.b * d.nh * d.P * d.S);
   if (err != cudaSuccess) return SSD_ERR_CUDA;
-  s = ssd_forward(dims, dtype, ws + hl.x, ws + hl.dt, reinterpret_cast<float *>(ws + hl.A),
-                  ws + hl.B, ws + hl.C, D ? reinterpret_cast<float *>(ws + hl.D) : nullptr,
-                  h0 ? reinterpret_cast<float *>(ws + hl.h0) : nullptr, ws + hl.y,
-                  final_state ? reinterpret_cast<float *>(ws + hl.fin) : nullptr, ws + hl.fwd,
-                  hl.fwd_bytes, stream);
+  // the forward's workspace sits at offset 0, so its error word is this
+  // workspace's
+  s = ssd_forward_ex(dims, dtype, ws + hl.x, ws + hl.dt, reinterpret_cast<float *>(ws + hl.A),
+                     ws + hl.B, ws + hl.C, D ? reinterpret_cast<float *>(ws + hl.D) : nullptr,
+                     h0 ? reinterpret_cast<float *>(ws + hl.h0) : nullptr, ws + hl.y,
+                     final_state ? reinterpret_cast<float *>(ws + hl.fin) : nullptr,
+                     ws + hl.fwd, hl.fwd_bytes, plan, stream);
   if (s != SSD_OK) return s;
   err = cudaMemcpyAsync(y, ws + hl.y, e * d.b * d.L * d.nh * d.P, cudaMemcpyDeviceToHost, st);
   if (err == cudaSuccess && final_state)

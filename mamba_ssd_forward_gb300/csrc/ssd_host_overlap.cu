@@ -45,11 +45,13 @@ std::vector<Slice> plan_slices(const ssd_dims &d, int n) {
 }
 
 // x, dt and y go through double buffers slice by slice (each slice's dt
-// then starts on a 256-byte boundary, as ssd_forward needs 16); B, C and h0
-// (whose slices start on 16-byte boundaries anyway) are uploaded whole
-// before the first slice, and the final state of batch slices is gathered
-// whole and downloaded after the last slice: fewer, larger copies, each copy
-// having a fixed cost on the copy engines.
+// then starts on a 256-byte boundary, as ssd_forward needs 16); B and C have
+// room for the whole tensors and each slice's rows (contiguous, starting on
+// 16-byte boundaries) are uploaded with that slice, so the first forward
+// pass waits only for its own inputs; h0 of batch slices is uploaded whole
+// before the first slice, and their final states are gathered whole and
+// downloaded after the last slice: fewer, larger copies, each copy having a
+// fixed cost on the copy engines.
 struct Layout {
   size_t fwd, fwd_bytes, A, D, B, C, h0, fin, carry[2], x[2], dt[2], y[2], total;
 };
@@ -109,8 +111,8 @@ ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype, co
                                        const void *dt, const float *A, const void *B,
                                        const void *C, const float *D, const float *h0,
                                        void *y, float *final_state, void *workspace,
-                                       size_t ws_bytes, int n_slices, void *stream,
-                                       void *h2d_stream, void *d2h_stream) {
+                                       size_t ws_bytes, int n_slices, const ssd_plan *plan,
+                                       void *stream, void *h2d_stream, void *d2h_stream) {
   // malformed or unsupported dims: the codes ssd_forward gives, nothing enqueued
   if (!valid_dims(dims))
     return ssd_forward(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, nullptr, 0, stream);
@@ -122,6 +124,14 @@ ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype, co
   const bool seq = d.batch == 1 && sl.size() > 1;
   const Layout l = layout(d, dtype, sl, D != nullptr, h0 != nullptr, final_state != nullptr);
   if (ws_bytes < l.total) return SSD_ERR_INVALID_ARG;
+  // the plan must suit every slice's dims before anything is enqueued
+  for (const Slice &s : sl) {
+    ssd_dims sd = d;
+    sd.batch = s.nb;
+    sd.seqlen = s.nt;
+    const ssd_status ps = ssd::plan_status(&sd, dtype, plan);
+    if (ps != SSD_OK) return ps;
+  }
   char *ws = static_cast<char *>(workspace);
   const size_t e = dtype == SSD_BF16 ? 2 : 4;
   cudaStream_t st = (cudaStream_t)stream;
@@ -130,9 +140,9 @@ ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype, co
   const size_t state = sizeof(float) * d.nheads * d.headdim * d.dstate;
   const int n = (int)sl.size();
 
-  // events: begin, the end of the uploads, and per slice: inputs in,
-  // forward done, outputs out
-  std::vector<cudaEvent_t> ev(2 + 3 * (size_t)n, nullptr);
+  // events: begin, the end of the uploads, the end of the downloads, and per
+  // slice: inputs in, forward done, outputs out
+  std::vector<cudaEvent_t> ev(3 + 3 * (size_t)n, nullptr);
   cudaError_t err = cudaSuccess;
   for (auto &v : ev)
     if (err == cudaSuccess) err = cudaEventCreateWithFlags(&v, cudaEventDisableTiming);
@@ -142,10 +152,10 @@ ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype, co
     return r == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
   };
   if (err != cudaSuccess) return done_with_events(err);
-  cudaEvent_t ev_begin = ev[0], ev_up_end = ev[1];
-  auto ev_in = [&](int i) { return ev[2 + 3 * i]; };
-  auto ev_done = [&](int i) { return ev[3 + 3 * i]; };
-  auto ev_out = [&](int i) { return ev[4 + 3 * i]; };
+  cudaEvent_t ev_begin = ev[0], ev_up_end = ev[1], ev_down_end = ev[2];
+  auto ev_in = [&](int i) { return ev[3 + 3 * i]; };
+  auto ev_done = [&](int i) { return ev[4 + 3 * i]; };
+  auto ev_out = [&](int i) { return ev[5 + 3 * i]; };
   auto ok = [&](cudaError_t r) {
     if (err == cudaSuccess) err = r;
     return err == cudaSuccess;
@@ -162,9 +172,6 @@ ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype, co
   if (ds != st) ok(cudaStreamWaitEvent(ds, ev_begin, 0));
   up(l.A, A, sizeof(float) * d.nheads);
   up(l.D, D, sizeof(float) * d.nheads);
-  const size_t tok_all = (size_t)d.batch * d.seqlen;
-  up(l.B, B, e * tok_all * d.ngroups * d.dstate);
-  up(l.C, C, e * tok_all * d.ngroups * d.dstate);
   if (seq)
     up(l.carry[0], h0, state);
   else
@@ -179,6 +186,9 @@ ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype, co
     up(l.x[p], static_cast<const char *>(x) + e * tok0 * d.nheads * d.headdim,
        e * ntok * d.nheads * d.headdim);
     up(l.dt[p], static_cast<const char *>(dt) + e * tok0 * d.nheads, e * ntok * d.nheads);
+    const size_t bc_off = e * tok0 * d.ngroups * d.dstate, bc_len = e * ntok * d.ngroups * d.dstate;
+    up(l.B + bc_off, static_cast<const char *>(B) + bc_off, bc_len);
+    up(l.C + bc_off, static_cast<const char *>(C) + bc_off, bc_len);
     ok(cudaEventRecord(ev_in(i), hs));
     // forward of slice i (its y buffer is free once the download of slice
     // i - 2 is done)
@@ -194,12 +204,14 @@ ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype, co
     float *h_out = seq ? reinterpret_cast<float *>(ws + l.carry[p ^ 1])
                        : (final_state ? reinterpret_cast<float *>(ws + l.fin + s.b0 * state)
                                       : nullptr);
-    status = ssd_forward(&sd, dtype, ws + l.x[p], ws + l.dt[p],
-                         reinterpret_cast<const float *>(ws + l.A),
-                         ws + l.B + e * tok0 * d.ngroups * d.dstate,
-                         ws + l.C + e * tok0 * d.ngroups * d.dstate,
-                         D ? reinterpret_cast<const float *>(ws + l.D) : nullptr, h_in,
-                         ws + l.y[p], h_out, ws + l.fwd, l.fwd_bytes, stream);
+    // the forward's workspace sits at offset 0: its error word is this
+    // workspace's
+    status = ssd_forward_ex(&sd, dtype, ws + l.x[p], ws + l.dt[p],
+                            reinterpret_cast<const float *>(ws + l.A),
+                            ws + l.B + e * tok0 * d.ngroups * d.dstate,
+                            ws + l.C + e * tok0 * d.ngroups * d.dstate,
+                            D ? reinterpret_cast<const float *>(ws + l.D) : nullptr, h_in,
+                            ws + l.y[p], h_out, ws + l.fwd, l.fwd_bytes, plan, stream);
     ok(cudaEventRecord(ev_done(i), st));
     // outputs of slice i
     ok(cudaStreamWaitEvent(ds, ev_done(i), 0));
@@ -213,12 +225,20 @@ ssd_status ssd_forward_host_overlapped(const ssd_dims *dims, ssd_dtype dtype, co
     }
     ok(cudaEventRecord(ev_out(i), ds));
   }
-  // the caller's stream is ordered after the uploads and the downloads
-  if (err == cudaSuccess && status == SSD_OK) {
-    ok(cudaEventRecord(ev_up_end, hs));
-    ok(cudaStreamWaitEvent(st, ev_up_end, 0));
-    ok(cudaStreamWaitEvent(st, ev_out(n - 1), 0));
-  }
+  // The caller's stream is ordered after everything enqueued on the two copy
+  // streams -- also when a step above failed, so that the caller never frees
+  // or reuses the host buffers or the workspace while a copy already queued
+  // is still running.  Each join is attempted whatever happened before.
+  cudaError_t jerr = cudaSuccess;
+  auto join = [&](cudaStream_t from, cudaEvent_t evt) {
+    if (from == st) return;
+    cudaError_t r = cudaEventRecord(evt, from);
+    if (r == cudaSuccess) r = cudaStreamWaitEvent(st, evt, 0);
+    if (jerr == cudaSuccess) jerr = r;
+  };
+  join(hs, ev_up_end);
+  join(ds, ev_down_end);
+  if (err == cudaSuccess) err = jerr;
   const ssd_status r = done_with_events(err);
   return status != SSD_OK ? status : r;
 }

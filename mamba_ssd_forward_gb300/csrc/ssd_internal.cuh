@@ -28,11 +28,41 @@ __device__ __forceinline__ void st_io(__nv_bfloat16 *p, float v) {
   *p = __float2bfloat16_rn(v);
 }
 
-// Address of the device error word (current device); kernels that give up a
-// bounded wait write a nonzero code there.
+// Address of the library-wide device error word (current device), used by
+// the calls that have no workspace of their own (the step-wise entry points,
+// ssd_forward_noalloc, the self-test by default); kernels that give up a
+// bounded wait write a nonzero code there.  Null if the look-up failed.
 int *device_error_word();
-// Copy the device error word to *code and clear it; synchronises `st`.
-cudaError_t read_and_clear_device_error(cudaStream_t st, int *code);
+// Copy the error word at `word` (device) to *code and clear it; synchronises
+// `st`.
+cudaError_t read_and_clear_error(int *word, cudaStream_t st, int *code);
+
+// SM count of the current device, looked up once per device and cached
+// (race-free under concurrent callers).
+int sm_count();
+
+// Workspace header of ssd_forward and the host-buffer calls: the first
+// SSD_WS_HEADER_BYTES bytes.  Word 0 is the call's error word.
+constexpr size_t kWsHeader = SSD_WS_HEADER_BYTES;
+
+// Argument checks of ssd_forward (dims, dtype and tensor pointers; not the
+// workspace), with the validated dims in *out.
+ssd_status check_forward_args(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                              const void *dt, const float *A, const void *B, const void *C,
+                              const float *D, const float *h0, const void *y,
+                              const float *final_state, Dims *out);
+// The forward pass behind ssd_forward, ssd_forward_ex and ssd_forward_profiled:
+// plan NULL = the default plan; err NULL = the workspace's own error word;
+// events / n_events / n_launches as for ssd_forward_profiled.
+ssd_status forward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
+                        const float *A, const void *B, const void *C, const float *D,
+                        const float *h0, void *y, float *final_state, void *workspace,
+                        size_t ws_bytes, const ssd_plan *plan, int *err, cudaStream_t st,
+                        void *const *events, int n_events, int *n_launches);
+
+// SSD_OK if `plan` (NULL = the default) can run these dims and dtype, else
+// the code ssd_forward_ex would return for it.
+ssd_status plan_status(const ssd_dims *dims, ssd_dtype dtype, const ssd_plan *plan);
 
 // Launchers (one per step).  Each enqueues its kernel(s) on `st` and returns
 // the cudaGetLastError() of the launch.
@@ -40,7 +70,7 @@ cudaError_t launch_chunk_cumsum(const Dims &d, ssd_dtype io, const void *dt,
                                 const float *A, float *G, cudaStream_t st);
 cudaError_t launch_chunk_state(const Dims &d, ssd_dtype io, const void *x,
                                const void *B, const void *dt, const float *G,
-                               float *dstates, cudaStream_t st);
+                               float *dstates, int *err, cudaStream_t st);
 cudaError_t launch_state_passing(const Dims &d, const float *dstates,
                                  const float *G, const float *h0,
                                  float *states, float *final_state,
@@ -48,7 +78,7 @@ cudaError_t launch_state_passing(const Dims &d, const float *dstates,
 cudaError_t launch_chunk_scan(const Dims &d, ssd_dtype io, const void *x,
                               const void *B, const void *C, const void *dt,
                               const float *G, const float *states,
-                              const float *D, void *y, cudaStream_t st);
+                              const float *D, void *y, int *err, cudaStream_t st);
 
 // Single-token decode step (decode_step.cu).
 cudaError_t launch_decode_step(int64_t b, int64_t nh, int64_t P, int64_t S, int64_t ng,

@@ -1,52 +1,23 @@
-// Launch plans of the bf16 forward path: the candidates, the cost-model
-// default, and the per-process table of installed plans that ssd_forward
-// reads.  Host code only; the plans change launch shapes, never results.
-#include <map>
-#include <mutex>
-#include <tuple>
-
+// Launch plans of the bf16 forward path: the candidates and the cost-model
+// default.  Host code only, and stateless: a plan is passed to each call
+// explicitly (or the default is used); the plans change launch shapes, never
+// results.
 #include "fwd.cuh"
 #include "ssd_internal.cuh"
 
 namespace ssd {
-namespace {
-
-using Key = std::tuple<int, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t>;
-
-std::mutex &table_mutex() {
-  static std::mutex m;
-  return m;
-}
-std::map<Key, FwdPlan> &table() {
-  static std::map<Key, FwdPlan> t;
-  return t;
-}
-
-bool key_of(const Dims &d, Key *k) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  *k = Key(dev, d.b, d.L, d.nh, d.P, d.S, d.ng, d.T);
-  return true;
-}
-
-}  // namespace
 
 FwdPlan fwd_default_plan(const Dims &d) {
   FwdPlan p;
   p.cs = chunk_state_plan(d);
+  if (false && fwd_out_supported(d)) {
+    p.scan_kernel = 3;
+    p.scan_heads = fwd_out_heads(d);
+    return p;
+  }
   p.scan_kernel = fwd_scan_chunk_supported(d) ? 1 : fwd_scan_chunk_split_supported(d) ? 2 : 0;
   p.scan_heads = p.scan_kernel ? fwd_scan_chunk_heads(d, p.scan_kernel == 2) : fwd_scan_heads(d);
   return p;
-}
-
-FwdPlan fwd_current_plan(const Dims &d) {
-  Key k;
-  if (key_of(d, &k)) {
-    std::lock_guard<std::mutex> g(table_mutex());
-    const auto it = table().find(k);
-    if (it != table().end()) return it->second;
-  }
-  return fwd_default_plan(d);
 }
 
 void fwd_cs_candidates(const Dims &d, std::vector<CsPlan> *out) {
@@ -58,6 +29,12 @@ void fwd_cs_candidates(const Dims &d, std::vector<CsPlan> *out) {
 void fwd_scan_candidates(const Dims &d, std::vector<FwdPlan> *out) {
   FwdPlan p{};
   p.cs = CsPlan{0, 0};
+  for (int hs = 1; hs <= d.hpg; ++hs)
+    if (false && fwd_out_heads_ok(d, hs)) {
+      p.scan_kernel = 3;
+      p.scan_heads = hs;
+      out->push_back(p);
+    }
   for (int kind = 1; kind <= 2; ++kind)
     for (int hs = 1; hs <= d.hpg; ++hs)
       if (fwd_scan_chunk_heads_ok(d, hs, kind == 2)) {
@@ -78,18 +55,8 @@ bool fwd_plan_ok(const Dims &d, const FwdPlan &p) {
   if (p.scan_kernel == 1 || p.scan_kernel == 2)
     return fwd_scan_chunk_heads_ok(d, p.scan_heads, p.scan_kernel == 2);
   if (p.scan_kernel == 0) return fwd_scan_heads_ok(d, p.scan_heads);
+  if (p.scan_kernel == 3) return fwd_out_heads_ok(d, p.scan_heads);
   return false;
-}
-
-bool fwd_install_plan(const Dims &d, const FwdPlan *p) {
-  Key k;
-  if (!key_of(d, &k)) return false;
-  std::lock_guard<std::mutex> g(table_mutex());
-  if (p)
-    table()[k] = *p;
-  else
-    table().erase(k);
-  return true;
 }
 
 }  // namespace ssd

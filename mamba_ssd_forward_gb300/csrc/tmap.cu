@@ -1,4 +1,6 @@
-// TMA tensor-map construction and the device error word.
+// TMA tensor-map construction, the library-wide device error word and the
+// per-device SM count.
+#include <atomic>
 #include <mutex>
 
 #include "ssd_internal.cuh"
@@ -49,15 +51,14 @@ bool make_tmap_sw128(CUtensorMap *map, const void *base, bool bf16, int rank,
   return r == CUDA_SUCCESS;
 }
 
-// Device error word: kernels that give up a bounded wait record a code here.
+// Device error word: kernels that give up a bounded wait record a code here
+// when the call has no workspace of its own.
 __device__ int g_device_error = 0;
 
-cudaError_t read_and_clear_device_error(cudaStream_t st, int *code) {
+cudaError_t read_and_clear_error(int *word, cudaStream_t st, int *code) {
   int zero = 0;
-  cudaError_t e = cudaMemcpyFromSymbolAsync(code, g_device_error, sizeof(int), 0,
-                                            cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess)
-    e = cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st);
+  cudaError_t e = cudaMemcpyAsync(code, word, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(word, &zero, sizeof(int), cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return e;
 }
@@ -66,6 +67,19 @@ int *device_error_word() {
   void *p = nullptr;
   if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
   return static_cast<int *>(p);
+}
+
+int sm_count() {
+  constexpr int kMaxDev = 256;
+  static std::atomic<int> cache[kMaxDev];  // 0 = not looked up yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 148;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  cache[dev].store(n, std::memory_order_relaxed);  // every thread stores the same value
+  return n;
 }
 
 }  // namespace ssd

@@ -63,3 +63,17 @@ def oracle_run(w, inp, bh=None, want=("y", "final_state")):
 
 def make(w, seed=0):
     return ssd_inputs.make_inputs(w, seed)
+
+
+def forward_checked(ssd, dev, chunk, h0=None, plan=None, workspace=None, y=None,
+                    final_state=None):
+    """ssd.forward on device inputs `dev` with a workspace of its own (or the
+    given one), then the workspace's error word must be clear: no bounded
+    device-side wait of the call gave up."""
+    if workspace is None:
+        workspace = ssd.new_workspace(ssd.workspace_size(dev["x"], dev["B"], chunk),
+                                      dev["x"].device)
+    out = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], h0,
+                      chunk=chunk, workspace=workspace, y=y, final_state=final_state, plan=plan)
+    ssd.workspace_error(workspace)
+    return out

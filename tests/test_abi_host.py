@@ -64,13 +64,14 @@ def dims(**kw):
 def test_workspace_size(lib):
     d = dims()
     nc = 4
+    hdr = 256  # SSD_WS_HEADER_BYTES: the call's error word
     # bf16: the per-chunk start states in bf16
     ws = lib.ssd_forward_workspace_size(ctypes.byref(d), 1)
-    assert ws >= 2 * 2 * 8 * nc * 64 * 128
+    assert ws >= hdr + 2 * 2 * 8 * nc * 64 * 128
     assert ws % 256 == 0
     # fp32: G, the chunk jump terms and the states, fp32
     ws = lib.ssd_forward_workspace_size(ctypes.byref(d), 0)
-    assert ws >= 4 * 2 * 8 * nc * 256 + 2 * 4 * 2 * 8 * nc * 64 * 128
+    assert ws >= hdr + 4 * 2 * 8 * nc * 256 + 2 * 4 * 2 * 8 * nc * 64 * 128
     assert ws % 256 == 0
     assert lib.ssd_forward_workspace_size(ctypes.byref(d), 7) == 0
     assert lib.ssd_forward_workspace_size(None, 1) == 0
@@ -154,6 +155,11 @@ def test_noalloc_limit_and_rejections(lib):
     assert lib.ssd_forward_workspace_size(ctypes.byref(big), 1) > _abi.SSD_NOALLOC_SCRATCH_BYTES
     args = [fake, fake, fake, fake, fake, None, None, fake, None, None]
     assert lib.ssd_forward_noalloc(ctypes.byref(big), 1, *args) == _abi.SSD_ERR_UNSUPPORTED
+    # pointers are checked before the size, with ssd_forward's codes
+    null_x = [None] + args[1:]
+    assert lib.ssd_forward_noalloc(ctypes.byref(big), 1, *null_x) == _abi.SSD_ERR_INVALID_ARG
+    odd_y = args[:7] + [ctypes.c_void_p((1 << 20) + 4)] + args[8:]
+    assert lib.ssd_forward_noalloc(ctypes.byref(big), 1, *odd_y) == _abi.SSD_ERR_INVALID_ARG
     assert lib.ssd_forward_noalloc(ctypes.byref(dims(ngroups=3)), 1, *args) == 1
     assert lib.ssd_forward_noalloc(ctypes.byref(dims(chunk=96)), 1, *args) == 2
     assert lib.ssd_forward_noalloc(ctypes.byref(dims()), 7, *args) == 1
@@ -194,11 +200,21 @@ def test_host_overlapped_sizes_and_rejections(lib):
     host = [ok] * 5 + [None, None, ok, None]
     ws = lib.ssd_forward_host_overlapped_workspace_size(ctypes.byref(d4), 1, 0, 0, 0, 2)
     assert lib.ssd_forward_host_overlapped(ctypes.byref(d4), 1, *host, ok, ws, 0, None, None,
-                                           None) == 1  # n_slices
+                                           None, None) == 1  # n_slices
     assert lib.ssd_forward_host_overlapped(ctypes.byref(d4), 1, *host, ok, ws - 256, 2, None,
-                                           None, None) == 1  # workspace too small
+                                           None, None, None) == 1  # workspace too small
     assert lib.ssd_forward_host_overlapped(ctypes.byref(dims(headdim=144)), 1, *host, ok, ws, 2,
-                                           None, None, None) == 2
+                                           None, None, None, None) == 2
+    # a plan that is not a candidate, rejected before any copy is enqueued
+    from mamba_ssd_forward_gb300 import _abi
+    bad = _abi.SsdPlan(3, 1, 1, 3)
+    assert lib.ssd_forward_host_overlapped(ctypes.byref(d4), 1, *host, ok, ws, 2,
+                                           ctypes.byref(bad), None, None, None) == 1
+    # any plan with fp32 I/O
+    good = _abi.SsdPlan(**__import__("mamba_ssd_forward_gb300").default_plan(d4))
+    ws32 = lib.ssd_forward_host_overlapped_workspace_size(ctypes.byref(d4), 0, 0, 0, 0, 2)
+    assert lib.ssd_forward_host_overlapped(ctypes.byref(d4), 0, *host, ok, ws32, 2,
+                                           ctypes.byref(good), None, None, None) == 1
 
 
 def _dims(b, L, nh, P, S, ng, T):
@@ -239,8 +255,6 @@ def test_plan_candidates_are_valid_and_hold_the_default(lib, shape):
     assert default in cands
     expect = 1 if chunk_kernel_ok else 2 if split_kernel_ok else 0
     assert default["scan_kernel"] == expect
-    # without an installed plan the forward pass uses the default
-    assert m.get_plan(d) == default
 
 
 def test_plan_rejections(lib):
@@ -260,16 +274,48 @@ def test_plan_rejections(lib):
         {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 0, "scan_heads": 8},
         {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 3, "scan_heads": 1},
     ]
+    # a plan that is not a candidate is rejected by every call taking one,
+    # before anything is launched (fake aligned pointers, never dereferenced)
+    ok = ctypes.c_void_p(1 << 20)
+    ws = lib.ssd_forward_workspace_size(ctypes.byref(d), 1)
+    args = [ok, ok, ok, ok, ok, None, None, ok, None, ok, ws]
+    n = ctypes.c_int(-1)
     for p in bad:
         assert p not in m.plan_candidates(d)
-        with pytest.raises(_abi.SsdError) as e:
-            m.set_plan(d, p)
-        assert e.value.code == _abi.SSD_ERR_INVALID_ARG
+        ref = ctypes.byref(_abi.SsdPlan(**p))
+        assert lib.ssd_forward_ex(ctypes.byref(d), 1, *args, ref, None) == 1
+        assert lib.ssd_forward_profiled(ctypes.byref(d), 1, *args, ref, None, None, 0,
+                                        ctypes.byref(n)) == 1
+        assert n.value == -1  # nothing launched, nothing reported
+        assert lib.ssd_forward_host(ctypes.byref(d), 1, *args, ref, None) == 1
+    # fp32 calls take no plan
+    good = ctypes.byref(_abi.SsdPlan(**m.default_plan(d)))
+    ws32 = lib.ssd_forward_workspace_size(ctypes.byref(d), 0)
+    assert lib.ssd_forward_ex(ctypes.byref(d), 0, *args[:-1], ws32, good, None) == 1
+    # events promised but missing
+    assert lib.ssd_forward_profiled(ctypes.byref(d), 1, *args, None, None, None, 2, None) == 1
     rc = lib.ssd_forward_tune(ctypes.byref(d), 1, *([None] * 10), 0, 5, None, None)
+    assert rc == _abi.SSD_ERR_INVALID_ARG
+    # a tuner call with valid arguments but nowhere to put the chosen plan
+    rc = lib.ssd_forward_tune(ctypes.byref(d), 1, *args, 5, None, None)
     assert rc == _abi.SSD_ERR_INVALID_ARG
 
 
-def test_selftest_rejects_limits_out_of_range(lib):
+def test_selftest_and_error_reads_reject_bad_arguments(lib):
     from mamba_ssd_forward_gb300 import _abi
     for bad in (0, 999, 1_000_000_001):
-        assert lib.ssd_selftest_bounded_wait(bad, None) == _abi.SSD_ERR_INVALID_ARG
+        assert lib.ssd_selftest_bounded_wait(bad, None, None) == _abi.SSD_ERR_INVALID_ARG
+    # an error word must be 4-byte aligned
+    assert lib.ssd_selftest_bounded_wait(2_000_000, ctypes.c_void_p((1 << 20) + 2), None) == 1
+    # a workspace's error word: NULL or misaligned workspaces are rejected
+    assert lib.ssd_workspace_error(None, None) == 1
+    assert lib.ssd_workspace_error(ctypes.c_void_p((1 << 20) + 16), None) == 1
+
+
+def test_library_keeps_no_plan_table():
+    """Launch plans are arguments, never stored: the plan code holds no
+    table, and the header declares no call that installs one."""
+    src = open(os.path.join(ROOT, "mamba_ssd_forward_gb300", "csrc", "ssd_plan.cu")).read()
+    assert "std::map" not in src and "mutex" not in src and "static" not in src
+    names = declared_functions()
+    assert "ssd_forward_set_plan" not in names and "ssd_forward_get_plan" not in names

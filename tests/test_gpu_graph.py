@@ -31,8 +31,7 @@ def ssd():
 ], ids=lambda w: w.name)
 def test_forward_replays_in_a_cuda_graph(ssd, w):
     dev = device_inputs(make(w, seed=0))
-    ws = torch.empty(ssd.workspace_size(dev["x"], dev["B"], w.chunk), dtype=torch.uint8,
-                     device="cuda")
+    ws = ssd.new_workspace(ssd.workspace_size(dev["x"], dev["B"], w.chunk), "cuda")
     y = torch.empty_like(dev["x"])
     fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32,
                       device="cuda")
@@ -57,7 +56,7 @@ def test_forward_replays_in_a_cuda_graph(ssd, w):
             dev[k].copy_(v)
     g.replay()
     torch.cuda.synchronize()
-    ssd.device_error()
+    ssd.workspace_error(ws)
     ref = oracle_run(w, inp2)
     check_io(to64(y), ref["y"], w.dtype, "graph replay y")
     check_io(to64(fin), ref["final_state"], w.dtype, "graph replay final_state")

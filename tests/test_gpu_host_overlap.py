@@ -45,14 +45,15 @@ def test_overlapped_matches_device_forward(ssd, w, n):
     h = {k: (None if v is None else v.contiguous().pin_memory()) for k, v in inp.items()}
     y = torch.full_like(h["x"], float("nan")).pin_memory()
     fin = torch.full((w.batch, w.nheads, w.headdim, w.dstate), float("nan")).pin_memory()
-    ws = torch.empty(ssd.host_overlapped_workspace_size(h["x"], h["B"], w.chunk, n, True,
-                                                        h["h0"] is not None, True),
-                     dtype=torch.uint8, device="cuda")
+    ws = ssd.new_workspace(ssd.host_overlapped_workspace_size(h["x"], h["B"], w.chunk, n, True,
+                                                              h["h0"] is not None, True),
+                           "cuda")
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ssd.forward_host_overlapped(h["x"], h["dt"], h["A"], h["B"], h["C"], h["D"], h["h0"],
                                 w.chunk, ws, y, fin, n_slices=n, h2d_stream=s_in,
                                 d2h_stream=s_out)
     torch.cuda.current_stream().synchronize()
+    ssd.workspace_error(ws)
     assert torch.isfinite(y.float()).all() and torch.isfinite(fin).all()
     assert rel_l2(to64(y), to64(y_dev)) < 1e-6
     assert rel_l2(to64(fin), to64(f_dev)) < 1e-6

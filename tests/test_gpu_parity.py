@@ -8,8 +8,8 @@ import numpy as np
 import pytest
 import torch
 
-from parity import (LN2, LOG2E, check_io, device_inputs, make, oracle_run, rel_l2,
-                    sample_pairs, to64)
+from parity import (LN2, LOG2E, check_io, device_inputs, forward_checked, make, oracle_run,
+                    rel_l2, sample_pairs, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -94,15 +94,13 @@ def test_each_step_small(ssd, w):
     check_io(to64(y), ref["y"], w.dtype, "chunk_scan y")
 
     # the whole forward pass
-    y2, fin2 = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
-                           h0, chunk=T)
-    torch.cuda.synchronize()
+    ssd.device_error()  # no bounded wait of the step-wise calls gave up
+    y2, fin2 = forward_checked(ssd, dev, T, h0=h0)
     check_io(to64(y2), ref["y"], w.dtype, "forward y")
     check_io(to64(fin2), ref["final_state"], w.dtype, "forward final_state")
     x64 = to64(inp["x"])
     Dx = to64(inp["D"])[None, None, :, None] * x64
     check_io(to64(y2) - Dx, ref["y"] - Dx, w.dtype, "forward y - D x")
-    ssd.device_error()  # no bounded device-side wait gave up
 
 
 def _forward_sampled(ssd, w, seed=0):
@@ -110,9 +108,7 @@ def _forward_sampled(ssd, w, seed=0):
     bh = sample_pairs(w)
     ref = oracle_run(w, inp, bh=bh)
     dev = device_inputs(inp)
-    y, fin = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
-                         dev["h0"], chunk=w.chunk)
-    ssd.device_error()
+    y, fin = forward_checked(ssd, dev, w.chunk, h0=dev["h0"])
     y64, fin64, x64 = to64(y), to64(fin), to64(inp["x"])
     D = to64(inp["D"])
     for pair in bh:
@@ -199,9 +195,7 @@ def test_steep_decay_blocks(ssd):
     assert (span > 96).any() and (span < 96).any()
     ref = oracle_run(w, inp)
     dev = device_inputs(inp)
-    y, fin = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
-                         dev["h0"], chunk=w.chunk)
-    ssd.device_error()
+    y, fin = forward_checked(ssd, dev, w.chunk, h0=dev["h0"])
     y64, x64 = to64(y), to64(inp["x"])
     Dx = to64(inp["D"])[None, None, :, None] * x64
     check_io(y64, ref["y"], w.dtype, "steep y")

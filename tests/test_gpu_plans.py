@@ -1,12 +1,13 @@
 """GPU checks of the launch plans and the timing autotuner: every candidate
 plan gives results within the parity tolerance of the oracle, plans that
 only change heads per CTA of the output kernel give identical bits, and the
-tuner installs one of the candidates."""
+tuner returns one of the candidates (installing nothing: later calls without
+a plan keep running the default)."""
 import numpy as np
 import pytest
 import torch
 
-from parity import check_io, device_inputs, make, oracle_run, to64
+from parity import check_io, device_inputs, forward_checked, make, oracle_run, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -35,15 +36,7 @@ def case(ssd):
     ref = oracle_run(CASE, inp)
     dev = device_inputs(inp)
     d = ssd.dims_of(dev["x"], dev["B"], CASE.chunk)
-    yield inp, ref, dev, d
-    ssd.set_plan(d, None)
-
-
-def _run(ssd, dev):
-    y, fin = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
-                         dev["h0"], chunk=CASE.chunk)
-    ssd.device_error()
-    return y, fin
+    return inp, ref, dev, d
 
 
 def test_every_candidate_plan_matches_the_oracle(ssd, case):
@@ -52,9 +45,7 @@ def test_every_candidate_plan_matches_the_oracle(ssd, case):
     assert len(cands) > 4
     by_kernel = {}
     for p in cands:
-        ssd.set_plan(d, p)
-        assert ssd.get_plan(d) == p
-        y, fin = _run(ssd, dev)
+        y, fin = forward_checked(ssd, dev, CASE.chunk, h0=dev["h0"], plan=p)
         check_io(to64(y), ref["y"], "bf16", f"y {p}")
         check_io(to64(fin), ref["final_state"], "bf16", f"final_state {p}")
         key = (p["chunk_state_heads"], p["chunk_state_ctas"], p["scan_kernel"])
@@ -63,22 +54,20 @@ def test_every_candidate_plan_matches_the_oracle(ssd, case):
     for ys in by_kernel.values():
         for y in ys[1:]:
             assert torch.equal(y, ys[0])
-    ssd.set_plan(d, None)
-    assert ssd.get_plan(d) == ssd.default_plan(d)
 
 
-def test_tune_installs_a_candidate(ssd, case):
+def test_tune_returns_a_candidate_and_installs_nothing(ssd, case):
     inp, ref, dev, d = case
+    y_def, _ = forward_checked(ssd, dev, CASE.chunk, h0=dev["h0"])
     plan, y, fin = ssd.tune(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
                             dev["h0"], chunk=CASE.chunk, reps=3)
-    ssd.device_error()
     assert plan in ssd.plan_candidates(d)
-    assert ssd.get_plan(d) == plan
     check_io(to64(y), ref["y"], "bf16", "tuned y")
     check_io(to64(fin), ref["final_state"], "bf16", "tuned final_state")
-    y2, _ = _run(ssd, dev)
-    assert torch.equal(y2, y)  # later calls use the installed plan
-    ssd.set_plan(d, None)
+    y2, _ = forward_checked(ssd, dev, CASE.chunk, h0=dev["h0"], plan=plan)
+    assert torch.equal(y2, y)  # the returned plan reproduces the tuner's last pass
+    y3, _ = forward_checked(ssd, dev, CASE.chunk, h0=dev["h0"])
+    assert torch.equal(y3, y_def)  # and calls without a plan still run the default
 
 
 def test_tune_rejects_fp32(ssd):
@@ -104,13 +93,7 @@ def test_candidates_other_dstate(ssd, S):
     cands = ssd.plan_candidates(d)
     assert any(p["scan_kernel"] == 2 for p in cands)
     assert all(p["scan_kernel"] != 1 for p in cands) or S == 64
-    try:
-        for p in cands:
-            ssd.set_plan(d, p)
-            y, fin = ssd.forward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
-                                 dev["h0"], chunk=w.chunk)
-            ssd.device_error()
-            check_io(to64(y), ref["y"], "bf16", f"y {p}")
-            check_io(to64(fin), ref["final_state"], "bf16", f"final_state {p}")
-    finally:
-        ssd.set_plan(d, None)
+    for p in cands:
+        y, fin = forward_checked(ssd, dev, w.chunk, h0=dev["h0"], plan=p)
+        check_io(to64(y), ref["y"], "bf16", f"y {p}")
+        check_io(to64(fin), ref["final_state"], "bf16", f"final_state {p}")

@@ -49,7 +49,12 @@ def _run(lib, w, dev, noalloc, ws=None):
                              stream)
     torch.cuda.synchronize()
     assert rc == _abi.SSD_OK, lib.ssd_status_string(rc).decode()
-    assert lib.ssd_device_error(stream) == _abi.SSD_OK
+    # the no-allocation call reports to the library-wide error word, the
+    # other to its workspace's word
+    if noalloc:
+        assert lib.ssd_device_error(stream) == _abi.SSD_OK
+    else:
+        assert lib.ssd_workspace_error(_vp(ws), stream) == _abi.SSD_OK
     return to64(y), to64(fin)
 
 
@@ -69,6 +74,7 @@ def test_noalloc_matches_forward_twice(lib, w):
     assert 0 < need <= _abi.SSD_NOALLOC_SCRATCH_BYTES
     dev = device_inputs(make(w, seed=3))
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws[:_abi.SSD_WS_HEADER_BYTES].zero_()  # a new workspace's error word starts clear
     y_ref, f_ref = _run(lib, w, dev, noalloc=False, ws=ws)
     for call in (1, 2):
         y, f = _run(lib, w, dev, noalloc=True)
