@@ -47,7 +47,8 @@ KERNEL_NAMES = {"bf16": ["fwd_chunk_state", "fwd_state_pass", "fwd_scan"],
 KERNEL_SOURCES = {"chunk_cumsum": "chunk_cumsum.cu", "chunk_state": "chunk_state.cu",
                   "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan.cu",
                   "fwd_chunk_state": "fwd_chunk_state.cu", "fwd_state_pass": "fwd_state_pass.cu",
-                  "fwd_scan": "fwd_scan.cu", "fwd_scan_chunk": "fwd_scan_chunk.cu"}
+                  "fwd_scan": "fwd_scan.cu", "fwd_scan_chunk": "fwd_scan_chunk.cu",
+                  "fwd_out": "fwd_out.cu"}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -92,11 +93,12 @@ def algorithmic_flops(w: W.Workload) -> float:
 def kernel_names(w: W.Workload, plan: dict | None = None) -> list:
     """Labels of the kernels ssd_forward launches for this workload, in
     launch order.  The bf16 output pass is the plan's output kernel:
-    fwd_scan_chunk (scan_kernel 1, or 2: one row tile per CTA) or fwd_scan
-    (0)."""
+    fwd_out (scan_kernel 3), fwd_scan_chunk (1, or 2: one row tile per CTA)
+    or fwd_scan (0)."""
     names = list(KERNEL_NAMES[w.dtype])
-    if w.dtype == "bf16" and plan is not None and plan["scan_kernel"] in (1, 2):
-        names[2] = "fwd_scan_chunk"
+    if w.dtype == "bf16" and plan is not None:
+        names[2] = {0: "fwd_scan", 1: "fwd_scan_chunk", 2: "fwd_scan_chunk",
+                    3: "fwd_out"}[plan["scan_kernel"]]
     return names
 
 
@@ -141,6 +143,7 @@ def kernel_bytes(w: W.Workload) -> dict:
         "fwd_state_pass": 2 * st16 + gam + h0 + fin,
         "fwd_scan": 2 * x + 2 * bc + dt + 2 * w.nheads * 4 + st16,
         "fwd_scan_chunk": 2 * x + 2 * bc + dt + 2 * w.nheads * 4 + st16,
+        "fwd_out": 2 * x + 2 * bc + dt + 2 * w.nheads * 4 + st16,
         "chunk_cumsum": dt + G + w.nheads * 4,
         "chunk_state": x + bc + dt + G + st,
         "state_passing": 2 * st + w.batch * w.nheads * w.nchunks * 4 + fin * (2 if w.has_h0 else 1),

@@ -11,24 +11,32 @@
 namespace ssd {
 
 // Sequential pass over chunks: per-chunk start states (bf16, [b, nh, nc, S,
-// P]) and the final state (fp32, [b, nh, P, S]) from the jump terms.
-cudaError_t launch_fwd_state_pass(const Dims &d, const void *dH, const float *gamma,
+// P]) and the final state (fp32, [b, nh, P, S]) from the jump terms and the
+// (decay, scale) pairs of fwd_chunk_state: each stored start state is the
+// carried state times its chunk's scale (a power of two: exact).
+cudaError_t launch_fwd_state_pass(const Dims &d, const void *dH, const float2 *gamma,
                                   const float *h0, void *states, float *final_state,
                                   cudaStream_t st);
 
 // Launch plans: knobs that change the speed of a kernel, never its results.
 
 // fwd_chunk_state: jump term of every chunk (bf16, [b, nh, nc, S, P]) and its
-// decay exp2(G_last) (fp32, [b, nh, nc]), all chunks in parallel, with H
-// heads per work item (sharing one load of B) and `ctas` CTAs per SM.
+// decay exp2(G_last) with the scale of its stored start state (fp32 pairs,
+// [b, nh, nc]; the scale is 1 unless the anchors are written), all chunks
+// in parallel, with H
+// heads per work item (sharing one load of B) and `ctas` CTAs per SM.  With
+// u, v, anchor not null it also writes the factored-decay inputs of
+// fwd_out: u, v fp32 [b, nh, nc * T] and anchor [b, nh, nc] = (alpha,
+// steep ? 1 : 0).
 struct CsPlan {
   int H, ctas;
 };
 CsPlan chunk_state_plan(const Dims &d);  // the cost-model choice
 bool chunk_state_plan_ok(const Dims &d, const CsPlan &plan);
 cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, const void *dt,
-                                   const float *A, void *dH, float *gamma, const CsPlan &plan,
-                                   int *err, cudaStream_t st);
+                                   const float *A, void *dH, float2 *gamma, float *u, float *v,
+                                   float2 *anchor, const CsPlan &plan, int *err,
+                                   cudaStream_t st);
 
 // Output pass, y from x, B, C, dt, A, D and the bf16 per-chunk states, by
 // one of two kernels with an explicit number of heads per CTA.
@@ -61,7 +69,8 @@ bool fwd_out_heads_ok(const Dims &d, int hs);
 int fwd_out_heads(const Dims &d);  // the cost-model choice
 cudaError_t launch_fwd_out(const Dims &d, const void *x, const void *B, const void *C,
                            const void *dt, const float *A, const void *states, const float *D,
-                           void *y, int hs, int *err, cudaStream_t st);
+                           const float *u, const float *v, const float2 *anchor, void *y,
+                           int hs, int *err, cudaStream_t st);
 
 // Heads per CTA of fwd_scan: the largest divisor of nheads/ngroups that is
 // at most 4 and keeps heads * P <= 256 tensor-memory columns.

@@ -1,7 +1,7 @@
 // Forward path, chunk jump terms (bf16 I/O): for every chunk k and head h,
 //
 //   dH[k] = sum_{j in chunk} (exp2(G_last - G_j) dt_j) B_j (outer) x_j      (S x P)
-//   gamma[k] = exp2(G_last)
+//   gamma[k] = (exp2(G_last), the scale of the stored start state)
 //
 // ("Accelerating Mamba-2 with High-Performance Forward Pass Kernels in NVIDIA
 // CUDA Tile", section "Mamba-2 architecture": the second term of the
@@ -30,7 +30,13 @@
 //                  over the item's stages): each dH tile staged in shared
 //                  memory and written by a TMA store as bf16
 //                  [b, nh, nc, S, P] (p contiguous, the layout the output
-//                  kernel reads); gamma as fp32.
+//                  kernel reads); gamma as fp32 pairs (decay, state
+//                  scale: 2^alpha with the factored output pass, else 1).
+// With the factored output pass (fwd_out.cu) selected, the row warps also
+// write what that pass needs of each chunk's in-chunk cumsum G: the anchor
+// alpha (the integer nearest G_last / 2) and whether the chunk is too steep
+// for the factored decay, and per token u = exp2(G - alpha) and
+// v = exp2(alpha - G) dt, all in fp32.
 #include "fwd.cuh"
 
 namespace ssd {
@@ -44,11 +50,20 @@ constexpr int kKB = 64;     // tokens per pipeline stage
 constexpr int kMaxNST = 4;  // pipeline stages (at most)
 constexpr int kBlk = kKB * 128;   // 64 rows of 128 bytes
 constexpr int kOutBlk = 128 * 128;  // one staged dH tile: 128 s rows x 64 p
+// Range limits of the factored decay of the output pass (fwd_out.cu): the
+// largest total decay of a chunk (log2 units), and the smallest column factor
+// of a real token.
+constexpr float kSpanMax = 180.f;
+constexpr float kMinFactor = 7.52316384526264e-37f;  // 2^-120
 
 struct CsArgs {
   const __nv_bfloat16 *dt;
   const float *A;
-  float *gamma;
+  float2 *gamma;
+  // factored-decay outputs (all null unless the output pass wants them):
+  // u, v [b, nh, nc * T]; anchor [b, nh, nc] = (alpha, steep ? 1 : 0)
+  float *u, *v;
+  float2 *anchor;
   int *err;
   int L, nh, P, S, hpg, T, nc, H, n_st, n_hg, nst, n_items, nout;
 };
@@ -85,6 +100,7 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
   __shared__ uint32_t tmem_slot;
   __shared__ float w_s[2][kMaxH][256];             // jump weights, by item parity
   __shared__ float warp_tot[2][kMaxH][kRowWarps];  // cumsum partials, by item parity
+  __shared__ int warp_fok[2][kMaxH][kRowWarps];    // factored-decay range checks
 
   const int L = a.L, nh = a.nh, P = a.P, T = a.T, nc = a.nc, H = a.H, nst = a.nst;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -345,10 +361,43 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
           if (w2 < warp) base += t;
         }
         if (tid < T) w[q][tid] = tid < valid ? exp2f(tot - (base + incl[q])) * d[q] : 0.f;
-        if (tid == 0 && it.st == 0)
-          a.gamma[((int64_t)it.b * nh + it.hbase + q) * nc + it.k] = exp2f(tot);
+        if (a.anchor && it.st == 0) {
+          // the factors of the output pass about alpha; a real token's
+          // column factor must stay a normal bf16 number
+          const float Gj = base + incl[q], alpha = rintf(0.5f * tot);
+          const float vj = d[q] > 0.f ? ptx::ex2_approx(alpha - Gj) * d[q] : 0.f;
+          const bool ok = d[q] == 0.f || vj >= kMinFactor;
+          const int all_ok = __all_sync(0xffffffffu, ok);
+          if ((tid & 31) == 0) warp_fok[jl & 1][q][warp] = all_ok;
+          if (tid < T) {
+            const int64_t o = ((int64_t)it.b * nh + it.hbase + q) * nc * T + (int64_t)it.k * T + tid;
+            a.u[o] = ptx::ex2_approx(Gj - alpha);
+            a.v[o] = vj;
+          }
+        }
       }
       ptx::named_bar_sync(1, kRowThreads);
+      if (it.st == 0 && tid < H) {
+        // thread q: head q's decay, and with the factored output pass its
+        // anchor, path and start-state scale
+        const int q = tid;
+        float tot = 0.f;
+        int ok = 1;
+#pragma unroll
+        for (int w2 = 0; w2 < kRowWarps; ++w2) {
+          tot += wt[q][w2];
+          if (a.anchor) ok &= warp_fok[jl & 1][q][w2];
+        }
+        const int64_t o = ((int64_t)it.b * nh + it.hbase + q) * nc + it.k;
+        float scale = 1.f;
+        if (a.anchor) {
+          const bool steep = !(ok && -tot <= kSpanMax);
+          const float alpha = steep ? 0.f : rintf(0.5f * tot);
+          a.anchor[o] = make_float2(alpha, steep ? 1.f : 0.f);
+          scale = __int_as_float((127 + (int)alpha) << 23);  // 2^alpha, alpha in [-91, 0]
+        }
+        a.gamma[o] = make_float2(exp2f(tot), scale);
+      }
       fetch(item + gridDim.x);  // in flight while this item is scaled
 
       // scale each head's x rows by its weights: thread = (row, quarter of
@@ -487,8 +536,9 @@ bool chunk_state_plan_ok(const Dims &d, const CsPlan &plan) {
 }
 
 cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, const void *dt,
-                                   const float *A, void *dH, float *gamma, const CsPlan &plan,
-                                   int *err, cudaStream_t st) {
+                                   const float *A, void *dH, float2 *gamma, float *u, float *v,
+                                   float2 *anchor, const CsPlan &plan, int *err,
+                                   cudaStream_t st) {
   if (!chunk_state_plan_ok(d, plan)) return cudaErrorInvalidValue;
   const int H = plan.H;
   CUtensorMap tB, tx, tD;
@@ -516,6 +566,9 @@ cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, 
   a.dt = static_cast<const __nv_bfloat16 *>(dt);
   a.A = A;
   a.gamma = gamma;
+  a.u = u;
+  a.v = v;
+  a.anchor = anchor;
   a.err = err;
   a.L = (int)d.L;
   a.nh = (int)d.nh;

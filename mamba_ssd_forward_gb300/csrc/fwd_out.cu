@@ -17,17 +17,21 @@
 //   u_i = exp2(G_i - alpha),   xh_j = exp2(alpha - G_j) dt_j x_j.
 //
 // The bracket is one accumulation: C (2^alpha h)^T plus (C B^T masked) Xh.
-// Per head the row warps only scale h by 2^alpha (alpha an integer: exact in
-// bf16) and each x row by its factor, and apply u_i in the epilogue; the
-// masked C B^T itself carries no decay, so it is computed and rounded to
-// bf16 once per chunk and shared by the heads of the group.  alpha is the
-// integer nearest half the chunk's total decay, so every factor stays within
-// 2^+-(span / 2): the method's own rule of never keeping positive exponents
-// holds for the product u_i xh_j (exponent G_i - G_j <= 0), while the two
-// factors are kept bounded.  A chunk whose decay is too steep for that
-// (span above kSpanMax, or a factor of a real token below 2^-120) takes an
-// exact per-element path instead (u_i exp2(G_i - G_j) formed per pair on
-// the CUDA cores; steep chunks are rare and that path is slow but exact).
+// The masked C B^T carries no decay, so it is computed and rounded to bf16
+// once per chunk and shared by the heads of the group; per head the row
+// warps only scale each x row by its factor and apply u_i in the epilogue.
+// alpha is the integer nearest half the chunk's total decay (so 2^alpha h
+// is exact in bf16, and every factor stays within 2^+-(span / 2): the
+// method's own rule of never keeping positive exponents holds for the
+// product u_i xh_j, exponent G_i - G_j <= 0, while each factor stays
+// bounded).  The chunk-jump kernel, which forms each chunk's cumsum anyway,
+// writes alpha, u and v, and the state pass stores the start states already
+// times 2^alpha.  A chunk whose decay is too steep for bounded factors (the
+// chunk-jump kernel flags it: total decay above 2^-180, or a real token's
+// factor below 2^-120) takes an exact per-element path here instead: its
+// state is stored unscaled, and the epilogue forms exp2(G_i - G_j) dt_j per
+// pair on the CUDA cores from the packed C B^T and the raw x rows (slow but
+// exact; such chunks are rare).
 //
 // One CTA per (slice of hs heads of one group, chunk, batch):
 //   producer warp: C of the chunk (resident), then through a ring of 16 KB
@@ -39,9 +43,11 @@
 //     sets: Acc_t = C_t (2^alpha h)^T, then + (C B^T)_t Xh with the packed
 //     masked tile read from tensor memory as the A operand;
 //   row warps (8): pack C B^T in place to masked bf16 pairs; per head the
-//     cumsum (one token per thread), the scaling of the state and x stages,
-//     and the epilogue y = u_i Acc_i + D x_i written over the x stage and
-//     stored by TMA.
+//     scaling of the x stages (thread = row) and the epilogue
+//     y = u_i Acc_i + D x_i, staged in a y buffer of its own and stored by
+//     TMA (so an x stage is free as soon as the MMAs that read it are done,
+//     and the ring never waits on an epilogue).  Stage barriers take one
+//     arrival per warp.
 // Supported: P = 64, S a multiple of 64 up to 256, T in {128, 256}.
 #include "fwd.cuh"
 
@@ -55,18 +61,16 @@ constexpr int kProducerWarp = kRowWarps, kMmaWarp = kRowWarps + 1;
 constexpr int kP = 64;
 constexpr int kStage = 128 * 128;  // one ring stage: 128 rows of 128 bytes
 constexpr int kMaxSlots = 8;
-// Largest total decay of a chunk (log2 units) for the factored path: each
-// factor then stays within 2^+-90.
-constexpr float kSpanMax = 180.f;
-// Smallest factor exp2(alpha - G_j) dt_j of a token with dt_j > 0 for the
-// factored path (bf16 keeps normal numbers down to 2^-126).
-constexpr float kMinFactor = 7.52316384526264e-37f;  // 2^-120
 
 struct OutArgs {
   const __nv_bfloat16 *dt;
   const float *A, *D;
+  // per-token factors u, v [b, nh, nc * T] and per-chunk anchors [b, nh,
+  // nc] = (alpha, steep ? 1 : 0), from the chunk-jump kernel
+  const float *u, *v;
+  const float2 *anchor;
   int *err;
-  int L, nh, S, hpg, T, nc, hs, nslot;
+  int L, nh, S, hpg, T, nc, hs, nslot, nyst;
 };
 
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
@@ -103,15 +107,10 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
   __shared__ __align__(8) uint64_t c_full, full[kMaxSlots], scaled[kMaxSlots], empty[kMaxSlots],
       sc_done, pack_done, acc_full[2], acc_free[2];
   __shared__ uint32_t tmem_slot;
-  // per head, by head parity: G (log2 units) and dt of every token, the
-  // anchor and the path; the column factors of the head being scaled
+  // a steep head's G (log2 units) and dt of every token, by head parity
   __shared__ __align__(16) float Gs[2][256];
   __shared__ __align__(16) float dts[2][256];
-  __shared__ float vs[256];
-  __shared__ float alpha_s[2];
-  __shared__ int steep_s[2];
   __shared__ float warp_tot[kRowWarps];
-  __shared__ int warp_ok[kRowWarps];
 
   const int L = a.L, nh = a.nh, S = a.S, hs = a.hs, nslot = a.nslot;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -125,19 +124,22 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
   uint8_t *Cs = smem;                  // C tile t, S block sb at (t nS + sb) kStage
   uint8_t *ring = smem + nT * nS * kStage;
   auto slot_ptr = [&](int u) { return ring + (u % nslot) * kStage; };
+  // y staging: one 128-row tile per row tile of the chunk, or (a.nyst = 1)
+  // one tile that the row tiles take in turn
+  uint8_t *ystage = ring + nslot * kStage;
 
   if (tid == 0) {
     ptx::mbar_init(&c_full, 1);
     for (int i = 0; i < nslot; ++i) {
       ptx::mbar_init(&full[i], 1);
-      ptx::mbar_init(&scaled[i], kRowThreads);
+      ptx::mbar_init(&scaled[i], kRowWarps);  // one arrival per row warp
       ptx::mbar_init(&empty[i], 1);
     }
     ptx::mbar_init(&sc_done, 1);
-    ptx::mbar_init(&pack_done, kRowThreads);
+    ptx::mbar_init(&pack_done, kRowWarps);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&acc_full[i], 1);
-      ptx::mbar_init(&acc_free[i], kRowThreads);
+      ptx::mbar_init(&acc_free[i], kRowWarps);
     }
     ptx::fence_mbar_init();
   }
@@ -233,18 +235,19 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     __syncwarp();
     const uint32_t idY = ptx::idesc_bf16(128, kP, false, true);
     ptx::mbar_wait(&pack_done, 0, a.err, 145);
+    ptx::griddep_wait();  // the anchors come from the chunk-jump kernel
     for (int q = 0; q < hs; ++q) {
       const int set = q & 1;
       if (q >= 2) ptx::mbar_wait(&acc_free[set], ((q >> 1) - 1) & 1, a.err, 146);
       ptx::tc_fence_after();
-      int steep = 0;
-      // Acc_t = C_t (2^alpha h)^T over the state stages
+      // the chunk's path, from its anchor
+      const int steep = a.anchor[((int64_t)b * nh + hbase + q) * a.nc + k].y != 0.f;
+      // Acc_t = C_t (2^alpha h)^T over the state stages (stored scaled by the
+      // state pass)
       for (int hh = 0; hh < nH; ++hh, ++u) {
         const int sl = u % nslot;
-        ptx::mbar_wait(&scaled[sl], (spar >> sl) & 1, a.err, 147);
-        spar ^= 1u << sl;
+        ptx::mbar_wait(&full[sl], (u / nslot) & 1, a.err, 147);
         ptx::tc_fence_after();
-        if (hh == 0) steep = *reinterpret_cast<volatile int *>(&steep_s[q & 1]);
         if (leader) {
           const uint32_t h0 = ptx::smem_u32(slot_ptr(u));
           const int nkk = min(128, S - hh * 128) / 16;  // rows of S in this stage / 16
@@ -261,8 +264,9 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
         }
         __syncwarp();
       }
-      // Acc_t += (C B^T)_t Xh over the x stages (skipped for a steep head,
-      // whose epilogue forms the in-chunk sum itself)
+      // Acc_t += (C B^T)_t Xh over the x stages, each stage free once its
+      // MMAs are done (skipped for a steep head, whose epilogue forms the
+      // in-chunk sum itself from the raw x stages and then frees them)
       for (int xt = 0; xt < nT; ++xt, ++u) {
         const int sl = u % nslot;
         ptx::mbar_wait(&scaled[sl], (spar >> sl) & 1, a.err, 148);
@@ -277,6 +281,7 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
               ptx::mma_ts_bf16(tmem + TC::acc(set, t), tmem + TC::pk(t) + 64 * xt + 8 * kk, xd,
                                idY, 1u);
             }
+          ptx::mma_commit(&empty[sl]);
         }
         __syncwarp();
       }
@@ -295,61 +300,31 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     const int etile = erow >> 7;
     const int ecol = kT == 256 ? 0 : 32 * (tid >> 7);
     const int lrow = erow & 127;  // row within its tile = TMEM lane
-
-    const unsigned short *dtp = reinterpret_cast<const unsigned short *>(a.dt);
     const bool tok_ok = tid < valid;
-    const int64_t dt_off = ((int64_t)b * L + tok0 + (tok_ok ? tid : 0)) * nh + hbase;
-    unsigned short draw = tok_ok ? dtp[dt_off] : (unsigned short)0;
-    float Aq = a.A[hbase];
 
-    // In-chunk cumsum of head q (one token per thread, threads < T), its
-    // anchor and path (every thread computes them; thread 0 also publishes
-    // them for the epilogue and the MMA warp), the column factors v_j, into
-    // the buffers of parity q & 1; then dt and A of head q + 1 are fetched.
-    float cur_alpha = 0.f;
-    int cur_steep = 0;
-    auto cumsum = [&](int q) {
-      const int pb = q & 1;
-      const float d = __uint_as_float((uint32_t)draw << 16);  // bf16 -> fp32, exact
-      float incl = Aq * kLog2e * d;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_up_sync(0xffffffffu, incl, off);
-        if ((tid & 31) >= off) incl += o;
-      }
-      if ((tid & 31) == 31) warp_tot[warp] = incl;
-      ptx::named_bar_sync(1, kRowThreads);
-      float Gj = incl, tot = 0.f;
-#pragma unroll
-      for (int w2 = 0; w2 < kRowWarps; ++w2) {
-        const float tw = warp_tot[w2];
-        if (w2 < warp) Gj += tw;
-        tot += tw;  // G at the last real token (padding adds nothing)
-      }
-      const float alpha = rintf(0.5f * tot);
-      const float v = d > 0.f ? ptx::ex2_approx(alpha - Gj) * d : 0.f;
-      const bool ok = d == 0.f || v >= kMinFactor;
-      const int all_ok = __all_sync(0xffffffffu, ok);
-      if (tid < kT) {
-        Gs[pb][tid] = Gj;
-        dts[pb][tid] = d;
-        vs[tid] = v;
-      }
-      if ((tid & 31) == 0) warp_ok[warp] = all_ok;
-      ptx::named_bar_sync(1, kRowThreads);
-      int okc = -tot <= kSpanMax;
-#pragma unroll
-      for (int w2 = 0; w2 < kRowWarps; ++w2) okc &= warp_ok[w2];
-      cur_alpha = okc ? alpha : 0.f;
-      cur_steep = !okc;
-      if (tid == 0) {
-        alpha_s[pb] = cur_alpha;
-        steep_s[pb] = cur_steep;
-      }
-      if (q + 1 < hs) {
-        draw = tok_ok ? dtp[dt_off + q + 1] : (unsigned short)0;
-        Aq = a.A[hbase + q + 1];
-      }
+    // one arrival per warp on a barrier, once every lane's writes are done
+    auto warp_arrive = [&](uint64_t *bar) {
+      __syncwarp();
+      if ((tid & 31) == 0) ptx::mbar_arrive(bar);
+    };
+
+    // A head's inputs from the chunk-jump kernel and the parameters: this
+    // row's factors u and v, the chunk's anchor (alpha, steep) and D,
+    // fetched one head ahead so no instruction waits on them.
+    struct HeadIn {
+      float u, v, D;
+      int steep;
+    };
+    auto fetch_head = [&](int q) {
+      HeadIn r;
+      const int h = hbase + q;
+      const int64_t bhk = ((int64_t)b * nh + h) * a.nc + k;
+      const int64_t o = bhk * kT + erow;
+      r.u = a.u[o];
+      r.v = a.v[o];
+      r.steep = a.anchor[bhk].y != 0.f;
+      r.D = a.D ? a.D[h] : 0.f;
+      return r;
     };
 
     // ---- phase 1 output: C B^T packed in place to masked bf16 pairs.  The
@@ -357,7 +332,6 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     // (T = 128: warps 0-3 only), reading 32 fp32 columns and writing 16
     // packed ones each step; each step's writes land on columns an earlier
     // step has read.
-    cumsum(0);
     ptx::mbar_wait(&sc_done, 0, a.err, 149);
     ptx::tc_fence_after();
     {
@@ -387,48 +361,70 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       }
     }
     ptx::tc_fence_before();
-    ptx::mbar_arrive(&pack_done);
+    warp_arrive(&pack_done);
+    // u, v and the anchors come from the chunk-jump kernel, two launches
+    // back: wait until the preceding grids are complete
+    ptx::griddep_wait();
+    HeadIn in_next = fetch_head(0);
 
-    // stage u of the ring (phase-1 stages come first)
-    int u = n_p1;
-    uint4 xkeep[kCols / 8];  // this thread's x row segment, for D x
-    // the epilogue of head q: y = u_i Acc_i + D x_i over the head's x
-    // stages, stored by TMA; the x stages are released once the store has
-    // read them (u_x = the first x stage of the head)
-    auto epilogue = [&](int q, int u_x) {
+    // In-chunk cumsum of a steep head (one token per thread, threads < T)
+    // into Gs / dts of parity q & 1, for the exact per-element epilogue.
+    auto steep_cumsum = [&](int q) {
+      const int pb = q & 1, h = hbase + q;
+      const unsigned short *dtp = reinterpret_cast<const unsigned short *>(a.dt);
+      const unsigned short raw =
+          tok_ok ? dtp[((int64_t)b * L + tok0 + tid) * nh + h] : (unsigned short)0;
+      const float d = __uint_as_float((uint32_t)raw << 16);  // bf16 -> fp32, exact
+      float incl = a.A[h] * kLog2e * d;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, incl, off);
+        if ((tid & 31) >= off) incl += o;
+      }
+      if ((tid & 31) == 31) warp_tot[warp] = incl;
+      ptx::named_bar_sync(1, kRowThreads);
+      float Gj = incl;
+#pragma unroll
+      for (int w2 = 0; w2 < kRowWarps; ++w2)
+        if (w2 < warp) Gj += warp_tot[w2];
+      if (tid < kT) {
+        Gs[pb][tid] = Gj;
+        dts[pb][tid] = d;
+      }
+      ptx::named_bar_sync(1, kRowThreads);
+    };
+
+    // The epilogue of head q (inputs `in`, raw x row segment `xk`; u_x =
+    // the head's first x stage, read raw only on the steep path):
+    // y = u_i Acc_i + D x_i, staged and stored by TMA.
+    auto epilogue = [&](int q, int u_x, const HeadIn &in, const uint4 (&xk)[kCols / 8]) {
       const int pb = q & 1, set = q & 1, h = hbase + q;
-      const float Dh = a.D ? a.D[h] : 0.f;
-      const int steep = steep_s[pb];
       ptx::mbar_wait(&acc_full[set], (q >> 1) & 1, a.err, 150);
       ptx::tc_fence_after();
       uint32_t acc[kCols];
 #pragma unroll
-      for (int c = 0; c < kCols / 16; ++c) {
-        uint32_t r16[16];
-        ptx::tmem_ld16(tmem + lane_base + TC::acc(set, etile) + ecol + 16 * c, r16);
-        ptx::tmem_ld_wait();
-        ptx::reg_fence(r16);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) acc[16 * c + e] = r16[e];
-      }
+      for (int c = 0; c < kCols / 16; ++c)
+        ptx::tmem_ld16(tmem + lane_base + TC::acc(set, etile) + ecol + 16 * c,
+                       *reinterpret_cast<uint32_t(*)[16]>(acc + 16 * c));
+      ptx::tmem_ld_wait();
+      ptx::reg_fence(acc);
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&acc_free[set]);  // the accumulators may take head q + 2
+      warp_arrive(&acc_free[set]);  // the accumulators may take head q + 2
       float yv[kCols];
-      uint8_t *xs = slot_ptr(u_x + etile);  // this row's x stage
-      if (!steep) {
-        const float ui = ptx::ex2_approx(Gs[pb][erow] - alpha_s[pb]);
+      if (!in.steep) {
 #pragma unroll
         for (int m = 0; m < kCols / 8; ++m) {
           float xv[8];
-          unpack16(xkeep[m], xv, (__nv_bfloat16 *)nullptr);
+          unpack16(xk[m], xv, (__nv_bfloat16 *)nullptr);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            yv[8 * m + e] = fmaf(Dh, xv[e], ui * __uint_as_float(acc[8 * m + e]));
+            yv[8 * m + e] = fmaf(in.D, xv[e], in.u * __uint_as_float(acc[8 * m + e]));
         }
       } else {
         // exact per-element path: the inter-chunk term from the accumulator
-        // (alpha = 0: plain C h^T), the in-chunk sum on the CUDA cores from
-        // the packed masked C B^T (this row's lane) and the raw x rows
+        // (the stored state of a steep chunk is unscaled: plain C h^T), the
+        // in-chunk sum on the CUDA cores from the packed masked C B^T (this
+        // row's lane) and the raw x rows
         const float Gi = Gs[pb][erow];
         const float ei = exp2f(Gi);
 #pragma unroll
@@ -461,89 +457,98 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
 #pragma unroll
         for (int m = 0; m < kCols / 8; ++m) {
           float xv[8];
-          unpack16(xkeep[m], xv, (__nv_bfloat16 *)nullptr);
+          unpack16(xk[m], xv, (__nv_bfloat16 *)nullptr);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) yv[8 * m + e] = fmaf(Dh, xv[e], yv[8 * m + e]);
+          for (int e = 0; e < 8; ++e) yv[8 * m + e] = fmaf(in.D, xv[e], yv[8 * m + e]);
         }
-        // every thread has read the raw x rows before any y overwrites them
+        // every thread has read the raw x stages: they may be refilled
         ptx::named_bar_sync(2, kRowThreads);
+        if (tid == 0)
+          for (int xt = 0; xt < nT; ++xt) ptx::mbar_arrive(&empty[(u_x + xt) % nslot]);
       }
+      // y through the staging buffer(s), stored by TMA (rows past the
+      // sequence are clipped by the store); the previous store must have
+      // read the buffer first
+      const int nyst = a.nyst;
+      for (int t = 0; t < nT; ++t) {
+        if (nyst == nT && t > 0) break;  // every tile staged at once
+        const bool mine = nyst == nT || etile == t;
+        if (tid == 0) ptx::bulk_wait_read<0>();
+        ptx::named_bar_sync(2, kRowThreads);
+        if (mine) {
+          uint8_t *yt = ystage + (nyst == nT ? etile : 0) * kStage;
 #pragma unroll
-      for (int m = 0; m < kCols / 8; ++m)
-        *reinterpret_cast<uint4 *>(xs + sw128(lrow, ((ecol >> 3) + m) * 16)) =
-            pack_io16(yv + 8 * m, (__nv_bfloat16 *)nullptr);
-      ptx::fence_async_smem();
-      ptx::named_bar_sync(2, kRowThreads);
-      if (tid == 0) {
-        for (int xt = 0; xt < nT; ++xt)
-          ptx::tma_store_4d(&tm_y, slot_ptr(u_x + xt), 0, h, tok0 + xt * 128, b);
-        ptx::bulk_commit();
-        ptx::bulk_wait_read<0>();  // the x stages may be refilled now
-        for (int xt = 0; xt < nT; ++xt) ptx::mbar_arrive(&empty[(u_x + xt) % nslot]);
+          for (int m = 0; m < kCols / 8; ++m)
+            *reinterpret_cast<uint4 *>(yt + sw128(lrow, ((ecol >> 3) + m) * 16)) =
+                pack_io16(yv + 8 * m, (__nv_bfloat16 *)nullptr);
+        }
+        ptx::fence_async_smem();
+        ptx::named_bar_sync(2, kRowThreads);
+        if (tid == 0) {
+          if (nyst == nT) {
+            for (int t2 = 0; t2 < nT; ++t2)
+              ptx::tma_store_4d(&tm_y, ystage + t2 * kStage, 0, h, tok0 + t2 * 128, b);
+          } else {
+            ptx::tma_store_4d(&tm_y, ystage, 0, h, tok0 + t * 128, b);
+          }
+          ptx::bulk_commit();
+        }
       }
     };
 
-    int u_prev_x = 0;
+    // Per head q: scale its x stages (each row times v_j; kept raw for a
+    // steep head) keeping this thread's raw segment for D x, then the
+    // previous head's epilogue (head q's MMAs overlap it).  A steep head's
+    // own epilogue follows at once, so its raw x stages are freed before the
+    // ring needs them again.
+    int u = n_p1;
+    uint4 xk_prev[kCols / 8];
+    HeadIn in_prev{};
+    int u_prev = 0;
+    bool pending = false;
     for (int q = 0; q < hs; ++q) {
-      // 1. the state stages of head q, times 2^alpha (exact: a power of two)
-      {
-        const float al = cur_alpha;
-        const __nv_bfloat162 sc2 = __floats2bfloat162_rn(exp2f(al), exp2f(al));
-        for (int hh = 0; hh < nH; ++hh, ++u) {
-          const int sl = u % nslot;
-          ptx::mbar_wait(&full[sl], (u / nslot) & 1, a.err, 151);
-          if (al != 0.f) {
-            uint8_t *st = slot_ptr(u);
-            const int n16 = hrows * 8;  // 16-byte chunks in the stage
-            for (int i = tid; i < n16; i += kRowThreads) {
-              uint4 *p = reinterpret_cast<uint4 *>(st + 16 * i);
-              uint4 v = *p;
-              __nv_bfloat162 *b2 = reinterpret_cast<__nv_bfloat162 *>(&v);
+      const HeadIn in = in_next;
+      if (q + 1 < hs) in_next = fetch_head(q + 1);
+      u += nH;  // the state stages go straight to the MMA warp
+      const int u_x = u;
+      uint4 xk[kCols / 8];
+      for (int xt = 0; xt < nT; ++xt, ++u) {
+        const int sl = u % nslot;
+        ptx::mbar_wait(&full[sl], (u / nslot) & 1, a.err, 152);
+        if (etile == xt) {
+          uint8_t *xs = slot_ptr(u);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) b2[e] = __hmul2(b2[e], sc2);
-              *p = v;
-            }
-          }
-          ptx::fence_async_smem();
-          ptx::mbar_arrive(&scaled[sl]);
-        }
-      }
-      // 2. the previous head's epilogue (its MMAs overlap step 1 above)
-      if (q > 0) epilogue(q - 1, u_prev_x);
-      // 3. the x stages of head q: each row times its factor v_j (kept raw
-      // for a steep head); this thread's segment of its own row kept for D x
-      {
-        const int steep = cur_steep;
-        const int u_x = u;
-        for (int xt = 0; xt < nT; ++xt, ++u) {
-          const int sl = u % nslot;
-          ptx::mbar_wait(&full[sl], (u / nslot) & 1, a.err, 152);
-          if (etile == xt) {
-            uint8_t *xs = slot_ptr(u);
-            const float vj = vs[erow];
+          for (int m = 0; m < kCols / 8; ++m)
+            xk[m] = *reinterpret_cast<const uint4 *>(xs + sw128(lrow, ((ecol >> 3) + m) * 16));
+          if (!in.steep) {
 #pragma unroll
             for (int m = 0; m < kCols / 8; ++m) {
-              uint4 *p = reinterpret_cast<uint4 *>(xs + sw128(lrow, ((ecol >> 3) + m) * 16));
-              const uint4 raw = *p;
-              xkeep[m] = raw;
-              if (!steep) {
-                float xv[8];
-                unpack16(raw, xv, (__nv_bfloat16 *)nullptr);
+              float xv[8];
+              unpack16(xk[m], xv, (__nv_bfloat16 *)nullptr);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) xv[e] *= vj;
-                *p = pack_io16(xv, (__nv_bfloat16 *)nullptr);
-              }
+              for (int e = 0; e < 8; ++e) xv[e] *= in.v;
+              *reinterpret_cast<uint4 *>(xs + sw128(lrow, ((ecol >> 3) + m) * 16)) =
+                  pack_io16(xv, (__nv_bfloat16 *)nullptr);
             }
           }
-          ptx::fence_async_smem();
-          ptx::mbar_arrive(&scaled[sl]);
         }
-        u_prev_x = u_x;
+        ptx::fence_async_smem();
+        warp_arrive(&scaled[sl]);
       }
-      // 4. the next head's cumsum
-      if (q + 1 < hs) cumsum(q + 1);
+      if (pending) epilogue(q - 1, u_prev, in_prev, xk_prev);
+      if (in.steep) {
+        steep_cumsum(q);
+        epilogue(q, u_x, in, xk);
+        pending = false;
+      } else {
+#pragma unroll
+        for (int m = 0; m < kCols / 8; ++m) xk_prev[m] = xk[m];
+        in_prev = in;
+        u_prev = u_x;
+        pending = true;
+      }
     }
-    epilogue(hs - 1, u_prev_x);
+    if (pending) epilogue(hs - 1, u_prev, in_prev, xk_prev);
     if (tid == 0) ptx::bulk_wait<0>();  // every y store complete
   }
   ptx::tc_fence_before();
@@ -552,15 +557,20 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
 }
 
 struct OutSmem {
-  int nslot, smem;
+  int nslot, nyst, smem;
 };
+// C of the chunk, the ring and the y staging within 220 KB of dynamic shared
+// memory (1 KB of it alignment slack; the static arrays, about 6 KB, sit
+// beside it): y staging for every row tile when at least a head's stages
+// (plus one) still fit the ring, else one staging tile.
 OutSmem out_smem(const Dims &d) {
   OutSmem m;
+  const int nT = (int)(d.T / 128), nH = (int)((d.S + 127) / 128);
   const int c_bytes = (int)(d.T * d.S * 2);
-  // dynamic shared memory within 220 KB (1 KB of it alignment slack), the
-  // static arrays (about 7 KB) beside it
-  m.nslot = std::min<int>(kMaxSlots, (220 * 1024 - 1024 - c_bytes) / kStage);
-  m.smem = c_bytes + m.nslot * kStage + 1024;
+  const int room = (220 * 1024 - 1024 - c_bytes) / kStage;  // 16 KB units
+  m.nyst = room - nT >= nT + nH + 1 ? nT : 1;
+  m.nslot = std::min<int>(kMaxSlots, room - m.nyst);
+  m.smem = c_bytes + (m.nslot + m.nyst) * kStage + 1024;
   return m;
 }
 
@@ -569,9 +579,10 @@ OutSmem out_smem(const Dims &d) {
 bool fwd_out_supported(const Dims &d) {
   if (d.P != kP || d.S % 64 || d.S > 256 || (d.T != 128 && d.T != 256)) return false;
   if (d.nc > 65535 || d.b > 65535) return false;
-  // the ring must hold one head's x stages and the next head's state stages
-  // besides a free stage, or the row warps' order could stall it
-  const int need = (int)(d.T / 128 + (d.S + 127) / 128 + 1);
+  // the ring must hold a steep head's x stages (released only by its
+  // epilogue) and the next head's state stages, or the row warps' order
+  // could stall it
+  const int need = (int)(d.T / 128 + (d.S + 127) / 128);
   return out_smem(d).nslot >= need;
 }
 
@@ -602,7 +613,8 @@ int fwd_out_heads(const Dims &d) {
 
 cudaError_t launch_fwd_out(const Dims &d, const void *x, const void *B, const void *C,
                            const void *dt, const float *A, const void *states, const float *D,
-                           void *y, int hs, int *err, cudaStream_t st) {
+                           const float *u, const float *v, const float2 *anchor, void *y,
+                           int hs, int *err, cudaStream_t st) {
   if (!fwd_out_heads_ok(d, hs)) return cudaErrorInvalidValue;
   CUtensorMap tC, tB, tx, tS, tY;
   if (!make_tmap_bl(&tC, C, true, d.b, d.L, d.ng, d.S, 128) ||
@@ -626,6 +638,9 @@ cudaError_t launch_fwd_out(const Dims &d, const void *x, const void *B, const vo
   a.dt = static_cast<const __nv_bfloat16 *>(dt);
   a.A = A;
   a.D = D;
+  a.u = u;
+  a.v = v;
+  a.anchor = anchor;
   a.err = err;
   a.L = (int)d.L;
   a.nh = (int)d.nh;
@@ -635,6 +650,7 @@ cudaError_t launch_fwd_out(const Dims &d, const void *x, const void *B, const vo
   a.nc = (int)d.nc;
   a.hs = hs;
   a.nslot = m.nslot;
+  a.nyst = m.nyst;
   // programmatic stream serialisation: the producer waits on the device
   // before loading the first start state
   cudaLaunchConfig_t cfg = {};

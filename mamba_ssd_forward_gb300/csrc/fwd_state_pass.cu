@@ -9,7 +9,10 @@
 // (batch, head) state in the [S][P] layout, keeps them in fp32 registers, and
 // walks the chunks with the next group of eight chunks' loads in flight.  dH
 // and the stored states are bf16 [b, nh, nc, S, P]; h0 and the final state
-// are fp32 [b, nh, P, S] (the public layout).
+// are fp32 [b, nh, P, S] (the public layout).  gamma holds per chunk the
+// decay and the scale of its stored start state (1, or 2^alpha_k for the
+// factored output pass: a power of two, so the scaling is exact); the
+// carried state stays unscaled.
 #include "fwd.cuh"
 
 namespace ssd {
@@ -18,14 +21,20 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kDepth = 8;  // chunks per prefetch group
 
-__global__ void __launch_bounds__(kThreads)
-fwd_state_pass_bf16(const uint4 *__restrict__ dH, const float *__restrict__ gamma,
+// two CTAs per SM (at most 128 registers a thread)
+__global__ void __launch_bounds__(kThreads, 2)
+fwd_state_pass_bf16(const uint4 *__restrict__ dH, const float2 *__restrict__ gamma,
                     const float *__restrict__ h0, uint4 *__restrict__ states,
                     float *__restrict__ final_state, int P, int S, int nc) {
+  // the CTA's (decay, scale) pairs, 256 chunks at a time
+  __shared__ float2 gsm[256];
   const int64_t bh = blockIdx.y;
   const int n8 = S * P / 8;
-  const int e8 = blockIdx.x * kThreads + threadIdx.x;
-  if (e8 >= n8) return;
+  const int e8x = blockIdx.x * kThreads + threadIdx.x;
+  // threads past the state (a partial last CTA) take part in the barriers
+  // only, working on element 0 without storing
+  const bool live = e8x < n8;
+  const int e8 = live ? e8x : 0;
   const int s = (e8 * 8) / P, p0 = (e8 * 8) % P;
   ptx::griddep_launch_dependents();  // the output pass may be scheduled now
   float h[8];
@@ -34,40 +43,43 @@ fwd_state_pass_bf16(const uint4 *__restrict__ dH, const float *__restrict__ gamm
   ptx::griddep_wait();  // dH and gamma come from the preceding kernel
   const uint4 *src = dH + bh * nc * n8 + e8;
   uint4 *dst = states + bh * nc * n8 + e8;
-  const float *gm = gamma + bh * nc;
+  const float2 *gm = gamma + bh * nc;
   // Two groups of kDepth chunks: the next group's loads are issued before the
   // current group is consumed, so up to 2 kDepth 16-byte loads are in flight.
+  // Every thread of the CTA works on the same (batch, head), so the group's
+  // per-chunk decays and anchors are the same for all: they are loaded
+  // together at the start of the group and come from L1.
   uint4 cur[kDepth], nxt[kDepth];
-  float gcur[kDepth], gnxt[kDepth];
 #pragma unroll
   for (int i = 0; i < kDepth; ++i)
-    if (i < nc) {
-      cur[i] = src[(int64_t)i * n8];
-      gcur[i] = gm[i];
-    }
+    if (i < nc) cur[i] = src[(int64_t)i * n8];
   for (int k0 = 0; k0 < nc; k0 += kDepth) {
+    if ((k0 & 255) == 0) {
+      // the next 256 chunks' (decay, scale) pairs into shared memory
+      __syncthreads();
+      if (k0 + (int)threadIdx.x < nc) gsm[threadIdx.x] = gm[k0 + threadIdx.x];
+      __syncthreads();
+    }
 #pragma unroll
     for (int i = 0; i < kDepth; ++i)
-      if (k0 + kDepth + i < nc) {
-        nxt[i] = src[(int64_t)(k0 + kDepth + i) * n8];
-        gnxt[i] = gm[k0 + kDepth + i];
-      }
+      if (k0 + kDepth + i < nc) nxt[i] = src[(int64_t)(k0 + kDepth + i) * n8];
 #pragma unroll
     for (int i = 0; i < kDepth; ++i)
       if (k0 + i < nc) {
-        dst[(int64_t)(k0 + i) * n8] = pack_io16(h, (__nv_bfloat16 *)nullptr);
+        const float2 g = gsm[(k0 + i) & 255];  // (decay, stored-state scale)
+        float hs[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hs[j] = g.y * h[j];
+        if (live) dst[(int64_t)(k0 + i) * n8] = pack_io16(hs, (__nv_bfloat16 *)nullptr);
         float d[8];
         unpack16(cur[i], d, (__nv_bfloat16 *)nullptr);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) h[j] = fmaf(gcur[i], h[j], d[j]);
+        for (int j = 0; j < 8; ++j) h[j] = fmaf(g.x, h[j], d[j]);
       }
 #pragma unroll
-    for (int i = 0; i < kDepth; ++i) {
-      cur[i] = nxt[i];
-      gcur[i] = gnxt[i];
-    }
+    for (int i = 0; i < kDepth; ++i) cur[i] = nxt[i];
   }
-  if (final_state) {
+  if (final_state && live) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) final_state[(bh * P + p0 + i) * S + s] = h[i];
   }
@@ -75,7 +87,7 @@ fwd_state_pass_bf16(const uint4 *__restrict__ dH, const float *__restrict__ gamm
 
 }  // namespace
 
-cudaError_t launch_fwd_state_pass(const Dims &d, const void *dH, const float *gamma,
+cudaError_t launch_fwd_state_pass(const Dims &d, const void *dH, const float2 *gamma,
                                   const float *h0, void *states, float *final_state,
                                   cudaStream_t st) {
   const int n8 = (int)(d.S * d.P / 8);

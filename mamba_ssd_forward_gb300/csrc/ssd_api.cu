@@ -57,11 +57,13 @@ ssd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR
 
 // Workspace of ssd_forward: the header (the call's error word), then for
 // bf16 I/O the per-chunk start states in bf16, [b, nh, nc, S, P], the chunk
-// jump terms and the per-chunk decays; for fp32 I/O G, the chunk jump terms
-// and the per-chunk states (fp32, the step-wise layouts).  Each part is
-// 256-byte aligned.
+// jump terms, the per-chunk decays, and the factored-decay inputs of the
+// fwd_out output kernel (per-token u and v, fp32 [b, nh, nc * T], and the
+// per-chunk anchors, float2 [b, nh, nc]); for fp32 I/O G, the chunk jump
+// terms and the per-chunk states (fp32, the step-wise layouts).  Each part
+// is 256-byte aligned.
 struct WsLayout {
-  size_t G, dstates, states, total;
+  size_t G, dstates, states, u, v, anchor, total;
 };
 
 size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
@@ -70,29 +72,55 @@ WsLayout ws_layout(const Dims &d, ssd_dtype t) {
   WsLayout w;
   const size_t h = ssd::kWsHeader;
   if (t == SSD_BF16) {
-    // header | states (bf16) | jump terms (bf16) | per-chunk decays (fp32)
+    // header | states (bf16) | jump terms (bf16) | per-chunk (decay, state scale) (fp32 pairs)
     const size_t st = round256(2 * (size_t)(d.b * d.nh * d.nc * d.S * d.P));
     w.states = h;
     w.dstates = h + st;
     w.G = h + 2 * st;
-    w.total = w.G + round256(sizeof(float) * d.b * d.nh * d.nc);
+    const size_t tok = round256(sizeof(float) * d.b * d.nh * d.nc * d.T);
+    w.u = w.G + round256(2 * sizeof(float) * d.b * d.nh * d.nc);
+    w.v = w.u + tok;
+    w.anchor = w.v + tok;
+    w.total = w.anchor + round256(2 * sizeof(float) * d.b * d.nh * d.nc);
     return w;
   }
   w.G = h;
   w.dstates = h + round256(sizeof(float) * d.b * d.nh * d.nc * d.T);
   const size_t st = round256(sizeof(float) * d.b * d.nh * d.nc * d.P * d.S);
   w.states = w.dstates + st;
+  w.u = w.v = w.anchor = 0;
   w.total = w.states + st;
   return w;
 }
 
 size_t io_size(ssd_dtype t) { return t == SSD_BF16 ? 2 : 4; }
 
+// The bf16 intermediates of one forward pass, carved from its workspace.
+struct Bf16Ws {
+  void *states, *dH;
+  float2 *gamma;
+  float *u, *v;
+  float2 *anchor;
+};
+Bf16Ws bf16_ws(const WsLayout &w, void *workspace) {
+  char *ws = static_cast<char *>(workspace);
+  Bf16Ws r;
+  r.states = ws + w.states;
+  r.dH = ws + w.dstates;
+  r.gamma = reinterpret_cast<float2 *>(ws + w.G);
+  r.u = reinterpret_cast<float *>(ws + w.u);
+  r.v = reinterpret_cast<float *>(ws + w.v);
+  r.anchor = reinterpret_cast<float2 *>(ws + w.anchor);
+  return r;
+}
+
 cudaError_t launch_scan(const Dims &d, const ssd::FwdPlan &plan, const void *x, const void *B,
-                        const void *C, const void *dt, const float *A, const void *states,
+                        const void *C, const void *dt, const float *A, const Bf16Ws &b,
                         const float *D, void *y, int *err, cudaStream_t st) {
+  const void *states = b.states;
   if (plan.scan_kernel == 3)
-    return ssd::launch_fwd_out(d, x, B, C, dt, A, states, D, y, plan.scan_heads, err, st);
+    return ssd::launch_fwd_out(d, x, B, C, dt, A, states, D, b.u, b.v, b.anchor, y,
+                               plan.scan_heads, err, st);
   return plan.scan_kernel
              ? ssd::launch_fwd_scan_chunk(d, x, B, C, dt, A, states, D, y, plan.scan_heads,
                                           plan.scan_kernel == 2, err, st)
@@ -334,15 +362,20 @@ ssd_status forward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
   cudaError_t e = mark(0);
   if (dtype == SSD_BF16) {
     // chunk jump terms (all chunks in parallel), the sequential pass over
-    // chunks, then the output pass
-    void *sts = ws + w.states;
-    void *dH = ws + w.dstates;
-    float *gam = reinterpret_cast<float *>(ws + w.G);
-    if (e == cudaSuccess) e = ssd::launch_fwd_chunk_state(d, x, B, dt, A, dH, gam, fp.cs, err, st);
+    // chunks, then the output pass; with the factored output kernel the
+    // first also writes its per-token factors and anchors and the second
+    // stores the start states scaled by them
+    const Bf16Ws bw = bf16_ws(w, workspace);
+    const bool fac = fp.scan_kernel == 3;
+    if (e == cudaSuccess)
+      e = ssd::launch_fwd_chunk_state(d, x, B, dt, A, bw.dH, bw.gamma, fac ? bw.u : nullptr,
+                                      fac ? bw.v : nullptr, fac ? bw.anchor : nullptr, fp.cs,
+                                      err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
-    if (e == cudaSuccess) e = ssd::launch_fwd_state_pass(d, dH, gam, h0, sts, final_state, st);
+    if (e == cudaSuccess)
+      e = ssd::launch_fwd_state_pass(d, bw.dH, bw.gamma, h0, bw.states, final_state, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
-    if (e == cudaSuccess) e = launch_scan(d, fp, x, B, C, dt, A, sts, D, y, err, st);
+    if (e == cudaSuccess) e = launch_scan(d, fp, x, B, C, dt, A, bw, D, y, err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
   } else {
     float *G = reinterpret_cast<float *>(ws + w.G);
@@ -443,10 +476,7 @@ ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x
   s = ssd_forward(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, workspace, ws_bytes,
                   stream);
   if (s != SSD_OK) return s;
-  char *ws = static_cast<char *>(workspace);
-  void *sts = ws + w.states;
-  void *dH = ws + w.dstates;
-  float *gam = reinterpret_cast<float *>(ws + w.G);
+  const Bf16Ws bw = bf16_ws(w, workspace);
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   cudaError_t e = cudaEventCreate(&e0);
   if (e == cudaSuccess) e = cudaEventCreate(&e1);
@@ -459,7 +489,10 @@ ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x
   for (size_t i = 0; i < cs.size() && e == cudaSuccess; ++i) {
     float ms = 0.f;
     e = time_launches(
-        [&] { return ssd::launch_fwd_chunk_state(d, x, B, dt, A, dH, gam, cs[i], err, st); },
+        [&] {
+          return ssd::launch_fwd_chunk_state(d, x, B, dt, A, bw.dH, bw.gamma, bw.u, bw.v,
+                                             bw.anchor, cs[i], err, st);
+        },
         reps, st, e0, e1, &ms);
     if (e == cudaSuccess && ms < best_ms) {
       best_ms = ms;
@@ -469,7 +502,7 @@ ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x
   best_ms = 3.0e38f;
   for (size_t i = 0; i < sc.size() && e == cudaSuccess; ++i) {
     float ms = 0.f;
-    e = time_launches([&] { return launch_scan(d, sc[i], x, B, C, dt, A, sts, D, y, err, st); },
+    e = time_launches([&] { return launch_scan(d, sc[i], x, B, C, dt, A, bw, D, y, err, st); },
                       reps, st, e0, e1, &ms);
     if (e == cudaSuccess && ms < best_ms) {
       best_ms = ms;

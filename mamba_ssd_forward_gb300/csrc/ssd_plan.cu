@@ -10,7 +10,7 @@ namespace ssd {
 FwdPlan fwd_default_plan(const Dims &d) {
   FwdPlan p;
   p.cs = chunk_state_plan(d);
-  if (false && fwd_out_supported(d)) {
+  if (fwd_out_supported(d)) {
     p.scan_kernel = 3;
     p.scan_heads = fwd_out_heads(d);
     return p;
@@ -30,7 +30,7 @@ void fwd_scan_candidates(const Dims &d, std::vector<FwdPlan> *out) {
   FwdPlan p{};
   p.cs = CsPlan{0, 0};
   for (int hs = 1; hs <= d.hpg; ++hs)
-    if (false && fwd_out_heads_ok(d, hs)) {
+    if (fwd_out_heads_ok(d, hs)) {
       p.scan_kernel = 3;
       p.scan_heads = hs;
       out->push_back(p);

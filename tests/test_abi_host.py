@@ -238,13 +238,16 @@ def test_plan_candidates_are_valid_and_hold_the_default(lib, shape):
     hpg = nh // ng
     chunk_kernel_ok = P == 64 and S in (64, 128) and T in (128, 256)
     split_kernel_ok = P == 64 and S in (64, 128, 256) and T in (128, 256)
+    factored_ok = P == 64 and S % 64 == 0 and S <= 256 and T in (128, 256)
     for c in cands:
         assert c["chunk_state_ctas"] in (1, 2)
         hmax = 4 if c["chunk_state_ctas"] == 1 else 2
         assert 1 <= c["chunk_state_heads"] <= hmax and hpg % c["chunk_state_heads"] == 0
         assert c["chunk_state_heads"] * P <= (256 if c["chunk_state_ctas"] == 1 else 128)
-        assert c["scan_kernel"] in (0, 1, 2) and hpg % c["scan_heads"] == 0
-        if c["scan_kernel"] == 1:
+        assert c["scan_kernel"] in (0, 1, 2, 3) and hpg % c["scan_heads"] == 0
+        if c["scan_kernel"] == 3:
+            assert factored_ok
+        elif c["scan_kernel"] == 1:
             assert chunk_kernel_ok
         elif c["scan_kernel"] == 2:
             assert split_kernel_ok
@@ -253,8 +256,12 @@ def test_plan_candidates_are_valid_and_hold_the_default(lib, shape):
     assert len({tuple(c.values()) for c in cands}) == len(cands)
     default = m.default_plan(d)
     assert default in cands
-    expect = 1 if chunk_kernel_ok else 2 if split_kernel_ok else 0
+    expect = 3 if factored_ok else 1 if chunk_kernel_ok else 2 if split_kernel_ok else 0
     assert default["scan_kernel"] == expect
+    # the factored output kernel takes every divisor of the heads per group
+    if factored_ok:
+        assert {c["scan_heads"] for c in cands if c["scan_kernel"] == 3} == \
+            {h for h in range(1, hpg + 1) if hpg % h == 0}
 
 
 def test_plan_rejections(lib):
@@ -272,7 +279,8 @@ def test_plan_rejections(lib):
         {"chunk_state_heads": 4, "chunk_state_ctas": 2, "scan_kernel": 1, "scan_heads": 20},
         {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 1, "scan_heads": 3},
         {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 0, "scan_heads": 8},
-        {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 3, "scan_heads": 1},
+        {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 4, "scan_heads": 1},
+        {"chunk_state_heads": 4, "chunk_state_ctas": 1, "scan_kernel": 3, "scan_heads": 3},
     ]
     # a plan that is not a candidate is rejected by every call taking one,
     # before anything is launched (fake aligned pointers, never dereferenced)
