@@ -104,8 +104,12 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
   constexpr int nT = kT / 128;  // row tiles of the chunk (and x stages per head)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t c_full, full[kMaxSlots], scaled[kMaxSlots], empty[kMaxSlots],
-      sc_done, pack_done, acc_full[2], acc_free[2];
+  // full: a B or state stage has landed (the MMA warp waits); xfull: an x
+  // stage has landed (the row warps wait; they skip the other stages, so
+  // their barrier must count x stages only); scaled: the row warps are done
+  // with an x stage; empty: the stage's readers are done
+  __shared__ __align__(8) uint64_t c_full, full[kMaxSlots], xfull[kMaxSlots], scaled[kMaxSlots],
+      empty[kMaxSlots], sc_done, pack_done, acc_full[2], acc_free[2];
   __shared__ uint32_t tmem_slot;
   // a steep head's G (log2 units) and dt of every token, by head parity
   __shared__ __align__(16) float Gs[2][256];
@@ -132,6 +136,7 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     ptx::mbar_init(&c_full, 1);
     for (int i = 0; i < nslot; ++i) {
       ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&xfull[i], 1);
       ptx::mbar_init(&scaled[i], kRowWarps);  // one arrival per row warp
       ptx::mbar_init(&empty[i], 1);
     }
@@ -198,22 +203,29 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       for (int xt = 0; xt < nT; ++xt, ++u) {
         acquire(142);
         if (leader) {
-          ptx::mbar_arrive_expect_tx(&full[u % nslot], kStage);
-          ptx::tma_load_4d(slot_ptr(u), &tm_x, 0, h, tok0 + xt * 128, b, &full[u % nslot]);
+          ptx::mbar_arrive_expect_tx(&xfull[u % nslot], kStage);
+          ptx::tma_load_4d(slot_ptr(u), &tm_x, 0, h, tok0 + xt * 128, b, &xfull[u % nslot]);
         }
         __syncwarp();
       }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    uint32_t spar = 0;  // parity of the next wait on scaled[slot], one bit per slot
+    // parity of the next wait on full[slot] / scaled[slot], one bit per slot
+    // (each barrier counts only the stages this warp waits on it for)
+    uint32_t fpar = 0, spar = 0;
+    auto wait_full = [&](int v, int code) {
+      const int sl = v % nslot;
+      ptx::mbar_wait(&full[sl], (fpar >> sl) & 1, a.err, code);
+      fpar ^= 1u << sl;
+    };
     ptx::mbar_wait(&c_full, 0, a.err, 143);
     ptx::tc_fence_after();
     int u = 0;
     const uint32_t idCB = ptx::idesc_bf16(128, 128, false, false);
     for (int sb = 0; sb < nS; ++sb)
       for (int th = 0; th < nT; ++th, ++u) {
-        ptx::mbar_wait(&full[u % nslot], (u / nslot) & 1, a.err, 144);
+        wait_full(u, 144);
         ptx::tc_fence_after();
         if (leader) {
           const uint32_t b0 = ptx::smem_u32(slot_ptr(u));
@@ -246,7 +258,7 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       // state pass)
       for (int hh = 0; hh < nH; ++hh, ++u) {
         const int sl = u % nslot;
-        ptx::mbar_wait(&full[sl], (u / nslot) & 1, a.err, 147);
+        wait_full(u, 147);
         ptx::tc_fence_after();
         if (leader) {
           const uint32_t h0 = ptx::smem_u32(slot_ptr(u));
@@ -502,6 +514,7 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     // own epilogue follows at once, so its raw x stages are freed before the
     // ring needs them again.
     int u = n_p1;
+    uint32_t xpar = 0;  // parity of the next wait on xfull[slot], one bit per slot
     uint4 xk_prev[kCols / 8];
     HeadIn in_prev{};
     int u_prev = 0;
@@ -514,7 +527,8 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       uint4 xk[kCols / 8];
       for (int xt = 0; xt < nT; ++xt, ++u) {
         const int sl = u % nslot;
-        ptx::mbar_wait(&full[sl], (u / nslot) & 1, a.err, 152);
+        ptx::mbar_wait(&xfull[sl], (xpar >> sl) & 1, a.err, 152);
+        xpar ^= 1u << sl;
         if (etile == xt) {
           uint8_t *xs = slot_ptr(u);
 #pragma unroll
