@@ -35,6 +35,12 @@
  *   returns an error code and enqueues nothing.  A launch failure returns
  *   SSD_ERR_CUDA.  SSD_ERR_TIMEOUT reports that a bounded device-side wait
  *   gave up (the results of that call are then undefined).  Nothing throws.
+ * - A debug-bounds build of the library (compiled with SSD_DEBUG_BOUNDS
+ *   defined; the release build never is) checks the index of every plain
+ *   global load and store of its kernels against the extent of the buffer
+ *   it addresses, skips an access that falls outside, and reports it through
+ *   the same error words as SSD_ERR_BOUNDS.  The checks cost time and
+ *   compile away in the release build.
  * - Preconditions that are documented but not checked: A <= 0 and dt >= 0 (so
  *   every a_t <= 0, the page's stability condition), finite inputs, and
  *   output buffers that do not overlap inputs.  The bf16 output kernels 1
@@ -86,7 +92,8 @@ typedef enum {
   SSD_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, nh % ng */
   SSD_ERR_UNSUPPORTED = 2, /* dims outside the supported range */
   SSD_ERR_CUDA = 3,        /* a CUDA call or launch failed */
-  SSD_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up */
+  SSD_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up */
+  SSD_ERR_BOUNDS = 5       /* a debug-bounds build caught an out-of-range access */
 } ssd_status;
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
@@ -108,7 +115,12 @@ typedef struct {
  *                      C B^T of a whole chunk between a slice of heads (P =
  *                      64, S in {64, 128}, T in {128, 256}); 2 = the same
  *                      with one 128-row tile of the chunk per CTA (P = 64,
- *                      S in {64, 128, 256}, T in {128, 256})
+ *                      S in {64, 128, 256}, T in {128, 256}); 3 = the
+ *                      output pass with the decay factored about one anchor
+ *                      per chunk, C B^T kept in bf16 without decay and
+ *                      shared by the slice's heads (P = 64, S a multiple of
+ *                      64 up to 256, T in {128, 256}; the default where it
+ *                      applies)
  *   scan_heads         heads per CTA of that output kernel (divides
  *                      nheads / ngroups; at most 4, and heads * P <= 256, for
  *                      kernel 0)

@@ -112,24 +112,28 @@ def forward(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, workspace=None,
     return y, final_state
 
 
-def chunk_cumsum(dt, A, chunk: int, headdim: int = 16, dstate: int = 16):
+def chunk_cumsum(dt, A, chunk: int, headdim: int = 16, dstate: int = 16, out=None):
     """G [b, nh, nc*T] float32 (log2 units) = ssd_chunk_cumsum.  headdim and
-    dstate only need to lie in the supported range; they do not affect G."""
+    dstate only need to lie in the supported range; they do not affect G.
+    `out` may be a preallocated G."""
     lib = _abi.load()
     b, L, nh = dt.shape
     d = _abi.SsdDims(b, L, nh, headdim, dstate, 1, int(chunk))
-    G = torch.empty((b, nh, _nchunks(d) * d.chunk), dtype=torch.float32, device=dt.device)
+    G = out if out is not None else torch.empty(
+        (b, nh, _nchunks(d) * d.chunk), dtype=torch.float32, device=dt.device)
     _abi.check("ssd_chunk_cumsum", lib.ssd_chunk_cumsum(
         ctypes.byref(d), _io_code(dt), _ptr(dt), _ptr(_f32(A, "A")), _ptr(G), _stream()))
     return G
 
 
-def chunk_state(x, B, dt, G, chunk: int):
-    """dstates [b, nh, nc, P, S] float32 = ssd_chunk_state."""
+def chunk_state(x, B, dt, G, chunk: int, out=None):
+    """dstates [b, nh, nc, P, S] float32 = ssd_chunk_state (`out` may be a
+    preallocated dstates)."""
     lib = _abi.load()
     d = dims_of(x, B, chunk)
-    out = torch.empty((d.batch, d.nheads, _nchunks(d), d.headdim, d.dstate),
-                      dtype=torch.float32, device=x.device)
+    if out is None:
+        out = torch.empty((d.batch, d.nheads, _nchunks(d), d.headdim, d.dstate),
+                          dtype=torch.float32, device=x.device)
     _abi.check("ssd_chunk_state", lib.ssd_chunk_state(
         ctypes.byref(d), _io_code(x), _ptr(x), _ptr(B), _ptr(dt), _ptr(_f32(G, "G")),
         _ptr(out), _stream()))
@@ -137,26 +141,31 @@ def chunk_state(x, B, dt, G, chunk: int):
 
 
 def state_passing(dstates, G, h0=None, chunk: int = 256, seqlen: int | None = None,
-                  ngroups: int = 1, return_final_state: bool = True):
-    """states [b, nh, nc, P, S], final_state [b, nh, P, S] = ssd_state_passing."""
+                  ngroups: int = 1, return_final_state: bool = True, states=None,
+                  final_state=None):
+    """states [b, nh, nc, P, S], final_state [b, nh, P, S] = ssd_state_passing
+    (`states` and `final_state` may be preallocated)."""
     lib = _abi.load()
     b, nh, nc, P, S = dstates.shape
     L = seqlen if seqlen is not None else nc * chunk
     d = _abi.SsdDims(b, L, nh, P, S, ngroups, int(chunk))
-    states = torch.empty_like(dstates)
-    final = (torch.empty((b, nh, P, S), dtype=torch.float32, device=dstates.device)
-             if return_final_state else None)
+    if states is None:
+        states = torch.empty_like(dstates)
+    final = final_state
+    if final is None and return_final_state:
+        final = torch.empty((b, nh, P, S), dtype=torch.float32, device=dstates.device)
     _abi.check("ssd_state_passing", lib.ssd_state_passing(
         ctypes.byref(d), _ptr(_f32(dstates, "dstates")), _ptr(_f32(G, "G")),
         _ptr(_f32(h0, "h0")), _ptr(states), _ptr(final), _stream()))
     return states, final
 
 
-def chunk_scan(x, B, C, dt, G, states, D=None, chunk: int = 256):
-    """y [b, L, nh, P] (I/O dtype) = ssd_chunk_scan."""
+def chunk_scan(x, B, C, dt, G, states, D=None, chunk: int = 256, y=None):
+    """y [b, L, nh, P] (I/O dtype) = ssd_chunk_scan (`y` may be preallocated)."""
     lib = _abi.load()
     d = dims_of(x, B, chunk)
-    y = torch.empty_like(x)
+    if y is None:
+        y = torch.empty_like(x)
     _abi.check("ssd_chunk_scan", lib.ssd_chunk_scan(
         ctypes.byref(d), _io_code(x), _ptr(x), _ptr(B), _ptr(C), _ptr(dt),
         _ptr(_f32(G, "G")), _ptr(_f32(states, "states")), _ptr(_f32(D, "D")), _ptr(y),

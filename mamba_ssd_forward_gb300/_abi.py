@@ -12,7 +12,8 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libssd_gb300.so")
 
-SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT = range(5)
+(SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT,
+ SSD_ERR_BOUNDS) = range(6)
 SSD_F32, SSD_BF16 = 0, 1
 # Size of the fixed scratch array of ssd_forward_noalloc (SSD_NOALLOC_SCRATCH_BYTES).
 SSD_NOALLOC_SCRATCH_BYTES = 32 << 20

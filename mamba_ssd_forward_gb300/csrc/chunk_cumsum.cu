@@ -20,7 +20,8 @@ constexpr int kThreads = 256;
 template <typename IO, int T>
 __global__ void __launch_bounds__(kThreads)
 chunk_cumsum_kernel(const IO *__restrict__ dt, const float *__restrict__ A,
-                    float *__restrict__ G, int64_t L, int64_t nh, int64_t nc) {
+                    float *__restrict__ G, int64_t L, int64_t nh, int64_t nc, int64_t nb,
+                    int *err) {
   constexpr int kPerLane = T / 32;
   __shared__ float tile[T][kHeadsPerBlock + 1];
   const int64_t k = blockIdx.x;
@@ -33,7 +34,10 @@ chunk_cumsum_kernel(const IO *__restrict__ dt, const float *__restrict__ A,
     const int t = idx / kHeadsPerBlock, hh = idx % kHeadsPerBlock;
     const int64_t tok = k * T + t, h = h_base + hh;
     float a = 0.f;
-    if (tok < L && h < nh) a = A[h] * ld_io(dt + (b * L + tok) * nh + h);
+    if (tok < L && h < nh) {
+      const int64_t i = (b * L + tok) * nh + h;
+      if (SSD_IN_BOUNDS(i >= 0 && i < nb * L * nh, err, 1)) a = A[h] * ld_io(dt + i);
+    }
     tile[t][hh] = a;
   }
   __syncthreads();
@@ -58,7 +62,9 @@ chunk_cumsum_kernel(const IO *__restrict__ dt, const float *__restrict__ A,
       if (lane >= off) incl += o;
     }
     const float excl = incl - run;
-    float *out = G + ((b * nh + h) * nc + k) * T + lane * kPerLane;
+    const int64_t o = ((b * nh + h) * nc + k) * T + lane * kPerLane;
+    if (!SSD_IN_BOUNDS(o >= 0 && o + kPerLane <= nb * nh * nc * T, err, 2)) continue;
+    float *out = G + o;
 #pragma unroll
     for (int i = 0; i < kPerLane; i += 2) {
       float2 w;
@@ -70,15 +76,15 @@ chunk_cumsum_kernel(const IO *__restrict__ dt, const float *__restrict__ A,
 }
 
 template <typename IO>
-cudaError_t launch_t(const Dims &d, const void *dt, const float *A, float *G,
+cudaError_t launch_t(const Dims &d, const void *dt, const float *A, float *G, int *err,
                      cudaStream_t st) {
   dim3 grid((unsigned)d.nc, (unsigned)((d.nh + kHeadsPerBlock - 1) / kHeadsPerBlock),
             (unsigned)d.b);
   const IO *p = static_cast<const IO *>(dt);
   switch (d.T) {
-    case 64: chunk_cumsum_kernel<IO, 64><<<grid, kThreads, 0, st>>>(p, A, G, d.L, d.nh, d.nc); break;
-    case 128: chunk_cumsum_kernel<IO, 128><<<grid, kThreads, 0, st>>>(p, A, G, d.L, d.nh, d.nc); break;
-    default: chunk_cumsum_kernel<IO, 256><<<grid, kThreads, 0, st>>>(p, A, G, d.L, d.nh, d.nc); break;
+    case 64: chunk_cumsum_kernel<IO, 64><<<grid, kThreads, 0, st>>>(p, A, G, d.L, d.nh, d.nc, d.b, err); break;
+    case 128: chunk_cumsum_kernel<IO, 128><<<grid, kThreads, 0, st>>>(p, A, G, d.L, d.nh, d.nc, d.b, err); break;
+    default: chunk_cumsum_kernel<IO, 256><<<grid, kThreads, 0, st>>>(p, A, G, d.L, d.nh, d.nc, d.b, err); break;
   }
   return cudaGetLastError();
 }
@@ -86,9 +92,9 @@ cudaError_t launch_t(const Dims &d, const void *dt, const float *A, float *G,
 }  // namespace
 
 cudaError_t launch_chunk_cumsum(const Dims &d, ssd_dtype io, const void *dt,
-                                const float *A, float *G, cudaStream_t st) {
-  return io == SSD_BF16 ? launch_t<__nv_bfloat16>(d, dt, A, G, st)
-                        : launch_t<float>(d, dt, A, G, st);
+                                const float *A, float *G, int *err, cudaStream_t st) {
+  return io == SSD_BF16 ? launch_t<__nv_bfloat16>(d, dt, A, G, err, st)
+                        : launch_t<float>(d, dt, A, G, err, st);
 }
 
 }  // namespace ssd

@@ -40,7 +40,7 @@ chunk_scan_tc(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
               const IO *__restrict__ dt, const float *__restrict__ G,
               const float *__restrict__ states, const float *__restrict__ Dv,
               IO *__restrict__ y, int *__restrict__ err, int L, int nh, int P, int S, int hpg,
-              int T, int nc) {
+              int T, int nc, int nb) {
   using Tr = IoT<IO>;
   constexpr int kAE = Tr::kAE;
   constexpr int kE = Tr::kE;
@@ -82,16 +82,22 @@ chunk_scan_tc(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
     ptx::tmem_alloc(&tmem_slot, ncols);
     ptx::tmem_relinquish();
   }
-  const float *Gc = G + ((int64_t)(b * nh + h) * nc + k) * T;
+  // extents of the buffers read and written below (debug-bounds builds)
+  const int64_t nG = (int64_t)nb * nh * nc * T, ndt = (int64_t)nb * L * nh;
+  const int64_t nst = (int64_t)nb * nh * nc * P * S, nx = (int64_t)nb * L * nh * P;
+  const int64_t g0 = ((int64_t)(b * nh + h) * nc + k) * T;
+  const float *Gc = G + g0;
   for (int j = tid; j < T; j += kThreads) {
-    Gs[j] = Gc[j];
-    dts[j] = j < valid ? ld_io(dt + ((int64_t)b * L + tok0 + j) * nh + h) : 0.f;
+    const int64_t idt = ((int64_t)b * L + tok0 + j) * nh + h;
+    Gs[j] = SSD_IN_BOUNDS(g0 + j < nG, err, 100) ? Gc[j] : 0.f;
+    dts[j] = j < valid && SSD_IN_BOUNDS(idt < ndt, err, 101) ? ld_io(dt + idt) : 0.f;
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const float *hst = states + ((int64_t)(b * nh + h) * nc + k) * P * S;
+  const int64_t h0i = ((int64_t)(b * nh + h) * nc + k) * P * S;
+  const float *hst = states + h0i;
 
   // ---------------- phase 1: Yoff = C h^T, S = C B^T over blocks of S
   auto load1 = [&](int sb) {
@@ -119,7 +125,8 @@ chunk_scan_tc(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
       const int p = c >> 3, ch = c & 7;
       const int s_first = sb * kAE + ch * (16 / kE);
       float v[8];
-      if (s_first < S) {
+      if (s_first < S &&
+          SSD_IN_BOUNDS(h0i + (int64_t)p * S + s_first + 16 / kE <= nst, err, 102)) {
         const float4 *src = reinterpret_cast<const float4 *>(hst + (int64_t)p * S + s_first);
         const float4 a = src[0];
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
@@ -207,7 +214,8 @@ chunk_scan_tc(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
       for (int idx = tid; idx < P * kAE; idx += kThreads) {
         const int pp = idx % P, j = idx / P, jt = jb * kAE + j;
         float v = 0.f;
-        if (jt < valid) v = ld_io(x + (((int64_t)b * L + tok0 + jt) * nh + h) * P + pp);
+        const int64_t ix = (((int64_t)b * L + tok0 + jt) * nh + h) * P + pp;
+        if (jt < valid && SSD_IN_BOUNDS(ix < nx, err, 103)) v = ld_io(x + ix);
         *reinterpret_cast<uint32_t *>(Xb + sw128(pp, j * 4)) = to_tf32(v);
       }
     } else {
@@ -249,7 +257,7 @@ chunk_scan_tc(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
     float a[16], d[16];
     ptx::tmem_ld16_sync(tmem + lane_base + col_off + c0, a);
     ptx::tmem_ld16_sync(tmem + lane_base + col_diag + c0, d);
-    if (row_ok) {
+    if (row_ok && SSD_IN_BOUNDS(yoff + P <= nx, err, 104)) {
       constexpr int per16 = 16 / kE;
 #pragma unroll
       for (int c = 0; c < 16 / per16; ++c) {
@@ -292,7 +300,7 @@ cudaError_t launch_t(const Dims &d, const void *x, const void *B, const void *C,
                                      static_cast<const IO *>(dt), G, states, D,
                                      static_cast<IO *>(y), err, (int)d.L,
                                      (int)d.nh, (int)d.P, (int)d.S, (int)d.hpg, (int)d.T,
-                                     (int)d.nc);
+                                     (int)d.nc, (int)d.b);
   return cudaGetLastError();
 }
 

@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(kThreads)
 chunk_state_tc(const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_x,
                const IO *__restrict__ dt, const float *__restrict__ G,
                float *__restrict__ dstates, int *__restrict__ err, int L, int nh, int P, int S,
-               int hpg, int T, int nc) {
+               int hpg, int T, int nc, int nb) {
   using Tr = IoT<IO>;
   constexpr int kAE = Tr::kAE;
   constexpr int nMb = kMT / kAE;  // A-operand 128-byte blocks along s
@@ -73,11 +73,15 @@ chunk_state_tc(const __grid_constant__ CUtensorMap tm_B, const __grid_constant__
     ptx::tmem_relinquish();
   }
   // w_j = exp2(G_last - G_j) dt_j, zero past the end of the sequence.
-  const float *Gc = G + ((int64_t)(b * nh + h) * nc + k) * T;
-  const float Glast = Gc[T - 1];
+  const int64_t nG = (int64_t)nb * nh * nc * T, ndt = (int64_t)nb * L * nh;
+  const int64_t g0 = ((int64_t)(b * nh + h) * nc + k) * T;
+  const float *Gc = G + g0;
+  const float Glast = SSD_IN_BOUNDS(g0 + T <= nG, err, 81) ? Gc[T - 1] : 0.f;
   for (int j = tid; j < T; j += kThreads) {
     float v = 0.f;
-    if (j < valid) v = exp2f(Glast - Gc[j]) * ld_io(dt + ((int64_t)b * L + tok0 + j) * nh + h);
+    const int64_t idt = ((int64_t)b * L + tok0 + j) * nh + h;
+    if (j < valid && SSD_IN_BOUNDS(g0 + j < nG && idt < ndt, err, 82))
+      v = exp2f(Glast - Gc[j]) * ld_io(dt + idt);
     w[j] = v;
   }
   ptx::tc_fence_before();
@@ -140,11 +144,13 @@ chunk_state_tc(const __grid_constant__ CUtensorMap tm_B, const __grid_constant__
   ptx::tc_fence_after();
 
   const int srow = s0 + warp * 32 + lane;
-  float *out = dstates + ((int64_t)(b * nh + h) * nc + k) * P * S;
+  const int64_t o0 = ((int64_t)(b * nh + h) * nc + k) * P * S;
+  float *out = dstates + o0;
   for (int c0 = 0; c0 < P; c0 += 16) {
     float v[16];
     ptx::tmem_ld16_sync(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
-    if (srow < S) {
+    if (srow < S &&
+        SSD_IN_BOUNDS(o0 + (int64_t)(c0 + 15) * S + srow < (int64_t)nb * nh * nc * P * S, err, 83)) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) out[(int64_t)(c0 + j) * S + srow] = v[j];
     }
@@ -161,7 +167,7 @@ __global__ void __launch_bounds__(kThreads)
 chunk_state_tf32(const float *__restrict__ x, const float *__restrict__ Bm,
                  const float *__restrict__ dt, const float *__restrict__ G,
                  float *__restrict__ dstates, int *__restrict__ err, int L, int nh, int P, int S,
-                 int hpg, int T, int nc) {
+                 int hpg, int T, int nc, int nb) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t mmad[2];
@@ -190,10 +196,17 @@ chunk_state_tf32(const float *__restrict__ x, const float *__restrict__ Bm,
     ptx::tmem_alloc(&tmem_slot, ncols);
     ptx::tmem_relinquish();
   }
-  const float *Gc = G + ((int64_t)(b * nh + h) * nc + k) * T;
-  const float Glast = Gc[T - 1];
-  for (int j = tid; j < T; j += kThreads)
-    w[j] = j < valid ? exp2f(Glast - Gc[j]) * dt[((int64_t)b * L + tok0 + j) * nh + h] : 0.f;
+  const int64_t nG = (int64_t)nb * nh * nc * T, ndt = (int64_t)nb * L * nh;
+  const int64_t g0 = ((int64_t)(b * nh + h) * nc + k) * T;
+  const float *Gc = G + g0;
+  const float Glast = SSD_IN_BOUNDS(g0 + T <= nG, err, 84) ? Gc[T - 1] : 0.f;
+  for (int j = tid; j < T; j += kThreads) {
+    const int64_t idt = ((int64_t)b * L + tok0 + j) * nh + h;
+    w[j] = j < valid && SSD_IN_BOUNDS(g0 + j < nG && idt < ndt, err, 85)
+               ? exp2f(Glast - Gc[j]) * dt[idt]
+               : 0.f;
+  }
+  const int64_t nB = (int64_t)nb * L * (nh / hpg) * S, nx = (int64_t)nb * L * nh * P;
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -209,15 +222,16 @@ chunk_state_tf32(const float *__restrict__ x, const float *__restrict__ Bm,
     for (int idx = tid; idx < kMT * kKB32; idx += kThreads) {
       const int sl = idx % kMT, j = idx / kMT, jt = kb * kKB32 + j;
       float v = 0.f;
-      if (s0 + sl < S && jt < valid)
-        v = Bm[(((int64_t)b * L + tok0 + jt) * (nh / hpg) + g) * S + s0 + sl];
+      const int64_t iB = (((int64_t)b * L + tok0 + jt) * (nh / hpg) + g) * S + s0 + sl;
+      if (s0 + sl < S && jt < valid && SSD_IN_BOUNDS(iB < nB, err, 86)) v = Bm[iB];
       *reinterpret_cast<uint32_t *>(A + sw128(sl, j * 4)) = to_tf32(v);
     }
     // X[p][j] = w_j x[token j][p]
     for (int idx = tid; idx < P * kKB32; idx += kThreads) {
       const int p = idx % P, j = idx / P, jt = kb * kKB32 + j;
       float v = 0.f;
-      if (jt < valid) v = w[jt] * x[(((int64_t)b * L + tok0 + jt) * nh + h) * P + p];
+      const int64_t ix = (((int64_t)b * L + tok0 + jt) * nh + h) * P + p;
+      if (jt < valid && SSD_IN_BOUNDS(ix < nx, err, 87)) v = w[jt] * x[ix];
       *reinterpret_cast<uint32_t *>(X + sw128(p, j * 4)) = to_tf32(v);
     }
     ptx::fence_async_smem();
@@ -238,11 +252,13 @@ chunk_state_tf32(const float *__restrict__ x, const float *__restrict__ Bm,
   ptx::tc_fence_after();
 
   const int srow = s0 + warp * 32 + lane;
-  float *out = dstates + ((int64_t)(b * nh + h) * nc + k) * P * S;
+  const int64_t o0 = ((int64_t)(b * nh + h) * nc + k) * P * S;
+  float *out = dstates + o0;
   for (int c0 = 0; c0 < P; c0 += 16) {
     float v[16];
     ptx::tmem_ld16_sync(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
-    if (srow < S) {
+    if (srow < S &&
+        SSD_IN_BOUNDS(o0 + (int64_t)(c0 + 15) * S + srow < (int64_t)nb * nh * nc * P * S, err, 88)) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) out[(int64_t)(c0 + j) * S + srow] = v[j];
     }
@@ -265,7 +281,7 @@ cudaError_t launch_t(const Dims &d, const void *x, const void *B, const void *dt
     chunk_state_tf32<<<grid, kThreads, smem, st>>>(
         static_cast<const float *>(x), static_cast<const float *>(B),
         static_cast<const float *>(dt), G, dstates, err, (int)d.L, (int)d.nh,
-        (int)d.P, (int)d.S, (int)d.hpg, (int)d.T, (int)d.nc);
+        (int)d.P, (int)d.S, (int)d.hpg, (int)d.T, (int)d.nc, (int)d.b);
     return cudaGetLastError();
   } else {
     constexpr bool bf = true;
@@ -280,7 +296,7 @@ cudaError_t launch_t(const Dims &d, const void *x, const void *B, const void *dt
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, st>>>(tB, tx, static_cast<const IO *>(dt), G, dstates,
                                        err, (int)d.L, (int)d.nh, (int)d.P,
-                                       (int)d.S, (int)d.hpg, (int)d.T, (int)d.nc);
+                                       (int)d.S, (int)d.hpg, (int)d.T, (int)d.nc, (int)d.b);
     return cudaGetLastError();
   }
 }

@@ -46,11 +46,13 @@ decode_step_kernel(const IO *__restrict__ x, const IO *__restrict__ dt,
                    const float *__restrict__ A, const IO *__restrict__ B,
                    const IO *__restrict__ C, const float *__restrict__ D,
                    float *__restrict__ state, IO *__restrict__ y, int nh, int P, int S, int hpg,
-                   int ng) {
+                   int ng, int64_t nbh, int *err) {
   const int64_t bh = blockIdx.x;
   const int64_t bi = bh / nh;
   const int h = (int)(bh % nh);
   const int g = h / hpg;
+  // x, dt, y and the state are indexed by bh < nbh, B and C by bi ng + g
+  if (!SSD_IN_BOUNDS(bh < nbh && g < ng, err, 20)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nsl = (S + 127) / 128;
   const float dtv = ld_io(dt + bh);
@@ -62,7 +64,7 @@ decode_step_kernel(const IO *__restrict__ x, const IO *__restrict__ dt,
 #pragma unroll
   for (int k = 0; k < kMaxSlices; ++k) {
     const int s0 = k * 128 + lane * 4;
-    if (k < nsl && s0 < S) {
+    if (k < nsl && s0 < S && SSD_IN_BOUNDS(s0 + 4 <= S, err, 21)) {
       load4(Brow + s0, Bv[k]);
       load4(Crow + s0, Cv[k]);
     } else {
@@ -87,7 +89,7 @@ decode_step_kernel(const IO *__restrict__ x, const IO *__restrict__ dt,
 #pragma unroll
     for (int k = 0; k < kMaxSlices; ++k) {
       const int s0 = k * 128 + lane * 4;
-      if (k >= nsl || s0 >= S) continue;
+      if (k >= nsl || s0 >= S || !SSD_IN_BOUNDS(s0 + 4 <= S, err, 22)) continue;
       float4 hv[kRows];
 #pragma unroll
       for (int r = 0; r < kRows; ++r) {
@@ -124,7 +126,7 @@ decode_step_kernel(const IO *__restrict__ x, const IO *__restrict__ dt,
 cudaError_t launch_decode_step(int64_t b, int64_t nh, int64_t P, int64_t S, int64_t ng,
                                ssd_dtype io, const void *x, const void *dt, const float *A,
                                const void *B, const void *C, const float *D, float *state,
-                               void *y, cudaStream_t st) {
+                               void *y, int *err, cudaStream_t st) {
   // slice P when the (batch, head) pairs alone would leave SMs idle
   // (measured: 96 pairs 10.1 -> 9.4 us; 5120 pairs are faster unsliced)
   const bool sliced = b * nh < 4 * (int64_t)sm_count();
@@ -135,13 +137,13 @@ cudaError_t launch_decode_step(int64_t b, int64_t nh, int64_t P, int64_t S, int6
         <<<grid, kWarps * 32, 0, st>>>(
         static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(dt), A,
         static_cast<const __nv_bfloat16 *>(B), static_cast<const __nv_bfloat16 *>(C), D, state,
-        static_cast<__nv_bfloat16 *>(y), (int)nh, (int)P, (int)S, hpg, (int)ng);
+        static_cast<__nv_bfloat16 *>(y), (int)nh, (int)P, (int)S, hpg, (int)ng, b * nh, err);
   else
     (sliced ? decode_step_kernel<float, true> : decode_step_kernel<float, false>)
         <<<grid, kWarps * 32, 0, st>>>(
         static_cast<const float *>(x), static_cast<const float *>(dt), A,
         static_cast<const float *>(B), static_cast<const float *>(C), D, state,
-        static_cast<float *>(y), (int)nh, (int)P, (int)S, hpg, (int)ng);
+        static_cast<float *>(y), (int)nh, (int)P, (int)S, hpg, (int)ng, b * nh, err);
   return cudaGetLastError();
 }
 

@@ -15,7 +15,7 @@ namespace ssd {
 // (decay, scale) pairs of fwd_chunk_state: each stored start state is the
 // carried state times its chunk's scale (a power of two: exact).
 cudaError_t launch_fwd_state_pass(const Dims &d, const void *dH, const float2 *gamma,
-                                  const float *h0, void *states, float *final_state,
+                                  const float *h0, void *states, float *final_state, int *err,
                                   cudaStream_t st);
 
 // Launch plans: knobs that change the speed of a kernel, never its results.

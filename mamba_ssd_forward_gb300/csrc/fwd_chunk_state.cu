@@ -66,6 +66,7 @@ struct CsArgs {
   float2 *anchor;
   int *err;
   int L, nh, P, S, hpg, T, nc, H, n_st, n_hg, nst, n_items, nout;
+  int nb;  // batch count (the extents the debug-bounds checks use)
 };
 
 // Work item -> (batch, chunk, S slice, first head).  The head groups of one
@@ -239,7 +240,7 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
       const unsigned short *dtp = reinterpret_cast<const unsigned short *>(a.dt);
 #pragma unroll
       for (int q = 0; q < kMaxH; ++q)
-        if (q < H) {
+        if (q < H && SSD_IN_BOUNDS(it.hbase + q < nh && it.b < a.nb, a.err, 40)) {
           Aq[q] = a.A[it.hbase + q];
           if (tid < valid) draw[q] = dtp[((int64_t)it.b * L + tok0 + tid) * nh + it.hbase + q];
         }
@@ -369,8 +370,8 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
           const bool ok = d[q] == 0.f || vj >= kMinFactor;
           const int all_ok = __all_sync(0xffffffffu, ok);
           if ((tid & 31) == 0) warp_fok[jl & 1][q][warp] = all_ok;
-          if (tid < T) {
-            const int64_t o = ((int64_t)it.b * nh + it.hbase + q) * nc * T + (int64_t)it.k * T + tid;
+          const int64_t o = ((int64_t)it.b * nh + it.hbase + q) * nc * T + (int64_t)it.k * T + tid;
+          if (tid < T && SSD_IN_BOUNDS(o < (int64_t)a.nb * nh * nc * T, a.err, 41)) {
             a.u[o] = ptx::ex2_approx(Gj - alpha);
             a.v[o] = vj;
           }
@@ -389,14 +390,15 @@ fwd_chunk_state_bf16(const __grid_constant__ CUtensorMap tm_B,
           if (a.anchor) ok &= warp_fok[jl & 1][q][w2];
         }
         const int64_t o = ((int64_t)it.b * nh + it.hbase + q) * nc + it.k;
+        const bool o_ok = SSD_IN_BOUNDS(o < (int64_t)a.nb * nh * nc, a.err, 42);
         float scale = 1.f;
         if (a.anchor) {
           const bool steep = !(ok && -tot <= kSpanMax);
           const float alpha = steep ? 0.f : rintf(0.5f * tot);
-          a.anchor[o] = make_float2(alpha, steep ? 1.f : 0.f);
+          if (o_ok) a.anchor[o] = make_float2(alpha, steep ? 1.f : 0.f);
           scale = __int_as_float((127 + (int)alpha) << 23);  // 2^alpha, alpha in [-91, 0]
         }
-        a.gamma[o] = make_float2(exp2f(tot), scale);
+        if (o_ok) a.gamma[o] = make_float2(exp2f(tot), scale);
       }
       fetch(item + gridDim.x);  // in flight while this item is scaled
 
@@ -577,6 +579,7 @@ cudaError_t launch_fwd_chunk_state(const Dims &d, const void *x, const void *B, 
   a.hpg = (int)d.hpg;
   a.T = (int)d.T;
   a.nc = (int)d.nc;
+  a.nb = (int)d.b;
   a.H = H;
   a.n_st = (int)((d.S + 128 * nsl - 1) / (128 * nsl));
   a.n_hg = (int)(d.nh / H);

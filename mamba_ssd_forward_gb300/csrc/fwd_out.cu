@@ -71,6 +71,7 @@ struct OutArgs {
   const float2 *anchor;
   int *err;
   int L, nh, S, hpg, T, nc, hs, nslot, nyst;
+  int nb;  // batch count (the extents the debug-bounds checks use)
 };
 
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
@@ -253,7 +254,10 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       if (q >= 2) ptx::mbar_wait(&acc_free[set], ((q >> 1) - 1) & 1, a.err, 146);
       ptx::tc_fence_after();
       // the chunk's path, from its anchor
-      const int steep = a.anchor[((int64_t)b * nh + hbase + q) * a.nc + k].y != 0.f;
+      const int64_t ai = ((int64_t)b * nh + hbase + q) * a.nc + k;
+      const int steep = SSD_IN_BOUNDS(ai < (int64_t)a.nb * nh * a.nc, a.err, 61)
+                            ? a.anchor[ai].y != 0.f
+                            : 0;
       // Acc_t = C_t (2^alpha h)^T over the state stages (stored scaled by the
       // state pass)
       for (int hh = 0; hh < nH; ++hh, ++u) {
@@ -332,10 +336,14 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       const int h = hbase + q;
       const int64_t bhk = ((int64_t)b * nh + h) * a.nc + k;
       const int64_t o = bhk * kT + erow;
-      r.u = a.u[o];
-      r.v = a.v[o];
-      r.steep = a.anchor[bhk].y != 0.f;
-      r.D = a.D ? a.D[h] : 0.f;
+      r.u = r.v = r.D = 0.f;
+      r.steep = 0;
+      if (SSD_IN_BOUNDS(h < nh && bhk < (int64_t)a.nb * nh * a.nc, a.err, 62)) {
+        r.u = a.u[o];
+        r.v = a.v[o];
+        r.steep = a.anchor[bhk].y != 0.f;
+        r.D = a.D ? a.D[h] : 0.f;
+      }
       return r;
     };
 
@@ -385,7 +393,9 @@ fwd_out_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       const int pb = q & 1, h = hbase + q;
       const unsigned short *dtp = reinterpret_cast<const unsigned short *>(a.dt);
       const unsigned short raw =
-          tok_ok ? dtp[((int64_t)b * L + tok0 + tid) * nh + h] : (unsigned short)0;
+          tok_ok && SSD_IN_BOUNDS(h < nh && b < a.nb, a.err, 63)
+              ? dtp[((int64_t)b * L + tok0 + tid) * nh + h]
+              : (unsigned short)0;
       const float d = __uint_as_float((uint32_t)raw << 16);  // bf16 -> fp32, exact
       float incl = a.A[h] * kLog2e * d;
 #pragma unroll
@@ -662,6 +672,7 @@ cudaError_t launch_fwd_out(const Dims &d, const void *x, const void *B, const vo
   a.hpg = (int)d.hpg;
   a.T = (int)d.T;
   a.nc = (int)d.nc;
+  a.nb = (int)d.b;
   a.hs = hs;
   a.nslot = m.nslot;
   a.nyst = m.nyst;

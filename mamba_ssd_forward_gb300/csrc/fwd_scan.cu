@@ -49,6 +49,7 @@ struct ScanArgs {
   __nv_bfloat16 *y;
   int *err;
   int L, nh, P, S, hpg, T, nc, H, nX;
+  int nb;  // batch count (the extents the debug-bounds checks use)
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -232,13 +233,13 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
     float dh[kMaxH];
 #pragma unroll
     for (int q = 0; q < kMaxH; ++q)
-      dh[q] = (q < H && tid < valid)
+      dh[q] = (q < H && tid < valid && SSD_IN_BOUNDS(hbase + q < nh && b < a.nb, a.err, 120))
                   ? __bfloat162float(a.dt[((int64_t)b * L + tok0 + tid) * nh + hbase + q])
                   : 0.f;
 #pragma unroll
     for (int q = 0; q < kMaxH; ++q) {
       if (q >= H) break;
-      const float run = a.A[hbase + q] * kLog2e * dh[q];
+      const float run = (hbase + q < nh ? a.A[hbase + q] : 0.f) * kLog2e * dh[q];
       float incl = run;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -281,8 +282,9 @@ fwd_scan_bf16(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
       ptx::tc_fence_after();
       const int h = hbase + q;
       const float Dh = a.D ? a.D[h] : 0.f;
-      const bool ok = i_rel < valid;
       const int64_t off = (((int64_t)b * L + tok0 + i_rel) * nh + h) * P;
+      const bool ok = i_rel < valid &&
+                      SSD_IN_BOUNDS(h < nh && off + P <= (int64_t)a.nb * L * nh * P, a.err, 121);
 #pragma unroll
       for (int gi = 0; gi < 2; ++gi) {
         const int c0 = (qtr + 4 * gi) * 16;
@@ -442,6 +444,7 @@ cudaError_t launch_fwd_scan(const Dims &d, const void *x, const void *B, const v
   a.hpg = (int)d.hpg;
   a.T = (int)d.T;
   a.nc = (int)d.nc;
+  a.nb = (int)d.b;
   a.H = H;
   a.nX = nX;
   const int n_it = (int)((d.T + 127) / 128);

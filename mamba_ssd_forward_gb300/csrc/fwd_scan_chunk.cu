@@ -98,6 +98,7 @@ struct ChunkArgs {
   __nv_bfloat16 *y;
   int *err;
   int L, nh, S, hpg, T, nc, hs;
+  int nb;  // batch count (the extents the debug-bounds checks use)
   // shared-memory layout (byte offsets from the 1024-aligned base)
   int off_C, off_B, off_hx0, off_hx1;
 };
@@ -312,8 +313,10 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
     const unsigned short *dtp = reinterpret_cast<const unsigned short *>(a.dt);
     const bool tok_ok = tid < valid;
     const int64_t dt_off = ((int64_t)b * L + tok0 + (tok_ok ? tid : 0)) * nh + hbase;
-    unsigned short draw = tok_ok ? dtp[dt_off] : (unsigned short)0;
-    float Aq = a.A[hbase];
+    // every head of the slice lies in [0, nh) and b in [0, nb)
+    const bool hok = SSD_IN_BOUNDS(hbase + hs <= nh && b < a.nb, a.err, 140);
+    unsigned short draw = tok_ok && hok ? dtp[dt_off] : (unsigned short)0;
+    float Aq = hok ? a.A[hbase] : 0.f;
     // in-chunk cumsum of head q (one token per thread, threads < T) into the
     // buffers of parity q & 1, and the column factors of the factored decay;
     // then the dt of head q + 1 is fetched
@@ -344,8 +347,8 @@ fwd_scan_chunk_bf16(const __grid_constant__ CUtensorMap tm_C,
       }
       ptx::named_bar_sync(1, kRowThreads);
       if (q + 1 < hs) {
-        draw = tok_ok ? dtp[dt_off + q + 1] : (unsigned short)0;
-        Aq = a.A[hbase + q + 1];
+        draw = tok_ok && hok ? dtp[dt_off + q + 1] : (unsigned short)0;
+        Aq = hok ? a.A[hbase + q + 1] : 0.f;
       }
     };
 
@@ -668,6 +671,7 @@ cudaError_t launch_fwd_scan_chunk(const Dims &d, const void *x, const void *B, c
   a.hpg = (int)d.hpg;
   a.T = (int)d.T;
   a.nc = (int)d.nc;
+  a.nb = (int)d.b;
   a.hs = hs;
   a.off_C = l.off_C;
   a.off_B = l.off_B;

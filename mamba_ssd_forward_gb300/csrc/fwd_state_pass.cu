@@ -25,15 +25,21 @@ constexpr int kDepth = 8;  // chunks per prefetch group
 __global__ void __launch_bounds__(kThreads, 2)
 fwd_state_pass_bf16(const uint4 *__restrict__ dH, const float2 *__restrict__ gamma,
                     const float *__restrict__ h0, uint4 *__restrict__ states,
-                    float *__restrict__ final_state, int P, int S, int nc) {
+                    float *__restrict__ final_state, int P, int S, int nc, int64_t nbh,
+                    int *err) {
   // the CTA's (decay, scale) pairs, 256 chunks at a time
   __shared__ float2 gsm[256];
-  const int64_t bh = blockIdx.y;
   const int n8 = S * P / 8;
   const int e8x = blockIdx.x * kThreads + threadIdx.x;
+  // every index below lies in [0, nbh nc n8) (dH, states), [0, nbh nc)
+  // (gamma) or [0, nbh P S) (h0, final state) when bh < nbh and e8 < n8; a
+  // failed check works on element 0 of head 0 without storing, so that the
+  // thread still takes part in the barriers
+  const bool ok = SSD_IN_BOUNDS((int64_t)blockIdx.y < nbh, err, 30);
+  const int64_t bh = ok ? blockIdx.y : 0;
   // threads past the state (a partial last CTA) take part in the barriers
   // only, working on element 0 without storing
-  const bool live = e8x < n8;
+  const bool live = e8x < n8 && ok;
   const int e8 = live ? e8x : 0;
   const int s = (e8 * 8) / P, p0 = (e8 * 8) % P;
   ptx::griddep_launch_dependents();  // the output pass may be scheduled now
@@ -88,7 +94,7 @@ fwd_state_pass_bf16(const uint4 *__restrict__ dH, const float2 *__restrict__ gam
 }  // namespace
 
 cudaError_t launch_fwd_state_pass(const Dims &d, const void *dH, const float2 *gamma,
-                                  const float *h0, void *states, float *final_state,
+                                  const float *h0, void *states, float *final_state, int *err,
                                   cudaStream_t st) {
   const int n8 = (int)(d.S * d.P / 8);
   dim3 grid((unsigned)((n8 + kThreads - 1) / kThreads), (unsigned)(d.b * d.nh));
@@ -106,7 +112,7 @@ cudaError_t launch_fwd_state_pass(const Dims &d, const void *dH, const float2 *g
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fwd_state_pass_bf16, static_cast<const uint4 *>(dH), gamma,
                             h0, static_cast<uint4 *>(states), final_state, (int)d.P,
-                            (int)d.S, (int)d.nc);
+                            (int)d.S, (int)d.nc, (int64_t)(d.b * d.nh), err);
 }
 
 }  // namespace ssd

@@ -214,6 +214,8 @@ const char *ssd_status_string(ssd_status s) {
     case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: dimensions outside the supported range";
     case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA call or kernel launch failed";
     case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: a bounded device-side wait gave up";
+    case SSD_ERR_BOUNDS:
+      return "SSD_ERR_BOUNDS: a debug-bounds build caught an out-of-range access";
   }
   return "SSD_ERR_UNKNOWN";
 }
@@ -223,7 +225,7 @@ ssd_status ssd_device_error(void *stream) {
   int code = 0;
   if (!word || ssd::read_and_clear_error(word, (cudaStream_t)stream, &code) != cudaSuccess)
     return SSD_ERR_CUDA;
-  return code ? SSD_ERR_TIMEOUT : SSD_OK;
+  return ssd::status_of_error_code(code);
 }
 
 ssd_status ssd_workspace_error(void *workspace, void *stream) {
@@ -232,7 +234,7 @@ ssd_status ssd_workspace_error(void *workspace, void *stream) {
   if (ssd::read_and_clear_error(static_cast<int *>(workspace), (cudaStream_t)stream, &code) !=
       cudaSuccess)
     return SSD_ERR_CUDA;
-  return code ? SSD_ERR_TIMEOUT : SSD_OK;
+  return ssd::status_of_error_code(code);
 }
 
 size_t ssd_forward_workspace_size(const ssd_dims *dims, ssd_dtype dtype) {
@@ -247,7 +249,9 @@ ssd_status ssd_chunk_cumsum(const ssd_dims *dims, ssd_dtype dtype, const void *d
   ssd_status s = check_dims(dims, &d);
   if (s != SSD_OK) return s;
   if (!valid_dtype(dtype) || !req(dt) || !req(A) || !req(G)) return SSD_ERR_INVALID_ARG;
-  return from_cuda(ssd::launch_chunk_cumsum(d, dtype, dt, A, G, (cudaStream_t)stream));
+  int *err = ssd::device_error_word();
+  if (!err) return SSD_ERR_CUDA;
+  return from_cuda(ssd::launch_chunk_cumsum(d, dtype, dt, A, G, err, (cudaStream_t)stream));
 }
 
 ssd_status ssd_chunk_state(const ssd_dims *dims, ssd_dtype dtype, const void *x,
@@ -272,7 +276,9 @@ ssd_status ssd_state_passing(const ssd_dims *dims, const float *dstates, const f
   if (s != SSD_OK) return s;
   if (!req(dstates) || !req(G) || !opt(h0) || !req(states) || !opt(final_state))
     return SSD_ERR_INVALID_ARG;
-  return from_cuda(ssd::launch_state_passing(d, dstates, G, h0, states, final_state,
+  int *err = ssd::device_error_word();
+  if (!err) return SSD_ERR_CUDA;
+  return from_cuda(ssd::launch_state_passing(d, dstates, G, h0, states, final_state, err,
                                              (cudaStream_t)stream));
 }
 
@@ -306,8 +312,10 @@ ssd_status ssd_decode_step(const ssd_dims *dims, ssd_dtype dtype, const void *x,
   if (!valid_dtype(dtype) || !req(x) || !req(dt) || !req(A) || !req(B) || !req(C) || !opt(D) ||
       !req(state) || !req(y))
     return SSD_ERR_INVALID_ARG;
+  int *err = ssd::device_error_word();
+  if (!err) return SSD_ERR_CUDA;
   return from_cuda(ssd::launch_decode_step(d.batch, d.nheads, d.headdim, d.dstate, d.ngroups,
-                                           dtype, x, dt, A, B, C, D, state, y,
+                                           dtype, x, dt, A, B, C, D, state, y, err,
                                            (cudaStream_t)stream));
 }
 
@@ -373,7 +381,7 @@ ssd_status forward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
                                       err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
     if (e == cudaSuccess)
-      e = ssd::launch_fwd_state_pass(d, bw.dH, bw.gamma, h0, bw.states, final_state, st);
+      e = ssd::launch_fwd_state_pass(d, bw.dH, bw.gamma, h0, bw.states, final_state, err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
     if (e == cudaSuccess) e = launch_scan(d, fp, x, B, C, dt, A, bw, D, y, err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
@@ -381,11 +389,12 @@ ssd_status forward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
     float *G = reinterpret_cast<float *>(ws + w.G);
     float *dst = reinterpret_cast<float *>(ws + w.dstates);
     float *sts = reinterpret_cast<float *>(ws + w.states);
-    if (e == cudaSuccess) e = ssd::launch_chunk_cumsum(d, dtype, dt, A, G, st);
+    if (e == cudaSuccess) e = ssd::launch_chunk_cumsum(d, dtype, dt, A, G, err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
     if (e == cudaSuccess) e = ssd::launch_chunk_state(d, dtype, x, B, dt, G, dst, err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
-    if (e == cudaSuccess) e = ssd::launch_state_passing(d, dst, G, h0, sts, final_state, st);
+    if (e == cudaSuccess)
+      e = ssd::launch_state_passing(d, dst, G, h0, sts, final_state, err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
     if (e == cudaSuccess)
       e = ssd::launch_chunk_scan(d, dtype, x, B, C, dt, G, sts, D, y, err, st);

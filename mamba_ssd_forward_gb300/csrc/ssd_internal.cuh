@@ -18,6 +18,24 @@ struct Dims {
   int64_t hpg;  // heads per group
 };
 
+// Debug-bounds builds (compiled with -DSSD_DEBUG_BOUNDS; the release library
+// never is): SSD_IN_BOUNDS(cond, err, site) evaluates `cond`, the index of a
+// global access checked against its buffer's extent; a false condition
+// records kErrBoundsBase + site in the error word `err` (when not null and
+// still clear) and the caller skips the access.  In release builds it is the
+// constant true and `cond` is not evaluated.  The host reports such a code as
+// SSD_ERR_BOUNDS.
+constexpr int kErrBoundsBase = 2000;
+#ifdef SSD_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds_check(bool ok, int *err, int site) {
+  if (!ok && err) atomicCAS(err, 0, kErrBoundsBase + site);
+  return ok;
+}
+#define SSD_IN_BOUNDS(cond, err, site) (::ssd::in_bounds_check((cond), (err), (site)))
+#else
+#define SSD_IN_BOUNDS(cond, err, site) (true)
+#endif
+
 // Element access for the two I/O types.
 __device__ __forceinline__ float ld_io(const float *p) { return *p; }
 __device__ __forceinline__ float ld_io(const __nv_bfloat16 *p) {
@@ -36,6 +54,13 @@ int *device_error_word();
 // Copy the error word at `word` (device) to *code and clear it; synchronises
 // `st`.
 cudaError_t read_and_clear_error(int *word, cudaStream_t st, int *code);
+// The status an error-word code stands for: 0 -> SSD_OK, a debug-bounds
+// code (kErrBoundsBase and up) -> SSD_ERR_BOUNDS, any other -> the code of a
+// bounded wait that gave up, SSD_ERR_TIMEOUT.
+inline ssd_status status_of_error_code(int code) {
+  if (code == 0) return SSD_OK;
+  return code >= kErrBoundsBase ? SSD_ERR_BOUNDS : SSD_ERR_TIMEOUT;
+}
 
 // SM count of the current device, looked up once per device and cached
 // (race-free under concurrent callers).
@@ -65,15 +90,16 @@ ssd_status forward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
 ssd_status plan_status(const ssd_dims *dims, ssd_dtype dtype, const ssd_plan *plan);
 
 // Launchers (one per step).  Each enqueues its kernel(s) on `st` and returns
-// the cudaGetLastError() of the launch.
+// the cudaGetLastError() of the launch; `err` is the device error word its
+// kernels report to.
 cudaError_t launch_chunk_cumsum(const Dims &d, ssd_dtype io, const void *dt,
-                                const float *A, float *G, cudaStream_t st);
+                                const float *A, float *G, int *err, cudaStream_t st);
 cudaError_t launch_chunk_state(const Dims &d, ssd_dtype io, const void *x,
                                const void *B, const void *dt, const float *G,
                                float *dstates, int *err, cudaStream_t st);
 cudaError_t launch_state_passing(const Dims &d, const float *dstates,
                                  const float *G, const float *h0,
-                                 float *states, float *final_state,
+                                 float *states, float *final_state, int *err,
                                  cudaStream_t st);
 cudaError_t launch_chunk_scan(const Dims &d, ssd_dtype io, const void *x,
                               const void *B, const void *C, const void *dt,
@@ -84,6 +110,6 @@ cudaError_t launch_chunk_scan(const Dims &d, ssd_dtype io, const void *x,
 cudaError_t launch_decode_step(int64_t b, int64_t nh, int64_t P, int64_t S, int64_t ng,
                                ssd_dtype io, const void *x, const void *dt, const float *A,
                                const void *B, const void *C, const float *D, float *state,
-                               void *y, cudaStream_t st);
+                               void *y, int *err, cudaStream_t st);
 
 }  // namespace ssd

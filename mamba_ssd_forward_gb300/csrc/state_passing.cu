@@ -19,10 +19,13 @@ __global__ void __launch_bounds__(kThreads)
 state_passing_kernel(const float4 *__restrict__ dstates,
                      const float *__restrict__ G, const float4 *__restrict__ h0,
                      float4 *__restrict__ states, float4 *__restrict__ final_state,
-                     int64_t ps4, int64_t nc, int64_t T) {
+                     int64_t ps4, int64_t nc, int64_t T, int64_t nbh, int *err) {
   const int64_t bh = blockIdx.y;
   const int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x;  // float4 index in P*S
   if (e >= ps4) return;
+  // every index below lies in [0, nbh nc ps4) (states, dstates), [0, nbh
+  // ps4) (h0, final_state) or [0, nbh nc T) (G)
+  if (!SSD_IN_BOUNDS(bh < nbh && e >= 0, err, 10)) return;
   float4 h = h0 ? h0[bh * ps4 + e] : make_float4(0.f, 0.f, 0.f, 0.f);
   const float *Gbh = G + bh * nc * T;
   const float4 *dsrc = dstates + bh * nc * ps4 + e;
@@ -45,14 +48,14 @@ state_passing_kernel(const float4 *__restrict__ dstates,
 
 cudaError_t launch_state_passing(const Dims &d, const float *dstates,
                                  const float *G, const float *h0,
-                                 float *states, float *final_state,
+                                 float *states, float *final_state, int *err,
                                  cudaStream_t st) {
   const int64_t ps4 = d.P * d.S / 4;
   dim3 grid((unsigned)((ps4 + kThreads - 1) / kThreads), (unsigned)(d.b * d.nh));
   state_passing_kernel<<<grid, kThreads, 0, st>>>(
       reinterpret_cast<const float4 *>(dstates), G,
       reinterpret_cast<const float4 *>(h0), reinterpret_cast<float4 *>(states),
-      reinterpret_cast<float4 *>(final_state), ps4, d.nc, d.T);
+      reinterpret_cast<float4 *>(final_state), ps4, d.nc, d.T, d.b * d.nh, err);
   return cudaGetLastError();
 }
 

@@ -48,9 +48,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(5):
+    for code in range(6):
         s = lib.ssd_status_string(code).decode()
-        assert s.startswith("SSD_")
+        assert s.startswith("SSD_") and "UNKNOWN" not in s
     assert lib.ssd_status_string(77).decode() == "SSD_ERR_UNKNOWN"
 
 
@@ -327,3 +327,15 @@ def test_library_keeps_no_plan_table():
     assert "std::map" not in src and "mutex" not in src and "static" not in src
     names = declared_functions()
     assert "ssd_forward_set_plan" not in names and "ssd_forward_get_plan" not in names
+
+
+def test_debug_bounds_library_builds_with_every_export():
+    """The debug-bounds variant (SSD_DEBUG_BOUNDS) compiles from the same
+    sources and exports the same C ABI; the GPU tests run it."""
+    import ctypes
+    from mamba_ssd_forward_gb300 import _abi, build
+    path = build.build_debug()
+    lib = ctypes.CDLL(path)
+    for n in _abi.EXPORTS:
+        assert hasattr(lib, n), n
+    assert path != _abi.LIB_PATH
