@@ -136,14 +136,19 @@ def kernel_bytes(w: W.Workload) -> dict:
     st = w.batch * w.nheads * w.nchunks * w.headdim * w.dstate * 4
     fin = w.batch * w.nheads * w.headdim * w.dstate * 4
     st16 = w.batch * w.nheads * w.nchunks * w.headdim * w.dstate * 2
-    gam = w.batch * w.nheads * w.nchunks * 4
+    # per (batch, head, chunk): (decay, start-state scale) and (anchor, path)
+    # float2 pairs; per token and head the fp32 factors u and v of the
+    # factored output pass
+    gam = w.batch * w.nheads * w.nchunks * 8
+    anc = w.batch * w.nheads * w.nchunks * 8
+    uv = 2 * w.batch * w.nheads * w.nchunks * w.chunk * 4
     h0 = fin if w.has_h0 else 0
     return {
-        "fwd_chunk_state": x + bc + dt + w.nheads * 4 + st16 + gam,
+        "fwd_chunk_state": x + bc + dt + w.nheads * 4 + st16 + gam + anc + uv,
         "fwd_state_pass": 2 * st16 + gam + h0 + fin,
         "fwd_scan": 2 * x + 2 * bc + dt + 2 * w.nheads * 4 + st16,
         "fwd_scan_chunk": 2 * x + 2 * bc + dt + 2 * w.nheads * 4 + st16,
-        "fwd_out": 2 * x + 2 * bc + dt + 2 * w.nheads * 4 + st16,
+        "fwd_out": 2 * x + 2 * bc + dt + 2 * w.nheads * 4 + st16 + anc + uv,
         "chunk_cumsum": dt + G + w.nheads * 4,
         "chunk_state": x + bc + dt + G + st,
         "state_passing": 2 * st + w.batch * w.nheads * w.nchunks * 4 + fin * (2 if w.has_h0 else 1),
