@@ -210,13 +210,30 @@ chunk_scan_tc(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ 
       }
     }
     if constexpr (Tr::kTf32) {
-      // X^T (rows p, tokens along the 128-byte row), rounded to tf32
-      for (int idx = tid; idx < P * kAE; idx += kThreads) {
-        const int pp = idx % P, j = idx / P, jt = jb * kAE + j;
-        float v = 0.f;
-        const int64_t ix = (((int64_t)b * L + tok0 + jt) * nh + h) * P + pp;
-        if (jt < valid && SSD_IN_BOUNDS(ix < nx, err, 103)) v = ld_io(x + ix);
-        *reinterpret_cast<uint32_t *>(Xb + sw128(pp, j * 4)) = to_tf32(v);
+      // X^T (rows p, tokens along the 128-byte row), rounded to tf32: lane =
+      // token j, each lane loads four consecutive p (16 bytes) and writes
+      // them down four rows at its column (a warp writes 32 consecutive
+      // words of a row); every load is issued before the first store
+      constexpr int kXqMax = (128 / 4) * kAE / kThreads;  // quads per thread, P <= 128
+      const int nXq = (P / 4) * kAE;
+      float4 xq[kXqMax];
+#pragma unroll
+      for (int r = 0; r < kXqMax; ++r) {
+        const int idx = tid + r * kThreads, j = idx % kAE, q = idx / kAE;
+        const int jt = jb * kAE + j;
+        const int64_t ix = (((int64_t)b * L + tok0 + jt) * nh + h) * P + 4 * q;
+        xq[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (idx < nXq && jt < valid && SSD_IN_BOUNDS(ix + 4 <= nx, err, 103))
+          xq[r] = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + ix);
+      }
+#pragma unroll
+      for (int r = 0; r < kXqMax; ++r) {
+        const int idx = tid + r * kThreads, j = idx % kAE, q = idx / kAE;
+        if (idx >= nXq) break;
+        *reinterpret_cast<uint32_t *>(Xb + sw128(4 * q + 0, j * 4)) = to_tf32(xq[r].x);
+        *reinterpret_cast<uint32_t *>(Xb + sw128(4 * q + 1, j * 4)) = to_tf32(xq[r].y);
+        *reinterpret_cast<uint32_t *>(Xb + sw128(4 * q + 2, j * 4)) = to_tf32(xq[r].z);
+        *reinterpret_cast<uint32_t *>(Xb + sw128(4 * q + 3, j * 4)) = to_tf32(xq[r].w);
       }
     } else {
       ptx::mbar_wait(&full[s], ph, err, 44);

@@ -218,21 +218,50 @@ chunk_state_tf32(const float *__restrict__ x, const float *__restrict__ Bm,
     if (kb >= 2) ptx::mbar_wait(&mmad[s], ((kb >> 1) - 1) & 1, err, 24);
     uint8_t *A = smem + s * stage_bytes;
     uint8_t *X = A + aBytes;
-    // A[s][j] = B[token j][s]: read along s (coalesced), write transposed
-    for (int idx = tid; idx < kMT * kKB32; idx += kThreads) {
-      const int sl = idx % kMT, j = idx / kMT, jt = kb * kKB32 + j;
-      float v = 0.f;
-      const int64_t iB = (((int64_t)b * L + tok0 + jt) * (nh / hpg) + g) * S + s0 + sl;
-      if (s0 + sl < S && jt < valid && SSD_IN_BOUNDS(iB < nB, err, 86)) v = Bm[iB];
-      *reinterpret_cast<uint32_t *>(A + sw128(sl, j * 4)) = to_tf32(v);
+    // A[s][j] = B[token j][s] and X[p][j] = w_j x[token j][p], transposed
+    // through registers: lane = token j of the block, each lane loads 16
+    // bytes (four consecutive s or p) and writes them down four rows at its
+    // column, so a warp writes 32 consecutive words of a row (no bank
+    // conflicts); every load of the block is issued before the first store.
+    constexpr int kAq = (kMT / 4) * kKB32 / kThreads;  // B quads per thread (8)
+    constexpr int kXqMax = (128 / 4) * kKB32 / kThreads;  // x quads per thread, P <= 128
+    const int nXq = (P / 4) * kKB32;
+    float4 bq[kAq], xq[kXqMax];
+#pragma unroll
+    for (int r = 0; r < kAq; ++r) {
+      const int idx = tid + r * kThreads, j = idx % kKB32, q = idx / kKB32;
+      const int jt = kb * kKB32 + j;
+      const int64_t iB = (((int64_t)b * L + tok0 + jt) * (nh / hpg) + g) * S + s0 + 4 * q;
+      bq[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s0 + 4 * q < S && jt < valid && SSD_IN_BOUNDS(iB + 4 <= nB, err, 86))
+        bq[r] = *reinterpret_cast<const float4 *>(Bm + iB);
     }
-    // X[p][j] = w_j x[token j][p]
-    for (int idx = tid; idx < P * kKB32; idx += kThreads) {
-      const int p = idx % P, j = idx / P, jt = kb * kKB32 + j;
-      float v = 0.f;
-      const int64_t ix = (((int64_t)b * L + tok0 + jt) * nh + h) * P + p;
-      if (jt < valid && SSD_IN_BOUNDS(ix < nx, err, 87)) v = w[jt] * x[ix];
-      *reinterpret_cast<uint32_t *>(X + sw128(p, j * 4)) = to_tf32(v);
+#pragma unroll
+    for (int r = 0; r < kXqMax; ++r) {
+      const int idx = tid + r * kThreads, j = idx % kKB32, q = idx / kKB32;
+      const int jt = kb * kKB32 + j;
+      const int64_t ix = (((int64_t)b * L + tok0 + jt) * nh + h) * P + 4 * q;
+      xq[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (idx < nXq && jt < valid && SSD_IN_BOUNDS(ix + 4 <= nx, err, 87))
+        xq[r] = *reinterpret_cast<const float4 *>(x + ix);
+    }
+#pragma unroll
+    for (int r = 0; r < kAq; ++r) {
+      const int idx = tid + r * kThreads, j = idx % kKB32, q = idx / kKB32;
+      *reinterpret_cast<uint32_t *>(A + sw128(4 * q + 0, j * 4)) = to_tf32(bq[r].x);
+      *reinterpret_cast<uint32_t *>(A + sw128(4 * q + 1, j * 4)) = to_tf32(bq[r].y);
+      *reinterpret_cast<uint32_t *>(A + sw128(4 * q + 2, j * 4)) = to_tf32(bq[r].z);
+      *reinterpret_cast<uint32_t *>(A + sw128(4 * q + 3, j * 4)) = to_tf32(bq[r].w);
+    }
+#pragma unroll
+    for (int r = 0; r < kXqMax; ++r) {
+      const int idx = tid + r * kThreads, j = idx % kKB32, q = idx / kKB32;
+      if (idx >= nXq) break;
+      const float wj = w[kb * kKB32 + j];
+      *reinterpret_cast<uint32_t *>(X + sw128(4 * q + 0, j * 4)) = to_tf32(wj * xq[r].x);
+      *reinterpret_cast<uint32_t *>(X + sw128(4 * q + 1, j * 4)) = to_tf32(wj * xq[r].y);
+      *reinterpret_cast<uint32_t *>(X + sw128(4 * q + 2, j * 4)) = to_tf32(wj * xq[r].z);
+      *reinterpret_cast<uint32_t *>(X + sw128(4 * q + 3, j * 4)) = to_tf32(wj * xq[r].w);
     }
     ptx::fence_async_smem();
     __syncthreads();
