@@ -620,7 +620,7 @@ def main(argv=None):
     ap.add_argument("--no-tune", dest="tune", action="store_false",
                     help="use the cost-model launch plan instead of timing the candidates")
     ap.add_argument("--skip-e2e", action="store_true")
-    ap.add_argument("--e2e-slices", type=int, default=4,
+    ap.add_argument("--e2e-slices", type=int, default=8,
                     help="slices of the host-buffer path (copies overlap the computation)")
     ap.add_argument("--flush", choices=["write+read", "write"], default="write+read",
                     help="L2 flush between steps (default: write a buffer, then read another)")
