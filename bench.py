@@ -371,13 +371,14 @@ def run_ours(args, w):
     nev = 8
 
     # launch plan: the timing autotuner's choice for this shape (once, before
-    # the warm-up; passed to every later call), or the cost model's
+    # the warm-up; every candidate timed from a cold L2, as the timed steps
+    # run; passed to every later call), or the cost model's
     plan, tuned = None, False
     if w.dtype == "bf16":
         dims = ssd.dims_of(d["x"], d["B"], w.chunk)
         if args.tune:
             plan, _, _ = ssd.tune(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"],
-                                  chunk=w.chunk, reps=5, workspace=ws)
+                                  chunk=w.chunk, reps=5, workspace=ws, flush=flush_w)
             tuned = True
         else:
             plan = ssd.default_plan(dims)

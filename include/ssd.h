@@ -217,18 +217,20 @@ SSD_API ssd_status ssd_forward_ex(const ssd_dims *dims, ssd_dtype dtype, const v
  * `workspace` (ssd_forward, ssd_forward_ex, ssd_forward_profiled,
  * ssd_forward_tune, ssd_forward_host, ssd_forward_host_overlapped) gave up a
  * bounded device-side wait since the word was last cleared
- * (SSD_ERR_TIMEOUT; the outputs of that call are undefined), then clears
- * the word.  Each workspace has its own word, so calls on other workspaces
+ * (SSD_ERR_TIMEOUT; the outputs of that call are undefined) or, in the
+ * debug-bounds build, made an out-of-range access (SSD_ERR_BOUNDS), then
+ * clears the word.  Each workspace has its own word, so calls on other workspaces
  * or streams neither see nor clear it.  SSD_ERR_INVALID_ARG for a NULL or
  * misaligned workspace; SSD_ERR_CUDA if the synchronisation fails. */
 SSD_API ssd_status ssd_workspace_error(void *workspace, void *stream);
 
 /* The same for the library-wide error word, which only the calls without a
- * workspace of their own report to: ssd_chunk_state, ssd_chunk_scan (the
- * step-wise entry points with tensor-core kernels) and ssd_forward_noalloc.
- * Synchronises `stream`, reports SSD_ERR_TIMEOUT if any of them gave up a
- * bounded wait on this device since the word was last cleared, and clears
- * it. */
+ * workspace of their own report to: the step-wise entry points
+ * (ssd_chunk_cumsum, ssd_chunk_state, ssd_state_passing, ssd_chunk_scan),
+ * ssd_decode_step and ssd_forward_noalloc.  Synchronises `stream`, reports
+ * SSD_ERR_TIMEOUT if any of them gave up a bounded wait on this device (or,
+ * in the debug-bounds build, SSD_ERR_BOUNDS for an out-of-range access)
+ * since the word was last cleared, and clears it. */
 SSD_API ssd_status ssd_device_error(void *stream);
 
 /* Self-test of the bounded device-side waits (no counterpart on the pages):
@@ -403,18 +405,24 @@ SSD_API ssd_status ssd_forward_default_plan(const ssd_dims *dims, ssd_dtype dtyp
  * ssd_forward (SSD_BF16 only, else SSD_ERR_UNSUPPORTED).  Runs the forward
  * pass once with the default plan, then times every chunk-jump plan and
  * every output-kernel plan on `stream` (one untimed launch, then `reps`
- * launches between two CUDA events, 1 <= reps <= 1000), picks the fastest
- * of each (the two kernels are independent), runs the forward pass once
- * more with that combination, and waits for the stream.  On return y and
- * final_state hold that last pass's results and *chosen (required) the
- * plan, which the caller passes to later calls (ssd_forward_ex); nothing is
- * installed or remembered.  Blocks the host and creates and destroys CUDA
- * events: not for use inside a stream capture. */
+ * timed launches, 1 <= reps <= 1000), picks the fastest of each (the two
+ * kernels are independent), runs the forward pass once more with that
+ * combination, and waits for the stream.  With flush NULL the `reps`
+ * launches run back to back between two CUDA events (a warm L2); with a
+ * device buffer `flush` of flush_bytes > 0 bytes -- larger than the L2 (for
+ * example 256 MB) -- each launch is timed alone after the buffer has been
+ * overwritten, so every candidate is timed from a cold L2, as a forward pass
+ * over fresh inputs runs.  On return y and final_state hold that last pass's
+ * results and *chosen (required) the plan, which the caller passes to later
+ * calls (ssd_forward_ex); nothing is installed or remembered.  Blocks the
+ * host and creates and destroys CUDA events: not for use inside a stream
+ * capture. */
 SSD_API ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x,
-                                    const void *dt, const float *A, const void *B,
-                                    const void *C, const float *D, const float *h0, void *y,
-                                    float *final_state, void *workspace, size_t ws_bytes,
-                                    int reps, void *stream, ssd_plan *chosen);
+                                   const void *dt, const float *A, const void *B,
+                                   const void *C, const float *D, const float *h0, void *y,
+                                   float *final_state, void *workspace, size_t ws_bytes,
+                                   int reps, void *flush, size_t flush_bytes, void *stream,
+                                   ssd_plan *chosen);
 
 #ifdef __cplusplus
 }

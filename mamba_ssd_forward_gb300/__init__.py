@@ -279,10 +279,14 @@ def default_plan(d: _abi.SsdDims, io: int = 1) -> dict:
     return p.as_dict()
 
 
-def tune(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, reps: int = 5, workspace=None):
+def tune(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, reps: int = 5, workspace=None,
+         flush=None):
     """Time every launch plan on these inputs (ssd_forward_tune).  Returns
     (plan dict, y, final_state) of the final pass with the fastest plan; pass
-    the plan to later calls (forward(..., plan=...)): nothing is installed."""
+    the plan to later calls (forward(..., plan=...)): nothing is installed.
+    `flush`, a device tensor larger than the L2 (e.g. 256 MB), makes every
+    candidate launch run from a cold L2 (the buffer is overwritten before
+    each, outside the timing); without it the launches run back to back."""
     lib = _abi.load()
     d = dims_of(x, B, chunk)
     io = _io_code(x)
@@ -295,7 +299,8 @@ def tune(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, reps: int = 5, works
     _abi.check("ssd_forward_tune", lib.ssd_forward_tune(
         ctypes.byref(d), io, _ptr(x), _ptr(dt), _ptr(_f32(A, "A")), _ptr(B), _ptr(C),
         _ptr(_f32(D, "D")), _ptr(_f32(h0, "h0")), _ptr(y), _ptr(final_state),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), int(reps), _stream(),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), int(reps),
+        _ptr(flush), 0 if flush is None else flush.numel() * flush.element_size(), _stream(),
         ctypes.byref(p)))
     return p.as_dict(), y, final_state
 

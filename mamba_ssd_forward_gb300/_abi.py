@@ -124,7 +124,7 @@ def load(path: str | None = None):
     lib.ssd_selftest_bounded_wait.restype = i32
     lib.ssd_selftest_bounded_wait.argtypes = [ctypes.c_uint64, vp, vp]
     lib.ssd_forward_tune.restype = i32
-    lib.ssd_forward_tune.argtypes = [dims_p, i32] + [vp] * 10 + [sz, i32, vp, plan_p]
+    lib.ssd_forward_tune.argtypes = [dims_p, i32] + [vp] * 10 + [sz, i32, vp, sz, vp, plan_p]
     if path is None:
         _lib = lib
     return lib

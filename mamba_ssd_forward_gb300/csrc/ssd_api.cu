@@ -159,17 +159,40 @@ ssd_status resolve_plan(const Dims &d, ssd_dtype t, const ssd_plan *plan, ssd::F
 }
 
 // Mean milliseconds per launch of `launch` over reps launches (after one
-// untimed launch), timed with two events on st.
-template <typename F>
+// untimed launch), timed with events on st: back to back between two events
+// (flush null), or each launch alone after overwriting the flush buffer and
+// running `prologue`.
+template <typename F, typename Pre>
 cudaError_t time_launches(F launch, int reps, cudaStream_t st, cudaEvent_t e0, cudaEvent_t e1,
-                          float *ms) {
+                          void *flush, size_t flush_bytes, Pre prologue, float *ms) {
   cudaError_t e = launch();
-  if (e == cudaSuccess) e = cudaEventRecord(e0, st);
-  for (int i = 0; i < reps && e == cudaSuccess; ++i) e = launch();
-  if (e == cudaSuccess) e = cudaEventRecord(e1, st);
-  if (e == cudaSuccess) e = cudaEventSynchronize(e1);
-  if (e == cudaSuccess) e = cudaEventElapsedTime(ms, e0, e1);
-  if (e == cudaSuccess) *ms /= (float)reps;
+  if (!flush) {
+    // back to back: one pair of events around all repetitions
+    if (e == cudaSuccess) e = cudaEventRecord(e0, st);
+    for (int i = 0; i < reps && e == cudaSuccess; ++i) e = launch();
+    if (e == cudaSuccess) e = cudaEventRecord(e1, st);
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(ms, e0, e1);
+    if (e == cudaSuccess) *ms /= (float)reps;
+    return e;
+  }
+  // each repetition after writing the flush buffer and running the
+  // prologue (the kernels that precede this one in a forward pass), both
+  // outside the events, so every launch sees the cache state it would see
+  // in a forward pass over fresh inputs
+  float total = 0.f;
+  for (int i = 0; i < reps && e == cudaSuccess; ++i) {
+    e = cudaMemsetAsync(flush, i & 0xff, flush_bytes, st);
+    if (e == cudaSuccess) e = prologue();
+    if (e == cudaSuccess) e = cudaEventRecord(e0, st);
+    if (e == cudaSuccess) e = launch();
+    if (e == cudaSuccess) e = cudaEventRecord(e1, st);
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    float one = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&one, e0, e1);
+    total += one;
+  }
+  if (e == cudaSuccess) *ms = total / (float)reps;
   return e;
 }
 
@@ -468,12 +491,13 @@ ssd_status ssd_forward_default_plan(const ssd_dims *dims, ssd_dtype dtype, ssd_p
 ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
                             const float *A, const void *B, const void *C, const float *D,
                             const float *h0, void *y, float *final_state, void *workspace,
-                            size_t ws_bytes, int reps, void *stream, ssd_plan *chosen) {
+                            size_t ws_bytes, int reps, void *flush, size_t flush_bytes,
+                            void *stream, ssd_plan *chosen) {
   Dims d;
   ssd_status s = ssd::check_forward_args(dims, dtype, x, dt, A, B, C, D, h0, y, final_state, &d);
   if (s != SSD_OK) return s;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || reps < 1 ||
-      reps > 1000 || !chosen)
+      reps > 1000 || !chosen || (flush && flush_bytes == 0))
     return SSD_ERR_INVALID_ARG;
   if (dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
   const WsLayout w = ws_layout(d, dtype);
@@ -502,7 +526,7 @@ ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x
           return ssd::launch_fwd_chunk_state(d, x, B, dt, A, bw.dH, bw.gamma, bw.u, bw.v,
                                              bw.anchor, cs[i], err, st);
         },
-        reps, st, e0, e1, &ms);
+        reps, st, e0, e1, flush, flush_bytes, [] { return cudaSuccess; }, &ms);
     if (e == cudaSuccess && ms < best_ms) {
       best_ms = ms;
       best.cs = cs[i];
@@ -511,8 +535,20 @@ ssd_status ssd_forward_tune(const ssd_dims *dims, ssd_dtype dtype, const void *x
   best_ms = 3.0e38f;
   for (size_t i = 0; i < sc.size() && e == cudaSuccess; ++i) {
     float ms = 0.f;
-    e = time_launches([&] { return launch_scan(d, sc[i], x, B, C, dt, A, bw, D, y, err, st); },
-                      reps, st, e0, e1, &ms);
+    // with a flush buffer each output launch follows the chunk-jump kernel
+    // (the plan chosen above) and the state pass, as in a forward pass
+    e = time_launches(
+        [&] { return launch_scan(d, sc[i], x, B, C, dt, A, bw, D, y, err, st); }, reps, st, e0,
+        e1, flush, flush_bytes,
+        [&] {
+          cudaError_t e2 = ssd::launch_fwd_chunk_state(d, x, B, dt, A, bw.dH, bw.gamma, bw.u,
+                                                       bw.v, bw.anchor, best.cs, err, st);
+          if (e2 == cudaSuccess)
+            e2 = ssd::launch_fwd_state_pass(d, bw.dH, bw.gamma, h0, bw.states, final_state, err,
+                                            st);
+          return e2;
+        },
+        &ms);
     if (e == cudaSuccess && ms < best_ms) {
       best_ms = ms;
       best.scan_kernel = sc[i].scan_kernel;

@@ -302,10 +302,14 @@ def test_plan_rejections(lib):
     assert lib.ssd_forward_ex(ctypes.byref(d), 0, *args[:-1], ws32, good, None) == 1
     # events promised but missing
     assert lib.ssd_forward_profiled(ctypes.byref(d), 1, *args, None, None, None, 2, None) == 1
-    rc = lib.ssd_forward_tune(ctypes.byref(d), 1, *([None] * 10), 0, 5, None, None)
+    rc = lib.ssd_forward_tune(ctypes.byref(d), 1, *([None] * 10), 0, 5, None, 0, None, None)
     assert rc == _abi.SSD_ERR_INVALID_ARG
     # a tuner call with valid arguments but nowhere to put the chosen plan
-    rc = lib.ssd_forward_tune(ctypes.byref(d), 1, *args, 5, None, None)
+    rc = lib.ssd_forward_tune(ctypes.byref(d), 1, *args, 5, None, 0, None, None)
+    assert rc == _abi.SSD_ERR_INVALID_ARG
+    # a flush buffer of zero bytes
+    plan = ctypes.byref(_abi.SsdPlan())
+    rc = lib.ssd_forward_tune(ctypes.byref(d), 1, *args, 5, ctypes.c_void_p(4096), 0, None, plan)
     assert rc == _abi.SSD_ERR_INVALID_ARG
 
 

@@ -70,6 +70,19 @@ def test_tune_returns_a_candidate_and_installs_nothing(ssd, case):
     assert torch.equal(y3, y_def)  # and calls without a plan still run the default
 
 
+def test_tune_from_a_cold_l2(ssd, case):
+    """With a flush buffer every candidate is timed after the buffer is
+    overwritten; the tuner still returns a candidate whose pass matches the
+    oracle."""
+    inp, ref, dev, d = case
+    flush = torch.empty(160 << 20, dtype=torch.uint8, device="cuda")
+    plan, y, fin = ssd.tune(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                            dev["h0"], chunk=CASE.chunk, reps=2, flush=flush)
+    assert plan in ssd.plan_candidates(d)
+    check_io(to64(y), ref["y"], "bf16", "cold-L2 tuned y")
+    check_io(to64(fin), ref["final_state"], "bf16", "cold-L2 tuned final_state")
+
+
 def test_tune_rejects_fp32(ssd):
     from mamba_ssd_forward_gb300 import _abi
     w = W.Workload("fp32_plans", 1, 256, 2, 64, 64, 1, 128, "fp32", False)
