@@ -17,14 +17,20 @@ CUDA Tile", section "Mamba-2 architecture":
   to cross-check the recurrence and to pin the chunking semantics.
 * ``decode_step`` -- one token of the recurrence for a batch of states, in
   numpy: the reference for the single-token decode step.
+* ``backward`` -- the gradients of a loss through the recurrence (the
+  adjoint recurrence token by token, numpy float64): the reference a
+  backward pass will be checked against; no CUDA path computes it yet.
 
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests
 (hand-worked example, brute-force unrolled sum, linear-attention, B = 0 and
 dt = 0 special cases, chunk invariance, padding, resume, linearity in h0;
 for decode_step: the hand-worked example token by token, agreement with the
-C recurrence over whole sequences, dt = 0, and planted mistakes).
+C recurrence over whole sequences, dt = 0, and planted mistakes; for
+backward: central finite differences of the C recurrence, closed forms of
+special cases, and planted mistakes).
 """
 from .ssd_oracle import (  # noqa: F401
+    backward,
     build,
     chunked,
     decode_step,

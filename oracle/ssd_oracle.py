@@ -213,3 +213,54 @@ def chunked(x, dt, A, B, C, D=None, h0=None, chunk=256):
             final[bi, h] = H
     return {"y": y, "final_state": final, "states": states, "dstates": dstates,
             "G": Gall, "max_kept_exponent": kept}
+
+
+def backward(x, dt, A, B, C, D=None, h0=None, gy=None, gfinal=None):
+    """Gradients of a loss L(y, final_state) through the forward recurrence,
+    given gy = dL/dy [b, L, nh, P] and gfinal = dL/dfinal_state [b, nh, P, S]
+    (None = 0), in float64 by the adjoint recurrence token by token (tiny
+    inputs only).
+
+    Forward ("Mamba-2 architecture"): a_t = exp(A dt_t), b_t = dt_t B_t,
+    h_t = a_t h_{t-1} + x_t b_t^T (P x S), y_t = h_t c_t + D x_t.  With
+    g_t = dL/dh_t (P x S), going backwards from g = gfinal:
+        g_t    = gy_t c_t^T + a_{t+1} g_{t+1}
+        dx_t   = g_t b_t + D gy_t
+        db_t   = g_t^T x_t            -> dB_t = dt_t db_t,   dt_t += <db_t, B_t>
+        dc_t   = h_t^T gy_t
+        da_t   = <g_t, h_{t-1}>       -> dt_t += A a_t da_t, dA += dt_t a_t da_t
+        dD    += <gy_t, x_t>,  dh0 = a_1 g_1 (the g carried past t = 1).
+    The gradients of B and C sum over the heads of a group.  Returns a dict
+    of dx, ddt, dA, dB, dC, dD, dh0 (float64)."""
+    x, dt, A, B, C, D, h0, gy, gfinal = map(_f64, (x, dt, A, B, C, D, h0, gy, gfinal))
+    b, L, nh, P, S, ng = _dims(x, dt, A, B)
+    hpg = nh // ng
+    out = {"dx": np.zeros_like(x), "ddt": np.zeros_like(dt), "dA": np.zeros_like(A),
+           "dB": np.zeros_like(B), "dC": np.zeros_like(C), "dD": np.zeros(nh),
+           "dh0": np.zeros((b, nh, P, S))}
+    for bi in range(b):
+        for h in range(nh):
+            g = h // hpg
+            # forward, keeping every state: hs[t + 1] = h_t, hs[0] = h0
+            hs = np.zeros((L + 1, P, S))
+            if h0 is not None:
+                hs[0] = h0[bi, h]
+            a = np.exp(A[h] * dt[bi, :, h])
+            for t in range(L):
+                hs[t + 1] = a[t] * hs[t] + np.outer(x[bi, t, h], dt[bi, t, h] * B[bi, t, g])
+            Dh = 0.0 if D is None else D[h]
+            G = np.zeros((P, S)) if gfinal is None else gfinal[bi, h].copy()
+            for t in range(L - 1, -1, -1):
+                G = G + np.outer(gy[bi, t, h], C[bi, t, g])    # dL/dh_t, complete
+                bt = dt[bi, t, h] * B[bi, t, g]
+                out["dx"][bi, t, h] = G @ bt + Dh * gy[bi, t, h]
+                db = G.T @ x[bi, t, h]
+                out["dB"][bi, t, g] += dt[bi, t, h] * db
+                out["dC"][bi, t, g] += hs[t + 1].T @ gy[bi, t, h]
+                da = float(np.sum(G * hs[t]))
+                out["ddt"][bi, t, h] = A[h] * a[t] * da + float(db @ B[bi, t, g])
+                out["dA"][h] += dt[bi, t, h] * a[t] * da
+                out["dD"][h] += float(gy[bi, t, h] @ x[bi, t, h])
+                G = a[t] * G                                      # dL/dh_{t-1} from h_t
+            out["dh0"][bi, h] = G
+    return out
