@@ -40,15 +40,16 @@ METRIC = "SSD forward tokens/s at 1 GB300; achieved TFLOP/s + HBM GB/s vs roofli
 # S 256, 8 groups), where the method's gain over other implementations is
 # said to grow with sequence length and state size.
 DEFAULT_WORKLOAD = W.LONG_32K
-# Launch sequence of ssd_forward: bf16 I/O runs the fused state pass and the
-# output pass; fp32 I/O runs the four step kernels.
+# Launch sequence of ssd_forward: bf16 I/O runs the chunk-jump kernel, the
+# state pass and the output pass; fp32 I/O runs the cumsum, chunk-state and
+# state-passing steps and an output pass (fwd_out_tf32 where it applies).
 KERNEL_NAMES = {"bf16": ["fwd_chunk_state", "fwd_state_pass", "fwd_scan"],
                 "fp32": ["chunk_cumsum", "chunk_state", "state_passing", "chunk_scan"]}
 KERNEL_SOURCES = {"chunk_cumsum": "chunk_cumsum.cu", "chunk_state": "chunk_state.cu",
                   "state_passing": "state_passing.cu", "chunk_scan": "chunk_scan.cu",
                   "fwd_chunk_state": "fwd_chunk_state.cu", "fwd_state_pass": "fwd_state_pass.cu",
                   "fwd_scan": "fwd_scan.cu", "fwd_scan_chunk": "fwd_scan_chunk.cu",
-                  "fwd_out": "fwd_out.cu"}
+                  "fwd_out": "fwd_out.cu", "fwd_out_tf32": "fwd_out_tf32.cu"}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -96,6 +97,9 @@ def kernel_names(w: W.Workload, plan: dict | None = None) -> list:
     fwd_out (scan_kernel 3), fwd_scan_chunk (1, or 2: one row tile per CTA)
     or fwd_scan (0)."""
     names = list(KERNEL_NAMES[w.dtype])
+    if w.dtype == "fp32" and w.headdim == 64 and w.dstate % 32 == 0 and w.dstate <= 128 \
+            and w.chunk in (128, 256):
+        names[3] = "fwd_out_tf32"  # the warp-specialised fp32 output kernel
     if w.dtype == "bf16" and plan is not None:
         names[2] = {0: "fwd_scan", 1: "fwd_scan_chunk", 2: "fwd_scan_chunk",
                     3: "fwd_out"}[plan["scan_kernel"]]
@@ -119,7 +123,7 @@ def kernel_method_bytes(w: W.Workload) -> dict:
            "chunk_state": x + bc + dt,
            "state_passing": h0 + fin,
            "chunk_scan": 2 * x + 2 * bc + dt + 2 * w.nheads * 4}
-    for k in ("fwd_scan", "fwd_scan_chunk", "fwd_out"):
+    for k in ("fwd_scan", "fwd_scan_chunk", "fwd_out", "fwd_out_tf32"):
         out[k] = out["chunk_scan"]
     return out
 
@@ -153,6 +157,7 @@ def kernel_bytes(w: W.Workload) -> dict:
         "chunk_state": x + bc + dt + G + st,
         "state_passing": 2 * st + w.batch * w.nheads * w.nchunks * 4 + fin * (2 if w.has_h0 else 1),
         "chunk_scan": 2 * x + 2 * bc + dt + G + st + w.nheads * 4,
+        "fwd_out_tf32": 2 * x + 2 * bc + dt + G + st + 2 * w.nheads * 4,
     }
 
 

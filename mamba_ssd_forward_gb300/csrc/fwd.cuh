@@ -72,6 +72,19 @@ cudaError_t launch_fwd_out(const Dims &d, const void *x, const void *B, const vo
                            const float *u, const float *v, const float2 *anchor, void *y,
                            int hs, int *err, cudaStream_t st);
 
+// fwd_out_tf32: the output pass for fp32 I/O (kind::tf32), one 128-row tile
+// of a chunk and a slice of hs heads per CTA, the masked C B^T of the tile
+// shared by the slice's heads with the decay factored about one anchor per
+// chunk and head (P = 64, S a multiple of 32 up to 128, T in {128, 256}).
+// It reads G (fp32, log2 units, [b, nh, nc * T]) and the fp32 start states
+// [b, nh, nc, P, S] rounded to tf32 (state_passing with round_tf32).
+bool fwd_out_tf32_supported(const Dims &d);
+bool fwd_out_tf32_heads_ok(const Dims &d, int hs);
+int fwd_out_tf32_heads(const Dims &d);  // the cost-model choice
+cudaError_t launch_fwd_out_tf32(const Dims &d, const float *x, const float *B, const float *C,
+                                const float *dt, const float *G, const float *states,
+                                const float *D, float *y, int hs, int *err, cudaStream_t st);
+
 // Heads per CTA of fwd_scan: the largest divisor of nheads/ngroups that is
 // at most 4 and keeps heads * P <= 256 tensor-memory columns.
 inline int fwd_scan_heads(const Dims &d) {

@@ -1,0 +1,626 @@
+// Forward path, output pass with fp32 I/O (kind::tf32 MMAs, fp32
+// accumulation): the chunked output equation of "Accelerating Mamba-2 with
+// High-Performance Forward Pass Kernels in NVIDIA CUDA Tile", section
+// "Mamba-2 architecture" (the compute_out step),
+//
+//   y_i = exp2(G_i) (h_k c_i) + sum_{j<=i in chunk} (c_i . B_j) exp2(G_i - G_j) dt_j x_j
+//         + D x_i,
+//
+// G the in-chunk cumsum of A dt in log2 units, h_k the chunk's start state.
+// As in the bf16 output pass (fwd_out.cu) the decay of the in-chunk sum is
+// factored about an anchor alpha = rint(G_last / 2):
+// exp2(G_i - G_j) = u_i v'_j with u_i = exp2(G_i - alpha), v'_j =
+// exp2(alpha - G_j), so the masked C B^T of the chunk carries no decay and is
+// shared unchanged by every head of the group; per head the x rows are only
+// scaled by v_j = v'_j dt_j.  Unlike fwd_out, the inter-chunk term keeps an
+// accumulator of its own, y_i = exp2(G_i) Acc_s,i + u_i Acc_i,i + D x_i, so
+// the start states need no scaling.  A chunk whose decay is too steep for
+// bounded factors (total decay above 2^-180, or a real token's factor below
+// 2^-120) takes an exact per-element path for the in-chunk sum on the CUDA
+// cores instead (rare, slow, exact).
+//
+// kind::tf32 takes K-major operands only, and every operand is rounded to
+// tf32 (nearest) before the tensor core sees it: C and B in shared memory by
+// the row warps as they land, the start states by the state pass that
+// stores them, x while it is transposed, C B^T in tensor memory.
+//
+// One CTA per (128-row tile t of a chunk, slice of hs heads of one group,
+// chunk, batch), 1 CTA per SM:
+//   producer warp: C of the tile (resident, K-major atoms of 32 s), then
+//     through a ring of 16 KB stages: B of tokens 0 .. 128 (t + 1) - 1 per
+//     atom of S, then per head its start state (two atoms of S per stage)
+//     and its x (two 32-token atoms per stage, as landed: p contiguous);
+//   MMA warp: C B^T of the tile into tensor memory (fp32, columns = tokens);
+//     per head into one of two accumulator sets Acc_s = C h^T (K = S) and
+//     Acc_i = (C B^T masked) Xh (K = tokens, A read from tensor memory, Xh
+//     from the row warps' transposed atoms);
+//   row warps (8): round C and the B stages; mask (j > i -> 0) and round
+//     C B^T in place; per head its factors, the transposition of each x
+//     atom into K-major Xh^T (tokens along the 128-byte rows, scaled by v_j,
+//     rounded), and the previous head's epilogue
+//     y = exp2(G_i) Acc_s + u_i Acc_i + D x_i.
+// Supported: P = 64, S a multiple of 32 up to 128, T in {128, 256}.
+#include "fwd.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kRowWarps = 8;
+constexpr int kRowThreads = kRowWarps * 32;
+constexpr int kThreads = kRowThreads + 64;
+constexpr int kProducerWarp = kRowWarps, kMmaWarp = kRowWarps + 1;
+constexpr int kP = 64;
+constexpr int kAtom = 128 * 128;  // C / B: 128 rows x 32 fp32 (one K atom of S)
+constexpr int kStage = 16384;     // one ring stage
+constexpr int kHAtom = 64 * 128;  // start state: 64 rows p x 32 fp32 of S
+constexpr int kXAtom = 64 * 128;  // x as landed: 32 tokens x 64 p (two 4 KB boxes);
+                                  // Xh^T: 64 rows p x 32 tokens
+constexpr int kMaxSlots = 10;
+constexpr int kXh = 4;            // Xh^T atoms in flight
+constexpr float kSpanMax = 180.f;
+constexpr float kMinFactor = 7.52316384526264e-37f;  // 2^-120
+
+// Tensor-memory columns: C B^T of the tile at [0, 128 (t + 1)); accumulator
+// set s: Acc_s at 256 + 128 s, Acc_i at 256 + 128 s + 64.
+__device__ __forceinline__ uint32_t acc_s(int set) { return 256u + 128u * (uint32_t)set; }
+__device__ __forceinline__ uint32_t acc_i(int set) { return 320u + 128u * (uint32_t)set; }
+
+struct OutArgs32 {
+  const float *x, *dt, *D;
+  const float *G;  // in-chunk cumsums, log2 units, [b, nh, nc * T]
+  float *y;
+  int *err;
+  int L, nh, S, hpg, T, nc, hs, nslot, nb;
+};
+
+__device__ __forceinline__ float tf32_rn(float v) { return __uint_as_float(to_tf32(v)); }
+
+template <int kT>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
+             const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_st,
+             const OutArgs32 a) {
+  constexpr int nT = kT / 128;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // full: a state stage landed (MMA waits); xfull: a B or x stage landed (row
+  // warps wait); scaled: the row warps rounded a B stage; empty: a stage's
+  // readers are done; xh_ready / xh_free: an Xh^T atom written / read
+  __shared__ __align__(8) uint64_t c_full, c_ready, full[kMaxSlots], xfull[kMaxSlots],
+      scaled[kMaxSlots], empty[kMaxSlots], sc_done, pack_done, acc_full[2], acc_free[2],
+      xh_ready[kXh], xh_free[kXh];
+  __shared__ uint32_t tmem_slot;
+  // per head (by head parity): G and dt of every token, v_j, alpha, path
+  __shared__ __align__(16) float Gs[2][256];
+  __shared__ __align__(16) float dts[2][256];
+  __shared__ __align__(16) float vs[2][256];
+  __shared__ float alphas[2];
+  __shared__ int steeps[2];
+  __shared__ int warp_ok[kRowWarps];
+
+  const int L = a.L, nh = a.nh, S = a.S, hs = a.hs, nslot = a.nslot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int t = blockIdx.x % nT;             // row tile of the chunk
+  const int hbase = (blockIdx.x / nT) * hs;  // first head of the slice
+  const int k = blockIdx.y, b = blockIdx.z;
+  const int g = hbase / a.hpg;
+  const int tok0 = k * kT;
+  const int valid = min(kT, L - tok0);
+  if (t * 128 >= valid) return;  // the whole tile lies past the sequence (uniform)
+  const int nS = S / 32;             // K atoms of S
+  const int nHs = (nS + 1) / 2;      // state stages per head
+  const int nJ = 4 * (t + 1);        // 32-token atoms of the in-chunk sum
+  const int nXs = nJ / 2;            // x stages per head
+  uint8_t *Cs = smem;                // atom sb at sb * kAtom
+  uint8_t *ring = smem + nS * kAtom;
+  uint8_t *xh = ring + nslot * kStage;
+  auto slot_ptr = [&](int u) { return ring + (u % nslot) * kStage; };
+
+  if (tid == 0) {
+    ptx::mbar_init(&c_full, 1);
+    ptx::mbar_init(&c_ready, kRowWarps);
+    for (int i = 0; i < nslot; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&xfull[i], 1);
+      ptx::mbar_init(&scaled[i], kRowWarps);
+      ptx::mbar_init(&empty[i], 1);
+    }
+    ptx::mbar_init(&sc_done, 1);
+    ptx::mbar_init(&pack_done, kRowWarps);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&acc_full[i], 1);
+      ptx::mbar_init(&acc_free[i], kRowWarps);
+    }
+    for (int i = 0; i < kXh; ++i) {
+      ptx::mbar_init(&xh_ready[i], kRowWarps);
+      ptx::mbar_init(&xh_free[i], 1);
+    }
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(&tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const bool leader = (tid & 31) == 0;
+  const int n_pa = nS * (t + 1);  // phase-A (B) stages
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (leader) {
+      ptx::prefetch_tmap(&tm_C);
+      ptx::prefetch_tmap(&tm_B);
+      ptx::prefetch_tmap(&tm_x);
+      ptx::prefetch_tmap(&tm_st);
+      ptx::mbar_arrive_expect_tx(&c_full, nS * kAtom);
+      for (int sb = 0; sb < nS; ++sb)
+        ptx::tma_load_4d(Cs + sb * kAtom, &tm_C, sb * 32, g, tok0 + t * 128, b, &c_full);
+    }
+    __syncwarp();
+    int u = 0;
+    auto acquire = [&](int code) {
+      ptx::mbar_wait(&empty[u % nslot], ((u / nslot) & 1) ^ 1, a.err, code);
+    };
+    for (int sb = 0; sb < nS; ++sb)
+      for (int th = 0; th <= t; ++th, ++u) {
+        acquire(160);
+        if (leader) {
+          ptx::mbar_arrive_expect_tx(&xfull[u % nslot], kStage);
+          ptx::tma_load_4d(slot_ptr(u), &tm_B, sb * 32, g, tok0 + th * 128, b, &xfull[u % nslot]);
+        }
+        __syncwarp();
+      }
+    for (int q = 0; q < hs; ++q) {
+      const int h = hbase + q;
+      const int row = (b * nh + h) * a.nc + k;  // this head's start state
+      for (int hh = 0; hh < nHs; ++hh, ++u) {
+        acquire(161);
+        if (leader) {
+          // the start states come from the preceding kernel (the state
+          // pass), which may still be running when this CTA starts
+          if (q == 0 && hh == 0) ptx::griddep_wait();
+          const int na = min(2, nS - 2 * hh);
+          ptx::mbar_arrive_expect_tx(&full[u % nslot], na * kHAtom);
+          for (int ai = 0; ai < na; ++ai)
+            ptx::tma_load_3d(slot_ptr(u) + ai * kHAtom, &tm_st, (2 * hh + ai) * 32, 0, row,
+                             &full[u % nslot]);
+        }
+        __syncwarp();
+      }
+      for (int xs = 0; xs < nXs; ++xs, ++u) {
+        acquire(162);
+        if (leader) {
+          ptx::mbar_arrive_expect_tx(&xfull[u % nslot], kStage);
+          for (int ai = 0; ai < 2; ++ai)
+            for (int ph = 0; ph < 2; ++ph)
+              ptx::tma_load_4d(slot_ptr(u) + ai * kXAtom + ph * 4096, &tm_x, ph * 32, h,
+                               tok0 + (2 * xs + ai) * 32, b, &xfull[u % nslot]);
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t fpar = 0, spar = 0;  // parity of the next wait, one bit per slot
+    ptx::mbar_wait(&c_ready, 0, a.err, 163);
+    ptx::tc_fence_after();
+    int u = 0;
+    const uint32_t idCB = ptx::idesc_tf32(128, 128, false, false);
+    for (int sb = 0; sb < nS; ++sb)
+      for (int th = 0; th <= t; ++th, ++u) {
+        const int sl = u % nslot;
+        ptx::mbar_wait(&scaled[sl], (spar >> sl) & 1, a.err, 164);
+        spar ^= 1u << sl;
+        ptx::tc_fence_after();
+        if (leader) {
+          const uint32_t c0 = ptx::smem_u32(Cs + sb * kAtom), b0 = ptx::smem_u32(slot_ptr(u));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t cd = ptx::smem_desc(c0 + kk * 32, 16, 1024, ptx::kSw128);
+            const uint64_t bd = ptx::smem_desc(b0 + kk * 32, 16, 1024, ptx::kSw128);
+            ptx::mma_ss<true>(tmem + 128 * th, cd, bd, idCB, (sb | kk) ? 1u : 0u);
+          }
+          ptx::mma_commit(&empty[sl]);
+        }
+        __syncwarp();
+      }
+    if (leader) ptx::mma_commit(&sc_done);
+    __syncwarp();
+    const uint32_t idY = ptx::idesc_tf32(128, kP, false, false);
+    ptx::mbar_wait(&pack_done, 0, a.err, 165);
+    int xv = 0;  // Xh^T atoms consumed so far
+    for (int q = 0; q < hs; ++q) {
+      const int set = q & 1;
+      if (q >= 2) ptx::mbar_wait(&acc_free[set], ((q >> 1) - 1) & 1, a.err, 166);
+      ptx::tc_fence_after();
+      // Acc_s = C h^T over the state stages
+      for (int hh = 0; hh < nHs; ++hh, ++u) {
+        const int sl = u % nslot;
+        ptx::mbar_wait(&full[sl], (fpar >> sl) & 1, a.err, 167);
+        fpar ^= 1u << sl;
+        ptx::tc_fence_after();
+        if (leader) {
+          const uint32_t h0 = ptx::smem_u32(slot_ptr(u));
+          const int na = min(2, nS - 2 * hh);
+          for (int ai = 0; ai < na; ++ai) {
+            const uint32_t c0 = ptx::smem_u32(Cs + (2 * hh + ai) * kAtom);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t cd = ptx::smem_desc(c0 + kk * 32, 16, 1024, ptx::kSw128);
+              const uint64_t hd =
+                  ptx::smem_desc(h0 + ai * kHAtom + kk * 32, 16, 1024, ptx::kSw128);
+              ptx::mma_ss<true>(tmem + acc_s(set), cd, hd, idY, (hh | ai | kk) ? 1u : 0u);
+            }
+          }
+          ptx::mma_commit(&empty[sl]);
+        }
+        __syncwarp();
+      }
+      u += nXs;  // the x stages go to the row warps
+      // Acc_i = (C B^T masked) Xh over the Xh^T atoms (none for a steep head,
+      // whose epilogue forms the in-chunk sum itself)
+      for (int ja = 0; ja < nJ; ++ja, ++xv) {
+        const int xs = xv % kXh;
+        ptx::mbar_wait(&xh_ready[xs], (xv / kXh) & 1, a.err, 168);
+        ptx::tc_fence_after();
+        const bool steep = steeps[q & 1] != 0;
+        if (leader) {
+          if (!steep) {
+            const uint32_t x0 = ptx::smem_u32(xh + xs * kXAtom);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t xd = ptx::smem_desc(x0 + kk * 32, 16, 1024, ptx::kSw128);
+              ptx::mma_ts_tf32(tmem + acc_i(set), tmem + ja * 32 + kk * 8, xd, idY,
+                               (ja | kk) ? 1u : 0u);
+            }
+          }
+          ptx::mma_commit(&xh_free[xs]);
+        }
+        __syncwarp();
+      }
+      if (leader) ptx::mma_commit(&acc_full[set]);
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ row warps
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, column half
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const int lrow = quad * 32 + (tid & 31);  // row of the tile = TMEM lane
+    const int i_rel = t * 128 + lrow;          // chunk-relative row
+    auto warp_arrive = [&](uint64_t *bar) {
+      __syncwarp();
+      if ((tid & 31) == 0) ptx::mbar_arrive(bar);
+    };
+    // round 16 KB of fp32 operand data in place (any layout)
+    auto round_block = [&](uint8_t *p, int bytes) {
+      for (int o = tid * 16; o < bytes; o += kRowThreads * 16) {
+        float4 v = *reinterpret_cast<const float4 *>(p + o);
+        v.x = tf32_rn(v.x);
+        v.y = tf32_rn(v.y);
+        v.z = tf32_rn(v.z);
+        v.w = tf32_rn(v.w);
+        *reinterpret_cast<float4 *>(p + o) = v;
+      }
+    };
+
+    // C of the tile, then the B stages, rounded as they land
+    ptx::mbar_wait(&c_full, 0, a.err, 169);
+    round_block(Cs, nS * kAtom);
+    ptx::fence_async_smem();
+    warp_arrive(&c_ready);
+    uint32_t xpar = 0;  // parity of the next wait on xfull[slot], one bit per slot
+    int u = 0;
+    for (; u < n_pa; ++u) {
+      const int sl = u % nslot;
+      ptx::mbar_wait(&xfull[sl], (xpar >> sl) & 1, a.err, 170);
+      xpar ^= 1u << sl;
+      round_block(slot_ptr(u), kStage);
+      ptx::fence_async_smem();
+      warp_arrive(&scaled[sl]);
+    }
+
+    // C B^T of the tile: j > i masked to zero, the rest rounded to tf32 in
+    // place (warp: its lane quadrant, half the tile's columns)
+    ptx::mbar_wait(&sc_done, 0, a.err, 171);
+    ptx::tc_fence_after();
+    {
+      const int ncol = 128 * (t + 1), c_lo = half * (ncol / 2), c_hi = c_lo + ncol / 2;
+      for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+        uint32_t r[16];
+        ptx::tmem_ld16(tmem + lane_base + c0, r);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence(r);
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          r[e] = (c0 + e <= i_rel) ? to_tf32(__uint_as_float(r[e])) : 0u;
+        ptx::tmem_stu<16>(tmem + lane_base + c0, r);
+      }
+      ptx::tmem_st_wait();
+    }
+    ptx::tc_fence_before();
+    warp_arrive(&pack_done);
+
+    // G and dt come from earlier kernels: wait until the preceding grids are
+    // complete
+    ptx::griddep_wait();
+    // a head's inputs for thread = token j (< T), fetched one head ahead
+    struct HeadIn {
+      float Gj, dtj, Glast, D;
+    };
+    auto fetch_head = [&](int q) {
+      HeadIn r{0.f, 0.f, 0.f, 0.f};
+      const int h = hbase + q;
+      const int64_t bhk = ((int64_t)b * nh + h) * a.nc + k;
+      if (SSD_IN_BOUNDS(h < nh && bhk < (int64_t)a.nb * nh * a.nc, a.err, 160)) {
+        const float *Gc = a.G + bhk * kT;
+        if (tid < kT) r.Gj = Gc[tid];
+        r.Glast = Gc[kT - 1];
+        if (tid < valid) r.dtj = a.dt[((int64_t)b * L + tok0 + tid) * nh + h];
+        r.D = a.D ? a.D[h] : 0.f;
+      }
+      return r;
+    };
+    // factors and path of head q into the parity-(q & 1) arrays
+    auto prep_head = [&](int q, const HeadIn &in) {
+      const int pb = q & 1;
+      const float alpha = rintf(0.5f * in.Glast);
+      const float vj = in.dtj > 0.f ? exp2f(alpha - in.Gj) * in.dtj : 0.f;
+      const bool ok = in.dtj == 0.f || vj >= kMinFactor;
+      const int all_ok = __all_sync(0xffffffffu, ok);
+      if ((tid & 31) == 0) warp_ok[warp] = all_ok;
+      if (tid < kT) {
+        Gs[pb][tid] = in.Gj;
+        dts[pb][tid] = in.dtj;
+        vs[pb][tid] = vj;
+      }
+      ptx::named_bar_sync(1, kRowThreads);
+      if (tid == 0) {
+        int okall = 1;
+#pragma unroll
+        for (int w2 = 0; w2 < kRowWarps; ++w2) okall &= warp_ok[w2];
+        steeps[pb] = !(okall && -in.Glast <= kSpanMax);
+        alphas[pb] = alpha;
+      }
+      ptx::named_bar_sync(1, kRowThreads);
+    };
+
+    // the epilogue of head q: y = exp2(G_i) Acc_s + u_i Acc_i + D x_i for
+    // this thread's row and 32 columns
+    auto epilogue = [&](int q, float Dh) {
+      const int set = q & 1, pb = q & 1, h = hbase + q;
+      const bool row_ok = i_rel < valid;
+      const int64_t xrow = (((int64_t)b * L + tok0 + i_rel) * nh + h) * kP + 32 * half;
+      const bool io_ok = row_ok && SSD_IN_BOUNDS(xrow + 32 <= (int64_t)a.nb * L * nh * kP,
+                                                 a.err, 161);
+      float xi[32];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const float4 v = io_ok ? *reinterpret_cast<const float4 *>(a.x + xrow + 4 * m)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        xi[4 * m] = v.x;
+        xi[4 * m + 1] = v.y;
+        xi[4 * m + 2] = v.z;
+        xi[4 * m + 3] = v.w;
+      }
+      ptx::mbar_wait(&acc_full[set], (q >> 1) & 1, a.err, 172);
+      ptx::tc_fence_after();
+      const bool steep = steeps[pb] != 0;
+      uint32_t as[32], ai[32];
+      ptx::tmem_ld16(tmem + lane_base + acc_s(set) + 32 * half,
+                     *reinterpret_cast<uint32_t(*)[16]>(as));
+      ptx::tmem_ld16(tmem + lane_base + acc_s(set) + 32 * half + 16,
+                     *reinterpret_cast<uint32_t(*)[16]>(as + 16));
+      ptx::tmem_ld16(tmem + lane_base + acc_i(set) + 32 * half,
+                     *reinterpret_cast<uint32_t(*)[16]>(ai));
+      ptx::tmem_ld16(tmem + lane_base + acc_i(set) + 32 * half + 16,
+                     *reinterpret_cast<uint32_t(*)[16]>(ai + 16));
+      ptx::tmem_ld_wait();
+      ptx::reg_fence(as);
+      ptx::reg_fence(ai);
+      const float Gi = Gs[pb][min(i_rel, kT - 1)];
+      const float ei = exp2f(Gi);
+      float yv[32];
+      if (!steep) {
+        ptx::tc_fence_before();
+        warp_arrive(&acc_free[set]);  // the accumulators may take head q + 2
+        const float ui = exp2f(Gi - alphas[pb]);
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          yv[c] = fmaf(Dh, xi[c], fmaf(ei, __uint_as_float(as[c]), ui * __uint_as_float(ai[c])));
+      } else {
+        // exact per-element path: the in-chunk sum from the masked C B^T of
+        // this row's lane and the raw x rows (L2), every factor exact
+#pragma unroll
+        for (int c = 0; c < 32; ++c) yv[c] = fmaf(Dh, xi[c], ei * __uint_as_float(as[c]));
+        const int jmax_warp = t * 128 + quad * 32 + 31;  // the warp's last row
+        for (int j0 = 0; j0 <= jmax_warp; j0 += 16) {
+          uint32_t cb[16];
+          ptx::tmem_ld16(tmem + lane_base + j0, cb);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence(cb);
+          for (int e = 0; e < 16; ++e) {
+            const int j = j0 + e;
+            if (j >= valid) break;
+            const float s = j <= i_rel
+                                ? __uint_as_float(cb[e]) * exp2f(Gi - Gs[pb][j]) * dts[pb][j]
+                                : 0.f;
+            const int64_t xj = (((int64_t)b * L + tok0 + j) * nh + h) * kP + 32 * half;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              const float4 v = *reinterpret_cast<const float4 *>(a.x + xj + 4 * m);
+              yv[4 * m] = fmaf(s, v.x, yv[4 * m]);
+              yv[4 * m + 1] = fmaf(s, v.y, yv[4 * m + 1]);
+              yv[4 * m + 2] = fmaf(s, v.z, yv[4 * m + 2]);
+              yv[4 * m + 3] = fmaf(s, v.w, yv[4 * m + 3]);
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        warp_arrive(&acc_free[set]);
+      }
+      if (io_ok) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+          *reinterpret_cast<float4 *>(a.y + xrow + 4 * m) =
+              make_float4(yv[4 * m], yv[4 * m + 1], yv[4 * m + 2], yv[4 * m + 3]);
+      }
+    };
+
+    // Per head q: its factors, the transposition of its x atoms into Xh^T,
+    // then the previous head's epilogue (head q's MMAs overlap it).
+    const int jl = tid & 31, pc = tid >> 5;  // token of an atom, 8-column group of p
+    int xv = 0;                              // Xh^T atoms written so far
+    HeadIn in_next = fetch_head(0);
+    float D_prev = 0.f;
+    for (int q = 0; q < hs; ++q) {
+      const HeadIn in = in_next;
+      if (q + 1 < hs) in_next = fetch_head(q + 1);
+      prep_head(q, in);
+      const int pb = q & 1;
+      u += nHs;  // the state stages go straight to the MMA warp
+      for (int xs = 0; xs < nXs; ++xs, ++u) {
+        const int sl = u % nslot;
+        ptx::mbar_wait(&xfull[sl], (xpar >> sl) & 1, a.err, 173);
+        xpar ^= 1u << sl;
+        for (int ai = 0; ai < 2; ++ai, ++xv) {
+          const int ja = 2 * xs + ai;
+          // the MMAs that read this Xh^T buffer last are done
+          ptx::mbar_wait(&xh_free[xv % kXh], ((xv / kXh) & 1) ^ 1, a.err, 174);
+          const uint8_t *src = slot_ptr(u) + ai * kXAtom + (pc >> 2) * 4096;
+          const uint4 q0 = *reinterpret_cast<const uint4 *>(src + sw128(jl, (pc & 3) * 32));
+          const uint4 q1 = *reinterpret_cast<const uint4 *>(src + sw128(jl, (pc & 3) * 32 + 16));
+          const float w = vs[pb][ja * 32 + jl];
+          const float v[8] = {__uint_as_float(q0.x), __uint_as_float(q0.y),
+                              __uint_as_float(q0.z), __uint_as_float(q0.w),
+                              __uint_as_float(q1.x), __uint_as_float(q1.y),
+                              __uint_as_float(q1.z), __uint_as_float(q1.w)};
+          uint8_t *dst = xh + (xv % kXh) * kXAtom;
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            *reinterpret_cast<uint32_t *>(dst + sw128(8 * pc + e, jl * 4)) = to_tf32(v[e] * w);
+          ptx::fence_async_smem();
+          warp_arrive(&xh_ready[xv % kXh]);
+        }
+        // every row thread has read the landed stage: it may be refilled
+        ptx::named_bar_sync(2, kRowThreads);
+        if (tid == 0) ptx::mbar_arrive(&empty[sl]);
+      }
+      if (q > 0) epilogue(q - 1, D_prev);
+      D_prev = in.D;
+    }
+    if (hs > 0) epilogue(hs - 1, D_prev);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, 512);
+}
+
+struct OutSmem32 {
+  int nslot, smem;
+};
+// C of the tile, the ring and the Xh^T buffers within 220 KB of dynamic
+// shared memory (1 KB of it alignment slack; the static arrays, about 7 KB,
+// sit beside it).
+OutSmem32 out_smem32(const Dims &d) {
+  OutSmem32 m;
+  const int c_bytes = (int)(d.S / 32) * kAtom;
+  const int room = (220 * 1024 - 1024 - c_bytes - kXh * kXAtom) / kStage;
+  m.nslot = std::min(kMaxSlots, room);
+  m.smem = c_bytes + m.nslot * kStage + kXh * kXAtom + 1024;
+  return m;
+}
+
+}  // namespace
+
+bool fwd_out_tf32_supported(const Dims &d) {
+  if (d.P != kP || d.S % 32 || d.S < 32 || d.S > 128 || (d.T != 128 && d.T != 256))
+    return false;
+  if (d.nc > 65535 || d.b > 65535) return false;
+  // a head's state and x stages in flight, plus one
+  return out_smem32(d).nslot >= 4;
+}
+
+bool fwd_out_tf32_heads_ok(const Dims &d, int hs) {
+  return fwd_out_tf32_supported(d) && hs >= 1 && hs <= d.hpg && d.hpg % hs == 0 &&
+         (d.nh / hs) * (d.T / 128) <= 65535;
+}
+
+// Heads per CTA: the divisor of the heads per group minimising the bytes the
+// busiest SM moves (waves of CTAs times a CTA's loads: C and B of the tile
+// once, per head its state, x and y).
+int fwd_out_tf32_heads(const Dims &d) {
+  const int64_t sms = sm_count();
+  const int nT = (int)(d.T / 128);
+  int best = 1;
+  double best_cost = 1e300;
+  for (int hs = 1; hs <= d.hpg; ++hs) {
+    if (!fwd_out_tf32_heads_ok(d, hs)) continue;
+    const int64_t ctas = d.b * d.nc * nT * (d.nh / hs);
+    const double per_cta = 4.0 * (128.0 * d.S + d.T * d.S) +
+                           hs * 4.0 * (d.S * 64.0 + d.T * 64.0 + 128.0 * 64.0);
+    const double cost = (double)((ctas + sms - 1) / sms) * per_cta;
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = hs;
+    }
+  }
+  return best;
+}
+
+cudaError_t launch_fwd_out_tf32(const Dims &d, const float *x, const float *B, const float *C,
+                                const float *dt, const float *G, const float *states,
+                                const float *D, float *y, int hs, int *err, cudaStream_t st) {
+  if (!fwd_out_tf32_heads_ok(d, hs)) return cudaErrorInvalidValue;
+  CUtensorMap tC, tB, tx, tS;
+  if (!make_tmap_bl(&tC, C, false, d.b, d.L, d.ng, d.S, 128) ||
+      !make_tmap_bl(&tB, B, false, d.b, d.L, d.ng, d.S, 128) ||
+      !make_tmap_bl(&tx, x, false, d.b, d.L, d.nh, d.P, 32))
+    return cudaErrorInvalidValue;
+  {
+    // start states as [b * nh * nc][P][S] fp32; one box = 64 rows of P x 32 of S
+    const uint64_t dims[3] = {(uint64_t)d.S, (uint64_t)d.P, (uint64_t)(d.b * d.nh * d.nc)};
+    const uint64_t strides[2] = {(uint64_t)d.S * 4, (uint64_t)(d.S * d.P * 4)};
+    const uint32_t box[3] = {32u, 64u, 1u};
+    if (!make_tmap_sw128(&tS, states, false, 3, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  const OutSmem32 m = out_smem32(d);
+  auto kernel = d.T == 256 ? fwd_out_tf32<256> : fwd_out_tf32<128>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, m.smem);
+  if (e != cudaSuccess) return e;
+  OutArgs32 a;
+  a.x = x;
+  a.dt = dt;
+  a.D = D;
+  a.G = G;
+  a.y = y;
+  a.err = err;
+  a.L = (int)d.L;
+  a.nh = (int)d.nh;
+  a.S = (int)d.S;
+  a.hpg = (int)d.hpg;
+  a.T = (int)d.T;
+  a.nc = (int)d.nc;
+  a.nb = (int)d.b;
+  a.hs = hs;
+  a.nslot = m.nslot;
+  // programmatic stream serialisation: the producer and the row warps wait
+  // on the device before reading the start states and G
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((d.nh / hs) * (d.T / 128)), (unsigned)d.nc, (unsigned)d.b);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = m.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tC, tB, tx, tS, a);
+}
+
+}  // namespace ssd

@@ -310,6 +310,17 @@ __device__ __forceinline__ void mma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// D (+)= A * B with A (M x 8, tf32) in tensor memory: lane m holds row m, one
+// 32-bit column per k; B from a shared-memory descriptor.
+__device__ __forceinline__ void mma_ts_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every MMA issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(

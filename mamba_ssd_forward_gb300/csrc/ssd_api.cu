@@ -416,11 +416,21 @@ ssd_status forward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
     if (e == cudaSuccess && ++launched) e = mark(launched);
     if (e == cudaSuccess) e = ssd::launch_chunk_state(d, dtype, x, B, dt, G, dst, err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
+    // the output pass: the warp-specialised tf32 kernel where the shape
+    // allows (it reads the stored states rounded to tf32), else the step
+    // kernel
+    const bool fast = ssd::fwd_out_tf32_supported(d);
     if (e == cudaSuccess)
-      e = ssd::launch_state_passing(d, dst, G, h0, sts, final_state, err, st);
+      e = ssd::launch_state_passing(d, dst, G, h0, sts, final_state, err, st, fast);
     if (e == cudaSuccess && ++launched) e = mark(launched);
     if (e == cudaSuccess)
-      e = ssd::launch_chunk_scan(d, dtype, x, B, C, dt, G, sts, D, y, err, st);
+      e = fast ? ssd::launch_fwd_out_tf32(d, static_cast<const float *>(x),
+                                          static_cast<const float *>(B),
+                                          static_cast<const float *>(C),
+                                          static_cast<const float *>(dt), G, sts, D,
+                                          static_cast<float *>(y), ssd::fwd_out_tf32_heads(d),
+                                          err, st)
+               : ssd::launch_chunk_scan(d, dtype, x, B, C, dt, G, sts, D, y, err, st);
     if (e == cudaSuccess && ++launched) e = mark(launched);
   }
   if (n_launches) *n_launches = launched;
