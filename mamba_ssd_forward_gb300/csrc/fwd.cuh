@@ -77,7 +77,8 @@ cudaError_t launch_fwd_out(const Dims &d, const void *x, const void *B, const vo
 // shared by the slice's heads with the decay factored about one anchor per
 // chunk and head (P = 64, S a multiple of 32 up to 128, T in {128, 256}).
 // It reads G (fp32, log2 units, [b, nh, nc * T]) and the fp32 start states
-// [b, nh, nc, P, S] rounded to tf32 (state_passing with round_tf32).
+// [b, nh, nc, P, S] times 2^alpha_k rounded to tf32 (state_passing with
+// tf32_out).
 bool fwd_out_tf32_supported(const Dims &d);
 bool fwd_out_tf32_heads_ok(const Dims &d, int hs);
 int fwd_out_tf32_heads(const Dims &d);  // the cost-model choice

@@ -12,33 +12,39 @@
 // exp2(G_i - G_j) = u_i v'_j with u_i = exp2(G_i - alpha), v'_j =
 // exp2(alpha - G_j), so the masked C B^T of the chunk carries no decay and is
 // shared unchanged by every head of the group; per head the x rows are only
-// scaled by v_j = v'_j dt_j.  Unlike fwd_out, the inter-chunk term keeps an
-// accumulator of its own, y_i = exp2(G_i) Acc_s,i + u_i Acc_i,i + D x_i, so
-// the start states need no scaling.  A chunk whose decay is too steep for
-// bounded factors (total decay above 2^-180, or a real token's factor below
-// 2^-120) takes an exact per-element path for the in-chunk sum on the CUDA
-// cores instead (rare, slow, exact).
+// scaled by v_j = v'_j dt_j, and with exp2(G_i) = u_i 2^alpha
+//
+//   y_i = u_i [ c_i . (2^alpha h_k) + sum_{j<=i} (c_i . B_j) v_j x_j ] + D x_i:
+//
+// one accumulation per head, C (2^alpha h)^T + (C B^T masked) Xh, with the
+// start states stored times 2^alpha by the state pass (an exact power of
+// two; alpha = 0 when the chunk's total decay exceeds 2^-180).  A chunk whose
+// decay is too steep for bounded factors (that, or a real token's factor
+// below 2^-120) takes an exact per-element path for the in-chunk sum on the
+// CUDA cores instead (rare, slow, exact).
 //
 // kind::tf32 takes K-major operands only, and every operand is rounded to
-// tf32 (nearest) before the tensor core sees it: C and B in shared memory by
-// the row warps as they land, the start states by the state pass that
-// stores them, x while it is transposed, C B^T in tensor memory.
+// tf32 (nearest) before the tensor core sees it: C as the row warps move it
+// into tensor memory, B in shared memory as it lands, the start states by
+// the state pass that stores them, x while it is transposed, C B^T in
+// tensor memory.
 //
 // One CTA per (128-row tile t of a chunk, slice of hs heads of one group,
-// chunk, batch), 1 CTA per SM:
-//   producer warp: C of the tile (resident, K-major atoms of 32 s), then
-//     through a ring of 16 KB stages: B of tokens 0 .. 128 (t + 1) - 1 per
-//     atom of S, then per head its start state (two atoms of S per stage)
-//     and its x (two 32-token atoms per stage, as landed: p contiguous);
-//   MMA warp: C B^T of the tile into tensor memory (fp32, columns = tokens);
-//     per head into one of two accumulator sets Acc_s = C h^T (K = S) and
-//     Acc_i = (C B^T masked) Xh (K = tokens, A read from tensor memory, Xh
-//     from the row warps' transposed atoms);
-//   row warps (8): round C and the B stages; mask (j > i -> 0) and round
-//     C B^T in place; per head its factors, the transposition of each x
-//     atom into K-major Xh^T (tokens along the 128-byte rows, scaled by v_j,
-//     rounded), and the previous head's epilogue
-//     y = exp2(G_i) Acc_s + u_i Acc_i + D x_i.
+// chunk, batch), 1 CTA per SM, everything staged through one ring of 16 KB
+// stages:
+//   producer warp: C of the tile (atoms of 32 s, rows = the tile's tokens),
+//     B of tokens 0 .. 128 (t + 1) - 1 per atom of S, then per head its
+//     start state (two atoms of S per stage) and its x (64 tokens per stage,
+//     as landed: p contiguous);
+//   MMA warp: C B^T of the tile (A = C from tensor memory) into tensor
+//     memory, fp32, columns = tokens; per head into one of two accumulator
+//     sets C (2^alpha h)^T (A = C) + (C B^T masked) Xh (A = C B^T, B = the
+//     row warps' transposed x atoms);
+//   row warps (8): C into tensor memory (rounded), the B stages rounded in
+//     place; C B^T masked (j > i -> 0) and rounded in place; per head its
+//     factors, the transposition of each 32-token x atom into K-major Xh^T
+//     (tokens along the 128-byte rows, scaled by v_j, rounded), and the
+//     previous head's epilogue y = u_i Acc_i + D x_i.
 // Supported: P = 64, S a multiple of 32 up to 128, T in {128, 256}.
 #include "fwd.cuh"
 
@@ -50,20 +56,19 @@ constexpr int kRowThreads = kRowWarps * 32;
 constexpr int kThreads = kRowThreads + 64;
 constexpr int kProducerWarp = kRowWarps, kMmaWarp = kRowWarps + 1;
 constexpr int kP = 64;
-constexpr int kAtom = 128 * 128;  // C / B: 128 rows x 32 fp32 (one K atom of S)
-constexpr int kStage = 16384;     // one ring stage
+constexpr int kStage = 16384;     // one ring stage: C or B (128 rows x 32 fp32 of
+                                  // S), two state atoms, or 64 tokens of x
 constexpr int kHAtom = 64 * 128;  // start state: 64 rows p x 32 fp32 of S
-constexpr int kXAtom = 64 * 128;  // x as landed: 32 tokens x 64 p (two 4 KB boxes);
-                                  // Xh^T: 64 rows p x 32 tokens
-constexpr int kMaxSlots = 10;
+constexpr int kXAtom = 64 * 128;  // Xh^T: 64 rows p x 32 tokens
+constexpr int kMaxSlots = 12;
 constexpr int kXh = 4;            // Xh^T atoms in flight
 constexpr float kSpanMax = 180.f;
 constexpr float kMinFactor = 7.52316384526264e-37f;  // 2^-120
 
-// Tensor-memory columns: C B^T of the tile at [0, 128 (t + 1)); accumulator
-// set s: Acc_s at 256 + 128 s, Acc_i at 256 + 128 s + 64.
-__device__ __forceinline__ uint32_t acc_s(int set) { return 256u + 128u * (uint32_t)set; }
-__device__ __forceinline__ uint32_t acc_i(int set) { return 320u + 128u * (uint32_t)set; }
+// Tensor-memory columns: C B^T of the tile at [0, 128 (t + 1)); C of the
+// tile at [256, 256 + S); accumulator set s at 384 + 64 s.
+constexpr uint32_t kColC = 256;
+__device__ __forceinline__ uint32_t acc_col(int set) { return 384u + 64u * (uint32_t)set; }
 
 struct OutArgs32 {
   const float *x, *dt, *D;
@@ -83,12 +88,14 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
   constexpr int nT = kT / 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  // full: a state stage landed (MMA waits); xfull: a B or x stage landed (row
-  // warps wait); scaled: the row warps rounded a B stage; empty: a stage's
-  // readers are done; xh_ready / xh_free: an Xh^T atom written / read
-  __shared__ __align__(8) uint64_t c_full, c_ready, full[kMaxSlots], xfull[kMaxSlots],
-      scaled[kMaxSlots], empty[kMaxSlots], sc_done, pack_done, acc_full[2], acc_free[2],
-      xh_ready[kXh], xh_free[kXh];
+  // full: a state stage landed (MMA waits); xfull: a C, B or x stage landed
+  // (row warps wait); scaled: the row warps rounded a B stage; empty: the
+  // MMAs reading a B or state stage are done; xrel: every row warp is done
+  // with a C or x stage; c_ready: C is in tensor memory; xh_ready / xh_free:
+  // an Xh^T atom written / read
+  __shared__ __align__(8) uint64_t c_ready, full[kMaxSlots], xfull[kMaxSlots],
+      scaled[kMaxSlots], empty[kMaxSlots], xrel[kMaxSlots], sc_done, pack_done, acc_full[2],
+      acc_free[2], xh_ready[kXh], xh_free[kXh];
   __shared__ uint32_t tmem_slot;
   // per head (by head parity): G and dt of every token, v_j, alpha, path
   __shared__ __align__(16) float Gs[2][256];
@@ -110,20 +117,19 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
   const int nS = S / 32;             // K atoms of S
   const int nHs = (nS + 1) / 2;      // state stages per head
   const int nJ = 4 * (t + 1);        // 32-token atoms of the in-chunk sum
-  const int nXs = nJ / 2;            // x stages per head
-  uint8_t *Cs = smem;                // atom sb at sb * kAtom
-  uint8_t *ring = smem + nS * kAtom;
+  const int nXs = nJ / 2;            // x stages per head (64 tokens each)
+  uint8_t *ring = smem;
   uint8_t *xh = ring + nslot * kStage;
   auto slot_ptr = [&](int u) { return ring + (u % nslot) * kStage; };
 
   if (tid == 0) {
-    ptx::mbar_init(&c_full, 1);
     ptx::mbar_init(&c_ready, kRowWarps);
     for (int i = 0; i < nslot; ++i) {
       ptx::mbar_init(&full[i], 1);
       ptx::mbar_init(&xfull[i], 1);
       ptx::mbar_init(&scaled[i], kRowWarps);
       ptx::mbar_init(&empty[i], 1);
+      ptx::mbar_init(&xrel[i], kRowWarps);
     }
     ptx::mbar_init(&sc_done, 1);
     ptx::mbar_init(&pack_done, kRowWarps);
@@ -146,7 +152,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const bool leader = (tid & 31) == 0;
-  const int n_pa = nS * (t + 1);  // phase-A (B) stages
+  const int n_pa = nS * (t + 1);  // B stages
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -155,18 +161,37 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       ptx::prefetch_tmap(&tm_B);
       ptx::prefetch_tmap(&tm_x);
       ptx::prefetch_tmap(&tm_st);
-      ptx::mbar_arrive_expect_tx(&c_full, nS * kAtom);
-      for (int sb = 0; sb < nS; ++sb)
-        ptx::tma_load_4d(Cs + sb * kAtom, &tm_C, sb * 32, g, tok0 + t * 128, b, &c_full);
     }
     __syncwarp();
     int u = 0;
-    auto acquire = [&](int code) {
-      ptx::mbar_wait(&empty[u % nslot], ((u / nslot) & 1) ^ 1, a.err, code);
+    // the previous use of a slot was released on empty (its reader the MMA
+    // warp) or on xrel (the row warps): one bit per slot says which, one
+    // parity bit per slot and barrier says which phase to wait for
+    uint32_t prev_x = 0, epar = 0, rpar = 0;
+    auto acquire = [&](int code, bool x_stage) {
+      const int sl = u % nslot;
+      if (u >= nslot) {
+        if ((prev_x >> sl) & 1) {
+          ptx::mbar_wait(&xrel[sl], (rpar >> sl) & 1, a.err, code);
+          rpar ^= 1u << sl;
+        } else {
+          ptx::mbar_wait(&empty[sl], (epar >> sl) & 1, a.err, code);
+          epar ^= 1u << sl;
+        }
+      }
+      prev_x = x_stage ? (prev_x | (1u << sl)) : (prev_x & ~(1u << sl));
     };
+    for (int sb = 0; sb < nS; ++sb, ++u) {
+      acquire(159, true);
+      if (leader) {
+        ptx::mbar_arrive_expect_tx(&xfull[u % nslot], kStage);
+        ptx::tma_load_4d(slot_ptr(u), &tm_C, sb * 32, g, tok0 + t * 128, b, &xfull[u % nslot]);
+      }
+      __syncwarp();
+    }
     for (int sb = 0; sb < nS; ++sb)
       for (int th = 0; th <= t; ++th, ++u) {
-        acquire(160);
+        acquire(160, false);
         if (leader) {
           ptx::mbar_arrive_expect_tx(&xfull[u % nslot], kStage);
           ptx::tma_load_4d(slot_ptr(u), &tm_B, sb * 32, g, tok0 + th * 128, b, &xfull[u % nslot]);
@@ -177,7 +202,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       const int h = hbase + q;
       const int row = (b * nh + h) * a.nc + k;  // this head's start state
       for (int hh = 0; hh < nHs; ++hh, ++u) {
-        acquire(161);
+        acquire(161, false);
         if (leader) {
           // the start states come from the preceding kernel (the state
           // pass), which may still be running when this CTA starts
@@ -191,13 +216,13 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
         __syncwarp();
       }
       for (int xs = 0; xs < nXs; ++xs, ++u) {
-        acquire(162);
+        acquire(162, true);
         if (leader) {
+          // two boxes of 64 tokens x 32 p (p halves), 8 KB each
           ptx::mbar_arrive_expect_tx(&xfull[u % nslot], kStage);
-          for (int ai = 0; ai < 2; ++ai)
-            for (int ph = 0; ph < 2; ++ph)
-              ptx::tma_load_4d(slot_ptr(u) + ai * kXAtom + ph * 4096, &tm_x, ph * 32, h,
-                               tok0 + (2 * xs + ai) * 32, b, &xfull[u % nslot]);
+          for (int ph = 0; ph < 2; ++ph)
+            ptx::tma_load_4d(slot_ptr(u) + ph * 8192, &tm_x, ph * 32, h, tok0 + xs * 64, b,
+                             &xfull[u % nslot]);
         }
         __syncwarp();
       }
@@ -207,7 +232,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     uint32_t fpar = 0, spar = 0;  // parity of the next wait, one bit per slot
     ptx::mbar_wait(&c_ready, 0, a.err, 163);
     ptx::tc_fence_after();
-    int u = 0;
+    int u = nS;  // the C stages went to the row warps
     const uint32_t idCB = ptx::idesc_tf32(128, 128, false, false);
     for (int sb = 0; sb < nS; ++sb)
       for (int th = 0; th <= t; ++th, ++u) {
@@ -216,12 +241,12 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
         spar ^= 1u << sl;
         ptx::tc_fence_after();
         if (leader) {
-          const uint32_t c0 = ptx::smem_u32(Cs + sb * kAtom), b0 = ptx::smem_u32(slot_ptr(u));
+          const uint32_t b0 = ptx::smem_u32(slot_ptr(u));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t cd = ptx::smem_desc(c0 + kk * 32, 16, 1024, ptx::kSw128);
             const uint64_t bd = ptx::smem_desc(b0 + kk * 32, 16, 1024, ptx::kSw128);
-            ptx::mma_ss<true>(tmem + 128 * th, cd, bd, idCB, (sb | kk) ? 1u : 0u);
+            ptx::mma_ts_tf32(tmem + 128 * th, tmem + kColC + sb * 32 + kk * 8, bd, idCB,
+                             (sb | kk) ? 1u : 0u);
           }
           ptx::mma_commit(&empty[sl]);
         }
@@ -236,7 +261,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       const int set = q & 1;
       if (q >= 2) ptx::mbar_wait(&acc_free[set], ((q >> 1) - 1) & 1, a.err, 166);
       ptx::tc_fence_after();
-      // Acc_s = C h^T over the state stages
+      // Acc = C (2^alpha h)^T over the state stages
       for (int hh = 0; hh < nHs; ++hh, ++u) {
         const int sl = u % nslot;
         ptx::mbar_wait(&full[sl], (fpar >> sl) & 1, a.err, 167);
@@ -246,13 +271,12 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
           const uint32_t h0 = ptx::smem_u32(slot_ptr(u));
           const int na = min(2, nS - 2 * hh);
           for (int ai = 0; ai < na; ++ai) {
-            const uint32_t c0 = ptx::smem_u32(Cs + (2 * hh + ai) * kAtom);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t cd = ptx::smem_desc(c0 + kk * 32, 16, 1024, ptx::kSw128);
               const uint64_t hd =
                   ptx::smem_desc(h0 + ai * kHAtom + kk * 32, 16, 1024, ptx::kSw128);
-              ptx::mma_ss<true>(tmem + acc_s(set), cd, hd, idY, (hh | ai | kk) ? 1u : 0u);
+              ptx::mma_ts_tf32(tmem + acc_col(set), tmem + kColC + (2 * hh + ai) * 32 + kk * 8,
+                               hd, idY, (hh | ai | kk) ? 1u : 0u);
             }
           }
           ptx::mma_commit(&empty[sl]);
@@ -260,7 +284,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
         __syncwarp();
       }
       u += nXs;  // the x stages go to the row warps
-      // Acc_i = (C B^T masked) Xh over the Xh^T atoms (none for a steep head,
+      // Acc += (C B^T masked) Xh over the Xh^T atoms (none for a steep head,
       // whose epilogue forms the in-chunk sum itself)
       for (int ja = 0; ja < nJ; ++ja, ++xv) {
         const int xs = xv % kXh;
@@ -273,8 +297,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t xd = ptx::smem_desc(x0 + kk * 32, 16, 1024, ptx::kSw128);
-              ptx::mma_ts_tf32(tmem + acc_i(set), tmem + ja * 32 + kk * 8, xd, idY,
-                               (ja | kk) ? 1u : 0u);
+              ptx::mma_ts_tf32(tmem + acc_col(set), tmem + ja * 32 + kk * 8, xd, idY, 1u);
             }
           }
           ptx::mma_commit(&xh_free[xs]);
@@ -306,14 +329,31 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       }
     };
 
-    // C of the tile, then the B stages, rounded as they land
-    ptx::mbar_wait(&c_full, 0, a.err, 169);
-    round_block(Cs, nS * kAtom);
-    ptx::fence_async_smem();
-    warp_arrive(&c_ready);
+    // C of the tile into tensor memory, rounded (warp: its lane quadrant, 16
+    // of the 32 columns of each atom), then the B stages rounded as they land
     uint32_t xpar = 0;  // parity of the next wait on xfull[slot], one bit per slot
     int u = 0;
-    for (; u < n_pa; ++u) {
+    for (int sb = 0; sb < nS; ++sb, ++u) {
+      const int sl = u % nslot;
+      ptx::mbar_wait(&xfull[sl], (xpar >> sl) & 1, a.err, 169);
+      xpar ^= 1u << sl;
+      uint32_t r[16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 v =
+            *reinterpret_cast<const uint4 *>(slot_ptr(u) + sw128(lrow, (half * 4 + c) * 16));
+        r[4 * c] = to_tf32(__uint_as_float(v.x));
+        r[4 * c + 1] = to_tf32(__uint_as_float(v.y));
+        r[4 * c + 2] = to_tf32(__uint_as_float(v.z));
+        r[4 * c + 3] = to_tf32(__uint_as_float(v.w));
+      }
+      warp_arrive(&xrel[sl]);  // the values are in registers: the stage may go
+      ptx::tmem_stu<16>(tmem + lane_base + kColC + sb * 32 + half * 16, r);
+    }
+    ptx::tmem_st_wait();
+    ptx::tc_fence_before();
+    warp_arrive(&c_ready);
+    for (; u < nS + n_pa; ++u) {
       const int sl = u % nslot;
       ptx::mbar_wait(&xfull[sl], (xpar >> sl) & 1, a.err, 170);
       xpar ^= 1u << sl;
@@ -363,13 +403,18 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       }
       return r;
     };
-    // factors and path of head q into the parity-(q & 1) arrays
+    // factors and path of head q into the parity-(q & 1) arrays.  The first
+    // barrier keeps every write behind the reads of head q - 2's epilogue
+    // (same parity), which the slowest row warps may still be doing; the
+    // second makes the arrays visible to all.
     auto prep_head = [&](int q, const HeadIn &in) {
       const int pb = q & 1;
-      const float alpha = rintf(0.5f * in.Glast);
+      // the anchor the state pass scaled the stored start state by
+      const float alpha = -in.Glast <= kSpanMax ? rintf(0.5f * in.Glast) : 0.f;
       const float vj = in.dtj > 0.f ? exp2f(alpha - in.Gj) * in.dtj : 0.f;
       const bool ok = in.dtj == 0.f || vj >= kMinFactor;
       const int all_ok = __all_sync(0xffffffffu, ok);
+      ptx::named_bar_sync(1, kRowThreads);
       if ((tid & 31) == 0) warp_ok[warp] = all_ok;
       if (tid < kT) {
         Gs[pb][tid] = in.Gj;
@@ -378,18 +423,19 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       }
       ptx::named_bar_sync(1, kRowThreads);
       if (tid == 0) {
+        // read by the MMA warp after this thread's next arrival on xh_ready,
+        // and by the epilogue of head q, behind head q + 1's barriers
         int okall = 1;
 #pragma unroll
         for (int w2 = 0; w2 < kRowWarps; ++w2) okall &= warp_ok[w2];
         steeps[pb] = !(okall && -in.Glast <= kSpanMax);
         alphas[pb] = alpha;
       }
-      ptx::named_bar_sync(1, kRowThreads);
     };
 
-    // the epilogue of head q: y = exp2(G_i) Acc_s + u_i Acc_i + D x_i for
-    // this thread's row and 32 columns
-    auto epilogue = [&](int q, float Dh) {
+    // the epilogue of head q: y = u_i Acc_i + D x_i for this thread's row
+    // and 32 columns (x_i as landed, kept from the transposition of its atom)
+    auto epilogue = [&](int q, float Dh, const uint4 (&xk)[8]) {
       const int set = q & 1, pb = q & 1, h = hbase + q;
       const bool row_ok = i_rel < valid;
       const int64_t xrow = (((int64_t)b * L + tok0 + i_rel) * nh + h) * kP + 32 * half;
@@ -398,43 +444,35 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       float xi[32];
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
-        const float4 v = io_ok ? *reinterpret_cast<const float4 *>(a.x + xrow + 4 * m)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-        xi[4 * m] = v.x;
-        xi[4 * m + 1] = v.y;
-        xi[4 * m + 2] = v.z;
-        xi[4 * m + 3] = v.w;
+        xi[4 * m] = __uint_as_float(xk[m].x);
+        xi[4 * m + 1] = __uint_as_float(xk[m].y);
+        xi[4 * m + 2] = __uint_as_float(xk[m].z);
+        xi[4 * m + 3] = __uint_as_float(xk[m].w);
       }
       ptx::mbar_wait(&acc_full[set], (q >> 1) & 1, a.err, 172);
       ptx::tc_fence_after();
       const bool steep = steeps[pb] != 0;
-      uint32_t as[32], ai[32];
-      ptx::tmem_ld16(tmem + lane_base + acc_s(set) + 32 * half,
-                     *reinterpret_cast<uint32_t(*)[16]>(as));
-      ptx::tmem_ld16(tmem + lane_base + acc_s(set) + 32 * half + 16,
-                     *reinterpret_cast<uint32_t(*)[16]>(as + 16));
-      ptx::tmem_ld16(tmem + lane_base + acc_i(set) + 32 * half,
-                     *reinterpret_cast<uint32_t(*)[16]>(ai));
-      ptx::tmem_ld16(tmem + lane_base + acc_i(set) + 32 * half + 16,
-                     *reinterpret_cast<uint32_t(*)[16]>(ai + 16));
+      uint32_t ac[32];
+      ptx::tmem_ld16(tmem + lane_base + acc_col(set) + 32 * half,
+                     *reinterpret_cast<uint32_t(*)[16]>(ac));
+      ptx::tmem_ld16(tmem + lane_base + acc_col(set) + 32 * half + 16,
+                     *reinterpret_cast<uint32_t(*)[16]>(ac + 16));
       ptx::tmem_ld_wait();
-      ptx::reg_fence(as);
-      ptx::reg_fence(ai);
+      ptx::reg_fence(ac);
       const float Gi = Gs[pb][min(i_rel, kT - 1)];
-      const float ei = exp2f(Gi);
+      const float ui = exp2f(Gi - alphas[pb]);
       float yv[32];
       if (!steep) {
         ptx::tc_fence_before();
         warp_arrive(&acc_free[set]);  // the accumulators may take head q + 2
-        const float ui = exp2f(Gi - alphas[pb]);
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          yv[c] = fmaf(Dh, xi[c], fmaf(ei, __uint_as_float(as[c]), ui * __uint_as_float(ai[c])));
+        for (int c = 0; c < 32; ++c) yv[c] = fmaf(Dh, xi[c], ui * __uint_as_float(ac[c]));
       } else {
-        // exact per-element path: the in-chunk sum from the masked C B^T of
+        // exact per-element path: the inter-chunk term from the accumulator
+        // (C (2^alpha h)^T only), the in-chunk sum from the masked C B^T of
         // this row's lane and the raw x rows (L2), every factor exact
 #pragma unroll
-        for (int c = 0; c < 32; ++c) yv[c] = fmaf(Dh, xi[c], ei * __uint_as_float(as[c]));
+        for (int c = 0; c < 32; ++c) yv[c] = fmaf(Dh, xi[c], ui * __uint_as_float(ac[c]));
         const int jmax_warp = t * 128 + quad * 32 + 31;  // the warp's last row
         for (int j0 = 0; j0 <= jmax_warp; j0 += 16) {
           uint32_t cb[16];
@@ -475,6 +513,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     int xv = 0;                              // Xh^T atoms written so far
     HeadIn in_next = fetch_head(0);
     float D_prev = 0.f;
+    uint4 xk[8], xk_prev[8];  // this thread's x row segment (head q, head q - 1)
     for (int q = 0; q < hs; ++q) {
       const HeadIn in = in_next;
       if (q + 1 < hs) in_next = fetch_head(q + 1);
@@ -489,9 +528,16 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
           const int ja = 2 * xs + ai;
           // the MMAs that read this Xh^T buffer last are done
           ptx::mbar_wait(&xh_free[xv % kXh], ((xv / kXh) & 1) ^ 1, a.err, 174);
-          const uint8_t *src = slot_ptr(u) + ai * kXAtom + (pc >> 2) * 4096;
+          const uint8_t *src = slot_ptr(u) + (pc >> 2) * 8192 + ai * 4096;
           const uint4 q0 = *reinterpret_cast<const uint4 *>(src + sw128(jl, (pc & 3) * 32));
           const uint4 q1 = *reinterpret_cast<const uint4 *>(src + sw128(jl, (pc & 3) * 32 + 16));
+          if (ja == 4 * t + quad) {
+            // the atom holding this warp's rows: keep the row segment for D x_i
+            const uint8_t *xr = slot_ptr(u) + half * 8192 + ai * 4096;
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+              xk[m] = *reinterpret_cast<const uint4 *>(xr + sw128(tid & 31, m * 16));
+          }
           const float w = vs[pb][ja * 32 + jl];
           const float v[8] = {__uint_as_float(q0.x), __uint_as_float(q0.y),
                               __uint_as_float(q0.z), __uint_as_float(q0.w),
@@ -504,14 +550,15 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
           ptx::fence_async_smem();
           warp_arrive(&xh_ready[xv % kXh]);
         }
-        // every row thread has read the landed stage: it may be refilled
-        ptx::named_bar_sync(2, kRowThreads);
-        if (tid == 0) ptx::mbar_arrive(&empty[sl]);
+        // this warp has read the landed stage: it may be refilled once all have
+        warp_arrive(&xrel[sl]);
       }
-      if (q > 0) epilogue(q - 1, D_prev);
+      if (q > 0) epilogue(q - 1, D_prev, xk_prev);
       D_prev = in.D;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) xk_prev[m] = xk[m];
     }
-    if (hs > 0) epilogue(hs - 1, D_prev);
+    if (hs > 0) epilogue(hs - 1, D_prev, xk_prev);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -521,15 +568,13 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
 struct OutSmem32 {
   int nslot, smem;
 };
-// C of the tile, the ring and the Xh^T buffers within 220 KB of dynamic
-// shared memory (1 KB of it alignment slack; the static arrays, about 7 KB,
-// sit beside it).
-OutSmem32 out_smem32(const Dims &d) {
+// The ring and the Xh^T buffers within 220 KB of dynamic shared memory (1 KB
+// of it alignment slack; the static arrays, about 7 KB, sit beside it).
+OutSmem32 out_smem32(const Dims &) {
   OutSmem32 m;
-  const int c_bytes = (int)(d.S / 32) * kAtom;
-  const int room = (220 * 1024 - 1024 - c_bytes - kXh * kXAtom) / kStage;
+  const int room = (220 * 1024 - 1024 - kXh * kXAtom) / kStage;
   m.nslot = std::min(kMaxSlots, room);
-  m.smem = c_bytes + m.nslot * kStage + kXh * kXAtom + 1024;
+  m.smem = m.nslot * kStage + kXh * kXAtom + 1024;
   return m;
 }
 
@@ -577,7 +622,7 @@ cudaError_t launch_fwd_out_tf32(const Dims &d, const float *x, const float *B, c
   CUtensorMap tC, tB, tx, tS;
   if (!make_tmap_bl(&tC, C, false, d.b, d.L, d.ng, d.S, 128) ||
       !make_tmap_bl(&tB, B, false, d.b, d.L, d.ng, d.S, 128) ||
-      !make_tmap_bl(&tx, x, false, d.b, d.L, d.nh, d.P, 32))
+      !make_tmap_bl(&tx, x, false, d.b, d.L, d.nh, d.P, 64))
     return cudaErrorInvalidValue;
   {
     // start states as [b * nh * nc][P][S] fp32; one box = 64 rows of P x 32 of S

@@ -100,7 +100,7 @@ cudaError_t launch_chunk_state(const Dims &d, ssd_dtype io, const void *x,
 cudaError_t launch_state_passing(const Dims &d, const float *dstates,
                                  const float *G, const float *h0,
                                  float *states, float *final_state, int *err,
-                                 cudaStream_t st, bool round_tf32 = false);
+                                 cudaStream_t st, bool tf32_out = false);
 cudaError_t launch_chunk_scan(const Dims &d, ssd_dtype io, const void *x,
                               const void *B, const void *C, const void *dt,
                               const float *G, const float *states,
