@@ -33,13 +33,13 @@
 // chunk, batch), 1 CTA per SM, everything staged through one ring of 16 KB
 // stages:
 //   producer warp: C of the tile (atoms of 32 s, rows = the tile's tokens),
-//     B of tokens 0 .. 128 (t + 1) - 1 per atom of S, then per head its
-//     start state (two atoms of S per stage) and its x (64 tokens per stage,
-//     as landed: p contiguous);
+//     B of tokens 0 .. 128 (t + 1) - 1 per atom of S, then per head its x
+//     (64 tokens per stage, as landed: p contiguous) and its start state
+//     (two atoms of S per stage);
 //   MMA warp: C B^T of the tile (A = C from tensor memory) into tensor
 //     memory, fp32, columns = tokens; per head into one of two accumulator
-//     sets C (2^alpha h)^T (A = C) + (C B^T masked) Xh (A = C B^T, B = the
-//     row warps' transposed x atoms);
+//     sets (C B^T masked) Xh (A = C B^T, B = the row warps' transposed x
+//     atoms) + C (2^alpha h)^T (A = C);
 //   row warps (8): C into tensor memory (rounded), the B stages rounded in
 //     place; C B^T masked (j > i -> 0) and rounded in place; per head its
 //     factors, the transposition of each 32-token x atom into K-major Xh^T
@@ -84,7 +84,7 @@ template <int kT>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
              const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_st,
-             const OutArgs32 a) {
+             const __grid_constant__ CUtensorMap tm_y, const OutArgs32 a) {
   constexpr int nT = kT / 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -120,6 +120,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
   const int nXs = nJ / 2;            // x stages per head (64 tokens each)
   uint8_t *ring = smem;
   uint8_t *xh = ring + nslot * kStage;
+  uint8_t *ystage = xh + kXh * kXAtom;  // y of one head: two 16 KB boxes
   auto slot_ptr = [&](int u) { return ring + (u % nslot) * kStage; };
 
   if (tid == 0) {
@@ -161,6 +162,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       ptx::prefetch_tmap(&tm_B);
       ptx::prefetch_tmap(&tm_x);
       ptx::prefetch_tmap(&tm_st);
+      ptx::prefetch_tmap(&tm_y);
     }
     __syncwarp();
     int u = 0;
@@ -201,6 +203,17 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     for (int q = 0; q < hs; ++q) {
       const int h = hbase + q;
       const int row = (b * nh + h) * a.nc + k;  // this head's start state
+      for (int xs = 0; xs < nXs; ++xs, ++u) {
+        acquire(162, true);
+        if (leader) {
+          // two boxes of 64 tokens x 32 p (p halves), 8 KB each
+          ptx::mbar_arrive_expect_tx(&xfull[u % nslot], kStage);
+          for (int ph = 0; ph < 2; ++ph)
+            ptx::tma_load_4d(slot_ptr(u) + ph * 8192, &tm_x, ph * 32, h, tok0 + xs * 64, b,
+                             &xfull[u % nslot]);
+        }
+        __syncwarp();
+      }
       for (int hh = 0; hh < nHs; ++hh, ++u) {
         acquire(161, false);
         if (leader) {
@@ -212,17 +225,6 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
           for (int ai = 0; ai < na; ++ai)
             ptx::tma_load_3d(slot_ptr(u) + ai * kHAtom, &tm_st, (2 * hh + ai) * 32, 0, row,
                              &full[u % nslot]);
-        }
-        __syncwarp();
-      }
-      for (int xs = 0; xs < nXs; ++xs, ++u) {
-        acquire(162, true);
-        if (leader) {
-          // two boxes of 64 tokens x 32 p (p halves), 8 KB each
-          ptx::mbar_arrive_expect_tx(&xfull[u % nslot], kStage);
-          for (int ph = 0; ph < 2; ++ph)
-            ptx::tma_load_4d(slot_ptr(u) + ph * 8192, &tm_x, ph * 32, h, tok0 + xs * 64, b,
-                             &xfull[u % nslot]);
         }
         __syncwarp();
       }
@@ -261,7 +263,32 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       const int set = q & 1;
       if (q >= 2) ptx::mbar_wait(&acc_free[set], ((q >> 1) - 1) & 1, a.err, 166);
       ptx::tc_fence_after();
-      // Acc = C (2^alpha h)^T over the state stages
+      // Acc = (C B^T masked) Xh over the Xh^T atoms first (none for a steep
+      // head, whose epilogue forms the in-chunk sum itself), so that the row
+      // warps' atoms never wait on a state stage
+      bool steep = false;
+      for (int ja = 0; ja < nJ; ++ja, ++xv) {
+        const int xs = xv % kXh;
+        ptx::mbar_wait(&xh_ready[xs], (xv / kXh) & 1, a.err, 168);
+        ptx::tc_fence_after();
+        steep = steeps[q & 1] != 0;
+        if (leader) {
+          if (!steep) {
+            const uint32_t x0 = ptx::smem_u32(xh + xs * kXAtom);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t xd = ptx::smem_desc(x0 + kk * 32, 16, 1024, ptx::kSw128);
+              ptx::mma_ts_tf32(tmem + acc_col(set), tmem + ja * 32 + kk * 8, xd, idY,
+                               (ja | kk) ? 1u : 0u);
+            }
+          }
+          ptx::mma_commit(&xh_free[xs]);
+        }
+        __syncwarp();
+      }
+      u += nXs;  // the x stages went to the row warps
+      // Acc += C (2^alpha h)^T over the state stages (the first MMA of a
+      // steep head starts the accumulator)
       for (int hh = 0; hh < nHs; ++hh, ++u) {
         const int sl = u % nslot;
         ptx::mbar_wait(&full[sl], (fpar >> sl) & 1, a.err, 167);
@@ -276,31 +303,10 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
               const uint64_t hd =
                   ptx::smem_desc(h0 + ai * kHAtom + kk * 32, 16, 1024, ptx::kSw128);
               ptx::mma_ts_tf32(tmem + acc_col(set), tmem + kColC + (2 * hh + ai) * 32 + kk * 8,
-                               hd, idY, (hh | ai | kk) ? 1u : 0u);
+                               hd, idY, (steep && (hh | ai | kk) == 0) ? 0u : 1u);
             }
           }
           ptx::mma_commit(&empty[sl]);
-        }
-        __syncwarp();
-      }
-      u += nXs;  // the x stages go to the row warps
-      // Acc += (C B^T masked) Xh over the Xh^T atoms (none for a steep head,
-      // whose epilogue forms the in-chunk sum itself)
-      for (int ja = 0; ja < nJ; ++ja, ++xv) {
-        const int xs = xv % kXh;
-        ptx::mbar_wait(&xh_ready[xs], (xv / kXh) & 1, a.err, 168);
-        ptx::tc_fence_after();
-        const bool steep = steeps[q & 1] != 0;
-        if (leader) {
-          if (!steep) {
-            const uint32_t x0 = ptx::smem_u32(xh + xs * kXAtom);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t xd = ptx::smem_desc(x0 + kk * 32, 16, 1024, ptx::kSw128);
-              ptx::mma_ts_tf32(tmem + acc_col(set), tmem + ja * 32 + kk * 8, xd, idY, 1u);
-            }
-          }
-          ptx::mma_commit(&xh_free[xs]);
         }
         __syncwarp();
       }
@@ -437,10 +443,6 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     // and 32 columns (x_i as landed, kept from the transposition of its atom)
     auto epilogue = [&](int q, float Dh, const uint4 (&xk)[8]) {
       const int set = q & 1, pb = q & 1, h = hbase + q;
-      const bool row_ok = i_rel < valid;
-      const int64_t xrow = (((int64_t)b * L + tok0 + i_rel) * nh + h) * kP + 32 * half;
-      const bool io_ok = row_ok && SSD_IN_BOUNDS(xrow + 32 <= (int64_t)a.nb * L * nh * kP,
-                                                 a.err, 161);
       float xi[32];
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
@@ -499,11 +501,22 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
         ptx::tc_fence_before();
         warp_arrive(&acc_free[set]);
       }
-      if (io_ok) {
+      // y of the tile through the staging buffer (two boxes of 128 rows x
+      // 32 p), stored by TMA (rows past the sequence are clipped); the
+      // previous head's store must have read the buffer first
+      if (tid == 0) ptx::bulk_wait_read<0>();
+      ptx::named_bar_sync(2, kRowThreads);
+      uint8_t *yt = ystage + half * kStage;
 #pragma unroll
-        for (int m = 0; m < 8; ++m)
-          *reinterpret_cast<float4 *>(a.y + xrow + 4 * m) =
-              make_float4(yv[4 * m], yv[4 * m + 1], yv[4 * m + 2], yv[4 * m + 3]);
+      for (int m = 0; m < 8; ++m)
+        *reinterpret_cast<float4 *>(yt + sw128(lrow, m * 16)) =
+            make_float4(yv[4 * m], yv[4 * m + 1], yv[4 * m + 2], yv[4 * m + 3]);
+      ptx::fence_async_smem();
+      ptx::named_bar_sync(2, kRowThreads);
+      if (tid == 0) {
+        for (int ph = 0; ph < 2; ++ph)
+          ptx::tma_store_4d(&tm_y, ystage + ph * kStage, ph * 32, h, tok0 + t * 128, b);
+        ptx::bulk_commit();
       }
     };
 
@@ -519,15 +532,15 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       if (q + 1 < hs) in_next = fetch_head(q + 1);
       prep_head(q, in);
       const int pb = q & 1;
-      u += nHs;  // the state stages go straight to the MMA warp
       for (int xs = 0; xs < nXs; ++xs, ++u) {
         const int sl = u % nslot;
         ptx::mbar_wait(&xfull[sl], (xpar >> sl) & 1, a.err, 173);
         xpar ^= 1u << sl;
-        for (int ai = 0; ai < 2; ++ai, ++xv) {
-          const int ja = 2 * xs + ai;
+        // both 32-token atoms of the stage, then one proxy fence for the two
+        for (int ai = 0; ai < 2; ++ai) {
+          const int ja = 2 * xs + ai, xa = xv + ai;
           // the MMAs that read this Xh^T buffer last are done
-          ptx::mbar_wait(&xh_free[xv % kXh], ((xv / kXh) & 1) ^ 1, a.err, 174);
+          ptx::mbar_wait(&xh_free[xa % kXh], ((xa / kXh) & 1) ^ 1, a.err, 174);
           const uint8_t *src = slot_ptr(u) + (pc >> 2) * 8192 + ai * 4096;
           const uint4 q0 = *reinterpret_cast<const uint4 *>(src + sw128(jl, (pc & 3) * 32));
           const uint4 q1 = *reinterpret_cast<const uint4 *>(src + sw128(jl, (pc & 3) * 32 + 16));
@@ -543,22 +556,26 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
                               __uint_as_float(q0.z), __uint_as_float(q0.w),
                               __uint_as_float(q1.x), __uint_as_float(q1.y),
                               __uint_as_float(q1.z), __uint_as_float(q1.w)};
-          uint8_t *dst = xh + (xv % kXh) * kXAtom;
+          uint8_t *dst = xh + (xa % kXh) * kXAtom;
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             *reinterpret_cast<uint32_t *>(dst + sw128(8 * pc + e, jl * 4)) = to_tf32(v[e] * w);
-          ptx::fence_async_smem();
-          warp_arrive(&xh_ready[xv % kXh]);
         }
+        ptx::fence_async_smem();
+        warp_arrive(&xh_ready[xv % kXh]);
+        warp_arrive(&xh_ready[(xv + 1) % kXh]);
+        xv += 2;
         // this warp has read the landed stage: it may be refilled once all have
         warp_arrive(&xrel[sl]);
       }
+      u += nHs;  // the state stages go straight to the MMA warp
       if (q > 0) epilogue(q - 1, D_prev, xk_prev);
       D_prev = in.D;
 #pragma unroll
       for (int m = 0; m < 8; ++m) xk_prev[m] = xk[m];
     }
     if (hs > 0) epilogue(hs - 1, D_prev, xk_prev);
+    if (tid == 0) ptx::bulk_wait<0>();  // every y store complete
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -568,13 +585,14 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
 struct OutSmem32 {
   int nslot, smem;
 };
-// The ring and the Xh^T buffers within 220 KB of dynamic shared memory (1 KB
-// of it alignment slack; the static arrays, about 7 KB, sit beside it).
+// The ring, the Xh^T buffers and the y staging within 220 KB of dynamic
+// shared memory (1 KB of it alignment slack; the static arrays, about 7 KB,
+// sit beside it).
 OutSmem32 out_smem32(const Dims &) {
   OutSmem32 m;
-  const int room = (220 * 1024 - 1024 - kXh * kXAtom) / kStage;
+  const int room = (220 * 1024 - 1024 - kXh * kXAtom - 2 * kStage) / kStage;
   m.nslot = std::min(kMaxSlots, room);
-  m.smem = m.nslot * kStage + kXh * kXAtom + 1024;
+  m.smem = m.nslot * kStage + kXh * kXAtom + 2 * kStage + 1024;
   return m;
 }
 
@@ -619,10 +637,11 @@ cudaError_t launch_fwd_out_tf32(const Dims &d, const float *x, const float *B, c
                                 const float *dt, const float *G, const float *states,
                                 const float *D, float *y, int hs, int *err, cudaStream_t st) {
   if (!fwd_out_tf32_heads_ok(d, hs)) return cudaErrorInvalidValue;
-  CUtensorMap tC, tB, tx, tS;
+  CUtensorMap tC, tB, tx, tS, tY;
   if (!make_tmap_bl(&tC, C, false, d.b, d.L, d.ng, d.S, 128) ||
       !make_tmap_bl(&tB, B, false, d.b, d.L, d.ng, d.S, 128) ||
-      !make_tmap_bl(&tx, x, false, d.b, d.L, d.nh, d.P, 64))
+      !make_tmap_bl(&tx, x, false, d.b, d.L, d.nh, d.P, 64) ||
+      !make_tmap_bl(&tY, y, false, d.b, d.L, d.nh, d.P, 128))
     return cudaErrorInvalidValue;
   {
     // start states as [b * nh * nc][P][S] fp32; one box = 64 rows of P x 32 of S
@@ -665,7 +684,7 @@ cudaError_t launch_fwd_out_tf32(const Dims &d, const float *x, const float *B, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tC, tB, tx, tS, a);
+  return cudaLaunchKernelEx(&cfg, kernel, tC, tB, tx, tS, tY, a);
 }
 
 }  // namespace ssd
