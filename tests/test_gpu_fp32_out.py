@@ -1,7 +1,9 @@
-"""The fp32 output kernel (fwd_out_tf32: kind::tf32 MMAs, the masked C B^T of a
-128-row tile shared by a slice of heads, the in-chunk decay factored about
-one anchor per chunk and head, an exact per-element path for steep chunks)
-through ssd_forward with fp32 I/O, against the oracle: every supported
+"""The fp32 kernels (fwd_chunk_state_tf32: the chunk jump terms with every
+landed box transposed in place for kind::tf32; fwd_out_tf32: the masked
+C B^T of a 128-row tile shared by a slice of heads, the in-chunk decay
+factored about one anchor per chunk and head, an exact per-element path for
+steep chunks) through ssd_forward with fp32 I/O, against the oracle: every
+supported
 dstate and chunk size, ragged last chunks, several groups, with and without
 h0, and chunks steep enough to need the exact path (alone and beside
 ordinary heads of the same CTA).  The relative error of y - D x is checked
@@ -37,6 +39,10 @@ CASES = [
     # the second row tile of the last chunk lies past the sequence
     W.Workload("fp32_short_tail", 1, 600, 4, 64, 128, 1, 256, "fp32", True),
     W.Workload("fp32_one_token", 1, 1, 2, 64, 128, 1, 256, "fp32", True),
+    # the tf32 chunk-jump kernel with two slices of S and one head per item
+    # (three heads per group), beside the step output kernel
+    W.Workload("fp32_S256_hpg3", 1, 700, 3, 64, 256, 1, 256, "fp32", True),
+    W.Workload("fp32_S256_T128_g2", 2, 333, 4, 64, 256, 2, 128, "fp32", False),
 ]
 
 
