@@ -59,9 +59,8 @@ constexpr int kP = 64;
 constexpr int kStage = 16384;     // one ring stage: C or B (128 rows x 32 fp32 of
                                   // S), two state atoms, or 64 tokens of x
 constexpr int kHAtom = 64 * 128;  // start state: 64 rows p x 32 fp32 of S
-constexpr int kXAtom = 64 * 128;  // Xh^T: 64 rows p x 32 tokens
+constexpr int kXAtom = 64 * 128;  // x of 32 tokens: two 32 x 32 boxes (p halves)
 constexpr int kMaxSlots = 12;
-constexpr int kXh = 4;            // Xh^T atoms in flight
 constexpr float kSpanMax = 180.f;
 constexpr float kMinFactor = 7.52316384526264e-37f;  // 2^-120
 
@@ -89,13 +88,13 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   // full: a state stage landed (MMA waits); xfull: a C, B or x stage landed
-  // (row warps wait); scaled: the row warps rounded a B stage; empty: the
-  // MMAs reading a B or state stage are done; xrel: every row warp is done
-  // with a C or x stage; c_ready: C is in tensor memory; xh_ready / xh_free:
-  // an Xh^T atom written / read
+  // (row warps wait); scaled: the row warps rounded a B stage or transposed
+  // an x stage in place; empty: the MMAs reading a B, x or state stage are
+  // done; xrel: every row warp is done with a C stage; c_ready: C is in
+  // tensor memory
   __shared__ __align__(8) uint64_t c_ready, full[kMaxSlots], xfull[kMaxSlots],
       scaled[kMaxSlots], empty[kMaxSlots], xrel[kMaxSlots], sc_done, pack_done, acc_full[2],
-      acc_free[2], xh_ready[kXh], xh_free[kXh];
+      acc_free[2];
   __shared__ uint32_t tmem_slot;
   // per head (by head parity): G and dt of every token, v_j, alpha, path
   __shared__ __align__(16) float Gs[2][256];
@@ -119,8 +118,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
   const int nJ = 4 * (t + 1);        // 32-token atoms of the in-chunk sum
   const int nXs = nJ / 2;            // x stages per head (64 tokens each)
   uint8_t *ring = smem;
-  uint8_t *xh = ring + nslot * kStage;
-  uint8_t *ystage = xh + kXh * kXAtom;  // y of one head: two 16 KB boxes
+  uint8_t *ystage = ring + nslot * kStage;  // y of one head: two 16 KB boxes
   auto slot_ptr = [&](int u) { return ring + (u % nslot) * kStage; };
 
   if (tid == 0) {
@@ -137,10 +135,6 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&acc_full[i], 1);
       ptx::mbar_init(&acc_free[i], kRowWarps);
-    }
-    for (int i = 0; i < kXh; ++i) {
-      ptx::mbar_init(&xh_ready[i], kRowWarps);
-      ptx::mbar_init(&xh_free[i], 1);
     }
     ptx::fence_mbar_init();
   }
@@ -204,13 +198,15 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       const int h = hbase + q;
       const int row = (b * nh + h) * a.nc + k;  // this head's start state
       for (int xs = 0; xs < nXs; ++xs, ++u) {
-        acquire(162, true);
+        acquire(162, false);
         if (leader) {
-          // two boxes of 64 tokens x 32 p (p halves), 8 KB each
+          // four boxes of 32 tokens x 32 p: token half ai, p half ph at
+          // ai * 8 KB + ph * 4 KB
           ptx::mbar_arrive_expect_tx(&xfull[u % nslot], kStage);
-          for (int ph = 0; ph < 2; ++ph)
-            ptx::tma_load_4d(slot_ptr(u) + ph * 8192, &tm_x, ph * 32, h, tok0 + xs * 64, b,
-                             &xfull[u % nslot]);
+          for (int ai = 0; ai < 2; ++ai)
+            for (int ph = 0; ph < 2; ++ph)
+              ptx::tma_load_4d(slot_ptr(u) + ai * kXAtom + ph * 4096, &tm_x, ph * 32, h,
+                               tok0 + xs * 64 + ai * 32, b, &xfull[u % nslot]);
         }
         __syncwarp();
       }
@@ -258,35 +254,36 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     __syncwarp();
     const uint32_t idY = ptx::idesc_tf32(128, kP, false, false);
     ptx::mbar_wait(&pack_done, 0, a.err, 165);
-    int xv = 0;  // Xh^T atoms consumed so far
     for (int q = 0; q < hs; ++q) {
       const int set = q & 1;
       if (q >= 2) ptx::mbar_wait(&acc_free[set], ((q >> 1) - 1) & 1, a.err, 166);
       ptx::tc_fence_after();
-      // Acc = (C B^T masked) Xh over the Xh^T atoms first (none for a steep
-      // head, whose epilogue forms the in-chunk sum itself), so that the row
-      // warps' atoms never wait on a state stage
+      // Acc = (C B^T masked) Xh over the x stages first (transposed in place
+      // by the row warps; no MMA for a steep head, whose epilogue forms the
+      // in-chunk sum itself)
       bool steep = false;
-      for (int ja = 0; ja < nJ; ++ja, ++xv) {
-        const int xs = xv % kXh;
-        ptx::mbar_wait(&xh_ready[xs], (xv / kXh) & 1, a.err, 168);
+      for (int xs = 0; xs < nXs; ++xs, ++u) {
+        const int sl = u % nslot;
+        ptx::mbar_wait(&scaled[sl], (spar >> sl) & 1, a.err, 168);
+        spar ^= 1u << sl;
         ptx::tc_fence_after();
         steep = steeps[q & 1] != 0;
         if (leader) {
           if (!steep) {
-            const uint32_t x0 = ptx::smem_u32(xh + xs * kXAtom);
+            const uint32_t x0 = ptx::smem_u32(slot_ptr(u));
+            for (int ai = 0; ai < 2; ++ai)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t xd = ptx::smem_desc(x0 + kk * 32, 16, 1024, ptx::kSw128);
-              ptx::mma_ts_tf32(tmem + acc_col(set), tmem + ja * 32 + kk * 8, xd, idY,
-                               (ja | kk) ? 1u : 0u);
-            }
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t xd =
+                    ptx::smem_desc(x0 + ai * kXAtom + kk * 32, 16, 1024, ptx::kSw128);
+                ptx::mma_ts_tf32(tmem + acc_col(set), tmem + (2 * xs + ai) * 32 + kk * 8, xd,
+                                 idY, (xs | ai | kk) ? 1u : 0u);
+              }
           }
-          ptx::mma_commit(&xh_free[xs]);
+          ptx::mma_commit(&empty[sl]);
         }
         __syncwarp();
       }
-      u += nXs;  // the x stages went to the row warps
       // Acc += C (2^alpha h)^T over the state stages (the first MMA of a
       // steep head starts the accumulator)
       for (int hh = 0; hh < nHs; ++hh, ++u) {
@@ -429,7 +426,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       }
       ptx::named_bar_sync(1, kRowThreads);
       if (tid == 0) {
-        // read by the MMA warp after this thread's next arrival on xh_ready,
+        // read by the MMA warp after this thread's next arrival on scaled,
         // and by the epilogue of head q, behind head q + 1's barriers
         int okall = 1;
 #pragma unroll
@@ -522,8 +519,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
 
     // Per head q: its factors, the transposition of its x atoms into Xh^T,
     // then the previous head's epilogue (head q's MMAs overlap it).
-    const int jl = tid & 31, pc = tid >> 5;  // token of an atom, 8-column group of p
-    int xv = 0;                              // Xh^T atoms written so far
+    const int jl = tid & 31, pc = tid >> 5;  // a box's row (token) and 16-byte piece
     HeadIn in_next = fetch_head(0);
     float D_prev = 0.f;
     uint4 xk[8], xk_prev[8];  // this thread's x row segment (head q, head q - 1)
@@ -536,37 +532,37 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
         const int sl = u % nslot;
         ptx::mbar_wait(&xfull[sl], (xpar >> sl) & 1, a.err, 173);
         xpar ^= 1u << sl;
-        // both 32-token atoms of the stage, then one proxy fence for the two
-        for (int ai = 0; ai < 2; ++ai) {
-          const int ja = 2 * xs + ai, xa = xv + ai;
-          // the MMAs that read this Xh^T buffer last are done
-          ptx::mbar_wait(&xh_free[xa % kXh], ((xa / kXh) & 1) ^ 1, a.err, 174);
-          const uint8_t *src = slot_ptr(u) + (pc >> 2) * 8192 + ai * 4096;
-          const uint4 q0 = *reinterpret_cast<const uint4 *>(src + sw128(jl, (pc & 3) * 32));
-          const uint4 q1 = *reinterpret_cast<const uint4 *>(src + sw128(jl, (pc & 3) * 32 + 16));
-          if (ja == 4 * t + quad) {
-            // the atom holding this warp's rows: keep the row segment for D x_i
-            const uint8_t *xr = slot_ptr(u) + half * 8192 + ai * 4096;
+        uint8_t *st = slot_ptr(u);
+        // read: this thread's 16-byte piece of row jl of the four boxes, and
+        // the warp's own rows for D x_i (raw) when they lie in this stage
+        float4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          v[i] = *reinterpret_cast<const float4 *>(st + i * 4096 + sw128(jl, pc * 16));
+#pragma unroll
+        for (int ai = 0; ai < 2; ++ai)
+          if (2 * xs + ai == 4 * t + quad) {
+            const uint8_t *xr = st + ai * kXAtom + half * 4096;
 #pragma unroll
             for (int m = 0; m < 8; ++m)
               xk[m] = *reinterpret_cast<const uint4 *>(xr + sw128(tid & 31, m * 16));
           }
-          const float w = vs[pb][ja * 32 + jl];
-          const float v[8] = {__uint_as_float(q0.x), __uint_as_float(q0.y),
-                              __uint_as_float(q0.z), __uint_as_float(q0.w),
-                              __uint_as_float(q1.x), __uint_as_float(q1.y),
-                              __uint_as_float(q1.z), __uint_as_float(q1.w)};
-          uint8_t *dst = xh + (xa % kXh) * kXAtom;
+        // every row thread has read before any writes (in place)
+        ptx::named_bar_sync(3, kRowThreads);
+        // write: element (token jl, p columns 4 pc .. +3 of box (ai, ph)) to
+        // (rows 4 pc .. +3, column jl), scaled by v_j and rounded: each
+        // 32-token atom becomes K-major Xh^T, 64 rows of p
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            *reinterpret_cast<uint32_t *>(dst + sw128(8 * pc + e, jl * 4)) = to_tf32(v[e] * w);
+        for (int i = 0; i < 4; ++i) {
+          const float w = vs[pb][(2 * xs + (i >> 1)) * 32 + jl];
+          const float e4[4] = {v[i].x * w, v[i].y * w, v[i].z * w, v[i].w * w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<uint32_t *>(st + i * 4096 + sw128(4 * pc + e, jl * 4)) =
+                to_tf32(e4[e]);
         }
         ptx::fence_async_smem();
-        warp_arrive(&xh_ready[xv % kXh]);
-        warp_arrive(&xh_ready[(xv + 1) % kXh]);
-        xv += 2;
-        // this warp has read the landed stage: it may be refilled once all have
-        warp_arrive(&xrel[sl]);
+        warp_arrive(&scaled[sl]);
       }
       u += nHs;  // the state stages go straight to the MMA warp
       if (q > 0) epilogue(q - 1, D_prev, xk_prev);
@@ -585,14 +581,14 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
 struct OutSmem32 {
   int nslot, smem;
 };
-// The ring, the Xh^T buffers and the y staging within 220 KB of dynamic
+// The ring and the y staging within 220 KB of dynamic
 // shared memory (1 KB of it alignment slack; the static arrays, about 7 KB,
 // sit beside it).
 OutSmem32 out_smem32(const Dims &) {
   OutSmem32 m;
-  const int room = (220 * 1024 - 1024 - kXh * kXAtom - 2 * kStage) / kStage;
+  const int room = (220 * 1024 - 1024 - 2 * kStage) / kStage;
   m.nslot = std::min(kMaxSlots, room);
-  m.smem = m.nslot * kStage + kXh * kXAtom + 2 * kStage + 1024;
+  m.smem = m.nslot * kStage + 2 * kStage + 1024;
   return m;
 }
 
@@ -640,7 +636,7 @@ cudaError_t launch_fwd_out_tf32(const Dims &d, const float *x, const float *B, c
   CUtensorMap tC, tB, tx, tS, tY;
   if (!make_tmap_bl(&tC, C, false, d.b, d.L, d.ng, d.S, 128) ||
       !make_tmap_bl(&tB, B, false, d.b, d.L, d.ng, d.S, 128) ||
-      !make_tmap_bl(&tx, x, false, d.b, d.L, d.nh, d.P, 64) ||
+      !make_tmap_bl(&tx, x, false, d.b, d.L, d.nh, d.P, 32) ||
       !make_tmap_bl(&tY, y, false, d.b, d.L, d.nh, d.P, 128))
     return cudaErrorInvalidValue;
   {
