@@ -607,9 +607,15 @@ bool fwd_out_tf32_heads_ok(const Dims &d, int hs) {
          (d.nh / hs) * (d.T / 128) <= 65535;
 }
 
-// Heads per CTA: the divisor of the heads per group minimising the bytes the
-// busiest SM moves (waves of CTAs times a CTA's loads: C and B of the tile
-// once, per head its state, x and y).
+// Heads per CTA: the divisor of the heads per group minimising the busiest
+// SM's cost, waves of CTAs times a CTA's cost: its loads (C and B of the tile
+// once, per head its state, x and y) plus a fixed start-up of about 8 us (C
+// and B of the tile must arrive, C B^T be formed and masked before the first
+// head; counted as the 192 KB an SM streams in that time), 10% more when
+// there are fewer than three waves of CTAs (the longer second row tile of a
+// chunk then balances out less well).  Measured on the fp32 sweep (b2 h32
+// S128 L16384 T256): 4 / 8 / 16 / 32 heads per CTA take 329 / 270 / 250 /
+// 266 us; the model picks 16.
 int fwd_out_tf32_heads(const Dims &d) {
   const int64_t sms = sm_count();
   const int nT = (int)(d.T / 128);
@@ -618,9 +624,9 @@ int fwd_out_tf32_heads(const Dims &d) {
   for (int hs = 1; hs <= d.hpg; ++hs) {
     if (!fwd_out_tf32_heads_ok(d, hs)) continue;
     const int64_t ctas = d.b * d.nc * nT * (d.nh / hs);
-    const double per_cta = 4.0 * (128.0 * d.S + d.T * d.S) +
+    const double per_cta = 192.0 * 1024 + 4.0 * (128.0 * d.S + d.T * d.S) +
                            hs * 4.0 * (d.S * 64.0 + d.T * 64.0 + 128.0 * 64.0);
-    const double cost = (double)((ctas + sms - 1) / sms) * per_cta;
+    const double cost = (double)((ctas + sms - 1) / sms) * per_cta * (ctas < 3 * sms ? 1.1 : 1.0);
     if (cost < best_cost * 0.999) {
       best_cost = cost;
       best = hs;
