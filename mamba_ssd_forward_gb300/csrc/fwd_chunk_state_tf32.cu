@@ -24,8 +24,8 @@
 // and item j - 1 is written out.  Warp roles:
 //   warp 8 (TMA):  per stage, B (four boxes of 32 tokens x 32 s) and each
 //                  head's x (two boxes of 32 tokens x 32 p);
-//   warp 9 (MMA):  per stage four K = 8 steps of D[s][(head, p)] into the
-//                  item's accumulator set;
+//   warp 9 (MMA):  per stage four K = 8 steps of D[s][(head, p)] (N = H P,
+//                  up to 256) into the item's accumulator set;
 //   warps 0-7:     per item the heads' jump weights, per stage the in-place
 //                  transposition, per item the previous item's epilogue
 //                  (thread = s: stores along s are coalesced).
@@ -42,7 +42,7 @@ constexpr int kProducerWarp = kRowWarps, kMmaWarp = kRowWarps + 1;
 constexpr int kP = 64;
 constexpr int kKB = 32;         // tokens per stage (one K atom of tf32)
 constexpr int kBox = 32 * 128;  // one 32 x 32 fp32 box
-constexpr int kMaxH = 2;        // heads per item
+constexpr int kMaxH = 4;        // heads per item
 constexpr int kMaxSt = 8;       // ring stages (at most)
 
 struct CsArgs32 {
@@ -99,7 +99,7 @@ fwd_chunk_state_tf32(const __grid_constant__ CUtensorMap tm_B,
     ptx::fence_mbar_init();
   }
   if (warp == kMmaWarp) {
-    ptx::tmem_alloc(&tmem_slot, 256);
+    ptx::tmem_alloc(&tmem_slot, 2 * HP <= 256 ? 256 : 512);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -279,10 +279,14 @@ fwd_chunk_state_tf32(const __grid_constant__ CUtensorMap tm_B,
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, 256);
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, 2 * HP <= 256 ? 256 : 512);
 }
 
-int cs32_heads(const Dims &d) { return d.hpg % 2 == 0 ? 2 : 1; }
+// Heads per item: four when the group allows (B is loaded once per four
+// heads; 95 us against 127 with two on the fp32 sweep b2 h32 S128 L16384
+// T256), else two or
+// one.
+int cs32_heads(const Dims &d) { return d.hpg % 4 == 0 ? 4 : d.hpg % 2 == 0 ? 2 : 1; }
 
 int cs32_stages(const Dims &d) {
   const int stage_bytes = 4 * kBox + cs32_heads(d) * 2 * kBox;
