@@ -99,11 +99,12 @@ def kernel_names(w: W.Workload, plan: dict | None = None) -> list:
     or fwd_scan (0)."""
     names = list(KERNEL_NAMES[w.dtype])
     if w.dtype == "fp32" and w.headdim == 64 and w.chunk in (128, 256):
-        # the warp-specialised fp32 kernels where the shape allows
-        if w.dstate % 128 == 0:
-            names[1] = "fwd_chunk_state_tf32"
+        # the warp-specialised fp32 kernels where the shape allows (the
+        # chunk-jump one forms the cumsum itself: one launch less)
         if w.dstate % 32 == 0 and w.dstate <= 128:
             names[3] = "fwd_out_tf32"
+        if w.dstate % 128 == 0:
+            names = ["fwd_chunk_state_tf32"] + names[2:]
     if w.dtype == "bf16" and plan is not None:
         names[2] = {0: "fwd_scan", 1: "fwd_scan_chunk", 2: "fwd_scan_chunk",
                     3: "fwd_out"}[plan["scan_kernel"]]
@@ -125,7 +126,7 @@ def kernel_method_bytes(w: W.Workload) -> dict:
            "fwd_state_pass": h0 + fin,
            "chunk_cumsum": dt + w.nheads * 4,
            "chunk_state": x + bc + dt,
-           "fwd_chunk_state_tf32": x + bc + dt,
+           "fwd_chunk_state_tf32": x + bc + dt + w.nheads * 4,
            "state_passing": h0 + fin,
            "chunk_scan": 2 * x + 2 * bc + dt + 2 * w.nheads * 4}
     for k in ("fwd_scan", "fwd_scan_chunk", "fwd_out", "fwd_out_tf32"):
@@ -160,7 +161,7 @@ def kernel_bytes(w: W.Workload) -> dict:
         "fwd_out": 2 * x + 2 * bc + dt + 2 * w.nheads * 4 + st16 + anc + uv,
         "chunk_cumsum": dt + G + w.nheads * 4,
         "chunk_state": x + bc + dt + G + st,
-        "fwd_chunk_state_tf32": x + bc + dt + G + st,
+        "fwd_chunk_state_tf32": x + bc + dt + w.nheads * 4 + G + st,
         "state_passing": 2 * st + w.batch * w.nheads * w.nchunks * 4 + fin * (2 if w.has_h0 else 1),
         "chunk_scan": 2 * x + 2 * bc + dt + G + st + w.nheads * 4,
         "fwd_out_tf32": 2 * x + 2 * bc + dt + G + st + 2 * w.nheads * 4,

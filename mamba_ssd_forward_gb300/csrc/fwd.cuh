@@ -87,12 +87,13 @@ cudaError_t launch_fwd_out_tf32(const Dims &d, const float *x, const float *B, c
                                 const float *D, float *y, int hs, int *err, cudaStream_t st);
 
 // fwd_chunk_state_tf32: the chunk jump terms for fp32 I/O (kind::tf32),
-// dstates [b, nh, nc, P, S] fp32 from x, B, dt and G (fp32, log2 units, [b,
-// nh, nc * T]); P = 64, S a multiple of 128, T in {128, 256}.
+// dstates [b, nh, nc, P, S] fp32 from x, B, dt and A, writing the in-chunk
+// cumsums G (fp32, log2 units, [b, nh, nc * T]) it forms on the way; P = 64,
+// S a multiple of 128, T in {128, 256}.
 bool fwd_chunk_state_tf32_supported(const Dims &d);
 cudaError_t launch_fwd_chunk_state_tf32(const Dims &d, const float *x, const float *B,
-                                        const float *dt, const float *G, float *dstates,
-                                        int *err, cudaStream_t st);
+                                        const float *dt, const float *A, float *G,
+                                        float *dstates, int *err, cudaStream_t st);
 
 // Heads per CTA of fwd_scan: the largest divisor of nheads/ngroups that is
 // at most 4 and keeps heads * P <= 256 tensor-memory columns.

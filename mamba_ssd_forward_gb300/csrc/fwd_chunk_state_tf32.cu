@@ -5,8 +5,9 @@
 //
 // ("Accelerating Mamba-2 with High-Performance Forward Pass Kernels in NVIDIA
 // CUDA Tile", section "Mamba-2 architecture": the second term of the
-// log-space jump h_{t+T} = exp(G_last) h_t + (exp(G_last - G) B)^T X), with G
-// the in-chunk cumsum in log2 units from the cumsum step.  The fp32 twin of
+// log-space jump h_{t+T} = exp(G_last) h_t + (exp(G_last - G) B)^T X, with G
+// the in-chunk cumsum of A dt of "Kernel 1", in log2 units, computed here
+// and written out for the state pass and the output pass).  The fp32 twin of
 // fwd_chunk_state.cu: the same contraction as an M = 128 (s) x N = H P MMA
 // over the chunk's tokens, with H heads of one group sharing each load of B.
 //
@@ -26,7 +27,9 @@
 //                  head's x (two boxes of 32 tokens x 32 p);
 //   warp 9 (MMA):  per stage four K = 8 steps of D[s][(head, p)] (N = H P,
 //                  up to 256) into the item's accumulator set;
-//   warps 0-7:     per item the heads' jump weights, per stage the in-place
+//   warps 0-7:     per item the heads' in-chunk cumsums (written to G once,
+//                  by the items of the first slice of S) and jump weights,
+//                  per stage the in-place
 //                  transposition, per item the previous item's epilogue
 //                  (thread = s: stores along s are coalesced).
 // Supported: P = 64, S a multiple of 128, T in {128, 256}.
@@ -46,7 +49,8 @@ constexpr int kMaxH = 4;        // heads per item
 constexpr int kMaxSt = 8;       // ring stages (at most)
 
 struct CsArgs32 {
-  const float *dt, *G;
+  const float *dt, *A;
+  float *G;  // in-chunk cumsums out, log2 units, [b, nh, nc * T]
   float *dstates;
   int *err;
   int L, nh, S, hpg, T, nc, nb, H, n_st, n_hg, nst, n_items;
@@ -79,6 +83,7 @@ fwd_chunk_state_tf32(const __grid_constant__ CUtensorMap tm_B,
       acc_free[2];
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(16) float ws[2][kMaxH][256];  // jump weights, by item parity
+  __shared__ float warp_tot[2][kMaxH][kRowWarps];     // cumsum partials, by item parity
 
   const int L = a.L, nh = a.nh, S = a.S, H = a.H, nst = a.nst, nc = a.nc;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -178,26 +183,23 @@ fwd_chunk_state_tf32(const __grid_constant__ CUtensorMap tm_B,
       __syncwarp();
       if ((tid & 31) == 0) ptx::mbar_arrive(bar);
     };
-    // the G and dt of thread = token tid for the H heads of an item, one
-    // item ahead
+    // dt of thread = token tid and A for the H heads of an item, one item
+    // ahead
     struct ItemIn {
-      float Gj[kMaxH], Glast[kMaxH], dtj[kMaxH];
+      float Aq[kMaxH], dtj[kMaxH];
     };
     auto fetch_item = [&](int item) {
       ItemIn in;
 #pragma unroll
-      for (int q = 0; q < kMaxH; ++q) in.Gj[q] = in.Glast[q] = in.dtj[q] = 0.f;
+      for (int q = 0; q < kMaxH; ++q) in.Aq[q] = in.dtj[q] = 0.f;
       if (item >= a.n_items) return in;
       const Item32 it = decode32(item, a);
       const int tok0 = it.k * kT, valid = min(kT, L - tok0);
 #pragma unroll
       for (int q = 0; q < kMaxH; ++q) {
         const int h = it.hbase + q;
-        const int64_t g0 = (((int64_t)it.b * nh + h) * nc + it.k) * kT;
-        if (q < H && SSD_IN_BOUNDS(h < nh && it.b < a.nb && g0 + kT <= (int64_t)a.nb * nh * nc * kT,
-                                   a.err, 180)) {
-          if (tid < kT) in.Gj[q] = a.G[g0 + tid];
-          in.Glast[q] = a.G[g0 + kT - 1];
+        if (q < H && SSD_IN_BOUNDS(h < nh && it.b < a.nb, a.err, 180)) {
+          in.Aq[q] = a.A[h];
           if (tid < valid) in.dtj[q] = a.dt[((int64_t)it.b * L + tok0 + tid) * nh + h];
         }
       }
@@ -236,13 +238,42 @@ fwd_chunk_state_tf32(const __grid_constant__ CUtensorMap tm_B,
       const ItemIn in = in_next;
       in_next = fetch_item(item + gridDim.x);  // in flight while this item runs
       float(*w)[256] = ws[jl & 1];
-      // the weights of the item's heads (thread = token); the stage barriers
-      // of the previous item keep every thread past its last use of this
-      // parity's weights (item jl - 2) before they are overwritten
+      float(*wt)[kRowWarps] = warp_tot[jl & 1];
+      // the in-chunk cumsums of the item's heads (thread = token; a padding
+      // token adds zero, so the chunk total is G at its last real token) and
+      // the jump weights.  The stage barriers of the previous item keep every
+      // thread past its last use of this parity's arrays (item jl - 2) before
+      // they are overwritten.
+      float incl[kMaxH];
 #pragma unroll
-      for (int q = 0; q < kMaxH; ++q)
-        if (q < H && tid < kT)
-          w[q][tid] = tid < valid ? exp2f(in.Glast[q] - in.Gj[q]) * in.dtj[q] : 0.f;
+      for (int q = 0; q < kMaxH; ++q) {
+        incl[q] = in.Aq[q] * kLog2e * in.dtj[q];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float o = __shfl_up_sync(0xffffffffu, incl[q], off);
+          if ((tid & 31) >= off) incl[q] += o;
+        }
+        if ((tid & 31) == 31 && q < H) wt[q][warp] = incl[q];
+      }
+      ptx::named_bar_sync(1, kRowThreads);
+#pragma unroll
+      for (int q = 0; q < kMaxH; ++q) {
+        if (q >= H) break;
+        float base = 0.f, tot = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kRowWarps; ++w2) {
+          const float t2 = wt[q][w2];
+          tot += t2;
+          if (w2 < warp) base += t2;
+        }
+        const float Gj = base + incl[q];
+        if (tid < kT) {
+          w[q][tid] = tid < valid ? exp2f(tot - Gj) * in.dtj[q] : 0.f;
+          const int64_t g0 = (((int64_t)it.b * nh + it.hbase + q) * nc + it.k) * kT;
+          if (it.st == 0 && SSD_IN_BOUNDS(g0 + kT <= (int64_t)a.nb * nh * nc * kT, a.err, 185))
+            a.G[g0 + tid] = Gj;
+        }
+      }
       ptx::named_bar_sync(1, kRowThreads);
 
       for (int kb = 0; kb < nkb; ++kb, ++u) {
@@ -300,8 +331,8 @@ bool fwd_chunk_state_tf32_supported(const Dims &d) {
 }
 
 cudaError_t launch_fwd_chunk_state_tf32(const Dims &d, const float *x, const float *B,
-                                        const float *dt, const float *G, float *dstates,
-                                        int *err, cudaStream_t st) {
+                                        const float *dt, const float *A, float *G,
+                                        float *dstates, int *err, cudaStream_t st) {
   if (!fwd_chunk_state_tf32_supported(d)) return cudaErrorInvalidValue;
   CUtensorMap tB, tx;
   if (!make_tmap_bl(&tB, B, false, d.b, d.L, d.ng, d.S, kKB) ||
@@ -314,6 +345,7 @@ cudaError_t launch_fwd_chunk_state_tf32(const Dims &d, const float *x, const flo
   if (e != cudaSuccess) return e;
   CsArgs32 a;
   a.dt = dt;
+  a.A = A;
   a.G = G;
   a.dstates = dstates;
   a.err = err;

@@ -412,16 +412,18 @@ ssd_status forward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
     float *G = reinterpret_cast<float *>(ws + w.G);
     float *dst = reinterpret_cast<float *>(ws + w.dstates);
     float *sts = reinterpret_cast<float *>(ws + w.states);
-    if (e == cudaSuccess) e = ssd::launch_chunk_cumsum(d, dtype, dt, A, G, err, st);
-    if (e == cudaSuccess && ++launched) e = mark(launched);
-    // the chunk jump terms: the warp-specialised tf32 kernel where the shape
-    // allows, else the step kernel
-    if (e == cudaSuccess)
-      e = ssd::fwd_chunk_state_tf32_supported(d)
-              ? ssd::launch_fwd_chunk_state_tf32(d, static_cast<const float *>(x),
-                                                 static_cast<const float *>(B),
-                                                 static_cast<const float *>(dt), G, dst, err, st)
-              : ssd::launch_chunk_state(d, dtype, x, B, dt, G, dst, err, st);
+    // the cumsum and the chunk jump terms: the warp-specialised tf32 kernel,
+    // which forms G itself, where the shape allows; else the two step kernels
+    if (ssd::fwd_chunk_state_tf32_supported(d)) {
+      if (e == cudaSuccess)
+        e = ssd::launch_fwd_chunk_state_tf32(d, static_cast<const float *>(x),
+                                             static_cast<const float *>(B),
+                                             static_cast<const float *>(dt), A, G, dst, err, st);
+    } else {
+      if (e == cudaSuccess) e = ssd::launch_chunk_cumsum(d, dtype, dt, A, G, err, st);
+      if (e == cudaSuccess && ++launched) e = mark(launched);
+      if (e == cudaSuccess) e = ssd::launch_chunk_state(d, dtype, x, B, dt, G, dst, err, st);
+    }
     if (e == cudaSuccess && ++launched) e = mark(launched);
     // the output pass: the warp-specialised tf32 kernel where the shape
     // allows (it reads the stored states rounded to tf32), else the step
