@@ -6,8 +6,11 @@
 //
 // A bandwidth kernel: each thread owns four consecutive elements of one
 // (batch, head) state and walks the chunks; one read of dstates, one write
-// of states.  The loads of the next chunk's dstates are issued before the
-// current chunk's stores so that each thread keeps two loads in flight.
+// of states.  The chunks go in groups of eight, the next group's loads in
+// flight while the current group is consumed; the CTA's (decay, scale) pairs
+// are formed once per 256 chunks in shared memory.  Launched with
+// programmatic stream serialisation: it waits on the device before reading
+// what the chunk-state step wrote.
 // With tf32_out (the fp32 forward, whose output kernel fwd_out_tf32 reads
 // the stored states as tf32 MMA operands with the decay factored about
 // alpha_k = rint(G_last,k / 2)) each stored state is the carried state times
@@ -20,6 +23,7 @@ namespace ssd {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kDepth = 8;  // chunks per prefetch group
 
 __global__ void __launch_bounds__(kThreads)
 state_passing_kernel(const float4 *__restrict__ dstates,
@@ -27,39 +31,69 @@ state_passing_kernel(const float4 *__restrict__ dstates,
                      float4 *__restrict__ states, float4 *__restrict__ final_state,
                      int64_t ps4, int64_t nc, int64_t T, int64_t nbh, int tf32_out,
                      int *err) {
-  const int64_t bh = blockIdx.y;
-  const int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x;  // float4 index in P*S
-  if (e >= ps4) return;
+  __shared__ float2 gsm[256];  // per chunk: decay, stored-state scale
   // every index below lies in [0, nbh nc ps4) (states, dstates), [0, nbh
-  // ps4) (h0, final_state) or [0, nbh nc T) (G)
-  if (!SSD_IN_BOUNDS(bh < nbh && e >= 0, err, 10)) return;
+  // ps4) (h0, final_state) or [0, nbh nc T) (G) when bh < nbh and e < ps4; a
+  // thread past the state (or failing the check) works on element 0 without
+  // storing, so that it still takes part in the barriers
+  const bool ok = SSD_IN_BOUNDS((int64_t)blockIdx.y < nbh, err, 10);
+  const int64_t bh = ok ? blockIdx.y : 0;
+  const int64_t ex = (int64_t)blockIdx.x * kThreads + threadIdx.x;  // float4 index in P*S
+  const bool live = ok && ex < ps4;
+  const int64_t e = live ? ex : 0;
+  ptx::griddep_launch_dependents();  // the output pass may be scheduled now
+  // dstates and G come from the preceding kernels (and h0 may too, on the
+  // step-wise path)
+  ptx::griddep_wait();
   float4 h = h0 ? h0[bh * ps4 + e] : make_float4(0.f, 0.f, 0.f, 0.f);
   const float *Gbh = G + bh * nc * T;
   const float4 *dsrc = dstates + bh * nc * ps4 + e;
   float4 *sdst = states + bh * nc * ps4 + e;
-  float4 next = nc > 0 ? dsrc[0] : h;
-  for (int64_t k = 0; k < nc; ++k) {
-    const float4 cur = next;
-    if (k + 1 < nc) next = dsrc[(k + 1) * ps4];
-    const float Glast = Gbh[k * T + T - 1];
-    const float decay = exp2f(Glast);
-    if (tf32_out) {
-      // the factored output pass's anchor (the same rule as fwd_out_tf32)
-      const int alpha = -Glast <= 180.f ? (int)rintf(0.5f * Glast) : 0;
-      const float sc = __int_as_float((127 + alpha) << 23);  // 2^alpha, alpha in [-90, 0]
-      sdst[k * ps4] = make_float4(__uint_as_float(to_tf32(sc * h.x)),
-                                  __uint_as_float(to_tf32(sc * h.y)),
-                                  __uint_as_float(to_tf32(sc * h.z)),
-                                  __uint_as_float(to_tf32(sc * h.w)));
-    } else {
-      sdst[k * ps4] = h;
+  float4 cur[kDepth], nxt[kDepth];
+#pragma unroll
+  for (int i = 0; i < kDepth; ++i)
+    if (i < nc) cur[i] = dsrc[(int64_t)i * ps4];
+  for (int64_t k0 = 0; k0 < nc; k0 += kDepth) {
+    if ((k0 & 255) == 0) {
+      // the next 256 chunks' decays and stored-state scales.  With tf32_out
+      // the scale is 2^alpha, the factored output pass's anchor (the same
+      // rule as fwd_out_tf32; a power of two, so exact), else 1.
+      __syncthreads();
+      if (k0 + threadIdx.x < nc) {
+        const float Glast = Gbh[(k0 + threadIdx.x) * T + T - 1];
+        float sc = 1.f;
+        if (tf32_out) {
+          const int alpha = -Glast <= 180.f ? (int)rintf(0.5f * Glast) : 0;
+          sc = __int_as_float((127 + alpha) << 23);  // 2^alpha, alpha in [-90, 0]
+        }
+        gsm[threadIdx.x] = make_float2(exp2f(Glast), sc);
+      }
+      __syncthreads();
     }
-    h.x = fmaf(decay, h.x, cur.x);
-    h.y = fmaf(decay, h.y, cur.y);
-    h.z = fmaf(decay, h.z, cur.z);
-    h.w = fmaf(decay, h.w, cur.w);
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i)
+      if (k0 + kDepth + i < nc) nxt[i] = dsrc[(k0 + kDepth + i) * ps4];
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i)
+      if (k0 + i < nc) {
+        const float2 g = gsm[(k0 + i) & 255];
+        if (live) {
+          sdst[(k0 + i) * ps4] =
+              tf32_out ? make_float4(__uint_as_float(to_tf32(g.y * h.x)),
+                                     __uint_as_float(to_tf32(g.y * h.y)),
+                                     __uint_as_float(to_tf32(g.y * h.z)),
+                                     __uint_as_float(to_tf32(g.y * h.w)))
+                       : h;
+        }
+        h.x = fmaf(g.x, h.x, cur[i].x);
+        h.y = fmaf(g.x, h.y, cur[i].y);
+        h.z = fmaf(g.x, h.z, cur[i].z);
+        h.w = fmaf(g.x, h.w, cur[i].w);
+      }
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i) cur[i] = nxt[i];
   }
-  if (final_state) final_state[bh * ps4 + e] = h;
+  if (final_state && live) final_state[bh * ps4 + e] = h;
 }
 
 }  // namespace
@@ -69,13 +103,20 @@ cudaError_t launch_state_passing(const Dims &d, const float *dstates,
                                  float *states, float *final_state, int *err,
                                  cudaStream_t st, bool tf32_out) {
   const int64_t ps4 = d.P * d.S / 4;
-  dim3 grid((unsigned)((ps4 + kThreads - 1) / kThreads), (unsigned)(d.b * d.nh));
-  state_passing_kernel<<<grid, kThreads, 0, st>>>(
-      reinterpret_cast<const float4 *>(dstates), G,
-      reinterpret_cast<const float4 *>(h0), reinterpret_cast<float4 *>(states),
-      reinterpret_cast<float4 *>(final_state), ps4, d.nc, d.T, d.b * d.nh, tf32_out ? 1 : 0,
-      err);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((ps4 + kThreads - 1) / kThreads), (unsigned)(d.b * d.nh));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, state_passing_kernel, reinterpret_cast<const float4 *>(dstates),
+                            G, reinterpret_cast<const float4 *>(h0),
+                            reinterpret_cast<float4 *>(states),
+                            reinterpret_cast<float4 *>(final_state), ps4, d.nc, d.T,
+                            d.b * d.nh, tf32_out ? 1 : 0, err);
 }
 
 }  // namespace ssd
