@@ -103,7 +103,7 @@ def kernel_names(w: W.Workload, plan: dict | None = None) -> list:
         # chunk-jump one forms the cumsum itself: one launch less)
         if w.dstate % 32 == 0 and w.dstate <= 128:
             names[3] = "fwd_out_tf32"
-        if w.dstate % 128 == 0:
+        if w.dstate % 64 == 0:
             names = ["fwd_chunk_state_tf32"] + names[2:]
     if w.dtype == "bf16" and plan is not None:
         names[2] = {0: "fwd_scan", 1: "fwd_scan_chunk", 2: "fwd_scan_chunk",

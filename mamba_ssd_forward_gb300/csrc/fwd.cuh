@@ -89,7 +89,7 @@ cudaError_t launch_fwd_out_tf32(const Dims &d, const float *x, const float *B, c
 // fwd_chunk_state_tf32: the chunk jump terms for fp32 I/O (kind::tf32),
 // dstates [b, nh, nc, P, S] fp32 from x, B, dt and A, writing the in-chunk
 // cumsums G (fp32, log2 units, [b, nh, nc * T]) it forms on the way; P = 64,
-// S a multiple of 128, T in {128, 256}.
+// S a multiple of 64, T in {128, 256}.
 bool fwd_chunk_state_tf32_supported(const Dims &d);
 cudaError_t launch_fwd_chunk_state_tf32(const Dims &d, const float *x, const float *B,
                                         const float *dt, const float *A, float *G,

@@ -32,7 +32,8 @@
 //                  per stage the in-place
 //                  transposition, per item the previous item's epilogue
 //                  (thread = s: stores along s are coalesced).
-// Supported: P = 64, S a multiple of 128, T in {128, 256}.
+// Supported: P = 64, S a multiple of 64, T in {128, 256} (S = 64 runs as a
+// 128-row slice whose upper half reads zeros: TMA fills the boxes past S).
 #include "fwd.cuh"
 
 namespace ssd {
@@ -214,7 +215,9 @@ fwd_chunk_state_tf32(const __grid_constant__ CUtensorMap tm_B,
       ptx::tc_fence_after();
       const int s = it.st * 128 + quad * 32 + (tid & 31);
       const int ncol = HP / 2, c_lo = half * ncol;
-      for (int c0 = c_lo; c0 < c_lo + ncol; c0 += 16) {
+      // rows of the slice past S (S = 64: the upper half, whose B boxes were
+      // zero-filled) hold nothing to store; whole warps skip them
+      for (int c0 = c_lo; c0 < c_lo + ncol && it.st * 128 + quad * 32 < S; c0 += 16) {
         float v[16];
         ptx::tmem_ld16_sync(tmem + lane_base + set * HP + c0, v);
         const int q = c0 / kP, p0 = c0 % kP;
@@ -327,7 +330,7 @@ int cs32_stages(const Dims &d) {
 }  // namespace
 
 bool fwd_chunk_state_tf32_supported(const Dims &d) {
-  return d.P == kP && d.S % 128 == 0 && (d.T == 128 || d.T == 256) && cs32_stages(d) >= 2;
+  return d.P == kP && d.S % 64 == 0 && (d.T == 128 || d.T == 256) && cs32_stages(d) >= 2;
 }
 
 cudaError_t launch_fwd_chunk_state_tf32(const Dims &d, const float *x, const float *B,
@@ -357,7 +360,7 @@ cudaError_t launch_fwd_chunk_state_tf32(const Dims &d, const float *x, const flo
   a.nc = (int)d.nc;
   a.nb = (int)d.b;
   a.H = H;
-  a.n_st = (int)(d.S / 128);
+  a.n_st = (int)((d.S + 127) / 128);
   a.n_hg = (int)(d.nh / H);
   a.nst = nst;
   const int64_t n_items = d.b * d.nc * a.n_st * a.n_hg;
