@@ -20,6 +20,9 @@ CUDA Tile", section "Mamba-2 architecture":
 * ``backward`` -- the gradients of a loss through the recurrence (the
   adjoint recurrence token by token, numpy float64): the reference a
   backward pass will be checked against; no CUDA path computes it yet.
+  ``backward_chunked`` restates it by the chunked formulas a chunk-parallel
+  kernel would use (reverse pass over chunks, per-chunk masked products,
+  the decay gradient as a reverse cumsum of dL/dG), pinned against it.
 
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests
 (hand-worked example, brute-force unrolled sum, linear-attention, B = 0 and
@@ -31,6 +34,7 @@ special cases, and planted mistakes).
 """
 from .ssd_oracle import (  # noqa: F401
     backward,
+    backward_chunked,
     build,
     chunked,
     decode_step,

@@ -264,3 +264,76 @@ def backward(x, dt, A, B, C, D=None, h0=None, gy=None, gfinal=None):
                 G = a[t] * G                                      # dL/dh_{t-1} from h_t
             out["dh0"][bi, h] = G
     return out
+
+
+def backward_chunked(x, dt, A, B, C, D=None, h0=None, gy=None, gfinal=None, chunk=256):
+    """The gradients of ``backward`` by the chunked formulas a chunk-parallel
+    kernel would use (numpy float64; derived from the forward of
+    "Mamba-2 architecture", its chunked output equation and state jump).
+    Per (batch, head), with G the inclusive in-chunk cumsum of l_t = A dt_t,
+    h_k the state entering chunk k and R_k = dL/dh_{k+1} coming from the
+    chunks after k (R of the last chunk = gfinal):
+
+      R_{k-1} = exp(G_last) R_k + sum_{s in k} exp(G_s) gy_s c_s^T   (dh0 = R_{-1})
+      dx_t  = dt_t [sum_{s>=t} exp(G_s - G_t) (B_t . C_s) gy_s + exp(G_last - G_t) R_k B_t] + D gy_t
+      q_t   = sum_{s>=t} exp(G_s - G_t) (gy_s . x_t) C_s + exp(G_last - G_t) R_k^T x_t
+      dB_t += dt_t q_t,   dC_t += exp(G_t) h_k^T gy_t + sum_{j<=t} exp(G_t - G_j) (gy_t . x_j) dt_j B_j
+      dL/dG_i = gy_i . ysm_i - x_i . dxsm_i  (+ <R_k, h_{k+1}> at the chunk's last token)
+      eta_t = dL/dl_t = sum_{i>=t in k} dL/dG_i
+      ddt_t = A eta_t + q_t . B_t,   dA += sum_t dt_t eta_t,   dD += sum_t gy_t . x_t
+    where ysm = y - D x and dxsm = dx - D gy.  Sums over heads of a group for
+    dB and dC.  Used to pin the chunked restatement against the adjoint
+    recurrence (``backward``)."""
+    x, dt, A, B, C, D, h0, gy, gfinal = map(_f64, (x, dt, A, B, C, D, h0, gy, gfinal))
+    b, L, nh, P, S, ng = _dims(x, dt, A, B)
+    hpg = nh // ng
+    T = int(chunk)
+    nc = -(-L // T)
+    out = {"dx": np.zeros_like(x), "ddt": np.zeros_like(dt), "dA": np.zeros_like(A),
+           "dB": np.zeros_like(B), "dC": np.zeros_like(C), "dD": np.zeros(nh),
+           "dh0": np.zeros((b, nh, P, S))}
+    for bi in range(b):
+        for h in range(nh):
+            g = h // hpg
+            Dh = 0.0 if D is None else D[h]
+            spans = [(k * T, min(T, L - k * T)) for k in range(nc)]
+            G = [np.cumsum(A[h] * dt[bi, t0:t0 + v, h]) for t0, v in spans]
+            # forward: the state entering each chunk (hk[nc] = final state)
+            hk = np.zeros((nc + 1, P, S))
+            if h0 is not None:
+                hk[0] = h0[bi, h]
+            for k, (t0, v) in enumerate(spans):
+                w = np.exp(G[k][-1] - G[k]) * dt[bi, t0:t0 + v, h]
+                hk[k + 1] = np.exp(G[k][-1]) * hk[k] + \
+                    (x[bi, t0:t0 + v, h] * w[:, None]).T @ B[bi, t0:t0 + v, g]
+            # backward over chunks: R[k] = dL/dh_{k+1} from the later chunks
+            R = np.zeros((nc, P, S))
+            carry = np.zeros((P, S)) if gfinal is None else gfinal[bi, h].copy()
+            for k in range(nc - 1, -1, -1):
+                t0, v = spans[k]
+                R[k] = carry
+                carry = np.exp(G[k][-1]) * carry + \
+                    (gy[bi, t0:t0 + v, h] * np.exp(G[k])[:, None]).T @ C[bi, t0:t0 + v, g]
+            out["dh0"][bi, h] = carry
+            for k, (t0, v) in enumerate(spans):
+                Gk, GL = G[k], G[k][-1]
+                xs, gys, dts = x[bi, t0:t0 + v, h], gy[bi, t0:t0 + v, h], dt[bi, t0:t0 + v, h]
+                Bs, Cs = B[bi, t0:t0 + v, g], C[bi, t0:t0 + v, g]
+                up = np.triu(np.exp(Gk[None, :] - Gk[:, None]))   # [t, s]: exp(G_s - G_t), s >= t
+                low = np.tril(np.exp(Gk[:, None] - Gk[None, :]))  # [t, j]: exp(G_t - G_j), j <= t
+                back = np.exp(GL - Gk)[:, None]
+                dxsm = dts[:, None] * ((up * (Bs @ Cs.T)) @ gys + back * (Bs @ R[k].T))
+                q = (up * (xs @ gys.T)) @ Cs + back * (xs @ R[k])
+                ysm = np.exp(Gk)[:, None] * (Cs @ hk[k].T) + \
+                    ((low * (Cs @ Bs.T)) * dts[None, :]) @ xs
+                dG = np.sum(gys * ysm, 1) - np.sum(xs * dxsm, 1)
+                dG[-1] += np.sum(R[k] * hk[k + 1])
+                eta = np.cumsum(dG[::-1])[::-1]
+                out["dx"][bi, t0:t0 + v, h] = dxsm + Dh * gys
+                out["dB"][bi, t0:t0 + v, g] += dts[:, None] * q
+                out["dC"][bi, t0:t0 + v, g] += np.exp(Gk)[:, None] * (gys @ hk[k]) + \
+                    ((low * (gys @ xs.T)) * dts[None, :]) @ Bs
+                out["ddt"][bi, t0:t0 + v, h] = A[h] * eta + np.sum(q * Bs, 1)
+                out["dA"][h] += float(np.sum(dts * eta))
+                out["dD"][h] += float(np.sum(gys * xs))
+    return out

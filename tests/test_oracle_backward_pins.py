@@ -202,3 +202,26 @@ def test_pins_catch_planted_mistakes(fd_cases, mistake):
         assert worst < 1e-7
     else:
         assert worst > 1e-3, mistake
+
+
+@pytest.mark.parametrize("dims,T,h0,gf", [
+    ((1, 7, 2, 3, 2, 1), 3, True, True),     # partial last chunk
+    ((2, 13, 4, 2, 3, 2), 4, True, False),   # groups, no gfinal
+    ((1, 20, 2, 4, 5, 1), 8, False, True),   # no h0
+    ((1, 9, 3, 2, 2, 3), 9, True, True),     # one chunk, one head per group
+    ((1, 16, 2, 3, 3, 1), 1, True, True),    # chunks of one token
+])
+def test_chunked_backward_matches_the_adjoint_recurrence(dims, T, h0, gf):
+    """The chunked restatement (reverse pass over chunks, per-chunk masked
+    products, dL/dl as a reverse cumsum of dL/dG) equals the token-by-token
+    adjoint to rounding, whatever the chunk size."""
+    rng = np.random.default_rng(31)
+    inp = rand_inputs(rng, *dims, h0=h0)
+    b, L, nh, P, S, ng = dims
+    gy = rng.standard_normal((b, L, nh, P))
+    gfinal = rng.standard_normal((b, nh, P, S)) if gf else None
+    args = (inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"], gy, gfinal)
+    ref = oracle.backward(*args)
+    got = oracle.backward_chunked(*args, chunk=T)
+    for k in ref:
+        assert rel_err(got[k], ref[k]) < 1e-12, (k, rel_err(got[k], ref[k]))
