@@ -101,7 +101,7 @@ def kernel_names(w: W.Workload, plan: dict | None = None) -> list:
     if w.dtype == "fp32" and w.headdim == 64 and w.chunk in (128, 256):
         # the warp-specialised fp32 kernels where the shape allows (the
         # chunk-jump one forms the cumsum itself: one launch less)
-        if w.dstate % 32 == 0 and w.dstate <= 128:
+        if w.dstate % 32 == 0 and w.dstate <= 256:
             names[3] = "fwd_out_tf32"
         if w.dstate % 64 == 0:
             names = ["fwd_chunk_state_tf32"] + names[2:]

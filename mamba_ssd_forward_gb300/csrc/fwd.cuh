@@ -75,7 +75,7 @@ cudaError_t launch_fwd_out(const Dims &d, const void *x, const void *B, const vo
 // fwd_out_tf32: the output pass for fp32 I/O (kind::tf32), one 128-row tile
 // of a chunk and a slice of hs heads per CTA, the masked C B^T of the tile
 // shared by the slice's heads with the decay factored about one anchor per
-// chunk and head (P = 64, S a multiple of 32 up to 128, T in {128, 256}).
+// chunk and head (P = 64, S a multiple of 32 up to 256, T in {128, 256}).
 // It reads G (fp32, log2 units, [b, nh, nc * T]) and the fp32 start states
 // [b, nh, nc, P, S] times 2^alpha_k rounded to tf32 (state_passing with
 // tf32_out).

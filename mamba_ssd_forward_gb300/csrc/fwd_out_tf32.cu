@@ -45,7 +45,10 @@
 //     factors, the transposition of each 32-token x atom into K-major Xh^T
 //     (tokens along the 128-byte rows, scaled by v_j, rounded), and the
 //     previous head's epilogue y = u_i Acc_i + D x_i.
-// Supported: P = 64, S a multiple of 32 up to 128, T in {128, 256}.
+// At S > 128, C's first 128 columns of S sit in tensor memory and the rest
+// in shared memory (the 512 tensor-memory columns hold C B^T, 128 of C and
+// the two accumulator sets); those MMAs read A from shared memory.
+// Supported: P = 64, S a multiple of 32 up to 256, T in {128, 256}.
 #include "fwd.cuh"
 
 namespace ssd {
@@ -92,7 +95,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
   // an x stage in place; empty: the MMAs reading a B, x or state stage are
   // done; xrel: every row warp is done with a C stage; c_ready: C is in
   // tensor memory
-  __shared__ __align__(8) uint64_t c_ready, full[kMaxSlots], xfull[kMaxSlots],
+  __shared__ __align__(8) uint64_t c_ready, c2_full, full[kMaxSlots], xfull[kMaxSlots],
       scaled[kMaxSlots], empty[kMaxSlots], xrel[kMaxSlots], sc_done, pack_done, acc_full[2],
       acc_free[2];
   __shared__ uint32_t tmem_slot;
@@ -114,15 +117,19 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
   const int valid = min(kT, L - tok0);
   if (t * 128 >= valid) return;  // the whole tile lies past the sequence (uniform)
   const int nS = S / 32;             // K atoms of S
+  const int nCt = min(nS, 4);        // atoms of C in tensor memory (S < 128 of it)
+  const int nCs = nS - nCt;          // atoms of C resident in shared memory (S > 128)
   const int nHs = (nS + 1) / 2;      // state stages per head
   const int nJ = 4 * (t + 1);        // 32-token atoms of the in-chunk sum
   const int nXs = nJ / 2;            // x stages per head (64 tokens each)
-  uint8_t *ring = smem;
+  uint8_t *Cres = smem;  // C atoms 4 .. nS - 1 of the tile (S > 128), 16 KB each
+  uint8_t *ring = smem + nCs * kStage;
   uint8_t *ystage = ring + nslot * kStage;  // y of one head: two 16 KB boxes
   auto slot_ptr = [&](int u) { return ring + (u % nslot) * kStage; };
 
   if (tid == 0) {
     ptx::mbar_init(&c_ready, kRowWarps);
+    ptx::mbar_init(&c2_full, 1);
     for (int i = 0; i < nslot; ++i) {
       ptx::mbar_init(&full[i], 1);
       ptx::mbar_init(&xfull[i], 1);
@@ -177,7 +184,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       }
       prev_x = x_stage ? (prev_x | (1u << sl)) : (prev_x & ~(1u << sl));
     };
-    for (int sb = 0; sb < nS; ++sb, ++u) {
+    for (int sb = 0; sb < nCt; ++sb, ++u) {
       acquire(159, true);
       if (leader) {
         ptx::mbar_arrive_expect_tx(&xfull[u % nslot], kStage);
@@ -185,6 +192,12 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       }
       __syncwarp();
     }
+    if (nCs > 0 && leader) {
+      ptx::mbar_arrive_expect_tx(&c2_full, nCs * kStage);
+      for (int i = 0; i < nCs; ++i)
+        ptx::tma_load_4d(Cres + i * kStage, &tm_C, (nCt + i) * 32, g, tok0 + t * 128, b, &c2_full);
+    }
+    __syncwarp();
     for (int sb = 0; sb < nS; ++sb)
       for (int th = 0; th <= t; ++th, ++u) {
         acquire(160, false);
@@ -230,7 +243,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     uint32_t fpar = 0, spar = 0;  // parity of the next wait, one bit per slot
     ptx::mbar_wait(&c_ready, 0, a.err, 163);
     ptx::tc_fence_after();
-    int u = nS;  // the C stages went to the row warps
+    int u = nCt;  // the C stages went to the row warps
     const uint32_t idCB = ptx::idesc_tf32(128, 128, false, false);
     for (int sb = 0; sb < nS; ++sb)
       for (int th = 0; th <= t; ++th, ++u) {
@@ -243,8 +256,15 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = ptx::smem_desc(b0 + kk * 32, 16, 1024, ptx::kSw128);
-            ptx::mma_ts_tf32(tmem + 128 * th, tmem + kColC + sb * 32 + kk * 8, bd, idCB,
-                             (sb | kk) ? 1u : 0u);
+            if (sb < nCt) {
+              ptx::mma_ts_tf32(tmem + 128 * th, tmem + kColC + sb * 32 + kk * 8, bd, idCB,
+                               (sb | kk) ? 1u : 0u);
+            } else {
+              const uint64_t cd = ptx::smem_desc(ptx::smem_u32(Cres + (sb - nCt) * kStage) +
+                                                     kk * 32,
+                                                 16, 1024, ptx::kSw128);
+              ptx::mma_ss<true>(tmem + 128 * th, cd, bd, idCB, 1u);
+            }
           }
           ptx::mma_commit(&empty[sl]);
         }
@@ -299,8 +319,17 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t hd =
                   ptx::smem_desc(h0 + ai * kHAtom + kk * 32, 16, 1024, ptx::kSw128);
-              ptx::mma_ts_tf32(tmem + acc_col(set), tmem + kColC + (2 * hh + ai) * 32 + kk * 8,
-                               hd, idY, (steep && (hh | ai | kk) == 0) ? 0u : 1u);
+              const int sa = 2 * hh + ai;  // atom of S
+              const uint32_t accf = (steep && (hh | ai | kk) == 0) ? 0u : 1u;
+              if (sa < nCt) {
+                ptx::mma_ts_tf32(tmem + acc_col(set), tmem + kColC + sa * 32 + kk * 8, hd, idY,
+                                 accf);
+              } else {
+                const uint64_t cd = ptx::smem_desc(ptx::smem_u32(Cres + (sa - nCt) * kStage) +
+                                                       kk * 32,
+                                                   16, 1024, ptx::kSw128);
+                ptx::mma_ss<true>(tmem + acc_col(set), cd, hd, idY, accf);
+              }
             }
           }
           ptx::mma_commit(&empty[sl]);
@@ -336,7 +365,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
     // of the 32 columns of each atom), then the B stages rounded as they land
     uint32_t xpar = 0;  // parity of the next wait on xfull[slot], one bit per slot
     int u = 0;
-    for (int sb = 0; sb < nS; ++sb, ++u) {
+    for (int sb = 0; sb < nCt; ++sb, ++u) {
       const int sl = u % nslot;
       ptx::mbar_wait(&xfull[sl], (xpar >> sl) & 1, a.err, 169);
       xpar ^= 1u << sl;
@@ -353,10 +382,17 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       warp_arrive(&xrel[sl]);  // the values are in registers: the stage may go
       ptx::tmem_stu<16>(tmem + lane_base + kColC + sb * 32 + half * 16, r);
     }
+    if (nCs > 0) {
+      // C's atoms past the first 128 of S stay in shared memory, rounded in
+      // place
+      ptx::mbar_wait(&c2_full, 0, a.err, 175);
+      round_block(Cres, nCs * kStage);
+      ptx::fence_async_smem();
+    }
     ptx::tmem_st_wait();
     ptx::tc_fence_before();
     warp_arrive(&c_ready);
-    for (; u < nS + n_pa; ++u) {
+    for (; u < nCt + n_pa; ++u) {
       const int sl = u % nslot;
       ptx::mbar_wait(&xfull[sl], (xpar >> sl) & 1, a.err, 170);
       xpar ^= 1u << sl;
@@ -584,18 +620,19 @@ struct OutSmem32 {
 // The ring and the y staging within 220 KB of dynamic
 // shared memory (1 KB of it alignment slack; the static arrays, about 7 KB,
 // sit beside it).
-OutSmem32 out_smem32(const Dims &) {
+OutSmem32 out_smem32(const Dims &d) {
   OutSmem32 m;
-  const int room = (220 * 1024 - 1024 - 2 * kStage) / kStage;
+  const int c_res = (int)std::max<int64_t>(0, (d.S - 128) / 32) * kStage;
+  const int room = (220 * 1024 - 1024 - c_res - 2 * kStage) / kStage;
   m.nslot = std::min(kMaxSlots, room);
-  m.smem = m.nslot * kStage + 2 * kStage + 1024;
+  m.smem = c_res + m.nslot * kStage + 2 * kStage + 1024;
   return m;
 }
 
 }  // namespace
 
 bool fwd_out_tf32_supported(const Dims &d) {
-  if (d.P != kP || d.S % 32 || d.S < 32 || d.S > 128 || (d.T != 128 && d.T != 256))
+  if (d.P != kP || d.S % 32 || d.S < 32 || d.S > 256 || (d.T != 128 && d.T != 256))
     return false;
   if (d.nc > 65535 || d.b > 65535) return false;
   // a head's state and x stages in flight, plus one
