@@ -387,6 +387,45 @@ SSD_API ssd_status ssd_forward_noalloc(const ssd_dims *dims, ssd_dtype dtype, co
                                        const void *C, const float *D, const float *h0,
                                        void *y, float *final_state, void *stream);
 
+/* ------------------------------------------------------------- backward */
+
+/* Bytes of device workspace ssd_backward needs, including the
+ * SSD_WS_HEADER_BYTES header (0 if the dims are invalid or the backward
+ * does not support them). */
+SSD_API size_t ssd_backward_workspace_size(const ssd_dims *dims, ssd_dtype dtype);
+
+/* Gradients of a loss through the forward pass of ssd_forward.  The pages
+ * (section "Mamba-2 architecture") name the backward pass without deriving
+ * it; this is the adjoint of the recurrence above, g_t = dL/dh_t =
+ * gy_t c_t^T + exp(a_{t+1}) g_{t+1} from g = gfinal after the last token,
+ * in the chunked form of the forward:
+ *   dx_t  = g_t b_t + D[h] gy_t
+ *   dB_t  = sum over the group's heads of dt_t g_t^T x_t
+ *   dC_t  = sum over the group's heads of h_t^T gy_t
+ *   ddt_t = <B_t, g_t^T x_t> + A[h] sum_{t' >= t} <g_{t'}, h_{t'-1}> exp(a_{t'})
+ *   dA[h] = sum over b, t of dt_t sum_{t' >= t} <g_{t'}, h_{t'-1}> exp(a_{t'})
+ *   dD[h] = sum over b, t of <gy_t, x_t>,   dh0 = exp(a_1) g_1
+ * (the inner sums run over the whole sequence; per chunk they become one
+ * reverse cumsum within the chunk and the adjoint state R_k carried between
+ * chunks).  In: x, dt, A, B, C, D, h0 as for ssd_forward, gy = dL/dy
+ * [b, L, nh, P] and gfinal = dL/dfinal_state [b, nh, P, S].  Out: dx, ddt,
+ * dA, dB, dC, dD, dh0 in the layouts of x, dt, A, B, C, D, h0.  D, h0 and
+ * gfinal may be NULL (zero); dD and dh0 may be NULL (not written).  The
+ * forward's intermediates (G, start states, final state) are recomputed in
+ * `workspace` (>= ssd_backward_workspace_size bytes, 256-byte aligned, its
+ * first SSD_WS_HEADER_BYTES zeroed before its first use).
+ * SSD_F32 only (SSD_BF16 returns SSD_ERR_UNSUPPORTED), with P = 64, S in
+ * {64, 128, 256}; every product of the backward, and of the forward
+ * states it recomputes, runs in fp32 on the CUDA cores.  dB, dC,
+ * dA and dD are summed in a fixed order: repeated calls give the same bits.
+ * Allocates nothing and never synchronises. */
+SSD_API ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                                const void *dt, const float *A, const void *B, const void *C,
+                                const float *D, const float *h0, const void *gy,
+                                const float *gfinal, void *dx, void *ddt, float *dA, void *dB,
+                                void *dC, float *dD, float *dh0, void *workspace,
+                                size_t ws_bytes, void *stream);
+
 /* ---------------------------------------------------------------- plans */
 
 /* Every valid plan for these dims: writes up to max_out plans to `out` (may

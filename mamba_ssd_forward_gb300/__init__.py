@@ -20,6 +20,7 @@ from ._abi import SSD_BF16, SSD_F32, SsdError  # noqa: F401
 
 __all__ = ["forward", "chunk_cumsum", "chunk_state", "state_passing", "chunk_scan",
            "decode_step", "workspace_size", "new_workspace", "workspace_error", "dims_of",
+           "backward", "backward_workspace_size",
            "SsdError"]
 
 
@@ -110,6 +111,43 @@ def forward(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, workspace=None,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _plan_ref(plan),
         _stream()))
     return y, final_state
+
+
+def backward_workspace_size(x: torch.Tensor, B: torch.Tensor, chunk: int = 256) -> int:
+    """Bytes of workspace ssd_backward needs (0: unsupported dims or dtype)."""
+    d = dims_of(x, B, chunk)
+    return int(_abi.load().ssd_backward_workspace_size(ctypes.byref(d), _io_code(x)))
+
+
+def backward(x, dt, A, B, C, D=None, h0=None, gy=None, gfinal=None, chunk: int = 256,
+             workspace=None, want_dD: bool = True, want_dh0: bool = True) -> dict:
+    """Gradients of a loss through forward() given gy = dL/dy and gfinal =
+    dL/dfinal_state (None = 0), by ssd_backward (fp32 I/O): a dict of dx,
+    ddt, dA, dB, dC, dD, dh0 (the last two None unless wanted).  `workspace`
+    may be a preallocated new_workspace(backward_workspace_size(...))."""
+    lib = _abi.load()
+    d = dims_of(x, B, chunk)
+    io = _io_code(x)
+    ws_need = lib.ssd_backward_workspace_size(ctypes.byref(d), io)
+    if ws_need == 0:
+        raise SsdError("ssd_backward_workspace_size", _abi.SSD_ERR_UNSUPPORTED,
+                       "dimensions or dtype are invalid or unsupported by the backward")
+    if gy is None:
+        raise ValueError("gy (dL/dy) is required")
+    if workspace is None:
+        workspace = new_workspace(ws_need, x.device)
+    out = {"dx": torch.empty_like(x), "ddt": torch.empty_like(dt),
+           "dA": torch.empty_like(A), "dB": torch.empty_like(B), "dC": torch.empty_like(C),
+           "dD": torch.empty_like(A) if want_dD else None,
+           "dh0": (torch.empty((d.batch, d.nheads, d.headdim, d.dstate), dtype=torch.float32,
+                               device=x.device) if want_dh0 else None)}
+    _abi.check("ssd_backward", lib.ssd_backward(
+        ctypes.byref(d), io, _ptr(x), _ptr(dt), _ptr(_f32(A, "A")), _ptr(B), _ptr(C),
+        _ptr(_f32(D, "D")), _ptr(_f32(h0, "h0")), _ptr(gy), _ptr(_f32(gfinal, "gfinal")),
+        _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]),
+        _ptr(out["dD"]), _ptr(out["dh0"]), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream()))
+    return out
 
 
 def chunk_cumsum(dt, A, chunk: int, headdim: int = 16, dstate: int = 16, out=None):

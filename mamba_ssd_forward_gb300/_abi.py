@@ -43,6 +43,8 @@ EXPORTS = (
     "ssd_forward_default_plan",
     "ssd_forward_tune",
     "ssd_selftest_bounded_wait",
+    "ssd_backward_workspace_size",
+    "ssd_backward",
 )
 
 
@@ -125,6 +127,10 @@ def load(path: str | None = None):
     lib.ssd_selftest_bounded_wait.argtypes = [ctypes.c_uint64, vp, vp]
     lib.ssd_forward_tune.restype = i32
     lib.ssd_forward_tune.argtypes = [dims_p, i32] + [vp] * 10 + [sz, i32, vp, sz, vp, plan_p]
+    lib.ssd_backward_workspace_size.restype = sz
+    lib.ssd_backward_workspace_size.argtypes = [dims_p, i32]
+    lib.ssd_backward.restype = i32
+    lib.ssd_backward.argtypes = [dims_p, i32] + [vp] * 17 + [sz, vp]
     if path is None:
         _lib = lib
     return lib

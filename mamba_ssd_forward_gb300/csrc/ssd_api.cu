@@ -641,3 +641,104 @@ ssd_status ssd_forward_host(const ssd_dims *dims, ssd_dtype dtype, const void *x
 }
 
 }  // extern "C"
+
+namespace {
+
+// Workspace of ssd_backward (fp32): the header (the call's error word), G,
+// the chunk jump terms (the forward's, then the adjoint's), the start states
+// h_k, the adjoint states R_k, the forward's final state, the per-head shares
+// of dB and dC (only when a group has several heads), the per-token q . B,
+// dL/dG and gy . x, and the per-chunk shares of dA and dD.  Each part is
+// 256-byte aligned.
+struct BwdLayout {
+  size_t G, dst, states, R, fin, dBh, dCh, qB, dG, gyx, part, total;
+};
+
+BwdLayout bwd_layout(const Dims &d) {
+  BwdLayout w;
+  const size_t tok = round256(sizeof(float) * d.b * d.nh * d.nc * d.T);
+  const size_t st = round256(sizeof(float) * d.b * d.nh * d.nc * d.P * d.S);
+  const size_t hs = d.hpg > 1 ? round256(sizeof(float) * d.b * d.L * d.nh * d.S) : 0;
+  w.G = ssd::kWsHeader;
+  w.dst = w.G + tok;
+  w.states = w.dst + st;
+  w.R = w.states + st;
+  w.fin = w.R + st;
+  w.dBh = w.fin + round256(sizeof(float) * d.b * d.nh * d.P * d.S);
+  w.dCh = w.dBh + hs;
+  w.qB = w.dCh + hs;
+  w.dG = w.qB + tok;
+  w.gyx = w.dG + tok;
+  w.part = w.gyx + tok;
+  w.total = w.part + round256(2 * sizeof(float) * d.b * d.nh * d.nc);
+  return w;
+}
+
+ssd_status check_backward_dims(const ssd_dims *dims, ssd_dtype dtype, Dims *d) {
+  const ssd_status s = check_dims(dims, d);
+  if (s != SSD_OK) return s;
+  if (!valid_dtype(dtype)) return SSD_ERR_INVALID_ARG;
+  if (dtype != SSD_F32 || !ssd::bwd_supported(*d)) return SSD_ERR_UNSUPPORTED;
+  return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssd_backward_workspace_size(const ssd_dims *dims, ssd_dtype dtype) {
+  Dims d;
+  if (check_backward_dims(dims, dtype, &d) != SSD_OK) return 0;
+  return bwd_layout(d).total;
+}
+
+ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
+                        const float *A, const void *B, const void *C, const float *D,
+                        const float *h0, const void *gy, const float *gfinal, void *dx,
+                        void *ddt, float *dA, void *dB, void *dC, float *dD, float *dh0,
+                        void *workspace, size_t ws_bytes, void *stream) {
+  Dims d;
+  ssd_status s = check_backward_dims(dims, dtype, &d);
+  if (s != SSD_OK) return s;
+  if (!req(x) || !req(dt) || !req(A) || !req(B) || !req(C) || !opt(D) || !opt(h0) ||
+      !req(gy) || !opt(gfinal) || !req(dx) || !req(ddt) || !req(dA) || !req(dB) || !req(dC) ||
+      !opt(dD) || !opt(dh0) || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return SSD_ERR_INVALID_ARG;
+  const BwdLayout w = bwd_layout(d);
+  if (ws_bytes < w.total) return SSD_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  int *err = static_cast<int *>(workspace);
+  char *ws = static_cast<char *>(workspace);
+  auto f = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
+  const float *xf = static_cast<const float *>(x), *dtf = static_cast<const float *>(dt),
+              *Bf = static_cast<const float *>(B), *Cf = static_cast<const float *>(C),
+              *gyf = static_cast<const float *>(gy);
+  float *G = f(w.G), *dst = f(w.dst), *sts = f(w.states), *R = f(w.R), *fin = f(w.fin);
+  // with one head per group the per-head shares of dB and dC are dB and dC
+  float *dBh = d.hpg > 1 ? f(w.dBh) : static_cast<float *>(dB);
+  float *dCh = d.hpg > 1 ? f(w.dCh) : static_cast<float *>(dC);
+  cudaError_t e = cudaSuccess;
+  // the forward's cumsum, jump terms, start states and final state, all in
+  // fp32 (the forward's own jump kernels take TF32 products)
+  e = ssd::launch_chunk_cumsum(d, dtype, dt, A, G, err, st);
+  if (e == cudaSuccess) e = ssd::launch_bwd_jump(d, xf, Bf, dtf, G, dst, err, st);
+  if (e == cudaSuccess) e = ssd::launch_state_passing(d, dst, G, h0, sts, fin, err, st);
+  // the adjoint: its jump terms (over the forward's, no longer needed), the
+  // backward pass over chunks for R_k and dh0, then the per-token gradients
+  if (e == cudaSuccess) e = ssd::launch_bwd_jump(d, gyf, Cf, nullptr, G, dst, err, st);
+  if (e == cudaSuccess)
+    e = ssd::launch_state_passing(d, dst, G, gfinal, R, dh0, err, st, false, true);
+  if (e == cudaSuccess)
+    e = ssd::launch_bwd_main(d, xf, dtf, Bf, Cf, D, gyf, G, sts, R, static_cast<float *>(dx),
+                             dBh, dCh, f(w.qB), f(w.dG), f(w.gyx), err, st);
+  float2 *part = reinterpret_cast<float2 *>(ws + w.part);
+  if (e == cudaSuccess)
+    e = ssd::launch_bwd_finish(d, dtf, A, R, sts, fin, f(w.qB), f(w.dG), f(w.gyx),
+                               static_cast<float *>(ddt), part, err, st);
+  if (e == cudaSuccess)
+    e = ssd::launch_bwd_reduce(d, dBh, dCh, part, static_cast<float *>(dB),
+                               static_cast<float *>(dC), dA, dD, st);
+  return from_cuda(e);
+}
+
+}  // extern "C"

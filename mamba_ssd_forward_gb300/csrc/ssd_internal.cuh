@@ -100,7 +100,7 @@ cudaError_t launch_chunk_state(const Dims &d, ssd_dtype io, const void *x,
 cudaError_t launch_state_passing(const Dims &d, const float *dstates,
                                  const float *G, const float *h0,
                                  float *states, float *final_state, int *err,
-                                 cudaStream_t st, bool tf32_out = false);
+                                 cudaStream_t st, bool tf32_out = false, bool reverse = false);
 cudaError_t launch_chunk_scan(const Dims &d, ssd_dtype io, const void *x,
                               const void *B, const void *C, const void *dt,
                               const float *G, const float *states,
@@ -111,5 +111,32 @@ cudaError_t launch_decode_step(int64_t b, int64_t nh, int64_t P, int64_t S, int6
                                ssd_dtype io, const void *x, const void *dt, const float *A,
                                const void *B, const void *C, const float *D, float *state,
                                void *y, int *err, cudaStream_t st);
+
+// Backward pass for fp32 I/O (bwd.cu), CUDA cores.  bwd_supported: P = 64,
+// S in {64, 128, 256}, T a multiple of 32 up to 256.  Shapes (fp32):
+// dR, R [b, nh, nc, P, S]; dBh, dCh [b, L, nh, S] (per-head shares of dB,
+// dC; may be dB and dC themselves when nh == ng); qB, dG, gyx [b, nh, nc*T];
+// part float2 [b, nh, nc].
+bool bwd_supported(const Dims &d);
+// chunk jump terms in fp32, out[k] = sum_{t in k} w_t v_t m_t^T: the
+// adjoint's (v = gy, m = C, dt null: w_t = exp2(G_t)) or the forward's
+// (v = x, m = B: w_t = exp2(G_last - G_t) dt_t)
+cudaError_t launch_bwd_jump(const Dims &d, const float *v, const float *m, const float *dt,
+                            const float *G, float *out, int *err, cudaStream_t st);
+// per token: dx, dt q (dBh), the head's dC (dCh), q . B, dL/dG, gy . x
+cudaError_t launch_bwd_main(const Dims &d, const float *x, const float *dt, const float *B,
+                            const float *C, const float *D, const float *gy, const float *G,
+                            const float *states, const float *R, float *dx, float *dBh,
+                            float *dCh, float *qB, float *dG, float *gyx, int *err,
+                            cudaStream_t st);
+// ddt, and the per-chunk shares of dA and dD
+cudaError_t launch_bwd_finish(const Dims &d, const float *dt, const float *A, const float *R,
+                              const float *states, const float *final_state, const float *qB,
+                              const float *dG, const float *gyx, float *ddt, float2 *part,
+                              int *err, cudaStream_t st);
+// dB, dC (sums over a group's heads, skipped when nh == ng), dA, dD (nullable)
+cudaError_t launch_bwd_reduce(const Dims &d, const float *dBh, const float *dCh,
+                              const float2 *part, float *dB, float *dC, float *dA, float *dD,
+                              cudaStream_t st);
 
 }  // namespace ssd

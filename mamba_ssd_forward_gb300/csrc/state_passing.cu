@@ -17,6 +17,10 @@
 // 2^alpha_k (alpha_k = 0 when the chunk decays by more than 2^-180; a power
 // of two, so exact), rounded to tf32 (nearest); the carried state and the
 // final state stay unscaled fp32.
+// With reverse (the backward pass) the chunks are walked from the last to
+// the first: from h0 = dL/dfinal_state it stores R_k = dL/dh_{k+1} for every
+// chunk and leaves R_{-1} = dL/dh0 in final_state, R_{k-1} = exp2(G_last,k)
+// R_k + dstates[k] (dstates holding the adjoint's jump terms).
 #include "tc_common.cuh"
 
 namespace ssd {
@@ -30,7 +34,7 @@ state_passing_kernel(const float4 *__restrict__ dstates,
                      const float *__restrict__ G, const float4 *__restrict__ h0,
                      float4 *__restrict__ states, float4 *__restrict__ final_state,
                      int64_t ps4, int64_t nc, int64_t T, int64_t nbh, int tf32_out,
-                     int *err) {
+                     int reverse, int *err) {
   __shared__ float2 gsm[256];  // per chunk: decay, stored-state scale
   // every index below lies in [0, nbh nc ps4) (states, dstates), [0, nbh
   // ps4) (h0, final_state) or [0, nbh nc T) (G) when bh < nbh and e < ps4; a
@@ -49,10 +53,12 @@ state_passing_kernel(const float4 *__restrict__ dstates,
   const float *Gbh = G + bh * nc * T;
   const float4 *dsrc = dstates + bh * nc * ps4 + e;
   float4 *sdst = states + bh * nc * ps4 + e;
+  // the chunk visited at step k: k itself, or nc - 1 - k walking backwards
+  auto ck = [&](int64_t k) { return reverse ? nc - 1 - k : k; };
   float4 cur[kDepth], nxt[kDepth];
 #pragma unroll
   for (int i = 0; i < kDepth; ++i)
-    if (i < nc) cur[i] = dsrc[(int64_t)i * ps4];
+    if (i < nc) cur[i] = dsrc[ck(i) * ps4];
   for (int64_t k0 = 0; k0 < nc; k0 += kDepth) {
     if ((k0 & 255) == 0) {
       // the next 256 chunks' decays and stored-state scales.  With tf32_out
@@ -60,7 +66,7 @@ state_passing_kernel(const float4 *__restrict__ dstates,
       // rule as fwd_out_tf32; a power of two, so exact), else 1.
       __syncthreads();
       if (k0 + threadIdx.x < nc) {
-        const float Glast = Gbh[(k0 + threadIdx.x) * T + T - 1];
+        const float Glast = Gbh[ck(k0 + threadIdx.x) * T + T - 1];
         float sc = 1.f;
         if (tf32_out) {
           const int alpha = -Glast <= 180.f ? (int)rintf(0.5f * Glast) : 0;
@@ -72,13 +78,13 @@ state_passing_kernel(const float4 *__restrict__ dstates,
     }
 #pragma unroll
     for (int i = 0; i < kDepth; ++i)
-      if (k0 + kDepth + i < nc) nxt[i] = dsrc[(k0 + kDepth + i) * ps4];
+      if (k0 + kDepth + i < nc) nxt[i] = dsrc[ck(k0 + kDepth + i) * ps4];
 #pragma unroll
     for (int i = 0; i < kDepth; ++i)
       if (k0 + i < nc) {
         const float2 g = gsm[(k0 + i) & 255];
         if (live) {
-          sdst[(k0 + i) * ps4] =
+          sdst[ck(k0 + i) * ps4] =
               tf32_out ? make_float4(__uint_as_float(to_tf32(g.y * h.x)),
                                      __uint_as_float(to_tf32(g.y * h.y)),
                                      __uint_as_float(to_tf32(g.y * h.z)),
@@ -101,7 +107,7 @@ state_passing_kernel(const float4 *__restrict__ dstates,
 cudaError_t launch_state_passing(const Dims &d, const float *dstates,
                                  const float *G, const float *h0,
                                  float *states, float *final_state, int *err,
-                                 cudaStream_t st, bool tf32_out) {
+                                 cudaStream_t st, bool tf32_out, bool reverse) {
   const int64_t ps4 = d.P * d.S / 4;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((ps4 + kThreads - 1) / kThreads), (unsigned)(d.b * d.nh));
@@ -116,7 +122,7 @@ cudaError_t launch_state_passing(const Dims &d, const float *dstates,
                             G, reinterpret_cast<const float4 *>(h0),
                             reinterpret_cast<float4 *>(states),
                             reinterpret_cast<float4 *>(final_state), ps4, d.nc, d.T,
-                            d.b * d.nh, tf32_out ? 1 : 0, err);
+                            d.b * d.nh, tf32_out ? 1 : 0, reverse ? 1 : 0, err);
 }
 
 }  // namespace ssd

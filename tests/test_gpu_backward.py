@@ -1,0 +1,134 @@
+"""The backward pass (ssd_backward, fp32 I/O) against the oracle's adjoint
+recurrence, which is pinned to finite differences of the forward
+recurrence: dx, ddt, dA, dB, dC, dD and dh0 for a loss
+L = <gy, y> + <gfinal, final_state> with seeded gy and gfinal.  Cases: every
+supported dstate, chunks of 64 (the step-kernel forward), 128 and 256,
+ragged last chunks, one token, several heads per group (dB, dC summed over
+heads) and one (written directly), with and without h0, gfinal and D,
+chunks steep enough to underflow their decay, and repeated calls (fixed
+summation order: the same bits)."""
+import pytest
+import torch
+
+from parity import check_io, device_inputs, make, to64
+
+pytestmark = pytest.mark.gpu
+
+from mamba_ssd_forward_gb300 import inputs as W  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def ssd():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mamba_ssd_forward_gb300 import build
+    build.build()
+    import mamba_ssd_forward_gb300 as m
+    return m
+
+
+CASES = [
+    # name, b, L, nh, P, S, ng, T, dtype, h0
+    W.Workload("bwd_S128_T256", 2, 1300, 8, 64, 128, 1, 256, "fp32", True),
+    W.Workload("bwd_S64_T128_g2_hpg3", 1, 515, 6, 64, 64, 2, 128, "fp32", False),
+    W.Workload("bwd_S256_T256", 1, 700, 4, 64, 256, 1, 256, "fp32", True),
+    W.Workload("bwd_S128_T64_g2", 1, 333, 4, 64, 128, 2, 64, "fp32", True),
+    W.Workload("bwd_S64_T256_hpg1", 2, 600, 4, 64, 64, 4, 256, "fp32", True),
+    W.Workload("bwd_one_token", 1, 1, 2, 64, 128, 1, 256, "fp32", True),
+    W.Workload("bwd_S256_T128_g2", 1, 400, 4, 64, 256, 2, 128, "fp32", False),
+]
+
+NAMES = ("dx", "ddt", "dA", "dB", "dC", "dD", "dh0")
+
+
+def grads_in(w, seed):
+    """Seeded dL/dy and dL/dfinal_state, fp32 values held in float64 on the
+    CPU (the library and the oracle see the same numbers)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(1000 + seed)
+    gy = torch.randn((w.batch, w.seqlen, w.nheads, w.headdim), generator=g, dtype=torch.float64)
+    gfinal = torch.randn((w.batch, w.nheads, w.headdim, w.dstate), generator=g,
+                         dtype=torch.float64)
+    return gy.float().double(), gfinal.float().double()
+
+
+def run(ssd, w, inp, gy, gfinal):
+    dev = device_inputs(inp)
+    gyd = gy.float().cuda().contiguous()
+    gfd = None if gfinal is None else gfinal.float().cuda().contiguous()
+    ws = ssd.new_workspace(ssd.backward_workspace_size(dev["x"], dev["B"], w.chunk), "cuda")
+    out = ssd.backward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], dev["h0"],
+                       gyd, gfd, chunk=w.chunk, workspace=ws)
+    ssd.workspace_error(ws)
+    return out
+
+
+def reference(inp, gy, gfinal):
+    import oracle
+    return oracle.backward(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                           inp["h0"], gy.numpy(), None if gfinal is None else gfinal.numpy())
+
+
+def compare(out, ref, what):
+    for n in NAMES:
+        check_io(to64(out[n]), ref[n], "fp32", f"{what} {n}")
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_backward_matches_the_adjoint(ssd, w):
+    inp = make(w, seed=31)
+    gy, gfinal = grads_in(w, 31)
+    out = run(ssd, w, inp, gy, gfinal)
+    compare(out, reference(inp, gy, gfinal), w.name)
+
+
+def test_backward_without_D_and_gfinal(ssd):
+    """D = None (no skip term; dD is still sum gy . x) and gfinal = None."""
+    w = W.Workload("bwd_noD", 1, 520, 4, 64, 128, 1, 256, "fp32", True)
+    inp = make(w, seed=32)
+    inp["D"] = None
+    gy, _ = grads_in(w, 32)
+    out = run(ssd, w, inp, gy, None)
+    compare(out, reference(inp, gy, None), "no D, no gfinal")
+
+
+def test_backward_steep_chunks(ssd):
+    """Heads 0 and 1 decay by far more than 2^-180 within a chunk: every
+    factor exp2(G_s - G_t) the backward forms has a non-positive exponent,
+    so these only underflow to zero, as the exact values do."""
+    w = W.Workload("bwd_steep", 1, 768, 4, 64, 128, 1, 256, "fp32", True)
+    inp = make(w, seed=33)
+    A = inp["A"].clone()
+    A[0] = A[1] = -16.0
+    dt = inp["dt"].clone()
+    dt[0, :, 0] = 0.5
+    dt[0, 300:, 1] = 0.1
+    inp["A"], inp["dt"] = A, dt
+    gy, gfinal = grads_in(w, 33)
+    out = run(ssd, w, inp, gy, gfinal)
+    compare(out, reference(inp, gy, gfinal), "steep")
+
+
+def test_backward_is_deterministic(ssd):
+    """dB, dC, dA and dD are sums in a fixed order: repeated calls on the
+    same inputs give the same bits."""
+    w = W.Workload("bwd_repeat", 2, 1024, 8, 64, 64, 2, 256, "fp32", True)
+    inp = make(w, seed=34)
+    gy, gfinal = grads_in(w, 34)
+    first = run(ssd, w, inp, gy, gfinal)
+    for _ in range(2):
+        again = run(ssd, w, inp, gy, gfinal)
+        for n in NAMES:
+            assert torch.equal(first[n], again[n]), n
+
+
+def test_backward_rejects_bf16_and_unsupported(ssd):
+    w = W.Workload("bwd_bf16", 1, 256, 2, 64, 128, 1, 256, "bf16", False)
+    inp = device_inputs(make(w, seed=0))
+    assert ssd.backward_workspace_size(inp["x"], inp["B"], 256) == 0
+    with pytest.raises(ssd.SsdError):
+        ssd.backward(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], None,
+                     torch.zeros_like(inp["x"]), None, chunk=256)
+    w = W.Workload("bwd_P32", 1, 256, 2, 32, 128, 1, 256, "fp32", False)
+    inp = device_inputs(make(w, seed=0))
+    assert ssd.backward_workspace_size(inp["x"], inp["B"], 256) == 0
