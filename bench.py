@@ -618,6 +618,138 @@ def run_decode(args, w):
     return 0
 
 
+# fp32 CUDA-core peak of one GB300: 152 SMs x 128 fp32 lanes x 2 flop per FMA
+# x the 2070 MHz maximum SM clock (the ALU roofline of the backward kernels)
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+BWD_KERNELS = ["chunk_cumsum", "bwd_jump(x, B)", "state_passing", "bwd_jump(gy, C)",
+               "state_passing(reverse)", "bwd_main", "bwd_finish", "bwd_reduce"]
+
+
+def backward_macs(w: W.Workload) -> dict:
+    """Multiply-adds the backward needs (the algorithmic count, with the
+    causal triangle of each chunk counted once and C . B shared by a group's
+    heads), split into the per-token kernel's share and the rest."""
+    P, S, T = w.headdim, w.dstate, w.chunk
+    main = rest = 0
+    for k in range(w.nchunks):
+        v = min(T, w.seqlen - k * T)
+        npair = v * (v + 1) // 2
+        # per head: the scores gy_i . x_j and the four masked products
+        # (ysm, dC, dx, q); the four state terms of every token
+        main += w.batch * w.nheads * (npair * (3 * P + 2 * S) + 4 * v * P * S)
+        main += w.batch * w.ngroups * npair * S  # c_i . B_j, once per group
+        rest += w.batch * w.nheads * (2 * v * P * S + P * S)  # jump terms, <R_k, h_k+1>
+    return {"bwd_main": main, "total": main + rest}
+
+
+def time_oracle_backward(w: W.Workload, inp, gy, gfinal, target_s: float):
+    """Time the oracle's chunked backward (numpy float64) on the first
+    (batch, head) pair, over as many tokens as fit in about target_s seconds.
+    Returns (tokens/s of the whole workload's heads, sample)."""
+    import oracle
+    g = 0
+    L = w.seqlen
+    sl = lambda t, n: t[:1, :n, :1].contiguous() if t.dim() == 4 else t[:1, :n, :1]
+    def run(n):
+        t0 = time.perf_counter()
+        oracle.backward_chunked(sl(inp["x"], n), sl(inp["dt"], n), inp["A"][:1],
+                                inp["B"][:1, :n, g:g + 1], inp["C"][:1, :n, g:g + 1],
+                                inp["D"][:1], None if inp["h0"] is None else inp["h0"][:1, :1],
+                                gy[:1, :n, :1], gfinal[:1, :1], chunk=w.chunk)
+        return time.perf_counter() - t0
+    n = min(L, 4 * w.chunk)
+    secs = run(n)
+    if secs < target_s and n < L:
+        n = min(L, max(n, int(n * target_s / max(secs, 1e-3)) // w.chunk * w.chunk))
+        secs = run(n)
+    return n / secs / w.nheads, f"1 (batch, head) pair, the first {n} of L={L} tokens"
+
+
+def run_backward(args, w):
+    """The backward pass (ssd_backward, fp32 I/O) on the workload's shape in
+    fp32, with seeded dL/dy and dL/dfinal_state; L2 flushed before every
+    step.  Prints its own JSON line (mode "backward"); not the headline."""
+    import torch
+
+    import mamba_ssd_forward_gb300 as ssd
+    from mamba_ssd_forward_gb300 import build
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    wf = w if w.dtype == "fp32" else W.Workload(w.name.replace("bf16", "fp32"), w.batch,
+                                                 w.seqlen, w.nheads, w.headdim, w.dstate,
+                                                 w.ngroups, w.chunk, "fp32", w.has_h0)
+    inp = host_inputs(wf)
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(1)
+    gy = torch.randn((wf.batch, wf.seqlen, wf.nheads, wf.headdim), generator=gen)
+    gfinal = torch.randn((wf.batch, wf.nheads, wf.headdim, wf.dstate), generator=gen)
+    d = {k: (None if v is None else v.to(dev).contiguous()) for k, v in inp.items()}
+    gyd, gfd = gy.to(dev), gfinal.to(dev)
+    ws = ssd.new_workspace(ssd.backward_workspace_size(d["x"], d["B"], wf.chunk), dev)
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    nk = len(BWD_KERNELS)
+    out = None
+
+    def step(events):
+        return ssd.backward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], gyd, gfd,
+                            chunk=wf.chunk, workspace=ws, out=out, events=events)
+
+    warm = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+    for _ in range(max(3, args.warmup)):
+        flush_w.zero_()
+        out = step(warm)
+    torch.cuda.synchronize()
+    ssd.workspace_error(ws)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(0)
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    launches = 0
+    for evs in ev:
+        flush_w.zero_()
+        launches += step(evs)["n_launches"]
+    torch.cuda.synchronize()
+    sampler.mark_end()
+    clocks = sampler.stop()
+    ssd.workspace_error(ws)
+    ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in ev)
+    per = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev)
+           for i, n in enumerate(BWD_KERNELS)}
+    macs = backward_macs(wf)
+    tf_main = 2 * macs["bwd_main"] / (per["bwd_main"] / 1e3) / 1e12
+    tf_all = 2 * macs["total"] / (ms / 1e3) / 1e12
+    tokens = wf.batch * wf.seqlen
+    cpu = None
+    if not args.skip_cpu_baseline:
+        v, sample = time_oracle_backward(wf, inp, gy.double(), gfinal.double(), 10.0)
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": sample + " (numpy float64, chunked backward)"}
+    line = {
+        "metric": "SSD backward tokens/s at 1 GB300 (fp32 I/O, gradients of every input)",
+        "mode": "backward", "value": tokens / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wf.name, "batch": wf.batch, "seqlen": wf.seqlen,
+                   "nheads": wf.nheads, "headdim": wf.headdim, "dstate": wf.dstate,
+                   "ngroups": wf.ngroups, "chunk": wf.chunk,
+                   "l2": "flushed before every step (256 MB write), outside the events"},
+        "kernels_ms": per,
+        "roofline": {"kernel": "bwd_main", "bound": "alu", "achieved": tf_main,
+                     "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
+                     "frac": tf_main / FP32_ALU_TFLOPS,
+                     "peak_source": "152 SMs x 128 fp32 lanes x 2 x 2070 MHz",
+                     "algorithmic_flops_per_launch": 2 * macs["bwd_main"], "traffic": None},
+        "whole_pass": {"achieved_tflops": tf_all, "frac": tf_all / FP32_ALU_TFLOPS,
+                       "algorithmic_flops": 2 * macs["total"]},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -639,6 +771,8 @@ def main(argv=None):
                     help="L2 flush between steps (default: write a buffer, then read another)")
     ap.add_argument("--decode", action="store_true",
                     help="time the single-token decode step instead of the forward pass")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (fp32 I/O) instead of the forward pass")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="sequences per decode step (default: the workload's batch)")
     args = ap.parse_args(argv)
@@ -649,6 +783,8 @@ def main(argv=None):
         return run_reference(args, w)
     if args.decode:
         return run_decode(args, w)
+    if args.backward:
+        return run_backward(args, w)
     return run_ours(args, w)
 
 

@@ -120,11 +120,15 @@ def backward_workspace_size(x: torch.Tensor, B: torch.Tensor, chunk: int = 256) 
 
 
 def backward(x, dt, A, B, C, D=None, h0=None, gy=None, gfinal=None, chunk: int = 256,
-             workspace=None, want_dD: bool = True, want_dh0: bool = True) -> dict:
+             workspace=None, want_dD: bool = True, want_dh0: bool = True, out=None,
+             events=None) -> dict:
     """Gradients of a loss through forward() given gy = dL/dy and gfinal =
     dL/dfinal_state (None = 0), by ssd_backward (fp32 I/O): a dict of dx,
     ddt, dA, dB, dC, dD, dh0 (the last two None unless wanted).  `workspace`
-    may be a preallocated new_workspace(backward_workspace_size(...))."""
+    may be a preallocated new_workspace(backward_workspace_size(...)) and
+    `out` a dict returned by an earlier call (its tensors are reused).  With
+    `events` (torch.cuda.Event, enable_timing) the call is
+    ssd_backward_profiled, recording them around its launches."""
     lib = _abi.load()
     d = dims_of(x, B, chunk)
     io = _io_code(x)
@@ -136,17 +140,28 @@ def backward(x, dt, A, B, C, D=None, h0=None, gy=None, gfinal=None, chunk: int =
         raise ValueError("gy (dL/dy) is required")
     if workspace is None:
         workspace = new_workspace(ws_need, x.device)
-    out = {"dx": torch.empty_like(x), "ddt": torch.empty_like(dt),
-           "dA": torch.empty_like(A), "dB": torch.empty_like(B), "dC": torch.empty_like(C),
-           "dD": torch.empty_like(A) if want_dD else None,
-           "dh0": (torch.empty((d.batch, d.nheads, d.headdim, d.dstate), dtype=torch.float32,
-                               device=x.device) if want_dh0 else None)}
-    _abi.check("ssd_backward", lib.ssd_backward(
-        ctypes.byref(d), io, _ptr(x), _ptr(dt), _ptr(_f32(A, "A")), _ptr(B), _ptr(C),
-        _ptr(_f32(D, "D")), _ptr(_f32(h0, "h0")), _ptr(gy), _ptr(_f32(gfinal, "gfinal")),
-        _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]),
-        _ptr(out["dD"]), _ptr(out["dh0"]), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream()))
+    if out is None:
+        out = {"dx": torch.empty_like(x), "ddt": torch.empty_like(dt),
+               "dA": torch.empty_like(A), "dB": torch.empty_like(B), "dC": torch.empty_like(C),
+               "dD": torch.empty_like(A) if want_dD else None,
+               "dh0": (torch.empty((d.batch, d.nheads, d.headdim, d.dstate),
+                                   dtype=torch.float32, device=x.device) if want_dh0 else None)}
+    args = [ctypes.byref(d), io, _ptr(x), _ptr(dt), _ptr(_f32(A, "A")), _ptr(B), _ptr(C),
+            _ptr(_f32(D, "D")), _ptr(_f32(h0, "h0")), _ptr(gy), _ptr(_f32(gfinal, "gfinal")),
+            _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dB"]),
+            _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dh0"]), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream()]
+    if events is None:
+        _abi.check("ssd_backward", lib.ssd_backward(*args))
+        return out
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event on its first record
+            e.record()
+    handles = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    n = ctypes.c_int(0)
+    _abi.check("ssd_backward_profiled", lib.ssd_backward_profiled(
+        *args, handles, len(events), ctypes.byref(n)))
+    out["n_launches"] = n.value
     return out
 
 

@@ -45,6 +45,7 @@ EXPORTS = (
     "ssd_selftest_bounded_wait",
     "ssd_backward_workspace_size",
     "ssd_backward",
+    "ssd_backward_profiled",
 )
 
 
@@ -131,6 +132,9 @@ def load(path: str | None = None):
     lib.ssd_backward_workspace_size.argtypes = [dims_p, i32]
     lib.ssd_backward.restype = i32
     lib.ssd_backward.argtypes = [dims_p, i32] + [vp] * 17 + [sz, vp]
+    lib.ssd_backward_profiled.restype = i32
+    lib.ssd_backward_profiled.argtypes = ([dims_p, i32] + [vp] * 17 +
+                                          [sz, vp, vp, i32, ctypes.POINTER(ctypes.c_int)])
     if path is None:
         _lib = lib
     return lib

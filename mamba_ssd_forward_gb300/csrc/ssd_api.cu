@@ -682,6 +682,74 @@ ssd_status check_backward_dims(const ssd_dims *dims, ssd_dtype dtype, Dims *d) {
   return SSD_OK;
 }
 
+// ssd_backward and ssd_backward_profiled: events (n_events of them, may be
+// none) are recorded before the first launch and after each launch.
+ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,
+                         const float *A, const void *B, const void *C, const float *D,
+                         const float *h0, const void *gy, const float *gfinal, void *dx,
+                         void *ddt, float *dA, void *dB, void *dC, float *dD, float *dh0,
+                         void *workspace, size_t ws_bytes, cudaStream_t st,
+                         void *const *events, int n_events, int *n_launches) {
+  Dims d;
+  ssd_status s = check_backward_dims(dims, dtype, &d);
+  if (s != SSD_OK) return s;
+  if (!req(x) || !req(dt) || !req(A) || !req(B) || !req(C) || !opt(D) || !opt(h0) ||
+      !req(gy) || !opt(gfinal) || !req(dx) || !req(ddt) || !req(dA) || !req(dB) || !req(dC) ||
+      !opt(dD) || !opt(dh0) || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      n_events < 0 || (n_events > 0 && !events))
+    return SSD_ERR_INVALID_ARG;
+  const BwdLayout w = bwd_layout(d);
+  if (ws_bytes < w.total) return SSD_ERR_INVALID_ARG;
+  int *err = static_cast<int *>(workspace);
+  char *ws = static_cast<char *>(workspace);
+  auto f = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
+  const float *xf = static_cast<const float *>(x), *dtf = static_cast<const float *>(dt),
+              *Bf = static_cast<const float *>(B), *Cf = static_cast<const float *>(C),
+              *gyf = static_cast<const float *>(gy);
+  float *G = f(w.G), *dst = f(w.dst), *sts = f(w.states), *R = f(w.R), *fin = f(w.fin);
+  // with one head per group the per-head shares of dB and dC are dB and dC
+  float *dBh = d.hpg > 1 ? f(w.dBh) : static_cast<float *>(dB);
+  float *dCh = d.hpg > 1 ? f(w.dCh) : static_cast<float *>(dC);
+  int launched = 0;
+  auto mark = [&](int i) -> cudaError_t {
+    if (events && i < n_events) return cudaEventRecord((cudaEvent_t)events[i], st);
+    return cudaSuccess;
+  };
+  // runs one launch unless an earlier step failed, then records its event
+  cudaError_t e = mark(0);
+  auto step = [&](auto &&launch) {
+    if (e == cudaSuccess) e = launch();
+    if (e == cudaSuccess) e = mark(++launched);
+  };
+  // the forward's cumsum, jump terms, start states and final state, all in
+  // fp32 (the forward's own jump kernels take TF32 products)
+  step([&] { return ssd::launch_chunk_cumsum(d, dtype, dt, A, G, err, st); });
+  step([&] { return ssd::launch_bwd_jump(d, xf, Bf, dtf, G, dst, err, st); });
+  step([&] { return ssd::launch_state_passing(d, dst, G, h0, sts, fin, err, st); });
+  // the adjoint: its jump terms (over the forward's, no longer needed), the
+  // backward pass over chunks for R_k and dh0, then the per-token gradients
+  step([&] { return ssd::launch_bwd_jump(d, gyf, Cf, nullptr, G, dst, err, st); });
+  step([&] {
+    return ssd::launch_state_passing(d, dst, G, gfinal, R, dh0, err, st, false, true);
+  });
+  step([&] {
+    return ssd::launch_bwd_main(d, xf, dtf, Bf, Cf, D, gyf, G, sts, R,
+                                static_cast<float *>(dx), dBh, dCh, f(w.qB), f(w.dG),
+                                f(w.gyx), err, st);
+  });
+  float2 *part = reinterpret_cast<float2 *>(ws + w.part);
+  step([&] {
+    return ssd::launch_bwd_finish(d, dtf, A, R, sts, fin, f(w.qB), f(w.dG), f(w.gyx),
+                                  static_cast<float *>(ddt), part, err, st);
+  });
+  step([&] {
+    return ssd::launch_bwd_reduce(d, dBh, dCh, part, static_cast<float *>(dB),
+                                  static_cast<float *>(dC), dA, dD, st);
+  });
+  if (n_launches) *n_launches = launched;
+  return from_cuda(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -697,48 +765,20 @@ ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, co
                         const float *h0, const void *gy, const float *gfinal, void *dx,
                         void *ddt, float *dA, void *dB, void *dC, float *dD, float *dh0,
                         void *workspace, size_t ws_bytes, void *stream) {
-  Dims d;
-  ssd_status s = check_backward_dims(dims, dtype, &d);
-  if (s != SSD_OK) return s;
-  if (!req(x) || !req(dt) || !req(A) || !req(B) || !req(C) || !opt(D) || !opt(h0) ||
-      !req(gy) || !opt(gfinal) || !req(dx) || !req(ddt) || !req(dA) || !req(dB) || !req(dC) ||
-      !opt(dD) || !opt(dh0) || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return SSD_ERR_INVALID_ARG;
-  const BwdLayout w = bwd_layout(d);
-  if (ws_bytes < w.total) return SSD_ERR_INVALID_ARG;
-  cudaStream_t st = (cudaStream_t)stream;
-  int *err = static_cast<int *>(workspace);
-  char *ws = static_cast<char *>(workspace);
-  auto f = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
-  const float *xf = static_cast<const float *>(x), *dtf = static_cast<const float *>(dt),
-              *Bf = static_cast<const float *>(B), *Cf = static_cast<const float *>(C),
-              *gyf = static_cast<const float *>(gy);
-  float *G = f(w.G), *dst = f(w.dst), *sts = f(w.states), *R = f(w.R), *fin = f(w.fin);
-  // with one head per group the per-head shares of dB and dC are dB and dC
-  float *dBh = d.hpg > 1 ? f(w.dBh) : static_cast<float *>(dB);
-  float *dCh = d.hpg > 1 ? f(w.dCh) : static_cast<float *>(dC);
-  cudaError_t e = cudaSuccess;
-  // the forward's cumsum, jump terms, start states and final state, all in
-  // fp32 (the forward's own jump kernels take TF32 products)
-  e = ssd::launch_chunk_cumsum(d, dtype, dt, A, G, err, st);
-  if (e == cudaSuccess) e = ssd::launch_bwd_jump(d, xf, Bf, dtf, G, dst, err, st);
-  if (e == cudaSuccess) e = ssd::launch_state_passing(d, dst, G, h0, sts, fin, err, st);
-  // the adjoint: its jump terms (over the forward's, no longer needed), the
-  // backward pass over chunks for R_k and dh0, then the per-token gradients
-  if (e == cudaSuccess) e = ssd::launch_bwd_jump(d, gyf, Cf, nullptr, G, dst, err, st);
-  if (e == cudaSuccess)
-    e = ssd::launch_state_passing(d, dst, G, gfinal, R, dh0, err, st, false, true);
-  if (e == cudaSuccess)
-    e = ssd::launch_bwd_main(d, xf, dtf, Bf, Cf, D, gyf, G, sts, R, static_cast<float *>(dx),
-                             dBh, dCh, f(w.qB), f(w.dG), f(w.gyx), err, st);
-  float2 *part = reinterpret_cast<float2 *>(ws + w.part);
-  if (e == cudaSuccess)
-    e = ssd::launch_bwd_finish(d, dtf, A, R, sts, fin, f(w.qB), f(w.dG), f(w.gyx),
-                               static_cast<float *>(ddt), part, err, st);
-  if (e == cudaSuccess)
-    e = ssd::launch_bwd_reduce(d, dBh, dCh, part, static_cast<float *>(dB),
-                               static_cast<float *>(dC), dA, dD, st);
-  return from_cuda(e);
+  return backward_impl(dims, dtype, x, dt, A, B, C, D, h0, gy, gfinal, dx, ddt, dA, dB, dC, dD,
+                       dh0, workspace, ws_bytes, (cudaStream_t)stream, nullptr, 0, nullptr);
+}
+
+ssd_status ssd_backward_profiled(const ssd_dims *dims, ssd_dtype dtype, const void *x,
+                                 const void *dt, const float *A, const void *B, const void *C,
+                                 const float *D, const float *h0, const void *gy,
+                                 const float *gfinal, void *dx, void *ddt, float *dA, void *dB,
+                                 void *dC, float *dD, float *dh0, void *workspace,
+                                 size_t ws_bytes, void *stream, void *const *events,
+                                 int n_events, int *n_launches) {
+  return backward_impl(dims, dtype, x, dt, A, B, C, D, h0, gy, gfinal, dx, ddt, dA, dB, dC, dD,
+                       dh0, workspace, ws_bytes, (cudaStream_t)stream, events, n_events,
+                       n_launches);
 }
 
 }  // extern "C"
