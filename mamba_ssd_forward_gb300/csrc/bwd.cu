@@ -106,14 +106,225 @@ bwd_jump_kernel(const float *__restrict__ v, const float *__restrict__ m,
 
 // -------------------------------------------------------------- main kernel
 
-// One CTA per (32-token tile of a chunk, chunk, batch * head); thread = (token
-// tt = tid / 8 of the tile, lane l8 = tid % 8), the lane holding columns
-// l8 + 8 m of its token's outputs and the 8 lanes of a token splitting every
-// dot product.  Shared memory (row strides padded by one float): the tile's
-// B, C, x, gy; one other tile at a time (C and gy for the s >= t sums, B and
-// x for the j <= t sums); the chunk's G and dt; R_k, then h_k, as [P][S].
-template <int kS>
-__global__ void __launch_bounds__(kThreads)
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool full) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem),
+               "r"(full ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ float dot4(const float4 &a, const float4 &b, float s) {
+  s = fmaf(a.x, b.x, s);
+  s = fmaf(a.y, b.y, s);
+  s = fmaf(a.z, b.z, s);
+  return fmaf(a.w, b.w, s);
+}
+__device__ __forceinline__ void axpy4(float a, const float4 &v, float4 &acc) {
+  acc.x = fmaf(a, v.x, acc.x);
+  acc.y = fmaf(a, v.y, acc.y);
+  acc.z = fmaf(a, v.z, acc.z);
+  acc.w = fmaf(a, v.w, acc.w);
+}
+__device__ __forceinline__ float comp(const float4 &v, int e) {
+  return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ void add_comp(float4 &v, int e, float a) {
+  if (e == 0) v.x += a;
+  else if (e == 1) v.y += a;
+  else if (e == 2) v.z += a;
+  else v.w += a;
+}
+__device__ __forceinline__ float sum8(float v) {  // over the 8 lanes of a token group
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  return v + __shfl_xor_sync(0xffffffffu, v, 4);
+}
+
+// Shared-memory plan of bwd_main_kernel (float4 units): two column tiles
+// U1 [NT][S/4] and U2 [NT][P/4] (double-buffered), the row tile's own rows
+// O1 [RT][S/4] and O2 [RT][P/4], the state Ms [P][S/4] (float4 slots XOR-
+// swizzled by bits 2..4 of the row), then G and dt of the chunk (256 each).
+template <int kS, int kTok>
+struct MainSmem {
+  static constexpr int RT = kTT * kTok, NT = kTT, S4 = kS / 4, P4 = kP / 4;
+  static constexpr int U1 = 0, U2 = U1 + 2 * NT * S4, O1 = U2 + 2 * NT * P4, O2 = O1 + RT * S4,
+                       Ms = O2 + RT * P4, end4 = Ms + kP * S4;
+  static constexpr size_t bytes = 16 * (size_t)end4 + 2 * 256 * sizeof(float);
+};
+
+// One CTA per (row tile of RT = 32 kTok tokens of a chunk, chunk, batch *
+// head), 256 threads: thread = (token group grp = tid / 8, lane l8 = tid % 8),
+// the group owning tokens grp + 32 r (r < kTok) of the tile and lane l8 the
+// feature columns 32 i + 4 l8 .. +3 of every row (float4 slot 8 i + l8).
+// Each lane keeps its slice of its tokens' own rows in registers; the 8
+// lanes of a group split every dot product and sum it with three shuffles.
+// Two passes over the chunk's 32-token column tiles, each tile double-
+// buffered through cp.async:
+//   upper (columns s >= t): dx_t += dt_t w (B_t . C_s) gy_s,
+//                           q_t  += w (x_t . gy_s) C_s,  w = exp2(G_s - G_t);
+//   lower (columns j <= t): ysm_t += w (C_t . B_j) x_j,
+//                           dC_t  += w (gy_t . x_j) B_j,  w = exp2(G_t - G_j) dt_j;
+// each followed by its state terms (R_k after the upper pass, h_k after the
+// lower one) from the state staged in shared memory.
+template <int kS, int kTok, bool kUpper>
+__device__ __forceinline__ void main_pass(
+    float4 *sm4, float *Gs, float *ds, const float *own_g, const float *own_h,
+    const float *col_g, const float *col_h, const float *state, int64_t st_row,
+    float4 (&accP)[kTok][kP / 32], float4 (&accS)[kTok][kS / 32],
+    float4 (&rS)[kTok][kS / 32], float4 (&rP)[kTok][kP / 32], const int (&t)[kTok],
+    const bool (&live)[kTok], int tau, int valid, int64_t rowh0, int64_t rowg0, int nh, int ng,
+    int tid, int l8, int grp) {
+  using SM = MainSmem<kS, kTok>;
+  constexpr int RT = SM::RT, NT = SM::NT, S4 = SM::S4, P4 = SM::P4;
+  constexpr int QS = kS / 32, QP = kP / 32;
+  float4 *U1 = sm4 + SM::U1, *U2 = sm4 + SM::U2, *O1 = sm4 + SM::O1, *O2 = sm4 + SM::O2,
+         *Ms = sm4 + SM::Ms;
+  // stage `rows` tokens from chunk-relative token t0 of a per-group (width
+  // S) or per-head (width P) tensor, zeros past the sequence
+  auto stage = [&](float4 *dst, const float *src, bool per_head, int t0, int rows) {
+    const int W4 = per_head ? P4 : S4;
+    for (int e = tid; e < rows * W4; e += kThreads) {
+      const int r = e / W4, c = e - r * W4, tok = t0 + r;
+      const bool ok = tok < valid;
+      const int64_t row = per_head ? rowh0 + (int64_t)(ok ? tok : 0) * nh
+                                   : rowg0 + (int64_t)(ok ? tok : 0) * ng;
+      cp_async16(dst + e, src + row * (W4 * 4) + c * 4, ok);
+    }
+  };
+  float Gt[kTok], dtt[kTok];
+#pragma unroll
+  for (int r = 0; r < kTok; ++r) {
+    Gt[r] = Gs[t[r]];
+    dtt[r] = ds[t[r]];
+    // this token's own rows: B_t, x_t (upper) or C_t, gy_t (lower)
+#pragma unroll
+    for (int i = 0; i < QS; ++i)
+      rS[r][i] = live[r] ? *reinterpret_cast<const float4 *>(
+                               own_g + (rowg0 + (int64_t)t[r] * ng) * kS + 32 * i + 4 * l8)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < QP; ++i)
+      rP[r][i] = live[r] ? *reinterpret_cast<const float4 *>(
+                               own_h + (rowh0 + (int64_t)t[r] * nh) * kP + 32 * i + 4 * l8)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int ucount = (valid + NT - 1) / NT;
+  const int u0 = kUpper ? tau * kTok : 0;
+  const int u1 = kUpper ? ucount : min(ucount, tau * kTok + kTok);
+  __syncthreads();  // the buffers of the previous pass are free
+  stage(O1, own_g, false, tau * RT, RT);
+  stage(O2, own_h, true, tau * RT, RT);
+  stage(U1, col_g, false, u0 * NT, NT);
+  stage(U2, col_h, true, u0 * NT, NT);
+  cp_async_commit();
+  for (int u = u0; u < u1; ++u) {
+    const int cur = (u - u0) & 1;
+    if (u + 1 < u1) {
+      stage(U1 + (cur ^ 1) * NT * S4, col_g, false, (u + 1) * NT, NT);
+      stage(U2 + (cur ^ 1) * NT * P4, col_h, true, (u + 1) * NT, NT);
+    }
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    const float4 *u1p = U1 + cur * NT * S4 + l8, *u2p = U2 + cur * NT * P4 + l8;
+#pragma unroll 2
+    for (int j = 0; j < NT; ++j) {
+      const int s = u * NT + j;
+      float4 cS[QS], cP[QP];
+#pragma unroll
+      for (int i = 0; i < QS; ++i) cS[i] = u1p[j * S4 + 8 * i];
+#pragma unroll
+      for (int i = 0; i < QP; ++i) cP[i] = u2p[j * P4 + 8 * i];
+      float d1[kTok], d2[kTok];
+#pragma unroll
+      for (int r = 0; r < kTok; ++r) {
+        float a = 0.f, c = 0.f;
+#pragma unroll
+        for (int i = 0; i < QS; ++i) a = dot4(rS[r][i], cS[i], a);
+#pragma unroll
+        for (int i = 0; i < QP; ++i) c = dot4(rP[r][i], cP[i], c);
+        d1[r] = sum8(a);
+        d2[r] = sum8(c);
+      }
+      const float Gc = Gs[s], dc = ds[s];
+#pragma unroll
+      for (int r = 0; r < kTok; ++r) {
+        float w = 0.f;
+        if (kUpper) {
+          if (s >= t[r] && s < valid && live[r]) w = exp2f(Gc - Gt[r]);
+        } else {
+          if (s <= t[r] && live[r]) w = exp2f(Gt[r] - Gc) * dc;  // dt = 0 past the sequence
+        }
+        // upper: dx += dt_t w (B_t . C_s) gy_s, q += w (x_t . gy_s) C_s;
+        // lower: ysm += w (C_t . B_j) x_j,      dC += w (gy_t . x_j) B_j
+        const float aP = (kUpper ? dtt[r] : 1.f) * w * d1[r], aS = w * d2[r];
+#pragma unroll
+        for (int i = 0; i < QP; ++i) axpy4(aP, cP[i], accP[r][i]);
+#pragma unroll
+        for (int i = 0; i < QS; ++i) axpy4(aS, cS[i], accS[r][i]);
+      }
+    }
+    __syncthreads();  // tile u's buffer is refilled two iterations on
+  }
+  cp_async_wait<0>();
+  // the state terms: M = R_k (upper: dx += dt_t exp2(G_last - G_t) R B_t,
+  // q += exp2(G_last - G_t) R^T x_t) or h_k (lower: ysm += exp2(G_t) h c_t,
+  // dC += exp2(G_t) h^T gy_t), M staged with float4 slot c4 of row p at
+  // c4 ^ ((p >> 2) & 7)
+  for (int e = tid; e < kP * S4; e += kThreads) {
+    const int p = e / S4, c4 = e - p * S4;
+    Ms[p * S4 + (c4 ^ ((p >> 2) & 7))] =
+        *reinterpret_cast<const float4 *>(state + st_row + 4 * (int64_t)e);
+  }
+  __syncthreads();
+  const float GL = Gs[valid - 1];
+  float fP[kTok], fS[kTok];
+#pragma unroll
+  for (int r = 0; r < kTok; ++r) {
+    const float f = live[r] ? (kUpper ? exp2f(GL - Gt[r]) : exp2f(Gt[r])) : 0.f;
+    fS[r] = f;
+    fP[r] = kUpper ? dtt[r] * f : f;
+  }
+  // accP[p] += fP sum_s M[p][s] O1_t[s] over this lane's rows p = 32 i + 4 l8 + e
+  for (int c4 = 0; c4 < S4; ++c4) {
+    float4 o[kTok];
+#pragma unroll
+    for (int r = 0; r < kTok; ++r) o[r] = O1[(kTT * r + grp) * S4 + c4];
+#pragma unroll
+    for (int i = 0; i < QP; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float4 m = Ms[(32 * i + 4 * l8 + e) * S4 + (c4 ^ l8)];
+#pragma unroll
+        for (int r = 0; r < kTok; ++r) add_comp(accP[r][i], e, fP[r] * dot4(m, o[r], 0.f));
+      }
+  }
+  // accS[s] += fS sum_p M[p][s] O2_t[p] over this lane's columns (slot 8 i + l8)
+  for (int p4 = 0; p4 < P4; ++p4) {
+    float4 o[kTok];
+#pragma unroll
+    for (int r = 0; r < kTok; ++r) o[r] = O2[(kTT * r + grp) * P4 + p4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int p = 4 * p4 + e;
+#pragma unroll
+      for (int i = 0; i < QS; ++i) {
+        const float4 m = Ms[p * S4 + ((8 * i + l8) ^ (p4 & 7))];
+#pragma unroll
+        for (int r = 0; r < kTok; ++r) axpy4(fS[r] * comp(o[r], e), m, accS[r][i]);
+      }
+    }
+  }
+}
+
+template <int kS, int kTok>
+__global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
                 const float *__restrict__ Bm, const float *__restrict__ Cm,
                 const float *__restrict__ D, const float *__restrict__ gy,
@@ -122,175 +333,100 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
                 float *__restrict__ dBh, float *__restrict__ dCh, float *__restrict__ qB,
                 float *__restrict__ dG, float *__restrict__ gyx, int *err, int L, int nh,
                 int hpg, int T, int nc, int nb) {
-  constexpr int SP = kS + 1, PP = kP + 1;
-  constexpr int kMS = kS / 8, kMP = kP / 8;
-  extern __shared__ float sm[];
-  float *Bt = sm;                 // [32][SP]
-  float *Ct = Bt + kTT * SP;      // [32][SP]
-  float *xt = Ct + kTT * SP;      // [32][PP]
-  float *gt = xt + kTT * PP;      // [32][PP]
-  float *U1 = gt + kTT * PP;      // [32][SP]  other tile: C (upper) or B (lower)
-  float *U2 = U1 + kTT * SP;      // [32][PP]  other tile: gy (upper) or x (lower)
-  float *Gs = U2 + kTT * PP;      // [256]
-  float *ds = Gs + 256;           // [256]
-  float *M = ds + 256;            // [64][SP]  R_k, then h_k
-
-  const int ntile = T / kTT;
+  using SM = MainSmem<kS, kTok>;
+  constexpr int RT = SM::RT, QS = kS / 32, QP = kP / 32;
+  extern __shared__ float4 sm4[];
+  float *Gs = reinterpret_cast<float *>(sm4 + SM::end4);
+  float *ds = Gs + 256;
+  const int ntile = T / RT;
   const int k = blockIdx.x / ntile, tau = blockIdx.x - k * ntile;
   const int bh = blockIdx.y, b = bh / nh, h = bh - b * nh, g = h / hpg, ng = nh / hpg;
   const int tok0 = k * T, valid = min(T, L - tok0);
-  const int tid = threadIdx.x, tt = tid >> 3, l8 = tid & 7;
+  const int tid = threadIdx.x, grp = tid >> 3, l8 = tid & 7;
   if (!SSD_IN_BOUNDS(b < nb && k < nc, err, 201)) return;  // uniform over the CTA
-  if (tau * kTT >= valid) return;                           // tile past the sequence
-  const int t = tau * kTT + tt;                             // chunk-relative token
-  const bool live = t < valid;
-
-  auto row_x = [&](int tok) { return (((int64_t)b * L + tok0 + tok) * nh + h) * kP; };
-  auto row_g = [&](int tok) { return (((int64_t)b * L + tok0 + tok) * ng + g) * kS; };
-  // load a 32-token tile of a [b, L, (heads or groups), width] tensor into a
-  // padded shared array (zeros past the sequence)
-  auto load_tile = [&](float *dst, int stride, const float *src, int width, bool per_head,
-                       int u) {
-    for (int e = tid; e < kTT * width; e += kThreads) {
-      const int r = e / width, c = e - r * width, tok = u * kTT + r;
-      float v = 0.f;
-      if (tok < valid) v = src[(per_head ? row_x(tok) : row_g(tok)) + c];
-      dst[r * stride + c] = v;
-    }
-  };
+  if (tau * RT >= valid) return;                            // tile past the sequence
+  int t[kTok];
+  bool live[kTok];
+#pragma unroll
+  for (int r = 0; r < kTok; ++r) {
+    t[r] = tau * RT + kTT * r + grp;
+    live[r] = t[r] < valid;
+  }
+  // row indices (in rows of the width) of the chunk's token 0
+  const int64_t rowh0 = ((int64_t)b * L + tok0) * nh + h, rowg0 = ((int64_t)b * L + tok0) * ng + g;
   const float *Gc = G + ((int64_t)bh * nc + k) * T;
   for (int i = tid; i < T; i += kThreads) {
     Gs[i] = Gc[i];
-    ds[i] = i < valid ? dt[((int64_t)b * L + tok0 + i) * nh + h] : 0.f;
+    ds[i] = i < valid ? dt[rowh0 + (int64_t)i * nh] : 0.f;
   }
-  load_tile(Bt, SP, Bm, kS, false, tau);
-  load_tile(Ct, SP, Cm, kS, false, tau);
-  load_tile(xt, PP, x, kP, true, tau);
-  load_tile(gt, PP, gy, kP, true, tau);
   __syncthreads();
-  const float Gt = Gs[min(t, T - 1)], dtt = ds[min(t, T - 1)];
-  const float GL = Gs[valid - 1];
-
-  float dxs[kMP], ysm[kMP], q[kMS], dc[kMS];
-#pragma unroll
-  for (int m = 0; m < kMP; ++m) dxs[m] = ysm[m] = 0.f;
-#pragma unroll
-  for (int m = 0; m < kMS; ++m) q[m] = dc[m] = 0.f;
-  // the dot product of this token's row a and row j of b over a width, split
-  // over the 8 lanes of the token
-  auto dot8 = [&](const float *a, const float *bb, int width) {
-    float s = 0.f;
-    for (int c = l8; c < width; c += 8) s = fmaf(a[c], bb[c], s);
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    s += __shfl_xor_sync(0xffffffffu, s, 4);
-    return s;
-  };
-
-  // s >= t: dx += dt_t exp2(G_s - G_t) (B_t . C_s) gy_s,  q += exp2(G_s - G_t) (gy_s . x_t) C_s
-  for (int u = tau; u < ntile && u * kTT < valid; ++u) {
-    __syncthreads();
-    load_tile(U1, SP, Cm, kS, false, u);
-    load_tile(U2, PP, gy, kP, true, u);
-    __syncthreads();
-    for (int j = 0; j < kTT; ++j) {
-      const int s = u * kTT + j;
-      const float S1 = dot8(Bt + tt * SP, U1 + j * SP, kS);
-      const float X1 = dot8(xt + tt * PP, U2 + j * PP, kP);
-      const float w = (s >= t && s < valid && live) ? exp2f(Gs[s] - Gt) : 0.f;
-      const float a1 = dtt * w * S1, b1 = w * X1;
-#pragma unroll
-      for (int m = 0; m < kMP; ++m) dxs[m] = fmaf(a1, U2[j * PP + l8 + 8 * m], dxs[m]);
-#pragma unroll
-      for (int m = 0; m < kMS; ++m) q[m] = fmaf(b1, U1[j * SP + l8 + 8 * m], q[m]);
-    }
-  }
-  // j <= t: ysm += exp2(G_t - G_j) dt_j (c_t . B_j) x_j,  dC += exp2(G_t - G_j) dt_j (gy_t . x_j) B_j
-  for (int u = 0; u <= tau; ++u) {
-    __syncthreads();
-    load_tile(U1, SP, Bm, kS, false, u);
-    load_tile(U2, PP, x, kP, true, u);
-    __syncthreads();
-    for (int j = 0; j < kTT; ++j) {
-      const int jj = u * kTT + j;
-      const float S2 = dot8(Ct + tt * SP, U1 + j * SP, kS);
-      const float X2 = dot8(gt + tt * PP, U2 + j * PP, kP);
-      const float w = (jj <= t && jj < valid && live) ? exp2f(Gt - Gs[jj]) * ds[jj] : 0.f;
-      const float a2 = w * S2, b2 = w * X2;
-#pragma unroll
-      for (int m = 0; m < kMP; ++m) ysm[m] = fmaf(a2, U2[j * PP + l8 + 8 * m], ysm[m]);
-#pragma unroll
-      for (int m = 0; m < kMS; ++m) dc[m] = fmaf(b2, U1[j * SP + l8 + 8 * m], dc[m]);
-    }
-  }
-  // state terms: R_k (dx: R B_t; q: R^T x_t), then h_k (ysm: h c_t; dC: h^T gy_t)
   const int64_t st_row = ((int64_t)bh * nc + k) * kP * kS;
-  for (int pass = 0; pass < 2; ++pass) {
-    __syncthreads();
-    const float *src = pass == 0 ? R + st_row : states + st_row;
-    for (int e = tid; e < kP * kS; e += kThreads) M[(e / kS) * SP + e % kS] = src[e];
-    __syncthreads();
-    const float fa = pass == 0 ? (live ? dtt * exp2f(GL - Gt) : 0.f) : (live ? exp2f(Gt) : 0.f);
-    const float fb = pass == 0 ? (live ? exp2f(GL - Gt) : 0.f) : fa;
-    const float *va = pass == 0 ? Bt + tt * SP : Ct + tt * SP;  // [S]
-    const float *vb = pass == 0 ? xt + tt * PP : gt + tt * PP;  // [P]
+  float4 rS[kTok][QS], rP[kTok][QP], aP[kTok][QP], aS[kTok][QS];
+  auto zero = [&]() {
 #pragma unroll
-    for (int m = 0; m < kMP; ++m) {  // rows p = l8 + 8 m: M[p] . va
-      const float *row = M + (l8 + 8 * m) * SP;
-      float s = 0.f;
-      for (int c = 0; c < kS; ++c) s = fmaf(row[c], va[c], s);
-      if (pass == 0)
-        dxs[m] = fmaf(fa, s, dxs[m]);
-      else
-        ysm[m] = fmaf(fa, s, ysm[m]);
-    }
+    for (int r = 0; r < kTok; ++r) {
 #pragma unroll
-    for (int m = 0; m < kMS; ++m) {  // columns s = l8 + 8 m: M[:, s] . vb
-      float s = 0.f;
-      for (int p = 0; p < kP; ++p) s = fmaf(M[p * SP + l8 + 8 * m], vb[p], s);
-      if (pass == 0)
-        q[m] = fmaf(fb, s, q[m]);
-      else
-        dc[m] = fmaf(fb, s, dc[m]);
+      for (int i = 0; i < QP; ++i) aP[r][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < QS; ++i) aS[r][i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-  }
-  // outputs of this token
+  };
+  // upper pass: dx and q (rS = B_t, rP = x_t)
+  zero();
+  main_pass<kS, kTok, true>(sm4, Gs, ds, Bm, x, Cm, gy, R, st_row, aP, aS, rS, rP, t, live, tau,
+                            valid, rowh0, rowg0, nh, ng, tid, l8, grp);
   const float Dh = D ? D[h] : 0.f;
-  float gdot = 0.f, xdot = 0.f, qb = 0.f, gx = 0.f;
+  float xdot[kTok], qb[kTok], gx[kTok];
 #pragma unroll
-  for (int m = 0; m < kMP; ++m) {
-    const int p = l8 + 8 * m;
-    gdot = fmaf(gt[tt * PP + p], ysm[m], gdot);
-    xdot = fmaf(xt[tt * PP + p], dxs[m], xdot);
-    gx = fmaf(gt[tt * PP + p], xt[tt * PP + p], gx);
+  for (int r = 0; r < kTok; ++r) {
+    float xd = 0.f, qv = 0.f, gv = 0.f;
+    const int64_t rh = rowh0 + (int64_t)t[r] * nh;
+#pragma unroll
+    for (int i = 0; i < QP; ++i) {
+      const float4 gq = live[r] ? *reinterpret_cast<const float4 *>(gy + rh * kP + 32 * i + 4 * l8)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+      xd = dot4(rP[r][i], aP[r][i], xd);  // x_t . (dx_t - D gy_t)
+      gv = dot4(rP[r][i], gq, gv);        // x_t . gy_t
+      if (live[r]) {
+        float4 o = aP[r][i];
+        axpy4(Dh, gq, o);
+        *reinterpret_cast<float4 *>(dx + rh * kP + 32 * i + 4 * l8) = o;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < QS; ++i) {
+      qv = dot4(aS[r][i], rS[r][i], qv);  // q_t . B_t
+      if (live[r]) {
+        const float4 a = aS[r][i];
+        *reinterpret_cast<float4 *>(dBh + rh * kS + 32 * i + 4 * l8) =
+            make_float4(ds[t[r]] * a.x, ds[t[r]] * a.y, ds[t[r]] * a.z, ds[t[r]] * a.w);
+      }
+    }
+    xdot[r] = sum8(xd);
+    qb[r] = sum8(qv);
+    gx[r] = sum8(gv);
   }
+  // lower pass: ysm and dC (rS = C_t, rP = gy_t)
+  zero();
+  main_pass<kS, kTok, false>(sm4, Gs, ds, Cm, gy, Bm, x, states, st_row, aP, aS, rS, rP, t,
+                             live, tau, valid, rowh0, rowg0, nh, ng, tid, l8, grp);
 #pragma unroll
-  for (int m = 0; m < kMS; ++m) qb = fmaf(q[m], Bt[tt * SP + l8 + 8 * m], qb);
+  for (int r = 0; r < kTok; ++r) {
+    float gd = 0.f;
 #pragma unroll
-  for (int o = 1; o < 8; o <<= 1) {
-    gdot += __shfl_xor_sync(0xffffffffu, gdot, o);
-    xdot += __shfl_xor_sync(0xffffffffu, xdot, o);
-    qb += __shfl_xor_sync(0xffffffffu, qb, o);
-    gx += __shfl_xor_sync(0xffffffffu, gx, o);
-  }
-  if (!live) return;  // no barrier follows
-  const int64_t rx = row_x(t);
+    for (int i = 0; i < QP; ++i) gd = dot4(rP[r][i], aP[r][i], gd);  // gy_t . ysm_t
+    gd = sum8(gd);
+    if (!live[r]) continue;
+    const int64_t rh = rowh0 + (int64_t)t[r] * nh;
 #pragma unroll
-  for (int m = 0; m < kMP; ++m) {
-    const int p = l8 + 8 * m;
-    dx[rx + p] = dxs[m] + Dh * gt[tt * PP + p];
-  }
-  const int64_t rs = (((int64_t)b * L + tok0 + t) * nh + h) * kS;
-#pragma unroll
-  for (int m = 0; m < kMS; ++m) {
-    dBh[rs + l8 + 8 * m] = dtt * q[m];
-    dCh[rs + l8 + 8 * m] = dc[m];
-  }
-  if (l8 == 0) {
-    const int64_t o = ((int64_t)bh * nc + k) * T + t;
-    qB[o] = qb;
-    dG[o] = gdot - xdot;
-    gyx[o] = gx;
+    for (int i = 0; i < QS; ++i)
+      *reinterpret_cast<float4 *>(dCh + rh * kS + 32 * i + 4 * l8) = aS[r][i];
+    if (l8 == 0) {
+      const int64_t o = ((int64_t)bh * nc + k) * T + t[r];
+      qB[o] = qb[r];
+      dG[o] = gd - xdot[r];
+      gyx[o] = gx[r];
+    }
   }
 }
 
@@ -413,11 +549,6 @@ bool bwd_supported(const Dims &d) {
   return d.P == kP && (d.S == 64 || d.S == 128 || d.S == 256) && d.T % kTT == 0 && d.T <= 256;
 }
 
-size_t bwd_main_smem(const Dims &d) {
-  const int SP = (int)d.S + 1, PP = kP + 1;
-  return sizeof(float) * (size_t)(3 * kTT * SP + 3 * kTT * PP + 512 + 64 * SP);
-}
-
 cudaError_t launch_bwd_jump(const Dims &d, const float *v, const float *m, const float *dt,
                             const float *G, float *out, int *err, cudaStream_t st) {
   dim3 grid((unsigned)d.nc, (unsigned)(d.b * d.nh));
@@ -431,44 +562,41 @@ cudaError_t launch_bwd_jump(const Dims &d, const float *v, const float *m, const
   return cudaGetLastError();
 }
 
+namespace {
+template <int kS, int kTok>
+cudaError_t launch_main(const Dims &d, const float *x, const float *dt, const float *B,
+                        const float *C, const float *D, const float *gy, const float *G,
+                        const float *states, const float *R, float *dx, float *dBh, float *dCh,
+                        float *qB, float *dG, float *gyx, int *err, cudaStream_t st) {
+  const size_t smem = MainSmem<kS, kTok>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<kS, kTok>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)(d.nc * (d.T / (kTT * kTok))), (unsigned)(d.b * d.nh));
+  bwd_main_kernel<kS, kTok><<<grid, kThreads, smem, st>>>(
+      x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG, gyx, err, (int)d.L, (int)d.nh,
+      (int)d.hpg, (int)d.T, (int)d.nc, (int)d.b);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_bwd_main(const Dims &d, const float *x, const float *dt, const float *B,
                             const float *C, const float *D, const float *gy, const float *G,
                             const float *states, const float *R, float *dx, float *dBh,
                             float *dCh, float *qB, float *dG, float *gyx, int *err,
                             cudaStream_t st) {
-  dim3 grid((unsigned)(d.nc * (d.T / kTT)), (unsigned)(d.b * d.nh));
-  const size_t smem = bwd_main_smem(d);
-  const int L = (int)d.L, nh = (int)d.nh, hpg = (int)d.hpg, T = (int)d.T, nc = (int)d.nc,
-            nb = (int)d.b;
-  cudaError_t e = cudaSuccess;
+  // two tokens per thread where the registers allow (dstate up to 128)
   switch (d.S) {
     case 64:
-      e = cudaFuncSetAttribute(bwd_main_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
-      if (e == cudaSuccess)
-        bwd_main_kernel<64><<<grid, kThreads, smem, st>>>(x, dt, B, C, D, gy, G, states, R, dx,
-                                                          dBh, dCh, qB, dG, gyx, err, L, nh,
-                                                          hpg, T, nc, nb);
-      break;
+      return launch_main<64, 2>(d, x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG, gyx,
+                                err, st);
     case 128:
-      e = cudaFuncSetAttribute(bwd_main_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
-      if (e == cudaSuccess)
-        bwd_main_kernel<128><<<grid, kThreads, smem, st>>>(x, dt, B, C, D, gy, G, states, R, dx,
-                                                           dBh, dCh, qB, dG, gyx, err, L, nh,
-                                                           hpg, T, nc, nb);
-      break;
+      return launch_main<128, 2>(d, x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG, gyx,
+                                 err, st);
     default:
-      e = cudaFuncSetAttribute(bwd_main_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
-      if (e == cudaSuccess)
-        bwd_main_kernel<256><<<grid, kThreads, smem, st>>>(x, dt, B, C, D, gy, G, states, R, dx,
-                                                           dBh, dCh, qB, dG, gyx, err, L, nh,
-                                                           hpg, T, nc, nb);
-      break;
+      return launch_main<256, 1>(d, x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG, gyx,
+                                 err, st);
   }
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_finish(const Dims &d, const float *dt, const float *A, const float *R,
