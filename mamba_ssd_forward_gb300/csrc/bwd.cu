@@ -36,6 +36,8 @@
 // All in fp32 on the CUDA cores (the tensor-core version is the next step):
 // about 30 million multiply-adds per chunk and head at T = 256, P = 64,
 // S = 128.
+#include <type_traits>
+
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -45,66 +47,7 @@ constexpr int kThreads = 256;
 constexpr int kTT = 32;  // tokens per tile of bwd_main_kernel
 constexpr int kP = 64;
 
-// ---------------------------------------------------------------- jump terms
-
-// out[b, h, k][p][s] = sum_{t in chunk k} w_t v_t[p] m_t[s], v per head
-// ([b, L, nh, P]) and m per group ([b, L, ng, S]): the adjoint's jump terms
-// (v = gy, m = C, w_t = exp2(G_t); dt null) or the forward's (v = x, m = B,
-// w_t = exp2(G_last - G_t) dt_t).  One CTA per (chunk, batch * head),
-// thread = kS / 4 outputs (e = tid + 256 i: p = e / S, s = e % S; a warp's
-// lanes share p and read consecutive s).
-template <int kS>
-__global__ void __launch_bounds__(kThreads)
-bwd_jump_kernel(const float *__restrict__ v, const float *__restrict__ m,
-                const float *__restrict__ dt, const float *__restrict__ G,
-                float *__restrict__ out, int *err, int L, int nh, int hpg, int T, int nc,
-                int nb) {
-  constexpr int kPer = kP * kS / kThreads;
-  const int ng = nh / hpg;
-  __shared__ float gys[kTT][kP];
-  __shared__ float cs[kTT][kS];
-  const int k = blockIdx.x, bh = blockIdx.y;
-  const int b = bh / nh, h = bh - b * nh, g = h / hpg;
-  const int tok0 = k * T, valid = min(T, L - tok0);
-  const int tid = threadIdx.x;
-  if (!SSD_IN_BOUNDS(b < nb && k < nc, err, 200)) return;  // uniform over the CTA
-  float acc[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
-  const float *Gc = G + ((int64_t)bh * nc + k) * T;
-  const float Glast = Gc[valid - 1];
-  for (int t0 = 0; t0 < valid; t0 += kTT) {
-    __syncthreads();
-    for (int e = tid; e < kTT * kP; e += kThreads) {
-      const int tt = e / kP, p = e % kP, t = t0 + tt;
-      float w = 0.f;
-      if (t < valid) {
-        const int64_t tok = (int64_t)b * L + tok0 + t;
-        w = dt ? exp2f(Glast - Gc[t]) * dt[tok * nh + h] : exp2f(Gc[t]);
-        w *= v[(tok * nh + h) * kP + p];
-      }
-      gys[tt][p] = w;
-    }
-    for (int e = tid; e < kTT * kS; e += kThreads) {
-      const int tt = e / kS, s = e % kS, t = t0 + tt;
-      cs[tt][s] = t < valid ? m[(((int64_t)b * L + tok0 + t) * ng + g) * kS + s] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int tt = 0; tt < kTT; ++tt) {
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = tid + kThreads * i;
-        acc[i] = fmaf(gys[tt][e / kS], cs[tt][e % kS], acc[i]);
-      }
-    }
-  }
-  float *dst = out + ((int64_t)bh * nc + k) * kP * kS;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) dst[tid + kThreads * i] = acc[i];
-}
-
-// -------------------------------------------------------------- main kernel
+// ------------------------------------------------------------------ helpers
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool full) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
@@ -134,17 +77,109 @@ __device__ __forceinline__ void axpy4(float a, const float4 &v, float4 &acc) {
 __device__ __forceinline__ float comp(const float4 &v, int e) {
   return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
 }
-__device__ __forceinline__ void add_comp(float4 &v, int e, float a) {
-  if (e == 0) v.x += a;
-  else if (e == 1) v.y += a;
-  else if (e == 2) v.z += a;
-  else v.w += a;
-}
 __device__ __forceinline__ float sum8(float v) {  // over the 8 lanes of a token group
   v += __shfl_xor_sync(0xffffffffu, v, 1);
   v += __shfl_xor_sync(0xffffffffu, v, 2);
   return v + __shfl_xor_sync(0xffffffffu, v, 4);
 }
+
+// ---------------------------------------------------------------- jump terms
+
+// out[b, h, k][p][s] = sum_{t in chunk k} w_t v_t[p] m_t[s], v per head
+// ([b, L, nh, P]) and m per group ([b, L, ng, S]): the adjoint's jump terms
+// (v = gy, m = C, w_t = exp2(G_t); dt null) or the forward's (v = x, m = B,
+// w_t = exp2(G_last - G_t) dt_t).  One CTA per (chunk, batch * head), 256
+// threads as a 16 x 16 grid, thread (py, sx) owning rows p = 4 py .. +3 and
+// the float4 columns s = 4 sx + 64 q of the [P][S] output; 32-token tiles of
+// v and m double-buffered through cp.async.  Shared memory (float4 units):
+// v tiles [2][32][P/4], m tiles [2][32][S/4], then the chunk's w (256).
+template <int kS>
+struct JumpSmem {
+  static constexpr int P4 = kP / 4, S4 = kS / 4, V = 0, M = 2 * kTT * P4, end4 = M + 2 * kTT * S4;
+  static constexpr size_t bytes = 16 * (size_t)end4 + 256 * sizeof(float);
+};
+
+template <int kS>
+__global__ void __launch_bounds__(kThreads)
+bwd_jump_kernel(const float *__restrict__ v, const float *__restrict__ m,
+                const float *__restrict__ dt, const float *__restrict__ G,
+                float *__restrict__ out, int *err, int L, int nh, int hpg, int T, int nc,
+                int nb) {
+  using SM = JumpSmem<kS>;
+  constexpr int QS = kS / 64, P4 = SM::P4, S4 = SM::S4;
+  extern __shared__ float4 smj[];
+  float4 *vs = smj + SM::V, *ms = smj + SM::M;
+  float *ws = reinterpret_cast<float *>(smj + SM::end4);
+  const int ng = nh / hpg;
+  const int k = blockIdx.x, bh = blockIdx.y;
+  const int b = bh / nh, h = bh - b * nh, g = h / hpg;
+  const int tok0 = k * T, valid = min(T, L - tok0);
+  const int tid = threadIdx.x, py = tid >> 4, sx = tid & 15;
+  if (!SSD_IN_BOUNDS(b < nb && k < nc, err, 200)) return;  // uniform over the CTA
+  const int64_t rowh0 = ((int64_t)b * L + tok0) * nh + h, rowg0 = ((int64_t)b * L + tok0) * ng + g;
+  const float *Gc = G + ((int64_t)bh * nc + k) * T;
+  const float Glast = Gc[valid - 1];
+  for (int i = tid; i < T; i += kThreads) {
+    float w = 0.f;
+    if (i < valid) w = dt ? exp2f(Glast - Gc[i]) * dt[rowh0 + (int64_t)i * nh] : exp2f(Gc[i]);
+    ws[i] = w;
+  }
+  // stage the 32 tokens from t0 (zeros past the sequence) into buffer buf
+  auto stage = [&](int buf, int t0) {
+    for (int e = tid; e < kTT * (P4 + S4); e += kThreads) {
+      if (e < kTT * P4) {
+        const int r = e / P4, c = e - r * P4, tok = t0 + r;
+        const bool ok = tok < valid;
+        cp_async16(vs + (buf * kTT + r) * P4 + c,
+                   v + (rowh0 + (int64_t)(ok ? tok : 0) * nh) * kP + 4 * c, ok);
+      } else {
+        const int e2 = e - kTT * P4, r = e2 / S4, c = e2 - r * S4, tok = t0 + r;
+        const bool ok = tok < valid;
+        cp_async16(ms + (buf * kTT + r) * S4 + c,
+                   m + (rowg0 + (int64_t)(ok ? tok : 0) * ng) * kS + 4 * c, ok);
+      }
+    }
+  };
+  float4 acc[4][QS];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int q = 0; q < QS; ++q) acc[a][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int ntile = (valid + kTT - 1) / kTT;
+  stage(0, 0);
+  cp_async_commit();
+  for (int u = 0; u < ntile; ++u) {
+    const int cur = u & 1;
+    if (u + 1 < ntile) stage(cur ^ 1, (u + 1) * kTT);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    const float4 *vb = vs + cur * kTT * P4 + py, *mb = ms + cur * kTT * S4 + sx;
+#pragma unroll 4
+    for (int j = 0; j < kTT; ++j) {
+      const float w = ws[u * kTT + j];
+      const float4 vq = vb[j * P4];
+      float4 mq[QS];
+#pragma unroll
+      for (int q = 0; q < QS; ++q) mq[q] = mb[j * S4 + 16 * q];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const float wv = w * comp(vq, a);
+#pragma unroll
+        for (int q = 0; q < QS; ++q) axpy4(wv, mq[q], acc[a][q]);
+      }
+    }
+    __syncthreads();  // buffer cur is refilled at the next iteration but one
+  }
+  float *dst = out + ((int64_t)bh * nc + k) * kP * kS;
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int q = 0; q < QS; ++q)
+      *reinterpret_cast<float4 *>(dst + (4 * py + a) * kS + 4 * sx + 64 * q) = acc[a][q];
+}
+
+// -------------------------------------------------------------- main kernel
 
 // Shared-memory plan of bwd_main_kernel (float4 units): two column tiles
 // U1 [NT][S/4] and U2 [NT][P/4] (double-buffered), the row tile's own rows
@@ -233,43 +268,64 @@ __device__ __forceinline__ void main_pass(
     cp_async_wait<1>();
     __syncthreads();
     const float4 *u1p = U1 + cur * NT * S4 + l8, *u2p = U2 + cur * NT * P4 + l8;
+    // token block r (tokens 32 r .. 32 r + 31 of the row tile) meets this
+    // column tile at all unless it lies wholly on the masked side of the
+    // diagonal; the loop body is compiled once per set of active blocks
+    // (a condition uniform over the CTA, so the shuffles stay warp-wide)
+    auto tile = [&](auto mask_c) {
+      constexpr int kMask = decltype(mask_c)::value;
 #pragma unroll 2
-    for (int j = 0; j < NT; ++j) {
-      const int s = u * NT + j;
-      float4 cS[QS], cP[QP];
+      for (int j = 0; j < NT; ++j) {
+        const int s = u * NT + j;
+        float4 cS[QS], cP[QP];
 #pragma unroll
-      for (int i = 0; i < QS; ++i) cS[i] = u1p[j * S4 + 8 * i];
+        for (int i = 0; i < QS; ++i) cS[i] = u1p[j * S4 + 8 * i];
 #pragma unroll
-      for (int i = 0; i < QP; ++i) cP[i] = u2p[j * P4 + 8 * i];
-      float d1[kTok], d2[kTok];
+        for (int i = 0; i < QP; ++i) cP[i] = u2p[j * P4 + 8 * i];
+        float d1[kTok], d2[kTok];
 #pragma unroll
-      for (int r = 0; r < kTok; ++r) {
-        float a = 0.f, c = 0.f;
+        for (int r = 0; r < kTok; ++r) {
+          d1[r] = d2[r] = 0.f;
+          if (!((kMask >> r) & 1)) continue;
+          float a = 0.f, c = 0.f;
 #pragma unroll
-        for (int i = 0; i < QS; ++i) a = dot4(rS[r][i], cS[i], a);
+          for (int i = 0; i < QS; ++i) a = dot4(rS[r][i], cS[i], a);
 #pragma unroll
-        for (int i = 0; i < QP; ++i) c = dot4(rP[r][i], cP[i], c);
-        d1[r] = sum8(a);
-        d2[r] = sum8(c);
-      }
-      const float Gc = Gs[s], dc = ds[s];
-#pragma unroll
-      for (int r = 0; r < kTok; ++r) {
-        float w = 0.f;
-        if (kUpper) {
-          if (s >= t[r] && s < valid && live[r]) w = exp2f(Gc - Gt[r]);
-        } else {
-          if (s <= t[r] && live[r]) w = exp2f(Gt[r] - Gc) * dc;  // dt = 0 past the sequence
+          for (int i = 0; i < QP; ++i) c = dot4(rP[r][i], cP[i], c);
+          d1[r] = sum8(a);
+          d2[r] = sum8(c);
         }
-        // upper: dx += dt_t w (B_t . C_s) gy_s, q += w (x_t . gy_s) C_s;
-        // lower: ysm += w (C_t . B_j) x_j,      dC += w (gy_t . x_j) B_j
-        const float aP = (kUpper ? dtt[r] : 1.f) * w * d1[r], aS = w * d2[r];
+        const float Gc = Gs[s], dc = ds[s];
 #pragma unroll
-        for (int i = 0; i < QP; ++i) axpy4(aP, cP[i], accP[r][i]);
+        for (int r = 0; r < kTok; ++r) {
+          if (!((kMask >> r) & 1)) continue;
+          float w = 0.f;
+          if (kUpper) {
+            if (s >= t[r] && s < valid && live[r]) w = exp2f(Gc - Gt[r]);
+          } else {
+            if (s <= t[r] && live[r]) w = exp2f(Gt[r] - Gc) * dc;  // dt = 0 past the sequence
+          }
+          // upper: dx += dt_t w (B_t . C_s) gy_s, q += w (x_t . gy_s) C_s;
+          // lower: ysm += w (C_t . B_j) x_j,      dC += w (gy_t . x_j) B_j
+          const float aP = (kUpper ? dtt[r] : 1.f) * w * d1[r], aS = w * d2[r];
 #pragma unroll
-        for (int i = 0; i < QS; ++i) axpy4(aS, cS[i], accS[r][i]);
+          for (int i = 0; i < QP; ++i) axpy4(aP, cP[i], accP[r][i]);
+#pragma unroll
+          for (int i = 0; i < QS; ++i) axpy4(aS, cS[i], accS[r][i]);
+        }
       }
-    }
+    };
+    int mask = 0;
+#pragma unroll
+    for (int r = 0; r < kTok; ++r)
+      if (kUpper ? u * NT + NT > tau * RT + kTT * r : u * NT < tau * RT + kTT * r + kTT)
+        mask |= 1 << r;
+    if (kTok == 1 || mask == 3)
+      tile(std::integral_constant<int, 3>{});
+    else if (mask == 1)
+      tile(std::integral_constant<int, 1>{});
+    else
+      tile(std::integral_constant<int, 2>{});
     __syncthreads();  // tile u's buffer is refilled two iterations on
   }
   cp_async_wait<0>();
@@ -295,15 +351,27 @@ __device__ __forceinline__ void main_pass(
   for (int c4 = 0; c4 < S4; ++c4) {
     float4 o[kTok];
 #pragma unroll
-    for (int r = 0; r < kTok; ++r) o[r] = O1[(kTT * r + grp) * S4 + c4];
+    for (int r = 0; r < kTok; ++r) {
+      o[r] = O1[(kTT * r + grp) * S4 + c4];
+      o[r].x *= fP[r];
+      o[r].y *= fP[r];
+      o[r].z *= fP[r];
+      o[r].w *= fP[r];
+    }
 #pragma unroll
-    for (int i = 0; i < QP; ++i)
+    for (int i = 0; i < QP; ++i) {
+      const float4 m0 = Ms[(32 * i + 4 * l8) * S4 + (c4 ^ l8)];
+      const float4 m1 = Ms[(32 * i + 4 * l8 + 1) * S4 + (c4 ^ l8)];
+      const float4 m2 = Ms[(32 * i + 4 * l8 + 2) * S4 + (c4 ^ l8)];
+      const float4 m3 = Ms[(32 * i + 4 * l8 + 3) * S4 + (c4 ^ l8)];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float4 m = Ms[(32 * i + 4 * l8 + e) * S4 + (c4 ^ l8)];
-#pragma unroll
-        for (int r = 0; r < kTok; ++r) add_comp(accP[r][i], e, fP[r] * dot4(m, o[r], 0.f));
+      for (int r = 0; r < kTok; ++r) {
+        accP[r][i].x = dot4(m0, o[r], accP[r][i].x);
+        accP[r][i].y = dot4(m1, o[r], accP[r][i].y);
+        accP[r][i].z = dot4(m2, o[r], accP[r][i].z);
+        accP[r][i].w = dot4(m3, o[r], accP[r][i].w);
       }
+    }
   }
   // accS[s] += fS sum_p M[p][s] O2_t[p] over this lane's columns (slot 8 i + l8)
   for (int p4 = 0; p4 < P4; ++p4) {
@@ -549,17 +617,28 @@ bool bwd_supported(const Dims &d) {
   return d.P == kP && (d.S == 64 || d.S == 128 || d.S == 256) && d.T % kTT == 0 && d.T <= 256;
 }
 
+namespace {
+template <int kS>
+cudaError_t launch_jump(const Dims &d, const float *v, const float *m, const float *dt,
+                        const float *G, float *out, int *err, cudaStream_t st) {
+  const size_t smem = JumpSmem<kS>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(bwd_jump_kernel<kS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)d.nc, (unsigned)(d.b * d.nh));
+  bwd_jump_kernel<kS><<<grid, kThreads, smem, st>>>(v, m, dt, G, out, err, (int)d.L, (int)d.nh,
+                                                    (int)d.hpg, (int)d.T, (int)d.nc, (int)d.b);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_bwd_jump(const Dims &d, const float *v, const float *m, const float *dt,
                             const float *G, float *out, int *err, cudaStream_t st) {
-  dim3 grid((unsigned)d.nc, (unsigned)(d.b * d.nh));
-  const int L = (int)d.L, nh = (int)d.nh, hpg = (int)d.hpg, T = (int)d.T, nc = (int)d.nc,
-            nb = (int)d.b;
   switch (d.S) {
-    case 64: bwd_jump_kernel<64><<<grid, kThreads, 0, st>>>(v, m, dt, G, out, err, L, nh, hpg, T, nc, nb); break;
-    case 128: bwd_jump_kernel<128><<<grid, kThreads, 0, st>>>(v, m, dt, G, out, err, L, nh, hpg, T, nc, nb); break;
-    default: bwd_jump_kernel<256><<<grid, kThreads, 0, st>>>(v, m, dt, G, out, err, L, nh, hpg, T, nc, nb); break;
+    case 64: return launch_jump<64>(d, v, m, dt, G, out, err, st);
+    case 128: return launch_jump<128>(d, v, m, dt, G, out, err, st);
+    default: return launch_jump<256>(d, v, m, dt, G, out, err, st);
   }
-  return cudaGetLastError();
 }
 
 namespace {
