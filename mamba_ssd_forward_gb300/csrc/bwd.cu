@@ -77,11 +77,6 @@ __device__ __forceinline__ void axpy4(float a, const float4 &v, float4 &acc) {
 __device__ __forceinline__ float comp(const float4 &v, int e) {
   return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
 }
-__device__ __forceinline__ float sum8(float v) {  // over the 8 lanes of a token group
-  v += __shfl_xor_sync(0xffffffffu, v, 1);
-  v += __shfl_xor_sync(0xffffffffu, v, 2);
-  return v + __shfl_xor_sync(0xffffffffu, v, 4);
-}
 
 // ---------------------------------------------------------------- jump terms
 
@@ -115,13 +110,21 @@ bwd_jump_kernel(const float *__restrict__ v, const float *__restrict__ m,
   const int b = bh / nh, h = bh - b * nh, g = h / hpg;
   const int tok0 = k * T, valid = min(T, L - tok0);
   const int tid = threadIdx.x, py = tid >> 4, sx = tid & 15;
-  if (!SSD_IN_BOUNDS(b < nb && k < nc, err, 200)) return;  // uniform over the CTA
+  // extents (elements) of the buffers read and written, for the debug-bounds checks
+  const int64_t ext_h = (int64_t)nb * L * nh, ext_g = (int64_t)nb * L * ng,
+                ext_chunk = (int64_t)nb * nh * nc;
+  // G and out of this (chunk, head): checked once, uniform over the CTA
+  if (!SSD_IN_BOUNDS(b < nb && k < nc && (int64_t)bh * nc + k < ext_chunk, err, 200)) return;
   const int64_t rowh0 = ((int64_t)b * L + tok0) * nh + h, rowg0 = ((int64_t)b * L + tok0) * ng + g;
   const float *Gc = G + ((int64_t)bh * nc + k) * T;
   const float Glast = Gc[valid - 1];
   for (int i = tid; i < T; i += kThreads) {
     float w = 0.f;
-    if (i < valid) w = dt ? exp2f(Glast - Gc[i]) * dt[rowh0 + (int64_t)i * nh] : exp2f(Gc[i]);
+    if (i < valid) {
+      const int64_t di = rowh0 + (int64_t)i * nh;
+      w = !dt ? exp2f(Gc[i])
+              : SSD_IN_BOUNDS(di < ext_h, err, 203) ? exp2f(Glast - Gc[i]) * dt[di] : 0.f;
+    }
     ws[i] = w;
   }
   // stage the 32 tokens from t0 (zeros past the sequence) into buffer buf
@@ -129,14 +132,14 @@ bwd_jump_kernel(const float *__restrict__ v, const float *__restrict__ m,
     for (int e = tid; e < kTT * (P4 + S4); e += kThreads) {
       if (e < kTT * P4) {
         const int r = e / P4, c = e - r * P4, tok = t0 + r;
-        const bool ok = tok < valid;
-        cp_async16(vs + (buf * kTT + r) * P4 + c,
-                   v + (rowh0 + (int64_t)(ok ? tok : 0) * nh) * kP + 4 * c, ok);
+        const int64_t si = (rowh0 + (int64_t)(tok < valid ? tok : 0) * nh) * kP + 4 * c;
+        const bool ok = tok < valid && SSD_IN_BOUNDS(si + 4 <= ext_h * kP, err, 204);
+        cp_async16(vs + (buf * kTT + r) * P4 + c, ok ? v + si : v, ok);
       } else {
         const int e2 = e - kTT * P4, r = e2 / S4, c = e2 - r * S4, tok = t0 + r;
-        const bool ok = tok < valid;
-        cp_async16(ms + (buf * kTT + r) * S4 + c,
-                   m + (rowg0 + (int64_t)(ok ? tok : 0) * ng) * kS + 4 * c, ok);
+        const int64_t si = (rowg0 + (int64_t)(tok < valid ? tok : 0) * ng) * kS + 4 * c;
+        const bool ok = tok < valid && SSD_IN_BOUNDS(si + 4 <= ext_g * kS, err, 205);
+        cp_async16(ms + (buf * kTT + r) * S4 + c, ok ? m + si : m, ok);
       }
     }
   };
@@ -185,39 +188,78 @@ bwd_jump_kernel(const float *__restrict__ v, const float *__restrict__ m,
 // U1 [NT][S/4] and U2 [NT][P/4] (double-buffered), the row tile's own rows
 // O1 [RT][S/4] and O2 [RT][P/4], the state Ms [P][S/4] (float4 slots XOR-
 // swizzled by bits 2..4 of the row), then G and dt of the chunk (256 each).
-template <int kS, int kTok>
+// kG lanes share a token group, which owns kTok tokens: RT = (256 / kG) kTok.
+template <int kS, int kG, int kTok>
 struct MainSmem {
-  static constexpr int RT = kTT * kTok, NT = kTT, S4 = kS / 4, P4 = kP / 4;
+  static constexpr int NG = kThreads / kG, RT = NG * kTok, NT = kTT, S4 = kS / 4, P4 = kP / 4;
   static constexpr int U1 = 0, U2 = U1 + 2 * NT * S4, O1 = U2 + 2 * NT * P4, O2 = O1 + RT * S4,
                        Ms = O2 + RT * P4, end4 = Ms + kP * S4;
   static constexpr size_t bytes = 16 * (size_t)end4 + 2 * 256 * sizeof(float);
+  static_assert(RT % kTT == 0 && RT <= 2 * kTT, "row tiles of 32 or 64 tokens");
+  static_assert(S4 % kG == 0 && P4 % kG == 0, "whole float4 slots per lane");
 };
 
-// One CTA per (row tile of RT = 32 kTok tokens of a chunk, chunk, batch *
-// head), 256 threads: thread = (token group grp = tid / 8, lane l8 = tid % 8),
-// the group owning tokens grp + 32 r (r < kTok) of the tile and lane l8 the
-// feature columns 32 i + 4 l8 .. +3 of every row (float4 slot 8 i + l8).
-// Each lane keeps its slice of its tokens' own rows in registers; the 8
-// lanes of a group split every dot product and sum it with three shuffles.
-// Two passes over the chunk's 32-token column tiles, each tile double-
-// buffered through cp.async:
+// Sums each of the V values v[] over the kG lanes of a token group (the
+// lanes that differ in their low log2(kG) bits; `lane` is the lane of the
+// warp, kG divides 32) and leaves every total in every lane: a reduce-scatter (at the step with lane bit o a lane keeps one
+// half of its values, adds the partner's copy of that half, and passes on
+// the other half), the remaining steps on the single value left, and a
+// gather of the V totals from the lanes holding them.  2V - 1 + log2(kG / V)
+// shuffles instead of V log2(kG).
+template <int V, int kG>
+__device__ __forceinline__ void group_sums(float (&v)[V], int lane) {
+  static_assert(V >= 1 && V <= kG && (V & (V - 1)) == 0, "V: a power of two up to kG");
+  int idx = 0;  // index (into v) of the total this lane ends up holding
+#pragma unroll
+  for (int n = V, o = 1; n > 1; n >>= 1, o <<= 1) {
+    const bool up = lane & o;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float keep = up ? v[i + n / 2] : v[i], send = up ? v[i] : v[i + n / 2];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+    if (up) idx += n / 2;
+  }
+#pragma unroll
+  for (int o = V; o < kG; o <<= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+  // lane (lane & ~(V - 1)) | m holds total idx(m): bit o of m (o = 1, 2, ..)
+  // adds V / 2o; gather every total from one such lane of this group
+  const float mine = v[0];
+  (void)idx;
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    int m = 0;
+#pragma unroll
+    for (int n = V, o = 1; n > 1; n >>= 1, o <<= 1)
+      if (k & (n / 2)) m |= o;
+    v[k] = __shfl_sync(0xffffffffu, mine, (lane & ~(V - 1)) | m);
+  }
+}
+
+// One CTA per (row tile of RT tokens of a chunk, chunk, batch * head), 256
+// threads: thread = (token group grp = tid / kG, lane lg = tid % kG), the
+// group owning tokens grp + NG r (r < kTok) of the tile and lane lg the
+// float4 slots kG i + lg of every feature row.  Each lane keeps its slice of
+// its tokens' own rows in registers; the kG lanes of a group split every
+// dot product.  Two passes over the chunk's 32-token column tiles, each tile
+// double-buffered through cp.async:
 //   upper (columns s >= t): dx_t += dt_t w (B_t . C_s) gy_s,
 //                           q_t  += w (x_t . gy_s) C_s,  w = exp2(G_s - G_t);
 //   lower (columns j <= t): ysm_t += w (C_t . B_j) x_j,
 //                           dC_t  += w (gy_t . x_j) B_j,  w = exp2(G_t - G_j) dt_j;
 // each followed by its state terms (R_k after the upper pass, h_k after the
 // lower one) from the state staged in shared memory.
-template <int kS, int kTok, bool kUpper>
+template <int kS, int kG, int kTok, bool kUpper>
 __device__ __forceinline__ void main_pass(
     float4 *sm4, float *Gs, float *ds, const float *own_g, const float *own_h,
     const float *col_g, const float *col_h, const float *state, int64_t st_row,
-    float4 (&accP)[kTok][kP / 32], float4 (&accS)[kTok][kS / 32],
-    float4 (&rS)[kTok][kS / 32], float4 (&rP)[kTok][kP / 32], const int (&t)[kTok],
+    float4 (&accP)[kTok][kP / 4 / kG], float4 (&accS)[kTok][kS / 4 / kG],
+    float4 (&rS)[kTok][kS / 4 / kG], float4 (&rP)[kTok][kP / 4 / kG], const int (&t)[kTok],
     const bool (&live)[kTok], int tau, int valid, int64_t rowh0, int64_t rowg0, int nh, int ng,
-    int tid, int l8, int grp) {
-  using SM = MainSmem<kS, kTok>;
-  constexpr int RT = SM::RT, NT = SM::NT, S4 = SM::S4, P4 = SM::P4;
-  constexpr int QS = kS / 32, QP = kP / 32;
+    int tid, int lg, int grp, int64_t ext_h, int64_t ext_g, int *err) {
+  using SM = MainSmem<kS, kG, kTok>;
+  constexpr int NG = SM::NG, RT = SM::RT, NT = SM::NT, S4 = SM::S4, P4 = SM::P4;
+  constexpr int QS = S4 / kG, QP = P4 / kG;
   float4 *U1 = sm4 + SM::U1, *U2 = sm4 + SM::U2, *O1 = sm4 + SM::O1, *O2 = sm4 + SM::O2,
          *Ms = sm4 + SM::Ms;
   // stage `rows` tokens from chunk-relative token t0 of a per-group (width
@@ -226,10 +268,12 @@ __device__ __forceinline__ void main_pass(
     const int W4 = per_head ? P4 : S4;
     for (int e = tid; e < rows * W4; e += kThreads) {
       const int r = e / W4, c = e - r * W4, tok = t0 + r;
-      const bool ok = tok < valid;
-      const int64_t row = per_head ? rowh0 + (int64_t)(ok ? tok : 0) * nh
-                                   : rowg0 + (int64_t)(ok ? tok : 0) * ng;
-      cp_async16(dst + e, src + row * (W4 * 4) + c * 4, ok);
+      const int64_t row = per_head ? rowh0 + (int64_t)(tok < valid ? tok : 0) * nh
+                                   : rowg0 + (int64_t)(tok < valid ? tok : 0) * ng;
+      const int64_t si = row * (W4 * 4) + c * 4;
+      const bool ok =
+          tok < valid && SSD_IN_BOUNDS(si + 4 <= (per_head ? ext_h * kP : ext_g * kS), err, 206);
+      cp_async16(dst + e, ok ? src + si : src, ok);
     }
   };
   float Gt[kTok], dtt[kTok];
@@ -239,19 +283,23 @@ __device__ __forceinline__ void main_pass(
     dtt[r] = ds[t[r]];
     // this token's own rows: B_t, x_t (upper) or C_t, gy_t (lower)
 #pragma unroll
-    for (int i = 0; i < QS; ++i)
-      rS[r][i] = live[r] ? *reinterpret_cast<const float4 *>(
-                               own_g + (rowg0 + (int64_t)t[r] * ng) * kS + 32 * i + 4 * l8)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < QS; ++i) {
+      const int64_t gi = (rowg0 + (int64_t)t[r] * ng) * kS + 4 * (kG * i + lg);
+      rS[r][i] = live[r] && SSD_IN_BOUNDS(gi + 4 <= ext_g * kS, err, 207)
+                     ? *reinterpret_cast<const float4 *>(own_g + gi)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
-    for (int i = 0; i < QP; ++i)
-      rP[r][i] = live[r] ? *reinterpret_cast<const float4 *>(
-                               own_h + (rowh0 + (int64_t)t[r] * nh) * kP + 32 * i + 4 * l8)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < QP; ++i) {
+      const int64_t hi = (rowh0 + (int64_t)t[r] * nh) * kP + 4 * (kG * i + lg);
+      rP[r][i] = live[r] && SSD_IN_BOUNDS(hi + 4 <= ext_h * kP, err, 208)
+                     ? *reinterpret_cast<const float4 *>(own_h + hi)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   const int ucount = (valid + NT - 1) / NT;
-  const int u0 = kUpper ? tau * kTok : 0;
-  const int u1 = kUpper ? ucount : min(ucount, tau * kTok + kTok);
+  const int u0 = kUpper ? tau * RT / NT : 0;
+  const int u1 = kUpper ? ucount : min(ucount, (tau + 1) * RT / NT);
   __syncthreads();  // the buffers of the previous pass are free
   stage(O1, own_g, false, tau * RT, RT);
   stage(O2, own_h, true, tau * RT, RT);
@@ -267,38 +315,40 @@ __device__ __forceinline__ void main_pass(
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();
-    const float4 *u1p = U1 + cur * NT * S4 + l8, *u2p = U2 + cur * NT * P4 + l8;
-    // token block r (tokens 32 r .. 32 r + 31 of the row tile) meets this
-    // column tile at all unless it lies wholly on the masked side of the
-    // diagonal; the loop body is compiled once per set of active blocks
-    // (a condition uniform over the CTA, so the shuffles stay warp-wide)
+    const float4 *u1p = U1 + cur * NT * S4 + lg, *u2p = U2 + cur * NT * P4 + lg;
+    // token r meets this column tile at all unless its 32-token block lies
+    // wholly on the masked side of the diagonal; the loop body is compiled
+    // once per set of active blocks (a condition uniform over the CTA, so
+    // the shuffles stay warp-wide); inactive tokens skip their arithmetic
     auto tile = [&](auto mask_c) {
       constexpr int kMask = decltype(mask_c)::value;
+      auto on = [](int r) { return ((kMask >> ((r * NG) / kTT)) & 1) != 0; };
 #pragma unroll 2
       for (int j = 0; j < NT; ++j) {
         const int s = u * NT + j;
         float4 cS[QS], cP[QP];
 #pragma unroll
-        for (int i = 0; i < QS; ++i) cS[i] = u1p[j * S4 + 8 * i];
+        for (int i = 0; i < QS; ++i) cS[i] = u1p[j * S4 + kG * i];
 #pragma unroll
-        for (int i = 0; i < QP; ++i) cP[i] = u2p[j * P4 + 8 * i];
-        float d1[kTok], d2[kTok];
+        for (int i = 0; i < QP; ++i) cP[i] = u2p[j * P4 + kG * i];
+        float d[2 * kTok];  // B_t . C_s and x_t . gy_s (upper) per token
 #pragma unroll
         for (int r = 0; r < kTok; ++r) {
-          d1[r] = d2[r] = 0.f;
-          if (!((kMask >> r) & 1)) continue;
           float a = 0.f, c = 0.f;
+          if (on(r)) {
 #pragma unroll
-          for (int i = 0; i < QS; ++i) a = dot4(rS[r][i], cS[i], a);
+            for (int i = 0; i < QS; ++i) a = dot4(rS[r][i], cS[i], a);
 #pragma unroll
-          for (int i = 0; i < QP; ++i) c = dot4(rP[r][i], cP[i], c);
-          d1[r] = sum8(a);
-          d2[r] = sum8(c);
+            for (int i = 0; i < QP; ++i) c = dot4(rP[r][i], cP[i], c);
+          }
+          d[2 * r] = a;
+          d[2 * r + 1] = c;
         }
+        group_sums<2 * kTok, kG>(d, tid & 31);
         const float Gc = Gs[s], dc = ds[s];
 #pragma unroll
         for (int r = 0; r < kTok; ++r) {
-          if (!((kMask >> r) & 1)) continue;
+          if (!on(r)) continue;
           float w = 0.f;
           if (kUpper) {
             if (s >= t[r] && s < valid && live[r]) w = exp2f(Gc - Gt[r]);
@@ -307,7 +357,7 @@ __device__ __forceinline__ void main_pass(
           }
           // upper: dx += dt_t w (B_t . C_s) gy_s, q += w (x_t . gy_s) C_s;
           // lower: ysm += w (C_t . B_j) x_j,      dC += w (gy_t . x_j) B_j
-          const float aP = (kUpper ? dtt[r] : 1.f) * w * d1[r], aS = w * d2[r];
+          const float aP = (kUpper ? dtt[r] : 1.f) * w * d[2 * r], aS = w * d[2 * r + 1];
 #pragma unroll
           for (int i = 0; i < QP; ++i) axpy4(aP, cP[i], accP[r][i]);
 #pragma unroll
@@ -315,12 +365,13 @@ __device__ __forceinline__ void main_pass(
         }
       }
     };
+    // active 32-token blocks of the row tile (RT is 32 or 64 tokens)
     int mask = 0;
 #pragma unroll
-    for (int r = 0; r < kTok; ++r)
-      if (kUpper ? u * NT + NT > tau * RT + kTT * r : u * NT < tau * RT + kTT * r + kTT)
-        mask |= 1 << r;
-    if (kTok == 1 || mask == 3)
+    for (int rb = 0; rb < RT / kTT; ++rb)
+      if (kUpper ? u * NT + NT > tau * RT + kTT * rb : u * NT < tau * RT + kTT * rb + kTT)
+        mask |= 1 << rb;
+    if (RT == kTT || mask == 3)
       tile(std::integral_constant<int, 3>{});
     else if (mask == 1)
       tile(std::integral_constant<int, 1>{});
@@ -347,12 +398,12 @@ __device__ __forceinline__ void main_pass(
     fS[r] = f;
     fP[r] = kUpper ? dtt[r] * f : f;
   }
-  // accP[p] += fP sum_s M[p][s] O1_t[s] over this lane's rows p = 32 i + 4 l8 + e
+  // accP[p] += fP sum_s M[p][s] O1_t[s] over this lane's rows p = 4 (kG i + lg) + e
   for (int c4 = 0; c4 < S4; ++c4) {
     float4 o[kTok];
 #pragma unroll
     for (int r = 0; r < kTok; ++r) {
-      o[r] = O1[(kTT * r + grp) * S4 + c4];
+      o[r] = O1[(NG * r + grp) * S4 + c4];
       o[r].x *= fP[r];
       o[r].y *= fP[r];
       o[r].z *= fP[r];
@@ -360,10 +411,9 @@ __device__ __forceinline__ void main_pass(
     }
 #pragma unroll
     for (int i = 0; i < QP; ++i) {
-      const float4 m0 = Ms[(32 * i + 4 * l8) * S4 + (c4 ^ l8)];
-      const float4 m1 = Ms[(32 * i + 4 * l8 + 1) * S4 + (c4 ^ l8)];
-      const float4 m2 = Ms[(32 * i + 4 * l8 + 2) * S4 + (c4 ^ l8)];
-      const float4 m3 = Ms[(32 * i + 4 * l8 + 3) * S4 + (c4 ^ l8)];
+      const int p0 = 4 * (kG * i + lg), sw = c4 ^ ((kG * i + lg) & 7);
+      const float4 m0 = Ms[p0 * S4 + sw], m1 = Ms[(p0 + 1) * S4 + sw],
+                   m2 = Ms[(p0 + 2) * S4 + sw], m3 = Ms[(p0 + 3) * S4 + sw];
 #pragma unroll
       for (int r = 0; r < kTok; ++r) {
         accP[r][i].x = dot4(m0, o[r], accP[r][i].x);
@@ -373,17 +423,17 @@ __device__ __forceinline__ void main_pass(
       }
     }
   }
-  // accS[s] += fS sum_p M[p][s] O2_t[p] over this lane's columns (slot 8 i + l8)
+  // accS[s] += fS sum_p M[p][s] O2_t[p] over this lane's columns (slot kG i + lg)
   for (int p4 = 0; p4 < P4; ++p4) {
     float4 o[kTok];
 #pragma unroll
-    for (int r = 0; r < kTok; ++r) o[r] = O2[(kTT * r + grp) * P4 + p4];
+    for (int r = 0; r < kTok; ++r) o[r] = O2[(NG * r + grp) * P4 + p4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int p = 4 * p4 + e;
 #pragma unroll
       for (int i = 0; i < QS; ++i) {
-        const float4 m = Ms[p * S4 + ((8 * i + l8) ^ (p4 & 7))];
+        const float4 m = Ms[p * S4 + ((kG * i + lg) ^ (p4 & 7))];
 #pragma unroll
         for (int r = 0; r < kTok; ++r) axpy4(fS[r] * comp(o[r], e), m, accS[r][i]);
       }
@@ -391,7 +441,7 @@ __device__ __forceinline__ void main_pass(
   }
 }
 
-template <int kS, int kTok>
+template <int kS, int kG, int kTok>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
                 const float *__restrict__ Bm, const float *__restrict__ Cm,
@@ -401,8 +451,8 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
                 float *__restrict__ dBh, float *__restrict__ dCh, float *__restrict__ qB,
                 float *__restrict__ dG, float *__restrict__ gyx, int *err, int L, int nh,
                 int hpg, int T, int nc, int nb) {
-  using SM = MainSmem<kS, kTok>;
-  constexpr int RT = SM::RT, QS = kS / 32, QP = kP / 32;
+  using SM = MainSmem<kS, kG, kTok>;
+  constexpr int NG = SM::NG, RT = SM::RT, QS = kS / 4 / kG, QP = kP / 4 / kG;
   extern __shared__ float4 sm4[];
   float *Gs = reinterpret_cast<float *>(sm4 + SM::end4);
   float *ds = Gs + 256;
@@ -410,14 +460,19 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
   const int k = blockIdx.x / ntile, tau = blockIdx.x - k * ntile;
   const int bh = blockIdx.y, b = bh / nh, h = bh - b * nh, g = h / hpg, ng = nh / hpg;
   const int tok0 = k * T, valid = min(T, L - tok0);
-  const int tid = threadIdx.x, grp = tid >> 3, l8 = tid & 7;
-  if (!SSD_IN_BOUNDS(b < nb && k < nc, err, 201)) return;  // uniform over the CTA
-  if (tau * RT >= valid) return;                            // tile past the sequence
+  const int tid = threadIdx.x, grp = tid / kG, lg = tid % kG;
+  // extents (elements per row width) of the buffers, for the debug-bounds checks
+  const int64_t ext_h = (int64_t)nb * L * nh, ext_g = (int64_t)nb * L * ng,
+                ext_chunk = (int64_t)nb * nh * nc;
+  // G, qB, dG, gyx and the states of this (chunk, head): checked once,
+  // uniform over the CTA
+  if (!SSD_IN_BOUNDS(b < nb && k < nc && (int64_t)bh * nc + k < ext_chunk, err, 201)) return;
+  if (tau * RT >= valid) return;  // tile past the sequence
   int t[kTok];
   bool live[kTok];
 #pragma unroll
   for (int r = 0; r < kTok; ++r) {
-    t[r] = tau * RT + kTT * r + grp;
+    t[r] = tau * RT + NG * r + grp;
     live[r] = t[r] < valid;
   }
   // row indices (in rows of the width) of the chunk's token 0
@@ -425,7 +480,8 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
   const float *Gc = G + ((int64_t)bh * nc + k) * T;
   for (int i = tid; i < T; i += kThreads) {
     Gs[i] = Gc[i];
-    ds[i] = i < valid ? dt[rowh0 + (int64_t)i * nh] : 0.f;
+    const int64_t di = rowh0 + (int64_t)i * nh;
+    ds[i] = i < valid && SSD_IN_BOUNDS(di < ext_h, err, 209) ? dt[di] : 0.f;
   }
   __syncthreads();
   const int64_t st_row = ((int64_t)bh * nc + k) * kP * kS;
@@ -441,58 +497,66 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
   };
   // upper pass: dx and q (rS = B_t, rP = x_t)
   zero();
-  main_pass<kS, kTok, true>(sm4, Gs, ds, Bm, x, Cm, gy, R, st_row, aP, aS, rS, rP, t, live, tau,
-                            valid, rowh0, rowg0, nh, ng, tid, l8, grp);
+  main_pass<kS, kG, kTok, true>(sm4, Gs, ds, Bm, x, Cm, gy, R, st_row, aP, aS, rS, rP, t, live,
+                                tau, valid, rowh0, rowg0, nh, ng, tid, lg, grp, ext_h, ext_g,
+                                err);
   const float Dh = D ? D[h] : 0.f;
   float xdot[kTok], qb[kTok], gx[kTok];
 #pragma unroll
   for (int r = 0; r < kTok; ++r) {
-    float xd = 0.f, qv = 0.f, gv = 0.f;
+    float v3[4] = {0.f, 0.f, 0.f, 0.f};  // x . (dx - D gy), q . B, x . gy (and a spare)
     const int64_t rh = rowh0 + (int64_t)t[r] * nh;
 #pragma unroll
     for (int i = 0; i < QP; ++i) {
-      const float4 gq = live[r] ? *reinterpret_cast<const float4 *>(gy + rh * kP + 32 * i + 4 * l8)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-      xd = dot4(rP[r][i], aP[r][i], xd);  // x_t . (dx_t - D gy_t)
-      gv = dot4(rP[r][i], gq, gv);        // x_t . gy_t
-      if (live[r]) {
+      const int f = 4 * (kG * i + lg);
+      const bool ok = live[r] && SSD_IN_BOUNDS(rh * kP + f + 4 <= ext_h * kP, err, 210);
+      const float4 gq = ok ? *reinterpret_cast<const float4 *>(gy + rh * kP + f)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      v3[0] = dot4(rP[r][i], aP[r][i], v3[0]);
+      v3[2] = dot4(rP[r][i], gq, v3[2]);
+      if (ok) {
         float4 o = aP[r][i];
         axpy4(Dh, gq, o);
-        *reinterpret_cast<float4 *>(dx + rh * kP + 32 * i + 4 * l8) = o;
+        *reinterpret_cast<float4 *>(dx + rh * kP + f) = o;
       }
     }
 #pragma unroll
     for (int i = 0; i < QS; ++i) {
-      qv = dot4(aS[r][i], rS[r][i], qv);  // q_t . B_t
-      if (live[r]) {
+      const int f = 4 * (kG * i + lg);
+      v3[1] = dot4(aS[r][i], rS[r][i], v3[1]);
+      if (live[r] && SSD_IN_BOUNDS(rh * kS + f + 4 <= ext_h * kS, err, 211)) {
         const float4 a = aS[r][i];
-        *reinterpret_cast<float4 *>(dBh + rh * kS + 32 * i + 4 * l8) =
-            make_float4(ds[t[r]] * a.x, ds[t[r]] * a.y, ds[t[r]] * a.z, ds[t[r]] * a.w);
+        const float dtv = ds[t[r]];
+        *reinterpret_cast<float4 *>(dBh + rh * kS + f) =
+            make_float4(dtv * a.x, dtv * a.y, dtv * a.z, dtv * a.w);
       }
     }
-    xdot[r] = sum8(xd);
-    qb[r] = sum8(qv);
-    gx[r] = sum8(gv);
+    group_sums<4, kG>(v3, tid & 31);
+    xdot[r] = v3[0];
+    qb[r] = v3[1];
+    gx[r] = v3[2];
   }
   // lower pass: ysm and dC (rS = C_t, rP = gy_t)
   zero();
-  main_pass<kS, kTok, false>(sm4, Gs, ds, Cm, gy, Bm, x, states, st_row, aP, aS, rS, rP, t,
-                             live, tau, valid, rowh0, rowg0, nh, ng, tid, l8, grp);
+  main_pass<kS, kG, kTok, false>(sm4, Gs, ds, Cm, gy, Bm, x, states, st_row, aP, aS, rS, rP, t,
+                                 live, tau, valid, rowh0, rowg0, nh, ng, tid, lg, grp, ext_h,
+                                 ext_g, err);
 #pragma unroll
   for (int r = 0; r < kTok; ++r) {
-    float gd = 0.f;
+    float gd[1] = {0.f};
 #pragma unroll
-    for (int i = 0; i < QP; ++i) gd = dot4(rP[r][i], aP[r][i], gd);  // gy_t . ysm_t
-    gd = sum8(gd);
+    for (int i = 0; i < QP; ++i) gd[0] = dot4(rP[r][i], aP[r][i], gd[0]);  // gy_t . ysm_t
+    group_sums<1, kG>(gd, tid & 31);
     if (!live[r]) continue;
     const int64_t rh = rowh0 + (int64_t)t[r] * nh;
 #pragma unroll
     for (int i = 0; i < QS; ++i)
-      *reinterpret_cast<float4 *>(dCh + rh * kS + 32 * i + 4 * l8) = aS[r][i];
-    if (l8 == 0) {
+      if (SSD_IN_BOUNDS(rh * kS + 4 * (kG * i + lg) + 4 <= ext_h * kS, err, 212))
+        *reinterpret_cast<float4 *>(dCh + rh * kS + 4 * (kG * i + lg)) = aS[r][i];
+    if (lg == 0) {
       const int64_t o = ((int64_t)bh * nc + k) * T + t[r];
       qB[o] = qb[r];
-      dG[o] = gd - xdot[r];
+      dG[o] = gd[0] - xdot[r];
       gyx[o] = gx[r];
     }
   }
@@ -517,7 +581,11 @@ bwd_finish_kernel(const float *__restrict__ dt, const float *__restrict__ A,
   const int k = blockIdx.x, bh = blockIdx.y, b = bh / nh, h = bh - b * nh;
   const int tok0 = k * T, valid = min(T, L - tok0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (!SSD_IN_BOUNDS(b < nb && k < nc, err, 202)) return;  // uniform over the CTA
+  // every chunk-indexed buffer of this (chunk, head) (R, states, qB, dG,
+  // gyx, part) and its final state: checked once, uniform over the CTA
+  if (!SSD_IN_BOUNDS(b < nb && k < nc && h < nh && (int64_t)bh * nc + k < (int64_t)nb * nh * nc,
+                     err, 202))
+    return;
   // <R_k, h_{k+1}> over P x S
   const float *Rk = R + ((int64_t)bh * nc + k) * P * S;
   const float *hn = k + 1 < nc ? states + ((int64_t)bh * nc + k + 1) * P * S
@@ -546,8 +614,10 @@ bwd_finish_kernel(const float *__restrict__ dt, const float *__restrict__ A,
   const float eta = incl + after;
   float dA_part = 0.f, dD_part = 0.f;
   if (tid < valid) {
-    const float dtt = dt[((int64_t)b * L + tok0 + tid) * nh + h];
-    ddt[((int64_t)b * L + tok0 + tid) * nh + h] = A[h] * eta + qB[o];
+    const int64_t di = ((int64_t)b * L + tok0 + tid) * nh + h;
+    const bool ok = SSD_IN_BOUNDS(di < (int64_t)nb * L * nh, err, 213);
+    const float dtt = ok ? dt[di] : 0.f;
+    if (ok) ddt[di] = A[h] * eta + qB[o];
     dA_part = dtt * eta;
     dD_part = gyx[o];
   }
@@ -581,7 +651,7 @@ __global__ void __launch_bounds__(kThreads)
 bwd_reduce_kernel(const float *__restrict__ dBh, const float *__restrict__ dCh,
                   const float2 *__restrict__ part, float *__restrict__ dB,
                   float *__restrict__ dC, float *__restrict__ dA, float *__restrict__ dD,
-                  int64_t n_bc, int nh, int hpg, int S, int nc, int nb) {
+                  int64_t n_bc, int nh, int hpg, int S, int nc, int nb, int *err) {
   const int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const int ng = nh / hpg;
   if (e < n_bc) {
@@ -592,6 +662,7 @@ bwd_reduce_kernel(const float *__restrict__ dBh, const float *__restrict__ dCh,
     float sb = 0.f, sc = 0.f;
     for (int i = 0; i < hpg; ++i) {
       const int64_t src = (bt * nh + g * hpg + i) * S + s;
+      if (!SSD_IN_BOUNDS(src < n_bc * hpg, err, 214)) continue;
       sb += dBh[src];
       sc += dCh[src];
     }
@@ -602,7 +673,9 @@ bwd_reduce_kernel(const float *__restrict__ dBh, const float *__restrict__ dCh,
     float a = 0.f, d = 0.f;
     for (int b = 0; b < nb; ++b)
       for (int k = 0; k < nc; ++k) {
-        const float2 v = part[((int64_t)b * nh + h) * nc + k];
+        const int64_t pi = ((int64_t)b * nh + h) * nc + k;
+        if (!SSD_IN_BOUNDS(pi < (int64_t)nb * nh * nc, err, 215)) continue;
+        const float2 v = part[pi];
         a += v.x;
         d += v.y;
       }
@@ -642,17 +715,18 @@ cudaError_t launch_bwd_jump(const Dims &d, const float *v, const float *m, const
 }
 
 namespace {
-template <int kS, int kTok>
+template <int kS, int kG, int kTok>
 cudaError_t launch_main(const Dims &d, const float *x, const float *dt, const float *B,
                         const float *C, const float *D, const float *gy, const float *G,
                         const float *states, const float *R, float *dx, float *dBh, float *dCh,
                         float *qB, float *dG, float *gyx, int *err, cudaStream_t st) {
-  const size_t smem = MainSmem<kS, kTok>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<kS, kTok>,
+  using SM = MainSmem<kS, kG, kTok>;
+  const size_t smem = SM::bytes;
+  cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<kS, kG, kTok>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(d.nc * (d.T / (kTT * kTok))), (unsigned)(d.b * d.nh));
-  bwd_main_kernel<kS, kTok><<<grid, kThreads, smem, st>>>(
+  dim3 grid((unsigned)(d.nc * (d.T / SM::RT)), (unsigned)(d.b * d.nh));
+  bwd_main_kernel<kS, kG, kTok><<<grid, kThreads, smem, st>>>(
       x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG, gyx, err, (int)d.L, (int)d.nh,
       (int)d.hpg, (int)d.T, (int)d.nc, (int)d.b);
   return cudaGetLastError();
@@ -664,17 +738,21 @@ cudaError_t launch_bwd_main(const Dims &d, const float *x, const float *dt, cons
                             const float *states, const float *R, float *dx, float *dBh,
                             float *dCh, float *qB, float *dG, float *gyx, int *err,
                             cudaStream_t st) {
-  // two tokens per thread where the registers allow (dstate up to 128)
+  // lanes per token group and tokens per group, measured at b2 L16384 h32
+  // (S 64, 128) and b1 L32768 h48 g8 (S 256): (8, 2) 7.65 ms at S = 64 against
+  // 8.88 for (16, 2) and 9.51 for (16, 4); (8, 2) 10.7 ms at S = 128 against
+  // 12.0 for (16, 4) and 14.4 for (16, 2); (16, 4) 26.8 ms at S = 256
+  // against 30.8 for (16, 2) and 39.0 for (8, 1)
   switch (d.S) {
     case 64:
-      return launch_main<64, 2>(d, x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG, gyx,
-                                err, st);
+      return launch_main<64, 8, 2>(d, x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG,
+                                   gyx, err, st);
     case 128:
-      return launch_main<128, 2>(d, x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG, gyx,
-                                 err, st);
+      return launch_main<128, 8, 2>(d, x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG,
+                                    gyx, err, st);
     default:
-      return launch_main<256, 1>(d, x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG, gyx,
-                                 err, st);
+      return launch_main<256, 16, 4>(d, x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG,
+                                     gyx, err, st);
   }
 }
 
@@ -691,12 +769,12 @@ cudaError_t launch_bwd_finish(const Dims &d, const float *dt, const float *A, co
 
 cudaError_t launch_bwd_reduce(const Dims &d, const float *dBh, const float *dCh,
                               const float2 *part, float *dB, float *dC, float *dA, float *dD,
-                              cudaStream_t st) {
+                              int *err, cudaStream_t st) {
   const int64_t n_bc = d.hpg > 1 ? d.b * d.L * d.ng * d.S : 0;
   const int64_t n = n_bc + d.nh;
   bwd_reduce_kernel<<<(unsigned)((n + kThreads - 1) / kThreads), kThreads, 0, st>>>(
       dBh, dCh, part, dB, dC, dA, dD, n_bc, (int)d.nh, (int)d.hpg, (int)d.S, (int)d.nc,
-      (int)d.b);
+      (int)d.b, err);
   return cudaGetLastError();
 }
 

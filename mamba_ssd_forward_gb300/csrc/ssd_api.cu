@@ -744,7 +744,7 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
   });
   step([&] {
     return ssd::launch_bwd_reduce(d, dBh, dCh, part, static_cast<float *>(dB),
-                                  static_cast<float *>(dC), dA, dD, st);
+                                  static_cast<float *>(dC), dA, dD, err, st);
   });
   if (n_launches) *n_launches = launched;
   return from_cuda(e);

@@ -137,6 +137,6 @@ cudaError_t launch_bwd_finish(const Dims &d, const float *dt, const float *A, co
 // dB, dC (sums over a group's heads, skipped when nh == ng), dA, dD (nullable)
 cudaError_t launch_bwd_reduce(const Dims &d, const float *dBh, const float *dCh,
                               const float2 *part, float *dB, float *dC, float *dA, float *dD,
-                              cudaStream_t st);
+                              int *err, cudaStream_t st);
 
 }  // namespace ssd

@@ -3,7 +3,8 @@ SSD_DEBUG_BOUNDS): every plain global load and store of the kernels checks
 its index against its buffer's extent, skips an access that falls outside
 and reports SSD_ERR_BOUNDS through the call's error word.  Run on small
 configurations through every entry point (both I/O types, every output
-kernel of the bf16 launch plans, the step-wise calls and the decode step):
+kernel of the bf16 launch plans, the step-wise calls, the decode step and
+the backward pass):
 no check may fire, and the results still match the oracle.
 
 The status mapping itself is checked on the release library: a debug-bounds
@@ -88,6 +89,35 @@ def test_steps_and_decode_in_bounds(ssd_debug, w):
     ref = oracle_run(w, inp)
     check_io(to64(y), ref["y"], w.dtype, "step-wise y")
     check_io(to64(fin), ref["final_state"], w.dtype, "step-wise final_state")
+
+
+BWD_CASES = [
+    W.Workload("dbg_bwd_S128_g2", 1, 300, 4, 64, 128, 2, 256, "fp32", True),
+    W.Workload("dbg_bwd_S64_T64_hpg1", 2, 150, 2, 64, 64, 2, 64, "fp32", False),
+    W.Workload("dbg_bwd_S256_T128", 1, 200, 2, 64, 256, 1, 128, "fp32", True),
+]
+
+
+@pytest.mark.parametrize("w", BWD_CASES, ids=lambda w: w.name)
+def test_backward_in_bounds(ssd_debug, w):
+    """ssd_backward (all eight launches) with every check compiled in: no
+    check fires and every gradient still matches the oracle's adjoint."""
+    import oracle
+    inp = make(w, seed=10)
+    dev = device_inputs(inp)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(10)
+    gy = torch.randn(inp["x"].shape, generator=g)
+    gfinal = torch.randn((w.batch, w.nheads, w.headdim, w.dstate), generator=g)
+    ws = ssd_debug.new_workspace(
+        ssd_debug.backward_workspace_size(dev["x"], dev["B"], w.chunk), "cuda")
+    out = ssd_debug.backward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                             dev["h0"], gy.cuda(), gfinal.cuda(), chunk=w.chunk, workspace=ws)
+    ssd_debug.workspace_error(ws)
+    ref = oracle.backward(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                          inp["h0"], gy.double().numpy(), gfinal.double().numpy())
+    for n in ("dx", "ddt", "dA", "dB", "dC", "dD", "dh0"):
+        check_io(to64(out[n]), ref[n], "fp32", f"{w.name} {n}")
 
 
 def test_error_codes_map_to_statuses():
