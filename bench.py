@@ -559,7 +559,48 @@ def e2e(args, w, inp, dev, overlapped=True, plan=None):
            "api": "ssd_forward_host_overlapped" if overlapped else "ssd_forward_host"}
     if overlapped:
         out["n_slices"] = n_slices
+    out["copy_ceiling"] = copy_ceiling(h2d, d2h, dev, n)
+    out["copy_ceiling"]["frac"] = out["copy_ceiling"]["ms_floor"] / ms
     return out
+
+
+def copy_ceiling(h2d: int, d2h: int, dev, reps: int) -> dict:
+    """The host link's own limit for the e2e step: one pinned host-to-device
+    copy of the step's input bytes and one device-to-host copy of its output
+    bytes, each timed alone (CUDA events, best of reps) and both at once on
+    two streams.  ms_floor = the concurrent time, the least any call moving
+    those bytes can take."""
+    import torch
+    hs = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+    hd = torch.empty(h2d, dtype=torch.uint8, device=dev)
+    ds = torch.empty(d2h, dtype=torch.uint8, device=dev)
+    dd = torch.empty(d2h, dtype=torch.uint8).pin_memory()
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def timed(f):
+        best = float("inf")
+        for _ in range(max(3, reps)):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            f()
+            torch.cuda.synchronize()
+            best = min(best, (time.perf_counter() - t0) * 1e3)
+        return best
+
+    def up():
+        with torch.cuda.stream(s1):
+            hd.copy_(hs, non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(s2):
+            dd.copy_(ds, non_blocking=True)
+
+    t_up, t_down = timed(up), timed(down)
+    t_both = timed(lambda: (up(), down()))
+    return {"h2d_gbs": h2d / t_up / 1e6, "d2h_gbs": d2h / t_down / 1e6,
+            "ms_h2d": t_up, "ms_d2h": t_down, "ms_floor": t_both,
+            "how": "pinned copies of the step's bytes, host-timed around a synchronize, best of "
+                   f"{max(3, reps)}"}
 
 
 def run_decode(args, w):
@@ -622,7 +663,7 @@ def run_decode(args, w):
 # x the 2070 MHz maximum SM clock (the ALU roofline of the backward kernels)
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 BWD_KERNELS = ["chunk_cumsum", "bwd_jump(x, B)", "state_passing", "bwd_jump(gy, C)",
-               "state_passing(reverse)", "bwd_main", "bwd_finish", "bwd_reduce"]
+               "state_passing(reverse)", "bwd_cb", "bwd_main", "bwd_finish", "bwd_reduce"]
 
 
 def backward_macs(w: W.Workload) -> dict:
@@ -637,7 +678,7 @@ def backward_macs(w: W.Workload) -> dict:
         # per head: the scores gy_i . x_j and the four masked products
         # (ysm, dC, dx, q); the four state terms of every token
         main += w.batch * w.nheads * (npair * (3 * P + 2 * S) + 4 * v * P * S)
-        main += w.batch * w.ngroups * npair * S  # c_i . B_j, once per group
+        rest += w.batch * w.ngroups * npair * S  # c_i . B_j, once per group (bwd_cb)
         rest += w.batch * w.nheads * (2 * v * P * S + P * S)  # jump terms, <R_k, h_k+1>
     return {"bwd_main": main, "total": main + rest}
 

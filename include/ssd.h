@@ -429,9 +429,9 @@ SSD_API ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const voi
 /* ssd_backward recording CUDA events around its launches, as
  * ssd_forward_profiled does: events[0] before the first launch and
  * events[i] after launch i (i < n_events), *n_launches (may be NULL) = the
- * number of launches, 8: the cumsum, the forward jump terms, the state pass,
- * the adjoint's jump terms, the backward state pass, the per-token kernel,
- * the per-chunk finish and the reduction. */
+ * number of launches, 9: the cumsum, the forward jump terms, the state pass,
+ * the adjoint's jump terms, the backward state pass, c_i . B_j per chunk and
+ * group, the per-token kernel, the per-chunk finish and the reduction. */
 SSD_API ssd_status ssd_backward_profiled(const ssd_dims *dims, ssd_dtype dtype, const void *x,
                                          const void *dt, const float *A, const void *B,
                                          const void *C, const float *D, const float *h0,

@@ -113,6 +113,7 @@ bwd_jump_kernel(const float *__restrict__ v, const float *__restrict__ m,
   // extents (elements) of the buffers read and written, for the debug-bounds checks
   const int64_t ext_h = (int64_t)nb * L * nh, ext_g = (int64_t)nb * L * ng,
                 ext_chunk = (int64_t)nb * nh * nc;
+  (void)ext_h, (void)ext_g, (void)ext_chunk;  // read by the debug-bounds checks only
   // G and out of this (chunk, head): checked once, uniform over the CTA
   if (!SSD_IN_BOUNDS(b < nb && k < nc && (int64_t)bh * nc + k < ext_chunk, err, 200)) return;
   const int64_t rowh0 = ((int64_t)b * L + tok0) * nh + h, rowg0 = ((int64_t)b * L + tok0) * ng + g;
@@ -182,18 +183,99 @@ bwd_jump_kernel(const float *__restrict__ v, const float *__restrict__ m,
       *reinterpret_cast<float4 *>(dst + (4 * py + a) * kS + 4 * sx + 64 * q) = acc[a][q];
 }
 
+// ------------------------------------------------------- c_i . B_j per group
+
+// Kcb[b, k, g][i][j] = c_i . B_j for the tokens i, j of chunk k, in the 64 x
+// 64 blocks on or below the diagonal (j-block <= i-block; the other blocks
+// are neither written nor read), zero past the sequence.  The masked
+// products of every head of the group read it instead of forming the dot
+// products over S themselves.  One CTA per (block pair, chunk, batch *
+// group), 256 threads as a 16 x 16 grid, thread (ty, tx) owning rows
+// ty + 16 a and columns tx + 16 b (a, b < 4) of the block; 32-wide slices of
+// S staged in shared memory (rows padded to 36 floats).
+template <int kS>
+__global__ void __launch_bounds__(kThreads)
+bwd_cb_kernel(const float *__restrict__ Bm, const float *__restrict__ Cm,
+              float *__restrict__ Kcb, int *err, int L, int ng, int T, int nc, int nb) {
+  constexpr int KS = 32, LD = KS + 4;
+  __shared__ __align__(16) float cs[64][LD];
+  __shared__ __align__(16) float bs[64][LD];
+  const int nblk = T / 64, npair = nblk * (nblk + 1) / 2;
+  const int k = blockIdx.x / npair, pr = blockIdx.x - k * npair;
+  const int bg = blockIdx.y, b = bg / ng, g = bg - b * ng;
+  // block pair pr -> (I, J), J <= I, in row order
+  int I = 0, rem = pr;
+  while (rem > I) {
+    rem -= I + 1;
+    ++I;
+  }
+  const int J = rem;
+  const int tok0 = k * T, valid = min(T, L - tok0);
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int64_t ext_g = (int64_t)nb * L * ng;
+  (void)ext_g;  // read by the debug-bounds checks only
+  // this (chunk, group)'s T x T block of Kcb: checked once, uniform over the CTA
+  if (!SSD_IN_BOUNDS(b < nb && k < nc && ((int64_t)bg * nc + k) < (int64_t)nb * ng * nc, err,
+                     216))
+    return;
+  const int64_t rowg0 = ((int64_t)b * L + tok0) * ng + g;
+  float acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+  for (int k0 = 0; k0 < kS; k0 += KS) {
+    __syncthreads();
+    // 64 rows x 8 float4 of C (rows of block I) and of B (rows of block J)
+    for (int e = tid; e < 2 * 64 * (KS / 4); e += kThreads) {
+      const bool isC = e < 64 * (KS / 4);
+      const int e2 = isC ? e : e - 64 * (KS / 4), r = e2 / (KS / 4), c4 = e2 - r * (KS / 4);
+      const int tok = (isC ? I : J) * 64 + r;
+      const int64_t gi = (rowg0 + (int64_t)(tok < valid ? tok : 0) * ng) * kS + k0 + 4 * c4;
+      const bool ok = tok < valid && SSD_IN_BOUNDS(gi + 4 <= ext_g * kS, err, 217);
+      cp_async16(isC ? &cs[r][4 * c4] : &bs[r][4 * c4], ok ? (isC ? Cm : Bm) + gi : Cm, ok);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < KS / 4; ++q) {
+      float4 cv[4], bv[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) cv[a] = *reinterpret_cast<const float4 *>(&cs[ty + 16 * a][4 * q]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) bv[c] = *reinterpret_cast<const float4 *>(&bs[tx + 16 * c][4 * q]);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[a][c] = dot4(cv[a], bv[c], acc[a][c]);
+    }
+  }
+  float *dst = Kcb + ((int64_t)bg * nc + k) * T * T;
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      dst[(int64_t)(I * 64 + ty + 16 * a) * T + J * 64 + tx + 16 * c] = acc[a][c];
+}
+
 // -------------------------------------------------------------- main kernel
 
 // Shared-memory plan of bwd_main_kernel (float4 units): two column tiles
-// U1 [NT][S/4] and U2 [NT][P/4] (double-buffered), the row tile's own rows
-// O1 [RT][S/4] and O2 [RT][P/4], the state Ms [P][S/4] (float4 slots XOR-
-// swizzled by bits 2..4 of the row), then G and dt of the chunk (256 each).
+// U1 [NT][S/4] and U2 [NT][P/4] (double-buffered), whose space holds the row
+// tile's own rows O1 [RT][S/4] and O2 [RT][P/4] once the column loop is
+// done (RT <= 2 NT), the state Ms [P][S/4] (float4 slots XOR-
+// swizzled by bits 2..4 of the row), the c . B block of the tile pair Kt
+// (double-buffered; [NT][RT + 4] floats in the upper pass, [RT][NT + 4] in
+// the lower one), then G and dt of the chunk (256 each).
 // kG lanes share a token group, which owns kTok tokens: RT = (256 / kG) kTok.
 template <int kS, int kG, int kTok>
 struct MainSmem {
   static constexpr int NG = kThreads / kG, RT = NG * kTok, NT = kTT, S4 = kS / 4, P4 = kP / 4;
-  static constexpr int U1 = 0, U2 = U1 + 2 * NT * S4, O1 = U2 + 2 * NT * P4, O2 = O1 + RT * S4,
-                       Ms = O2 + RT * P4, end4 = Ms + kP * S4;
+  static constexpr int KU = RT + 4, KL = NT + 4;  // row strides (floats) of the Kt layouts
+  static constexpr int KT4 = (NT * KU > RT * KL ? NT * KU : RT * KL) / 4;
+  static constexpr int U1 = 0, U2 = U1 + 2 * NT * S4, O1 = U1, O2 = U2, Ms = U2 + 2 * NT * P4,
+                       Kt = Ms + kP * S4, end4 = Kt + 2 * KT4;
   static constexpr size_t bytes = 16 * (size_t)end4 + 2 * 256 * sizeof(float);
   static_assert(RT % kTT == 0 && RT <= 2 * kTT, "row tiles of 32 or 64 tokens");
   static_assert(S4 % kG == 0 && P4 % kG == 0, "whole float4 slots per lane");
@@ -253,15 +335,31 @@ template <int kS, int kG, int kTok, bool kUpper>
 __device__ __forceinline__ void main_pass(
     float4 *sm4, float *Gs, float *ds, const float *own_g, const float *own_h,
     const float *col_g, const float *col_h, const float *state, int64_t st_row,
-    float4 (&accP)[kTok][kP / 4 / kG], float4 (&accS)[kTok][kS / 4 / kG],
-    float4 (&rS)[kTok][kS / 4 / kG], float4 (&rP)[kTok][kP / 4 / kG], const int (&t)[kTok],
+    const float *Kc, int T, float4 (&accP)[kTok][kP / 4 / kG],
+    float4 (&accS)[kTok][kS / 4 / kG], float4 (&rP)[kTok][kP / 4 / kG], const int (&t)[kTok],
     const bool (&live)[kTok], int tau, int valid, int64_t rowh0, int64_t rowg0, int nh, int ng,
     int tid, int lg, int grp, int64_t ext_h, int64_t ext_g, int *err) {
   using SM = MainSmem<kS, kG, kTok>;
   constexpr int NG = SM::NG, RT = SM::RT, NT = SM::NT, S4 = SM::S4, P4 = SM::P4;
   constexpr int QS = S4 / kG, QP = P4 / kG;
+  constexpr int KU = SM::KU, KL = SM::KL, KTF = 4 * SM::KT4;
   float4 *U1 = sm4 + SM::U1, *U2 = sm4 + SM::U2, *O1 = sm4 + SM::O1, *O2 = sm4 + SM::O2,
          *Ms = sm4 + SM::Ms;
+  float *Kt = reinterpret_cast<float *>(sm4 + SM::Kt);
+  // stage the c . B values of column tile u and the row tile into buffer
+  // buf: upper pass Kt[j][rr] = c_s . B_t (s = u NT + j, t = tau RT + rr),
+  // lower pass Kt[rr][j] = c_t . B_j (j = u NT + j); every entry lies in a
+  // block on or below the diagonal, which bwd_cb_kernel wrote
+  auto stage_k = [&](int buf, int u) {
+    float *dst = Kt + buf * KTF;
+    constexpr int rows = kUpper ? NT : RT, cols4 = (kUpper ? RT : NT) / 4;
+    for (int e = tid; e < rows * cols4; e += kThreads) {
+      const int r = e / cols4, c4 = e - r * cols4;
+      const int i = kUpper ? u * NT + r : tau * RT + r, j = kUpper ? tau * RT + 4 * c4
+                                                                  : u * NT + 4 * c4;
+      cp_async16(dst + r * (kUpper ? KU : KL) + 4 * c4, Kc + (int64_t)i * T + j, true);
+    }
+  };
   // stage `rows` tokens from chunk-relative token t0 of a per-group (width
   // S) or per-head (width P) tensor, zeros past the sequence
   auto stage = [&](float4 *dst, const float *src, bool per_head, int t0, int rows) {
@@ -281,14 +379,7 @@ __device__ __forceinline__ void main_pass(
   for (int r = 0; r < kTok; ++r) {
     Gt[r] = Gs[t[r]];
     dtt[r] = ds[t[r]];
-    // this token's own rows: B_t, x_t (upper) or C_t, gy_t (lower)
-#pragma unroll
-    for (int i = 0; i < QS; ++i) {
-      const int64_t gi = (rowg0 + (int64_t)t[r] * ng) * kS + 4 * (kG * i + lg);
-      rS[r][i] = live[r] && SSD_IN_BOUNDS(gi + 4 <= ext_g * kS, err, 207)
-                     ? *reinterpret_cast<const float4 *>(own_g + gi)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    // this token's own row x_t (upper) or gy_t (lower)
 #pragma unroll
     for (int i = 0; i < QP; ++i) {
       const int64_t hi = (rowh0 + (int64_t)t[r] * nh) * kP + 4 * (kG * i + lg);
@@ -301,21 +392,22 @@ __device__ __forceinline__ void main_pass(
   const int u0 = kUpper ? tau * RT / NT : 0;
   const int u1 = kUpper ? ucount : min(ucount, (tau + 1) * RT / NT);
   __syncthreads();  // the buffers of the previous pass are free
-  stage(O1, own_g, false, tau * RT, RT);
-  stage(O2, own_h, true, tau * RT, RT);
   stage(U1, col_g, false, u0 * NT, NT);
   stage(U2, col_h, true, u0 * NT, NT);
+  stage_k(0, u0);
   cp_async_commit();
   for (int u = u0; u < u1; ++u) {
     const int cur = (u - u0) & 1;
     if (u + 1 < u1) {
       stage(U1 + (cur ^ 1) * NT * S4, col_g, false, (u + 1) * NT, NT);
       stage(U2 + (cur ^ 1) * NT * P4, col_h, true, (u + 1) * NT, NT);
+      stage_k(cur ^ 1, u + 1);
     }
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();
     const float4 *u1p = U1 + cur * NT * S4 + lg, *u2p = U2 + cur * NT * P4 + lg;
+    const float *ktp = Kt + cur * KTF;
     // token r meets this column tile at all unless its 32-token block lies
     // wholly on the masked side of the diagonal; the loop body is compiled
     // once per set of active blocks (a condition uniform over the CTA, so
@@ -331,20 +423,17 @@ __device__ __forceinline__ void main_pass(
         for (int i = 0; i < QS; ++i) cS[i] = u1p[j * S4 + kG * i];
 #pragma unroll
         for (int i = 0; i < QP; ++i) cP[i] = u2p[j * P4 + kG * i];
-        float d[2 * kTok];  // B_t . C_s and x_t . gy_s (upper) per token
+        float d[kTok];  // x_t . gy_s (upper) or gy_t . x_j (lower) per token
 #pragma unroll
         for (int r = 0; r < kTok; ++r) {
-          float a = 0.f, c = 0.f;
+          float c = 0.f;
           if (on(r)) {
-#pragma unroll
-            for (int i = 0; i < QS; ++i) a = dot4(rS[r][i], cS[i], a);
 #pragma unroll
             for (int i = 0; i < QP; ++i) c = dot4(rP[r][i], cP[i], c);
           }
-          d[2 * r] = a;
-          d[2 * r + 1] = c;
+          d[r] = c;
         }
-        group_sums<2 * kTok, kG>(d, tid & 31);
+        group_sums<kTok, kG>(d, tid & 31);
         const float Gc = Gs[s], dc = ds[s];
 #pragma unroll
         for (int r = 0; r < kTok; ++r) {
@@ -357,7 +446,9 @@ __device__ __forceinline__ void main_pass(
           }
           // upper: dx += dt_t w (B_t . C_s) gy_s, q += w (x_t . gy_s) C_s;
           // lower: ysm += w (C_t . B_j) x_j,      dC += w (gy_t . x_j) B_j
-          const float aP = (kUpper ? dtt[r] : 1.f) * w * d[2 * r], aS = w * d[2 * r + 1];
+          const int rr = NG * r + grp;
+          const float cb = kUpper ? ktp[j * KU + rr] : ktp[rr * KL + j];
+          const float aP = (kUpper ? dtt[r] : 1.f) * w * cb, aS = w * d[r];
 #pragma unroll
           for (int i = 0; i < QP; ++i) axpy4(aP, cP[i], accP[r][i]);
 #pragma unroll
@@ -380,6 +471,11 @@ __device__ __forceinline__ void main_pass(
     __syncthreads();  // tile u's buffer is refilled two iterations on
   }
   cp_async_wait<0>();
+  // (the loop ended with a barrier: the column buffers are free) the row
+  // tile's own rows into them, for the state terms
+  stage(O1, own_g, false, tau * RT, RT);
+  stage(O2, own_h, true, tau * RT, RT);
+  cp_async_commit();
   // the state terms: M = R_k (upper: dx += dt_t exp2(G_last - G_t) R B_t,
   // q += exp2(G_last - G_t) R^T x_t) or h_k (lower: ysm += exp2(G_t) h c_t,
   // dC += exp2(G_t) h^T gy_t), M staged with float4 slot c4 of row p at
@@ -389,6 +485,7 @@ __device__ __forceinline__ void main_pass(
     Ms[p * S4 + (c4 ^ ((p >> 2) & 7))] =
         *reinterpret_cast<const float4 *>(state + st_row + 4 * (int64_t)e);
   }
+  cp_async_wait<0>();
   __syncthreads();
   const float GL = Gs[valid - 1];
   float fP[kTok], fS[kTok];
@@ -447,10 +544,10 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
                 const float *__restrict__ Bm, const float *__restrict__ Cm,
                 const float *__restrict__ D, const float *__restrict__ gy,
                 const float *__restrict__ G, const float *__restrict__ states,
-                const float *__restrict__ R, float *__restrict__ dx,
-                float *__restrict__ dBh, float *__restrict__ dCh, float *__restrict__ qB,
-                float *__restrict__ dG, float *__restrict__ gyx, int *err, int L, int nh,
-                int hpg, int T, int nc, int nb) {
+                const float *__restrict__ R, const float *__restrict__ Kcb,
+                float *__restrict__ dx, float *__restrict__ dBh, float *__restrict__ dCh,
+                float *__restrict__ qB, float *__restrict__ dG, float *__restrict__ gyx, int *err,
+                int L, int nh, int hpg, int T, int nc, int nb) {
   using SM = MainSmem<kS, kG, kTok>;
   constexpr int NG = SM::NG, RT = SM::RT, QS = kS / 4 / kG, QP = kP / 4 / kG;
   extern __shared__ float4 sm4[];
@@ -464,9 +561,13 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
   // extents (elements per row width) of the buffers, for the debug-bounds checks
   const int64_t ext_h = (int64_t)nb * L * nh, ext_g = (int64_t)nb * L * ng,
                 ext_chunk = (int64_t)nb * nh * nc;
+  (void)ext_h, (void)ext_g, (void)ext_chunk;  // read by the debug-bounds checks only
   // G, qB, dG, gyx and the states of this (chunk, head): checked once,
   // uniform over the CTA
-  if (!SSD_IN_BOUNDS(b < nb && k < nc && (int64_t)bh * nc + k < ext_chunk, err, 201)) return;
+  if (!SSD_IN_BOUNDS(b < nb && k < nc && (int64_t)bh * nc + k < ext_chunk &&
+                         ((int64_t)(b * ng + g) * nc + k) < (int64_t)nb * ng * nc,
+                     err, 201))
+    return;
   if (tau * RT >= valid) return;  // tile past the sequence
   int t[kTok];
   bool live[kTok];
@@ -485,7 +586,8 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
   }
   __syncthreads();
   const int64_t st_row = ((int64_t)bh * nc + k) * kP * kS;
-  float4 rS[kTok][QS], rP[kTok][QP], aP[kTok][QP], aS[kTok][QS];
+  const float *Kc = Kcb + ((int64_t)(b * ng + g) * nc + k) * T * T;
+  float4 rP[kTok][QP], aP[kTok][QP], aS[kTok][QS];
   auto zero = [&]() {
 #pragma unroll
     for (int r = 0; r < kTok; ++r) {
@@ -497,9 +599,10 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
   };
   // upper pass: dx and q (rS = B_t, rP = x_t)
   zero();
-  main_pass<kS, kG, kTok, true>(sm4, Gs, ds, Bm, x, Cm, gy, R, st_row, aP, aS, rS, rP, t, live,
-                                tau, valid, rowh0, rowg0, nh, ng, tid, lg, grp, ext_h, ext_g,
-                                err);
+  main_pass<kS, kG, kTok, true>(sm4, Gs, ds, Bm, x, Cm, gy, R, st_row, Kc, T, aP, aS, rP, t,
+                                live, tau, valid, rowh0, rowg0, nh, ng, tid, lg, grp, ext_h,
+                                ext_g, err);
+  const float4 *O1 = sm4 + SM::O1;  // B rows of the tile, until the lower pass restages
   const float Dh = D ? D[h] : 0.f;
   float xdot[kTok], qb[kTok], gx[kTok];
 #pragma unroll
@@ -523,7 +626,7 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
 #pragma unroll
     for (int i = 0; i < QS; ++i) {
       const int f = 4 * (kG * i + lg);
-      v3[1] = dot4(aS[r][i], rS[r][i], v3[1]);
+      v3[1] = dot4(aS[r][i], O1[(NG * r + grp) * (kS / 4) + kG * i + lg], v3[1]);
       if (live[r] && SSD_IN_BOUNDS(rh * kS + f + 4 <= ext_h * kS, err, 211)) {
         const float4 a = aS[r][i];
         const float dtv = ds[t[r]];
@@ -538,8 +641,8 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
   }
   // lower pass: ysm and dC (rS = C_t, rP = gy_t)
   zero();
-  main_pass<kS, kG, kTok, false>(sm4, Gs, ds, Cm, gy, Bm, x, states, st_row, aP, aS, rS, rP, t,
-                                 live, tau, valid, rowh0, rowg0, nh, ng, tid, lg, grp, ext_h,
+  main_pass<kS, kG, kTok, false>(sm4, Gs, ds, Cm, gy, Bm, x, states, st_row, Kc, T, aP, aS, rP,
+                                 t, live, tau, valid, rowh0, rowg0, nh, ng, tid, lg, grp, ext_h,
                                  ext_g, err);
 #pragma unroll
   for (int r = 0; r < kTok; ++r) {
@@ -715,11 +818,22 @@ cudaError_t launch_bwd_jump(const Dims &d, const float *v, const float *m, const
 }
 
 namespace {
+template <int kS>
+cudaError_t launch_cb(const Dims &d, const float *B, const float *C, float *Kcb, int *err,
+                      cudaStream_t st) {
+  const int nblk = (int)d.T / 64;
+  dim3 grid((unsigned)(d.nc * (nblk * (nblk + 1) / 2)), (unsigned)(d.b * d.ng));
+  bwd_cb_kernel<kS><<<grid, kThreads, 0, st>>>(B, C, Kcb, err, (int)d.L, (int)d.ng, (int)d.T,
+                                               (int)d.nc, (int)d.b);
+  return cudaGetLastError();
+}
+
 template <int kS, int kG, int kTok>
 cudaError_t launch_main(const Dims &d, const float *x, const float *dt, const float *B,
                         const float *C, const float *D, const float *gy, const float *G,
-                        const float *states, const float *R, float *dx, float *dBh, float *dCh,
-                        float *qB, float *dG, float *gyx, int *err, cudaStream_t st) {
+                        const float *states, const float *R, const float *Kcb, float *dx,
+                        float *dBh, float *dCh, float *qB, float *dG, float *gyx, int *err,
+                        cudaStream_t st) {
   using SM = MainSmem<kS, kG, kTok>;
   const size_t smem = SM::bytes;
   cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<kS, kG, kTok>,
@@ -727,31 +841,40 @@ cudaError_t launch_main(const Dims &d, const float *x, const float *dt, const fl
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(d.nc * (d.T / SM::RT)), (unsigned)(d.b * d.nh));
   bwd_main_kernel<kS, kG, kTok><<<grid, kThreads, smem, st>>>(
-      x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG, gyx, err, (int)d.L, (int)d.nh,
-      (int)d.hpg, (int)d.T, (int)d.nc, (int)d.b);
+      x, dt, B, C, D, gy, G, states, R, Kcb, dx, dBh, dCh, qB, dG, gyx, err, (int)d.L,
+      (int)d.nh, (int)d.hpg, (int)d.T, (int)d.nc, (int)d.b);
   return cudaGetLastError();
 }
 }  // namespace
 
+cudaError_t launch_bwd_cb(const Dims &d, const float *B, const float *C, float *Kcb, int *err,
+                          cudaStream_t st) {
+  switch (d.S) {
+    case 64: return launch_cb<64>(d, B, C, Kcb, err, st);
+    case 128: return launch_cb<128>(d, B, C, Kcb, err, st);
+    default: return launch_cb<256>(d, B, C, Kcb, err, st);
+  }
+}
+
 cudaError_t launch_bwd_main(const Dims &d, const float *x, const float *dt, const float *B,
                             const float *C, const float *D, const float *gy, const float *G,
-                            const float *states, const float *R, float *dx, float *dBh,
-                            float *dCh, float *qB, float *dG, float *gyx, int *err,
+                            const float *states, const float *R, const float *Kcb, float *dx,
+                            float *dBh, float *dCh, float *qB, float *dG, float *gyx, int *err,
                             cudaStream_t st) {
-  // lanes per token group and tokens per group, measured at b2 L16384 h32
-  // (S 64, 128) and b1 L32768 h48 g8 (S 256): (8, 2) 7.65 ms at S = 64 against
-  // 8.88 for (16, 2) and 9.51 for (16, 4); (8, 2) 10.7 ms at S = 128 against
-  // 12.0 for (16, 4) and 14.4 for (16, 2); (16, 4) 26.8 ms at S = 256
-  // against 30.8 for (16, 2) and 39.0 for (8, 1)
+  // lanes per token group and tokens per group, measured with the shared
+  // c . B tiles at b2 L16384 h32 (S 64, 128) and b1 L32768 h48 g8 (S 256):
+  // (8, 2) 6.48 ms at S = 64 against 7.84 for (16, 4) and 10.0 for (16, 2);
+  // (8, 2) 9.12 ms at S = 128 against 10.6 for (16, 4) and 13.2 for (16, 2);
+  // (16, 4) 20.7 ms at S = 256 against 21.0 for (8, 2) and 26.0 for (16, 2)
   switch (d.S) {
     case 64:
-      return launch_main<64, 8, 2>(d, x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG,
+      return launch_main<64, 8, 2>(d, x, dt, B, C, D, gy, G, states, R, Kcb, dx, dBh, dCh, qB, dG,
                                    gyx, err, st);
     case 128:
-      return launch_main<128, 8, 2>(d, x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG,
+      return launch_main<128, 8, 2>(d, x, dt, B, C, D, gy, G, states, R, Kcb, dx, dBh, dCh, qB, dG,
                                     gyx, err, st);
     default:
-      return launch_main<256, 16, 4>(d, x, dt, B, C, D, gy, G, states, R, dx, dBh, dCh, qB, dG,
+      return launch_main<256, 16, 4>(d, x, dt, B, C, D, gy, G, states, R, Kcb, dx, dBh, dCh, qB, dG,
                                      gyx, err, st);
   }
 }

@@ -648,10 +648,10 @@ namespace {
 // the chunk jump terms (the forward's, then the adjoint's), the start states
 // h_k, the adjoint states R_k, the forward's final state, the per-head shares
 // of dB and dC (only when a group has several heads), the per-token q . B,
-// dL/dG and gy . x, and the per-chunk shares of dA and dD.  Each part is
-// 256-byte aligned.
+// dL/dG and gy . x, the per-chunk shares of dA and dD, and c_i . B_j of every
+// chunk and group (T x T).  Each part is 256-byte aligned.
 struct BwdLayout {
-  size_t G, dst, states, R, fin, dBh, dCh, qB, dG, gyx, part, total;
+  size_t G, dst, states, R, fin, dBh, dCh, qB, dG, gyx, part, Kcb, total;
 };
 
 BwdLayout bwd_layout(const Dims &d) {
@@ -670,7 +670,8 @@ BwdLayout bwd_layout(const Dims &d) {
   w.dG = w.qB + tok;
   w.gyx = w.dG + tok;
   w.part = w.gyx + tok;
-  w.total = w.part + round256(2 * sizeof(float) * d.b * d.nh * d.nc);
+  w.Kcb = w.part + round256(2 * sizeof(float) * d.b * d.nh * d.nc);
+  w.total = w.Kcb + round256(sizeof(float) * d.b * d.ng * d.nc * d.T * d.T);
   return w;
 }
 
@@ -732,8 +733,9 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
   step([&] {
     return ssd::launch_state_passing(d, dst, G, gfinal, R, dh0, err, st, false, true);
   });
+  step([&] { return ssd::launch_bwd_cb(d, Bf, Cf, f(w.Kcb), err, st); });
   step([&] {
-    return ssd::launch_bwd_main(d, xf, dtf, Bf, Cf, D, gyf, G, sts, R,
+    return ssd::launch_bwd_main(d, xf, dtf, Bf, Cf, D, gyf, G, sts, R, f(w.Kcb),
                                 static_cast<float *>(dx), dBh, dCh, f(w.qB), f(w.dG),
                                 f(w.gyx), err, st);
   });

@@ -123,11 +123,15 @@ bool bwd_supported(const Dims &d);
 // (v = x, m = B: w_t = exp2(G_last - G_t) dt_t)
 cudaError_t launch_bwd_jump(const Dims &d, const float *v, const float *m, const float *dt,
                             const float *G, float *out, int *err, cudaStream_t st);
+// Kcb [b, nc, ng, T, T]: c_i . B_j of every chunk and group, in the 64 x 64
+// blocks on or below the diagonal
+cudaError_t launch_bwd_cb(const Dims &d, const float *B, const float *C, float *Kcb, int *err,
+                          cudaStream_t st);
 // per token: dx, dt q (dBh), the head's dC (dCh), q . B, dL/dG, gy . x
 cudaError_t launch_bwd_main(const Dims &d, const float *x, const float *dt, const float *B,
                             const float *C, const float *D, const float *gy, const float *G,
-                            const float *states, const float *R, float *dx, float *dBh,
-                            float *dCh, float *qB, float *dG, float *gyx, int *err,
+                            const float *states, const float *R, const float *Kcb, float *dx,
+                            float *dBh, float *dCh, float *qB, float *dG, float *gyx, int *err,
                             cudaStream_t st);
 // ddt, and the per-chunk shares of dA and dD
 cudaError_t launch_bwd_finish(const Dims &d, const float *dt, const float *A, const float *R,
