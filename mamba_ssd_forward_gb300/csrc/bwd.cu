@@ -267,7 +267,8 @@ bwd_cb_kernel(const float *__restrict__ Bm, const float *__restrict__ Cm,
 // done (RT <= 2 NT), the state Ms [P][S/4] (float4 slots XOR-
 // swizzled by bits 2..4 of the row), the c . B block of the tile pair Kt
 // (double-buffered; [NT][RT + 4] floats in the upper pass, [RT][NT + 4] in
-// the lower one), then G and dt of the chunk (256 each).
+// the lower one), the two weights of every (token, column) pair of a tile
+// Wt [2][RT][NT + 4] floats, then G and dt of the chunk (256 each).
 // kG lanes share a token group, which owns kTok tokens: RT = (256 / kG) kTok.
 template <int kS, int kG, int kTok>
 struct MainSmem {
@@ -275,7 +276,7 @@ struct MainSmem {
   static constexpr int KU = RT + 4, KL = NT + 4;  // row strides (floats) of the Kt layouts
   static constexpr int KT4 = (NT * KU > RT * KL ? NT * KU : RT * KL) / 4;
   static constexpr int U1 = 0, U2 = U1 + 2 * NT * S4, O1 = U1, O2 = U2, Ms = U2 + 2 * NT * P4,
-                       Kt = Ms + kP * S4, end4 = Kt + 2 * KT4;
+                       Kt = Ms + kP * S4, Wt = Kt + 2 * KT4, end4 = Wt + RT * KL / 2;
   static constexpr size_t bytes = 16 * (size_t)end4 + 2 * 256 * sizeof(float);
   static_assert(RT % kTT == 0 && RT <= 2 * kTT, "row tiles of 32 or 64 tokens");
   static_assert(S4 % kG == 0 && P4 % kG == 0, "whole float4 slots per lane");
@@ -318,6 +319,26 @@ __device__ __forceinline__ void group_sums(float (&v)[V], int lane) {
   }
 }
 
+// Sums each of the kG values v[] over the kG lanes of a token group and
+// leaves one total in each lane: the reduce-scatter of group_sums (kG - 1
+// shuffles).  Returns the total; *idx = the index (into v) it belongs to.
+template <int kG>
+__device__ __forceinline__ float group_scatter(float (&v)[kG], int lane, int *idx) {
+  int id = 0;
+#pragma unroll
+  for (int n = kG, o = 1; n > 1; n >>= 1, o <<= 1) {
+    const bool up = lane & o;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float keep = up ? v[i + n / 2] : v[i], send = up ? v[i] : v[i + n / 2];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+    if (up) id += n / 2;
+  }
+  *idx = id;
+  return v[0];
+}
+
 // One CTA per (row tile of RT tokens of a chunk, chunk, batch * head), 256
 // threads: thread = (token group grp = tid / kG, lane lg = tid % kG), the
 // group owning tokens grp + NG r (r < kTok) of the tile and lane lg the
@@ -346,6 +367,7 @@ __device__ __forceinline__ void main_pass(
   float4 *U1 = sm4 + SM::U1, *U2 = sm4 + SM::U2, *O1 = sm4 + SM::O1, *O2 = sm4 + SM::O2,
          *Ms = sm4 + SM::Ms;
   float *Kt = reinterpret_cast<float *>(sm4 + SM::Kt);
+  float *Wt = reinterpret_cast<float *>(sm4 + SM::Wt);
   // stage the c . B values of column tile u and the row tile into buffer
   // buf: upper pass Kt[j][rr] = c_s . B_t (s = u NT + j, t = tau RT + rr),
   // lower pass Kt[rr][j] = c_t . B_j (j = u NT + j); every entry lies in a
@@ -412,49 +434,73 @@ __device__ __forceinline__ void main_pass(
     // wholly on the masked side of the diagonal; the loop body is compiled
     // once per set of active blocks (a condition uniform over the CTA, so
     // the shuffles stay warp-wide); inactive tokens skip their arithmetic
+    // two phases: first the scores of all the tile's columns, then the
+    // updates
     auto tile = [&](auto mask_c) {
       constexpr int kMask = decltype(mask_c)::value;
       auto on = [](int r) { return ((kMask >> ((r * NG) / kTT)) & 1) != 0; };
+      // scores: x_t . gy_s (upper) or gy_t . x_j (lower) of this group's
+      // tokens and kG / kTok columns at a time, summed over the group's lanes
+      // by one reduce-scatter (one total per lane), which each lane turns
+      // into the pair's two weights in Wt
+      constexpr int CB = kG / kTok;
+      static_assert(CB >= 1 && NT % CB == 0, "columns per reduce-scatter");
+#pragma unroll 2
+      for (int j0 = 0; j0 < NT; j0 += CB) {
+        float v[kG];
+#pragma unroll
+        for (int c = 0; c < CB; ++c) {
+          float4 cP[QP];
+#pragma unroll
+          for (int i = 0; i < QP; ++i) cP[i] = u2p[(j0 + c) * P4 + kG * i];
+#pragma unroll
+          for (int r = 0; r < kTok; ++r) {
+            float a = 0.f;
+            if (on(r)) {
+#pragma unroll
+              for (int i = 0; i < QP; ++i) a = dot4(rP[r][i], cP[i], a);
+            }
+            v[c * kTok + r] = a;
+          }
+        }
+        int idx;
+        const float d = group_scatter<kG>(v, tid & 31, &idx);
+        const int r = idx % kTok, j = j0 + idx / kTok, s = u * NT + j;
+        const int rr = NG * r + grp, tr = tau * RT + rr;
+        const float Gc = Gs[s], Gr = Gs[tr];
+        float w = 0.f;
+        if (kUpper) {
+          if (s >= tr && s < valid && tr < valid) w = exp2f(Gc - Gr);
+        } else {
+          if (s <= tr && tr < valid) w = exp2f(Gr - Gc) * ds[s];  // dt = 0 past the sequence
+        }
+        // upper: dx += dt_t w (B_t . C_s) gy_s, q += w (x_t . gy_s) C_s;
+        // lower: ysm += w (C_t . B_j) x_j,      dC += w (gy_t . x_j) B_j
+        const float cb = kUpper ? ktp[j * KU + rr] : ktp[rr * KL + j];
+        Wt[rr * KL + j] = (kUpper ? ds[tr] : 1.f) * w * cb;
+        Wt[RT * KL + rr * KL + j] = w * d;
+      }
+      __syncwarp();  // a group's weights come from its own lanes
+      // updates: every column row loaded serves the group's kTok tokens
 #pragma unroll 2
       for (int j = 0; j < NT; ++j) {
-        const int s = u * NT + j;
         float4 cS[QS], cP[QP];
 #pragma unroll
         for (int i = 0; i < QS; ++i) cS[i] = u1p[j * S4 + kG * i];
 #pragma unroll
         for (int i = 0; i < QP; ++i) cP[i] = u2p[j * P4 + kG * i];
-        float d[kTok];  // x_t . gy_s (upper) or gy_t . x_j (lower) per token
-#pragma unroll
-        for (int r = 0; r < kTok; ++r) {
-          float c = 0.f;
-          if (on(r)) {
-#pragma unroll
-            for (int i = 0; i < QP; ++i) c = dot4(rP[r][i], cP[i], c);
-          }
-          d[r] = c;
-        }
-        group_sums<kTok, kG>(d, tid & 31);
-        const float Gc = Gs[s], dc = ds[s];
 #pragma unroll
         for (int r = 0; r < kTok; ++r) {
           if (!on(r)) continue;
-          float w = 0.f;
-          if (kUpper) {
-            if (s >= t[r] && s < valid && live[r]) w = exp2f(Gc - Gt[r]);
-          } else {
-            if (s <= t[r] && live[r]) w = exp2f(Gt[r] - Gc) * dc;  // dt = 0 past the sequence
-          }
-          // upper: dx += dt_t w (B_t . C_s) gy_s, q += w (x_t . gy_s) C_s;
-          // lower: ysm += w (C_t . B_j) x_j,      dC += w (gy_t . x_j) B_j
           const int rr = NG * r + grp;
-          const float cb = kUpper ? ktp[j * KU + rr] : ktp[rr * KL + j];
-          const float aP = (kUpper ? dtt[r] : 1.f) * w * cb, aS = w * d[r];
+          const float aP = Wt[rr * KL + j], aS = Wt[RT * KL + rr * KL + j];
 #pragma unroll
           for (int i = 0; i < QP; ++i) axpy4(aP, cP[i], accP[r][i]);
 #pragma unroll
           for (int i = 0; i < QS; ++i) axpy4(aS, cS[i], accS[r][i]);
         }
       }
+      __syncwarp();  // the weights are rewritten for the next tile
     };
     // active 32-token blocks of the row tile (RT is 32 or 64 tokens)
     int mask = 0;
@@ -861,21 +907,22 @@ cudaError_t launch_bwd_main(const Dims &d, const float *x, const float *dt, cons
                             const float *states, const float *R, const float *Kcb, float *dx,
                             float *dBh, float *dCh, float *qB, float *dG, float *gyx, int *err,
                             cudaStream_t st) {
-  // lanes per token group and tokens per group, measured with the shared
-  // c . B tiles at b2 L16384 h32 (S 64, 128) and b1 L32768 h48 g8 (S 256):
-  // (8, 2) 6.48 ms at S = 64 against 7.84 for (16, 4) and 10.0 for (16, 2);
-  // (8, 2) 9.12 ms at S = 128 against 10.6 for (16, 4) and 13.2 for (16, 2);
-  // (16, 4) 20.7 ms at S = 256 against 21.0 for (8, 2) and 26.0 for (16, 2)
+  // 16-lane token groups of four tokens for every dstate: measured against
+  // (8, 2) with the column loop in one phase (each column's dot products
+  // summed over the group and used at once) at b2 L16384 h32 (S 64, 128)
+  // and b1 L32768 h48 g8 (S 256): 6.51 against 6.48 ms at S = 64, 8.25
+  // against 9.12 ms at S = 128, 18.2 against 20.6 ms at S = 256; (8, 2) in
+  // two phases took 7.09 / 9.56 / 22.0 ms
   switch (d.S) {
     case 64:
-      return launch_main<64, 8, 2>(d, x, dt, B, C, D, gy, G, states, R, Kcb, dx, dBh, dCh, qB, dG,
-                                   gyx, err, st);
+      return launch_main<64, 16, 4>(d, x, dt, B, C, D, gy, G, states, R, Kcb, dx, dBh, dCh, qB,
+                                    dG, gyx, err, st);
     case 128:
-      return launch_main<128, 8, 2>(d, x, dt, B, C, D, gy, G, states, R, Kcb, dx, dBh, dCh, qB, dG,
-                                    gyx, err, st);
+      return launch_main<128, 16, 4>(d, x, dt, B, C, D, gy, G, states, R, Kcb, dx, dBh, dCh, qB,
+                                     dG, gyx, err, st);
     default:
-      return launch_main<256, 16, 4>(d, x, dt, B, C, D, gy, G, states, R, Kcb, dx, dBh, dCh, qB, dG,
-                                     gyx, err, st);
+      return launch_main<256, 16, 4>(d, x, dt, B, C, D, gy, G, states, R, Kcb, dx, dBh, dCh, qB,
+                                     dG, gyx, err, st);
   }
 }
 
