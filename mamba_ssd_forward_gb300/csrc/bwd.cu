@@ -268,15 +268,22 @@ bwd_cb_kernel(const float *__restrict__ Bm, const float *__restrict__ Cm,
 // swizzled by bits 2..4 of the row), the c . B block of the tile pair Kt
 // (double-buffered; [NT][RT + 4] floats in the upper pass, [RT][NT + 4] in
 // the lower one), the two weights of every (token, column) pair of a tile
-// Wt [2][RT][NT + 4] floats, then G and dt of the chunk (256 each).
+// Wt [2][RT][NT + 4] floats, then G and dt of the chunk (256 each).  Ms
+// overlays Kt and Wt up to dstate 128.
 // kG lanes share a token group, which owns kTok tokens: RT = (256 / kG) kTok.
 template <int kS, int kG, int kTok>
 struct MainSmem {
   static constexpr int NG = kThreads / kG, RT = NG * kTok, NT = kTT, S4 = kS / 4, P4 = kP / 4;
   static constexpr int KU = RT + 4, KL = NT + 4;  // row strides (floats) of the Kt layouts
   static constexpr int KT4 = (NT * KU > RT * KL ? NT * KU : RT * KL) / 4;
-  static constexpr int U1 = 0, U2 = U1 + 2 * NT * S4, O1 = U1, O2 = U2, Ms = U2 + 2 * NT * P4,
-                       Kt = Ms + kP * S4, Wt = Kt + 2 * KT4, end4 = Wt + RT * KL / 2;
+  // up to dstate 128 the state shares the space of Kt and Wt, which the
+  // column loop is done with when the state is staged: two CTAs fit on an SM
+  static constexpr bool kShare = kS <= 128;
+  static constexpr int U1 = 0, U2 = U1 + 2 * NT * S4, O1 = U1, O2 = U2, X = U2 + 2 * NT * P4;
+  static constexpr int Ms = X, Kt = kShare ? X : Ms + kP * S4, Wt = Kt + 2 * KT4;
+  static constexpr int end4 = kShare && Ms + kP * S4 > Wt + RT * KL / 2 ? Ms + kP * S4
+                                                                        : Wt + RT * KL / 2;
+  static constexpr int kCtas = kShare ? 2 : 1;  // CTAs per SM
   static constexpr size_t bytes = 16 * (size_t)end4 + 2 * 256 * sizeof(float);
   static_assert(RT % kTT == 0 && RT <= 2 * kTT, "row tiles of 32 or 64 tokens");
   static_assert(S4 % kG == 0 && P4 % kG == 0, "whole float4 slots per lane");
@@ -585,7 +592,7 @@ __device__ __forceinline__ void main_pass(
 }
 
 template <int kS, int kG, int kTok>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, MainSmem<kS, kG, kTok>::kCtas)
 bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
                 const float *__restrict__ Bm, const float *__restrict__ Cm,
                 const float *__restrict__ D, const float *__restrict__ gy,
