@@ -5,8 +5,9 @@ L = <gy, y> + <gfinal, final_state> with seeded gy and gfinal.  Cases: every
 supported dstate, chunks of 64 (the step-kernel forward), 128 and 256,
 ragged last chunks, one token, several heads per group (dB, dC summed over
 heads) and one (written directly), with and without h0, gfinal and D,
-chunks steep enough to underflow their decay, and repeated calls (fixed
-summation order: the same bits)."""
+chunks steep enough to underflow their decay, repeated calls (fixed
+summation order: the same bits), and the full-size shapes the bench times,
+checked on one group of one batch."""
 import pytest
 import torch
 
@@ -132,3 +133,37 @@ def test_backward_rejects_bf16_and_unsupported(ssd):
     w = W.Workload("bwd_P32", 1, 256, 2, 32, 128, 1, 256, "fp32", False)
     inp = device_inputs(make(w, seed=0))
     assert ssd.backward_workspace_size(inp["x"], inp["B"], 256) == 0
+
+
+FULL = [W.LONG_32K.with_(name=W.LONG_32K.name.replace("bf16", "fp32"), dtype="fp32"),
+        W.Workload("sweep_fp32_S128_L16384_T256", 2, 16384, 32, 64, 128, 1, 256, "fp32", True)]
+
+
+@pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
+def test_backward_full_size_sampled(ssd, w):
+    """The full-size shapes the bench times (the long-context layer in fp32
+    and a sweep shape), in the bench's launch configuration: every output
+    of one group of one batch -- dx, ddt, dA, dD, dh0 of its heads and the
+    group's dB, dC (sums over exactly those heads) -- against the oracle's
+    chunked backward on that slice (pinned to the adjoint recurrence)."""
+    import oracle
+    inp = make(w, seed=35)
+    gy, gfinal = grads_in(w, 35)
+    out = run(ssd, w, inp, gy, gfinal)
+    hpg = w.nheads // w.ngroups
+    bi, g = w.batch - 1, w.ngroups // 2
+    hs = slice(g * hpg, (g + 1) * hpg)
+    sl = lambda t: None if t is None else t[bi:bi + 1, :, hs]
+    ref = oracle.backward_chunked(
+        sl(inp["x"]), sl(inp["dt"]), inp["A"][hs], inp["B"][bi:bi + 1, :, g:g + 1],
+        inp["C"][bi:bi + 1, :, g:g + 1], inp["D"][hs],
+        None if inp["h0"] is None else inp["h0"][bi:bi + 1, hs], sl(gy).numpy(),
+        gfinal[bi:bi + 1, hs].numpy(), chunk=w.chunk)
+    got = {"dx": out["dx"][bi:bi + 1, :, hs], "ddt": out["ddt"][bi:bi + 1, :, hs],
+           "dB": out["dB"][bi:bi + 1, :, g:g + 1], "dC": out["dC"][bi:bi + 1, :, g:g + 1],
+           "dh0": out["dh0"][bi:bi + 1, hs]}
+    for n, v in got.items():
+        check_io(to64(v), ref[n], "fp32", f"{w.name} {n}")
+    if w.batch == 1:  # dA and dD sum over the batch
+        check_io(to64(out["dA"][hs]), ref["dA"], "fp32", f"{w.name} dA")
+        check_io(to64(out["dD"][hs]), ref["dD"], "fp32", f"{w.name} dD")
