@@ -414,9 +414,11 @@ SSD_API size_t ssd_backward_workspace_size(const ssd_dims *dims, ssd_dtype dtype
  * forward's intermediates (G, start states, final state) are recomputed in
  * `workspace` (>= ssd_backward_workspace_size bytes, 256-byte aligned, its
  * first SSD_WS_HEADER_BYTES zeroed before its first use).
- * SSD_F32 only (SSD_BF16 returns SSD_ERR_UNSUPPORTED), with P = 64, S in
- * {64, 128, 256}; every product of the backward, and of the forward
- * states it recomputes, runs in fp32 on the CUDA cores.  dB, dC,
+ * P = 64, S in {64, 128, 256}.  Every product of the backward, and of the
+ * forward states it recomputes, runs in fp32 on the CUDA cores.  With
+ * SSD_BF16, x, dt, B, C, gy and dx, ddt, dB, dC are bf16 (converted to and
+ * from fp32 copies in the workspace, one launch each way); dA, dD, dh0, A,
+ * D, h0 and gfinal are fp32 with either dtype.  dB, dC,
  * dA and dD are summed in a fixed order: repeated calls give the same bits.
  * Allocates nothing and never synchronises. */
 SSD_API ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x,
@@ -431,7 +433,8 @@ SSD_API ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const voi
  * events[i] after launch i (i < n_events), *n_launches (may be NULL) = the
  * number of launches, 9: the cumsum, the forward jump terms, the state pass,
  * the adjoint's jump terms, the backward state pass, c_i . B_j per chunk and
- * group, the per-token kernel, the per-chunk finish and the reduction. */
+ * group, the per-token kernel, the per-chunk finish and the reduction (11
+ * with SSD_BF16: the input conversion first, the output conversion last). */
 SSD_API ssd_status ssd_backward_profiled(const ssd_dims *dims, ssd_dtype dtype, const void *x,
                                          const void *dt, const float *A, const void *B,
                                          const void *C, const float *D, const float *h0,

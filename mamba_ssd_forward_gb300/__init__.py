@@ -123,8 +123,9 @@ def backward(x, dt, A, B, C, D=None, h0=None, gy=None, gfinal=None, chunk: int =
              workspace=None, want_dD: bool = True, want_dh0: bool = True, out=None,
              events=None) -> dict:
     """Gradients of a loss through forward() given gy = dL/dy and gfinal =
-    dL/dfinal_state (None = 0), by ssd_backward (fp32 I/O): a dict of dx,
-    ddt, dA, dB, dC, dD, dh0 (the last two None unless wanted).  `workspace`
+    dL/dfinal_state (None = 0), by ssd_backward (fp32 or bf16 I/O, computed in
+    fp32): a dict of dx, ddt, dB, dC (in the I/O dtype), dA, dD, dh0 (fp32;
+    the last two None unless wanted).  `workspace`
     may be a preallocated new_workspace(backward_workspace_size(...)) and
     `out` a dict returned by an earlier call (its tensors are reused).  With
     `events` (torch.cuda.Event, enable_timing) the call is

@@ -36,6 +36,7 @@
 // All in fp32 on the CUDA cores (the tensor-core version is the next step):
 // about 30 million multiply-adds per chunk and head at T = 256, P = 64,
 // S = 128.
+#include <algorithm>
 #include <type_traits>
 
 #include "ssd_internal.cuh"
@@ -840,7 +841,58 @@ bwd_reduce_kernel(const float *__restrict__ dBh, const float *__restrict__ dCh,
   }
 }
 
+// ------------------------------------------------------------ bf16 <-> fp32
+
+// The bf16 I/O of ssd_backward: up to five tensors converted in one launch
+// (bf16 -> fp32 before the fp32 pass, fp32 -> bf16 of its outputs after
+// it), eight elements a step where a segment allows (16-byte aligned
+// pointers, as the library requires), the tail one by one.
+__global__ void __launch_bounds__(kThreads)
+bwd_convert_kernel(const BwdConvert a) {
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  const int64_t first = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  for (int sg = 0; sg < a.nseg; ++sg) {
+    const int64_t n = a.seg[sg].n, n8 = n / 8;
+    if (a.to_bf16) {
+      const float4 *src = static_cast<const float4 *>(a.seg[sg].src);
+      uint4 *dst = static_cast<uint4 *>(a.seg[sg].dst);
+      for (int64_t i = first; i < n8; i += stride) {
+        const float4 lo = src[2 * i], hi = src[2 * i + 1];
+        __nv_bfloat162 o[4] = {__floats2bfloat162_rn(lo.x, lo.y), __floats2bfloat162_rn(lo.z, lo.w),
+                               __floats2bfloat162_rn(hi.x, hi.y), __floats2bfloat162_rn(hi.z, hi.w)};
+        dst[i] = *reinterpret_cast<const uint4 *>(o);
+      }
+      const float *s1 = static_cast<const float *>(a.seg[sg].src);
+      __nv_bfloat16 *d1 = static_cast<__nv_bfloat16 *>(a.seg[sg].dst);
+      for (int64_t i = 8 * n8 + first; i < n; i += stride) d1[i] = __float2bfloat16_rn(s1[i]);
+    } else {
+      const uint4 *src = static_cast<const uint4 *>(a.seg[sg].src);
+      float4 *dst = static_cast<float4 *>(a.seg[sg].dst);
+      for (int64_t i = first; i < n8; i += stride) {
+        const uint4 v = src[i];
+        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
+        const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]),
+                     f2 = __bfloat1622float2(b2[2]), f3 = __bfloat1622float2(b2[3]);
+        dst[2 * i] = make_float4(f0.x, f0.y, f1.x, f1.y);
+        dst[2 * i + 1] = make_float4(f2.x, f2.y, f3.x, f3.y);
+      }
+      const __nv_bfloat16 *s1 = static_cast<const __nv_bfloat16 *>(a.seg[sg].src);
+      float *d1 = static_cast<float *>(a.seg[sg].dst);
+      for (int64_t i = 8 * n8 + first; i < n; i += stride) d1[i] = __bfloat162float(s1[i]);
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_convert(const BwdConvert &a, cudaStream_t st) {
+  int64_t n = 0;
+  for (int i = 0; i < a.nseg; ++i) n = std::max<int64_t>(n, a.seg[i].n);
+  const int64_t want = (n / 8 + kThreads - 1) / kThreads;
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(want, 4 * (int64_t)sm_count()));
+  bwd_convert_kernel<<<blocks, kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
 
 bool bwd_supported(const Dims &d) {
   return d.P == kP && (d.S == 64 || d.S == 128 || d.S == 256) && d.T % kTT == 0 && d.T <= 256;

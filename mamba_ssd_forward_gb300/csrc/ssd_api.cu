@@ -649,13 +649,16 @@ namespace {
 // h_k, the adjoint states R_k, the forward's final state, the per-head shares
 // of dB and dC (only when a group has several heads), the per-token q . B,
 // dL/dG and gy . x, the per-chunk shares of dA and dD, and c_i . B_j of every
-// chunk and group (T x T).  Each part is 256-byte aligned.
+// chunk and group (T x T); with bf16 I/O then fp32 copies of x, dt, B, C, gy
+// and fp32 buffers for dx, ddt, dB, dC.  Each part is 256-byte aligned.
 struct BwdLayout {
-  size_t G, dst, states, R, fin, dBh, dCh, qB, dG, gyx, part, Kcb, total;
+  size_t G, dst, states, R, fin, dBh, dCh, qB, dG, gyx, part, Kcb;
+  size_t cx, cdt, cB, cC, cgy, cdx, cddt, cdB, cdC;  // bf16 I/O only
+  size_t total;
 };
 
-BwdLayout bwd_layout(const Dims &d) {
-  BwdLayout w;
+BwdLayout bwd_layout(const Dims &d, ssd_dtype dtype) {
+  BwdLayout w{};
   const size_t tok = round256(sizeof(float) * d.b * d.nh * d.nc * d.T);
   const size_t st = round256(sizeof(float) * d.b * d.nh * d.nc * d.P * d.S);
   const size_t hs = d.hpg > 1 ? round256(sizeof(float) * d.b * d.L * d.nh * d.S) : 0;
@@ -672,6 +675,21 @@ BwdLayout bwd_layout(const Dims &d) {
   w.part = w.gyx + tok;
   w.Kcb = w.part + round256(2 * sizeof(float) * d.b * d.nh * d.nc);
   w.total = w.Kcb + round256(sizeof(float) * d.b * d.ng * d.nc * d.T * d.T);
+  if (dtype == SSD_BF16) {
+    const size_t xs = round256(sizeof(float) * d.b * d.L * d.nh * d.P),
+                 ts = round256(sizeof(float) * d.b * d.L * d.nh),
+                 gs = round256(sizeof(float) * d.b * d.L * d.ng * d.S);
+    w.cx = w.total;
+    w.cdt = w.cx + xs;
+    w.cB = w.cdt + ts;
+    w.cC = w.cB + gs;
+    w.cgy = w.cC + gs;
+    w.cdx = w.cgy + xs;
+    w.cddt = w.cdx + xs;
+    w.cdB = w.cddt + ts;
+    w.cdC = w.cdB + gs;
+    w.total = w.cdC + gs;
+  }
   return w;
 }
 
@@ -679,7 +697,7 @@ ssd_status check_backward_dims(const ssd_dims *dims, ssd_dtype dtype, Dims *d) {
   const ssd_status s = check_dims(dims, d);
   if (s != SSD_OK) return s;
   if (!valid_dtype(dtype)) return SSD_ERR_INVALID_ARG;
-  if (dtype != SSD_F32 || !ssd::bwd_supported(*d)) return SSD_ERR_UNSUPPORTED;
+  if (!ssd::bwd_supported(*d)) return SSD_ERR_UNSUPPORTED;
   return SSD_OK;
 }
 
@@ -699,18 +717,29 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
       !opt(dD) || !opt(dh0) || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
       n_events < 0 || (n_events > 0 && !events))
     return SSD_ERR_INVALID_ARG;
-  const BwdLayout w = bwd_layout(d);
+  const BwdLayout w = bwd_layout(d, dtype);
   if (ws_bytes < w.total) return SSD_ERR_INVALID_ARG;
   int *err = static_cast<int *>(workspace);
   char *ws = static_cast<char *>(workspace);
   auto f = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
-  const float *xf = static_cast<const float *>(x), *dtf = static_cast<const float *>(dt),
-              *Bf = static_cast<const float *>(B), *Cf = static_cast<const float *>(C),
-              *gyf = static_cast<const float *>(gy);
+  // bf16 I/O: the fp32 pass below reads fp32 copies of the inputs and writes
+  // fp32 gradients into the workspace, converted to bf16 at the end
+  const bool bf = dtype == SSD_BF16;
+  const float *xf = bf ? f(w.cx) : static_cast<const float *>(x),
+              *dtf = bf ? f(w.cdt) : static_cast<const float *>(dt),
+              *Bf = bf ? f(w.cB) : static_cast<const float *>(B),
+              *Cf = bf ? f(w.cC) : static_cast<const float *>(C),
+              *gyf = bf ? f(w.cgy) : static_cast<const float *>(gy);
+  float *dxf = bf ? f(w.cdx) : static_cast<float *>(dx),
+        *ddtf = bf ? f(w.cddt) : static_cast<float *>(ddt),
+        *dBf = bf ? f(w.cdB) : static_cast<float *>(dB),
+        *dCf = bf ? f(w.cdC) : static_cast<float *>(dC);
   float *G = f(w.G), *dst = f(w.dst), *sts = f(w.states), *R = f(w.R), *fin = f(w.fin);
   // with one head per group the per-head shares of dB and dC are dB and dC
-  float *dBh = d.hpg > 1 ? f(w.dBh) : static_cast<float *>(dB);
-  float *dCh = d.hpg > 1 ? f(w.dCh) : static_cast<float *>(dC);
+  float *dBh = d.hpg > 1 ? f(w.dBh) : dBf;
+  float *dCh = d.hpg > 1 ? f(w.dCh) : dCf;
+  const int64_t n_x = d.b * d.L * d.nh * d.P, n_t = d.b * d.L * d.nh,
+                n_g = d.b * d.L * d.ng * d.S;
   int launched = 0;
   auto mark = [&](int i) -> cudaError_t {
     if (events && i < n_events) return cudaEventRecord((cudaEvent_t)events[i], st);
@@ -722,9 +751,20 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
     if (e == cudaSuccess) e = launch();
     if (e == cudaSuccess) e = mark(++launched);
   };
+  if (bf) {
+    ssd::BwdConvert cv{};
+    cv.seg[0] = {x, f(w.cx), n_x};
+    cv.seg[1] = {dt, f(w.cdt), n_t};
+    cv.seg[2] = {B, f(w.cB), n_g};
+    cv.seg[3] = {C, f(w.cC), n_g};
+    cv.seg[4] = {gy, f(w.cgy), n_x};
+    cv.nseg = 5;
+    cv.to_bf16 = 0;
+    step([&] { return ssd::launch_bwd_convert(cv, st); });
+  }
   // the forward's cumsum, jump terms, start states and final state, all in
   // fp32 (the forward's own jump kernels take TF32 products)
-  step([&] { return ssd::launch_chunk_cumsum(d, dtype, dt, A, G, err, st); });
+  step([&] { return ssd::launch_chunk_cumsum(d, SSD_F32, dtf, A, G, err, st); });
   step([&] { return ssd::launch_bwd_jump(d, xf, Bf, dtf, G, dst, err, st); });
   step([&] { return ssd::launch_state_passing(d, dst, G, h0, sts, fin, err, st); });
   // the adjoint: its jump terms (over the forward's, no longer needed), the
@@ -735,19 +775,27 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
   });
   step([&] { return ssd::launch_bwd_cb(d, Bf, Cf, f(w.Kcb), err, st); });
   step([&] {
-    return ssd::launch_bwd_main(d, xf, dtf, Bf, Cf, D, gyf, G, sts, R, f(w.Kcb),
-                                static_cast<float *>(dx), dBh, dCh, f(w.qB), f(w.dG),
-                                f(w.gyx), err, st);
+    return ssd::launch_bwd_main(d, xf, dtf, Bf, Cf, D, gyf, G, sts, R, f(w.Kcb), dxf, dBh, dCh,
+                                f(w.qB), f(w.dG), f(w.gyx), err, st);
   });
   float2 *part = reinterpret_cast<float2 *>(ws + w.part);
   step([&] {
-    return ssd::launch_bwd_finish(d, dtf, A, R, sts, fin, f(w.qB), f(w.dG), f(w.gyx),
-                                  static_cast<float *>(ddt), part, err, st);
+    return ssd::launch_bwd_finish(d, dtf, A, R, sts, fin, f(w.qB), f(w.dG), f(w.gyx), ddtf, part,
+                                  err, st);
   });
   step([&] {
-    return ssd::launch_bwd_reduce(d, dBh, dCh, part, static_cast<float *>(dB),
-                                  static_cast<float *>(dC), dA, dD, err, st);
+    return ssd::launch_bwd_reduce(d, dBh, dCh, part, dBf, dCf, dA, dD, err, st);
   });
+  if (bf) {
+    ssd::BwdConvert cv{};
+    cv.seg[0] = {dxf, dx, n_x};
+    cv.seg[1] = {ddtf, ddt, n_t};
+    cv.seg[2] = {dBf, dB, n_g};
+    cv.seg[3] = {dCf, dC, n_g};
+    cv.nseg = 4;
+    cv.to_bf16 = 1;
+    step([&] { return ssd::launch_bwd_convert(cv, st); });
+  }
   if (n_launches) *n_launches = launched;
   return from_cuda(e);
 }
@@ -759,7 +807,7 @@ extern "C" {
 size_t ssd_backward_workspace_size(const ssd_dims *dims, ssd_dtype dtype) {
   Dims d;
   if (check_backward_dims(dims, dtype, &d) != SSD_OK) return 0;
-  return bwd_layout(d).total;
+  return bwd_layout(d, dtype).total;
 }
 
 ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const void *x, const void *dt,

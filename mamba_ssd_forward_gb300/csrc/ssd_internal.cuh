@@ -112,6 +112,19 @@ cudaError_t launch_decode_step(int64_t b, int64_t nh, int64_t P, int64_t S, int6
                                const void *B, const void *C, const float *D, float *state,
                                void *y, int *err, cudaStream_t st);
 
+// bf16 <-> fp32 conversion of up to five tensors in one launch (the bf16
+// I/O of ssd_backward): to_bf16 = 0 reads bf16 and writes fp32, 1 the
+// reverse; n elements per segment, 16-byte aligned pointers.
+struct BwdConvert {
+  struct Seg {
+    const void *src;
+    void *dst;
+    int64_t n;
+  } seg[5];
+  int nseg, to_bf16;
+};
+cudaError_t launch_bwd_convert(const BwdConvert &a, cudaStream_t st);
+
 // Backward pass for fp32 I/O (bwd.cu), CUDA cores.  bwd_supported: P = 64,
 // S in {64, 128, 256}, T a multiple of 32 up to 256.  Shapes (fp32):
 // dR, R [b, nh, nc, P, S]; dBh, dCh [b, L, nh, S] (per-head shares of dB,

@@ -123,16 +123,41 @@ def test_backward_is_deterministic(ssd):
             assert torch.equal(first[n], again[n]), n
 
 
-def test_backward_rejects_bf16_and_unsupported(ssd):
-    w = W.Workload("bwd_bf16", 1, 256, 2, 64, 128, 1, 256, "bf16", False)
+def test_backward_rejects_unsupported(ssd):
+    w = W.Workload("bwd_P32", 1, 256, 2, 32, 128, 1, 256, "fp32", False)
     inp = device_inputs(make(w, seed=0))
     assert ssd.backward_workspace_size(inp["x"], inp["B"], 256) == 0
     with pytest.raises(ssd.SsdError):
         ssd.backward(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], None,
                      torch.zeros_like(inp["x"]), None, chunk=256)
-    w = W.Workload("bwd_P32", 1, 256, 2, 32, 128, 1, 256, "fp32", False)
-    inp = device_inputs(make(w, seed=0))
-    assert ssd.backward_workspace_size(inp["x"], inp["B"], 256) == 0
+
+
+BF16 = [
+    W.Workload("bwd_bf16_S128_T256_g2", 1, 700, 8, 64, 128, 2, 256, "bf16", True),
+    W.Workload("bwd_bf16_S64_T128_hpg1", 2, 333, 4, 64, 64, 4, 128, "bf16", False),
+    W.Workload("bwd_bf16_S256_T256", 1, 520, 4, 64, 256, 1, 256, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("w", BF16, ids=lambda w: w.name)
+def test_backward_bf16_io(ssd, w):
+    """bf16 I/O: the same fp32 computation on the bf16 inputs (gy rounded to
+    bf16 as well), dx, ddt, dB, dC rounded to bf16 at the end and held to
+    the bf16 bound; dA, dD, dh0 stay fp32 and keep the fp32 bound."""
+    inp = make(w, seed=36)
+    gy, gfinal = grads_in(w, 36)
+    gy = gy.to(torch.bfloat16)
+    dev = device_inputs(inp)
+    ws = ssd.new_workspace(ssd.backward_workspace_size(dev["x"], dev["B"], w.chunk), "cuda")
+    out = ssd.backward(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], dev["h0"],
+                       gy.cuda(), gfinal.float().cuda(), chunk=w.chunk, workspace=ws)
+    ssd.workspace_error(ws)
+    ref = reference(inp, gy.double(), gfinal)
+    for n in ("dx", "ddt", "dB", "dC"):
+        assert out[n].dtype == torch.bfloat16
+        check_io(to64(out[n]), ref[n], "bf16", f"{w.name} {n}")
+    for n in ("dA", "dD", "dh0"):
+        check_io(to64(out[n]), ref[n], "fp32", f"{w.name} {n}")
 
 
 FULL = [W.LONG_32K.with_(name=W.LONG_32K.name.replace("bf16", "fp32"), dtype="fp32"),
