@@ -20,7 +20,7 @@ from ._abi import SSD_BF16, SSD_F32, SsdError  # noqa: F401
 
 __all__ = ["forward", "chunk_cumsum", "chunk_state", "state_passing", "chunk_scan",
            "decode_step", "workspace_size", "new_workspace", "workspace_error", "dims_of",
-           "backward", "backward_workspace_size",
+           "backward", "backward_workspace_size", "ssd",
            "SsdError"]
 
 
@@ -371,3 +371,38 @@ def device_error() -> None:
     workspace (the step-wise entry points, ssd_forward_noalloc) gave up a
     bounded wait since the last check (ssd_device_error)."""
     _abi.check("ssd_device_error", _abi.load().ssd_device_error(_stream()))
+
+
+class _SsdFunction(torch.autograd.Function):
+    """forward() and backward() as one differentiable operation: the forward
+    pass through ssd_forward, the gradients of every tensor input through
+    ssd_backward (which recomputes the forward's intermediates itself, so
+    only the inputs are saved)."""
+
+    @staticmethod
+    def forward(ctx, x, dt, A, B, C, D, h0, chunk):
+        y, final_state = forward(x, dt, A, B, C, D, h0, chunk=chunk)
+        ctx.save_for_backward(x, dt, A, B, C, D, h0)
+        ctx.chunk = chunk
+        return y, final_state
+
+    @staticmethod
+    def backward(ctx, gy, gfinal):
+        x, dt, A, B, C, D, h0 = ctx.saved_tensors
+        need = ctx.needs_input_grad
+        if gy is None:
+            gy = torch.zeros_like(x)
+        g = backward(x, dt, A, B, C, D, h0, gy.contiguous(),
+                     None if gfinal is None else gfinal.float().contiguous(), chunk=ctx.chunk,
+                     want_dD=D is not None and need[5], want_dh0=h0 is not None and need[6])
+        return (g["dx"] if need[0] else None, g["ddt"] if need[1] else None,
+                g["dA"] if need[2] else None, g["dB"] if need[3] else None,
+                g["dC"] if need[4] else None, g["dD"] if D is not None and need[5] else None,
+                g["dh0"] if h0 is not None and need[6] else None, None)
+
+
+def ssd(x, dt, A, B, C, D=None, h0=None, chunk: int = 256):
+    """y, final_state = the SSD forward pass, differentiable with respect to
+    x, dt, A, B, C, D and h0 (autograd; the backward pass is ssd_backward,
+    P = 64, S in {64, 128, 256})."""
+    return _SsdFunction.apply(x, dt, A, B, C, D, h0, chunk)

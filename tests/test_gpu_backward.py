@@ -192,3 +192,24 @@ def test_backward_full_size_sampled(ssd, w):
     if w.batch == 1:  # dA and dD sum over the batch
         check_io(to64(out["dA"][hs]), ref["dA"], "fp32", f"{w.name} dA")
         check_io(to64(out["dD"][hs]), ref["dD"], "fp32", f"{w.name} dD")
+
+
+def test_autograd_function(ssd):
+    """ssd.ssd() under torch.autograd: the gradients of a loss
+    <gy, y> + <gfinal, final_state> reach every input and match the oracle's
+    adjoint recurrence; inputs that do not require grad get none."""
+    w = W.Workload("bwd_autograd", 1, 400, 4, 64, 64, 2, 128, "fp32", True)
+    inp = make(w, seed=37)
+    gy, gfinal = grads_in(w, 37)
+    dev = device_inputs(inp)
+    leaves = {k: dev[k].clone().requires_grad_(k != "D") for k in
+              ("x", "dt", "A", "B", "C", "D", "h0")}
+    y, fin = ssd.ssd(leaves["x"], leaves["dt"], leaves["A"], leaves["B"], leaves["C"],
+                     leaves["D"], leaves["h0"], chunk=w.chunk)
+    loss = (y * gy.float().cuda()).sum() + (fin * gfinal.float().cuda()).sum()
+    loss.backward()
+    ref = reference(inp, gy, gfinal)
+    names = {"x": "dx", "dt": "ddt", "A": "dA", "B": "dB", "C": "dC", "h0": "dh0"}
+    for k, n in names.items():
+        check_io(to64(leaves[k].grad), ref[n], "fp32", f"autograd {n}")
+    assert leaves["D"].grad is None
