@@ -343,3 +343,43 @@ def test_debug_bounds_library_builds_with_every_export():
     for n in _abi.EXPORTS:
         assert hasattr(lib, n), n
     assert path != _abi.LIB_PATH
+
+
+def test_backward_workspace_and_rejections(lib):
+    """ssd_backward: its workspace holds at least G, the jump terms, the
+    start and adjoint states and the c . B blocks (and the fp32 copies with
+    bf16 I/O); unsupported dims give 0 / SSD_ERR_UNSUPPORTED, bad pointers,
+    a short or misaligned workspace SSD_ERR_INVALID_ARG, all before any
+    launch."""
+    from mamba_ssd_forward_gb300 import _abi
+    d = dims()  # b2 L1000 h8 P64 S128 ng2 T256 (nc = 4)
+    nc, T = 4, 256
+    ws32 = lib.ssd_backward_workspace_size(ctypes.byref(d), 0)
+    st = 4 * 2 * 8 * nc * 64 * 128
+    assert ws32 >= 256 + 4 * 2 * 8 * nc * T + 3 * st + 4 * 2 * 2 * nc * T * T
+    assert ws32 % 256 == 0
+    ws16 = lib.ssd_backward_workspace_size(ctypes.byref(d), 1)
+    assert ws16 >= ws32 + 4 * 2 * 1000 * (2 * 8 * 64 + 2 * 2 * 128)  # fp32 copies of x, gy, B, C
+    assert lib.ssd_backward_workspace_size(ctypes.byref(d), 7) == 0
+    for bad in (dims(headdim=32), dims(dstate=96), dims(headdim=128)):
+        assert lib.ssd_backward_workspace_size(ctypes.byref(bad), 0) == 0
+    ok = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    args = [ok, ok, ok, ok, ok, None, None, ok, None, ok, ok, ok, ok, ok, None, None]
+
+    def call(dd, dtype, a, wsp, nbytes):
+        return lib.ssd_backward(ctypes.byref(dd), dtype, *a, wsp, nbytes, None)
+
+    assert call(dims(dstate=96), 0, args, ok, ws32) == _abi.SSD_ERR_UNSUPPORTED
+    for i in range(len(args)):  # x dt A B C D h0 gy gfinal dx ddt dA dB dC dD dh0
+        a = list(args)
+        if args[i] is not None:  # required: NULL is rejected
+            a[i] = None
+            assert call(d, 0, a, ok, ws32) == _abi.SSD_ERR_INVALID_ARG, i
+        a[i] = odd  # required or optional: misaligned is rejected
+        assert call(d, 0, a, ok, ws32) == _abi.SSD_ERR_INVALID_ARG, i
+    assert call(d, 0, args, ok, ws32 - 1) == _abi.SSD_ERR_INVALID_ARG
+    assert call(d, 0, args, ctypes.c_void_p((1 << 20) + 16), ws32) == _abi.SSD_ERR_INVALID_ARG
+    assert call(d, 1, args, ok, ws16 - 1) == _abi.SSD_ERR_INVALID_ARG
+    assert lib.ssd_backward_profiled(ctypes.byref(d), 0, *args, ok, ws32, None, None, 2,
+                                     None) == _abi.SSD_ERR_INVALID_ARG  # events NULL, n 2
