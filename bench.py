@@ -675,9 +675,12 @@ def backward_macs(w: W.Workload) -> dict:
     for k in range(w.nchunks):
         v = min(T, w.seqlen - k * T)
         npair = v * (v + 1) // 2
-        # per head: the scores gy_i . x_j and the four masked products
-        # (ysm, dC, dx, q); the four state terms of every token
-        main += w.batch * w.nheads * (npair * (3 * P + 2 * S) + 4 * v * P * S)
+        # per head: the scores gy_i . x_j and the P-wide masked products
+        # (ysm, dx); the four state terms of every token.  Per group: the
+        # S-wide masked products (dB, dC), whose weights add up over the
+        # group's heads before they meet B or C
+        main += w.batch * w.nheads * (npair * 3 * P + 4 * v * P * S)
+        main += w.batch * w.ngroups * npair * 2 * S
         rest += w.batch * w.ngroups * npair * S  # c_i . B_j, once per group (bwd_cb)
         rest += w.batch * w.nheads * (2 * v * P * S + P * S)  # jump terms, <R_k, h_k+1>
     return {"bwd_main": main, "total": main + rest}

@@ -646,13 +646,12 @@ namespace {
 
 // Workspace of ssd_backward (fp32): the header (the call's error word), G,
 // the chunk jump terms (the forward's, then the adjoint's), the start states
-// h_k, the adjoint states R_k, the forward's final state, the per-head shares
-// of dB and dC (only when a group has several heads), the per-token q . B,
+// h_k, the adjoint states R_k, the forward's final state, the per-token q . B,
 // dL/dG and gy . x, the per-chunk shares of dA and dD, and c_i . B_j of every
 // chunk and group (T x T); with bf16 I/O then fp32 copies of x, dt, B, C, gy
 // and fp32 buffers for dx, ddt, dB, dC.  Each part is 256-byte aligned.
 struct BwdLayout {
-  size_t G, dst, states, R, fin, dBh, dCh, qB, dG, gyx, part, Kcb;
+  size_t G, dst, states, R, fin, qB, dG, gyx, part, Kcb;
   size_t cx, cdt, cB, cC, cgy, cdx, cddt, cdB, cdC;  // bf16 I/O only
   size_t total;
 };
@@ -661,15 +660,12 @@ BwdLayout bwd_layout(const Dims &d, ssd_dtype dtype) {
   BwdLayout w{};
   const size_t tok = round256(sizeof(float) * d.b * d.nh * d.nc * d.T);
   const size_t st = round256(sizeof(float) * d.b * d.nh * d.nc * d.P * d.S);
-  const size_t hs = d.hpg > 1 ? round256(sizeof(float) * d.b * d.L * d.nh * d.S) : 0;
   w.G = ssd::kWsHeader;
   w.dst = w.G + tok;
   w.states = w.dst + st;
   w.R = w.states + st;
   w.fin = w.R + st;
-  w.dBh = w.fin + round256(sizeof(float) * d.b * d.nh * d.P * d.S);
-  w.dCh = w.dBh + hs;
-  w.qB = w.dCh + hs;
+  w.qB = w.fin + round256(sizeof(float) * d.b * d.nh * d.P * d.S);
   w.dG = w.qB + tok;
   w.gyx = w.dG + tok;
   w.part = w.gyx + tok;
@@ -735,9 +731,6 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
         *dBf = bf ? f(w.cdB) : static_cast<float *>(dB),
         *dCf = bf ? f(w.cdC) : static_cast<float *>(dC);
   float *G = f(w.G), *dst = f(w.dst), *sts = f(w.states), *R = f(w.R), *fin = f(w.fin);
-  // with one head per group the per-head shares of dB and dC are dB and dC
-  float *dBh = d.hpg > 1 ? f(w.dBh) : dBf;
-  float *dCh = d.hpg > 1 ? f(w.dCh) : dCf;
   const int64_t n_x = d.b * d.L * d.nh * d.P, n_t = d.b * d.L * d.nh,
                 n_g = d.b * d.L * d.ng * d.S;
   int launched = 0;
@@ -775,7 +768,7 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
   });
   step([&] { return ssd::launch_bwd_cb(d, Bf, Cf, f(w.Kcb), err, st); });
   step([&] {
-    return ssd::launch_bwd_main(d, xf, dtf, Bf, Cf, D, gyf, G, sts, R, f(w.Kcb), dxf, dBh, dCh,
+    return ssd::launch_bwd_main(d, xf, dtf, Bf, Cf, D, gyf, G, sts, R, f(w.Kcb), dxf, dBf, dCf,
                                 f(w.qB), f(w.dG), f(w.gyx), err, st);
   });
   float2 *part = reinterpret_cast<float2 *>(ws + w.part);
@@ -784,7 +777,7 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
                                   err, st);
   });
   step([&] {
-    return ssd::launch_bwd_reduce(d, dBh, dCh, part, dBf, dCf, dA, dD, err, st);
+    return ssd::launch_bwd_reduce(d, part, dA, dD, err, st);
   });
   if (bf) {
     ssd::BwdConvert cv{};

@@ -127,8 +127,7 @@ cudaError_t launch_bwd_convert(const BwdConvert &a, cudaStream_t st);
 
 // Backward pass for fp32 I/O (bwd.cu), CUDA cores.  bwd_supported: P = 64,
 // S in {64, 128, 256}, T a multiple of 32 up to 256.  Shapes (fp32):
-// dR, R [b, nh, nc, P, S]; dBh, dCh [b, L, nh, S] (per-head shares of dB,
-// dC; may be dB and dC themselves when nh == ng); qB, dG, gyx [b, nh, nc*T];
+// dR, R [b, nh, nc, P, S]; dB, dC [b, L, ng, S]; qB, dG, gyx [b, nh, nc*T];
 // part float2 [b, nh, nc].
 bool bwd_supported(const Dims &d);
 // chunk jump terms in fp32, out[k] = sum_{t in k} w_t v_t m_t^T: the
@@ -140,20 +139,20 @@ cudaError_t launch_bwd_jump(const Dims &d, const float *v, const float *m, const
 // blocks on or below the diagonal
 cudaError_t launch_bwd_cb(const Dims &d, const float *B, const float *C, float *Kcb, int *err,
                           cudaStream_t st);
-// per token: dx, dt q (dBh), the head's dC (dCh), q . B, dL/dG, gy . x
+// per (row tile, chunk, group): dx of its heads, the group's dB and dC, and
+// per token and head q . B, dL/dG, gy . x
 cudaError_t launch_bwd_main(const Dims &d, const float *x, const float *dt, const float *B,
                             const float *C, const float *D, const float *gy, const float *G,
                             const float *states, const float *R, const float *Kcb, float *dx,
-                            float *dBh, float *dCh, float *qB, float *dG, float *gyx, int *err,
+                            float *dB, float *dC, float *qB, float *dG, float *gyx, int *err,
                             cudaStream_t st);
 // ddt, and the per-chunk shares of dA and dD
 cudaError_t launch_bwd_finish(const Dims &d, const float *dt, const float *A, const float *R,
                               const float *states, const float *final_state, const float *qB,
                               const float *dG, const float *gyx, float *ddt, float2 *part,
                               int *err, cudaStream_t st);
-// dB, dC (sums over a group's heads, skipped when nh == ng), dA, dD (nullable)
-cudaError_t launch_bwd_reduce(const Dims &d, const float *dBh, const float *dCh,
-                              const float2 *part, float *dB, float *dC, float *dA, float *dD,
-                              int *err, cudaStream_t st);
+// dA, dD (nullable): the per-chunk shares summed in a fixed order
+cudaError_t launch_bwd_reduce(const Dims &d, const float2 *part, float *dA, float *dD, int *err,
+                              cudaStream_t st);
 
 }  // namespace ssd
