@@ -385,7 +385,7 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
                 const float *__restrict__ R, const float *__restrict__ Kcb,
                 float *__restrict__ dx, float *__restrict__ dB, float *__restrict__ dC,
                 float *__restrict__ qB, float *__restrict__ dG, float *__restrict__ gyx, int *err,
-                int L, int nh, int hpg, int T, int nc, int nb) {
+                int L, int nh, int hpg, int T, int nc, int nb, int nslice) {
   using SM = MainSmem<kS, kG, kTok>;
   constexpr int NG = SM::NG, RT = SM::RT, NT = SM::NT, S4 = SM::S4, P4 = SM::P4;
   constexpr int KU = SM::KU, KL = SM::KL, WR = SM::WR, CB = SM::CB, KTF = 4 * SM::KT4;
@@ -400,7 +400,11 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
   float *ds = Gs + 256;
   const int ntile = T / RT, ng = nh / hpg;
   const int k = blockIdx.x / ntile, tau = blockIdx.x - k * ntile;
-  const int bg = blockIdx.y, b = bg / ng, g = bg - b * ng;
+  // blockIdx.y = (batch * group) * nslice + slice: the slice's heads are
+  // hps consecutive heads of the group; with several slices dB and dC are
+  // this slice's share, slice-major (summed by bwd_reduce_kernel)
+  const int sl = blockIdx.y % nslice, bg = blockIdx.y / nslice, b = bg / ng, g = bg - b * ng;
+  const int hps = hpg / nslice;
   const int tok0 = k * T, valid = min(T, L - tok0);
   const int tid = threadIdx.x, grp = tid / kG, lg = tid % kG, lane = tid & 31;
   // extents (elements per row width) of the buffers, for the debug-bounds checks
@@ -464,7 +468,7 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
         cp_async16(dst + r * (kUp ? KU : KL) + 4 * c4, Kc + (int64_t)i * T + j, true);
       }
     };
-    for (int hi = 0; hi < hpg; ++hi) {
+    for (int hi = sl * hps; hi < (sl + 1) * hps; ++hi) {
       const int h = g * hpg + hi;
       const int64_t rowh0 = tokrow0 * nh + h, bh = (int64_t)b * nh + h;
       __syncthreads();  // the previous head is done with Gs, ds, U2, Kt, Wt, Qp and Big
@@ -748,7 +752,7 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
       __syncthreads();
     }
     cp_async_wait<0>();
-    float *out = kUp ? dB : dC;
+    float *out = (kUp ? dB : dC) + (int64_t)sl * ext_g * kS;
 #pragma unroll
     for (int r = 0; r < kTok; ++r) {
       if (!live[r]) continue;
@@ -844,13 +848,28 @@ bwd_finish_kernel(const float *__restrict__ dt, const float *__restrict__ A,
 
 // ------------------------------------------------------------------ reduce
 
-// dA and dD per head, the sums of the per-chunk shares over batches and
-// chunks in a fixed order; one thread per head.
+// dB and dC, the sums of the head slices' shares (slice-major, nslice > 1)
+// in slice order, one thread per element; then (threads past those) dA and
+// dD per head, the sums of the per-chunk shares over batches and chunks in a
+// fixed order.
 __global__ void __launch_bounds__(kThreads)
-bwd_reduce_kernel(const float2 *__restrict__ part, float *__restrict__ dA, float *__restrict__ dD,
+bwd_reduce_kernel(const float *__restrict__ sB, const float *__restrict__ sC,
+                  float *__restrict__ dB, float *__restrict__ dC, int64_t n_bc, int nslice,
+                  const float2 *__restrict__ part, float *__restrict__ dA, float *__restrict__ dD,
                   int nh, int nc, int nb, int *err) {
-  const int h = blockIdx.x * kThreads + threadIdx.x;
-  if (h >= nh) return;
+  const int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  if (e < n_bc) {
+    float sb = 0.f, sc = 0.f;
+    for (int i = 0; i < nslice; ++i) {
+      sb += sB[i * n_bc + e];
+      sc += sC[i * n_bc + e];
+    }
+    dB[e] = sb;
+    dC[e] = sc;
+    return;
+  }
+  if (e - n_bc >= nh) return;
+  const int h = (int)(e - n_bc);
   float a = 0.f, d = 0.f;
   for (int b = 0; b < nb; ++b)
     for (int k = 0; k < nc; ++k) {
@@ -921,6 +940,22 @@ bool bwd_supported(const Dims &d) {
   return d.P == kP && (d.S == 64 || d.S == 128 || d.S == 256) && d.T % kTT == 0 && d.T <= 256;
 }
 
+int bwd_head_slices(const Dims &d) {
+  // 64-token row tiles, one CTA per SM, at dstate 256; 32-token tiles, two
+  // CTAs per SM, below: slice the heads of a group until the grid fills two
+  // waves of a 152-SM GB300 (the fewest slices that do; a divisor of the
+  // heads per group, at most 8)
+  const int64_t rt = d.S == 256 ? 64 : 32, per_sm = d.S == 256 ? 1 : 2;
+  const int64_t base = d.b * d.ng * d.nc * (d.T / rt), want = 2 * 152 * per_sm;
+  int best = 1;
+  for (int n = 1; n <= 8 && n <= d.hpg; ++n)
+    if (d.hpg % n == 0) {
+      best = n;
+      if (base * n >= want) break;
+    }
+  return best;
+}
+
 namespace {
 template <int kS>
 cudaError_t launch_jump(const Dims &d, const float *v, const float *m, const float *dt,
@@ -967,10 +1002,11 @@ cudaError_t launch_main(const Dims &d, const float *x, const float *dt, const fl
   cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<kS, kG, kTok>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(d.nc * (d.T / SM::RT)), (unsigned)(d.b * d.ng));
+  const int nslice = bwd_head_slices(d);
+  dim3 grid((unsigned)(d.nc * (d.T / SM::RT)), (unsigned)(d.b * d.ng * nslice));
   bwd_main_kernel<kS, kG, kTok><<<grid, kThreads, smem, st>>>(
       x, dt, B, C, D, gy, G, states, R, Kcb, dx, dB, dC, qB, dG, gyx, err, (int)d.L,
-      (int)d.nh, (int)d.hpg, (int)d.T, (int)d.nc, (int)d.b);
+      (int)d.nh, (int)d.hpg, (int)d.T, (int)d.nc, (int)d.b, nslice);
   return cudaGetLastError();
 }
 }  // namespace
@@ -1018,10 +1054,14 @@ cudaError_t launch_bwd_finish(const Dims &d, const float *dt, const float *A, co
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_reduce(const Dims &d, const float2 *part, float *dA, float *dD, int *err,
+cudaError_t launch_bwd_reduce(const Dims &d, const float *sB, const float *sC, float *dB,
+                              float *dC, const float2 *part, float *dA, float *dD, int *err,
                               cudaStream_t st) {
-  bwd_reduce_kernel<<<(unsigned)((d.nh + kThreads - 1) / kThreads), kThreads, 0, st>>>(
-      part, dA, dD, (int)d.nh, (int)d.nc, (int)d.b, err);
+  const int nslice = bwd_head_slices(d);
+  const int64_t n_bc = nslice > 1 ? d.b * d.L * d.ng * d.S : 0;
+  const int64_t n = n_bc + d.nh;
+  bwd_reduce_kernel<<<(unsigned)((n + kThreads - 1) / kThreads), kThreads, 0, st>>>(
+      sB, sC, dB, dC, n_bc, nslice, part, dA, dD, (int)d.nh, (int)d.nc, (int)d.b, err);
   return cudaGetLastError();
 }
 

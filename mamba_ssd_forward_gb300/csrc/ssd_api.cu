@@ -651,7 +651,7 @@ namespace {
 // chunk and group (T x T); with bf16 I/O then fp32 copies of x, dt, B, C, gy
 // and fp32 buffers for dx, ddt, dB, dC.  Each part is 256-byte aligned.
 struct BwdLayout {
-  size_t G, dst, states, R, fin, qB, dG, gyx, part, Kcb;
+  size_t G, dst, states, R, fin, qB, dG, gyx, part, Kcb, sB, sC;
   size_t cx, cdt, cB, cC, cgy, cdx, cddt, cdB, cdC;  // bf16 I/O only
   size_t total;
 };
@@ -670,7 +670,12 @@ BwdLayout bwd_layout(const Dims &d, ssd_dtype dtype) {
   w.gyx = w.dG + tok;
   w.part = w.gyx + tok;
   w.Kcb = w.part + round256(2 * sizeof(float) * d.b * d.nh * d.nc);
-  w.total = w.Kcb + round256(sizeof(float) * d.b * d.ng * d.nc * d.T * d.T);
+  w.sB = w.Kcb + round256(sizeof(float) * d.b * d.ng * d.nc * d.T * d.T);
+  // the head slices' shares of dB and dC, when a group's heads are split
+  const int ns = ssd::bwd_head_slices(d);
+  const size_t slc = ns > 1 ? round256(sizeof(float) * ns * d.b * d.L * d.ng * d.S) : 0;
+  w.sC = w.sB + slc;
+  w.total = w.sC + slc;
   if (dtype == SSD_BF16) {
     const size_t xs = round256(sizeof(float) * d.b * d.L * d.nh * d.P),
                  ts = round256(sizeof(float) * d.b * d.L * d.nh),
@@ -731,6 +736,7 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
         *dBf = bf ? f(w.cdB) : static_cast<float *>(dB),
         *dCf = bf ? f(w.cdC) : static_cast<float *>(dC);
   float *G = f(w.G), *dst = f(w.dst), *sts = f(w.states), *R = f(w.R), *fin = f(w.fin);
+  const bool sliced = ssd::bwd_head_slices(d) > 1;
   const int64_t n_x = d.b * d.L * d.nh * d.P, n_t = d.b * d.L * d.nh,
                 n_g = d.b * d.L * d.ng * d.S;
   int launched = 0;
@@ -768,8 +774,9 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
   });
   step([&] { return ssd::launch_bwd_cb(d, Bf, Cf, f(w.Kcb), err, st); });
   step([&] {
-    return ssd::launch_bwd_main(d, xf, dtf, Bf, Cf, D, gyf, G, sts, R, f(w.Kcb), dxf, dBf, dCf,
-                                f(w.qB), f(w.dG), f(w.gyx), err, st);
+    return ssd::launch_bwd_main(d, xf, dtf, Bf, Cf, D, gyf, G, sts, R, f(w.Kcb), dxf,
+                                sliced ? f(w.sB) : dBf, sliced ? f(w.sC) : dCf, f(w.qB),
+                                f(w.dG), f(w.gyx), err, st);
   });
   float2 *part = reinterpret_cast<float2 *>(ws + w.part);
   step([&] {
@@ -777,7 +784,7 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
                                   err, st);
   });
   step([&] {
-    return ssd::launch_bwd_reduce(d, part, dA, dD, err, st);
+    return ssd::launch_bwd_reduce(d, f(w.sB), f(w.sC), dBf, dCf, part, dA, dD, err, st);
   });
   if (bf) {
     ssd::BwdConvert cv{};

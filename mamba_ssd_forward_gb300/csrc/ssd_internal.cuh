@@ -151,8 +151,14 @@ cudaError_t launch_bwd_finish(const Dims &d, const float *dt, const float *A, co
                               const float *states, const float *final_state, const float *qB,
                               const float *dG, const float *gyx, float *ddt, float2 *part,
                               int *err, cudaStream_t st);
-// dA, dD (nullable): the per-chunk shares summed in a fixed order
-cudaError_t launch_bwd_reduce(const Dims &d, const float2 *part, float *dA, float *dD, int *err,
+// heads of a group per bwd_main CTA are hpg / bwd_head_slices(d); with more
+// than one slice bwd_main writes each slice's share of dB and dC (slice-major,
+// [nslice, b, L, ng, S]) for bwd_reduce to add up
+int bwd_head_slices(const Dims &d);
+// dB, dC from the slices' shares sB, sC (when there are several slices),
+// then dA, dD (nullable): every sum in a fixed order
+cudaError_t launch_bwd_reduce(const Dims &d, const float *sB, const float *sC, float *dB,
+                              float *dC, const float2 *part, float *dA, float *dD, int *err,
                               cudaStream_t st);
 
 }  // namespace ssd
