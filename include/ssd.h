@@ -1,5 +1,6 @@
 /*
- * ssd.h -- C ABI of the GB300 (sm_103a) Mamba-2 chunked SSD forward pass.
+ * ssd.h -- C ABI of the GB300 (sm_103a) Mamba-2 chunked SSD forward pass (and
+ * its backward, ssd_backward).
  *
  * Method: "Accelerating Mamba-2 with High-Performance Forward Pass Kernels in
  * NVIDIA CUDA Tile", section "Mamba-2 architecture".  Per batch b and head h,
