@@ -82,7 +82,10 @@ struct OutArgs32 {
 
 __device__ __forceinline__ float tf32_rn(float v) { return __uint_as_float(to_tf32(v)); }
 
-template <int kT>
+// kSplitC: dstate above 128, C split between tensor and shared memory (a
+// compile-time choice, so that the MMA warp's issue loop at dstate <= 128
+// carries no test of where C lies)
+template <int kT, bool kSplitC>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_B,
              const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_st,
@@ -117,8 +120,8 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
   const int valid = min(kT, L - tok0);
   if (t * 128 >= valid) return;  // the whole tile lies past the sequence (uniform)
   const int nS = S / 32;             // K atoms of S
-  const int nCt = min(nS, 4);        // atoms of C in tensor memory (S < 128 of it)
-  const int nCs = nS - nCt;          // atoms of C resident in shared memory (S > 128)
+  const int nCt = kSplitC ? 4 : nS;  // atoms of C in tensor memory (S < 128 of it)
+  const int nCs = kSplitC ? nS - 4 : 0;  // atoms of C resident in shared memory (S > 128)
   const int nHs = (nS + 1) / 2;      // state stages per head
   const int nJ = 4 * (t + 1);        // 32-token atoms of the in-chunk sum
   const int nXs = nJ / 2;            // x stages per head (64 tokens each)
@@ -192,7 +195,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       }
       __syncwarp();
     }
-    if (nCs > 0 && leader) {
+    if (kSplitC && leader) {
       ptx::mbar_arrive_expect_tx(&c2_full, nCs * kStage);
       for (int i = 0; i < nCs; ++i)
         ptx::tma_load_4d(Cres + i * kStage, &tm_C, (nCt + i) * 32, g, tok0 + t * 128, b, &c2_full);
@@ -256,7 +259,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = ptx::smem_desc(b0 + kk * 32, 16, 1024, ptx::kSw128);
-            if (sb < nCt) {
+            if (!kSplitC || sb < nCt) {
               ptx::mma_ts_tf32(tmem + 128 * th, tmem + kColC + sb * 32 + kk * 8, bd, idCB,
                                (sb | kk) ? 1u : 0u);
             } else {
@@ -321,7 +324,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
                   ptx::smem_desc(h0 + ai * kHAtom + kk * 32, 16, 1024, ptx::kSw128);
               const int sa = 2 * hh + ai;  // atom of S
               const uint32_t accf = (steep && (hh | ai | kk) == 0) ? 0u : 1u;
-              if (sa < nCt) {
+              if (!kSplitC || sa < nCt) {
                 ptx::mma_ts_tf32(tmem + acc_col(set), tmem + kColC + sa * 32 + kk * 8, hd, idY,
                                  accf);
               } else {
@@ -382,7 +385,7 @@ fwd_out_tf32(const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ C
       warp_arrive(&xrel[sl]);  // the values are in registers: the stage may go
       ptx::tmem_stu<16>(tmem + lane_base + kColC + sb * 32 + half * 16, r);
     }
-    if (nCs > 0) {
+    if (kSplitC) {
       // C's atoms past the first 128 of S stay in shared memory, rounded in
       // place
       ptx::mbar_wait(&c2_full, 0, a.err, 175);
@@ -691,7 +694,9 @@ cudaError_t launch_fwd_out_tf32(const Dims &d, const float *x, const float *B, c
       return cudaErrorInvalidValue;
   }
   const OutSmem32 m = out_smem32(d);
-  auto kernel = d.T == 256 ? fwd_out_tf32<256> : fwd_out_tf32<128>;
+  const bool split = d.S > 128;
+  auto kernel = d.T == 256 ? (split ? fwd_out_tf32<256, true> : fwd_out_tf32<256, false>)
+                           : (split ? fwd_out_tf32<128, true> : fwd_out_tf32<128, false>);
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, m.smem);
   if (e != cudaSuccess) return e;
