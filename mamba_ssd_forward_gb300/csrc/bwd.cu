@@ -1,4 +1,4 @@
-// Backward pass of the chunked SSD (fp32 I/O): the gradients of a loss L
+// Backward pass of the chunked SSD (fp32 arithmetic): the gradients of a loss L
 // through the forward recurrence of "Accelerating Mamba-2 with
 // High-Performance Forward Pass Kernels in NVIDIA CUDA Tile", section
 // "Mamba-2 architecture" (h_t = a_t h_{t-1} + dt_t x_t B_t^T, y_t = h_t c_t +
@@ -34,11 +34,15 @@
 //                     weights summed over the heads before one update;
 //   bwd_finish_kernel per (batch, head, chunk): the reverse cumsum for eta,
 //                     ddt, and the chunk's shares of dA and dD;
-//   bwd_reduce_kernel the sums over batches and chunks (dA, dD), in a fixed
-//                     order.
-// All in fp32 on the CUDA cores (the tensor-core version is the next step):
-// about 30 million multiply-adds per chunk and head at T = 256, P = 64,
-// S = 128.
+//   bwd_reduce_kernel dB, dC summed over head slices (when a group's heads
+//                     are split over CTAs), and the sums over batches and
+//                     chunks (dA, dD), in a fixed order;
+//   bwd_convert_kernel with bf16 I/O, the inputs to fp32 copies before and
+//                     the gradients back to bf16 after.
+// All in fp32 on the CUDA cores (TF32 tensor-core products would put dA off
+// by about 1 %; a 3xTF32 version is the next step): about 25 million
+// multiply-adds per chunk and head at T = 256, P = 64, S = 256 with the S-wide
+// products shared by a group of six heads.
 #include <algorithm>
 #include <type_traits>
 
