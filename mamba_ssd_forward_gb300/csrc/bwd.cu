@@ -625,6 +625,7 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
       for (int r = 0; r < kTok; ++r)
 #pragma unroll
         for (int i = 0; i < QP; ++i) tmp[r][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
       for (int c4 = 0; c4 < S4; ++c4) {
         float4 o[kTok];
 #pragma unroll
