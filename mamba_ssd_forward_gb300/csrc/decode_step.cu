@@ -13,6 +13,8 @@
 // each lane four consecutive state columns of every 128-wide slice of S,
 // with B and C in registers.  The row's dot product with C is a warp
 // reduction.
+#include <type_traits>
+
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -22,6 +24,11 @@ constexpr int kWarps = 8;
 constexpr int kMaxSlices = 8;  // S <= 1024
 constexpr int kRows = 4;       // rows per warp in flight
 constexpr int kSliceRows = kWarps * kRows;  // rows of P per CTA when sliced
+
+template <typename T>
+struct type_tag {
+  using type = T;
+};
 
 __device__ __forceinline__ void load4(const float *p, float (&v)[4]) {
   const float4 f = *reinterpret_cast<const float4 *>(p);
@@ -40,8 +47,11 @@ __device__ __forceinline__ void load4(const __nv_bfloat16 *p, float (&v)[4]) {
   v[3] = c.y;
 }
 
-template <typename IO, bool kSliced>
-__global__ void __launch_bounds__(kWarps * 32)
+// kNsl: 128-wide slices of S the kernel handles (1, 2, or up to kMaxSlices),
+// a compile-time bound so that B and C of small dstates take few registers
+// and four CTAs fit on an SM
+template <typename IO, bool kSliced, int kNsl>
+__global__ void __launch_bounds__(kWarps * 32, kNsl <= 2 ? 4 : 2)
 decode_step_kernel(const IO *__restrict__ x, const IO *__restrict__ dt,
                    const float *__restrict__ A, const IO *__restrict__ B,
                    const IO *__restrict__ C, const float *__restrict__ D,
@@ -60,9 +70,9 @@ decode_step_kernel(const IO *__restrict__ x, const IO *__restrict__ dt,
   const float Dh = D ? D[h] : 0.f;
   const IO *Brow = B + (bi * ng + g) * S;
   const IO *Crow = C + (bi * ng + g) * S;
-  float Bv[kMaxSlices][4], Cv[kMaxSlices][4];
+  float Bv[kNsl][4], Cv[kNsl][4];
 #pragma unroll
-  for (int k = 0; k < kMaxSlices; ++k) {
+  for (int k = 0; k < kNsl; ++k) {
     const int s0 = k * 128 + lane * 4;
     if (k < nsl && s0 < S && SSD_IN_BOUNDS(s0 + 4 <= S, err, 21)) {
       load4(Brow + s0, Bv[k]);
@@ -87,7 +97,7 @@ decode_step_kernel(const IO *__restrict__ x, const IO *__restrict__ dt,
       acc[r] = 0.f;
     }
 #pragma unroll
-    for (int k = 0; k < kMaxSlices; ++k) {
+    for (int k = 0; k < kNsl; ++k) {
       const int s0 = k * 128 + lane * 4;
       if (k >= nsl || s0 >= S || !SSD_IN_BOUNDS(s0 + 4 <= S, err, 22)) continue;
       float4 hv[kRows];
@@ -132,18 +142,33 @@ cudaError_t launch_decode_step(int64_t b, int64_t nh, int64_t P, int64_t S, int6
   const bool sliced = b * nh < 4 * (int64_t)sm_count();
   const dim3 grid((unsigned)(b * nh), sliced ? (unsigned)((P + kSliceRows - 1) / kSliceRows) : 1u);
   const int hpg = (int)(nh / ng);
+  const int nsl = (int)((S + 127) / 128);
+  auto launch = [&](auto io_c, auto sliced_c, auto nsl_c) {
+    using IO = typename decltype(io_c)::type;
+    decode_step_kernel<IO, decltype(sliced_c)::value, decltype(nsl_c)::value>
+        <<<grid, kWarps * 32, 0, st>>>(
+            static_cast<const IO *>(x), static_cast<const IO *>(dt), A,
+            static_cast<const IO *>(B), static_cast<const IO *>(C), D, state,
+            static_cast<IO *>(y), (int)nh, (int)P, (int)S, hpg, (int)ng, b * nh, err);
+  };
+  auto by_slices = [&](auto io_c, auto sliced_c) {
+    if (nsl == 1)
+      launch(io_c, sliced_c, std::integral_constant<int, 1>{});
+    else if (nsl == 2)
+      launch(io_c, sliced_c, std::integral_constant<int, 2>{});
+    else
+      launch(io_c, sliced_c, std::integral_constant<int, kMaxSlices>{});
+  };
+  auto by_sliced = [&](auto io_c) {
+    if (sliced)
+      by_slices(io_c, std::true_type{});
+    else
+      by_slices(io_c, std::false_type{});
+  };
   if (io == SSD_BF16)
-    (sliced ? decode_step_kernel<__nv_bfloat16, true> : decode_step_kernel<__nv_bfloat16, false>)
-        <<<grid, kWarps * 32, 0, st>>>(
-        static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(dt), A,
-        static_cast<const __nv_bfloat16 *>(B), static_cast<const __nv_bfloat16 *>(C), D, state,
-        static_cast<__nv_bfloat16 *>(y), (int)nh, (int)P, (int)S, hpg, (int)ng, b * nh, err);
+    by_sliced(type_tag<__nv_bfloat16>{});
   else
-    (sliced ? decode_step_kernel<float, true> : decode_step_kernel<float, false>)
-        <<<grid, kWarps * 32, 0, st>>>(
-        static_cast<const float *>(x), static_cast<const float *>(dt), A,
-        static_cast<const float *>(B), static_cast<const float *>(C), D, state,
-        static_cast<float *>(y), (int)nh, (int)P, (int)S, hpg, (int)ng, b * nh, err);
+    by_sliced(type_tag<float>{});
   return cudaGetLastError();
 }
 
