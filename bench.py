@@ -663,7 +663,8 @@ def run_decode(args, w):
 # x the 2070 MHz maximum SM clock (the ALU roofline of the backward kernels)
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 BWD_KERNELS = ["chunk_cumsum", "bwd_jump(x, B)", "state_passing", "bwd_jump(gy, C)",
-               "state_passing(reverse)", "bwd_cb", "bwd_main", "bwd_finish", "bwd_reduce"]
+               "state_passing(reverse)", "bwd_cb", "bwd_scale", "state GEMMs (dx, ysm)",
+               "bwd_main", "bwd_finish", "bwd_reduce", "state GEMMs (dB, dC)"]
 
 
 def backward_macs(w: W.Workload) -> dict:
@@ -671,19 +672,34 @@ def backward_macs(w: W.Workload) -> dict:
     causal triangle of each chunk counted once and C . B shared by a group's
     heads), split into the per-token kernel's share and the rest."""
     P, S, T = w.headdim, w.dstate, w.chunk
-    main = rest = 0
+    main = gemm = rest = 0
     for k in range(w.nchunks):
         v = min(T, w.seqlen - k * T)
         npair = v * (v + 1) // 2
         # per head: the scores gy_i . x_j and the P-wide masked products
-        # (ysm, dx); the four state terms of every token.  Per group: the
-        # S-wide masked products (dB, dC), whose weights add up over the
-        # group's heads before they meet B or C
-        main += w.batch * w.nheads * (npair * 3 * P + 4 * v * P * S)
+        # (ysm, dx).  Per group: the S-wide masked products (dB, dC), whose
+        # weights add up over the group's heads before they meet B or C
+        main += w.batch * w.nheads * npair * 3 * P
         main += w.batch * w.ngroups * npair * 2 * S
+        # the four state terms of every token (R B, h c, R^T x~, h^T g~y):
+        # two GEMM launches of two products each
+        gemm += w.batch * w.nheads * 4 * v * P * S
         rest += w.batch * w.ngroups * npair * S  # c_i . B_j, once per group (bwd_cb)
         rest += w.batch * w.nheads * (2 * v * P * S + P * S)  # jump terms, <R_k, h_k+1>
-    return {"bwd_main": main, "total": main + rest}
+    return {"bwd_main": main, "state_gemms": gemm, "total": main + gemm + rest}
+
+
+def state_gemm_bytes(w: W.Workload) -> int:
+    """HBM bytes the two state-term GEMM steps must move: the states R_k and
+    h_k twice (fp32), B and C once each way into dx~S, ysm~S, the scaled x and
+    gy read, and dB, dC read and written by the accumulating products."""
+    f = 4
+    states = 2 * w.batch * w.nchunks * w.nheads * w.headdim * w.dstate * f
+    bc = 2 * w.batch * w.seqlen * w.ngroups * w.dstate * f
+    xp = 2 * w.batch * w.seqlen * w.nheads * w.headdim * f
+    before = states + bc + xp          # read R, h, B, C; write dxS, ysmS
+    after = states + xp + 2 * bc       # read R, h, x~, g~y; read and write dB, dC
+    return before + after
 
 
 def time_oracle_backward(w: W.Workload, inp, gy, gfinal, target_s: float):
@@ -753,7 +769,9 @@ def run_backward(args, w):
     launches = 0
     for evs in ev:
         flush_w.zero_()
-        launches += step(evs)["n_launches"]
+        # every launch step runs at least one kernel of ours but the last
+        # GEMM step (dB, dC state terms), which launches cuBLAS only
+        launches += step(evs)["n_launches"] - 1
     torch.cuda.synchronize()
     sampler.mark_end()
     clocks = sampler.stop()
@@ -764,6 +782,9 @@ def run_backward(args, w):
     macs = backward_macs(wf)
     tf_main = 2 * macs["bwd_main"] / (per["bwd_main"] / 1e3) / 1e12
     tf_all = 2 * macs["total"] / (ms / 1e3) / 1e12
+    ms_gemm = per["state GEMMs (dx, ysm)"] + per["state GEMMs (dB, dC)"]
+    tf_gemm = 2 * macs["state_gemms"] / (ms_gemm / 1e3) / 1e12
+    gemm_bytes = state_gemm_bytes(wf)
     tokens = wf.batch * wf.seqlen
     cpu = None
     if not args.skip_cpu_baseline:
@@ -788,7 +809,12 @@ def run_backward(args, w):
                      "algorithmic_flops_per_launch": 2 * macs["bwd_main"], "traffic": None},
         "whole_pass": {"achieved_tflops": tf_all, "frac": tf_all / FP32_ALU_TFLOPS,
                        "algorithmic_flops": 2 * macs["total"]},
-        "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": clocks,
+        "state_gemms": {"achieved_tflops": tf_gemm, "ms": ms_gemm,
+                        "algorithmic_flops": 2 * macs["state_gemms"],
+                        "hbm_bytes": gemm_bytes, "hbm_frac": gemm_bytes / (ms_gemm / 1e3) / 1e9
+                        / hbm_peak()[0]},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches,
+        "library_gemm_calls": 4 * args.steps, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
     return 0

@@ -43,7 +43,10 @@
 // by about 1 %; a 3xTF32 version is the next step): about 25 million
 // multiply-adds per chunk and head at T = 256, P = 64, S = 256 with the S-wide
 // products shared by a group of six heads.
+#include <cublas_v2.h>
+
 #include <algorithm>
+#include <cstdint>
 #include <type_traits>
 
 #include "ssd_internal.cuh"
@@ -267,6 +270,82 @@ bwd_cb_kernel(const float *__restrict__ Bm, const float *__restrict__ Cm,
       dst[(int64_t)(I * 64 + ty + 16 * a) * T + J * 64 + tx + 16 * c] = acc[a][c];
 }
 
+// ------------------------------------------------------------ state terms
+
+// The state terms of the backward as GEMMs (fp32, on the tensor cores through
+// cuBLAS's bf16x9 emulation of fp32 products), per (batch, chunk, group)
+// with the group's heads side by side:
+//   dxS[t][(h, p)]  = sum_s B_t[s] R_h[p][s]        (dx += dt exp2(G_last - G_t) dxS)
+//   ysmS[t][(h, p)] = sum_s c_t[s] h_h[p][s]        (ysm += exp2(G_t) ysmS)
+//   dB_t[s] += sum_(h, p) X~_t[(h, p)] R_h[p][s],   X~ = dt exp2(G_last - G_t) x
+//   dC_t[s] += sum_(h, p) Gy~_t[(h, p)] h_h[p][s],  Gy~ = exp2(G_t) gy
+// with R and h stored chunk-major ([b, nc, nh, P, S]: a group's heads at one
+// chunk are one [hpg P][S] matrix).  bwd_scale_kernel writes X~ and Gy~, one
+// thread per four elements of [b, L, nh, P].
+__global__ void __launch_bounds__(kThreads)
+bwd_scale_kernel(const float *__restrict__ x, const float *__restrict__ gy,
+                 const float *__restrict__ dt, const float *__restrict__ G,
+                 float *__restrict__ xs, float *__restrict__ gys, int *err, int L, int nh,
+                 int T, int nc, int nb) {
+  constexpr int P4 = kP / 4;
+  const int64_t n4 = (int64_t)nb * L * nh * P4;
+  for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < n4;
+       e += (int64_t)gridDim.x * kThreads) {
+    const int64_t rowh = e / P4;  // (b * L + t) * nh + h
+    const int h = (int)(rowh % nh);
+    const int64_t tok = rowh / nh;
+    const int b = (int)(tok / L), t = (int)(tok - (int64_t)b * L);
+    const int k = t / T, tt = t - k * T, valid = min(T, L - k * T);
+    const float *Gc = G + (((int64_t)b * nh + h) * nc + k) * T;
+    const float Gt = Gc[tt], GL = Gc[valid - 1];
+    const float fx = dt[rowh] * exp2f(GL - Gt), fg = exp2f(Gt);
+    if (!SSD_IN_BOUNDS(e < n4, err, 220)) continue;
+    const float4 xv = reinterpret_cast<const float4 *>(x)[e];
+    const float4 gv = reinterpret_cast<const float4 *>(gy)[e];
+    reinterpret_cast<float4 *>(xs)[e] = make_float4(fx * xv.x, fx * xv.y, fx * xv.z, fx * xv.w);
+    reinterpret_cast<float4 *>(gys)[e] = make_float4(fg * gv.x, fg * gv.y, fg * gv.z, fg * gv.w);
+  }
+}
+
+// The GEMMs' pointer arrays, ptr[m][i] for matrix m of batch entry i: the
+// entries are (b, k, g) for the chunks of full length, then (b, g) for the
+// partial last chunk when there is one.
+enum { kPB, kPC, kPR, kPH, kPXs, kPGs, kPDx, kPYs, kPdB, kPdC, kNPtr };
+__global__ void __launch_bounds__(kThreads)
+bwd_gemm_ptrs_kernel(const float *B, const float *C, const float *R, const float *H,
+                     const float *xs, const float *gys, float *dxS, float *ysmS, float *dB,
+                     float *dC, void **ptr, int nbatch, int nfull, int L, int nh, int ng,
+                     int S, int T, int nc) {
+  const int i = blockIdx.x * kThreads + threadIdx.x;
+  if (i >= nbatch) return;
+  const int hpg = nh / ng;
+  int b, k, g;
+  const int ncf = L / T;  // chunks of full length per sequence
+  if (i < nfull) {
+    g = i % ng;
+    k = (i / ng) % ncf;
+    b = i / (ng * ncf);
+  } else {
+    const int j = i - nfull;
+    g = j % ng;
+    b = j / ng;
+    k = nc - 1;
+  }
+  const int64_t rowg = ((int64_t)b * L + (int64_t)k * T) * ng + g;    // row of B, C, dB, dC
+  const int64_t rowh = ((int64_t)b * L + (int64_t)k * T) * nh + g * hpg;  // of x~, dxS, ...
+  const int64_t st = (((int64_t)b * nc + k) * nh + g * hpg) * kP * S;  // of R, h
+  ptr[kPB * nbatch + i] = (void *)(B + rowg * S);
+  ptr[kPC * nbatch + i] = (void *)(C + rowg * S);
+  ptr[kPR * nbatch + i] = (void *)(R + st);
+  ptr[kPH * nbatch + i] = (void *)(H + st);
+  ptr[kPXs * nbatch + i] = (void *)(xs + rowh * kP);
+  ptr[kPGs * nbatch + i] = (void *)(gys + rowh * kP);
+  ptr[kPDx * nbatch + i] = (void *)(dxS + rowh * kP);
+  ptr[kPYs * nbatch + i] = (void *)(ysmS + rowh * kP);
+  ptr[kPdB * nbatch + i] = (void *)(dB + rowg * S);
+  ptr[kPdC * nbatch + i] = (void *)(dC + rowg * S);
+}
+
 // -------------------------------------------------------------- main kernel
 
 
@@ -331,17 +410,12 @@ __device__ __forceinline__ float group_scatter(float (&v)[kG], int lane, int *id
 // Shared-memory plan of bwd_main_kernel (float4 units unless noted):
 //   Wsum [RT][WR] floats  the S-side weights of the pass summed over the
 //                         group's heads (WR = 256 + 4)
-//   U2   [2][NT][P/4]     a head's P-wide column tiles (gy upper, x lower),
-//                         then its own rows O2 [RT][P/4] for its state term
+//   U2   [2][NT][P/4]     a head's P-wide column tiles (gy upper, x lower)
 //   Kt   [2] x KT4        the c . B block of the tile pair ([NT][RT + 4]
 //                         floats in the upper pass, [RT][NT + 4] in the lower)
 //   Wt   [RT][NT + 4]     floats: a head's P-side weights of one tile
 //   Qp   [RT][CB]         floats: the lanes' shares of q . B (upper pass)
-//   O1   [RT][S/4]        the row tile's B (upper) or C (lower) rows, up to
-//                         dstate 128 (read from global memory above)
-//   Big                   a head's state Ms [P][S/4] (float4 slots XOR-
-//                         swizzled by bits 2..4 of the row), then the S-wide
-//                         column tiles U1 [2][NT][S/4] of the group update
+//   Big  [2][NT][S/4]     the S-wide column tiles of the group update
 //   Gs, ds                floats: the head's G and dt of the chunk (256 each)
 // kG lanes share a token group, which owns kTok tokens: RT = (256 / kG) kTok.
 template <int kS, int kG, int kTok>
@@ -349,17 +423,14 @@ struct MainSmem {
   static constexpr int NG = kThreads / kG, RT = NG * kTok, NT = kTT, S4 = kS / 4, P4 = kP / 4;
   static constexpr int KU = RT + 4, KL = NT + 4, WR = 256 + 4, CB = kG / kTok;
   static constexpr int KT4 = (NT * KU > RT * KL ? NT * KU : RT * KL) / 4;
-  static constexpr bool kO1Smem = false;
-  static constexpr int BIG = kP * S4 > 2 * NT * S4 ? kP * S4 : 2 * NT * S4;
   static constexpr int Wsum = 0, U2 = Wsum + RT * WR / 4, Kt = U2 + 2 * NT * P4,
-                       Wt = Kt + 2 * KT4, Qp = Wt + RT * KL / 4, O1 = Qp + RT * CB / 4,
-                       Big = O1 + (kO1Smem ? RT * S4 : 0), end4 = Big + BIG;
+                       Wt = Kt + 2 * KT4, Qp = Wt + RT * KL / 4, Big = Qp + RT * CB / 4,
+                       end4 = Big + 2 * NT * S4;
   static constexpr size_t bytes = 16 * (size_t)end4 + 2 * 256 * sizeof(float);
   static constexpr int kCtas = bytes <= 113 * 1024 ? 2 : 1;  // CTAs per SM
   static_assert(RT % kTT == 0 && RT <= 2 * kTT, "row tiles of 32 or 64 tokens");
   static_assert(S4 % kG == 0 && P4 % kG == 0, "whole float4 slots per lane");
   static_assert(CB >= 1 && NT % CB == 0 && (RT * CB) % 4 == 0, "columns per reduce-scatter");
-  static_assert(RT <= 2 * NT, "a head's own rows fit the column tiles' space");
 };
 
 // One CTA per (row tile of RT tokens of a chunk, chunk, batch * group), 256
@@ -376,17 +447,17 @@ struct MainSmem {
 // scalars), while the S-side weights dt_t w (x . gy) or w (gy . x) are
 // added up over the heads in Wsum; the S-wide update then runs once per
 // group, B and C being shared by its heads, and writes dB or dC.  c_t . B_j
-// comes from bwd_cb_kernel.  Each head's state terms (R_k: dx += dt_t
-// exp2(G_last - G_t) R B_t, dB += dt_t exp2(G_last - G_t) R^T x_t; h_k: ysm
-// += exp2(G_t) h c_t, dC += exp2(G_t) h^T gy_t) read its state from shared
-// memory.
+// comes from bwd_cb_kernel, and the state terms from the GEMMs around this
+// kernel: dx += dt_t exp2(G_last - G_t) (R B_t) and ysm += exp2(G_t) (h c_t)
+// from dxS and ysmS computed before it; dB and dC get R^T x~ and h^T gy~
+// added after it.
 template <int kS, int kG, int kTok>
 __global__ void __launch_bounds__(kThreads, MainSmem<kS, kG, kTok>::kCtas)
 bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
                 const float *__restrict__ Bm, const float *__restrict__ Cm,
                 const float *__restrict__ D, const float *__restrict__ gy,
-                const float *__restrict__ G, const float *__restrict__ states,
-                const float *__restrict__ R, const float *__restrict__ Kcb,
+                const float *__restrict__ G, const float *__restrict__ dxS,
+                const float *__restrict__ ysmS, const float *__restrict__ Kcb,
                 float *__restrict__ dx, float *__restrict__ dB, float *__restrict__ dC,
                 float *__restrict__ qB, float *__restrict__ dG, float *__restrict__ gyx, int *err,
                 int L, int nh, int hpg, int T, int nc, int nb, int nslice) {
@@ -396,7 +467,7 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
   constexpr int QS = S4 / kG, QP = P4 / kG;
   extern __shared__ float4 sm4[];
   float *Wsum = reinterpret_cast<float *>(sm4 + SM::Wsum);
-  float4 *U2 = sm4 + SM::U2, *O1 = sm4 + SM::O1, *Big = sm4 + SM::Big;
+  float4 *U2 = sm4 + SM::U2, *Big = sm4 + SM::Big;
   float *Kt = reinterpret_cast<float *>(sm4 + SM::Kt);
   float *Wt = reinterpret_cast<float *>(sm4 + SM::Wt);
   float *Qp = reinterpret_cast<float *>(sm4 + SM::Qp);
@@ -443,17 +514,14 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
   // one pass: kUp = the upper one (dx, dB) or the lower one (ysm, dC)
   auto pass = [&](auto up_c) {
     constexpr bool kUp = decltype(up_c)::value;
-    const float *own_g = kUp ? Bm : Cm;   // O1 rows (the group's B or C)
     const float *own_h = kUp ? x : gy;    // a head's own rows (x or gy)
     const float *col_h = kUp ? gy : x;    // a head's P-wide column rows
     const float *col_g = kUp ? Cm : Bm;   // the S-wide column rows of the group update
-    const float *state = kUp ? R : states;
     const int ucount = (valid + NT - 1) / NT;
     const int u0 = kUp ? tau * RT / NT : 0;
     const int u1 = kUp ? ucount : min(ucount, (tau + 1) * RT / NT);
     __syncthreads();  // the previous pass is done with every buffer
     for (int e = tid; e < RT * WR; e += kThreads) Wsum[e] = 0.f;
-    if (SM::kO1Smem) stage(O1, own_g, rowg0, ng, S4, tau * RT, RT, ext_g);
     cp_async_commit();
     float4 accS[kTok][QS];
 #pragma unroll
@@ -596,89 +664,24 @@ bwd_main_kernel(const float *__restrict__ x, const float *__restrict__ dt,
         __syncthreads();  // tile u's buffers are refilled two iterations on
       }
       cp_async_wait<0>();
-      // the head's own rows of the tile (for its S-side state term) into
-      // U2's space, its state into Big: M = R_k (upper) or h_k (lower), float4
-      // slot c4 of row p at c4 ^ ((p >> 2) & 7)
-      float4 *O2 = U2;
-      stage(O2, own_h, rowh0, nh, P4, tau * RT, RT, ext_h);
-      cp_async_commit();
-      const int64_t st_row = (bh * nc + k) * kP * kS;
-      for (int e = tid; e < kP * S4; e += kThreads) {
-        const int p = e / S4, c4 = e - p * S4;
-        Big[p * S4 + (c4 ^ ((p >> 2) & 7))] =
-            *reinterpret_cast<const float4 *>(state + st_row + 4 * (int64_t)e);
-      }
-      cp_async_wait<0>();
-      __syncthreads();
+      // the state term of this head's tokens, formed by the GEMMs before
+      // this kernel: raw = R_k B_t (upper) or h_k c_t (lower), this lane's
+      // P slots; dx += dt_t exp2(G_last - G_t) raw, ysm += exp2(G_t) raw
       const float GL = Gs[valid - 1];
-      float fP[kTok], fS[kTok];
-#pragma unroll
-      for (int r = 0; r < kTok; ++r) {
-        const float f = live[r] ? (kUp ? exp2f(GL - Gt[r]) : exp2f(Gt[r])) : 0.f;
-        fS[r] = kUp ? dtt[r] * f : f;
-        fP[r] = fS[r];
-      }
-      // P side: tmp[p] = sum_s M[p][s] O1_t[s] over this lane's rows p = 4
-      // (kG i + lg) + e (R B_t upper, h c_t lower)
-      float4 tmp[kTok][QP];
-#pragma unroll
-      for (int r = 0; r < kTok; ++r)
-#pragma unroll
-        for (int i = 0; i < QP; ++i) tmp[r][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int c4 = 0; c4 < S4; ++c4) {
-        float4 o[kTok];
-#pragma unroll
-        for (int r = 0; r < kTok; ++r) {
-          if (SM::kO1Smem) {
-            o[r] = O1[(NG * r + grp) * S4 + c4];
-          } else {
-            const int64_t gi = (rowg0 + (int64_t)t[r] * ng) * kS + 4 * c4;
-            o[r] = live[r] && SSD_IN_BOUNDS(gi + 4 <= ext_g * kS, err, 207)
-                       ? __ldg(reinterpret_cast<const float4 *>(own_g + gi))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < QP; ++i) {
-          const int p0 = 4 * (kG * i + lg), sw = c4 ^ ((kG * i + lg) & 7);
-          const float4 m0 = Big[p0 * S4 + sw], m1 = Big[(p0 + 1) * S4 + sw],
-                       m2 = Big[(p0 + 2) * S4 + sw], m3 = Big[(p0 + 3) * S4 + sw];
-#pragma unroll
-          for (int r = 0; r < kTok; ++r) {
-            tmp[r][i].x = dot4(m0, o[r], tmp[r][i].x);
-            tmp[r][i].y = dot4(m1, o[r], tmp[r][i].y);
-            tmp[r][i].z = dot4(m2, o[r], tmp[r][i].z);
-            tmp[r][i].w = dot4(m3, o[r], tmp[r][i].w);
-          }
-        }
-      }
+      const float *stP = kUp ? dxS : ysmS;
       float qst[kTok];  // x_t . (R B_t), this lane's slots (upper)
 #pragma unroll
       for (int r = 0; r < kTok; ++r) {
+        const float f = live[r] ? (kUp ? dtt[r] * exp2f(GL - Gt[r]) : exp2f(Gt[r])) : 0.f;
         qst[r] = 0.f;
 #pragma unroll
         for (int i = 0; i < QP; ++i) {
-          if (kUp) qst[r] = dot4(rP[r][i], tmp[r][i], qst[r]);
-          axpy4(fP[r], tmp[r][i], accP[r][i]);
-        }
-      }
-      // S side: accS[s] += fS sum_p M[p][s] O2_t[p] over this lane's columns
-      // (slot kG i + lg): dt_t exp2(G_last - G_t) R^T x_t (upper) or
-      // exp2(G_t) h^T gy_t (lower), summed over the group's heads
-      for (int p4 = 0; p4 < P4; ++p4) {
-        float4 o[kTok];
-#pragma unroll
-        for (int r = 0; r < kTok; ++r) o[r] = O2[(NG * r + grp) * P4 + p4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int p = 4 * p4 + e;
-#pragma unroll
-          for (int i = 0; i < QS; ++i) {
-            const float4 m = Big[p * S4 + ((kG * i + lg) ^ (p4 & 7))];
-#pragma unroll
-            for (int r = 0; r < kTok; ++r) axpy4(fS[r] * comp(o[r], e), m, accS[r][i]);
-          }
+          const int64_t si = (rowh0 + (int64_t)t[r] * nh) * kP + 4 * (kG * i + lg);
+          const float4 raw = live[r] && SSD_IN_BOUNDS(si + 4 <= ext_h * kP, err, 207)
+                                 ? *reinterpret_cast<const float4 *>(stP + si)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (kUp) qst[r] = dot4(rP[r][i], raw, qst[r]);
+          axpy4(f, raw, accP[r][i]);
         }
       }
       // the head's per-token outputs
@@ -797,8 +800,9 @@ bwd_finish_kernel(const float *__restrict__ dt, const float *__restrict__ A,
                      err, 202))
     return;
   // <R_k, h_{k+1}> over P x S
-  const float *Rk = R + ((int64_t)bh * nc + k) * P * S;
-  const float *hn = k + 1 < nc ? states + ((int64_t)bh * nc + k + 1) * P * S
+  // R and the states are chunk-major, [b, nc, nh, P, S]
+  const float *Rk = R + (((int64_t)b * nc + k) * nh + h) * P * S;
+  const float *hn = k + 1 < nc ? states + (((int64_t)b * nc + k + 1) * nh + h) * P * S
                                : final_state + (int64_t)bh * P * S;
   float s = 0.f;
   for (int e = tid; e < P * S; e += kThreads) s = fmaf(Rk[e], hn[e], s);
@@ -999,7 +1003,7 @@ cudaError_t launch_cb(const Dims &d, const float *B, const float *C, float *Kcb,
 template <int kS, int kG, int kTok>
 cudaError_t launch_main(const Dims &d, const float *x, const float *dt, const float *B,
                         const float *C, const float *D, const float *gy, const float *G,
-                        const float *states, const float *R, const float *Kcb, float *dx,
+                        const float *dxS, const float *ysmS, const float *Kcb, float *dx,
                         float *dB, float *dC, float *qB, float *dG, float *gyx, int *err,
                         cudaStream_t st) {
   using SM = MainSmem<kS, kG, kTok>;
@@ -1010,7 +1014,7 @@ cudaError_t launch_main(const Dims &d, const float *x, const float *dt, const fl
   const int nslice = bwd_head_slices(d);
   dim3 grid((unsigned)(d.nc * (d.T / SM::RT)), (unsigned)(d.b * d.ng * nslice));
   bwd_main_kernel<kS, kG, kTok><<<grid, kThreads, smem, st>>>(
-      x, dt, B, C, D, gy, G, states, R, Kcb, dx, dB, dC, qB, dG, gyx, err, (int)d.L,
+      x, dt, B, C, D, gy, G, dxS, ysmS, Kcb, dx, dB, dC, qB, dG, gyx, err, (int)d.L,
       (int)d.nh, (int)d.hpg, (int)d.T, (int)d.nc, (int)d.b, nslice);
   return cudaGetLastError();
 }
@@ -1027,7 +1031,7 @@ cudaError_t launch_bwd_cb(const Dims &d, const float *B, const float *C, float *
 
 cudaError_t launch_bwd_main(const Dims &d, const float *x, const float *dt, const float *B,
                             const float *C, const float *D, const float *gy, const float *G,
-                            const float *states, const float *R, const float *Kcb, float *dx,
+                            const float *dxS, const float *ysmS, const float *Kcb, float *dx,
                             float *dB, float *dC, float *qB, float *dG, float *gyx, int *err,
                             cudaStream_t st) {
   // 16-lane token groups: four tokens (64-token row tiles, one CTA per SM)
@@ -1037,15 +1041,117 @@ cudaError_t launch_bwd_main(const Dims &d, const float *x, const float *dt, cons
   // and one CTA
   switch (d.S) {
     case 64:
-      return launch_main<64, 16, 2>(d, x, dt, B, C, D, gy, G, states, R, Kcb, dx, dB, dC, qB,
+      return launch_main<64, 16, 2>(d, x, dt, B, C, D, gy, G, dxS, ysmS, Kcb, dx, dB, dC, qB,
                                     dG, gyx, err, st);
     case 128:
-      return launch_main<128, 16, 2>(d, x, dt, B, C, D, gy, G, states, R, Kcb, dx, dB, dC, qB,
+      return launch_main<128, 16, 2>(d, x, dt, B, C, D, gy, G, dxS, ysmS, Kcb, dx, dB, dC, qB,
                                      dG, gyx, err, st);
     default:
-      return launch_main<256, 16, 4>(d, x, dt, B, C, D, gy, G, states, R, Kcb, dx, dB, dC, qB,
+      return launch_main<256, 16, 4>(d, x, dt, B, C, D, gy, G, dxS, ysmS, Kcb, dx, dB, dC, qB,
                                      dG, gyx, err, st);
   }
+}
+
+namespace {
+// One cuBLAS handle per device and host thread, created on the first
+// backward call of that thread on that device (the call's one-time set-up;
+// later calls allocate nothing and can be captured in a CUDA graph).  The
+// handle is bound to the caller's stream and to a slice of the caller's
+// workspace at every call.
+cublasHandle_t bwd_cublas(int *fail) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *fail = 1;
+    return nullptr;
+  }
+  thread_local cublasHandle_t handles[64] = {};
+  if (!handles[dev] && cublasCreate(&handles[dev]) != CUBLAS_STATUS_SUCCESS) {
+    handles[dev] = nullptr;
+    *fail = 1;
+  }
+  return handles[dev];
+}
+}  // namespace
+
+size_t bwd_gemm_ptr_bytes(const Dims &d) {
+  const int64_t ncf = d.L / d.T, part = d.L % d.T ? 1 : 0;
+  const int64_t nbatch = d.b * d.ng * (ncf + part);
+  return sizeof(void *) * (size_t)(kNPtr * nbatch);
+}
+
+cudaError_t launch_bwd_scale(const Dims &d, const float *x, const float *gy, const float *dt,
+                             const float *G, float *xs, float *gys, int *err, cudaStream_t st) {
+  const int64_t n4 = d.b * d.L * d.nh * (kP / 4);
+  const int blocks = (int)std::max<int64_t>(
+      1, std::min<int64_t>((n4 + kThreads - 1) / kThreads, 8 * (int64_t)sm_count()));
+  bwd_scale_kernel<<<blocks, kThreads, 0, st>>>(x, gy, dt, G, xs, gys, err, (int)d.L, (int)d.nh,
+                                                (int)d.T, (int)d.nc, (int)d.b);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_state_gemms(const Dims &d, bool after, const float *B, const float *C,
+                                   const float *R, const float *H, const float *xs,
+                                   const float *gys, float *dxS, float *ysmS, float *dB,
+                                   float *dC, void **ptrs, void *cublas_ws, size_t ws_bytes,
+                                   cudaStream_t st) {
+  const int ncf = (int)(d.L / d.T), part = d.L % d.T ? 1 : 0;
+  const int nfull = (int)(d.b * d.ng * ncf), npart = (int)(d.b * d.ng * part);
+  const int nbatch = nfull + npart;
+  if (!after) {
+    // the pointer arrays (for both halves; the second reuses them)
+    bwd_gemm_ptrs_kernel<<<(nbatch + kThreads - 1) / kThreads, kThreads, 0, st>>>(
+        B, C, R, H, xs, gys, dxS, ysmS, dB, dC, ptrs, nbatch, nfull, (int)d.L, (int)d.nh,
+        (int)d.ng, (int)d.S, (int)d.T, (int)d.nc);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // cuBLAS's emulated-fp32 kernels want a workspace aligned beyond 256
+  // bytes (with 256 some small batches fail to launch): start it on a 4 KiB
+  // boundary inside the slice given
+  const uintptr_t wa = ((uintptr_t)cublas_ws + 4095) & ~(uintptr_t)4095;
+  if (ws_bytes < (wa - (uintptr_t)cublas_ws) + (1u << 20)) return cudaErrorInvalidValue;
+  ws_bytes -= wa - (uintptr_t)cublas_ws;
+  int fail = 0;
+  cublasHandle_t h = bwd_cublas(&fail);
+  if (fail || cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS ||
+      cublasSetWorkspace(h, reinterpret_cast<void *>(wa), ws_bytes) != CUBLAS_STATUS_SUCCESS)
+    return cudaErrorUnknown;
+  const float one = 1.f, zero = 0.f;
+  const int hp = (int)(d.hpg * d.P), S = (int)d.S;
+  const int ldg = (int)(d.ng * d.S), ldh = (int)(d.nh * d.P);
+  auto arr = [&](int m, int off) { return reinterpret_cast<void **>(ptrs + m * nbatch + off); };
+  // each batch segment: the full chunks (T rows), then the partial last chunk
+  for (int seg = 0; seg < 2; ++seg) {
+    const int off = seg ? nfull : 0, cnt = seg ? npart : nfull;
+    const int rows = seg ? (int)(d.L - (int64_t)ncf * d.T) : (int)d.T;
+    if (cnt == 0) continue;
+    cublasStatus_t cs;
+    if (!after) {
+      // column-major: dxS^T [(h,p)][t] = R [(h,p)][s] (op T of S x hp) . B^T [s][t]
+      cs = cublasGemmBatchedEx(h, CUBLAS_OP_T, CUBLAS_OP_N, hp, rows, S, &one, arr(kPR, off),
+                               CUDA_R_32F, S, arr(kPB, off), CUDA_R_32F, ldg, &zero,
+                               arr(kPDx, off), CUDA_R_32F, ldh, cnt,
+                               CUBLAS_COMPUTE_32F_EMULATED_16BFX9, CUBLAS_GEMM_DEFAULT);
+      if (cs == CUBLAS_STATUS_SUCCESS)
+        cs = cublasGemmBatchedEx(h, CUBLAS_OP_T, CUBLAS_OP_N, hp, rows, S, &one, arr(kPH, off),
+                                 CUDA_R_32F, S, arr(kPC, off), CUDA_R_32F, ldg, &zero,
+                                 arr(kPYs, off), CUDA_R_32F, ldh, cnt,
+                                 CUBLAS_COMPUTE_32F_EMULATED_16BFX9, CUBLAS_GEMM_DEFAULT);
+    } else {
+      // column-major: dB^T [s][t] += R^T [s][(h,p)] . x~^T [(h,p)][t]
+      cs = cublasGemmBatchedEx(h, CUBLAS_OP_N, CUBLAS_OP_N, S, rows, hp, &one, arr(kPR, off),
+                               CUDA_R_32F, S, arr(kPXs, off), CUDA_R_32F, ldh, &one,
+                               arr(kPdB, off), CUDA_R_32F, ldg, cnt,
+                               CUBLAS_COMPUTE_32F_EMULATED_16BFX9, CUBLAS_GEMM_DEFAULT);
+      if (cs == CUBLAS_STATUS_SUCCESS)
+        cs = cublasGemmBatchedEx(h, CUBLAS_OP_N, CUBLAS_OP_N, S, rows, hp, &one, arr(kPH, off),
+                                 CUDA_R_32F, S, arr(kPGs, off), CUDA_R_32F, ldh, &one,
+                                 arr(kPdC, off), CUDA_R_32F, ldg, cnt,
+                                 CUBLAS_COMPUTE_32F_EMULATED_16BFX9, CUBLAS_GEMM_DEFAULT);
+    }
+    if (cs != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_finish(const Dims &d, const float *dt, const float *A, const float *R,

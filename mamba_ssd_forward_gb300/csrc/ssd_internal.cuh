@@ -100,7 +100,8 @@ cudaError_t launch_chunk_state(const Dims &d, ssd_dtype io, const void *x,
 cudaError_t launch_state_passing(const Dims &d, const float *dstates,
                                  const float *G, const float *h0,
                                  float *states, float *final_state, int *err,
-                                 cudaStream_t st, bool tf32_out = false, bool reverse = false);
+                                 cudaStream_t st, bool tf32_out = false, bool reverse = false,
+                                 bool chunk_major = false);
 cudaError_t launch_chunk_scan(const Dims &d, ssd_dtype io, const void *x,
                               const void *B, const void *C, const void *dt,
                               const float *G, const float *states,
@@ -139,11 +140,26 @@ cudaError_t launch_bwd_jump(const Dims &d, const float *v, const float *m, const
 // blocks on or below the diagonal
 cudaError_t launch_bwd_cb(const Dims &d, const float *B, const float *C, float *Kcb, int *err,
                           cudaStream_t st);
-// per (row tile, chunk, group): dx of its heads, the group's dB and dC, and
-// per token and head q . B, dL/dG, gy . x
+// the state terms' GEMMs (cuBLAS, fp32 emulated on the tensor cores; R and
+// H = the start states chunk-major [b, nc, nh, P, S]): before bwd_main
+// (after = false) dxS = B R^T and ysmS = C H^T per (batch, chunk, group), in
+// the layout of x; after it (after = true) dB += x~ R and dC += gy~ H.  ptrs:
+// bwd_gemm_ptr_bytes(d) of workspace for the batched GEMMs' pointer arrays,
+// filled by the first call; cublas_ws: the cuBLAS workspace.
+size_t bwd_gemm_ptr_bytes(const Dims &d);
+cudaError_t launch_bwd_state_gemms(const Dims &d, bool after, const float *B, const float *C,
+                                   const float *R, const float *H, const float *xs,
+                                   const float *gys, float *dxS, float *ysmS, float *dB,
+                                   float *dC, void **ptrs, void *cublas_ws, size_t ws_bytes,
+                                   cudaStream_t st);
+// x~ = dt exp2(G_last - G_t) x and gy~ = exp2(G_t) gy, in the layout of x
+cudaError_t launch_bwd_scale(const Dims &d, const float *x, const float *gy, const float *dt,
+                             const float *G, float *xs, float *gys, int *err, cudaStream_t st);
+// per (row tile, chunk, group): dx of its heads, the group's dB and dC
+// in-chunk parts, and per token and head q . B, dL/dG, gy . x
 cudaError_t launch_bwd_main(const Dims &d, const float *x, const float *dt, const float *B,
                             const float *C, const float *D, const float *gy, const float *G,
-                            const float *states, const float *R, const float *Kcb, float *dx,
+                            const float *dxS, const float *ysmS, const float *Kcb, float *dx,
                             float *dB, float *dC, float *qB, float *dG, float *gyx, int *err,
                             cudaStream_t st);
 // ddt, and the per-chunk shares of dA and dD

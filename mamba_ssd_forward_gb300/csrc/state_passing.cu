@@ -21,6 +21,8 @@
 // the first: from h0 = dL/dfinal_state it stores R_k = dL/dh_{k+1} for every
 // chunk and leaves R_{-1} = dL/dh0 in final_state, R_{k-1} = exp2(G_last,k)
 // R_k + dstates[k] (dstates holding the adjoint's jump terms).
+// With chunk_major the stored states are laid out [b, nc, nh, P, S], so that
+// the heads of a group at one chunk form one matrix (the backward's GEMMs).
 #include "tc_common.cuh"
 
 namespace ssd {
@@ -34,7 +36,7 @@ state_passing_kernel(const float4 *__restrict__ dstates,
                      const float *__restrict__ G, const float4 *__restrict__ h0,
                      float4 *__restrict__ states, float4 *__restrict__ final_state,
                      int64_t ps4, int64_t nc, int64_t T, int64_t nbh, int tf32_out,
-                     int reverse, int *err) {
+                     int reverse, int64_t cm_nh, int *err) {
   __shared__ float2 gsm[256];  // per chunk: decay, stored-state scale
   // every index below lies in [0, nbh nc ps4) (states, dstates), [0, nbh
   // ps4) (h0, final_state) or [0, nbh nc T) (G) when bh < nbh and e < ps4; a
@@ -52,7 +54,12 @@ state_passing_kernel(const float4 *__restrict__ dstates,
   float4 h = h0 ? h0[bh * ps4 + e] : make_float4(0.f, 0.f, 0.f, 0.f);
   const float *Gbh = G + bh * nc * T;
   const float4 *dsrc = dstates + bh * nc * ps4 + e;
-  float4 *sdst = states + bh * nc * ps4 + e;
+  // stored state of chunk k: [b, nh, nc, P, S], or chunk-major [b, nc, nh,
+  // P, S] when cm_nh (= nh) is set
+  auto dst_row = [&](int64_t k) {
+    return cm_nh ? ((bh / cm_nh * nc + k) * cm_nh + bh % cm_nh) * ps4 : (bh * nc + k) * ps4;
+  };
+  float4 *sdst = states + e;
   // the chunk visited at step k: k itself, or nc - 1 - k walking backwards
   auto ck = [&](int64_t k) { return reverse ? nc - 1 - k : k; };
   float4 cur[kDepth], nxt[kDepth];
@@ -84,7 +91,7 @@ state_passing_kernel(const float4 *__restrict__ dstates,
       if (k0 + i < nc) {
         const float2 g = gsm[(k0 + i) & 255];
         if (live) {
-          sdst[ck(k0 + i) * ps4] =
+          sdst[dst_row(ck(k0 + i))] =
               tf32_out ? make_float4(__uint_as_float(to_tf32(g.y * h.x)),
                                      __uint_as_float(to_tf32(g.y * h.y)),
                                      __uint_as_float(to_tf32(g.y * h.z)),
@@ -107,7 +114,8 @@ state_passing_kernel(const float4 *__restrict__ dstates,
 cudaError_t launch_state_passing(const Dims &d, const float *dstates,
                                  const float *G, const float *h0,
                                  float *states, float *final_state, int *err,
-                                 cudaStream_t st, bool tf32_out, bool reverse) {
+                                 cudaStream_t st, bool tf32_out, bool reverse,
+                                 bool chunk_major) {
   const int64_t ps4 = d.P * d.S / 4;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((ps4 + kThreads - 1) / kThreads), (unsigned)(d.b * d.nh));
@@ -122,7 +130,8 @@ cudaError_t launch_state_passing(const Dims &d, const float *dstates,
                             G, reinterpret_cast<const float4 *>(h0),
                             reinterpret_cast<float4 *>(states),
                             reinterpret_cast<float4 *>(final_state), ps4, d.nc, d.T,
-                            d.b * d.nh, tf32_out ? 1 : 0, reverse ? 1 : 0, err);
+                            d.b * d.nh, tf32_out ? 1 : 0, reverse ? 1 : 0,
+                            chunk_major ? d.nh : (int64_t)0, err);
 }
 
 }  // namespace ssd
