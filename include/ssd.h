@@ -416,11 +416,11 @@ SSD_API size_t ssd_backward_workspace_size(const ssd_dims *dims, ssd_dtype dtype
  * `workspace` (>= ssd_backward_workspace_size bytes, 256-byte aligned, its
  * first SSD_WS_HEADER_BYTES zeroed before its first use).
  * P = 64, S in {64, 128, 256}.  Every product of the backward, and of the
- * forward states it recomputes, runs in fp32: on the CUDA cores, and the
- * four state-term GEMMs per chunk and group through cuBLAS with its fp32
- * emulation on the tensor cores (CUBLAS_COMPUTE_32F_EMULATED_16BFX9).  The
- * first call on a device and host thread creates that thread's cuBLAS
- * handle (a one-time set-up, like ssd_forward's).  With
+ * forward states it recomputes, runs in fp32 or near it: the in-chunk
+ * products on the CUDA cores in fp32, the GEMM-shaped ones (the chunks'
+ * jump terms and the state terms of every token) on the tensor cores with
+ * each fp32 operand split into two TF32 parts (three products, about 2^-21
+ * relative error each).  With
  * SSD_BF16, x, dt, B, C, gy and dx, ddt, dB, dC are bf16 (converted to and
  * from fp32 copies in the workspace, one launch each way); dA, dD, dh0, A,
  * D, h0 and gfinal are fp32 with either dtype.  dB, dC,
@@ -436,13 +436,12 @@ SSD_API ssd_status ssd_backward(const ssd_dims *dims, ssd_dtype dtype, const voi
 /* ssd_backward recording CUDA events around its launches, as
  * ssd_forward_profiled does: events[0] before the first launch and
  * events[i] after launch i (i < n_events), *n_launches (may be NULL) = the
- * number of launch steps, 12: the cumsum, the forward jump terms, the state
- * pass, the adjoint's jump terms, the backward state pass, c_i . B_j per chunk
- * and group, the scaled inputs of the state GEMMs, the GEMMs for the dx and
- * ysm state terms (a pointer-array kernel and two cuBLAS GEMMs), the
- * per-token kernel, the per-chunk finish, the reduction and the GEMMs for
- * the dB and dC state terms (14 with SSD_BF16: the input conversion first,
- * the output conversion last). */
+ * number of launches, 12: the cumsum, the scaled inputs x~ and gy~, the
+ * forward jump terms, the state pass, the adjoint's jump terms, the
+ * backward state pass, c_i . B_j per chunk and group, the dx and ysm state
+ * terms, the per-token kernel, the per-chunk finish, the reduction and the
+ * dB and dC state terms (14 with SSD_BF16: the input conversion first, the
+ * output conversion last). */
 SSD_API ssd_status ssd_backward_profiled(const ssd_dims *dims, ssd_dtype dtype, const void *x,
                                          const void *dt, const float *A, const void *B,
                                          const void *C, const float *D, const float *h0,

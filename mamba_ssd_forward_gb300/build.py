@@ -83,7 +83,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     fd, tmp = tempfile.mkstemp(suffix=".so", dir=PKG)
     os.close(fd)
     try:
-        r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-lcublas"],
+        r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"],
                            capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

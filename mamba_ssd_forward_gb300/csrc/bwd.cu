@@ -20,14 +20,17 @@
 //
 // (dB and dC sum over the heads of a group.)  The forward's cumsum kernel
 // gives G; then:
-//   bwd_jump_kernel   the forward's chunk jump terms sum_j exp2(G_last - G_j)
-//                     dt_j x_j B_j^T in fp32 (the forward's own kernels take
-//                     TF32 products, whose rounding the sums through
-//                     <R_k, h_{k+1}> into dA would carry at about 3e-3);
+//   bwd_scale_kernel  x~ = dt_t exp2(G_last - G_t) x_t, gy~ = exp2(G_t) gy_t;
+//   bwd_state_gemm    (bwd_gemm.cu, split-TF32 tensor-core GEMMs) the
+//                     forward's chunk jump terms sum_j x~_j B_j^T (the
+//                     forward's own kernels take plain TF32 products, whose
+//                     rounding the sums through <R_k, h_{k+1}> into dA would
+//                     carry at about 3e-3);
 //   state_passing     forwards over the chunks for h_k and the final state;
-//   bwd_jump_kernel   the adjoint's chunk jump terms sum_s exp2(G_s) gy_s c_s^T;
+//   bwd_state_gemm    the adjoint's chunk jump terms sum_s gy~_s c_s^T;
 //   state_passing     backwards over the chunks for R_k and dh0;
 //   bwd_cb_kernel     c_i . B_j of every chunk and group;
+//   bwd_state_gemm    the state terms R_k B_t and h_k c_t per token and head;
 //   bwd_main_kernel   per (row tile, chunk, batch * group), walking the
 //                     group's heads: dx of each head and per token q . B,
 //                     dL/dG, gy . x, and the group's dB and dC, the S-side
@@ -37,13 +40,12 @@
 //   bwd_reduce_kernel dB, dC summed over head slices (when a group's heads
 //                     are split over CTAs), and the sums over batches and
 //                     chunks (dA, dD), in a fixed order;
+//   bwd_state_gemm    dB += x~ R_k, dC += gy~ h_k (summed over the group's heads);
 //   bwd_convert_kernel with bf16 I/O, the inputs to fp32 copies before and
 //                     the gradients back to bf16 after.
-// All in fp32 on the CUDA cores (TF32 tensor-core products would put dA off
-// by about 1 %; a 3xTF32 version is the next step): about 25 million
-// multiply-adds per chunk and head at T = 256, P = 64, S = 256 with the S-wide
-// products shared by a group of six heads.
-#include <cublas_v2.h>
+// The kernels of this file run in fp32 on the CUDA cores (plain TF32
+// tensor-core products would put dA off by about 1 %), the state terms'
+// GEMMs in split TF32 on the tensor cores.
 
 #include <algorithm>
 #include <cstdint>
@@ -87,111 +89,6 @@ __device__ __forceinline__ void axpy4(float a, const float4 &v, float4 &acc) {
 }
 __device__ __forceinline__ float comp(const float4 &v, int e) {
   return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
-}
-
-// ---------------------------------------------------------------- jump terms
-
-// out[b, h, k][p][s] = sum_{t in chunk k} w_t v_t[p] m_t[s], v per head
-// ([b, L, nh, P]) and m per group ([b, L, ng, S]): the adjoint's jump terms
-// (v = gy, m = C, w_t = exp2(G_t); dt null) or the forward's (v = x, m = B,
-// w_t = exp2(G_last - G_t) dt_t).  One CTA per (chunk, batch * head), 256
-// threads as a 16 x 16 grid, thread (py, sx) owning rows p = 4 py .. +3 and
-// the float4 columns s = 4 sx + 64 q of the [P][S] output; 32-token tiles of
-// v and m double-buffered through cp.async.  Shared memory (float4 units):
-// v tiles [2][32][P/4], m tiles [2][32][S/4], then the chunk's w (256).
-template <int kS>
-struct JumpSmem {
-  static constexpr int P4 = kP / 4, S4 = kS / 4, V = 0, M = 2 * kTT * P4, end4 = M + 2 * kTT * S4;
-  static constexpr size_t bytes = 16 * (size_t)end4 + 256 * sizeof(float);
-};
-
-template <int kS>
-__global__ void __launch_bounds__(kThreads)
-bwd_jump_kernel(const float *__restrict__ v, const float *__restrict__ m,
-                const float *__restrict__ dt, const float *__restrict__ G,
-                float *__restrict__ out, int *err, int L, int nh, int hpg, int T, int nc,
-                int nb) {
-  using SM = JumpSmem<kS>;
-  constexpr int QS = kS / 64, P4 = SM::P4, S4 = SM::S4;
-  extern __shared__ float4 smj[];
-  float4 *vs = smj + SM::V, *ms = smj + SM::M;
-  float *ws = reinterpret_cast<float *>(smj + SM::end4);
-  const int ng = nh / hpg;
-  const int k = blockIdx.x, bh = blockIdx.y;
-  const int b = bh / nh, h = bh - b * nh, g = h / hpg;
-  const int tok0 = k * T, valid = min(T, L - tok0);
-  const int tid = threadIdx.x, py = tid >> 4, sx = tid & 15;
-  // extents (elements) of the buffers read and written, for the debug-bounds checks
-  const int64_t ext_h = (int64_t)nb * L * nh, ext_g = (int64_t)nb * L * ng,
-                ext_chunk = (int64_t)nb * nh * nc;
-  (void)ext_h, (void)ext_g, (void)ext_chunk;  // read by the debug-bounds checks only
-  // G and out of this (chunk, head): checked once, uniform over the CTA
-  if (!SSD_IN_BOUNDS(b < nb && k < nc && (int64_t)bh * nc + k < ext_chunk, err, 200)) return;
-  const int64_t rowh0 = ((int64_t)b * L + tok0) * nh + h, rowg0 = ((int64_t)b * L + tok0) * ng + g;
-  const float *Gc = G + ((int64_t)bh * nc + k) * T;
-  const float Glast = Gc[valid - 1];
-  for (int i = tid; i < T; i += kThreads) {
-    float w = 0.f;
-    if (i < valid) {
-      const int64_t di = rowh0 + (int64_t)i * nh;
-      w = !dt ? exp2f(Gc[i])
-              : SSD_IN_BOUNDS(di < ext_h, err, 203) ? exp2f(Glast - Gc[i]) * dt[di] : 0.f;
-    }
-    ws[i] = w;
-  }
-  // stage the 32 tokens from t0 (zeros past the sequence) into buffer buf
-  auto stage = [&](int buf, int t0) {
-    for (int e = tid; e < kTT * (P4 + S4); e += kThreads) {
-      if (e < kTT * P4) {
-        const int r = e / P4, c = e - r * P4, tok = t0 + r;
-        const int64_t si = (rowh0 + (int64_t)(tok < valid ? tok : 0) * nh) * kP + 4 * c;
-        const bool ok = tok < valid && SSD_IN_BOUNDS(si + 4 <= ext_h * kP, err, 204);
-        cp_async16(vs + (buf * kTT + r) * P4 + c, ok ? v + si : v, ok);
-      } else {
-        const int e2 = e - kTT * P4, r = e2 / S4, c = e2 - r * S4, tok = t0 + r;
-        const int64_t si = (rowg0 + (int64_t)(tok < valid ? tok : 0) * ng) * kS + 4 * c;
-        const bool ok = tok < valid && SSD_IN_BOUNDS(si + 4 <= ext_g * kS, err, 205);
-        cp_async16(ms + (buf * kTT + r) * S4 + c, ok ? m + si : m, ok);
-      }
-    }
-  };
-  float4 acc[4][QS];
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int q = 0; q < QS; ++q) acc[a][q] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int ntile = (valid + kTT - 1) / kTT;
-  stage(0, 0);
-  cp_async_commit();
-  for (int u = 0; u < ntile; ++u) {
-    const int cur = u & 1;
-    if (u + 1 < ntile) stage(cur ^ 1, (u + 1) * kTT);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    const float4 *vb = vs + cur * kTT * P4 + py, *mb = ms + cur * kTT * S4 + sx;
-#pragma unroll 4
-    for (int j = 0; j < kTT; ++j) {
-      const float w = ws[u * kTT + j];
-      const float4 vq = vb[j * P4];
-      float4 mq[QS];
-#pragma unroll
-      for (int q = 0; q < QS; ++q) mq[q] = mb[j * S4 + 16 * q];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const float wv = w * comp(vq, a);
-#pragma unroll
-        for (int q = 0; q < QS; ++q) axpy4(wv, mq[q], acc[a][q]);
-      }
-    }
-    __syncthreads();  // buffer cur is refilled at the next iteration but one
-  }
-  float *dst = out + ((int64_t)bh * nc + k) * kP * kS;
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int q = 0; q < QS; ++q)
-      *reinterpret_cast<float4 *>(dst + (4 * py + a) * kS + 4 * sx + 64 * q) = acc[a][q];
 }
 
 // ------------------------------------------------------- c_i . B_j per group
@@ -305,45 +202,6 @@ bwd_scale_kernel(const float *__restrict__ x, const float *__restrict__ gy,
     reinterpret_cast<float4 *>(xs)[e] = make_float4(fx * xv.x, fx * xv.y, fx * xv.z, fx * xv.w);
     reinterpret_cast<float4 *>(gys)[e] = make_float4(fg * gv.x, fg * gv.y, fg * gv.z, fg * gv.w);
   }
-}
-
-// The GEMMs' pointer arrays, ptr[m][i] for matrix m of batch entry i: the
-// entries are (b, k, g) for the chunks of full length, then (b, g) for the
-// partial last chunk when there is one.
-enum { kPB, kPC, kPR, kPH, kPXs, kPGs, kPDx, kPYs, kPdB, kPdC, kNPtr };
-__global__ void __launch_bounds__(kThreads)
-bwd_gemm_ptrs_kernel(const float *B, const float *C, const float *R, const float *H,
-                     const float *xs, const float *gys, float *dxS, float *ysmS, float *dB,
-                     float *dC, void **ptr, int nbatch, int nfull, int L, int nh, int ng,
-                     int S, int T, int nc) {
-  const int i = blockIdx.x * kThreads + threadIdx.x;
-  if (i >= nbatch) return;
-  const int hpg = nh / ng;
-  int b, k, g;
-  const int ncf = L / T;  // chunks of full length per sequence
-  if (i < nfull) {
-    g = i % ng;
-    k = (i / ng) % ncf;
-    b = i / (ng * ncf);
-  } else {
-    const int j = i - nfull;
-    g = j % ng;
-    b = j / ng;
-    k = nc - 1;
-  }
-  const int64_t rowg = ((int64_t)b * L + (int64_t)k * T) * ng + g;    // row of B, C, dB, dC
-  const int64_t rowh = ((int64_t)b * L + (int64_t)k * T) * nh + g * hpg;  // of x~, dxS, ...
-  const int64_t st = (((int64_t)b * nc + k) * nh + g * hpg) * kP * S;  // of R, h
-  ptr[kPB * nbatch + i] = (void *)(B + rowg * S);
-  ptr[kPC * nbatch + i] = (void *)(C + rowg * S);
-  ptr[kPR * nbatch + i] = (void *)(R + st);
-  ptr[kPH * nbatch + i] = (void *)(H + st);
-  ptr[kPXs * nbatch + i] = (void *)(xs + rowh * kP);
-  ptr[kPGs * nbatch + i] = (void *)(gys + rowh * kP);
-  ptr[kPDx * nbatch + i] = (void *)(dxS + rowh * kP);
-  ptr[kPYs * nbatch + i] = (void *)(ysmS + rowh * kP);
-  ptr[kPdB * nbatch + i] = (void *)(dB + rowg * S);
-  ptr[kPdC * nbatch + i] = (void *)(dC + rowg * S);
 }
 
 // -------------------------------------------------------------- main kernel
@@ -946,7 +804,8 @@ cudaError_t launch_bwd_convert(const BwdConvert &a, cudaStream_t st) {
 }
 
 bool bwd_supported(const Dims &d) {
-  return d.P == kP && (d.S == 64 || d.S == 128 || d.S == 256) && d.T % kTT == 0 && d.T <= 256;
+  return d.P == kP && (d.S == 64 || d.S == 128 || d.S == 256) && d.T % kTT == 0 && d.T <= 256 &&
+         bwd_state_gemm_supported(d);
 }
 
 int bwd_head_slices(const Dims &d) {
@@ -963,30 +822,6 @@ int bwd_head_slices(const Dims &d) {
       if (base * n >= want) break;
     }
   return best;
-}
-
-namespace {
-template <int kS>
-cudaError_t launch_jump(const Dims &d, const float *v, const float *m, const float *dt,
-                        const float *G, float *out, int *err, cudaStream_t st) {
-  const size_t smem = JumpSmem<kS>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(bwd_jump_kernel<kS>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)d.nc, (unsigned)(d.b * d.nh));
-  bwd_jump_kernel<kS><<<grid, kThreads, smem, st>>>(v, m, dt, G, out, err, (int)d.L, (int)d.nh,
-                                                    (int)d.hpg, (int)d.T, (int)d.nc, (int)d.b);
-  return cudaGetLastError();
-}
-}  // namespace
-
-cudaError_t launch_bwd_jump(const Dims &d, const float *v, const float *m, const float *dt,
-                            const float *G, float *out, int *err, cudaStream_t st) {
-  switch (d.S) {
-    case 64: return launch_jump<64>(d, v, m, dt, G, out, err, st);
-    case 128: return launch_jump<128>(d, v, m, dt, G, out, err, st);
-    default: return launch_jump<256>(d, v, m, dt, G, out, err, st);
-  }
 }
 
 namespace {
@@ -1052,33 +887,6 @@ cudaError_t launch_bwd_main(const Dims &d, const float *x, const float *dt, cons
   }
 }
 
-namespace {
-// One cuBLAS handle per device and host thread, created on the first
-// backward call of that thread on that device (the call's one-time set-up;
-// later calls allocate nothing and can be captured in a CUDA graph).  The
-// handle is bound to the caller's stream and to a slice of the caller's
-// workspace at every call.
-cublasHandle_t bwd_cublas(int *fail) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    *fail = 1;
-    return nullptr;
-  }
-  thread_local cublasHandle_t handles[64] = {};
-  if (!handles[dev] && cublasCreate(&handles[dev]) != CUBLAS_STATUS_SUCCESS) {
-    handles[dev] = nullptr;
-    *fail = 1;
-  }
-  return handles[dev];
-}
-}  // namespace
-
-size_t bwd_gemm_ptr_bytes(const Dims &d) {
-  const int64_t ncf = d.L / d.T, part = d.L % d.T ? 1 : 0;
-  const int64_t nbatch = d.b * d.ng * (ncf + part);
-  return sizeof(void *) * (size_t)(kNPtr * nbatch);
-}
-
 cudaError_t launch_bwd_scale(const Dims &d, const float *x, const float *gy, const float *dt,
                              const float *G, float *xs, float *gys, int *err, cudaStream_t st) {
   const int64_t n4 = d.b * d.L * d.nh * (kP / 4);
@@ -1086,71 +894,6 @@ cudaError_t launch_bwd_scale(const Dims &d, const float *x, const float *gy, con
       1, std::min<int64_t>((n4 + kThreads - 1) / kThreads, 8 * (int64_t)sm_count()));
   bwd_scale_kernel<<<blocks, kThreads, 0, st>>>(x, gy, dt, G, xs, gys, err, (int)d.L, (int)d.nh,
                                                 (int)d.T, (int)d.nc, (int)d.b);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_state_gemms(const Dims &d, bool after, const float *B, const float *C,
-                                   const float *R, const float *H, const float *xs,
-                                   const float *gys, float *dxS, float *ysmS, float *dB,
-                                   float *dC, void **ptrs, void *cublas_ws, size_t ws_bytes,
-                                   cudaStream_t st) {
-  const int ncf = (int)(d.L / d.T), part = d.L % d.T ? 1 : 0;
-  const int nfull = (int)(d.b * d.ng * ncf), npart = (int)(d.b * d.ng * part);
-  const int nbatch = nfull + npart;
-  if (!after) {
-    // the pointer arrays (for both halves; the second reuses them)
-    bwd_gemm_ptrs_kernel<<<(nbatch + kThreads - 1) / kThreads, kThreads, 0, st>>>(
-        B, C, R, H, xs, gys, dxS, ysmS, dB, dC, ptrs, nbatch, nfull, (int)d.L, (int)d.nh,
-        (int)d.ng, (int)d.S, (int)d.T, (int)d.nc);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  // cuBLAS's emulated-fp32 kernels want a workspace aligned beyond 256
-  // bytes (with 256 some small batches fail to launch): start it on a 4 KiB
-  // boundary inside the slice given
-  const uintptr_t wa = ((uintptr_t)cublas_ws + 4095) & ~(uintptr_t)4095;
-  if (ws_bytes < (wa - (uintptr_t)cublas_ws) + (1u << 20)) return cudaErrorInvalidValue;
-  ws_bytes -= wa - (uintptr_t)cublas_ws;
-  int fail = 0;
-  cublasHandle_t h = bwd_cublas(&fail);
-  if (fail || cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS ||
-      cublasSetWorkspace(h, reinterpret_cast<void *>(wa), ws_bytes) != CUBLAS_STATUS_SUCCESS)
-    return cudaErrorUnknown;
-  const float one = 1.f, zero = 0.f;
-  const int hp = (int)(d.hpg * d.P), S = (int)d.S;
-  const int ldg = (int)(d.ng * d.S), ldh = (int)(d.nh * d.P);
-  auto arr = [&](int m, int off) { return reinterpret_cast<void **>(ptrs + m * nbatch + off); };
-  // each batch segment: the full chunks (T rows), then the partial last chunk
-  for (int seg = 0; seg < 2; ++seg) {
-    const int off = seg ? nfull : 0, cnt = seg ? npart : nfull;
-    const int rows = seg ? (int)(d.L - (int64_t)ncf * d.T) : (int)d.T;
-    if (cnt == 0) continue;
-    cublasStatus_t cs;
-    if (!after) {
-      // column-major: dxS^T [(h,p)][t] = R [(h,p)][s] (op T of S x hp) . B^T [s][t]
-      cs = cublasGemmBatchedEx(h, CUBLAS_OP_T, CUBLAS_OP_N, hp, rows, S, &one, arr(kPR, off),
-                               CUDA_R_32F, S, arr(kPB, off), CUDA_R_32F, ldg, &zero,
-                               arr(kPDx, off), CUDA_R_32F, ldh, cnt,
-                               CUBLAS_COMPUTE_32F_EMULATED_16BFX9, CUBLAS_GEMM_DEFAULT);
-      if (cs == CUBLAS_STATUS_SUCCESS)
-        cs = cublasGemmBatchedEx(h, CUBLAS_OP_T, CUBLAS_OP_N, hp, rows, S, &one, arr(kPH, off),
-                                 CUDA_R_32F, S, arr(kPC, off), CUDA_R_32F, ldg, &zero,
-                                 arr(kPYs, off), CUDA_R_32F, ldh, cnt,
-                                 CUBLAS_COMPUTE_32F_EMULATED_16BFX9, CUBLAS_GEMM_DEFAULT);
-    } else {
-      // column-major: dB^T [s][t] += R^T [s][(h,p)] . x~^T [(h,p)][t]
-      cs = cublasGemmBatchedEx(h, CUBLAS_OP_N, CUBLAS_OP_N, S, rows, hp, &one, arr(kPR, off),
-                               CUDA_R_32F, S, arr(kPXs, off), CUDA_R_32F, ldh, &one,
-                               arr(kPdB, off), CUDA_R_32F, ldg, cnt,
-                               CUBLAS_COMPUTE_32F_EMULATED_16BFX9, CUBLAS_GEMM_DEFAULT);
-      if (cs == CUBLAS_STATUS_SUCCESS)
-        cs = cublasGemmBatchedEx(h, CUBLAS_OP_N, CUBLAS_OP_N, S, rows, hp, &one, arr(kPH, off),
-                                 CUDA_R_32F, S, arr(kPGs, off), CUDA_R_32F, ldh, &one,
-                                 arr(kPdC, off), CUDA_R_32F, ldg, cnt,
-                                 CUBLAS_COMPUTE_32F_EMULATED_16BFX9, CUBLAS_GEMM_DEFAULT);
-    }
-    if (cs != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
-  }
   return cudaGetLastError();
 }
 

@@ -1,0 +1,379 @@
+// Backward pass: its GEMM-shaped products on the tensor cores in split TF32
+// (fp32-grade products on kind::tf32 MMAs).
+//
+// The adjoint of the chunked recurrence ("State Space Duality (Mamba-2)
+// Part III: The Algorithm", section "The SSD algorithm": the chunk states
+// h_k enter the outputs of chunk k through C_t h_k and are built from the
+// chunk's dt_t exp2(G_last - G_t) x_t B_t^T; the adjoint states R_k =
+// dL/dh_{k+1} from exp2(G_s) gy_s c_s^T) needs, per chunk k and group g,
+// with x~_t = dt_t exp2(G_last - G_t) x_t and g~y_t = exp2(G_t) gy_t:
+//
+//   mode 2, the chunks' jump terms (per head h of the group):
+//     dH[h][p][s] = sum_t x~_t[(h,p)] B_t[s]      (forward states)
+//     dR[h][p][s] = sum_t g~y_t[(h,p)] c_t[s]     (adjoint states)
+//   mode 0, before the per-token kernel (rows (h, p) of the group's heads):
+//     dxS[t][(h,p)] = sum_s B_t[s] R_k[(h,p)][s],  ysmS[t][(h,p)] = sum_s c_t[s] h_k[(h,p)][s]
+//   mode 1, after it:
+//     dB_t[s] += sum_(h,p) x~_t[(h,p)] R_k[(h,p)][s],  dC_t[s] += sum_(h,p) g~y_t[(h,p)] h_k[(h,p)][s]
+//
+// (the per-token kernel applies the factors dt_t exp2(G_last - G_t) and
+// exp2(G_t) of dxS and ysmS as it reads them).
+//
+// Precision.  A TF32 product keeps 11 bits of each operand, which puts the
+// gradient of A off by up to 1.6 % (its terms cancel over the sequence), so
+// every operand a is split into hi = tf32(a) (nearest) and lo = a - hi
+// (exact in fp32; the tensor core reads its leading 11 bits) and each
+// product is lo_a hi_b + hi_a lo_b + hi_a hi_b, accumulated in fp32 in
+// tensor memory: the dropped lo_a lo_b and the truncation of lo leave about
+// 2^-21 relative per product, near fp32 (the "3xTF32" split used by fp32
+// GEMM libraries on TF32 tensor cores).
+//
+// One CTA per (product, batch, chunk, group, M tile, N tile of 128 or 64
+// columns), 256 threads, two CTAs per SM.  M tiles: 128 tokens (modes 0
+// and 1; with chunks shorter than 128 tokens the rows past the chunk are
+// computed and not stored) or the rows (h, p) of two heads of the group
+// (mode 2; an odd group's last tile repeats its head and stores one).  K
+// runs in slices of 32 (one 128-byte row of fp32), double-buffered by TMA.
+// K-major operands (the token rows of modes 0 and 1, the states of mode 0)
+// land as 128-byte rows; the others (the states of mode 1, both operands
+// of mode 2) land as 32 x 32 boxes with K along the rows and are transposed
+// by the split.  Per slice the eight warps split the operands -- hi in
+// place (transposed: every thread reads its pieces, a barrier, then writes
+// down the columns), lo into a buffer of its own -- and thread 0 issues
+// 3 x 4 MMAs (M = 128, N, K = 8) and commits them.  The next slice's split
+// waits for that commit (the lo buffers are single); the other CTA on the
+// SM runs meanwhile.  The epilogue reads the accumulator (warp = TMEM lane
+// quadrant x column half) and stores, or adds into dB / dC.
+#include "tc_common.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kGThreads = 256;
+constexpr int kGM = 128;            // MMA M: tokens (modes 0, 1) or rows (h, p) (mode 2)
+constexpr int kASlice = kGM * 128;  // bytes of an M x 32 slice (16 KB)
+constexpr int kPh = 64;             // headdim
+
+struct GemmArgs {
+  float *out[2];
+  int *err;
+  int L, nh, ng, hpg, S, T, nc, nb, nmt, nnt, nk, n_items;
+};
+
+// hi = tf32(a) (nearest), lo = a - hi (exact) of four values
+__device__ __forceinline__ void split4(const float4 v, uint4 &hi, uint4 &lo) {
+  hi = make_uint4(to_tf32(v.x), to_tf32(v.y), to_tf32(v.z), to_tf32(v.w));
+  lo = make_uint4(__float_as_uint(v.x - __uint_as_float(hi.x)),
+                  __float_as_uint(v.y - __uint_as_float(hi.y)),
+                  __float_as_uint(v.z - __uint_as_float(hi.z)),
+                  __float_as_uint(v.w - __uint_as_float(hi.w)));
+}
+
+// split a K-major slice in place: hi over the data, lo at the same offsets
+template <int kBytes>
+__device__ __forceinline__ void split_kmajor(uint8_t *buf, uint8_t *lo, int tid) {
+#pragma unroll
+  for (int i = 0; i < kBytes / 16 / kGThreads; ++i) {
+    const int off = 16 * (tid + i * kGThreads);
+    uint4 h, l;
+    split4(*reinterpret_cast<const float4 *>(buf + off), h, l);
+    *reinterpret_cast<uint4 *>(buf + off) = h;
+    *reinterpret_cast<uint4 *>(lo + off) = l;
+  }
+}
+
+// A slice that landed as kBoxes boxes of 32 (K) x 32 (M or N) fp32: box j,
+// row = K index, 16-byte piece c = M/N indices 32 j + 4 c .. + 3.  Warp w
+// takes pieces w, w + 8, ... of the 8 kBoxes pieces per row, lane = row.
+template <int kBoxes>
+__device__ __forceinline__ void t_read(const uint8_t *buf, int warp, int lane,
+                                       float4 (&v)[kBoxes]) {
+#pragma unroll
+  for (int i = 0; i < kBoxes; ++i) {
+    const int idx = warp + 8 * i, j = idx >> 3, c = idx & 7;
+    v[i] = *reinterpret_cast<const float4 *>(buf + j * 4096 + sw128(lane, 16 * c));
+  }
+}
+// ... and written back K-major: row 32 j + 4 c + e (an M or N index), K
+// index = lane, hi over the boxes' space, lo into its own buffer
+template <int kBoxes>
+__device__ __forceinline__ void t_write(uint8_t *buf, uint8_t *lo, int warp, int lane,
+                                        const float4 (&v)[kBoxes]) {
+#pragma unroll
+  for (int i = 0; i < kBoxes; ++i) {
+    const int idx = warp + 8 * i, j = idx >> 3, c = idx & 7;
+    uint4 h, l;
+    split4(v[i], h, l);
+    const uint32_t h4[4] = {h.x, h.y, h.z, h.w}, l4[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t o = sw128(32 * j + 4 * c + e, 4 * lane);
+      *reinterpret_cast<uint32_t *>(buf + o) = h4[e];
+      *reinterpret_cast<uint32_t *>(lo + o) = l4[e];
+    }
+  }
+}
+
+template <int kMode, int kN>
+__global__ void __launch_bounds__(kGThreads, 2)
+bwd_state_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
+                      const __grid_constant__ CUtensorMap tA1,
+                      const __grid_constant__ CUtensorMap tS0,
+                      const __grid_constant__ CUtensorMap tS1, const GemmArgs a) {
+  constexpr bool kTransA = kMode == 2, kTransB = kMode >= 1;
+  constexpr int kBSlice = kN * 128;  // bytes of an N x 32 slice
+  constexpr int kStage = kASlice + kBSlice;
+  constexpr int kTmemCols = kN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *loA = smem + 2 * kStage, *loB = loA + kASlice;
+  __shared__ __align__(8) uint64_t full[2], done;
+  __shared__ uint32_t tmem_slot;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the work item: N tile fastest, then the M tile (CTAs in flight share
+  // their operands in L2)
+  int r = blockIdx.x;
+  const int nt = r % a.nnt;
+  r /= a.nnt;
+  const int mt = r % a.nmt;
+  r /= a.nmt;
+  const int g = r % a.ng;
+  r /= a.ng;
+  const int k = r % a.nc;
+  r /= a.nc;
+  const int b = r % a.nb;
+  const int which = r / a.nb;  // the product: 0 or 1
+  const CUtensorMap *tA = which ? &tA1 : &tA0;
+  const CUtensorMap *tS = which ? &tS1 : &tS0;
+  const int tok0 = k * a.T, valid = min(a.T, a.L - tok0);
+  const int t0 = tok0 + mt * kGM;                               // modes 0, 1: first token
+  const int srow = ((b * a.nc + k) * a.nh + g * a.hpg) * kPh;   // modes 0, 1: first state row
+  const int h0 = g * a.hpg + 2 * mt;                            // mode 2: the tile's heads
+  const int h1 = h0 + 1 < (g + 1) * a.hpg ? h0 + 1 : h0;
+  const int nk = kMode == 2 ? (valid + 31) / 32 : a.nk;
+
+  if (tid == 0) {
+    ptx::mbar_init(&full[0], 1);
+    ptx::mbar_init(&full[1], 1);
+    ptx::mbar_init(&done, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_slot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  // TMA of K slice kb into stage kb & 1 (thread 0)
+  auto load = [&](int kb) {
+    uint8_t *st = smem + (kb & 1) * kStage;
+    uint64_t *bar = &full[kb & 1];
+    ptx::mbar_arrive_expect_tx(bar, kStage);
+    if (kMode == 0) {
+      ptx::tma_load_4d(st, tA, 32 * kb, g, t0, b, bar);
+      ptx::tma_load_2d(st + kASlice, tS, 32 * kb, srow + nt * kN, bar);
+    } else if (kMode == 1) {
+      ptx::tma_load_4d(st, tA, 32 * (kb & 1), g * a.hpg + (kb >> 1), t0, b, bar);
+#pragma unroll
+      for (int j = 0; j < kN / 32; ++j)
+        ptx::tma_load_2d(st + kASlice + j * 4096, tS, nt * kN + 32 * j, srow + 32 * kb, bar);
+    } else {
+      const int tk = tok0 + 32 * kb;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        ptx::tma_load_4d(st + q * 4096, tA, 32 * (q & 1), q < 2 ? h0 : h1, tk, b, bar);
+#pragma unroll
+      for (int j = 0; j < kN / 32; ++j)
+        ptx::tma_load_4d(st + kASlice + j * 4096, tS, nt * kN + 32 * j, g, tk, b, bar);
+    }
+  };
+  if (tid == 0) {
+    ptx::prefetch_tmap(tA);
+    ptx::prefetch_tmap(tS);
+    load(0);
+    if (nk > 1) load(1);
+  }
+
+  const uint32_t idesc = ptx::idesc_tf32(kGM, kN, false, false);
+  for (int kb = 0; kb < nk; ++kb) {
+    uint8_t *st = smem + (kb & 1) * kStage, *sb = st + kASlice;
+    ptx::mbar_wait(&full[kb & 1], (kb >> 1) & 1, a.err, 240);
+    if (kb > 0) {
+      // the previous slice's MMAs are done: its stage and the lo buffers
+      // are free
+      ptx::mbar_wait(&done, (kb - 1) & 1, a.err, 241);
+      ptx::tc_fence_after();
+      if (tid == 0 && kb + 1 < nk) load(kb + 1);
+    }
+    if (!kTransA) split_kmajor<kASlice>(st, loA, tid);
+    if (!kTransB) split_kmajor<kBSlice>(sb, loB, tid);
+    if (kTransA || kTransB) {
+      float4 va[kTransA ? 4 : 1], vb[kTransB ? kN / 32 : 1];
+      if constexpr (kTransA) t_read<4>(st, warp, lane, va);
+      if constexpr (kTransB) t_read<kN / 32>(sb, warp, lane, vb);
+      __syncthreads();  // every piece read before the transposed writes
+      if constexpr (kTransA) t_write<4>(st, loA, warp, lane, va);
+      if constexpr (kTransB) t_write<kN / 32>(sb, loB, warp, lane, vb);
+    }
+    ptx::fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      ptx::tc_fence_after();
+      const uint32_t ah = ptx::smem_u32(st), al = ptx::smem_u32(loA);
+      const uint32_t bh = ptx::smem_u32(sb), bl = ptx::smem_u32(loB);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t dah = ptx::smem_desc(ah + 32 * kk, 16, 1024, ptx::kSw128);
+        const uint64_t dal = ptx::smem_desc(al + 32 * kk, 16, 1024, ptx::kSw128);
+        const uint64_t dbh = ptx::smem_desc(bh + 32 * kk, 16, 1024, ptx::kSw128);
+        const uint64_t dbl = ptx::smem_desc(bl + 32 * kk, 16, 1024, ptx::kSw128);
+        ptx::mma_ss<true>(tmem, dal, dbh, idesc, (kb | kk) ? 1u : 0u);
+        ptx::mma_ss<true>(tmem, dah, dbl, idesc, 1u);
+        ptx::mma_ss<true>(tmem, dah, dbh, idesc, 1u);
+      }
+      ptx::mma_commit(&done);
+    }
+  }
+
+  // epilogue: warp = TMEM lane quadrant (32 rows) x half of the N columns
+  ptx::mbar_wait(&done, (nk - 1) & 1, a.err, 242);
+  ptx::tc_fence_after();
+  const int quad = warp & 3, half = warp >> 2, m = quad * 32 + lane;
+  bool live;
+  int64_t o_row;  // the element offset of column nt kN of this thread's row
+  if (kMode == 2) {
+    const int hl = m >> 6, p = m & (kPh - 1);
+    live = hl == 0 || h1 != h0;
+    o_row = ((((int64_t)b * a.nh + (hl ? h1 : h0)) * a.nc + k) * kPh + p) * a.S + nt * kN;
+  } else {
+    const int tl = mt * kGM + m;  // chunk-relative token
+    live = tl < valid;
+    const int64_t tok = (int64_t)b * a.L + tok0 + tl;
+    o_row = kMode == 0 ? (tok * a.nh + (int64_t)g * a.hpg) * kPh + nt * kN
+                       : (tok * a.ng + g) * a.S + nt * kN;
+  }
+  const int64_t o_end = kMode == 1 ? (int64_t)a.nb * a.L * a.ng * a.S
+                      : kMode == 0 ? (int64_t)a.nb * a.L * a.nh * kPh
+                                   : (int64_t)a.nb * a.nh * a.nc * kPh * a.S;
+  float *out = which ? a.out[1] : a.out[0];
+  constexpr int kHalf = kN / 2;
+#pragma unroll
+  for (int ci = 0; ci < kHalf / 16; ++ci) {
+    const int c0 = half * kHalf + 16 * ci;
+    float v[16];
+    ptx::tmem_ld16_sync(tmem + ((uint32_t)(quad * 32) << 16) + c0, v);
+    const int64_t o = o_row + c0;
+    if (!live || !SSD_IN_BOUNDS(o + 16 <= o_end, a.err, 243)) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float4 u = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      if (kMode == 1) {
+        const float4 w = *reinterpret_cast<const float4 *>(out + o + 4 * q);
+        u.x += w.x;
+        u.y += w.y;
+        u.z += w.z;
+        u.w += w.w;
+      }
+      *reinterpret_cast<float4 *>(out + o + 4 * q) = u;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int kMode, int kN>
+cudaError_t run_gemm(const CUtensorMap &ta0, const CUtensorMap &ta1, const CUtensorMap &ts0,
+                     const CUtensorMap &ts1, const GemmArgs &a, cudaStream_t st) {
+  constexpr int smem = 2 * (kASlice + kN * 128) + kASlice + kN * 128 + 1024;
+  auto kernel = bwd_state_gemm_kernel<kMode, kN>;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<a.n_items, kGThreads, smem, st>>>(ta0, ta1, ts0, ts1, a);
+  return cudaGetLastError();
+}
+
+template <int kMode>
+cudaError_t run_mode(int kN, const CUtensorMap &ta0, const CUtensorMap &ta1,
+                     const CUtensorMap &ts0, const CUtensorMap &ts1, const GemmArgs &a,
+                     cudaStream_t st) {
+  return kN == 128 ? run_gemm<kMode, 128>(ta0, ta1, ts0, ts1, a, st)
+                   : run_gemm<kMode, 64>(ta0, ta1, ts0, ts1, a, st);
+}
+
+}  // namespace
+
+bool bwd_state_gemm_supported(const Dims &d) {
+  return d.P == kPh && (d.S == 64 || d.S == 128 || d.S == 256) && d.T >= 32 && d.T % 32 == 0 &&
+         d.b * d.nc * d.nh * kPh < (1LL << 31) && d.b * d.L < (1LL << 31);
+}
+
+cudaError_t launch_bwd_gemm(const Dims &d, int mode, int nprod, const float *A0, const float *A1,
+                            const float *S0, const float *S1, float *out0, float *out1, int *err,
+                            cudaStream_t st) {
+  if (!bwd_state_gemm_supported(d) || mode < 0 || mode > 2 || nprod < 1 || nprod > 2)
+    return cudaErrorInvalidValue;
+  if (nprod == 1) {
+    A1 = A0;
+    S1 = S0;
+    out1 = out0;
+  }
+  const int64_t hp = d.hpg * kPh;
+  const int kN = (mode == 0 ? hp : d.S) % 128 == 0 ? 128 : 64;
+  CUtensorMap ta0, ta1, ts0, ts1;
+  // token-row operands: B, C ([b, L, ng, S]) or x~, gy~ ([b, L, nh, P]), in
+  // boxes of 32 columns x 128 tokens (modes 0, 1) or 32 tokens (mode 2)
+  const bool a_bc = mode == 0;
+  const int rows = mode == 2 ? 32 : kGM;
+  if (!make_tmap_bl(&ta0, A0, false, d.b, d.L, a_bc ? d.ng : d.nh, a_bc ? d.S : kPh, rows) ||
+      !make_tmap_bl(&ta1, A1, false, d.b, d.L, a_bc ? d.ng : d.nh, a_bc ? d.S : kPh, rows))
+    return cudaErrorInvalidValue;
+  if (mode == 2) {
+    // B, C in boxes of 32 s x 32 tokens
+    if (!make_tmap_bl(&ts0, S0, false, d.b, d.L, d.ng, d.S, 32) ||
+        !make_tmap_bl(&ts1, S1, false, d.b, d.L, d.ng, d.S, 32))
+      return cudaErrorInvalidValue;
+  } else {
+    // the states as a [b nc nh P][S] matrix: boxes of 32 s x (N rows in
+    // mode 0, 32 rows in mode 1)
+    const uint64_t dims[2] = {(uint64_t)d.S, (uint64_t)(d.b * d.nc * d.nh * kPh)};
+    const uint64_t strides[1] = {(uint64_t)d.S * 4};
+    const uint32_t box[2] = {32u, mode == 1 ? 32u : (uint32_t)kN};
+    if (!make_tmap_sw128(&ts0, S0, false, 2, dims, strides, box) ||
+        !make_tmap_sw128(&ts1, S1, false, 2, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  GemmArgs a;
+  a.out[0] = out0;
+  a.out[1] = out1;
+  a.err = err;
+  a.L = (int)d.L;
+  a.nh = (int)d.nh;
+  a.ng = (int)d.ng;
+  a.hpg = (int)d.hpg;
+  a.S = (int)d.S;
+  a.T = (int)d.T;
+  a.nc = (int)d.nc;
+  a.nb = (int)d.b;
+  a.nmt = (int)(mode == 2 ? (d.hpg + 1) / 2 : (d.T + kGM - 1) / kGM);
+  a.nnt = (int)((mode == 0 ? hp : d.S) / kN);
+  a.nk = (int)(mode == 0 ? d.S / 32 : mode == 1 ? 2 * d.hpg : 0);
+  const int64_t n_items = nprod * d.b * d.nc * d.ng * a.nmt * a.nnt;
+  if (n_items <= 0 || n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  a.n_items = (int)n_items;
+  switch (mode) {
+    case 0:
+      return run_mode<0>(kN, ta0, ta1, ts0, ts1, a, st);
+    case 1:
+      return run_mode<1>(kN, ta0, ta1, ts0, ts1, a, st);
+    default:
+      return run_mode<2>(kN, ta0, ta1, ts0, ts1, a, st);
+  }
+}
+
+}  // namespace ssd

@@ -651,13 +651,10 @@ namespace {
 // chunk and group (T x T); with bf16 I/O then fp32 copies of x, dt, B, C, gy
 // and fp32 buffers for dx, ddt, dB, dC.  Each part is 256-byte aligned.
 struct BwdLayout {
-  size_t G, dst, states, R, fin, qB, dG, gyx, part, Kcb, sB, sC, dxS, ysmS, xs, gys, ptrs, cws;
+  size_t G, dst, states, R, fin, qB, dG, gyx, part, Kcb, sB, sC, dxS, ysmS, xs, gys;
   size_t cx, cdt, cB, cC, cgy, cdx, cddt, cdB, cdC;  // bf16 I/O only
   size_t total;
 };
-
-// cuBLAS workspace of the state terms' GEMMs
-constexpr size_t kBwdCublasWs = 32u << 20;
 
 BwdLayout bwd_layout(const Dims &d, ssd_dtype dtype) {
   BwdLayout w{};
@@ -679,15 +676,13 @@ BwdLayout bwd_layout(const Dims &d, ssd_dtype dtype) {
   const size_t slc = ns > 1 ? round256(sizeof(float) * ns * d.b * d.L * d.ng * d.S) : 0;
   w.sC = w.sB + slc;
   // the state terms' GEMMs: their results dxS, ysmS and scaled inputs x~,
-  // gy~ (each in the layout of x), pointer arrays and the cuBLAS workspace
+  // gy~ (each in the layout of x)
   const size_t xsz = round256(sizeof(float) * d.b * d.L * d.nh * d.P);
   w.dxS = w.sC + slc;
   w.ysmS = w.dxS + xsz;
   w.xs = w.ysmS + xsz;
   w.gys = w.xs + xsz;
-  w.ptrs = w.gys + xsz;
-  w.cws = w.ptrs + round256(ssd::bwd_gemm_ptr_bytes(d));
-  w.total = w.cws + kBwdCublasWs;
+  w.total = w.gys + xsz;
   if (dtype == SSD_BF16) {
     const size_t xs = round256(sizeof(float) * d.b * d.L * d.nh * d.P),
                  ts = round256(sizeof(float) * d.b * d.L * d.nh),
@@ -773,29 +768,31 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
     cv.to_bf16 = 0;
     step([&] { return ssd::launch_bwd_convert(cv, st); });
   }
-  // the forward's cumsum, jump terms, start states and final state, all in
-  // fp32 (the forward's own jump kernels take TF32 products)
+  // the forward's cumsum, the scaled inputs x~ = dt exp2(G_last - G) x and
+  // gy~ = exp2(G) gy, the jump terms, start states and final state (the
+  // forward's own jump kernels take plain TF32 products)
   step([&] { return ssd::launch_chunk_cumsum(d, SSD_F32, dtf, A, G, err, st); });
-  step([&] { return ssd::launch_bwd_jump(d, xf, Bf, dtf, G, dst, err, st); });
+  step([&] {
+    return ssd::launch_bwd_scale(d, xf, gyf, dtf, G, f(w.xs), f(w.gys), err, st);
+  });
+  step([&] {
+    return ssd::launch_bwd_gemm(d, 2, 1, f(w.xs), nullptr, Bf, nullptr, dst, nullptr, err, st);
+  });
   step([&] {
     return ssd::launch_state_passing(d, dst, G, h0, sts, fin, err, st, false, false, true);
   });
   // the adjoint: its jump terms (over the forward's, no longer needed), the
   // backward pass over chunks for R_k and dh0, then the per-token gradients
-  step([&] { return ssd::launch_bwd_jump(d, gyf, Cf, nullptr, G, dst, err, st); });
+  step([&] {
+    return ssd::launch_bwd_gemm(d, 2, 1, f(w.gys), nullptr, Cf, nullptr, dst, nullptr, err, st);
+  });
   step([&] {
     return ssd::launch_state_passing(d, dst, G, gfinal, R, dh0, err, st, false, true, true);
   });
   step([&] { return ssd::launch_bwd_cb(d, Bf, Cf, f(w.Kcb), err, st); });
-  // the state terms as GEMMs: dxS, ysmS before the per-token kernel, dB and
-  // dC after it
-  void **ptrs = reinterpret_cast<void **>(ws + w.ptrs);
+  // the state terms: dxS, ysmS before the per-token kernel, dB and dC after it
   step([&] {
-    return ssd::launch_bwd_scale(d, xf, gyf, dtf, G, f(w.xs), f(w.gys), err, st);
-  });
-  step([&] {
-    return ssd::launch_bwd_state_gemms(d, false, Bf, Cf, R, sts, f(w.xs), f(w.gys), f(w.dxS),
-                                       f(w.ysmS), dBf, dCf, ptrs, ws + w.cws, kBwdCublasWs, st);
+    return ssd::launch_bwd_gemm(d, 0, 2, Bf, Cf, R, sts, f(w.dxS), f(w.ysmS), err, st);
   });
   step([&] {
     return ssd::launch_bwd_main(d, xf, dtf, Bf, Cf, D, gyf, G, f(w.dxS), f(w.ysmS), f(w.Kcb), dxf,
@@ -811,8 +808,7 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
     return ssd::launch_bwd_reduce(d, f(w.sB), f(w.sC), dBf, dCf, part, dA, dD, err, st);
   });
   step([&] {
-    return ssd::launch_bwd_state_gemms(d, true, Bf, Cf, R, sts, f(w.xs), f(w.gys), f(w.dxS),
-                                       f(w.ysmS), dBf, dCf, ptrs, ws + w.cws, kBwdCublasWs, st);
+    return ssd::launch_bwd_gemm(d, 1, 2, f(w.xs), f(w.gys), R, sts, dBf, dCf, err, st);
   });
   if (bf) {
     ssd::BwdConvert cv{};

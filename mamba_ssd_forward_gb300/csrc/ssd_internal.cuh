@@ -131,27 +131,23 @@ cudaError_t launch_bwd_convert(const BwdConvert &a, cudaStream_t st);
 // dR, R [b, nh, nc, P, S]; dB, dC [b, L, ng, S]; qB, dG, gyx [b, nh, nc*T];
 // part float2 [b, nh, nc].
 bool bwd_supported(const Dims &d);
-// chunk jump terms in fp32, out[k] = sum_{t in k} w_t v_t m_t^T: the
-// adjoint's (v = gy, m = C, dt null: w_t = exp2(G_t)) or the forward's
-// (v = x, m = B: w_t = exp2(G_last - G_t) dt_t)
-cudaError_t launch_bwd_jump(const Dims &d, const float *v, const float *m, const float *dt,
-                            const float *G, float *out, int *err, cudaStream_t st);
 // Kcb [b, nc, ng, T, T]: c_i . B_j of every chunk and group, in the 64 x 64
 // blocks on or below the diagonal
 cudaError_t launch_bwd_cb(const Dims &d, const float *B, const float *C, float *Kcb, int *err,
                           cudaStream_t st);
-// the state terms' GEMMs (cuBLAS, fp32 emulated on the tensor cores; R and
-// H = the start states chunk-major [b, nc, nh, P, S]): before bwd_main
-// (after = false) dxS = B R^T and ysmS = C H^T per (batch, chunk, group), in
-// the layout of x; after it (after = true) dB += x~ R and dC += gy~ H.  ptrs:
-// bwd_gemm_ptr_bytes(d) of workspace for the batched GEMMs' pointer arrays,
-// filled by the first call; cublas_ws: the cuBLAS workspace.
-size_t bwd_gemm_ptr_bytes(const Dims &d);
-cudaError_t launch_bwd_state_gemms(const Dims &d, bool after, const float *B, const float *C,
-                                   const float *R, const float *H, const float *xs,
-                                   const float *gys, float *dxS, float *ysmS, float *dB,
-                                   float *dC, void **ptrs, void *cublas_ws, size_t ws_bytes,
-                                   cudaStream_t st);
+// the backward's GEMMs on the tensor cores in split TF32 (bwd_gemm.cu),
+// nprod (1 or 2) products per launch: product i reads Ai and Si and writes
+// outi.  R and H: the start states, chunk-major [b, nc, nh, P, S].
+//   mode 2, jump terms: A = x~ or gy~, S = B or C ([b, L, ng, S]), out
+//     [b, nh, nc, P, S] = per chunk and head sum_t A_t^T S_t;
+//   mode 0, before bwd_main: A = B or C, S = R or H, out = dxS = B R^T or
+//     ysmS = C H^T per (batch, chunk, group), in the layout of x;
+//   mode 1, after it: A = x~ or gy~, S = R or H, out = dB += x~ R or
+//     dC += gy~ H.
+bool bwd_state_gemm_supported(const Dims &d);
+cudaError_t launch_bwd_gemm(const Dims &d, int mode, int nprod, const float *A0, const float *A1,
+                            const float *S0, const float *S1, float *out0, float *out1, int *err,
+                            cudaStream_t st);
 // x~ = dt exp2(G_last - G_t) x and gy~ = exp2(G_t) gy, in the layout of x
 cudaError_t launch_bwd_scale(const Dims &d, const float *x, const float *gy, const float *dt,
                              const float *G, float *xs, float *gys, int *err, cudaStream_t st);
