@@ -663,10 +663,11 @@ def run_decode(args, w):
 # x the 2070 MHz maximum SM clock (the ALU roofline of the backward kernels)
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 BWD_KERNELS = ["chunk_cumsum", "bwd_scale", "jump GEMM (x~, B)", "state_passing",
-               "jump GEMM (gy~, C)", "state_passing(reverse)", "bwd_cb", "state GEMMs (dx, ysm)",
-               "bwd_main", "bwd_finish", "bwd_reduce", "state GEMMs (dB, dC)"]
-GEMM_STEPS = ["jump GEMM (x~, B)", "jump GEMM (gy~, C)", "state GEMMs (dx, ysm)",
-              "state GEMMs (dB, dC)"]
+               "jump GEMM (gy~, C)", "state_passing(reverse)", "Kcb GEMM (c . B)",
+               "state GEMMs (dx, ysm)", "bwd_main", "bwd_finish", "bwd_reduce",
+               "state GEMMs (dB, dC)"]
+GEMM_STEPS = ["jump GEMM (x~, B)", "jump GEMM (gy~, C)", "Kcb GEMM (c . B)",
+              "state GEMMs (dx, ysm)", "state GEMMs (dB, dC)"]
 
 
 def backward_macs(w: W.Workload) -> dict:
@@ -687,24 +688,27 @@ def backward_macs(w: W.Workload) -> dict:
         # two GEMM launches of two products each
         gemm += w.batch * w.nheads * 4 * v * P * S
         jump += w.batch * w.nheads * 2 * v * P * S  # the two jump terms
-        rest += w.batch * w.ngroups * npair * S  # c_i . B_j, once per group (bwd_cb)
+        jump += w.batch * w.ngroups * npair * S  # c_i . B_j, once per group (Kcb)
         rest += w.batch * w.nheads * P * S  # <R_k, h_k+1>
     return {"bwd_main": main, "gemms": gemm + jump, "total": main + gemm + jump + rest}
 
 
 def state_gemm_bytes(w: W.Workload) -> int:
-    """HBM bytes the four GEMM steps must move (fp32): the jump terms read x~,
-    g~y, B, C and write two state-sized buffers; the state terms read R_k and
-    h_k twice, B and C, x~ and g~y once, write dx~S and ysm~S, and read and
-    write dB and dC."""
+    """HBM bytes the five GEMM steps must move (fp32): the jump terms read x~,
+    g~y, B, C and write two state-sized buffers; Kcb reads B and C and writes
+    the lower triangle of every chunk's T x T block; the state terms read R_k
+    and h_k twice, B and C, x~ and g~y once, write dx~S and ysm~S, and read
+    and write dB and dC."""
     f = 4
     states = 2 * w.batch * w.nchunks * w.nheads * w.headdim * w.dstate * f
     bc = 2 * w.batch * w.seqlen * w.ngroups * w.dstate * f
     xp = 2 * w.batch * w.seqlen * w.nheads * w.headdim * f
     jump = xp + bc + states            # read x~, g~y, B, C; write dH, dR
+    T = w.chunk
+    kcb = bc + w.batch * w.ngroups * w.nchunks * T * (T + 1) // 2 * f
     before = states + bc + xp          # read R, h, B, C; write dxS, ysmS
     after = states + xp + 2 * bc       # read R, h, x~, g~y; read and write dB, dC
-    return jump + before + after
+    return jump + kcb + before + after
 
 
 def time_oracle_backward(w: W.Workload, inp, gy, gfinal, target_s: float):

@@ -29,7 +29,7 @@
 //   state_passing     forwards over the chunks for h_k and the final state;
 //   bwd_state_gemm    the adjoint's chunk jump terms sum_s gy~_s c_s^T;
 //   state_passing     backwards over the chunks for R_k and dh0;
-//   bwd_cb_kernel     c_i . B_j of every chunk and group;
+//   bwd_state_gemm    c_i . B_j of every chunk and group (Kcb);
 //   bwd_state_gemm    the state terms R_k B_t and h_k c_t per token and head;
 //   bwd_main_kernel   per (row tile, chunk, batch * group), walking the
 //                     group's heads: dx of each head and per token q . B,
@@ -89,82 +89,6 @@ __device__ __forceinline__ void axpy4(float a, const float4 &v, float4 &acc) {
 }
 __device__ __forceinline__ float comp(const float4 &v, int e) {
   return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
-}
-
-// ------------------------------------------------------- c_i . B_j per group
-
-// Kcb[b, k, g][i][j] = c_i . B_j for the tokens i, j of chunk k, in the 64 x
-// 64 blocks on or below the diagonal (j-block <= i-block; the other blocks
-// are neither written nor read), zero past the sequence.  The masked
-// products of every head of the group read it instead of forming the dot
-// products over S themselves.  One CTA per (block pair, chunk, batch *
-// group), 256 threads as a 16 x 16 grid, thread (ty, tx) owning rows
-// ty + 16 a and columns tx + 16 b (a, b < 4) of the block; 32-wide slices of
-// S staged in shared memory (rows padded to 36 floats).
-template <int kS>
-__global__ void __launch_bounds__(kThreads)
-bwd_cb_kernel(const float *__restrict__ Bm, const float *__restrict__ Cm,
-              float *__restrict__ Kcb, int *err, int L, int ng, int T, int nc, int nb) {
-  constexpr int KS = 32, LD = KS + 4;
-  __shared__ __align__(16) float cs[64][LD];
-  __shared__ __align__(16) float bs[64][LD];
-  const int nblk = T / 64, npair = nblk * (nblk + 1) / 2;
-  const int k = blockIdx.x / npair, pr = blockIdx.x - k * npair;
-  const int bg = blockIdx.y, b = bg / ng, g = bg - b * ng;
-  // block pair pr -> (I, J), J <= I, in row order
-  int I = 0, rem = pr;
-  while (rem > I) {
-    rem -= I + 1;
-    ++I;
-  }
-  const int J = rem;
-  const int tok0 = k * T, valid = min(T, L - tok0);
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  const int64_t ext_g = (int64_t)nb * L * ng;
-  (void)ext_g;  // read by the debug-bounds checks only
-  // this (chunk, group)'s T x T block of Kcb: checked once, uniform over the CTA
-  if (!SSD_IN_BOUNDS(b < nb && k < nc && ((int64_t)bg * nc + k) < (int64_t)nb * ng * nc, err,
-                     216))
-    return;
-  const int64_t rowg0 = ((int64_t)b * L + tok0) * ng + g;
-  float acc[4][4];
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
-  for (int k0 = 0; k0 < kS; k0 += KS) {
-    __syncthreads();
-    // 64 rows x 8 float4 of C (rows of block I) and of B (rows of block J)
-    for (int e = tid; e < 2 * 64 * (KS / 4); e += kThreads) {
-      const bool isC = e < 64 * (KS / 4);
-      const int e2 = isC ? e : e - 64 * (KS / 4), r = e2 / (KS / 4), c4 = e2 - r * (KS / 4);
-      const int tok = (isC ? I : J) * 64 + r;
-      const int64_t gi = (rowg0 + (int64_t)(tok < valid ? tok : 0) * ng) * kS + k0 + 4 * c4;
-      const bool ok = tok < valid && SSD_IN_BOUNDS(gi + 4 <= ext_g * kS, err, 217);
-      cp_async16(isC ? &cs[r][4 * c4] : &bs[r][4 * c4], ok ? (isC ? Cm : Bm) + gi : Cm, ok);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-#pragma unroll
-    for (int q = 0; q < KS / 4; ++q) {
-      float4 cv[4], bv[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) cv[a] = *reinterpret_cast<const float4 *>(&cs[ty + 16 * a][4 * q]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) bv[c] = *reinterpret_cast<const float4 *>(&bs[tx + 16 * c][4 * q]);
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[a][c] = dot4(cv[a], bv[c], acc[a][c]);
-    }
-  }
-  float *dst = Kcb + ((int64_t)bg * nc + k) * T * T;
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      dst[(int64_t)(I * 64 + ty + 16 * a) * T + J * 64 + tx + 16 * c] = acc[a][c];
 }
 
 // ------------------------------------------------------------ state terms
@@ -305,7 +229,7 @@ struct MainSmem {
 // scalars), while the S-side weights dt_t w (x . gy) or w (gy . x) are
 // added up over the heads in Wsum; the S-wide update then runs once per
 // group, B and C being shared by its heads, and writes dB or dC.  c_t . B_j
-// comes from bwd_cb_kernel, and the state terms from the GEMMs around this
+// comes from the Kcb GEMM, and the state terms from the GEMMs around this
 // kernel: dx += dt_t exp2(G_last - G_t) (R B_t) and ysm += exp2(G_t) (h c_t)
 // from dxS and ysmS computed before it; dB and dC get R^T x~ and h^T gy~
 // added after it.
@@ -824,17 +748,9 @@ int bwd_head_slices(const Dims &d) {
   return best;
 }
 
-namespace {
-template <int kS>
-cudaError_t launch_cb(const Dims &d, const float *B, const float *C, float *Kcb, int *err,
-                      cudaStream_t st) {
-  const int nblk = (int)d.T / 64;
-  dim3 grid((unsigned)(d.nc * (nblk * (nblk + 1) / 2)), (unsigned)(d.b * d.ng));
-  bwd_cb_kernel<kS><<<grid, kThreads, 0, st>>>(B, C, Kcb, err, (int)d.L, (int)d.ng, (int)d.T,
-                                               (int)d.nc, (int)d.b);
-  return cudaGetLastError();
-}
 
+
+namespace {
 template <int kS, int kG, int kTok>
 cudaError_t launch_main(const Dims &d, const float *x, const float *dt, const float *B,
                         const float *C, const float *D, const float *gy, const float *G,
@@ -854,15 +770,6 @@ cudaError_t launch_main(const Dims &d, const float *x, const float *dt, const fl
   return cudaGetLastError();
 }
 }  // namespace
-
-cudaError_t launch_bwd_cb(const Dims &d, const float *B, const float *C, float *Kcb, int *err,
-                          cudaStream_t st) {
-  switch (d.S) {
-    case 64: return launch_cb<64>(d, B, C, Kcb, err, st);
-    case 128: return launch_cb<128>(d, B, C, Kcb, err, st);
-    default: return launch_cb<256>(d, B, C, Kcb, err, st);
-  }
-}
 
 cudaError_t launch_bwd_main(const Dims &d, const float *x, const float *dt, const float *B,
                             const float *C, const float *D, const float *gy, const float *G,

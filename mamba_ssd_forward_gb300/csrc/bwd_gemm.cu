@@ -15,6 +15,9 @@
 //     dxS[t][(h,p)] = sum_s B_t[s] R_k[(h,p)][s],  ysmS[t][(h,p)] = sum_s c_t[s] h_k[(h,p)][s]
 //   mode 1, after it:
 //     dB_t[s] += sum_(h,p) x~_t[(h,p)] R_k[(h,p)][s],  dC_t[s] += sum_(h,p) g~y_t[(h,p)] h_k[(h,p)][s]
+//   mode 3, the in-chunk scores the per-token kernel weighs (once per group):
+//     Kcb[i][j] = c_i . B_j for the 128 x 128 token tiles on or below the
+//     chunk's diagonal
 //
 // (the per-token kernel applies the factors dt_t exp2(G_last - G_t) and
 // exp2(G_t) of dxS and ysmS as it reads them).
@@ -29,12 +32,12 @@
 // GEMM libraries on TF32 tensor cores).
 //
 // One CTA per (product, batch, chunk, group, M tile, N tile of 128 or 64
-// columns), 256 threads, two CTAs per SM.  M tiles: 128 tokens (modes 0
-// and 1; with chunks shorter than 128 tokens the rows past the chunk are
+// columns), 256 threads, two CTAs per SM.  M tiles: 128 tokens (modes 0,
+// 1 and 3; with chunks shorter than 128 tokens the rows past the chunk are
 // computed and not stored) or the rows (h, p) of two heads of the group
 // (mode 2; an odd group's last tile repeats its head and stores one).  K
 // runs in slices of 32 (one 128-byte row of fp32), double-buffered by TMA.
-// K-major operands (the token rows of modes 0 and 1, the states of mode 0)
+// K-major operands (the token rows of modes 0, 1 and 3, the states of mode 0)
 // land as 128-byte rows; the others (the states of mode 1, both operands
 // of mode 2) land as 32 x 32 boxes with K along the rows and are transposed
 // by the split.  Per slice the eight warps split the operands -- hi in
@@ -120,7 +123,7 @@ bwd_state_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
                       const __grid_constant__ CUtensorMap tA1,
                       const __grid_constant__ CUtensorMap tS0,
                       const __grid_constant__ CUtensorMap tS1, const GemmArgs a) {
-  constexpr bool kTransA = kMode == 2, kTransB = kMode >= 1;
+  constexpr bool kTransA = kMode == 2, kTransB = kMode == 1 || kMode == 2;
   constexpr int kBSlice = kN * 128;  // bytes of an N x 32 slice
   constexpr int kStage = kASlice + kBSlice;
   constexpr int kTmemCols = kN;
@@ -147,7 +150,11 @@ bwd_state_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
   const CUtensorMap *tA = which ? &tA1 : &tA0;
   const CUtensorMap *tS = which ? &tS1 : &tS0;
   const int tok0 = k * a.T, valid = min(a.T, a.L - tok0);
-  const int t0 = tok0 + mt * kGM;                               // modes 0, 1: first token
+  // mode 3: the row and column token tiles (mi, ni), ni <= mi, of tile pair mt
+  int mi = 0, ni = mt;
+  if (kMode == 3)
+    while (ni > mi) ni -= ++mi;
+  const int t0 = tok0 + (kMode == 3 ? mi : mt) * kGM;          // modes 0, 1, 3: first token
   const int srow = ((b * a.nc + k) * a.nh + g * a.hpg) * kPh;   // modes 0, 1: first state row
   const int h0 = g * a.hpg + 2 * mt;                            // mode 2: the tile's heads
   const int h1 = h0 + 1 < (g + 1) * a.hpg ? h0 + 1 : h0;
@@ -176,6 +183,9 @@ bwd_state_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
     if (kMode == 0) {
       ptx::tma_load_4d(st, tA, 32 * kb, g, t0, b, bar);
       ptx::tma_load_2d(st + kASlice, tS, 32 * kb, srow + nt * kN, bar);
+    } else if (kMode == 3) {
+      ptx::tma_load_4d(st, tA, 32 * kb, g, t0, b, bar);
+      ptx::tma_load_4d(st + kASlice, tS, 32 * kb, g, tok0 + ni * kGM, b, bar);
     } else if (kMode == 1) {
       ptx::tma_load_4d(st, tA, 32 * (kb & 1), g * a.hpg + (kb >> 1), t0, b, bar);
 #pragma unroll
@@ -249,6 +259,10 @@ bwd_state_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
     const int hl = m >> 6, p = m & (kPh - 1);
     live = hl == 0 || h1 != h0;
     o_row = ((((int64_t)b * a.nh + (hl ? h1 : h0)) * a.nc + k) * kPh + p) * a.S + nt * kN;
+  } else if (kMode == 3) {
+    const int i = mi * kGM + m;  // row token of the chunk
+    live = i < a.T;
+    o_row = (((int64_t)b * a.ng + g) * a.nc + k) * a.T * a.T + (int64_t)i * a.T + ni * kGM;
   } else {
     const int tl = mt * kGM + m;  // chunk-relative token
     live = tl < valid;
@@ -258,6 +272,7 @@ bwd_state_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
   }
   const int64_t o_end = kMode == 1 ? (int64_t)a.nb * a.L * a.ng * a.S
                       : kMode == 0 ? (int64_t)a.nb * a.L * a.nh * kPh
+                      : kMode == 3 ? (int64_t)a.nb * a.ng * a.nc * a.T * a.T
                                    : (int64_t)a.nb * a.nh * a.nc * kPh * a.S;
   float *out = which ? a.out[1] : a.out[0];
   constexpr int kHalf = kN / 2;
@@ -267,6 +282,7 @@ bwd_state_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
     float v[16];
     ptx::tmem_ld16_sync(tmem + ((uint32_t)(quad * 32) << 16) + c0, v);
     const int64_t o = o_row + c0;
+    if (kMode == 3 && ni * kGM + c0 >= a.T) continue;  // columns past the chunk
     if (!live || !SSD_IN_BOUNDS(o + 16 <= o_end, a.err, 243)) continue;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -316,7 +332,7 @@ bool bwd_state_gemm_supported(const Dims &d) {
 cudaError_t launch_bwd_gemm(const Dims &d, int mode, int nprod, const float *A0, const float *A1,
                             const float *S0, const float *S1, float *out0, float *out1, int *err,
                             cudaStream_t st) {
-  if (!bwd_state_gemm_supported(d) || mode < 0 || mode > 2 || nprod < 1 || nprod > 2)
+  if (!bwd_state_gemm_supported(d) || mode < 0 || mode > 3 || nprod < 1 || nprod > 2)
     return cudaErrorInvalidValue;
   if (nprod == 1) {
     A1 = A0;
@@ -324,19 +340,20 @@ cudaError_t launch_bwd_gemm(const Dims &d, int mode, int nprod, const float *A0,
     out1 = out0;
   }
   const int64_t hp = d.hpg * kPh;
-  const int kN = (mode == 0 ? hp : d.S) % 128 == 0 ? 128 : 64;
+  const int kN = mode == 3 ? 128 : (mode == 0 ? hp : d.S) % 128 == 0 ? 128 : 64;
   CUtensorMap ta0, ta1, ts0, ts1;
   // token-row operands: B, C ([b, L, ng, S]) or x~, gy~ ([b, L, nh, P]), in
   // boxes of 32 columns x 128 tokens (modes 0, 1) or 32 tokens (mode 2)
-  const bool a_bc = mode == 0;
+  const bool a_bc = mode == 0 || mode == 3;
   const int rows = mode == 2 ? 32 : kGM;
   if (!make_tmap_bl(&ta0, A0, false, d.b, d.L, a_bc ? d.ng : d.nh, a_bc ? d.S : kPh, rows) ||
       !make_tmap_bl(&ta1, A1, false, d.b, d.L, a_bc ? d.ng : d.nh, a_bc ? d.S : kPh, rows))
     return cudaErrorInvalidValue;
-  if (mode == 2) {
-    // B, C in boxes of 32 s x 32 tokens
-    if (!make_tmap_bl(&ts0, S0, false, d.b, d.L, d.ng, d.S, 32) ||
-        !make_tmap_bl(&ts1, S1, false, d.b, d.L, d.ng, d.S, 32))
+  if (mode >= 2) {
+    // B, C in boxes of 32 s x 32 tokens (mode 2) or 128 tokens (mode 3)
+    const int srows = mode == 2 ? 32 : kGM;
+    if (!make_tmap_bl(&ts0, S0, false, d.b, d.L, d.ng, d.S, srows) ||
+        !make_tmap_bl(&ts1, S1, false, d.b, d.L, d.ng, d.S, srows))
       return cudaErrorInvalidValue;
   } else {
     // the states as a [b nc nh P][S] matrix: boxes of 32 s x (N rows in
@@ -360,9 +377,10 @@ cudaError_t launch_bwd_gemm(const Dims &d, int mode, int nprod, const float *A0,
   a.T = (int)d.T;
   a.nc = (int)d.nc;
   a.nb = (int)d.b;
-  a.nmt = (int)(mode == 2 ? (d.hpg + 1) / 2 : (d.T + kGM - 1) / kGM);
-  a.nnt = (int)((mode == 0 ? hp : d.S) / kN);
-  a.nk = (int)(mode == 0 ? d.S / 32 : mode == 1 ? 2 * d.hpg : 0);
+  const int64_t ntok = (d.T + kGM - 1) / kGM;  // 128-token tiles per chunk
+  a.nmt = (int)(mode == 2 ? (d.hpg + 1) / 2 : mode == 3 ? ntok * (ntok + 1) / 2 : ntok);
+  a.nnt = (int)(mode == 3 ? 1 : (mode == 0 ? hp : d.S) / kN);
+  a.nk = (int)(mode == 1 ? 2 * d.hpg : mode == 2 ? 0 : d.S / 32);
   const int64_t n_items = nprod * d.b * d.nc * d.ng * a.nmt * a.nnt;
   if (n_items <= 0 || n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
   a.n_items = (int)n_items;
@@ -371,8 +389,10 @@ cudaError_t launch_bwd_gemm(const Dims &d, int mode, int nprod, const float *A0,
       return run_mode<0>(kN, ta0, ta1, ts0, ts1, a, st);
     case 1:
       return run_mode<1>(kN, ta0, ta1, ts0, ts1, a, st);
-    default:
+    case 2:
       return run_mode<2>(kN, ta0, ta1, ts0, ts1, a, st);
+    default:
+      return run_gemm<3, 128>(ta0, ta1, ts0, ts1, a, st);
   }
 }
 

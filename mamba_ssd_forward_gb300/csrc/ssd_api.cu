@@ -789,7 +789,10 @@ ssd_status backward_impl(const ssd_dims *dims, ssd_dtype dtype, const void *x, c
   step([&] {
     return ssd::launch_state_passing(d, dst, G, gfinal, R, dh0, err, st, false, true, true);
   });
-  step([&] { return ssd::launch_bwd_cb(d, Bf, Cf, f(w.Kcb), err, st); });
+  // Kcb: c_i . B_j per chunk and group
+  step([&] {
+    return ssd::launch_bwd_gemm(d, 3, 1, Cf, nullptr, Bf, nullptr, f(w.Kcb), nullptr, err, st);
+  });
   // the state terms: dxS, ysmS before the per-token kernel, dB and dC after it
   step([&] {
     return ssd::launch_bwd_gemm(d, 0, 2, Bf, Cf, R, sts, f(w.dxS), f(w.ysmS), err, st);

@@ -131,10 +131,6 @@ cudaError_t launch_bwd_convert(const BwdConvert &a, cudaStream_t st);
 // dR, R [b, nh, nc, P, S]; dB, dC [b, L, ng, S]; qB, dG, gyx [b, nh, nc*T];
 // part float2 [b, nh, nc].
 bool bwd_supported(const Dims &d);
-// Kcb [b, nc, ng, T, T]: c_i . B_j of every chunk and group, in the 64 x 64
-// blocks on or below the diagonal
-cudaError_t launch_bwd_cb(const Dims &d, const float *B, const float *C, float *Kcb, int *err,
-                          cudaStream_t st);
 // the backward's GEMMs on the tensor cores in split TF32 (bwd_gemm.cu),
 // nprod (1 or 2) products per launch: product i reads Ai and Si and writes
 // outi.  R and H: the start states, chunk-major [b, nc, nh, P, S].
@@ -143,7 +139,9 @@ cudaError_t launch_bwd_cb(const Dims &d, const float *B, const float *C, float *
 //   mode 0, before bwd_main: A = B or C, S = R or H, out = dxS = B R^T or
 //     ysmS = C H^T per (batch, chunk, group), in the layout of x;
 //   mode 1, after it: A = x~ or gy~, S = R or H, out = dB += x~ R or
-//     dC += gy~ H.
+//     dC += gy~ H;
+//   mode 3, A = C, S = B: out = Kcb [b, ng, nc, T, T], c_i . B_j of every
+//     chunk and group on and below the diagonal (128 x 128 token tiles).
 bool bwd_state_gemm_supported(const Dims &d);
 cudaError_t launch_bwd_gemm(const Dims &d, int mode, int nprod, const float *A0, const float *A1,
                             const float *S0, const float *S1, float *out0, float *out1, int *err,
