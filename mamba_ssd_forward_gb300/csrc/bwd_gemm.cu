@@ -52,7 +52,6 @@
 namespace ssd {
 namespace {
 
-constexpr int kGThreads = 256;
 constexpr int kGM = 128;            // MMA M: tokens (modes 0, 1) or rows (h, p) (mode 2)
 constexpr int kASlice = kGM * 128;  // bytes of an M x 32 slice (16 KB)
 constexpr int kPh = 64;             // headdim
@@ -72,16 +71,39 @@ __device__ __forceinline__ void split4(const float4 v, uint4 &hi, uint4 &lo) {
                   __float_as_uint(v.w - __uint_as_float(hi.w)));
 }
 
-// split a K-major slice in place: hi over the data, lo at the same offsets
+constexpr int kRowWarps = 8;                  // split warps 0..7
+constexpr int kRowThreads = 32 * kRowWarps;
+constexpr int kProdWarp = 8, kMmaWarp = 9;    // TMA producer, MMA issuer
+constexpr int kEpiWarp0 = 10;                 // epilogue warps 10..13
+constexpr int kPThreads = 32 * (kEpiWarp0 + 4);
+constexpr int kRing = 3;                      // TMA landing stages
+
+// A landed K-major slice of kBytes: this thread's 16-byte pieces tid + 256 i
+// into registers ...
 template <int kBytes>
-__device__ __forceinline__ void split_kmajor(uint8_t *buf, uint8_t *lo, int tid) {
+__device__ __forceinline__ void k_read(const uint8_t *buf, int tid,
+                                       float4 (&v)[kBytes / 16 / kRowThreads]) {
 #pragma unroll
-  for (int i = 0; i < kBytes / 16 / kGThreads; ++i) {
-    const int off = 16 * (tid + i * kGThreads);
-    uint4 h, l;
-    split4(*reinterpret_cast<const float4 *>(buf + off), h, l);
-    *reinterpret_cast<uint4 *>(buf + off) = h;
-    *reinterpret_cast<uint4 *>(lo + off) = l;
+  for (int i = 0; i < kBytes / 16 / kRowThreads; ++i)
+    v[i] = *reinterpret_cast<const float4 *>(buf + 16 * (tid + i * kRowThreads));
+}
+// ... split in registers ...
+template <int kN4>
+__device__ __forceinline__ void split_regs(const float4 (&v)[kN4], uint4 (&h)[kN4],
+                                           uint4 (&l)[kN4]) {
+#pragma unroll
+  for (int i = 0; i < kN4; ++i) split4(v[i], h[i], l[i]);
+}
+// ... and stored: hi and lo at the same offsets of their buffers
+template <int kBytes>
+__device__ __forceinline__ void k_store(uint8_t *hi, uint8_t *lo, int tid,
+                                        const uint4 (&h)[kBytes / 16 / kRowThreads],
+                                        const uint4 (&l)[kBytes / 16 / kRowThreads]) {
+#pragma unroll
+  for (int i = 0; i < kBytes / 16 / kRowThreads; ++i) {
+    const int off = 16 * (tid + i * kRowThreads);
+    *reinterpret_cast<uint4 *>(hi + off) = h[i];
+    *reinterpret_cast<uint4 *>(lo + off) = l[i];
   }
 }
 
@@ -97,76 +119,103 @@ __device__ __forceinline__ void t_read(const uint8_t *buf, int warp, int lane,
     v[i] = *reinterpret_cast<const float4 *>(buf + j * 4096 + sw128(lane, 16 * c));
   }
 }
-// ... and written back K-major: row 32 j + 4 c + e (an M or N index), K
-// index = lane, hi over the boxes' space, lo into its own buffer
+// ... and, split, stored K-major: row 32 j + 4 c + e (an M or N index), K
+// index = lane, hi and lo into their buffers
 template <int kBoxes>
-__device__ __forceinline__ void t_write(uint8_t *buf, uint8_t *lo, int warp, int lane,
-                                        const float4 (&v)[kBoxes]) {
+__device__ __forceinline__ void t_store(uint8_t *hi, uint8_t *lo, int warp, int lane,
+                                        const uint4 (&h)[kBoxes], const uint4 (&l)[kBoxes]) {
 #pragma unroll
   for (int i = 0; i < kBoxes; ++i) {
     const int idx = warp + 8 * i, j = idx >> 3, c = idx & 7;
-    uint4 h, l;
-    split4(v[i], h, l);
-    const uint32_t h4[4] = {h.x, h.y, h.z, h.w}, l4[4] = {l.x, l.y, l.z, l.w};
+    const uint32_t h4[4] = {h[i].x, h[i].y, h[i].z, h[i].w};
+    const uint32_t l4[4] = {l[i].x, l[i].y, l[i].z, l[i].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const uint32_t o = sw128(32 * j + 4 * c + e, 4 * lane);
-      *reinterpret_cast<uint32_t *>(buf + o) = h4[e];
+      *reinterpret_cast<uint32_t *>(hi + o) = h4[e];
       *reinterpret_cast<uint32_t *>(lo + o) = l4[e];
     }
   }
 }
 
+// A work item (one output tile): product, batch, chunk, group, M tile, N
+// tile, N fastest (CTAs in flight share their operands in L2).
+struct Tile {
+  int nt, mt, g, k, b, which, mi, ni, tok0, valid, nk;
+};
+template <int kMode>
+__device__ __forceinline__ Tile decode_tile(int item, const GemmArgs &a) {
+  Tile t;
+  int r = item;
+  t.nt = r % a.nnt;
+  r /= a.nnt;
+  t.mt = r % a.nmt;
+  r /= a.nmt;
+  t.g = r % a.ng;
+  r /= a.ng;
+  t.k = r % a.nc;
+  r /= a.nc;
+  t.b = r % a.nb;
+  t.which = r / a.nb;
+  // mode 3: the row and column token tiles (mi, ni), ni <= mi, of pair mt
+  t.mi = 0;
+  t.ni = t.mt;
+  if (kMode == 3)
+    while (t.ni > t.mi) t.ni -= ++t.mi;
+  t.tok0 = t.k * a.T;
+  t.valid = min(a.T, a.L - t.tok0);
+  t.nk = kMode == 2 ? (t.valid + 31) / 32 : a.nk;
+  return t;
+}
+
+// Persistent: one CTA per SM walks a strided list of tiles; the slices of
+// consecutive tiles stream through one pipeline.  Warp roles:
+//   warp 8 (TMA):       slices into a ring of kRing landing stages;
+//   warps 0-7 (split):  a landed slice into registers (the stage is then
+//                       free), split into hi and lo, written K-major into
+//                       one of two operand sets;
+//   warp 9 (MMA):       per slice 3 x 4 MMAs from an operand set into the
+//                       tile's accumulator (two in tensor memory, by tile
+//                       parity), each commit freeing the set;
+//   warps 10-13:        per tile the epilogue of its accumulator (warp =
+//                       TMEM lane quadrant), which it then frees.
 template <int kMode, int kN>
-__global__ void __launch_bounds__(kGThreads, 2)
+__global__ void __launch_bounds__(kPThreads, 1)
 bwd_state_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
                       const __grid_constant__ CUtensorMap tA1,
                       const __grid_constant__ CUtensorMap tS0,
                       const __grid_constant__ CUtensorMap tS1, const GemmArgs a) {
   constexpr bool kTransA = kMode == 2, kTransB = kMode == 1 || kMode == 2;
-  constexpr int kBSlice = kN * 128;  // bytes of an N x 32 slice
-  constexpr int kStage = kASlice + kBSlice;
-  constexpr int kTmemCols = kN;
+  constexpr int kBSlice = kN * 128;           // bytes of an N x 32 slice
+  constexpr int kStage = kASlice + kBSlice;   // one landed slice
+  constexpr int kOps = 2 * kStage;            // operand set: hi A | hi B | lo A | lo B
+  constexpr int kTmemCols = 2 * kN;
+  constexpr int kNA = kASlice / 16 / kRowThreads, kNB = kBSlice / 16 / kRowThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t *loA = smem + 2 * kStage, *loB = loA + kASlice;
-  __shared__ __align__(8) uint64_t full[2], done;
+  uint8_t *ring = smem, *ops = smem + kRing * kStage;
+  // full: a slice landed; empty: the split warps have read it; opfull: an
+  // operand set is written; opfree: its MMAs are done; accfull: a tile's
+  // MMAs are done; accfree: its epilogue has read the accumulator
+  __shared__ __align__(8) uint64_t full[kRing], empty[kRing], opfull[2], opfree[2], accfull[2],
+      accfree[2];
   __shared__ uint32_t tmem_slot;
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // the work item: N tile fastest, then the M tile (CTAs in flight share
-  // their operands in L2)
-  int r = blockIdx.x;
-  const int nt = r % a.nnt;
-  r /= a.nnt;
-  const int mt = r % a.nmt;
-  r /= a.nmt;
-  const int g = r % a.ng;
-  r /= a.ng;
-  const int k = r % a.nc;
-  r /= a.nc;
-  const int b = r % a.nb;
-  const int which = r / a.nb;  // the product: 0 or 1
-  const CUtensorMap *tA = which ? &tA1 : &tA0;
-  const CUtensorMap *tS = which ? &tS1 : &tS0;
-  const int tok0 = k * a.T, valid = min(a.T, a.L - tok0);
-  // mode 3: the row and column token tiles (mi, ni), ni <= mi, of tile pair mt
-  int mi = 0, ni = mt;
-  if (kMode == 3)
-    while (ni > mi) ni -= ++mi;
-  const int t0 = tok0 + (kMode == 3 ? mi : mt) * kGM;          // modes 0, 1, 3: first token
-  const int srow = ((b * a.nc + k) * a.nh + g * a.hpg) * kPh;   // modes 0, 1: first state row
-  const int h0 = g * a.hpg + 2 * mt;                            // mode 2: the tile's heads
-  const int h1 = h0 + 1 < (g + 1) * a.hpg ? h0 + 1 : h0;
-  const int nk = kMode == 2 ? (valid + 31) / 32 : a.nk;
 
   if (tid == 0) {
-    ptx::mbar_init(&full[0], 1);
-    ptx::mbar_init(&full[1], 1);
-    ptx::mbar_init(&done, 1);
+    for (int i = 0; i < kRing; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], kRowWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&opfull[i], kRowWarps);
+      ptx::mbar_init(&opfree[i], 1);
+      ptx::mbar_init(&accfull[i], 1);
+      ptx::mbar_init(&accfree[i], 4);
+    }
     ptx::fence_mbar_init();
   }
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(&tmem_slot, kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -175,142 +224,201 @@ bwd_state_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  // TMA of K slice kb into stage kb & 1 (thread 0)
-  auto load = [&](int kb) {
-    uint8_t *st = smem + (kb & 1) * kStage;
-    uint64_t *bar = &full[kb & 1];
-    ptx::mbar_arrive_expect_tx(bar, kStage);
-    if (kMode == 0) {
-      ptx::tma_load_4d(st, tA, 32 * kb, g, t0, b, bar);
-      ptx::tma_load_2d(st + kASlice, tS, 32 * kb, srow + nt * kN, bar);
-    } else if (kMode == 3) {
-      ptx::tma_load_4d(st, tA, 32 * kb, g, t0, b, bar);
-      ptx::tma_load_4d(st + kASlice, tS, 32 * kb, g, tok0 + ni * kGM, b, bar);
-    } else if (kMode == 1) {
-      ptx::tma_load_4d(st, tA, 32 * (kb & 1), g * a.hpg + (kb >> 1), t0, b, bar);
-#pragma unroll
-      for (int j = 0; j < kN / 32; ++j)
-        ptx::tma_load_2d(st + kASlice + j * 4096, tS, nt * kN + 32 * j, srow + 32 * kb, bar);
-    } else {
-      const int tk = tok0 + 32 * kb;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        ptx::tma_load_4d(st + q * 4096, tA, 32 * (q & 1), q < 2 ? h0 : h1, tk, b, bar);
-#pragma unroll
-      for (int j = 0; j < kN / 32; ++j)
-        ptx::tma_load_4d(st + kASlice + j * 4096, tS, nt * kN + 32 * j, g, tk, b, bar);
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tA0);
+      ptx::prefetch_tmap(&tA1);
+      ptx::prefetch_tmap(&tS0);
+      ptx::prefetch_tmap(&tS1);
     }
-  };
-  if (tid == 0) {
-    ptx::prefetch_tmap(tA);
-    ptx::prefetch_tmap(tS);
-    load(0);
-    if (nk > 1) load(1);
-  }
-
-  const uint32_t idesc = ptx::idesc_tf32(kGM, kN, false, false);
-  for (int kb = 0; kb < nk; ++kb) {
-    uint8_t *st = smem + (kb & 1) * kStage, *sb = st + kASlice;
-    ptx::mbar_wait(&full[kb & 1], (kb >> 1) & 1, a.err, 240);
-    if (kb > 0) {
-      // the previous slice's MMAs are done: its stage and the lo buffers
-      // are free
-      ptx::mbar_wait(&done, (kb - 1) & 1, a.err, 241);
-      ptx::tc_fence_after();
-      if (tid == 0 && kb + 1 < nk) load(kb + 1);
-    }
-    if (!kTransA) split_kmajor<kASlice>(st, loA, tid);
-    if (!kTransB) split_kmajor<kBSlice>(sb, loB, tid);
-    if (kTransA || kTransB) {
-      float4 va[kTransA ? 4 : 1], vb[kTransB ? kN / 32 : 1];
-      if constexpr (kTransA) t_read<4>(st, warp, lane, va);
-      if constexpr (kTransB) t_read<kN / 32>(sb, warp, lane, vb);
-      __syncthreads();  // every piece read before the transposed writes
-      if constexpr (kTransA) t_write<4>(st, loA, warp, lane, va);
-      if constexpr (kTransB) t_write<kN / 32>(sb, loB, warp, lane, vb);
-    }
-    ptx::fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      ptx::tc_fence_after();
-      const uint32_t ah = ptx::smem_u32(st), al = ptx::smem_u32(loA);
-      const uint32_t bh = ptx::smem_u32(sb), bl = ptx::smem_u32(loB);
+    int u = 0;  // slices issued
+    for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+      const Tile t = decode_tile<kMode>(item, a);
+      const CUtensorMap *tA = t.which ? &tA1 : &tA0;
+      const CUtensorMap *tS = t.which ? &tS1 : &tS0;
+      const int t0 = t.tok0 + (kMode == 3 ? t.mi : t.mt) * kGM;
+      const int srow = ((t.b * a.nc + t.k) * a.nh + t.g * a.hpg) * kPh;
+      const int h0 = t.g * a.hpg + 2 * t.mt;
+      const int h1 = h0 + 1 < (t.g + 1) * a.hpg ? h0 + 1 : h0;
+      for (int kb = 0; kb < t.nk; ++kb, ++u) {
+        const int s = u % kRing, j = u / kRing;
+        if (j > 0) ptx::mbar_wait(&empty[s], (j - 1) & 1, a.err, 244);
+        if (lane == 0) {
+          uint8_t *st = ring + s * kStage;
+          uint64_t *bar = &full[s];
+          ptx::mbar_arrive_expect_tx(bar, kStage);
+          if (kMode == 0) {
+            ptx::tma_load_4d(st, tA, 32 * kb, t.g, t0, t.b, bar);
+            ptx::tma_load_2d(st + kASlice, tS, 32 * kb, srow + t.nt * kN, bar);
+          } else if (kMode == 3) {
+            ptx::tma_load_4d(st, tA, 32 * kb, t.g, t0, t.b, bar);
+            ptx::tma_load_4d(st + kASlice, tS, 32 * kb, t.g, t.tok0 + t.ni * kGM, t.b, bar);
+          } else if (kMode == 1) {
+            ptx::tma_load_4d(st, tA, 32 * (kb & 1), t.g * a.hpg + (kb >> 1), t0, t.b, bar);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t dah = ptx::smem_desc(ah + 32 * kk, 16, 1024, ptx::kSw128);
-        const uint64_t dal = ptx::smem_desc(al + 32 * kk, 16, 1024, ptx::kSw128);
-        const uint64_t dbh = ptx::smem_desc(bh + 32 * kk, 16, 1024, ptx::kSw128);
-        const uint64_t dbl = ptx::smem_desc(bl + 32 * kk, 16, 1024, ptx::kSw128);
-        ptx::mma_ss<true>(tmem, dal, dbh, idesc, (kb | kk) ? 1u : 0u);
-        ptx::mma_ss<true>(tmem, dah, dbl, idesc, 1u);
-        ptx::mma_ss<true>(tmem, dah, dbh, idesc, 1u);
+            for (int jb = 0; jb < kN / 32; ++jb)
+              ptx::tma_load_2d(st + kASlice + jb * 4096, tS, t.nt * kN + 32 * jb, srow + 32 * kb,
+                               bar);
+          } else {
+            const int tk = t.tok0 + 32 * kb;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              ptx::tma_load_4d(st + q * 4096, tA, 32 * (q & 1), q < 2 ? h0 : h1, tk, t.b, bar);
+#pragma unroll
+            for (int jb = 0; jb < kN / 32; ++jb)
+              ptx::tma_load_4d(st + kASlice + jb * 4096, tS, t.nt * kN + 32 * jb, t.g, tk, t.b,
+                               bar);
+          }
+        }
+        __syncwarp();
       }
-      ptx::mma_commit(&done);
     }
-  }
-
-  // epilogue: warp = TMEM lane quadrant (32 rows) x half of the N columns
-  ptx::mbar_wait(&done, (nk - 1) & 1, a.err, 242);
-  ptx::tc_fence_after();
-  const int quad = warp & 3, half = warp >> 2, m = quad * 32 + lane;
-  bool live;
-  int64_t o_row;  // the element offset of column nt kN of this thread's row
-  if (kMode == 2) {
-    const int hl = m >> 6, p = m & (kPh - 1);
-    live = hl == 0 || h1 != h0;
-    o_row = ((((int64_t)b * a.nh + (hl ? h1 : h0)) * a.nc + k) * kPh + p) * a.S + nt * kN;
-  } else if (kMode == 3) {
-    const int i = mi * kGM + m;  // row token of the chunk
-    live = i < a.T;
-    o_row = (((int64_t)b * a.ng + g) * a.nc + k) * a.T * a.T + (int64_t)i * a.T + ni * kGM;
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = ptx::idesc_tf32(kGM, kN, false, false);
+    int u = 0, jl = 0;
+    for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++jl) {
+      const Tile t = decode_tile<kMode>(item, a);
+      const int acc = jl & 1;
+      if (jl >= 2) ptx::mbar_wait(&accfree[acc], ((jl >> 1) - 1) & 1, a.err, 245);
+      ptx::tc_fence_after();
+      for (int kb = 0; kb < t.nk; ++kb, ++u) {
+        const int ob = u & 1;
+        ptx::mbar_wait(&opfull[ob], (u >> 1) & 1, a.err, 246);
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t o = ptx::smem_u32(ops + ob * kOps);
+          const uint32_t ah = o, bh = o + kASlice, al = o + kStage, bl = o + kStage + kASlice;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t dah = ptx::smem_desc(ah + 32 * kk, 16, 1024, ptx::kSw128);
+            const uint64_t dal = ptx::smem_desc(al + 32 * kk, 16, 1024, ptx::kSw128);
+            const uint64_t dbh = ptx::smem_desc(bh + 32 * kk, 16, 1024, ptx::kSw128);
+            const uint64_t dbl = ptx::smem_desc(bl + 32 * kk, 16, 1024, ptx::kSw128);
+            const uint32_t d = tmem + acc * kN;
+            ptx::mma_ss<true>(d, dal, dbh, idesc, (kb | kk) ? 1u : 0u);
+            ptx::mma_ss<true>(d, dah, dbl, idesc, 1u);
+            ptx::mma_ss<true>(d, dah, dbh, idesc, 1u);
+          }
+          ptx::mma_commit(&opfree[ob]);
+        }
+        __syncwarp();
+      }
+      if (lane == 0) ptx::mma_commit(&accfull[acc]);
+      __syncwarp();
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3, m = quad * 32 + lane;  // TMEM lane quadrant, row
+    int jl = 0;
+    for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++jl) {
+      const Tile t = decode_tile<kMode>(item, a);
+      const int acc = jl & 1;
+      bool live;
+      int64_t o_row;  // the element offset of column nt kN of this thread's row
+      if (kMode == 2) {
+        const int h0 = t.g * a.hpg + 2 * t.mt;
+        const int h1 = h0 + 1 < (t.g + 1) * a.hpg ? h0 + 1 : h0;
+        const int hl = m >> 6, p = m & (kPh - 1);
+        live = hl == 0 || h1 != h0;
+        o_row = ((((int64_t)t.b * a.nh + (hl ? h1 : h0)) * a.nc + t.k) * kPh + p) * a.S +
+                t.nt * kN;
+      } else if (kMode == 3) {
+        const int i = t.mi * kGM + m;  // row token of the chunk
+        live = i < a.T;
+        o_row = (((int64_t)t.b * a.ng + t.g) * a.nc + t.k) * a.T * a.T + (int64_t)i * a.T +
+                t.ni * kGM;
+      } else {
+        const int tl = t.mt * kGM + m;  // chunk-relative token
+        live = tl < t.valid;
+        const int64_t tok = (int64_t)t.b * a.L + t.tok0 + tl;
+        o_row = kMode == 0 ? (tok * a.nh + (int64_t)t.g * a.hpg) * kPh + t.nt * kN
+                           : (tok * a.ng + t.g) * a.S + t.nt * kN;
+      }
+      const int64_t o_end = kMode == 1 ? (int64_t)a.nb * a.L * a.ng * a.S
+                          : kMode == 0 ? (int64_t)a.nb * a.L * a.nh * kPh
+                          : kMode == 3 ? (int64_t)a.nb * a.ng * a.nc * a.T * a.T
+                                       : (int64_t)a.nb * a.nh * a.nc * kPh * a.S;
+      (void)o_end;  // read by the debug-bounds checks only
+      float *out = t.which ? a.out[1] : a.out[0];
+      ptx::mbar_wait(&accfull[acc], (jl >> 1) & 1, a.err, 247);
+      ptx::tc_fence_after();
+#pragma unroll 2
+      for (int c0 = 0; c0 < kN; c0 += 16) {
+        float v[16];
+        ptx::tmem_ld16_sync(tmem + ((uint32_t)(quad * 32) << 16) + acc * kN + c0, v);
+        const int64_t o = o_row + c0;
+        if (kMode == 3 && t.ni * kGM + c0 >= a.T) continue;  // columns past the chunk
+        if (!live || !SSD_IN_BOUNDS(o + 16 <= o_end, a.err, 243)) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float4 w4 = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          if (kMode == 1) {
+            const float4 w = *reinterpret_cast<const float4 *>(out + o + 4 * q);
+            w4.x += w.x;
+            w4.y += w.y;
+            w4.z += w.z;
+            w4.w += w.w;
+          }
+          *reinterpret_cast<float4 *>(out + o + 4 * q) = w4;
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&accfree[acc]);
+    }
   } else {
-    const int tl = mt * kGM + m;  // chunk-relative token
-    live = tl < valid;
-    const int64_t tok = (int64_t)b * a.L + tok0 + tl;
-    o_row = kMode == 0 ? (tok * a.nh + (int64_t)g * a.hpg) * kPh + nt * kN
-                       : (tok * a.ng + g) * a.S + nt * kN;
-  }
-  const int64_t o_end = kMode == 1 ? (int64_t)a.nb * a.L * a.ng * a.S
-                      : kMode == 0 ? (int64_t)a.nb * a.L * a.nh * kPh
-                      : kMode == 3 ? (int64_t)a.nb * a.ng * a.nc * a.T * a.T
-                                   : (int64_t)a.nb * a.nh * a.nc * kPh * a.S;
-  float *out = which ? a.out[1] : a.out[0];
-  constexpr int kHalf = kN / 2;
-#pragma unroll
-  for (int ci = 0; ci < kHalf / 16; ++ci) {
-    const int c0 = half * kHalf + 16 * ci;
-    float v[16];
-    ptx::tmem_ld16_sync(tmem + ((uint32_t)(quad * 32) << 16) + c0, v);
-    const int64_t o = o_row + c0;
-    if (kMode == 3 && ni * kGM + c0 >= a.T) continue;  // columns past the chunk
-    if (!live || !SSD_IN_BOUNDS(o + 16 <= o_end, a.err, 243)) continue;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float4 u = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      if (kMode == 1) {
-        const float4 w = *reinterpret_cast<const float4 *>(out + o + 4 * q);
-        u.x += w.x;
-        u.y += w.y;
-        u.z += w.z;
-        u.w += w.w;
+    // ------------------------------------------------------------ split warps
+    int u = 0;  // slices consumed
+    for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+      const Tile t = decode_tile<kMode>(item, a);
+      for (int kb = 0; kb < t.nk; ++kb, ++u) {
+        const int s = u % kRing, ob = u & 1;
+        ptx::mbar_wait(&full[s], (u / kRing) & 1, a.err, 240);
+        const uint8_t *st = ring + s * kStage, *sb = st + kASlice;
+        float4 va[kNA], vb[kNB];
+        if constexpr (kTransA) t_read<kNA>(st, warp, lane, va);
+        else k_read<kASlice>(st, tid, va);
+        if constexpr (kTransB) t_read<kNB>(sb, warp, lane, vb);
+        else k_read<kBSlice>(sb, tid, vb);
+        // split in registers: the loads have returned before the stage is
+        // handed back to the TMA (an async-proxy write after these
+        // generic-proxy reads, ordered by the proxy fence and the barrier)
+        uint4 ha[kNA], la[kNA], hb[kNB], lb[kNB];
+        split_regs(va, ha, la);
+        split_regs(vb, hb, lb);
+        ptx::fence_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&empty[s]);  // the stage may be refilled
+        if (u >= 2) ptx::mbar_wait(&opfree[ob], ((u >> 1) - 1) & 1, a.err, 241);
+        uint8_t *o = ops + ob * kOps;
+        if constexpr (kTransA) t_store<kNA>(o, o + kStage, warp, lane, ha, la);
+        else k_store<kASlice>(o, o + kStage, tid, ha, la);
+        if constexpr (kTransB) t_store<kNB>(o + kASlice, o + kStage + kASlice, warp, lane, hb, lb);
+        else k_store<kBSlice>(o + kASlice, o + kStage + kASlice, tid, hb, lb);
+        ptx::fence_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&opfull[ob]);
       }
-      *reinterpret_cast<float4 *>(out + o + 4 * q) = u;
     }
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int kMode, int kN>
 cudaError_t run_gemm(const CUtensorMap &ta0, const CUtensorMap &ta1, const CUtensorMap &ts0,
                      const CUtensorMap &ts1, const GemmArgs &a, cudaStream_t st) {
-  constexpr int smem = 2 * (kASlice + kN * 128) + kASlice + kN * 128 + 1024;
+  constexpr int kStage = kASlice + kN * 128;
+  constexpr int smem = kRing * kStage + 2 * 2 * kStage + 1024;  // ring, two operand sets
   auto kernel = bwd_state_gemm_kernel<kMode, kN>;
   const cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<a.n_items, kGThreads, smem, st>>>(ta0, ta1, ts0, ts1, a);
+  const int grid = (int)std::min<int64_t>(a.n_items, sm_count());
+  kernel<<<grid, kPThreads, smem, st>>>(ta0, ta1, ts0, ts1, a);
   return cudaGetLastError();
 }
 
