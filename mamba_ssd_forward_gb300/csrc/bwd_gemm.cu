@@ -31,22 +31,25 @@
 // 2^-21 relative per product, near fp32 (the "3xTF32" split used by fp32
 // GEMM libraries on TF32 tensor cores).
 //
-// One CTA per (product, batch, chunk, group, M tile, N tile of 128 or 64
-// columns), 256 threads, two CTAs per SM.  M tiles: 128 tokens (modes 0,
-// 1 and 3; with chunks shorter than 128 tokens the rows past the chunk are
-// computed and not stored) or the rows (h, p) of two heads of the group
-// (mode 2; an odd group's last tile repeats its head and stores one).  K
-// runs in slices of 32 (one 128-byte row of fp32), double-buffered by TMA.
-// K-major operands (the token rows of modes 0, 1 and 3, the states of mode 0)
-// land as 128-byte rows; the others (the states of mode 1, both operands
-// of mode 2) land as 32 x 32 boxes with K along the rows and are transposed
-// by the split.  Per slice the eight warps split the operands -- hi in
-// place (transposed: every thread reads its pieces, a barrier, then writes
-// down the columns), lo into a buffer of its own -- and thread 0 issues
-// 3 x 4 MMAs (M = 128, N, K = 8) and commits them.  The next slice's split
-// waits for that commit (the lo buffers are single); the other CTA on the
-// SM runs meanwhile.  The epilogue reads the accumulator (warp = TMEM lane
-// quadrant x column half) and stores, or adds into dB / dC.
+// Work items (output tiles): (product, batch, chunk, group, M tile, N tile
+// of 128 or 64 columns).  M tiles: 128 tokens (modes 0, 1 and 3; with
+// chunks shorter than 128 tokens the rows past the chunk are computed and
+// not stored) or the rows (h, p) of two heads of the group (mode 2; an odd
+// group's last tile repeats its head and stores one).  K runs in slices of
+// 32 (one 128-byte row of fp32).  K-major operands (the token rows of modes
+// 0, 1 and 3, the states of mode 0) land by TMA as 128-byte swizzled rows;
+// the others (the states of mode 1, both operands of mode 2) as 32 x 32
+// boxes with K along the rows, transposed by the split.
+//
+// Persistent, one CTA per SM (448 threads, 225 KB of shared memory at N
+// tiles of 128): a producer warp streams the slices of the CTA's tiles
+// through a three-stage TMA ring; eight split warps read a landed slice
+// into registers, split it (hi and lo), hand the stage back and store the
+// halves K-major into one of two operand sets; one warp issues per slice
+// 3 x 4 MMAs (M = 128, N, K = 8) into the tile's accumulator (two in
+// tensor memory, by tile parity) and commits them, freeing the operand
+// set; four warps read each finished accumulator (warp = TMEM lane
+// quadrant) and store, or add into dB / dC.  Every wait is bounded.
 #include "tc_common.cuh"
 
 namespace ssd {

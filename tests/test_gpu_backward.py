@@ -131,10 +131,17 @@ def test_backward_steep_chunks(ssd):
     compare(out, reference(inp, gy, gfinal), "steep")
 
 
-def test_backward_is_deterministic(ssd):
-    """dB, dC, dA and dD are sums in a fixed order: repeated calls on the
-    same inputs give the same bits."""
-    w = W.Workload("bwd_repeat", 2, 1024, 8, 64, 64, 2, 256, "fp32", True)
+REPEAT = [W.Workload("bwd_repeat", 2, 1024, 8, 64, 64, 2, 256, "fp32", True),
+          # the long-context layer's group shape on a shorter sequence: the
+          # GEMM kernel's CTAs each take several tiles through one pipeline
+          W.Workload("bwd_repeat_S256_g8", 1, 2048, 48, 64, 256, 8, 256, "fp32", True)]
+
+
+@pytest.mark.parametrize("w", REPEAT, ids=lambda w: w.name)
+def test_backward_is_deterministic(ssd, w):
+    """dB, dC, dA and dD are sums in a fixed order, and every GEMM tile is
+    computed by one CTA in a fixed order: repeated calls on the same inputs
+    give the same bits."""
     inp = make(w, seed=34)
     gy, gfinal = grads_in(w, 34)
     first = run(ssd, w, inp, gy, gfinal)
