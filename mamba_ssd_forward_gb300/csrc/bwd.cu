@@ -93,16 +93,13 @@ __device__ __forceinline__ float comp(const float4 &v, int e) {
 
 // ------------------------------------------------------------ state terms
 
-// The state terms of the backward as GEMMs (fp32, on the tensor cores through
-// cuBLAS's bf16x9 emulation of fp32 products), per (batch, chunk, group)
-// with the group's heads side by side:
-//   dxS[t][(h, p)]  = sum_s B_t[s] R_h[p][s]        (dx += dt exp2(G_last - G_t) dxS)
-//   ysmS[t][(h, p)] = sum_s c_t[s] h_h[p][s]        (ysm += exp2(G_t) ysmS)
-//   dB_t[s] += sum_(h, p) X~_t[(h, p)] R_h[p][s],   X~ = dt exp2(G_last - G_t) x
-//   dC_t[s] += sum_(h, p) Gy~_t[(h, p)] h_h[p][s],  Gy~ = exp2(G_t) gy
-// with R and h stored chunk-major ([b, nc, nh, P, S]: a group's heads at one
-// chunk are one [hpg P][S] matrix).  bwd_scale_kernel writes X~ and Gy~, one
-// thread per four elements of [b, L, nh, P].
+// The token-row operands of the backward's GEMMs (bwd_gemm.cu) that carry
+// a per-token factor: X~ = dt exp2(G_last - G_t) x (the forward's jump
+// terms, dB += X~ R) and Gy~ = exp2(G_t) gy (the adjoint's jump terms, dC
+// += Gy~ h), in the layout of x, one thread per four elements of [b, L, nh,
+// P].  (Applying the factors inside the GEMM's split instead was measured
+// slower on the long-context layer: the factor loads land on the GEMM's
+// critical path.)
 __global__ void __launch_bounds__(kThreads)
 bwd_scale_kernel(const float *__restrict__ x, const float *__restrict__ gy,
                  const float *__restrict__ dt, const float *__restrict__ G,
