@@ -79,7 +79,7 @@ constexpr int kRowThreads = 32 * kRowWarps;
 constexpr int kProdWarp = 8, kMmaWarp = 9;    // TMA producer, MMA issuer
 constexpr int kEpiWarp0 = 10;                 // epilogue warps 10..13
 constexpr int kPThreads = 32 * (kEpiWarp0 + 4);
-constexpr int kRing = 3;                      // TMA landing stages
+constexpr int kRing = 5;                      // TMA landing stages
 
 // A landed K-major slice of kBytes: this thread's 16-byte pieces tid + 256 i
 // into registers ...
@@ -191,9 +191,12 @@ bwd_state_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
   constexpr bool kTransA = kMode == 2, kTransB = kMode == 1 || kMode == 2;
   constexpr int kBSlice = kN * 128;           // bytes of an N x 32 slice
   constexpr int kStage = kASlice + kBSlice;   // one landed slice
-  constexpr int kOps = 2 * kStage;            // operand set: hi A | hi B | lo A | lo B
-  constexpr int kTmemCols = 2 * kN;
-  constexpr int kNA = kASlice / 16 / kRowThreads, kNB = kBSlice / 16 / kRowThreads;
+  constexpr int kOps = 2 * kBSlice;           // operand set in smem: hi B | lo B
+  // tensor memory: two accumulators (kN columns each), then two operand
+  // sets of A (hi in 32 columns, lo in the next 32)
+  constexpr int kAcol = 2 * kN;
+  constexpr int kTmemCols = kAcol + 128 <= 256 ? 256 : 512;
+  constexpr int kNB = kBSlice / 16 / kRowThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *ring = smem, *ops = smem + kRing * kStage;
@@ -292,17 +295,16 @@ bwd_state_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
         ptx::tc_fence_after();
         if (lane == 0) {
           const uint32_t o = ptx::smem_u32(ops + ob * kOps);
-          const uint32_t ah = o, bh = o + kASlice, al = o + kStage, bl = o + kStage + kASlice;
+          const uint32_t bh = o, bl = o + kBSlice;
+          const uint32_t ah = tmem + kAcol + 64 * ob, al = ah + 32;  // A in tensor memory
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t dah = ptx::smem_desc(ah + 32 * kk, 16, 1024, ptx::kSw128);
-            const uint64_t dal = ptx::smem_desc(al + 32 * kk, 16, 1024, ptx::kSw128);
             const uint64_t dbh = ptx::smem_desc(bh + 32 * kk, 16, 1024, ptx::kSw128);
             const uint64_t dbl = ptx::smem_desc(bl + 32 * kk, 16, 1024, ptx::kSw128);
             const uint32_t d = tmem + acc * kN;
-            ptx::mma_ss<true>(d, dal, dbh, idesc, (kb | kk) ? 1u : 0u);
-            ptx::mma_ss<true>(d, dah, dbl, idesc, 1u);
-            ptx::mma_ss<true>(d, dah, dbh, idesc, 1u);
+            ptx::mma_ts_tf32(d, al + 8 * kk, dbh, idesc, (kb | kk) ? 1u : 0u);
+            ptx::mma_ts_tf32(d, ah + 8 * kk, dbl, idesc, 1u);
+            ptx::mma_ts_tf32(d, ah + 8 * kk, dbh, idesc, 1u);
           }
           ptx::mma_commit(&opfree[ob]);
         }
@@ -380,27 +382,54 @@ bwd_state_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
         const int s = u % kRing, ob = u & 1;
         ptx::mbar_wait(&full[s], (u / kRing) & 1, a.err, 240);
         const uint8_t *st = ring + s * kStage, *sb = st + kASlice;
-        float4 va[kNA], vb[kNB];
-        if constexpr (kTransA) t_read<kNA>(st, warp, lane, va);
-        else k_read<kASlice>(st, tid, va);
+        // A: this warp's TMEM lane quadrant q (row m = 32 q + lane) and half
+        // kh of the slice's K, 16 values; B: pieces as for a K-major or
+        // transposed slice
+        const int q = warp & 3, kh = warp >> 2, m = 32 * q + lane;
+        float av[16];
+        if constexpr (kTransA) {
+          // box q holds rows K (tokens) x 32 M-rows: column lane, rows 16 kh ..
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            av[e] = *reinterpret_cast<const float *>(st + q * 4096 + sw128(16 * kh + e, 4 * lane));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 v = *reinterpret_cast<const float4 *>(st + sw128(m, 64 * kh + 16 * j));
+            av[4 * j] = v.x;
+            av[4 * j + 1] = v.y;
+            av[4 * j + 2] = v.z;
+            av[4 * j + 3] = v.w;
+          }
+        }
+        float4 vb[kNB];
         if constexpr (kTransB) t_read<kNB>(sb, warp, lane, vb);
         else k_read<kBSlice>(sb, tid, vb);
         // split in registers: the loads have returned before the stage is
         // handed back to the TMA (an async-proxy write after these
         // generic-proxy reads, ordered by the proxy fence and the barrier)
-        uint4 ha[kNA], la[kNA], hb[kNB], lb[kNB];
-        split_regs(va, ha, la);
+        uint32_t ahi[16], alo[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          ahi[e] = to_tf32(av[e]);
+          alo[e] = __float_as_uint(av[e] - __uint_as_float(ahi[e]));
+        }
+        uint4 hb[kNB], lb[kNB];
         split_regs(vb, hb, lb);
         ptx::fence_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&empty[s]);  // the stage may be refilled
         if (u >= 2) ptx::mbar_wait(&opfree[ob], ((u >> 1) - 1) & 1, a.err, 241);
+        ptx::tc_fence_after();
+        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kAcol + 64 * ob + 16 * kh;
+        ptx::tmem_st16u(ta, ahi);
+        ptx::tmem_st16u(ta + 32, alo);
         uint8_t *o = ops + ob * kOps;
-        if constexpr (kTransA) t_store<kNA>(o, o + kStage, warp, lane, ha, la);
-        else k_store<kASlice>(o, o + kStage, tid, ha, la);
-        if constexpr (kTransB) t_store<kNB>(o + kASlice, o + kStage + kASlice, warp, lane, hb, lb);
-        else k_store<kBSlice>(o + kASlice, o + kStage + kASlice, tid, hb, lb);
+        if constexpr (kTransB) t_store<kNB>(o, o + kBSlice, warp, lane, hb, lb);
+        else k_store<kBSlice>(o, o + kBSlice, tid, hb, lb);
+        ptx::tmem_st_wait();
         ptx::fence_async_smem();
+        ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&opfull[ob]);
       }
@@ -415,7 +444,7 @@ template <int kMode, int kN>
 cudaError_t run_gemm(const CUtensorMap &ta0, const CUtensorMap &ta1, const CUtensorMap &ts0,
                      const CUtensorMap &ts1, const GemmArgs &a, cudaStream_t st) {
   constexpr int kStage = kASlice + kN * 128;
-  constexpr int smem = kRing * kStage + 2 * 2 * kStage + 1024;  // ring, two operand sets
+  constexpr int smem = kRing * kStage + 2 * 2 * kN * 128 + 1024;  // ring, two B operand sets
   auto kernel = bwd_state_gemm_kernel<kMode, kN>;
   const cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
