@@ -43,13 +43,16 @@
 //
 // Persistent, one CTA per SM (448 threads, 225 KB of shared memory at N
 // tiles of 128): a producer warp streams the slices of the CTA's tiles
-// through a three-stage TMA ring; eight split warps read a landed slice
+// through a five-stage TMA ring; eight split warps read a landed slice
 // into registers, split it (hi and lo), hand the stage back and store the
-// halves K-major into one of two operand sets; one warp issues per slice
-// 3 x 4 MMAs (M = 128, N, K = 8) into the tile's accumulator (two in
-// tensor memory, by tile parity) and commits them, freeing the operand
-// set; four warps read each finished accumulator (warp = TMEM lane
-// quadrant) and store, or add into dB / dC.  Every wait is bounded.
+// halves K-major: the token rows' (A) into tensor memory (warp = TMEM lane
+// quadrant x half of the slice's K), the other operand's (B) into shared
+// memory, each in one of two operand sets; one warp issues per slice
+// 3 x 4 MMAs (M = 128, N, K = 8; A from tensor memory) into the tile's
+// accumulator (two in tensor memory, by tile parity) and commits them,
+// freeing the operand set; four warps read each finished accumulator (warp
+// = TMEM lane quadrant) and store, or add into dB / dC.  Every wait is
+// bounded.
 #include "tc_common.cuh"
 
 namespace ssd {
