@@ -725,8 +725,11 @@ cudaError_t launch_bwd_convert(const BwdConvert &a, cudaStream_t st) {
 }
 
 bool bwd_supported(const Dims &d) {
-  return d.P == kP && (d.S == 64 || d.S == 128 || d.S == 256) && d.T % kTT == 0 && d.T <= 256 &&
-         bwd_state_gemm_supported(d);
+  // chunks of whole row tiles of the per-token kernel: 64 tokens at dstate
+  // 256, 32 below
+  const int64_t rt = d.S == 256 ? 2 * kTT : kTT;
+  return d.P == kP && (d.S == 64 || d.S == 128 || d.S == 256) && d.T >= rt && d.T % rt == 0 &&
+         d.T <= 256 && bwd_state_gemm_supported(d);
 }
 
 int bwd_head_slices(const Dims &d) {

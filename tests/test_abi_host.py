@@ -361,8 +361,12 @@ def test_backward_workspace_and_rejections(lib):
     ws16 = lib.ssd_backward_workspace_size(ctypes.byref(d), 1)
     assert ws16 >= ws32 + 4 * 2 * 1000 * (2 * 8 * 64 + 2 * 2 * 128)  # fp32 copies of x, gy, B, C
     assert lib.ssd_backward_workspace_size(ctypes.byref(d), 7) == 0
-    for bad in (dims(headdim=32), dims(dstate=96), dims(headdim=128)):
+    for bad in (dims(headdim=32), dims(dstate=96), dims(headdim=128),
+                # chunk lengths other than 64, 128 and 256
+                dims(dstate=256, chunk=96), dims(chunk=32), dims(chunk=512)):
         assert lib.ssd_backward_workspace_size(ctypes.byref(bad), 0) == 0
+    for good in (dims(chunk=64), dims(dstate=256, chunk=64), dims(dstate=64, chunk=128)):
+        assert lib.ssd_backward_workspace_size(ctypes.byref(good), 0) > 0
     ok = ctypes.c_void_p(1 << 20)
     odd = ctypes.c_void_p((1 << 20) + 4)
     args = [ok, ok, ok, ok, ok, None, None, ok, None, ok, ok, ok, ok, ok, None, None]
