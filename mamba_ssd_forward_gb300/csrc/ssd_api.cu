@@ -646,10 +646,13 @@ namespace {
 
 // Workspace of ssd_backward (fp32): the header (the call's error word), G,
 // the chunk jump terms (the forward's, then the adjoint's), the start states
-// h_k, the adjoint states R_k, the forward's final state, the per-token q . B,
-// dL/dG and gy . x, the per-chunk shares of dA and dD, and c_i . B_j of every
-// chunk and group (T x T); with bf16 I/O then fp32 copies of x, dt, B, C, gy
-// and fp32 buffers for dx, ddt, dB, dC.  Each part is 256-byte aligned.
+// h_k and the adjoint states R_k (both chunk-major), the forward's final
+// state, the per-token q . B, dL/dG and gy . x, the per-chunk shares of dA
+// and dD, c_i . B_j of every chunk and group (T x T), the head slices' dB,
+// dC shares (when a group's heads are split), the state terms dxS, ysmS and
+// the scaled inputs x~, gy~ (in the layout of x); with bf16 I/O then fp32
+// copies of x, dt, B, C, gy and fp32 buffers for dx, ddt, dB, dC.  Each part
+// is 256-byte aligned.
 struct BwdLayout {
   size_t G, dst, states, R, fin, qB, dG, gyx, part, Kcb, sB, sC, dxS, ysmS, xs, gys;
   size_t cx, cdt, cB, cC, cgy, cdx, cddt, cdB, cdC;  // bf16 I/O only
